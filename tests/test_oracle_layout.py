@@ -1,0 +1,122 @@
+"""Pins for the oracle's packed layouts (CPU only): byte accounting from the explainer page,
+hand-computed offsets, and pack/unpack round trips on ragged shapes."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import layout as L
+from oracle import quant as Q
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "int4_worked_example.json")
+
+
+def test_group_accounting_matches_page():
+    g = json.load(open(GOLDEN))
+    # one unit is 128 rows x (128 INT4 values + one 16-bit scale)
+    assert L.unit_bytes(L.FMT_W4A16_INT4, False) == 128 * g["group_bytes"]
+    assert g["weight_bytes"] == g["group_values"] * 4 // 8
+    assert L.unit_bytes(L.FMT_W4A16_INT4, False) * 8 / (128 * 128) == g["bits_per_value"]
+    # with a u4 zero-point per group: 4 + 16/128 + 4/128 bits
+    assert L.unit_bytes(L.FMT_W4A16_INT4, True) * 8 / (128 * 128) == 4 + 20 / 128
+
+
+def test_payload_sizes():
+    assert L.payload_bytes(L.FMT_W4A16_MXFP4, 256, 256) == 4 * 8704
+    assert L.payload_bytes(L.FMT_W4A8_MXFP4, 4096, 4096) == 4096 * 2048 + 32 * 32 * 512
+    assert L.payload_bytes(L.FMT_W4A4_NVFP4, 8192, 8192) == 8192 * 4096 + 64 * 128 * 512
+    assert L.packed_size(L.FMT_W4A16_INT4, 130, 128) == 256 + 2 * 8448   # N padded to 256
+
+
+def test_hand_computed_offsets():
+    pos = lambda kk: tuple(int(v) for v in L.nibble_position(kk))
+    assert pos(0) == (0, 0)
+    assert pos(1) == (2, 0)        # odd k in the high half-word
+    assert pos(2) == (0, 4)
+    assert pos(3) == (2, 4)
+    assert pos(6) == (1, 4)
+    assert pos(7) == (3, 4)
+    assert pos(8) == (4, 0)
+    assert pos(32) == (2048, 0)
+    assert pos(127) == (3 * 2048 + 12 + 3, 4)
+    assert int(L.atom_offset(0, 0)) == 0
+    assert int(L.atom_offset(1, 0)) == 16
+    assert int(L.atom_offset(32, 0)) == 4
+    assert int(L.atom_offset(33, 2)) == 22
+    assert int(L.atom_offset(127, 3)) == 511
+    offs = L.atom_offset(np.arange(128)[:, None], np.arange(4)[None, :])
+    assert sorted(offs.ravel().tolist()) == list(range(512))   # a permutation of the atom
+
+
+def test_header_fields():
+    buf = L.pack_w4a4_nvfp4(np.zeros((3, 64), np.uint8), np.zeros((3, 4), np.uint8), 0.5)
+    h = L.parse_header(buf)
+    assert h == dict(magic=L.MAGIC, fmt=4, N=3, K=64, N_pad=128, K_pad=256, has_zero=False,
+                     tensor_scale=0.5, payload_bytes=128 * 128 + 4 * 512)
+    assert len(buf) == L.packed_size(4, 3, 64)
+
+
+@pytest.mark.parametrize("has_zero", [False, True])
+def test_int4_round_trip(has_zero):
+    rng = np.random.default_rng(0)
+    n, k = 200, 256
+    w = rng.standard_normal((n, k)) * 0.02
+    z = rng.integers(0, 16, size=(n, k // 128)) if has_zero else None
+    q, s = Q.quant_int4(w, zeros=z)
+    buf = L.pack_w4a16_int4(q, s, z)
+    assert len(buf) == L.packed_size(1, n, k, has_zero)
+    nib, units = L.unpack_units(buf)
+    np.testing.assert_array_equal(nib, q if has_zero else q + 8)
+    sb = units[:, :, 8192:8448].view(np.uint16)          # [nt, kb, 128]
+    got = sb.transpose(0, 2, 1).reshape(-1, k // 128)[:n]
+    from oracle.formats import bf16_bits
+    np.testing.assert_array_equal(got, bf16_bits(s))
+    if has_zero:
+        zb = units[:, :, 8448:8512]
+        zz = np.stack([zb & 0xF, zb >> 4], axis=-1).reshape(zb.shape[0], zb.shape[1], 128)
+        np.testing.assert_array_equal(zz.transpose(0, 2, 1).reshape(-1, k // 128)[:n], z)
+    # padded rows are all zero
+    assert np.all(units[1, :, :][:, [16 * r for r in range(72, 128)]] == 0)
+
+
+def test_mxfp4_tiled_round_trip():
+    rng = np.random.default_rng(1)
+    w = rng.standard_normal((130, 128)) * 0.02
+    codes, e = Q.quant_mxfp4(w)
+    buf = L.pack_w4a16_mxfp4(codes, e)
+    nib, units = L.unpack_units(buf)
+    np.testing.assert_array_equal(nib, codes)
+    eb = units[:, 0, 8192:8704].reshape(-1, 128, 4).reshape(-1, 4)[:130]
+    np.testing.assert_array_equal(eb, e)
+
+
+@pytest.mark.parametrize("fmt", [3, 4])
+def test_rowmajor_round_trip(fmt):
+    rng = np.random.default_rng(2)
+    n, k = 150, 512
+    w = rng.standard_normal((n, k)) * 0.02
+    if fmt == 3:
+        codes, sf = Q.quant_mxfp4(w)
+        buf = L.pack_w4a8_mxfp4(codes, sf)
+        chunks = k // 128
+    else:
+        codes, sf, g = Q.quant_nvfp4(w)
+        buf = L.pack_w4a4_nvfp4(codes, sf, g)
+        chunks = k // 64
+    h = L.parse_header(buf)
+    body_len = h["N_pad"] * h["K_pad"] // 2
+    body = buf[L.HEADER:L.HEADER + body_len]
+    np.testing.assert_array_equal(L.unpack_codes_rowmajor(body, h["N_pad"], k)[:n], codes)
+    atoms = buf[L.HEADER + body_len:]
+    np.testing.assert_array_equal(L.unpack_atoms(atoms, n, chunks), np.asarray(sf, np.uint8))
+
+
+def test_act_nvfp4_layout():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((70, 128))
+    codes, sb, g = Q.quant_nvfp4(x)
+    body, atoms = L.pack_act_nvfp4(codes, sb)
+    assert body.shape == (70, 64) and atoms.size == L.act_scale_bytes(70, 128) == 2 * 512
+    np.testing.assert_array_equal(L.unpack_codes_rowmajor(body, 70, 128), codes)
+    np.testing.assert_array_equal(L.unpack_atoms(atoms, 70, 2), sb)

@@ -1,0 +1,184 @@
+"""Pins for the oracle's quantizers (CPU only): the explainer page's worked INT4 example,
+hand-computed closed forms, and invariants every correct quantizer satisfies."""
+import json
+import os
+
+import numpy as np
+
+from oracle import formats as F
+from oracle import quant as Q
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "int4_worked_example.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def test_page_worked_example_quantize_restore():
+    g = golden()
+    q = int(Q.int4_code(g["w"], g["scale"]))
+    assert q == g["q"]
+    assert abs(float(Q.int4_restore(q, g["scale"])) - g["restored"]) < 1e-12
+
+
+def test_page_worked_example_range_clamp():
+    lo, hi = golden()["int4_range"]
+    assert int(Q.int4_code(1.0, 0.1)) == hi          # 10 -> 7
+    assert int(Q.int4_code(-1.0, 0.1)) == lo         # -10 -> -8
+    assert int(Q.int4_code(0.74, 0.1)) == hi
+
+
+def test_page_worked_example_dot_product():
+    g = golden()
+    w = np.array(g["dot_weights"])
+    x = np.array(g["dot_activations"], dtype=np.float64)
+    assert abs(float(w @ x) - g["dot_exact"]) < 1e-12
+    what = Q.int4_restore(Q.int4_code(w, g["scale"]), g["scale"])
+    np.testing.assert_allclose(what, g["dot_quantized_weights"], atol=1e-12)
+    assert abs(float(what @ x) - g["dot_after_quantization"]) < 1e-12
+
+
+def _group(vals):
+    w = np.zeros((1, 128), dtype=np.float64)
+    w[0, :len(vals)] = vals
+    return w
+
+
+def test_int4_symmetric_closed_form():
+    # amax 0.875 -> s = 0.875/7 = 0.125 exactly -> q = w/0.125
+    w = _group([0.875, -0.5, 0.125, 0.0, 0.3125, -0.0625])
+    q, s = Q.quant_int4(w)
+    assert s.shape == (1, 1) and s[0, 0] == 0.125
+    np.testing.assert_array_equal(q[0, :6], [7, -4, 1, 0, 2, 0])   # 2.5 -> 2, -0.5 -> -0 (even)
+    np.testing.assert_array_equal(Q.dequant_int4(q, s)[0, :6], [0.875, -0.5, 0.125, 0, 0.25, 0])
+
+
+def test_int4_zero_point_closed_form():
+    w = _group([0.875, -0.5, 0.125, 0.0])
+    z = np.array([[3]])
+    q, s = Q.quant_int4(w, zeros=z)
+    np.testing.assert_array_equal(q[0, :4], [10, 0, 4, 3])           # -4+3 = -1 clamps to 0
+    np.testing.assert_array_equal(Q.dequant_int4(q, s, z)[0, :4], [0.875, -0.375, 0.125, 0])
+
+
+def test_int4_scale_is_bf16_of_fp32_quotient():
+    w = _group([0.7])
+    _, s = Q.quant_int4(w)
+    want = F.bf16r(np.float64(np.float32(np.float32(0.7) / np.float32(7.0))))
+    assert s[0, 0] == want and s[0, 0] != 0.1
+
+
+def test_int4_zero_group():
+    q, s = Q.quant_int4(np.zeros((2, 256)))
+    assert np.all(s == 0) and np.all(q == 0)
+    q, s = Q.quant_int4(np.zeros((1, 128)), zeros=np.array([[5]]))
+    assert np.all(q == 5)
+
+
+def test_int4_invariants_random():
+    rng = np.random.default_rng(0)
+    w = (rng.standard_normal((64, 512)) * 0.02).astype(np.float32)
+    q, s = Q.quant_int4(w)
+    assert q.min() >= -7 and q.max() <= 7              # s = amax/7 never reaches -8
+    sf = np.repeat(s, 128, axis=1)
+    err = np.abs(w - q * sf)
+    assert np.all(err <= sf * (0.5 + 1e-3))            # round-to-nearest bound (bf16 scale)
+    g = np.abs(w.reshape(64, 4, 128))
+    arg = g.argmax(axis=2)
+    qmax = np.take_along_axis(np.abs(q.reshape(64, 4, 128)), arg[..., None], axis=2)
+    assert np.all(qmax == 7)
+
+
+def test_int4_zero_point_invariants_random():
+    rng = np.random.default_rng(1)
+    w = (rng.standard_normal((32, 256)) * 0.02).astype(np.float32)
+    z = rng.integers(0, 16, size=(32, 2))
+    q, s = Q.quant_int4(w, zeros=z)
+    assert q.min() >= 0 and q.max() <= 15
+    sf = np.repeat(s, 128, axis=1)
+    zf = np.repeat(z, 128, axis=1)
+    inside = (q > 0) & (q < 15)
+    err = np.abs(w - (q - zf) * sf)
+    assert np.all(err[inside] <= sf[inside] * (0.5 + 1e-3))
+    # clamped entries moved towards the range edge
+    assert np.all(w[q == 0] / sf[q == 0] - (0 - zf[q == 0]) <= 0.5 + 1e-3)
+
+
+def test_mxfp4_scale_rule_closed_forms():
+    def one(amax_val, probe):
+        w = np.zeros((1, 32))
+        w[0, 0] = amax_val
+        w[0, 1] = probe
+        codes, e = Q.quant_mxfp4(w)
+        return int(e[0, 0]), int(codes[0, 0]), int(codes[0, 1])
+    assert one(6.0, 0.0) == (127, 7, 0)        # floor(log2 6) = 2 -> 2-2+127
+    assert one(5.0, 0.75) == (127, 6, 2)       # 5 is a tie between 4 and 6 -> 4; 0.75 -> 1
+    assert one(12.0, -3.0) == (128, 7, 0xB)    # scale 2: 12/2 = 6, -3/2 = -1.5
+    assert one(0.1, 0.0) == (121, 7, 0)        # 0.1 * 2^6 = 6.4 saturates to 6
+    codes, e = Q.quant_mxfp4(np.zeros((1, 32)))
+    assert e[0, 0] == 0 and np.all(codes == 0)
+
+
+def test_mxfp4_invariants_random():
+    rng = np.random.default_rng(2)
+    w = (rng.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    codes, e = Q.quant_mxfp4(w)
+    what = Q.dequant_mxfp4(codes, e)
+    scale = np.repeat(F.decode_e8m0(e), 32, axis=1)
+    mags = np.abs(F.decode_e2m1(codes))
+    assert mags.max() <= 6
+    # the block maximum lands on 4 or 6 (amax / 2^(floor(log2 amax)-2) is in [4, 8))
+    blk = np.abs(w.reshape(16, 8, 32)).argmax(axis=2)
+    top = np.take_along_axis(mags.reshape(16, 8, 32), blk[..., None], axis=2)
+    assert set(np.unique(top)) <= {4.0, 6.0}
+    # error of RNE on the e2m1 grid: at most half the local spacing (1 above 2, 2 above 4)
+    r = np.abs(w) / scale
+    spacing = np.where(r < 2, 0.5, np.where(r < 4, 1.0, 2.0))
+    assert np.all(np.abs(w - what) <= scale * spacing / 2 + scale * np.maximum(r - 6, 0) + 1e-12)
+
+
+def test_fp8_per_token_closed_form():
+    x = np.array([[448.0, -1.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0], [2.0, 1.0, -0.5, 0.25]])
+    xq, s = Q.quant_fp8_per_token(x)
+    np.testing.assert_array_equal(s, [1.0, 0.0, np.float32(2.0 / 448.0)])
+    np.testing.assert_array_equal(xq[0], [0x7E, 0xB8, 0x30, 0x00])
+    assert np.all(xq[1] == 0)
+    assert xq[2, 0] == 0x7E                           # the row maximum maps to 448
+
+
+def test_fp8_per_token_invariants_random():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((8, 1024)).astype(np.float32)
+    x = x.astype(np.float64)
+    xq, s = Q.quant_fp8_per_token(x)
+    back = Q.dequant_fp8_per_token(xq, s)
+    big = np.abs(x) > 2.0 ** -6 * s[:, None] * 448 / 448  # normal range of e4m3 after scaling
+    rel = np.abs(back - x)[big] / np.abs(x)[big]
+    assert rel.max() <= 2.0 ** -4 + 1e-6                # 3 fraction bits: half-ulp relative
+    assert np.all(np.abs(F.decode_e4m3(xq)).max(axis=1) == 448)
+
+
+def test_nvfp4_closed_form():
+    # tensor amax 2688 -> g = 1; block amax 6 -> sb = 1 (code 0x38)
+    v = np.zeros((1, 32))
+    v[0, 0] = 2688.0
+    v[0, 16:20] = [6.0, -3.0, 1.0, 0.25]
+    codes, sb, g = Q.quant_nvfp4(v)
+    assert g == 1.0
+    assert sb[0, 1] == 0x38
+    np.testing.assert_array_equal(codes[0, 16:20], [7, 0xD, 2, 0])
+    assert sb[0, 0] == 0x7E and codes[0, 0] == 7      # 2688/6 = 448 -> element 6
+    c, s2, g2 = Q.quant_nvfp4(np.zeros((2, 16)))
+    assert g2 == 1.0 and np.all(s2 == 0) and np.all(c == 0)
+
+
+def test_nvfp4_invariants_random():
+    rng = np.random.default_rng(4)
+    v = (rng.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    codes, sb, g = Q.quant_nvfp4(v)
+    assert g == np.float32(np.abs(v).max() / np.float32(2688.0))
+    back = Q.dequant_nvfp4(codes, sb, g)
+    scale = np.repeat(F.decode_e4m3(sb), 16, axis=1) * g
+    assert np.all(np.abs(back - v) <= scale * 1.0 + 1e-12)  # half of the widest e2m1 gap (2)
