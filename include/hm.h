@@ -1,0 +1,202 @@
+/*
+ * hm.h — C ABI of libhm.so, a GB300 (sm_103a) library for the weight-quantized linear
+ * layer Y[M,N] = X[M,K] * dequant(Wq[N,K])^T and its grouped MoE variant.
+ *
+ * Method: the Humming quantized-inference kernels as described on the explainer page
+ * "vLLM Humming은 4비트를 어떻게 계산하나" (portfolio.ywsung.com): weights are put in a
+ * common quantized representation, preprocessed once into a device-friendly layout
+ * (section "표현을 맞춘 다음 GPU가 읽기 좋은 배치로 바꾼다"), and combined with activations
+ * that arrive per call (same section, figure "Humming의 전처리·세 설정·JIT 컴파일·추론
+ * 흐름"). The linear layer is X*W^T with W stored [N,K] (section "같은 가중치도 한
+ * 토큰과 많은 토큰에서 비용이 다르다"); MoE splits tokens by expert (same section, MoE
+ * paragraph). Formats named on the news pages (news.cocoloop.cn, "하나의 라이브러리로 긴
+ * 포맷 목록을 포괄"): W4A16, W4A8, W4A4, MXFP4, NVFP4.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, unless stated otherwise.
+ *     The library never allocates device memory; sizes come from the *_size queries.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls are
+ *     stream-ordered and asynchronous: no host synchronisation, no host reads of device data.
+ *   - Arguments are validated on the host before any launch; a failed check returns
+ *     HM_ERR_INVALID_ARG / HM_ERR_UNSUPPORTED / HM_ERR_WORKSPACE and launches nothing.
+ *     A CUDA launch error returns HM_ERR_CUDA. No C++ exception crosses the ABI.
+ *   - Device-side failures (a packed-weight header that does not match the call, or a
+ *     pipeline wait that exceeded its time limit) set a device error word that
+ *     hm_get_device_error() returns and clears; the kernel then stops its work early.
+ *   - All matrices are row-major. bf16 is IEEE bfloat16. Output Y is bf16, rounded once
+ *     (nearest-even) from an fp32 accumulator.
+ *   - Concurrent calls that share a workspace buffer on different streams race.
+ */
+#ifndef HM_H_
+#define HM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hm_status {
+  HM_OK = 0,
+  HM_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad offsets length */
+  HM_ERR_UNSUPPORTED = 2,   /* format/shape combination not implemented */
+  HM_ERR_WORKSPACE = 3,     /* workspace smaller than hm_workspace_size() */
+  HM_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  HM_ERR_DEVICE = 5         /* device error word was set (see hm_get_device_error) */
+} hm_status;
+
+/* Weight formats.
+ *  HM_W4A16_INT4  : INT4 codes, one bf16 scale per 128 along K, optional u4 zero-point per
+ *                   group; restored weight bf16((q - z) * s) (z = 0, q signed, when no
+ *                   zero-point). bf16 activations, kind::f16 tensor-core MMA.
+ *  HM_W4A16_MXFP4 : e2m1 codes with an E8M0 scale per 32 along K (OCP MX v1.0); restored
+ *                   e2m1 * 2^(e-127); bf16 activations (the MoE "MXFP4 W4A16" path).
+ *  HM_W4A8_MXFP4  : same weights; activations FP8 e4m3 with one fp32 scale per token.
+ *  HM_W4A4_NVFP4  : e2m1 codes, e4m3 scale per 16 along K and one fp32 tensor scale, for
+ *                   both weights and activations. */
+typedef enum hm_format {
+  HM_W4A16_INT4 = 1,
+  HM_W4A16_MXFP4 = 2,
+  HM_W4A8_MXFP4 = 3,
+  HM_W4A4_NVFP4 = 4
+} hm_format;
+
+/* Description of one quantized weight matrix W[N,K] in the common ("standard") format.
+ *  has_zero     : HM_W4A16_INT4 only; 1 = zero-points present.
+ *  tensor_scale : HM_W4A4_NVFP4 only; the fp32 per-tensor scale gW (ignored otherwise).
+ * Shape rules: N >= 1; K % 128 == 0 for formats 1-3, K % 64 == 0 for format 4. */
+typedef struct hm_weight_desc {
+  int32_t fmt;
+  int32_t has_zero;
+  int64_t N;
+  int64_t K;
+  float tensor_scale;
+} hm_weight_desc;
+
+/* ---------------------------------------------------------------- preprocessing (once) */
+
+/* Bytes of the packed weight buffer for `desc` (256-byte header + padded payload), or 0 if
+ * the description is invalid. Host-only, no CUDA call. */
+size_t hm_packed_size(const hm_weight_desc* desc);
+
+/* Quantize an fp32 weight W[N,K] (device) into the standard format by round-to-nearest
+ * (the explainer page's INT4 rule, section "4비트 값에는 스케일이라는 해석 규칙이 붙는다",
+ * generalised per format):
+ *   HM_W4A16_INT4 : s = bf16(fp32(max|w| over 128)/7); q = clamp(rne(fp32(w/s)) [+z]) into
+ *                   [-8,7] (or [0,15] with the zero-points read from `zeros_in`).
+ *   MXFP4 formats : E8M0 e = clamp(floor(log2 amax32) - 2 + 127, 0, 254); code = e2m1(w/2^(e-127)).
+ *   HM_W4A4_NVFP4 : g = fp32(amax/2688) computed on the device and written to *g_out;
+ *                   sb = e4m3(fp32(fp32(amax16/6)/g)); code = e2m1(fp32(w/fp32(sb*g))).
+ * Outputs (device): q_out packed codes [N][K/2] (even k in the low nibble; INT4 nibbles are
+ * two's complement without zero-points, unsigned with them); scales_out [N][K/g] (bf16 for
+ * INT4 g=128; one byte per code for MXFP4 g=32 and NVFP4 g=16); g_out (NVFP4 only, fp32).
+ * `ws` needs hm_quantize_workspace_size() bytes (NVFP4 amax partials; may be NULL otherwise). */
+size_t hm_quantize_workspace_size(const hm_weight_desc* desc);
+hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const uint8_t* zeros_in,
+                             void* q_out, void* scales_out, float* g_out, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Pad and relayout the standard-format weight into `packed` (device, hm_packed_size bytes,
+ * 256-byte aligned). Inputs (device): q [N][K/2] packed codes as above; scales [N][K/g];
+ * zeros [N][K/128] one u4 value per byte (HM_W4A16_INT4 with has_zero, else NULL).
+ * For HM_W4A4_NVFP4 the header records desc->tensor_scale as gW.
+ * Layout (tiles of 128 rows; the order the GEMM kernels stream): see README of the packed
+ * layout in DESIGN; INT4/MXFP4-W4A16 use 128x128 "units" holding interleaved nibbles plus
+ * per-row scales (and zero-points); W4A8/W4A4 use row-major codes plus 512-byte scale atoms. */
+hm_status hm_transform(const hm_weight_desc* desc, const void* q, const void* scales,
+                       const void* zeros, void* packed, void* stream);
+
+/* Test hook: restore the packed weight to bf16 W[N,K] (device). Bit-exact definition of the
+ * restored values used by the GEMM (bf16((q-z)*s), e2m1*2^(e-127), or, for NVFP4,
+ * bf16(e2m1*sb) without the tensor scale, exact). */
+hm_status hm_dequant(const hm_weight_desc* desc, const void* packed, void* w_bf16, void* stream);
+
+/* ---------------------------------------------------------------- activations (per call) */
+
+/* Per-token FP8 quantization of bf16 X[M,K] (K % 16 == 0): per row amax; s_tok = fp32(amax/448);
+ * inv = fp32(448/amax); xq = e4m3 (RNE, satfinite) of fp32(x*inv). A zero row gives s_tok = 0
+ * and xq = 0. Outputs: xq [M][K] bytes, s_tok [M] fp32. (The W4A8 activation path of the
+ * explainer page, section "가중치 형식, 활성값, 백엔드를 한 줄에 적는다".) */
+hm_status hm_quant_act_fp8(const void* x, int64_t M, int64_t K, void* xq, float* s_tok,
+                           void* stream);
+
+/* NVFP4 quantization of bf16 X[M,K] (K % 64 == 0). If `g_in` is non-NULL it is a device fp32
+ * holding gX; else gX = fp32(amax(X)/2688) (1 for an all-zero X) is computed on the device
+ * (needs `ws` of hm_act_workspace_size bytes). gX is written to *g_out (device fp32).
+ * Outputs: codes [M][K/2] (even k low nibble); block scales (e4m3) in 512-byte atoms
+ * [ceil(M/128)][K/64], byte (m%32)*16 + ((m%128)/32)*4 + (k%64)/16 within an atom;
+ * hm_act_scale_size() bytes. */
+size_t hm_act_scale_size(int64_t M, int64_t K);
+size_t hm_act_workspace_size(int64_t M, int64_t K);
+hm_status hm_quant_act_nvfp4(const void* x, int64_t M, int64_t K, const float* g_in, void* xq,
+                             void* xs, float* g_out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- GEMM */
+
+/* Workspace bytes hm_gemm / hm_moe_gemm need for this problem (split-K partials and tile
+ * counters, internal activation quantization). Host-only. `M` is rows for MoE. */
+size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
+
+/* The workspace must be zero-filled once after allocation (cudaMemset); the library leaves
+ * the counters it uses back at zero after every call, so it can be reused across calls. */
+
+/* Y[M,N] (bf16) = X[M,K] * dequant(W)^T.
+ *  HM_W4A16_INT4 / HM_W4A16_MXFP4 : x = bf16 [M][K]; x_scale, x_global ignored.
+ *  HM_W4A8_MXFP4 : x = e4m3 [M][K] with x_scale = s_tok fp32 [M]; or, when x_scale is NULL,
+ *                  x = bf16 [M][K] quantized internally (hm_quant_act_fp8) into `ws`.
+ *                  Y = s_tok[m] * sum_k e4m3(x)*what.
+ *  HM_W4A4_NVFP4 : x = codes [M][K/2], x_scale = scale atoms, x_global = device fp32 gX; or,
+ *                  when x_scale is NULL, x = bf16 [M][K] quantized internally.
+ *                  Y = gX*gW*sum(blocks) sbX*sbW*sum e2m1X*e2m1W.
+ * M >= 0 (M = 0 is a no-op), N and K must match the packed header (checked on the device).
+ * x must be 16-byte aligned, packed 256-byte aligned. ws: hm_workspace_size bytes. */
+hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* x_global,
+                  const void* packed, void* y, int64_t M, int64_t N, int64_t K, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* Grouped GEMM over expert-sorted rows: for each expert e, rows
+ * [expert_offsets[e], expert_offsets[e+1]) of x are multiplied by expert e's weight:
+ * y[r,:] = x[r,:] * dequant(W_e)^T. expert_offsets: device int32 [E+1], non-decreasing,
+ * offsets[0] = 0, offsets[E] = rows (read on the device only). packed: device array of E
+ * device pointers, each a packed weight of the same (fmt, N, K). Formats HM_W4A16_INT4 and
+ * HM_W4A16_MXFP4. Experts with no rows cost nothing. */
+hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
+                      const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- plan / diagnostics */
+
+/* The kernel configuration hm_gemm would use: token tile (MMA N), pipeline stages, split
+ * (number of CTAs sharing one output tile along K; 1 = none) and grid size, for a device
+ * with `num_sms` SMs. Host-only, no CUDA call. */
+typedef struct hm_plan_info {
+  int32_t bucket;      /* M bucket index: 0: M<=16, 1: <=64, 2: <=256, 3: <=1024, 4: >1024 */
+  int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension) */
+  int32_t tile_n;      /* weight rows per tile (tcgen05 MMA M dimension, 128) */
+  int32_t tile_k;      /* K per pipeline stage */
+  int32_t stages;      /* load-pipeline depth */
+  int32_t stream_k;    /* 1 if the K loop is split across CTAs (stream-K) */
+  int32_t grid;        /* CTAs launched */
+  int32_t tiles;       /* output tiles */
+} hm_plan_info;
+hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                  hm_plan_info* out);
+
+/* Returns and clears the device error word on the current device (synchronises `stream`).
+ * 0 = no error; bit 0: packed header mismatch; bit 1: pipeline wait timed out;
+ * bit 2: bad expert offsets. */
+uint32_t hm_get_device_error(void* stream);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on an mbarrier
+ * nothing will complete, with a limit of `timeout_ns` nanoseconds; the kernel gives up,
+ * sets bit 1 of the device error word and returns. */
+hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
+
+const char* hm_status_string(hm_status s);
+const char* hm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HM_H_ */

@@ -1,0 +1,476 @@
+// C ABI of libhm.so (declared in include/hm.h): argument validation, the per-M-bucket plan,
+// tensor-map encoding, workspace carving and kernel dispatch. Host code only; every step of
+// the computation runs in the kernels of the other translation units.
+//
+// The split between a once-per-layer preprocessing call (hm_transform) and per-call GEMMs
+// follows the explainer page "vLLM Humming은 4비트를 어떻게 계산하나", section "표현을 맞춘
+// 다음 GPU가 읽기 좋은 배치로 바꾼다" (transform() once, then layer(inputs)); the page's
+// "Tuning Config" (tile shape, pipeline stages) is reduced here to a fixed table keyed by
+// the M bucket, the device-specific heuristic the news page says Humming also uses
+// (news.cocoloop.cn, section "명시된 약점").
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "hm.h"
+#include "hm_kernels.h"
+#include "hm_layout.h"
+
+namespace hm {
+
+__device__ uint32_t g_hm_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSmsForSizing = 256;  // workspace queries do not know the device
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+struct DeviceInfo {
+  int dev;
+  int num_sms;
+  uint32_t* err;
+};
+
+// Per-device set-up, done once with that device current: SM count and the device address of
+// the error word.
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_hm_error) != cudaSuccess) return false;
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  out->dev = dev;
+  out->num_sms = g_num_sms[dev];
+  out->err = g_err_ptr[dev];
+  return true;
+}
+
+uint64_t timeout_ns() {
+  const char* s = std::getenv("HM_WAIT_TIMEOUT_NS");
+  if (s && *s) return std::strtoull(s, nullptr, 10);
+  return kDefaultTimeoutNs;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* s = std::getenv(name);
+  return (s && *s) ? std::atoi(s) : dflt;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A4Nv; }
+
+bool valid_k(int32_t fmt, int64_t k) {
+  if (k <= 0) return false;
+  return fmt == kW4A4Nv ? (k % 64 == 0) : (k % 128 == 0);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int bucket;
+  int tile_m;
+  int tile_k;
+  int stages;
+  int stream_k;
+  int grid;
+  int64_t tiles;
+  int64_t num_m_tiles;
+  int64_t num_n_tiles;
+  int64_t kb_total;
+};
+
+int bucket_of(int64_t m) {
+  if (m <= 16) return 0;
+  if (m <= 64) return 1;
+  if (m <= 256) return 2;
+  if (m <= 1024) return 3;
+  return 4;
+}
+
+// Token tile (tcgen05 MMA N) per M: the smallest of 16/32/64/128 covering M, 128 beyond.
+int tile_m_for(int32_t fmt, int64_t m) {
+  const int forced = env_int("HM_TILE_M", 0);
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
+  (void)fmt;
+  if (m <= 16) return 16;
+  if (m <= 32) return 32;
+  if (m <= 64) return 64;
+  return 128;
+}
+
+Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
+  Plan p{};
+  p.bucket = bucket_of(m);
+  p.tile_m = tile_m_for(fmt, m);
+  p.tile_k = fmt == kW4A4Nv ? 256 : 128;
+  p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(p.tile_m) : mx_stages(fmt, p.tile_m);
+  p.num_m_tiles = ceil_div(m > 0 ? m : 1, p.tile_m);
+  p.num_n_tiles = pad_n(n) / 128;
+  p.kb_total = pad_k(fmt, k) / p.tile_k;
+  p.tiles = p.num_m_tiles * p.num_n_tiles;
+  const int sk_env = env_int("HM_STREAM_K", -1);
+  p.stream_k = sk_env >= 0 ? (sk_env != 0) : (p.tiles < num_sms ? 1 : 0);
+  const int64_t total = p.tiles * p.kb_total;
+  const int64_t units = p.stream_k ? total : p.tiles;
+  p.grid = static_cast<int>(units < num_sms ? units : num_sms);
+  if (p.grid < 1) p.grid = 1;
+  return p;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t partial, counters, act_q, act_s, act_g, act_amax, total;
+};
+
+WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_act) {
+  const Plan p = make_plan(fmt, m, n, k, kMaxSmsForSizing);
+  WsLayout w{};
+  size_t off = 0;
+  w.partial = off;
+  off += align_up(static_cast<size_t>(kMaxSmsForSizing) * 2 * p.tile_m * 128 * sizeof(float));
+  w.counters = off;
+  off += align_up(static_cast<size_t>(p.tiles) * 4 * sizeof(uint32_t));
+  w.act_q = w.act_s = w.act_g = w.act_amax = off;
+  if (internal_act && fmt == kW4A8Mx) {
+    w.act_q = off;
+    off += align_up(static_cast<size_t>(m) * k);
+    w.act_s = off;
+    off += align_up(static_cast<size_t>(m) * sizeof(float));
+  } else if (internal_act && fmt == kW4A4Nv) {
+    w.act_q = off;
+    off += align_up(static_cast<size_t>(m) * k / 2);
+    w.act_s = off;
+    off += align_up(static_cast<size_t>(ceil_div(m, 128)) * (k / 64) * kAtomBytes);
+    w.act_g = off;
+    off += align_up(sizeof(float));
+    w.act_amax = off;
+    off += align_up(static_cast<size_t>(act_amax_blocks(m, k)) * sizeof(float));
+  }
+  w.total = off;
+  return w;
+}
+
+hm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HM_OK : HM_ERR_CUDA; }
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace hm
+
+using namespace hm;
+
+extern "C" {
+
+size_t hm_packed_size(const hm_weight_desc* d) {
+  if (d == nullptr || !valid_fmt(d->fmt) || d->N <= 0 || !valid_k(d->fmt, d->K)) return 0;
+  if (d->has_zero && d->fmt != kW4A16Int4) return 0;
+  return kHeaderBytes + payload_bytes(d->fmt, d->N, d->K, d->has_zero != 0);
+}
+
+size_t hm_quantize_workspace_size(const hm_weight_desc* d) {
+  if (d == nullptr || d->fmt != kW4A4Nv) return 0;
+  return 512 * sizeof(float);
+}
+
+hm_status hm_quantize_weight(const hm_weight_desc* d, const float* w, const uint8_t* zeros_in, void* q_out,
+                             void* scales_out, float* g_out, void* ws, size_t ws_bytes, void* stream) {
+  if (hm_packed_size(d) == 0 || w == nullptr || q_out == nullptr || scales_out == nullptr)
+    return HM_ERR_INVALID_ARG;
+  if (d->has_zero && zeros_in == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(q_out, 4)) return HM_ERR_INVALID_ARG;
+  if (d->fmt == kW4A4Nv) {
+    if (g_out == nullptr) return HM_ERR_INVALID_ARG;
+    if (ws == nullptr || ws_bytes < hm_quantize_workspace_size(d)) return HM_ERR_WORKSPACE;
+  }
+  if (d->fmt != kW4A4Nv && d->K % 128 != 0) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_quantize_weight(d->fmt, d->has_zero, d->N, d->K, w, zeros_in,
+                                            static_cast<uint8_t*>(q_out), scales_out, g_out,
+                                            static_cast<float*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+hm_status hm_transform(const hm_weight_desc* d, const void* q, const void* scales, const void* zeros, void* packed,
+                       void* stream) {
+  if (hm_packed_size(d) == 0 || q == nullptr || scales == nullptr || packed == nullptr) return HM_ERR_INVALID_ARG;
+  if (d->has_zero && zeros == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(q, 16) || !aligned(scales, 4)) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_transform(d->fmt, d->has_zero, d->N, d->K, d->tensor_scale,
+                                      static_cast<const uint8_t*>(q), scales, static_cast<const uint8_t*>(zeros),
+                                      static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream)));
+}
+
+hm_status hm_dequant(const hm_weight_desc* d, const void* packed, void* w_bf16, void* stream) {
+  if (hm_packed_size(d) == 0 || packed == nullptr || w_bf16 == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(w_bf16, 16)) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_dequant(d->fmt, d->has_zero, d->N, d->K, static_cast<const uint8_t*>(packed),
+                                    static_cast<__nv_bfloat16*>(w_bf16), static_cast<cudaStream_t>(stream)));
+}
+
+hm_status hm_quant_act_fp8(const void* x, int64_t M, int64_t K, void* xq, float* s_tok, void* stream) {
+  if (M < 0 || K <= 0 || K % 16 != 0) return HM_ERR_INVALID_ARG;
+  if (M == 0) return HM_OK;
+  if (x == nullptr || xq == nullptr || s_tok == nullptr || !aligned(x, 16) || !aligned(xq, 8))
+    return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_act_fp8(static_cast<const __nv_bfloat16*>(x), M, K, static_cast<uint8_t*>(xq), s_tok,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t hm_act_scale_size(int64_t M, int64_t K) {
+  if (M < 0 || K <= 0 || K % 64 != 0) return 0;
+  return static_cast<size_t>(ceil_div(M, 128)) * (K / 64) * kAtomBytes;
+}
+
+size_t hm_act_workspace_size(int64_t M, int64_t K) {
+  return static_cast<size_t>(act_amax_blocks(M, K)) * sizeof(float);
+}
+
+hm_status hm_quant_act_nvfp4(const void* x, int64_t M, int64_t K, const float* g_in, void* xq, void* xs,
+                             float* g_out, void* ws, size_t ws_bytes, void* stream) {
+  if (M < 0 || K <= 0 || K % 64 != 0) return HM_ERR_INVALID_ARG;
+  if (M == 0) return HM_OK;
+  if (x == nullptr || xq == nullptr || xs == nullptr || g_out == nullptr || !aligned(x, 16) || !aligned(xq, 8))
+    return HM_ERR_INVALID_ARG;
+  if (g_in == nullptr && (ws == nullptr || ws_bytes < hm_act_workspace_size(M, K))) return HM_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_act_nvfp4(static_cast<const __nv_bfloat16*>(x), M, K, g_in, static_cast<uint8_t*>(xq),
+                                      static_cast<uint8_t*>(xs), g_out, static_cast<float*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K) {
+  if (!valid_fmt(fmt) || M < 0 || N <= 0 || !valid_k(fmt, K)) return 0;
+  return ws_layout(fmt, M, N, K, true).total;
+}
+
+hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms, hm_plan_info* out) {
+  if (out == nullptr || !valid_fmt(fmt) || M < 0 || N <= 0 || !valid_k(fmt, K) || num_sms <= 0 ||
+      num_sms > kMaxSmsForSizing)
+    return HM_ERR_INVALID_ARG;
+  const Plan p = make_plan(fmt, M, N, K, num_sms);
+  out->bucket = p.bucket;
+  out->tile_m = p.tile_m;
+  out->tile_n = 128;
+  out->tile_k = p.tile_k;
+  out->stages = p.stages;
+  out->stream_k = p.stream_k;
+  out->grid = p.grid;
+  out->tiles = static_cast<int32_t>(p.tiles);
+  return HM_OK;
+}
+
+hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* x_global, const void* packed,
+                  void* y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_fmt(fmt) || M < 0 || N <= 0 || !valid_k(fmt, K)) return HM_ERR_INVALID_ARG;
+  if (M == 0) return HM_OK;
+  if (x == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 4) || (N % 2) != 0) return HM_ERR_INVALID_ARG;
+  const bool internal_act = (fmt == kW4A8Mx || fmt == kW4A4Nv) && x_scale == nullptr;
+  if (fmt == kW4A4Nv && !internal_act && x_global == nullptr) return HM_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(fmt, M, N, K, internal_act);
+  if (ws == nullptr || ws_bytes < wl.total) return HM_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+
+  if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
+    F16Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, p.tile_m))
+      return HM_ERR_CUDA;
+    prm.packed = static_cast<const uint8_t*>(packed);
+    prm.y = static_cast<__nv_bfloat16*>(y);
+    prm.partial = reinterpret_cast<float*>(wsb + wl.partial);
+    prm.counters = reinterpret_cast<uint32_t*>(wsb + wl.counters);
+    prm.err = di.err;
+    prm.m = M;
+    prm.n = N;
+    prm.k = K;
+    prm.fmt = fmt;
+    prm.num_experts = 0;
+    prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
+    prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
+    prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
+    prm.timeout_ns = timeout_ns();
+    return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
+  }
+
+  // Block-scaled formats: quantize bf16 activations first when the caller passed none.
+  const uint8_t* xq = static_cast<const uint8_t*>(x);
+  const void* xs = x_scale;
+  const float* xg = x_global;
+  if (internal_act) {
+    if (!aligned(x, 16)) return HM_ERR_INVALID_ARG;
+    uint8_t* q = wsb + wl.act_q;
+    if (fmt == kW4A8Mx) {
+      float* s = reinterpret_cast<float*>(wsb + wl.act_s);
+      const cudaError_t e = launch_act_fp8(static_cast<const __nv_bfloat16*>(x), M, K, q, s, st);
+      if (e != cudaSuccess) return HM_ERR_CUDA;
+      xs = s;
+    } else {
+      float* g = reinterpret_cast<float*>(wsb + wl.act_g);
+      const cudaError_t e = launch_act_nvfp4(static_cast<const __nv_bfloat16*>(x), M, K, nullptr, q,
+                                             wsb + wl.act_s, g, reinterpret_cast<float*>(wsb + wl.act_amax), st);
+      if (e != cudaSuccess) return HM_ERR_CUDA;
+      xs = wsb + wl.act_s;
+      xg = g;
+    }
+    xq = q;
+  }
+  MxParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const int64_t n_pad = pad_n(N), k_pad = pad_k(fmt, K);
+  const uint8_t* body = static_cast<const uint8_t*>(packed) + kHeaderBytes;
+  bool ok;
+  if (fmt == kW4A8Mx) {
+    // weights: e2m1 codes, expanded by TMA to one byte per code in shared memory
+    ok = encode_2d(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, body, k_pad, n_pad, k_pad / 2, 128, 128) &&
+         encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K, M, K, 128, p.tile_m);
+  } else {
+    ok = encode_2d(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, body, k_pad / 2, n_pad, k_pad / 2, 128, 128) &&
+         encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K / 2, M, K / 2, 128, p.tile_m);
+  }
+  if (!ok) return HM_ERR_CUDA;
+  prm.packed = static_cast<const uint8_t*>(packed);
+  prm.w_atoms = body + static_cast<size_t>(n_pad) * k_pad / 2;
+  prm.x_atoms = static_cast<const uint8_t*>(xs);
+  prm.s_tok = static_cast<const float*>(xs);
+  prm.x_global = xg;
+  prm.y = static_cast<__nv_bfloat16*>(y);
+  prm.partial = reinterpret_cast<float*>(wsb + wl.partial);
+  prm.counters = reinterpret_cast<uint32_t*>(wsb + wl.counters);
+  prm.err = di.err;
+  prm.m = M;
+  prm.n = N;
+  prm.k = K;
+  prm.fmt = fmt;
+  prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
+  prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
+  prm.k_blocks = static_cast<int32_t>(p.kb_total);
+  prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
+  prm.timeout_ns = timeout_ns();
+  const cudaError_t e = launch_mx_gemm(prm, p.tile_m, st);
+  if (e == cudaErrorNotSupported) return HM_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
+                      const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (fmt != kW4A16Int4 && fmt != kW4A16Mx) return valid_fmt(fmt) ? HM_ERR_UNSUPPORTED : HM_ERR_INVALID_ARG;
+  if (rows < 0 || N <= 0 || !valid_k(fmt, K) || E < 1 || E > 1024) return HM_ERR_INVALID_ARG;
+  if (rows == 0) return HM_OK;
+  if (x == nullptr || expert_offsets == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 4) || (N % 2) != 0 || !aligned(packed, 8)) return HM_ERR_INVALID_ARG;
+  (void)ws;
+  (void)ws_bytes;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  // Token tile from the mean rows per expert (per-expert counts stay on the device).
+  const int64_t mean = rows / E;
+  int tile_m = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : 128));
+  const int forced = env_int("HM_MOE_TILE_M", 0);
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) tile_m = forced;
+  F16Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, rows, K * 2, 64, tile_m)) return HM_ERR_CUDA;
+  prm.packed_list = reinterpret_cast<const uint8_t* const*>(packed);
+  prm.offsets = expert_offsets;
+  prm.y = static_cast<__nv_bfloat16*>(y);
+  prm.err = di.err;
+  prm.m = rows;
+  prm.n = N;
+  prm.k = K;
+  prm.fmt = fmt;
+  prm.num_experts = E;
+  prm.num_m_tiles = 0;
+  prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
+  prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
+  prm.timeout_ns = timeout_ns();
+  return cuda_status(launch_f16_gemm(prm, tile_m, true, cudaStream_t(stream)));
+}
+
+uint32_t hm_get_device_error(void* stream) {
+  DeviceInfo di;
+  if (!device_info(&di)) return 0xFFFFFFFFu;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_hm_error, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return 0xFFFFFFFFu;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_hm_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return 0xFFFFFFFFu;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+}
+
+hm_status hm_debug_wait_timeout(uint64_t timeout_ns_, void* stream) {
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_wait_timeout_probe(di.err, timeout_ns_, static_cast<cudaStream_t>(stream)));
+}
+
+const char* hm_status_string(hm_status s) {
+  switch (s) {
+    case HM_OK: return "ok";
+    case HM_ERR_INVALID_ARG: return "invalid argument";
+    case HM_ERR_UNSUPPORTED: return "unsupported format or shape";
+    case HM_ERR_WORKSPACE: return "workspace too small";
+    case HM_ERR_CUDA: return "CUDA error";
+    case HM_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+const char* hm_version(void) { return "hm 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

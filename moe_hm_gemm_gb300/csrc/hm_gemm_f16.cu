@@ -1,0 +1,493 @@
+// W4A16 GEMM on tcgen05: Y[M,N] = X[M,K] * dequant(W)^T with 4-bit weights restored to bf16
+// in registers and multiplied on the 5th-generation tensor cores (kind::f16, fp32 accumulate
+// in TMEM). Dense and grouped-MoE variants.
+//
+// The computation is the explainer page's linear layer ("vLLM Humming은 4비트를 어떻게
+// 계산하나", section "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다": Y = X * W^T, W
+// stored [N,K], read once and reused over the M rows) with W replaced by its restored value
+// (section "4비트 값에는 스케일이라는 해석 규칙이 붙는다"); the MoE variant is the same
+// product per expert over that expert's contiguous token rows (MoE paragraph of the first
+// section).
+//
+// Design (GB300-first; the pages give no kernel design):
+//  * weights are the MMA's A operand (M = 128 weight rows), tokens its B operand (N =
+//    tile_m in 16..256), so even M = 1 fills the 128-row side of the tensor core;
+//  * one persistent CTA per SM, 10 warps: warp 0 issues the TMA loads (one bulk copy of a
+//    packed 128x128 unit with its scales, two 2-D tensor loads of the X tile), warp 1 owns
+//    TMEM and issues tcgen05.mma from one thread, warps 2-5 restore the unit to bf16 into the
+//    128-byte-swizzled K-major layout the MMA reads, warps 6-9 drain TMEM (tcgen05.ld), round
+//    to bf16 and store Y;
+//  * the accumulator is double-buffered in TMEM so the epilogue of one tile overlaps the
+//    main loop of the next;
+//  * small M uses stream-K (see hm_sched.cuh) so that every SM streams weights; partial tiles
+//    are summed in k order by the last CTA to finish (deterministic, no spinning);
+//  * every wait is bounded (hm_device.cuh).
+#include <cuda_bf16.h>
+
+#include "hm_dequant.cuh"
+#include "hm_device.cuh"
+#include "hm_kernels.h"
+#include "hm_layout.h"
+#include "hm_sched.cuh"
+
+namespace hm {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
+
+template <int BT>
+struct F16Shape {
+  static constexpr int kSL = BT <= 32 ? 8 : (BT == 64 ? 6 : (BT == 128 ? 3 : 2));  // load stages
+  static constexpr int kSA = BT <= 16 ? 3 : 2;                                      // A stages
+  static constexpr int kXStage = BT * 128 * 2;
+  static constexpr int kAOff = 0;
+  static constexpr int kXOff = kSA * kAStage;
+  static constexpr int kWOff = kXOff + kSL * kXStage;
+  static constexpr int kWStage = kUnitMx;  // room for the largest unit
+  static constexpr int kBarOff = kWOff + kSL * kWStage;
+  static constexpr int kNumBars = 3 * kSL + 2 * kSA + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kLutOff = kMiscOff + 32;
+  static constexpr int kMoeOff = kLutOff + 64;
+  static constexpr uint32_t kTmemCols = 2 * BT < 32 ? 32 : 2 * BT;
+  static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
+};
+
+struct TileInfo {
+  int32_t m0, m_end, n0;
+  const uint8_t* base;   // packed weight (header) of this tile's matrix
+  const uint8_t* wbase;  // first unit of this n-tile
+};
+
+// Largest e with prefix[e] <= tile (prefix[0] = 0 <= tile < prefix[E]).
+__device__ __forceinline__ int find_expert(const int32_t* prefix, int experts, int tile) {
+  int lo = 0, hi = experts;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int BT, bool MOE>
+__device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, const int32_t* prefix,
+                                                const int32_t* offs, uint32_t unit) {
+  TileInfo t;
+  const int64_t kb_total = p.k / 128;
+  if (!MOE) {
+    const int mt = tile % p.num_m_tiles;
+    const int nt = tile / p.num_m_tiles;
+    t.m0 = mt * BT;
+    t.m_end = static_cast<int32_t>(p.m < t.m0 + BT ? p.m : t.m0 + BT);
+    t.n0 = nt * 128;
+    t.base = p.packed;
+    t.wbase = p.packed + kHeaderBytes + static_cast<size_t>(nt) * kb_total * unit;
+  } else {
+    const int e = find_expert(prefix, p.num_experts, tile);
+    const int local = tile - prefix[e];
+    const int cnt = offs[e + 1] - offs[e];
+    const int mte = (cnt + BT - 1) / BT;
+    const int nt = local / mte;
+    const int mt = local - nt * mte;
+    t.m0 = offs[e] + mt * BT;
+    t.m_end = min(offs[e + 1], t.m0 + BT);
+    t.n0 = nt * 128;
+    t.base = p.packed_list[e];
+    t.wbase = t.base + kHeaderBytes + static_cast<size_t>(nt) * kb_total * unit;
+  }
+  return t;
+}
+
+__device__ __forceinline__ bool header_ok(const uint8_t* packed, const F16Params& p, uint32_t has_zero) {
+  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
+  return h->magic == kMagic && static_cast<int32_t>(h->fmt) == p.fmt && h->n == p.n &&
+         h->k == p.k && h->has_zero == has_zero;
+}
+
+// Wait without looking at the abort flag (used to drain in-flight work before exit).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > limit_ns) return;
+  }
+}
+
+// WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4.
+template <int BT, int WK, bool MOE>
+__global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
+  using S = F16Shape<BT>;
+  constexpr int SL = S::kSL;
+  constexpr int SA = S::kSA;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* full_w = bars;
+  uint64_t* full_x = bars + SL;
+  uint64_t* empty_l = bars + 2 * SL;
+  uint64_t* full_a = bars + 3 * SL;
+  uint64_t* empty_a = full_a + SA;
+  uint64_t* acc_full = empty_a + SA;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 4);
+  float* lut = reinterpret_cast<float*>(smem + S::kLutOff);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + S::kMoeOff);
+  int32_t* offs = prefix + (MOE ? p.num_experts + 1 : 0);
+  volatile uint32_t* hz_sh = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(&full_w[s], 1);
+      mbar_init(&full_x[s], 1);
+      mbar_init(&empty_l[s], 1 + 4);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&full_a[s], 4);
+      mbar_init(&empty_a[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    *abort_flag = 0u;
+    // The first weight's header decides whether INT4 units carry zero-points; every weight
+    // used must agree with it and with the call's (fmt, N, K).
+    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
+    const uint32_t hz = reinterpret_cast<const PackedHeader*>(first)->has_zero;
+    *hz_sh = (WK == 0 && hz == 1u) ? 1u : 0u;
+    if (!header_ok(first, p, hz)) {
+      atomicOr(p.err, kErrHeader);
+      *abort_flag = 1u;
+    }
+  }
+  if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
+  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+
+  int32_t num_tiles = p.sched.num_tiles;
+  if (MOE) {
+    // Per-expert tile counts and their exclusive prefix (warp 2), offsets copied to shared.
+    if (warp == 2) {
+      const int E = p.num_experts;
+      const int per = (E + 31) / 32;
+      const int e0 = lane * per;
+      int local = 0;
+      bool bad = false;
+      for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+          const int a = p.offsets[e], b = p.offsets[e + 1];
+          bad |= (b < a) || (a < 0) || (b > p.m);
+          offs[e] = a;
+          local += b > a ? ((b - a + BT - 1) / BT) * p.num_n_tiles : 0;
+        }
+      }
+      if (lane == 0) {
+        offs[E] = p.offsets[E];
+        bad |= p.offsets[0] != 0;
+      }
+      int incl = local;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      int run = incl - local;
+      for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+          prefix[e] = run;
+          const int a = p.offsets[e], b = p.offsets[e + 1];
+          run += b > a ? ((b - a + BT - 1) / BT) * p.num_n_tiles : 0;
+        }
+      }
+      if (lane == 31) prefix[E] = incl;
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        atomicOr(p.err, kErrOffsets);
+        *abort_flag = 1u;
+      }
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (MOE) num_tiles = prefix[p.num_experts];
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  SchedIter sched;
+  sched.init(p.sched, num_tiles, blockIdx.x);
+  const int kb_total = p.sched.kb_total;
+  const bool aborted_early = *abort_flag != 0u;
+  const uint32_t has_zero = *hz_sh;
+  const uint32_t kUnit = WK == 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+
+  if (aborted_early) {
+    // nothing to do: fall through to teardown
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_x);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int ls = 0;
+      uint32_t lph = 0;
+      int issued = 0;
+      const uint8_t* last_checked = nullptr;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+        if (MOE) {
+          if (t.base != last_checked) {
+            if (!header_ok(t.base, p, has_zero)) {
+              atomicOr(p.err, kErrHeader);
+              *abort_flag = 1u;
+              break;
+            }
+            last_checked = t.base;
+          }
+        }
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
+          uint8_t* ws = smem + S::kWOff + ls * S::kWStage;
+          uint8_t* xs = smem + S::kXOff + ls * S::kXStage;
+          mbar_arrive_expect_tx(&full_w[ls], kUnit);
+          bulk_g2s(ws, t.wbase + static_cast<size_t>(kb) * kUnit, kUnit, &full_w[ls], pol_w);
+          mbar_arrive_expect_tx(&full_x[ls], S::kXStage);
+          tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[ls], pol_x);
+          tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[ls], pol_x);
+          ++issued;
+          if (++ls == SL) { ls = 0; lph ^= 1u; }
+        }
+      }
+      if (*abort_flag) {
+        // Let copies already in flight land before the CTA's shared memory goes away.
+        const int n = issued < SL ? issued : SL;
+        for (int i = 0; i < n; ++i) {
+          if (--ls < 0) { ls = SL - 1; lph ^= 1u; }
+          drain_wait(&full_w[ls], lph, 100000000ull);
+          drain_wait(&full_x[ls], lph, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, BT);
+      int ls = 0, as = 0;
+      uint32_t lph = 0, aph = 0, acc_i = 0;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        const uint32_t b = acc_i & 1u;
+        if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BT;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(&full_x[ls], lph, wc) || !mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
+            const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+            mma_bf16(d, ad, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty_l[ls]);
+          tc_commit(&empty_a[as]);
+          if (++ls == SL) { ls = 0; lph ^= 1u; }
+          if (++as == SA) { as = 0; aph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[b]);
+        ++acc_i;
+      }
+      // All tcgen05 work of this thread has completed once `drain` flips.
+      tc_commit(drain);
+      drain_wait(drain, 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ dequant warps
+    const int r = threadIdx.x - 64;  // weight row within the tile
+    int ls = 0, as = 0;
+    uint32_t lph = 0, aph = 0;
+    Segment seg;
+    bool ok = true;
+    while (ok && sched.next(seg)) {
+      for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+        if (!mbar_wait(&full_w[ls], lph, wc) || !mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
+        const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage);
+        uint4 c[4];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) c[c4] = ld_shared_v4(wsa + c4 * 2048 + r * 16);
+        __nv_bfloat162 zz, ss;
+        uint32_t e4 = 0;
+        if (WK == 2) {
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e4) : "r"(wsa + kUnitCodes + 4 * r));
+        } else {
+          uint16_t sb;
+          asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(wsa + kUnitCodes + 2 * r));
+          ss = bf16_pair(sb);
+          uint32_t z = 8u;
+          if (has_zero) {
+            uint16_t zb;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitInt4 + (r >> 1)));
+            z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
+          }
+          zz = int4_zero_pair(z);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_l[ls]);
+        const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
+          float scale = 0.f;
+          if (WK == 2) scale = pow2f(static_cast<int>((e4 >> (8 * c4)) & 0xFFu) - 127);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t o[4];
+            if (WK == 2) dq_mx_word(words[j], lut, scale, o);
+            else dq_int4_word(words[j], zz, ss, o);
+            const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
+            const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
+                                 ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
+            st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[as]);
+        if (++ls == SL) { ls = 0; lph ^= 1u; }
+        if (++as == SA) { as = 0; aph ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int row = 32 * q + lane;       // weight row within the tile
+    const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
+    uint32_t acc_i = 0;
+    bool first_seg = true;
+    Segment seg;
+    while (sched.next(seg)) {
+      const uint32_t b = acc_i & 1u;
+      if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
+      tc_fence_after();
+      const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+      const int64_t n = static_cast<int64_t>(t.n0) + row;
+      const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
+      float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128;
+#pragma unroll 1
+      for (int j0 = 0; j0 < BT; j0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + j0, v);
+        tmem_wait_ld();
+        if (full) {
+          if (n < p.n) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
+              if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(__uint_as_float(v[jj]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) slot[(j0 + jj) * 128 + row] = __uint_as_float(v[jj]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++acc_i;
+      if (!full) {
+        // Stream-K fix-up, per warp (32 rows): publish the partial, count arrivals; the last
+        // CTA to arrive sums every CTA's partial for these rows in k order.
+        __threadfence();
+        __syncwarp();
+        uint32_t old = 0;
+        uint32_t* ctr = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+        if (lane == 0) old = atomicAdd(ctr, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        const int64_t c_lo = sk_owner(static_cast<int64_t>(seg.tile) * kb_total, total_it, p.sched.grid);
+        const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        if (old == static_cast<uint32_t>(c_hi - c_lo)) {
+          __threadfence();
+#pragma unroll 1
+          for (int j = 0; j < BT; ++j) {
+            const int64_t m = static_cast<int64_t>(t.m0) + j;
+            float acc = 0.f;
+            for (int64_t c = c_lo; c <= c_hi; ++c) {
+              const int which = (sk_start(c, total_it, p.sched.grid) / kb_total == seg.tile) ? 0 : 1;
+              const float* src = p.partial + (static_cast<size_t>(c) * 2 + which) * BT * 128;
+              acc += __ldcg(src + j * 128 + row);
+            }
+            if (m < t.m_end && n < p.n) p.y[m * p.n + n] = __float2bfloat16_rn(acc);
+          }
+          if (lane == 0) *ctr = 0u;
+        }
+      }
+      first_seg = false;
+    }
+  }
+
+  __syncwarp();  // reconverge lanes that skipped a single-thread role before the CTA barrier
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::kTmemCols);
+  }
+}
+
+template <int BT, int WK, bool MOE>
+cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
+  using S = F16Shape<BT>;
+  auto kern = f16_gemm_kernel<BT, WK, MOE>;
+  const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.sched.grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int WK, bool MOE>
+cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
+  switch (tile_m) {
+    case 16: return launch_one<16, WK, MOE>(p, st);
+    case 32: return launch_one<32, WK, MOE>(p, st);
+    case 64: return launch_one<64, WK, MOE>(p, st);
+    case 128: return launch_one<128, WK, MOE>(p, st);
+    case 256: return launch_one<256, WK, MOE>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int f16_stages(int tile_m) {
+  switch (tile_m) {
+    case 16: return F16Shape<16>::kSL;
+    case 32: return F16Shape<32>::kSL;
+    case 64: return F16Shape<64>::kSL;
+    case 128: return F16Shape<128>::kSL;
+    default: return F16Shape<256>::kSL;
+  }
+}
+
+cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st) {
+  if (p.fmt == kW4A16Mx) return moe ? launch_bt<2, true>(p, tile_m, st) : launch_bt<2, false>(p, tile_m, st);
+  return moe ? launch_bt<0, true>(p, tile_m, st) : launch_bt<0, false>(p, tile_m, st);
+}
+
+}  // namespace hm

@@ -1,0 +1,76 @@
+// Kernel parameter blocks and launcher entry points shared between the C ABI (hm_api.cu)
+// and the kernel translation units. Internal to libhm.so.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hm_sched.cuh"
+
+namespace hm {
+
+// W4A16 GEMM (INT4 or MXFP4 weights restored to bf16, kind::f16 MMA), dense or MoE.
+struct F16Params {
+  CUtensorMap tmap_x;                 // X bf16 [rows][K], box {64, tile_m}, 128-byte swizzle
+  const uint8_t* packed;              // dense: packed weight (header first)
+  const uint8_t* const* packed_list;  // MoE: device array of E packed weights
+  const int32_t* offsets;             // MoE: expert offsets [E+1]
+  __nv_bfloat16* y;                   // [rows][N]
+  float* partial;                     // stream-K partial tiles [grid][2][tile_m][128]
+  uint32_t* counters;                 // stream-K arrival counters [num_tiles][4]
+  uint32_t* err;                      // device error word
+  int64_t m, n, k;                    // m = rows
+  int32_t fmt;
+  int32_t num_experts;
+  int32_t num_m_tiles;                // dense only
+  int32_t num_n_tiles;
+  SchedParams sched;
+  uint64_t timeout_ns;
+};
+
+// Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
+struct MxParams {
+  CUtensorMap tmap_w;                 // weight codes
+  CUtensorMap tmap_x;                 // activation codes
+  const uint8_t* packed;              // packed weight (header; scale atoms after the codes)
+  const uint8_t* w_atoms;             // first weight scale atom
+  const uint8_t* x_atoms;             // NVFP4 activation scale atoms
+  const float* s_tok;                 // W4A8 per-token scales [M]
+  const float* x_global;              // W4A4 activation tensor scale (device scalar)
+  __nv_bfloat16* y;
+  float* partial;
+  uint32_t* counters;
+  uint32_t* err;
+  int64_t m, n, k;
+  int32_t fmt;
+  int32_t num_m_tiles;
+  int32_t num_n_tiles;
+  int32_t k_blocks;                   // K_pad / tile_k
+  SchedParams sched;
+  uint64_t timeout_ns;
+};
+
+// Launchers (return a cudaError_t of the launch). `tile_m` and `stages` select an instantiation.
+cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st);
+int f16_stages(int tile_m);
+int mx_stages(int fmt, int tile_m);
+
+// Weight preprocessing and activation quantization launchers (hm_weights.cu, hm_act.cu).
+cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k,
+                                   const float* w, const uint8_t* zeros_in, uint8_t* q_out,
+                                   void* scales_out, float* g_out, float* ws, cudaStream_t st);
+cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, float gw,
+                             const uint8_t* q, const void* scales, const uint8_t* zeros,
+                             uint8_t* packed, cudaStream_t st);
+cudaError_t launch_dequant(int32_t fmt, int32_t has_zero, int64_t n, int64_t k,
+                           const uint8_t* packed, __nv_bfloat16* w, cudaStream_t st);
+cudaError_t launch_act_fp8(const __nv_bfloat16* x, int64_t m, int64_t k, uint8_t* xq, float* s_tok,
+                           cudaStream_t st);
+cudaError_t launch_act_nvfp4(const __nv_bfloat16* x, int64_t m, int64_t k, const float* g_in,
+                             uint8_t* xq, uint8_t* xs, float* g_out, float* ws, cudaStream_t st);
+int act_amax_blocks(int64_t m, int64_t k);
+cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace hm

@@ -1,0 +1,57 @@
+// Packed-weight and activation layout constants shared by the host API and the kernels.
+//
+// The preprocessed weight is a 256-byte header followed by a payload (see include/hm.h).
+// W4A16 formats are stored as 128x128 "units" (128 weight rows x 128 K), n-tile major, each
+// holding the 8 KB of 4-bit codes in the order the dequant warps read them plus the per-row
+// scales (and zero-points) of that K block, so one bulk copy fetches everything a pipeline
+// stage needs. Inside a unit the code of (row r, column kk) sits in the little-endian 32-bit
+// word at byte (kk/32)*2048 + r*16 + ((kk%32)/8)*4, bit 4*((kk%8)/2) + 16*(kk%2): even
+// columns fill the low half-word and odd columns the high one, so a mask of 0x000F000F
+// after a shift yields a bf16x2 pair of consecutive columns. INT4 nibbles are stored offset
+// by 8 when there is no zero-point (u = q + 8), so every INT4 unit restores (u - z) * s.
+#pragma once
+#include <cstdint>
+
+namespace hm {
+
+constexpr uint32_t kMagic = 0x31574D48u;  // "HMW1"
+constexpr uint32_t kHeaderBytes = 256;
+constexpr int kTileN = 128;               // weight rows per tile (tcgen05 MMA M)
+constexpr int kUnitK = 128;               // K per unit / per W4A16 pipeline stage
+constexpr uint32_t kUnitCodes = 8192;     // 128 x 128 nibbles
+constexpr uint32_t kUnitInt4 = 8448;      // + 128 bf16 scales
+constexpr uint32_t kUnitInt4Zp = 8512;    // + 64 bytes of u4 zero-points
+constexpr uint32_t kUnitMx = 8704;        // + 128 x 4 E8M0 scales
+constexpr uint32_t kAtomBytes = 512;      // scale-factor atom (128 rows x 4 scales)
+
+struct PackedHeader {
+  uint32_t magic;
+  uint32_t fmt;
+  int64_t n;
+  int64_t k;
+  int64_t n_pad;
+  int64_t k_pad;
+  uint32_t has_zero;
+  float tensor_scale;
+  uint64_t payload_bytes;
+};
+static_assert(sizeof(PackedHeader) == 56, "header layout");
+
+enum Fmt : int32_t { kW4A16Int4 = 1, kW4A16Mx = 2, kW4A8Mx = 3, kW4A4Nv = 4 };
+
+inline int64_t pad_n(int64_t n) { return (n + kTileN - 1) / kTileN * kTileN; }
+inline int64_t pad_k(int32_t fmt, int64_t k) { return fmt == kW4A4Nv ? (k + 255) / 256 * 256 : k; }
+
+inline uint32_t unit_bytes(int32_t fmt, bool has_zero) {
+  return fmt == kW4A16Mx ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+}
+
+inline uint64_t payload_bytes(int32_t fmt, int64_t n, int64_t k, bool has_zero) {
+  const int64_t np = pad_n(n), kp = pad_k(fmt, k);
+  if (fmt == kW4A16Int4 || fmt == kW4A16Mx)
+    return static_cast<uint64_t>(np / 128) * (kp / 128) * unit_bytes(fmt, has_zero);
+  const int64_t chunk = fmt == kW4A8Mx ? 128 : 64;
+  return static_cast<uint64_t>(np) * kp / 2 + static_cast<uint64_t>(np / 128) * (kp / chunk) * kAtomBytes;
+}
+
+}  // namespace hm

@@ -1,0 +1,201 @@
+"""Python binding of libhm.so (include/hm.h): argument marshalling only.
+
+Every function takes torch tensors (device memory owned by the caller), passes their
+pointers and sizes to the C ABI on the current CUDA stream, and raises HmError on a
+non-OK status. No computation happens here; if the shared library is missing the import
+fails loudly (there is no fallback).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhm.so")
+
+W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4 = 1, 2, 3, 4
+FORMATS = {"w4a16_int4": W4A16_INT4, "w4a16_mxfp4": W4A16_MXFP4,
+           "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4}
+
+
+class HmError(RuntimeError):
+    def __init__(self, status, where):
+        super().__init__(f"{where}: {_lib.hm_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+class WeightDesc(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("has_zero", ctypes.c_int32), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("tensor_scale", ctypes.c_float)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("bucket", "tile_m", "tile_n", "tile_k", "stages", "stream_k", "grid", "tiles")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libhm.so not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, SZ, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    D = ctypes.POINTER(WeightDesc)
+    sig = {
+        "hm_packed_size": (SZ, [D]),
+        "hm_quantize_workspace_size": (SZ, [D]),
+        "hm_quantize_weight": (I32, [D, P, P, P, P, P, P, SZ, P]),
+        "hm_transform": (I32, [D, P, P, P, P, P]),
+        "hm_dequant": (I32, [D, P, P, P]),
+        "hm_quant_act_fp8": (I32, [P, I64, I64, P, P, P]),
+        "hm_act_scale_size": (SZ, [I64, I64]),
+        "hm_act_workspace_size": (SZ, [I64, I64]),
+        "hm_quant_act_nvfp4": (I32, [P, I64, I64, P, P, P, P, P, SZ, P]),
+        "hm_workspace_size": (SZ, [I32, I64, I64, I64]),
+        "hm_gemm": (I32, [I32, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "hm_moe_gemm": (I32, [I32, P, P, I32, P, P, I64, I64, I64, P, SZ, P]),
+        "hm_plan": (I32, [I32, I64, I64, I64, I32, ctypes.POINTER(PlanInfo)]),
+        "hm_get_device_error": (ctypes.c_uint32, [P]),
+        "hm_debug_wait_timeout": (I32, [ctypes.c_uint64, P]),
+        "hm_status_string": (ctypes.c_char_p, [I32]),
+        "hm_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _ = F
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise HmError(status, where)
+
+
+def desc(fmt, n, k, has_zero=False, tensor_scale=1.0):
+    return WeightDesc(int(fmt), int(bool(has_zero)), int(n), int(k), float(tensor_scale))
+
+
+def packed_size(d):
+    return _lib.hm_packed_size(ctypes.byref(d))
+
+
+def quantize_weight(d, w, zeros=None):
+    """fp32 W [N,K] (device) -> (q [N,K/2] uint8, scales, g) in the standard format."""
+    dev = w.device
+    q = torch.empty((d.N, d.K // 2), dtype=torch.uint8, device=dev)
+    if d.fmt == W4A16_INT4:
+        scales = torch.empty((d.N, d.K // 128), dtype=torch.bfloat16, device=dev)
+    elif d.fmt in (W4A16_MXFP4, W4A8_MXFP4):
+        scales = torch.empty((d.N, d.K // 32), dtype=torch.uint8, device=dev)
+    else:
+        scales = torch.empty((d.N, d.K // 16), dtype=torch.uint8, device=dev)
+    g = torch.empty((1,), dtype=torch.float32, device=dev)
+    wsz = _lib.hm_quantize_workspace_size(ctypes.byref(d))
+    ws = torch.empty((max(wsz, 4),), dtype=torch.uint8, device=dev)
+    _check(_lib.hm_quantize_weight(ctypes.byref(d), _ptr(w), _ptr(zeros), _ptr(q), _ptr(scales), _ptr(g),
+                                   _ptr(ws), wsz, _stream()), "hm_quantize_weight")
+    return q, scales, g
+
+
+def alloc_packed(d, device="cuda"):
+    size = packed_size(d)
+    if size == 0:
+        raise HmError(1, "hm_packed_size")
+    return torch.empty((size,), dtype=torch.uint8, device=device)
+
+
+def transform(d, q, scales, zeros=None, out=None):
+    packed = alloc_packed(d, q.device) if out is None else out
+    _check(_lib.hm_transform(ctypes.byref(d), _ptr(q), _ptr(scales), _ptr(zeros), _ptr(packed), _stream()),
+           "hm_transform")
+    return packed
+
+
+def dequant(d, packed):
+    w = torch.empty((d.N, d.K), dtype=torch.bfloat16, device=packed.device)
+    _check(_lib.hm_dequant(ctypes.byref(d), _ptr(packed), _ptr(w), _stream()), "hm_dequant")
+    return w
+
+
+def quant_act_fp8(x):
+    m, k = x.shape
+    xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    s = torch.empty((m,), dtype=torch.float32, device=x.device)
+    _check(_lib.hm_quant_act_fp8(_ptr(x), m, k, _ptr(xq), _ptr(s), _stream()), "hm_quant_act_fp8")
+    return xq, s
+
+
+def quant_act_nvfp4(x, g_in=None):
+    m, k = x.shape
+    xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+    xs = torch.empty((max(_lib.hm_act_scale_size(m, k), 1),), dtype=torch.uint8, device=x.device)
+    g = torch.empty((1,), dtype=torch.float32, device=x.device)
+    wsz = _lib.hm_act_workspace_size(m, k)
+    ws = torch.empty((max(wsz, 4),), dtype=torch.uint8, device=x.device)
+    _check(_lib.hm_quant_act_nvfp4(_ptr(x), m, k, _ptr(g_in), _ptr(xq), _ptr(xs), _ptr(g), _ptr(ws), wsz,
+                                   _stream()), "hm_quant_act_nvfp4")
+    return xq, xs, g
+
+
+def workspace_size(fmt, m, n, k):
+    return _lib.hm_workspace_size(int(fmt), int(m), int(n), int(k))
+
+
+def alloc_workspace(fmt, m, n, k, device="cuda"):
+    """Zero-filled workspace (the library needs its counters zero before first use)."""
+    return torch.zeros((max(workspace_size(fmt, m, n, k), 256),), dtype=torch.uint8, device=device)
+
+
+def gemm(fmt, x, packed, n, k, x_scale=None, x_global=None, ws=None, out=None):
+    m = x.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    if ws is None:
+        ws = alloc_workspace(fmt, m, n, k, x.device)
+    _check(_lib.hm_gemm(int(fmt), _ptr(x), _ptr(x_scale), _ptr(x_global), _ptr(packed), _ptr(y), m, n, k,
+                        _ptr(ws), ws.numel(), _stream()), "hm_gemm")
+    return y
+
+
+def moe_gemm(fmt, x, offsets, packed_ptrs, n, k, out=None, ws=None):
+    """x: expert-sorted rows [R,K] bf16; offsets int32 [E+1] (device); packed_ptrs int64 [E] (device)."""
+    rows = x.shape[0]
+    e = offsets.numel() - 1
+    y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    wsz = 0 if ws is None else ws.numel()
+    _check(_lib.hm_moe_gemm(int(fmt), _ptr(x), _ptr(offsets), e, _ptr(packed_ptrs), _ptr(y), rows, n, k,
+                            _ptr(ws), wsz, _stream()), "hm_moe_gemm")
+    return y
+
+
+def plan(fmt, m, n, k, num_sms):
+    info = PlanInfo()
+    _check(_lib.hm_plan(int(fmt), int(m), int(n), int(k), int(num_sms), ctypes.byref(info)), "hm_plan")
+    return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+def device_error():
+    return int(_lib.hm_get_device_error(_stream()))
+
+
+def debug_wait_timeout(ns):
+    _check(_lib.hm_debug_wait_timeout(int(ns), _stream()), "hm_debug_wait_timeout")
+
+
+def version():
+    return _lib.hm_version().decode()

@@ -1,0 +1,99 @@
+"""C-ABI checks that need no GPU: libhm.so loads, exports every function include/hm.h
+declares, and its host-only queries and argument validation behave (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import layout as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hm():
+    import __graft_entry__
+    __graft_entry__.build()
+    from moe_hm_gemm_gb300 import hm as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "hm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(hm):
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(hm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@pytest.mark.parametrize("fmt,n,k,hz", [(1, 4096, 4096, False), (1, 130, 256, True), (2, 256, 512, False),
+                                        (3, 7168, 7168, False), (4, 8192, 8192, False), (4, 100, 64, False)])
+def test_packed_size_matches_layout_spec(hm, fmt, n, k, hz):
+    assert hm.packed_size(hm.desc(fmt, n, k, hz)) == L.packed_size(fmt, n, k, hz)
+
+
+def test_packed_size_rejects_bad_shapes(hm):
+    assert hm.packed_size(hm.desc(1, 128, 100)) == 0      # K not a multiple of 128
+    assert hm.packed_size(hm.desc(4, 128, 96)) == 0       # NVFP4 K % 64
+    assert hm.packed_size(hm.desc(2, 128, 128, True)) == 0  # zero-points only for INT4
+    assert hm.packed_size(hm.desc(9, 128, 128)) == 0
+    assert hm.packed_size(hm.desc(1, 0, 128)) == 0
+
+
+def test_invalid_arguments_fail_before_any_launch(hm):
+    lib = hm.lib()
+    P = ctypes.c_void_p
+    # null pointers / bad shapes are rejected on the host with HM_ERR_INVALID_ARG (1)
+    assert lib.hm_gemm(1, None, None, None, None, None, 4, 256, 512, None, 0, None) == 1
+    assert lib.hm_gemm(1, P(16), None, None, P(256), P(16), 4, 256, 100, P(256), 1 << 20, None) == 1
+    assert lib.hm_gemm(7, P(16), None, None, P(256), P(16), 4, 256, 512, P(256), 1 << 20, None) == 1
+    # misaligned packed pointer
+    assert lib.hm_gemm(1, P(16), None, None, P(272), P(16), 4, 256, 512, P(256), 1 << 20, None) == 1
+    # too small a workspace -> HM_ERR_WORKSPACE (3)
+    assert lib.hm_gemm(1, P(16), None, None, P(256), P(16), 4, 256, 512, P(256), 16, None) == 3
+    # M = 0 is a no-op
+    assert lib.hm_gemm(1, None, None, None, None, None, 0, 256, 512, None, 0, None) == 0
+    # MoE: unsupported format, bad expert count
+    assert lib.hm_moe_gemm(3, P(16), P(16), 4, P(16), P(16), 8, 256, 512, None, 0, None) == 2
+    assert lib.hm_moe_gemm(1, P(16), P(16), 0, P(16), P(16), 8, 256, 512, None, 0, None) == 1
+    assert lib.hm_quant_act_fp8(P(16), 4, 100, P(16), P(16), None) == 1
+    assert lib.hm_quant_act_nvfp4(P(16), 4, 96, None, P(16), P(16), P(16), None, 0, None) == 1
+    assert lib.hm_quant_act_nvfp4(P(16), 4, 128, None, P(16), P(16), P(16), None, 0, None) == 3
+
+
+def test_plan_buckets(hm):
+    seen = {}
+    for m in (1, 16, 17, 64, 65, 256, 257, 1024, 1025, 8192):
+        p = hm.plan(1, m, 4096, 4096, 152)
+        seen[m] = p
+        assert p["tile_n"] == 128 and p["tile_k"] == 128
+        assert p["tile_m"] >= min(m, 16) and p["tile_m"] in (16, 32, 64, 128, 256)
+        assert 1 <= p["grid"] <= 152
+    assert [seen[m]["bucket"] for m in (1, 16, 17, 64, 65, 256, 257, 1024, 1025)] == [0, 0, 1, 1, 2, 2, 3, 3, 4]
+    assert seen[1]["stream_k"] == 1 and seen[1]["grid"] == 152   # 32 tiles < 152 SMs
+    assert seen[8192]["stream_k"] == 0 and seen[8192]["tiles"] == 32 * 64
+    # every stream-K CTA gets at least one k-block
+    p = hm.plan(1, 1, 128, 256, 152)
+    assert p["grid"] == 2
+
+
+def test_workspace_sizes(hm):
+    for fmt in (1, 2, 3, 4):
+        assert hm.workspace_size(fmt, 16, 4096, 4096) > 0
+    # the internal activation buffers are included for the A8/A4 formats
+    assert hm.workspace_size(3, 1024, 4096, 4096) >= 1024 * 4096 + hm.workspace_size(1, 1024, 4096, 4096) // 2
+    assert hm.lib().hm_act_scale_size(130, 128) == L.act_scale_bytes(130, 128)
+
+
+def test_status_strings(hm):
+    lib = hm.lib()
+    assert lib.hm_status_string(0) == b"ok"
+    assert b"workspace" in lib.hm_status_string(3)
+    assert hm.version().startswith("hm ")

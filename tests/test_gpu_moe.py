@@ -1,0 +1,76 @@
+"""GPU parity of the grouped MoE GEMM (W4A16 INT4 and MXFP4-W4A16) against the oracle's
+per-expert product over expert-sorted rows."""
+import numpy as np
+import pytest
+import torch
+
+from moe_hm_gemm_gb300 import synth
+from oracle import gemm as og
+
+from .gpu_util import QuantWeight, assert_close, bf16_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hm():
+    import __graft_entry__
+    __graft_entry__.build()
+    from moe_hm_gemm_gb300 import hm as mod
+    return mod
+
+
+def moe_case(hm, fmt, counts, n, k, has_zero=False, seed=0):
+    e = len(counts)
+    offsets = np.zeros(e + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    rows = int(offsets[-1])
+    qws, packs = [], []
+    for i in range(e):
+        z = synth.zero_points(n, k // 128, seed=seed + 100 + i) if has_zero else None
+        qw = QuantWeight(fmt, synth.weights(n, k, seed=seed + i), z)
+        qws.append(qw)
+        packs.append(qw.transform(hm)[1])
+    ptrs = torch.tensor([p.data_ptr() for p in packs], dtype=torch.int64, device="cuda")
+    x = synth.activations(rows, k, seed=seed + 999)
+    y = hm.moe_gemm(fmt, x.cuda(), torch.from_numpy(offsets).cuda(), ptrs, n, k)
+    torch.cuda.synchronize()
+    yref = og.moe_gemm(bf16_np(x), offsets, [q.what for q in qws])
+    assert_close(y, yref, f"moe fmt={fmt} counts={counts}")
+    assert hm.device_error() == 0
+    return y
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_skewed_with_empty_experts(hm, fmt):
+    moe_case(hm, fmt, [37, 0, 1, 200, 0, 5, 16, 0], 256, 512, has_zero=(fmt == 1))
+
+
+def test_single_expert_equals_dense(hm):
+    n, k, m = 384, 1024, 70
+    qw = QuantWeight(1, synth.weights(n, k, seed=1), synth.zero_points(n, k // 128, seed=2))
+    _, packed = qw.transform(hm)
+    x = synth.activations(m, k, seed=3).cuda()
+    ptrs = torch.tensor([packed.data_ptr()], dtype=torch.int64, device="cuda")
+    y_moe = hm.moe_gemm(1, x, torch.tensor([0, m], dtype=torch.int32, device="cuda"), ptrs, n, k)
+    y_dense = hm.gemm(1, x, packed, n, k)
+    torch.cuda.synchronize()
+    assert_close(y_moe, og.gemm(bf16_np(x), qw.what), "single expert")
+    assert_close(y_dense, og.gemm(bf16_np(x), qw.what), "dense")
+
+
+def test_zipf_routing_small(hm):
+    tok, exp, offsets = synth.moe_routing(tokens=64, experts=16, topk=4, seed=0)
+    counts = np.diff(offsets).tolist()
+    moe_case(hm, 1, counts, 256, 256, has_zero=True, seed=3)
+
+
+def test_bad_offsets_set_device_error(hm):
+    n, k = 128, 128
+    qw = QuantWeight(1, synth.weights(n, k, seed=1))
+    _, packed = qw.transform(hm)
+    ptrs = torch.tensor([packed.data_ptr()] * 2, dtype=torch.int64, device="cuda")
+    x = synth.activations(8, k, seed=2).cuda()
+    offs = torch.tensor([0, 6, 3], dtype=torch.int32, device="cuda")   # decreasing
+    hm.moe_gemm(1, x, offs, ptrs, n, k)
+    assert hm.device_error() & 4
