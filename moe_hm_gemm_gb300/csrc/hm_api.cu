@@ -117,10 +117,15 @@ int bucket_of(int64_t m) {
 }
 
 // Token tile (tcgen05 MMA N) per M: the smallest of 16/32/64/128 covering M, 128 beyond.
+// The block-scaled kernels stop at 128 (TMEM holds their scale factors too), and a W4A4 tile
+// narrower than 128 must cover all of M (its activation scale atoms hold 128 rows).
 int tile_m_for(int32_t fmt, int64_t m) {
+  const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
-  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
-  (void)fmt;
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !block_scaled)) {
+    if (fmt == kW4A4Nv && forced < 128 && m > forced) return 128;
+    return forced;
+  }
   if (m <= 16) return 16;
   if (m <= 32) return 32;
   if (m <= 64) return 64;
@@ -312,6 +317,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (M == 0) return HM_OK;
   if (x == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 4) || (N % 2) != 0) return HM_ERR_INVALID_ARG;
+  if (fmt == kW4A4Nv && K % 256 != 0) return HM_ERR_UNSUPPORTED;  // GEMM K blocks are 256 wide
   const bool internal_act = (fmt == kW4A8Mx || fmt == kW4A4Nv) && x_scale == nullptr;
   if (fmt == kW4A4Nv && !internal_act && x_global == nullptr) return HM_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(fmt, M, N, K, internal_act);

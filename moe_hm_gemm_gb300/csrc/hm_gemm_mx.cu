@@ -1,7 +1,350 @@
-// Block-scaled GEMMs (placeholder until the kernels land).
+// Block-scaled GEMMs on tcgen05: the W4A8 (MXFP4 weights x per-token FP8 activations) and
+// W4A4 (NVFP4 x NVFP4) formats named on the news page's format list (news.cocoloop.cn,
+// section "하나의 라이브러리로 긴 포맷 목록을 포괄"), computing the explainer page's linear layer
+// Y = X * W^T ("vLLM Humming은 4비트를 어떻게 계산하나", section "같은 가중치도 한 토큰과 많은
+// 토큰에서 비용이 다르다") with both operands in their quantized form.
+//
+//  * W4A8: kind::mxf8f6f4.block_scale.scale_vec::1X. A = weight codes (e2m1), expanded by
+//    TMA (16 x 4-bit packed -> 16-byte aligned) into one byte per code in shared memory;
+//    B = e4m3 activations; A scales = the weight's E8M0 per 32 along K; B scales = 1
+//    (E8M0 127); the per-token fp32 scale multiplies each output column in the epilogue:
+//    Y[m,n] = s_tok[m] * sum_k e4m3(x[m,k]) * e2m1(w[n,k]) * 2^(e[n,k/32]-127).
+//  * W4A4: kind::mxf4nvf4.block_scale.scale_vec::4X. A and B = packed e2m1 codes, scales
+//    = e4m3 per 16 along K for both; the two fp32 tensor scales multiply in the epilogue.
+//
+// Scale factors are staged by a bulk copy into shared memory in 512-byte atoms (128 rows x 4
+// scales, row r at byte (r%32)*16 + (r/32)*4) and moved to TMEM with
+// tcgen05.cp.32x128b.warpx4, which puts row r's four scales in lane r%32 (every 32-lane
+// group) of column r/32 of a 4-column slot; the MMA picks the byte with the scale-factor id
+// (1X) or uses all four (4X). Same persistent structure as the W4A16 kernel: warp 0 loads,
+// warp 1 issues MMAs (and the scale copies), warps 2-5 drain TMEM.
+#include <cuda_bf16.h>
+
+#include "hm_device.cuh"
 #include "hm_kernels.h"
+#include "hm_layout.h"
+#include "hm_sched.cuh"
 
 namespace hm {
-int mx_stages(int, int) { return 4; }
-cudaError_t launch_mx_gemm(const MxParams&, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kWTile = 128 * 128;  // weight stage: 128 rows x 128 bytes (swizzled)
+
+template <int BT, bool NV>
+struct MxShape {
+  static constexpr int kXStage = BT * 128;                          // 128 bytes of K per row
+  static constexpr int kSfaBytes = NV ? 4 * kAtomBytes : kAtomBytes;  // per stage
+  static constexpr int kSfbBytes = NV ? 4 * kAtomBytes : 0;
+  static constexpr int kStageBytes = kWTile + kXStage + kSfaBytes + kSfbBytes;
+  static constexpr int kSL = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  static constexpr int kWOff = 0;
+  static constexpr int kXOff = kWOff + kSL * kWTile;
+  static constexpr int kSfaOff = kXOff + kSL * kXStage;
+  static constexpr int kSfbOff = kSfaOff + kSL * kSfaBytes;
+  static constexpr int kUnitSfOff = kSfbOff + kSL * kSfbBytes;     // W4A8: atom of 1.0 scales
+  static constexpr int kBarOff = kUnitSfOff + kAtomBytes;
+  static constexpr int kNumBars = 2 * kSL + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmem = 1024 + kMiscOff + 64;
+  // TMEM: accumulators [0, 2*BT), then scale-factor slots
+  static constexpr int kSfCols = NV ? kSL * 32 : kSL * 4 + 4;
+  static constexpr int kColsNeeded = 2 * BT + kSfCols;
+  static constexpr uint32_t kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
+                                        : kColsNeeded <= 256 ? 256 : 512;
+  static_assert(kColsNeeded <= 512, "TMEM budget");
+  static_assert(kSL >= 2, "pipeline depth");
+};
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > limit_ns) return;
+  }
+}
+
+template <int BT, bool NV>
+__global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_constant__ MxParams p) {
+  using S = MxShape<BT, NV>;
+  constexpr int SL = S::kSL;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + SL;
+  uint64_t* acc_full = bars + 2 * SL;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 4);
+  float* gw_sh = reinterpret_cast<float*>(smem + S::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    *abort_flag = 0u;
+    const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
+    if (!(h->magic == kMagic && static_cast<int32_t>(h->fmt) == p.fmt && h->n == p.n && h->k == p.k)) {
+      atomicOr(p.err, kErrHeader);
+      *abort_flag = 1u;
+    }
+    *gw_sh = NV ? h->tensor_scale * (*p.x_global) : 1.0f;
+  }
+  if (!NV) {
+    // unit activation scales (E8M0 127 = 1.0) for every row
+    for (int i = threadIdx.x; i < kAtomBytes / 4; i += kThreads)
+      reinterpret_cast<uint32_t*>(smem + S::kUnitSfOff)[i] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sf_col0 = 2 * BT;  // first scale-factor column
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  SchedIter sched;
+  sched.init(p.sched, p.sched.num_tiles, blockIdx.x);
+  const int kb_total = p.sched.kb_total;
+  const bool aborted_early = *abort_flag != 0u;
+
+  if (aborted_early) {
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_w);
+      prefetch_tmap(&p.tmap_x);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t tx = static_cast<uint32_t>(kWTile + S::kXStage + S::kSfaBytes + S::kSfbBytes);
+      int ls = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        const int mt = seg.tile % p.num_m_tiles;
+        const int nt = seg.tile / p.num_m_tiles;
+        const int m0 = mt * BT;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(&empty[ls], ph ^ 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[ls], tx);
+          tma_2d_g2s(smem + S::kWOff + ls * kWTile, &p.tmap_w, NV ? kb * 128 : kb * 128, nt * 128, &full[ls], pol_w);
+          tma_2d_g2s(smem + S::kXOff + ls * S::kXStage, &p.tmap_x, kb * 128, m0, &full[ls], pol_x);
+          if (NV) {
+            const size_t kc = static_cast<size_t>(kb) * 4;  // 64-K chunks
+            bulk_g2s(smem + S::kSfaOff + ls * S::kSfaBytes,
+                     p.w_atoms + (static_cast<size_t>(nt) * (kb_total * 4) + kc) * kAtomBytes, S::kSfaBytes,
+                     &full[ls], pol_w);
+            bulk_g2s(smem + S::kSfbOff + ls * S::kSfbBytes,
+                     p.x_atoms + (static_cast<size_t>(m0 / 128) * (p.k / 64) + kc) * kAtomBytes, S::kSfbBytes,
+                     &full[ls], pol_x);
+          } else {
+            bulk_g2s(smem + S::kSfaOff + ls * S::kSfaBytes,
+                     p.w_atoms + (static_cast<size_t>(nt) * kb_total + kb) * kAtomBytes, S::kSfaBytes, &full[ls],
+                     pol_w);
+          }
+          ++issued;
+          if (++ls == SL) { ls = 0; ph ^= 1u; }
+        }
+      }
+      if (*abort_flag) {
+        const int n = issued < SL ? issued : SL;
+        for (int i = 0; i < n; ++i) {
+          if (--ls < 0) { ls = SL - 1; ph ^= 1u; }
+          drain_wait(&full[ls], ph, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t unit_sfb = tmem + sf_col0 + (NV ? 0 : SL * 4);
+      if (!NV) tc_cp_32x128b_x4(unit_sfb, sdesc_sf(smem_u32(smem + S::kUnitSfOff)));
+      int ls = 0;
+      uint32_t ph = 0, acc_i = 0;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        const uint32_t b = acc_i & 1u;
+        if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BT;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(&full[ls], ph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t w_base = smem_u32(smem + S::kWOff + ls * kWTile);
+          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
+          const uint32_t sfa_base = smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes);
+          if (NV) {
+            const uint32_t sfb_base = smem_u32(smem + S::kSfbOff + ls * S::kSfbBytes);
+            const uint32_t slot = tmem + sf_col0 + ls * 32;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tc_cp_32x128b_x4(slot + 4 * j, sdesc_sf(sfa_base + j * kAtomBytes));
+              tc_cp_32x128b_x4(slot + 16 + 4 * j, sdesc_sf(sfb_base + j * kAtomBytes));
+            }
+            constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(w_base + k * 32);
+              const uint64_t bd = sdesc_sw128(x_base + k * 32);
+              mma_mxf4nvf4_4x(d, ad, bd, idesc, slot + 4 * k, slot + 16 + 4 * k, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t slot = tmem + sf_col0 + ls * 4;
+            tc_cp_32x128b_x4(slot, sdesc_sf(sfa_base));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, k, k);
+              const uint64_t ad = sdesc_sw128(w_base + k * 32);
+              const uint64_t bd = sdesc_sw128(x_base + k * 32);
+              mma_mxf8f6f4(d, ad, bd, idesc, slot, unit_sfb, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(&empty[ls]);
+          if (++ls == SL) { ls = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[b]);
+        ++acc_i;
+      }
+      tc_commit(drain);
+      drain_wait(drain, 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps (2..5)
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const int64_t total_it = static_cast<int64_t>(p.sched.num_tiles) * kb_total;
+    const float gscale = *gw_sh;
+    uint32_t acc_i = 0;
+    bool first_seg = true;
+    Segment seg;
+    while (sched.next(seg)) {
+      const uint32_t b = acc_i & 1u;
+      if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
+      tc_fence_after();
+      const int mt = seg.tile % p.num_m_tiles;
+      const int nt = seg.tile / p.num_m_tiles;
+      const int64_t m0 = static_cast<int64_t>(mt) * BT;
+      const int64_t m_end = p.m < m0 + BT ? p.m : m0 + BT;
+      const int64_t n = static_cast<int64_t>(nt) * 128 + row;
+      const bool full_seg = seg.kb0 == 0 && seg.kb1 == kb_total;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
+      float* slotp = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128;
+#pragma unroll 1
+      for (int j0 = 0; j0 < BT; j0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + j0, v);
+        tmem_wait_ld();
+        if (full_seg) {
+          if (n < p.n) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int64_t m = m0 + j0 + jj;
+              if (m < m_end) {
+                const float sc = NV ? gscale : p.s_tok[m];
+                p.y[m * p.n + n] = __float2bfloat16_rn(__uint_as_float(v[jj]) * sc);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) slotp[(j0 + jj) * 128 + row] = __uint_as_float(v[jj]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++acc_i;
+      if (!full_seg) {
+        __threadfence();
+        __syncwarp();
+        uint32_t old = 0;
+        uint32_t* ctr = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+        if (lane == 0) old = atomicAdd(ctr, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        const int64_t c_lo = sk_owner(static_cast<int64_t>(seg.tile) * kb_total, total_it, p.sched.grid);
+        const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        if (old == static_cast<uint32_t>(c_hi - c_lo)) {
+          __threadfence();
+#pragma unroll 1
+          for (int j = 0; j < BT; ++j) {
+            const int64_t m = m0 + j;
+            float acc = 0.f;
+            for (int64_t c = c_lo; c <= c_hi; ++c) {
+              const int which = (sk_start(c, total_it, p.sched.grid) / kb_total == seg.tile) ? 0 : 1;
+              acc += __ldcg(p.partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 + j * 128 + row);
+            }
+            if (m < m_end && n < p.n) {
+              const float sc = NV ? gscale : p.s_tok[m];
+              p.y[m * p.n + n] = __float2bfloat16_rn(acc * sc);
+            }
+          }
+          if (lane == 0) *ctr = 0u;
+        }
+      }
+      first_seg = false;
+    }
+  }
+
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::kTmemCols);
+  }
+}
+
+template <int BT, bool NV>
+cudaError_t launch_one(const MxParams& p, cudaStream_t st) {
+  using S = MxShape<BT, NV>;
+  auto kern = mx_gemm_kernel<BT, NV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.sched.grid, kThreads, S::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool NV>
+cudaError_t launch_bt(const MxParams& p, int tile_m, cudaStream_t st) {
+  switch (tile_m) {
+    case 16: return launch_one<16, NV>(p, st);
+    case 32: return launch_one<32, NV>(p, st);
+    case 64: return launch_one<64, NV>(p, st);
+    case 128: return launch_one<128, NV>(p, st);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace
+
+int mx_stages(int fmt, int tile_m) {
+  const bool nv = fmt == kW4A4Nv;
+  switch (tile_m) {
+    case 16: return nv ? MxShape<16, true>::kSL : MxShape<16, false>::kSL;
+    case 32: return nv ? MxShape<32, true>::kSL : MxShape<32, false>::kSL;
+    case 64: return nv ? MxShape<64, true>::kSL : MxShape<64, false>::kSL;
+    default: return nv ? MxShape<128, true>::kSL : MxShape<128, false>::kSL;
+  }
+}
+
+cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st) {
+  return p.fmt == kW4A4Nv ? launch_bt<true>(p, tile_m, st) : launch_bt<false>(p, tile_m, st);
+}
+
 }  // namespace hm
