@@ -1,0 +1,496 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the weight-quantized GEMM library on GB300.
+
+Default workload: the W4A16 dense LLM-layer sweep -- (N, K) in {(4096, 4096), (14336, 4096),
+(4096, 14336)} x M in {1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096, 8192}, INT4 weights with a
+bf16 scale and a u4 zero-point (~U{0..15}) per 128 along K, X bf16 ~ N(0, 1), W ~ N(0, 0.02)
+(seeded, generated on the device). Other workloads (--workload): w4a8 (MXFP4 x per-token FP8,
+N=K=7168 and N=18432, K=7168), w4a4 (NVFP4, N=K=8192, M in {16, 128, 1024, 8192}), moe_w4a16 and
+moe_mxfp4 (E=256 experts, gate-up N=4096/K=7168 and down N=7168/K=2048, top-8 Zipf(1.1) routing
+of T in {16, 256, 4096, 16384} tokens).
+
+A step runs every (shape, M) point of the workload once per rotation copy of its packed weight
+(enough copies to cover 4x the L2 size, so every launch streams its weights from HBM); each
+point is one CUDA graph of those launches. Per-point times come from CUDA events on the
+launching stream. `value` is the aggregate TFLOP/s of the whole step; the per-point TFLOP/s,
+weight GB/s and roofline fractions are in `sweep`. `e2e` repeats one pass over the points
+through the public API with host (pinned) inputs and outputs, copies included.
+
+--impl reference times the CPU oracle (fp64 NumPy) on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica (the path does not shard);
+rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantized GEMM TFLOP/s and weight GB/s vs M, % of GB300 HBM/tensor roofline"
+MS = [1, 2, 4, 8, 16, 32, 64, 128, 256, 1024, 4096, 8192]
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+# nominal dense ratios of the MMA kinds to kind::f16 (bf16): fp8 x2, fp4 x4
+KIND_RATIO = {"kind::f16": 1.0, "kind::mxf8f6f4": 2.0, "kind::mxf4nvf4": 4.0}
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class Point:
+    def __init__(self, label, fmt, m, n, k, flops, weight_bytes, act_bytes, out_bytes, kind, launches):
+        self.label, self.fmt, self.m, self.n, self.k = label, fmt, m, n, k
+        self.flops, self.weight_bytes, self.act_bytes, self.out_bytes = flops, weight_bytes, act_bytes, out_bytes
+        self.kind, self.launches_per_call = kind, launches
+        self.calls = []        # list of zero-arg callables, one per rotation copy
+        self.e2e = None        # (host_in, dev_in, host_out, dev_out, call)
+        self.graph = None
+        self.times_ms = []
+
+    @property
+    def bytes(self):
+        return self.weight_bytes + self.act_bytes + self.out_bytes
+
+
+def rotations(weight_bytes):
+    return max(2, math.ceil(4 * L2_BYTES / max(weight_bytes, 1)))
+
+
+def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick):
+    points = []
+    for si, (n, k) in enumerate(shapes):
+        has_zero = fmt == hm.W4A16_INT4
+        d = hm.desc(fmt, n, k, has_zero)
+        w = synth.device_weights(n, k, seed=seed0 + si)
+        z = synth.device_zero_points(n, k // 128, seed=seed0 + 100 + si) if has_zero else None
+        q, s, g = hm.quantize_weight(d, w, z)
+        if fmt == hm.W4A4_NVFP4:
+            d = hm.desc(fmt, n, k, False, float(g.item()))
+        packed = hm.transform(d, q, s, z)
+        del w, q, s
+        payload = hm.packed_size(d) - 256
+        copies = [packed] + [packed.clone() for _ in range(rotations(payload) - 1)]
+        for m in ms:
+            x = synth.device_activations(m, k, seed=seed0 + 1000 + m,
+                                         outlier_frac=0.01 if fmt == hm.W4A8_MXFP4 else 0.0)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+            ws = hm.alloc_workspace(fmt, m, n, k)
+            if fmt == hm.W4A16_INT4 or fmt == hm.W4A16_MXFP4:
+                act = 2 * m * k
+                launches = 1
+            elif fmt == hm.W4A8_MXFP4:
+                act = 2 * m * k          # bf16 in, quantized inside the call
+                launches = 2
+            else:
+                act = 2 * m * k
+                launches = 3
+            p = Point(f"{n}x{k} M={m}", fmt, m, n, k, 2.0 * m * n * k, payload, act, 2 * m * n, kind, launches)
+            for c in copies:
+                p.calls.append(lambda c=c, x=x, y=y, ws=ws, n=n, k=k, fmt=fmt: hm.gemm(fmt, x, c, n, k, ws=ws, out=y))
+            xh = x.cpu().pin_memory()
+            yh = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+            p.e2e = (xh, x, yh, y, p.calls[0])
+            points.append(p)
+        torch.cuda.synchronize()
+    if quick:
+        points = [p for p in points if p.m in (1, 16, 1024)]
+    return points
+
+
+def moe_points(hm, synth, fmt, quick):
+    e, topk = 256, 8
+    layers = [("gate_up", 4096, 7168), ("down", 7168, 2048)]
+    tokens = [16, 256, 4096, 16384] if not quick else [16, 4096]
+    points = []
+    for li, (name, n, k) in enumerate(layers):
+        d = hm.desc(fmt, n, k, fmt == hm.W4A16_INT4)
+        packs = []
+        for ei in range(e):
+            w = synth.device_weights(n, k, seed=10000 * (li + 1) + ei)
+            z = synth.device_zero_points(n, k // 128, seed=20000 * (li + 1) + ei) if d.has_zero else None
+            q, s, _ = hm.quantize_weight(d, w, z)
+            packs.append(hm.transform(d, q, s, z))
+            del w, q, s
+        per_expert = hm.packed_size(d) - 256
+        ptrs = torch.tensor([p.data_ptr() for p in packs], dtype=torch.int64, device="cuda")
+        for t in tokens:
+            _, _, offsets = synth.moe_routing(t, experts=e, topk=topk, seed=0)
+            rows = int(offsets[-1])
+            nonempty = int((np.diff(offsets) > 0).sum())
+            x = synth.device_activations(rows, k, seed=30000 + t)
+            y = torch.empty((rows, n), dtype=torch.bfloat16, device="cuda")
+            offs = torch.from_numpy(offsets).cuda()
+            p = Point(f"moe {name} T={t}", fmt, rows, n, k, 2.0 * rows * n * k, nonempty * per_expert,
+                      2 * rows * k, 2 * rows * n, "kind::f16", 1)
+            p.calls.append(lambda x=x, offs=offs, ptrs=ptrs, y=y, n=n, k=k: hm.moe_gemm(fmt, x, offs, ptrs, n, k, out=y))
+            xh = x.cpu().pin_memory()
+            yh = torch.empty((rows, n), dtype=torch.bfloat16).pin_memory()
+            p.e2e = (xh, x, yh, y, p.calls[0])
+            p._keep = (packs, ptrs)
+            points.append(p)
+        torch.cuda.synchronize()
+    return points
+
+
+def build_points(args, hm, synth):
+    pts = _build_points(args, hm, synth)
+    if args.m:
+        keep = {int(v) for v in args.m.split(",")}
+        pts = [p for p in pts if p.m in keep or any(p.label.endswith(f"T={v}") for v in keep)]
+    if args.shape:
+        pts = [p for p in pts if p.label.startswith(args.shape + " ") or f" {args.shape} " in p.label]
+    if not pts:
+        raise SystemExit("no benchmark point matches the filters")
+    return pts
+
+
+def _build_points(args, hm, synth):
+    w = args.workload
+    if w == "w4a16":
+        return dense_points(hm, synth, hm.W4A16_INT4, [(4096, 4096), (14336, 4096), (4096, 14336)], MS, 1,
+                            "kind::f16", args.quick)
+    if w == "w4a8":
+        return dense_points(hm, synth, hm.W4A8_MXFP4, [(7168, 7168), (18432, 7168)], MS, 2, "kind::mxf8f6f4",
+                            args.quick)
+    if w == "w4a4":
+        return dense_points(hm, synth, hm.W4A4_NVFP4, [(8192, 8192)], [16, 128, 1024, 8192], 3, "kind::mxf4nvf4",
+                            args.quick)
+    if w == "moe_w4a16":
+        return moe_points(hm, synth, hm.W4A16_INT4, args.quick)
+    if w == "moe_mxfp4":
+        return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick)
+    raise SystemExit(f"unknown workload {w}")
+
+
+WORKLOAD_NAMES = {
+    "w4a16": "W4A16 dense LLM layer: (N,K) in {(4096,4096),(14336,4096),(4096,14336)} x M in "
+             "{1,2,4,8,16,32,64,128,256,1024,4096,8192}; INT4 g128 bf16 scales + u4 zero-points",
+    "w4a8": "W4A8-MXFP4 dense: (N,K) in {(7168,7168),(18432,7168)} x M sweep 1..8192; e2m1 + E8M0/32, "
+            "per-token FP8 e4m3 activations (1% outliers x10) quantized inside the call",
+    "w4a4": "W4A4-NVFP4 dense: N=K=8192, M in {16,128,1024,8192}; activations quantized inside the call",
+    "moe_w4a16": "MoE grouped W4A16 INT4: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
+                 "T in {16,256,4096,16384}",
+    "moe_mxfp4": "MoE grouped MXFP4-W4A16: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
+                 "T in {16,256,4096,16384}",
+}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    torch.cuda.set_device(local_rank)
+    from moe_hm_gemm_gb300 import hm, synth
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        points = build_points(args, hm, synth)
+        # warm-up calls (sets kernel attributes) and graph capture, one graph per point
+        for p in points:
+            for c in p.calls:
+                c()
+        torch.cuda.synchronize()
+        for p in points:
+            p.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(p.graph, stream=stream):
+                for c in p.calls:
+                    c()
+        torch.cuda.synchronize()
+        if hm.device_error() != 0:
+            raise SystemExit("device error during warm-up")
+
+        def step(events=None):
+            for i, p in enumerate(points):
+                if events is not None:
+                    events[i][0].record(stream)
+                p.graph.replay()
+                if events is not None:
+                    events[i][1].record(stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in points] for _ in range(args.steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with Clocks(local_rank) as clk:
+            t0.record(stream)
+            for s in range(args.steps):
+                step(evs[s])
+            t1.record(stream)
+            torch.cuda.synchronize()
+        barrier(world)
+        total_ms = t0.elapsed_time(t1)
+        for s in range(args.steps):
+            for i, p in enumerate(points):
+                p.times_ms.append(evs[s][i][0].elapsed_time(evs[s][i][1]) / len(p.calls))
+        clocks = clk.summary()
+        err = hm.device_error()
+
+        # end-to-end pass through the public API with host buffers
+        e2e_ms = None
+        h2d = d2h = 0
+        if not args.no_e2e:
+            def e2e_pass():
+                for p in points:
+                    xh, xd, yh, yd, call = p.e2e
+                    xd.copy_(xh, non_blocking=True)
+                    call()
+                    yh.copy_(yd, non_blocking=True)
+            e2e_pass()
+            torch.cuda.synchronize()
+            reps = max(1, args.steps)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                e2e_pass()
+            b.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms = a.elapsed_time(b) / reps
+            h2d = sum(p.e2e[0].numel() * p.e2e[0].element_size() for p in points)
+            d2h = sum(p.e2e[2].numel() * p.e2e[2].element_size() for p in points)
+
+    step_ms = total_ms / args.steps
+    flops_step = sum(p.flops * len(p.calls) for p in points)
+    step_ms_max = max_over_ranks(step_ms, world)
+    value = world * flops_step / (step_ms_max * 1e-3) / 1e12
+    launches = args.steps * sum(p.launches_per_call * len(p.calls) for p in points)
+
+    sweep = []
+    dom, dom_share = None, -1.0
+    total_pt = sum(sum(p.times_ms) * len(p.calls) for p in points)
+    for p in points:
+        t = statistics.mean(p.times_ms) * 1e-3
+        peak_t = pk["bf16_sus"] * KIND_RATIO[p.kind]
+        tf = p.flops / t / 1e12
+        gbs = p.bytes / t / 1e9
+        wgbs = p.weight_bytes / t / 1e9
+        share = sum(p.times_ms) * len(p.calls) / total_pt
+        bound = "hbm" if p.bytes / (pk["hbm"] * 1e9) > p.flops / (peak_t * 1e12) else "tensor"
+        sweep.append({"point": p.label, "us": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+                      "weight_gbs": round(wgbs, 1), "bound": bound,
+                      "frac_hbm": round(gbs / pk["hbm"], 3), "frac_tensor": round(tf / peak_t, 3),
+                      "share": round(share, 4)})
+        if share > dom_share:
+            dom, dom_share = p, share
+    t = statistics.mean(dom.times_ms) * 1e-3
+    peak_t = pk["bf16_sus"] * KIND_RATIO[dom.kind]
+    dom_bound = "hbm" if dom.bytes / (pk["hbm"] * 1e9) > dom.flops / (peak_t * 1e12) else "tensor"
+    if dom_bound == "tensor":
+        ach, peak, unit = dom.flops / t / 1e12, peak_t, "TFLOP/s"
+    else:
+        ach, peak, unit = dom.bytes / t / 1e9, pk["hbm"], "GB/s"
+    roofline = {"bound": dom_bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
+                "frac": round(ach / peak, 4), "traffic": None, "kernel": dom.label,
+                "peak_source": f"{pk['source']} ({'bf16 sustained' if dom_bound == 'tensor' else 'hbm copy'}"
+                               f"{' x nominal ' + str(KIND_RATIO[dom.kind]) + ' for ' + dom.kind if dom.kind != 'kind::f16' and dom_bound == 'tensor' else ''})"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"kind::f16": "bf16", "kind::mxf8f6f4": "fp8xfp4",
+                                       "kind::mxf4nvf4": "fp4"}[points[0].kind],
+        "data": "synthetic (seeded, generated on the device)",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "parallelism": f"replicas x{world}",
+                   "l2": "packed weights rotated over copies covering 4x L2 per shape"},
+        "roofline": roofline, "gpu_launches": launches, "clocks": clocks, "device_error": err,
+        "sweep": sweep,
+    }
+    if e2e_ms is not None:
+        out["e2e"] = {"value": round(world * sum(p.flops for p in points) / (max_over_ranks(e2e_ms, world) * 1e-3) / 1e12, 3),
+                      "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(workload):
+    """A bounded sample of the workload for the CPU oracle: (description, flops, run callable)."""
+    from moe_hm_gemm_gb300 import synth
+    from oracle import gemm as og
+    from oracle import quant as oq
+    if workload in ("w4a16", "moe_w4a16", "moe_mxfp4"):
+        n, k, m = 4096, 4096, 64
+        w = synth.weights(n, k, seed=1)
+        z = synth.zero_points(n, k // 128, seed=2)
+        q, s = oq.quant_int4(w, zeros=z)
+        x = synth.activations(m, k, seed=3).float().numpy().astype(np.float64)
+        desc = f"oracle W4A16 INT4+zp dequant + fp64 GEMM, N=K=4096, M={m} rows"
+        return desc, 2.0 * m * n * k, lambda: og.gemm_w4a16_int4(x, q, s, z)
+    if workload == "w4a8":
+        n, k, m = 7168, 7168, 64
+        codes, e = oq.quant_mxfp4(synth.weights(n, k, seed=1))
+        x = synth.activations(m, k, seed=3, outlier_frac=0.01).float().numpy().astype(np.float64)
+
+        def run():
+            xq, st = oq.quant_fp8_per_token(x)
+            return og.gemm_w4a8_mxfp4(xq, st, codes, e)
+        return f"oracle W4A8 FP8 act-quant + dequant + fp64 GEMM, N=K=7168, M={m}", 2.0 * m * n * k, run
+    n, k, m = 8192, 8192, 16
+    wc, wsb, gw = oq.quant_nvfp4(synth.weights(n, k, seed=1))
+    x = synth.activations(m, k, seed=3).float().numpy().astype(np.float64)
+
+    def run():
+        xc, xsb, gx = oq.quant_nvfp4(x)
+        return og.gemm_w4a4_nvfp4(xc, xsb, gx, wc, wsb, gw)
+    return f"oracle W4A4 NVFP4 act-quant + dequant + fp64 GEMM, N=K=8192, M={m}", 2.0 * m * n * k, run
+
+
+def cpu_baseline(workload, seconds=15.0):
+    desc, flops, run = oracle_sample(workload)
+    run()
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < seconds:
+        run()
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{desc}; {reps} repetitions, {dt:.2f} s each"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    desc, flops, run = oracle_sample(args.workload)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = flops / dt / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": WORKLOAD_NAMES[args.workload], "sample": desc},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_NAMES), default="w4a16")
+    ap.add_argument("--quick", action="store_true", help="a subset of M values (for profiling)")
+    ap.add_argument("--m", default="", help="comma-separated M (or MoE T) values to keep")
+    ap.add_argument("--shape", default="", help="keep one NxK shape, e.g. 4096x4096 (MoE: gate_up/down)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -455,8 +455,17 @@ cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
   using S = F16Shape<BT>;
   auto kern = f16_gemm_kernel<BT, WK, MOE>;
   const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
+  // instantiation can ask for), so that later calls, including ones under stream capture, only launch.
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::smem_bytes(1024));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
   kern<<<p.sched.grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }

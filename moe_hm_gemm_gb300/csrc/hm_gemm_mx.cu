@@ -314,8 +314,15 @@ template <int BT, bool NV>
 cudaError_t launch_one(const MxParams& p, cudaStream_t st) {
   using S = MxShape<BT, NV>;
   auto kern = mx_gemm_kernel<BT, NV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
-  if (e != cudaSuccess) return e;
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
   kern<<<p.sched.grid, kThreads, S::kSmem, st>>>(p);
   return cudaGetLastError();
 }
