@@ -328,8 +328,7 @@ def run_ours(args, rank, world, local_rank):
 
     step_ms = total_ms / args.steps
     flops_step = sum(p.flops * len(p.calls) for p in points)
-    step_ms_max = max_over_ranks(step_ms, world)
-    value = world * flops_step / (step_ms_max * 1e-3) / 1e12
+    value, step_ms_max = aggregate_tflops(flops_step, step_ms, world)
     launches = args.steps * sum(p.launches_per_call * len(p.calls) for p in points)
 
     sweep = []
@@ -343,7 +342,11 @@ def run_ours(args, rank, world, local_rank):
         wgbs = p.weight_bytes / t / 1e9
         share = sum(p.times_ms) * len(p.calls) / total_pt
         bound = "hbm" if p.bytes / (pk["hbm"] * 1e9) > p.flops / (peak_t * 1e12) else "tensor"
-        sweep.append({"point": p.label, "us": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+        plan = None
+        if not p.label.startswith("moe"):
+            plan = hm.plan(p.fmt, p.m, p.n, p.k, torch.cuda.get_device_properties(local_rank).multi_processor_count)
+            plan = {k: plan[k] for k in ("tile_m", "stages", "stream_k", "grid")}
+        sweep.append({"point": p.label, "plan": plan, "us": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
                       "weight_gbs": round(wgbs, 1), "bound": bound,
                       "frac_hbm": round(gbs / pk["hbm"], 3), "frac_tensor": round(tf / peak_t, 3),
                       "share": round(share, 4)})
@@ -386,12 +389,19 @@ def barrier(world):
         torch.distributed.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The slowest rank's time: replicas run concurrently, so the job ends with the last one."""
     if world == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(work_flops_per_rank, ms_per_step, world, device="cuda"):
+    """Whole-job throughput of N replicas: all ranks' work over the max-over-ranks step time."""
+    ms = max_over_ranks(ms_per_step, world, device)
+    return world * work_flops_per_rank / (ms * 1e-3) / 1e12, ms
 
 
 # ----------------------------------------------------------------------------- CPU oracle

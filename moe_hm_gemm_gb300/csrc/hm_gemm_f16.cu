@@ -33,7 +33,8 @@
 namespace hm {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kDqWarps = 8;                     // dequant warps (2 per scheduler)
+constexpr int kThreads = 32 * (2 + kDqWarps + 4);  // producer, MMA, dequant, epilogue
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
 template <int BT>
@@ -76,8 +77,9 @@ __device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, co
   TileInfo t;
   const int64_t kb_total = p.k / 128;
   if (!MOE) {
-    const int mt = tile % p.num_m_tiles;
-    const int nt = tile / p.num_m_tiles;
+    // m-major: concurrent CTAs share one X tile and stream different weight tiles
+    const int nt = tile % p.num_n_tiles;
+    const int mt = tile / p.num_n_tiles;
     t.m0 = mt * BT;
     t.m_end = static_cast<int32_t>(p.m < t.m0 + BT ? p.m : t.m0 + BT);
     t.n0 = nt * 128;
@@ -147,10 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
-      mbar_init(&empty_l[s], 1 + 4);
+      mbar_init(&empty_l[s], 1 + kDqWarps);
     }
     for (int s = 0; s < SA; ++s) {
-      mbar_init(&full_a[s], 4);
+      mbar_init(&full_a[s], kDqWarps);
       mbar_init(&empty_a[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -316,9 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       drain_wait(drain, 0, 1000000000ull);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 2 + kDqWarps) {
     // ------------------------------------------------------------ dequant warps
-    const int r = threadIdx.x - 64;  // weight row within the tile
+    // two threads per weight row, each restoring 64 of the stage's 128 K
+    const int dq = threadIdx.x - 64;
+    const int r = dq & 127;          // weight row within the tile
+    const int half = dq >> 7;        // K half: 16-byte code groups c4 in {2*half, 2*half+1}
     int ls = 0, as = 0;
     uint32_t lph = 0, aph = 0;
     Segment seg;
@@ -327,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
         if (!mbar_wait(&full_w[ls], lph, wc) || !mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
         const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage);
-        uint4 c[4];
+        uint4 c[2];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) c[c4] = ld_shared_v4(wsa + c4 * 2048 + r * 16);
+        for (int i = 0; i < 2; ++i) c[i] = ld_shared_v4(wsa + (2 * half + i) * 2048 + r * 16);
         __nv_bfloat162 zz, ss;
         uint32_t e4 = 0;
         if (WK == 2) {
@@ -350,8 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&empty_l[ls]);
         const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
+        for (int i = 0; i < 2; ++i) {
+          const int c4 = 2 * half + i;
+          const uint32_t words[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
           float scale = 0.f;
           if (WK == 2) scale = pow2f(static_cast<int>((e4 >> (8 * c4)) & 0xFFu) - 127);
 #pragma unroll
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps
+    // ------------------------------------------------------------ epilogue warps (10..13)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;       // weight row within the tile
     const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
@@ -388,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       const int64_t n = static_cast<int64_t>(t.n0) + row;
       const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
-      float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128;
+      float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
+                    static_cast<size_t>(row) * BT;
 #pragma unroll 1
       for (int j0 = 0; j0 < BT; j0 += 16) {
         uint32_t v[16];
@@ -403,8 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             }
           }
         } else {
+          float4* dst = reinterpret_cast<float4*>(slot + j0);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) slot[(j0 + jj) * 128 + row] = __uint_as_float(v[jj]);
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
       }
       tc_fence_before();
@@ -424,17 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
         if (old == static_cast<uint32_t>(c_hi - c_lo)) {
           __threadfence();
-#pragma unroll 1
-          for (int j = 0; j < BT; ++j) {
-            const int64_t m = static_cast<int64_t>(t.m0) + j;
-            float acc = 0.f;
-            for (int64_t c = c_lo; c <= c_hi; ++c) {
-              const int which = (sk_start(c, total_it, p.sched.grid) / kb_total == seg.tile) ? 0 : 1;
-              const float* src = p.partial + (static_cast<size_t>(c) * 2 + which) * BT * 128;
-              acc += __ldcg(src + j * 128 + row);
-            }
-            if (m < t.m_end && n < p.n) p.y[m * p.n + n] = __float2bfloat16_rn(acc);
-          }
+          streamk_fixup<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, c_lo, c_hi, row,
+                            [&](int j, float acc) {
+                              const int64_t m = static_cast<int64_t>(t.m0) + j;
+                              if (m < t.m_end && n < p.n) p.y[m * p.n + n] = __float2bfloat16_rn(acc);
+                            });
           if (lane == 0) *ctr = 0u;
         }
       }

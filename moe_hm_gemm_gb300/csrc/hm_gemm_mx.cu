@@ -128,15 +128,18 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       prefetch_tmap(&p.tmap_x);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint32_t tx = static_cast<uint32_t>(kWTile + S::kXStage + S::kSfaBytes + S::kSfbBytes);
+      // The W4A8 weight load reads 8 KB of packed codes and spreads them over 16 KB of shared
+      // memory (16U4_ALIGN16B); its transaction count is the 8 KB read.
+      const uint32_t w_tx = NV ? kWTile : kWTile / 2;
+      const uint32_t tx = static_cast<uint32_t>(w_tx + S::kXStage + S::kSfaBytes + S::kSfbBytes);
       int ls = 0;
       uint32_t ph = 0;
       int issued = 0;
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
-        const int mt = seg.tile % p.num_m_tiles;
-        const int nt = seg.tile / p.num_m_tiles;
+        const int nt = seg.tile % p.num_n_tiles;  // m-major tile order
+        const int mt = seg.tile / p.num_n_tiles;
         const int m0 = mt * BT;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!mbar_wait(&empty[ls], ph ^ 1u, wc)) { ok = false; break; }
@@ -238,14 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       const uint32_t b = acc_i & 1u;
       if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
       tc_fence_after();
-      const int mt = seg.tile % p.num_m_tiles;
-      const int nt = seg.tile / p.num_m_tiles;
+      const int nt = seg.tile % p.num_n_tiles;
+      const int mt = seg.tile / p.num_n_tiles;
       const int64_t m0 = static_cast<int64_t>(mt) * BT;
       const int64_t m_end = p.m < m0 + BT ? p.m : m0 + BT;
       const int64_t n = static_cast<int64_t>(nt) * 128 + row;
       const bool full_seg = seg.kb0 == 0 && seg.kb1 == kb_total;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
-      float* slotp = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128;
+      float* slotp = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
+                     static_cast<size_t>(row) * BT;
 #pragma unroll 1
       for (int j0 = 0; j0 < BT; j0 += 16) {
         uint32_t v[16];
@@ -263,8 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
             }
           }
         } else {
+          float4* dst = reinterpret_cast<float4*>(slotp + j0);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) slotp[(j0 + jj) * 128 + row] = __uint_as_float(v[jj]);
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
       }
       tc_fence_before();
@@ -282,19 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
         const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
         if (old == static_cast<uint32_t>(c_hi - c_lo)) {
           __threadfence();
-#pragma unroll 1
-          for (int j = 0; j < BT; ++j) {
-            const int64_t m = m0 + j;
-            float acc = 0.f;
-            for (int64_t c = c_lo; c <= c_hi; ++c) {
-              const int which = (sk_start(c, total_it, p.sched.grid) / kb_total == seg.tile) ? 0 : 1;
-              acc += __ldcg(p.partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 + j * 128 + row);
-            }
-            if (m < m_end && n < p.n) {
-              const float sc = NV ? gscale : p.s_tok[m];
-              p.y[m * p.n + n] = __float2bfloat16_rn(acc * sc);
-            }
-          }
+          streamk_fixup<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, c_lo, c_hi, row,
+                            [&](int j, float acc) {
+                              const int64_t m = m0 + j;
+                              if (m < m_end && n < p.n) {
+                                const float sc = NV ? gscale : p.s_tok[m];
+                                p.y[m * p.n + n] = __float2bfloat16_rn(acc * sc);
+                              }
+                            });
           if (lane == 0) *ctr = 0u;
         }
       }

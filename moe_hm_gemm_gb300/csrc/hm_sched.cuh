@@ -76,4 +76,62 @@ struct SchedIter {
   }
 };
 
+// Sum the stream-K partials of one tile for one accumulator row, in k order (CTA c_lo first),
+// and hand each column's total to `emit(j, value)`. Partials are laid out
+// [cta][first/last segment][row][tile_m] (fp32), so each lane reads its row's columns with
+// 16-byte loads; four contributors' loads are issued before any of them is summed, which keeps
+// many independent L2 reads in flight instead of one dependent read per column.
+template <int BT, typename Emit>
+__device__ __forceinline__ void streamk_fixup(const float* partial, int64_t total_it, int32_t grid,
+                                              int32_t kb_total, int32_t tile, int64_t c_lo, int64_t c_hi,
+                                              int row, Emit emit) {
+  auto src = [&](int64_t c) {
+    const int which = (sk_start(c, total_it, grid) / kb_total == tile) ? 0 : 1;
+    return partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 + static_cast<size_t>(row) * BT;
+  };
+#pragma unroll 1
+  for (int j0 = 0; j0 < BT; j0 += 16) {
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    int64_t c = c_lo;
+#pragma unroll 1
+    for (; c + 3 <= c_hi; c += 4) {
+      float4 v[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4* s4 = reinterpret_cast<const float4*>(src(c + u) + j0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[u][i] = __ldcg(s4 + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[4 * i] += v[u][i].x;
+          acc[4 * i + 1] += v[u][i].y;
+          acc[4 * i + 2] += v[u][i].z;
+          acc[4 * i + 3] += v[u][i].w;
+        }
+      }
+    }
+#pragma unroll 1
+    for (; c <= c_hi; ++c) {
+      const float4* s4 = reinterpret_cast<const float4*>(src(c) + j0);
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldcg(s4 + i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[4 * i] += v[i].x;
+        acc[4 * i + 1] += v[i].y;
+        acc[4 * i + 2] += v[i].z;
+        acc[4 * i + 3] += v[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) emit(j0 + i, acc[i]);
+  }
+}
+
 }  // namespace hm
