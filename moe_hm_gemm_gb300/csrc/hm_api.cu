@@ -31,6 +31,8 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 
 std::mutex g_mu;
 uint32_t* g_err_ptr[kMaxDevices] = {};
+uint64_t* g_trace[kMaxDevices] = {};
+size_t g_trace_bytes[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -71,6 +73,11 @@ bool device_info(DeviceInfo* out) {
   out->num_sms = g_num_sms[dev];
   out->err = g_err_ptr[dev];
   return true;
+}
+
+// Trace buffer of the current device if it holds one 16-slot row per CTA of this launch.
+uint64_t* trace_for(const DeviceInfo& di, int grid) {
+  return g_trace_bytes[di.dev] >= static_cast<size_t>(grid) * 16 * sizeof(uint64_t) ? g_trace[di.dev] : nullptr;
 }
 
 uint64_t timeout_ns() {
@@ -117,9 +124,12 @@ int bucket_of(int64_t m) {
 }
 
 // Token tile (tcgen05 MMA N) per M: the smallest of 16/32/64/128 covering M, 128 beyond.
-// The block-scaled kernels stop at 128 (TMEM holds their scale factors too), and a W4A4 tile
-// narrower than 128 must cover all of M (its activation scale atoms hold 128 rows).
-int tile_m_for(int32_t fmt, int64_t m) {
+// Token tile (tcgen05 MMA N) per M: the smallest of 16/32/64/128 covering M; beyond 128 the
+// W4A16 kernel takes 256 (half the dequant work and X traffic per FLOP) as long as that still
+// gives every SM a tile. The block-scaled kernels stop at 128 (TMEM also holds their scale
+// factors), and a W4A4 tile narrower than 128 must cover all of M (its activation scale atoms
+// hold 128 rows).
+int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !block_scaled)) {
@@ -129,13 +139,15 @@ int tile_m_for(int32_t fmt, int64_t m) {
   if (m <= 16) return 16;
   if (m <= 32) return 32;
   if (m <= 64) return 64;
-  return 128;
+  if (m <= 128 || block_scaled) return 128;
+  const int64_t n_tiles = pad_n(n) / 128;
+  return ceil_div(m, 256) * n_tiles >= num_sms ? 256 : 128;
 }
 
 Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   Plan p{};
   p.bucket = bucket_of(m);
-  p.tile_m = tile_m_for(fmt, m);
+  p.tile_m = tile_m_for(fmt, m, n, num_sms);
   p.tile_k = fmt == kW4A4Nv ? 256 : 128;
   p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(p.tile_m) : mx_stages(fmt, p.tile_m);
   p.num_m_tiles = ceil_div(m > 0 ? m : 1, p.tile_m);
@@ -158,14 +170,19 @@ struct WsLayout {
   size_t partial, counters, act_q, act_s, act_g, act_amax, total;
 };
 
+// The workspace must fit whatever plan any device picks: size the stream-K partials for the
+// widest token tile and the counters for the most tiles the planner can choose for this M.
 WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_act) {
-  const Plan p = make_plan(fmt, m, n, k, kMaxSmsForSizing);
+  int widest = tile_m_for(fmt, m, n, 1);          // one SM: the widest choice
+  const int narrowest = tile_m_for(fmt, m, n, 1 << 30);
+  if (narrowest > widest) widest = narrowest;
+  const int64_t max_tiles = ceil_div(m > 0 ? m : 1, narrowest < widest ? narrowest : widest) * (pad_n(n) / 128);
   WsLayout w{};
   size_t off = 0;
   w.partial = off;
-  off += align_up(static_cast<size_t>(kMaxSmsForSizing) * 2 * p.tile_m * 128 * sizeof(float));
+  off += align_up(static_cast<size_t>(kMaxSmsForSizing) * 2 * widest * 128 * sizeof(float));
   w.counters = off;
-  off += align_up(static_cast<size_t>(p.tiles) * 4 * sizeof(uint32_t));
+  off += align_up(static_cast<size_t>(max_tiles) * 4 * sizeof(uint32_t));
   w.act_q = w.act_s = w.act_g = w.act_amax = off;
   if (internal_act && fmt == kW4A8Mx) {
     w.act_q = off;
@@ -347,6 +364,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
     prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
     prm.timeout_ns = timeout_ns();
+    prm.trace = trace_for(di, p.grid);
     return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
   }
 
@@ -475,6 +493,15 @@ const char* hm_status_string(hm_status s) {
     case HM_ERR_DEVICE: return "device error word set";
   }
   return "unknown status";
+}
+
+hm_status hm_set_trace_buffer(void* trace, size_t bytes) {
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  if ((trace == nullptr) != (bytes == 0) || !aligned(trace, 8)) return HM_ERR_INVALID_ARG;
+  g_trace[di.dev] = static_cast<uint64_t*>(trace);
+  g_trace_bytes[di.dev] = bytes;
+  return HM_OK;
 }
 
 const char* hm_version(void) { return "hm 0.1.0 (sm_103a)"; }

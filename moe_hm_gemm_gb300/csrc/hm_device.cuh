@@ -24,6 +24,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Diagnostics: record the global timer in slot `i` of this CTA's trace row (no-op when the
+// caller installed no trace buffer).
+__device__ __forceinline__ void trace_mark(uint64_t* trace, int i) {
+  if (trace != nullptr) trace[blockIdx.x * 16 + i] = globaltimer();
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ bool elect_one() {

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, 0);
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   const int kb_total = p.sched.kb_total;
   const bool aborted_early = *abort_flag != 0u;
   const uint32_t has_zero = *hz_sh;
+  if (threadIdx.x == 0) trace_mark(p.trace, 1);
   const uint32_t kUnit = WK == 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
 
   if (aborted_early) {
@@ -266,10 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           mbar_arrive_expect_tx(&full_x[ls], S::kXStage);
           tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[ls], pol_x);
           tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[ls], pol_x);
+          if (issued == 0) trace_mark(p.trace, 2);
           ++issued;
           if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
       }
+      trace_mark(p.trace, 3);
       if (*abort_flag) {
         // Let copies already in flight land before the CTA's shared memory goes away.
         const int n = issued < SL ? issued : SL;
@@ -296,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!mbar_wait(&full_x[ls], lph, wc) || !mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
           tc_fence_after();
+          if (acc_i == 0 && kb == seg.kb0) trace_mark(p.trace, 6);
           const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
           const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
 #pragma unroll
@@ -313,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         tc_commit(&acc_full[b]);
         ++acc_i;
       }
+      trace_mark(p.trace, 7);
       // All tcgen05 work of this thread has completed once `drain` flips.
       tc_commit(drain);
       drain_wait(drain, 0, 1000000000ull);
@@ -326,11 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     const int half = dq >> 7;        // K half: 16-byte code groups c4 in {2*half, 2*half+1}
     int ls = 0, as = 0;
     uint32_t lph = 0, aph = 0;
+    bool first_dq = true;
     Segment seg;
     bool ok = true;
     while (ok && sched.next(seg)) {
       for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
         if (!mbar_wait(&full_w[ls], lph, wc) || !mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
+        if (dq == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
         const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage);
         uint4 c[2];
 #pragma unroll
@@ -390,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       const uint32_t b = acc_i & 1u;
       if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
       tc_fence_after();
+      if (row == 0 && acc_i == 0) trace_mark(p.trace, 8);
       const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
       const int64_t n = static_cast<int64_t>(t.n0) + row;
       const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
@@ -421,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++acc_i;
+      if (row == 0) trace_mark(p.trace, 9);
       if (!full) {
         // Stream-K fix-up, per warp (32 rows): publish the partial, count arrivals; the last
         // CTA to arrive sums every CTA's partial for these rows in k order.
@@ -430,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         uint32_t* ctr = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
         if (lane == 0) old = atomicAdd(ctr, 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
+        if (row == 0) trace_mark(p.trace, 10);
         const int64_t c_lo = sk_owner(static_cast<int64_t>(seg.tile) * kb_total, total_it, p.sched.grid);
         const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
         if (old == static_cast<uint32_t>(c_hi - c_lo)) {
@@ -440,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
                               if (m < t.m_end && n < p.n) p.y[m * p.n + n] = __float2bfloat16_rn(acc);
                             });
           if (lane == 0) *ctr = 0u;
+          if (row == 0) trace_mark(p.trace, 11);
         }
       }
       first_seg = false;
@@ -451,6 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, S::kTmemCols);
+    if (lane == 0) {
+      trace_mark(p.trace, 12);
+      if (p.trace) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[blockIdx.x * 16 + 13] = smid;
+      }
+    }
   }
 }
 

@@ -27,6 +27,7 @@ struct F16Params {
   int32_t num_n_tiles;
   SchedParams sched;
   uint64_t timeout_ns;
+  uint64_t* trace;                    // optional per-CTA timestamps [grid][16] (diagnostics)
 };
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
@@ -49,6 +50,7 @@ struct MxParams {
   int32_t k_blocks;                   // K_pad / tile_k
   SchedParams sched;
   uint64_t timeout_ns;
+  uint64_t* trace;
 };
 
 // Launchers (return a cudaError_t of the launch). `tile_m` and `stages` select an instantiation.

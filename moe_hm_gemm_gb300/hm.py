@@ -56,6 +56,7 @@ def _load():
         "hm_plan": (I32, [I32, I64, I64, I64, I32, ctypes.POINTER(PlanInfo)]),
         "hm_get_device_error": (ctypes.c_uint32, [P]),
         "hm_debug_wait_timeout": (I32, [ctypes.c_uint64, P]),
+        "hm_set_trace_buffer": (I32, [P, SZ]),
         "hm_status_string": (ctypes.c_char_p, [I32]),
         "hm_version": (ctypes.c_char_p, []),
     }
@@ -195,6 +196,14 @@ def device_error():
 
 def debug_wait_timeout(ns):
     _check(_lib.hm_debug_wait_timeout(int(ns), _stream()), "hm_debug_wait_timeout")
+
+
+def set_trace_buffer(buf):
+    """Install a uint64 device tensor as the per-CTA timestamp buffer (None removes it)."""
+    if buf is None:
+        _check(_lib.hm_set_trace_buffer(None, 0), "hm_set_trace_buffer")
+    else:
+        _check(_lib.hm_set_trace_buffer(_ptr(buf), buf.numel() * buf.element_size()), "hm_set_trace_buffer")
 
 
 def version():
