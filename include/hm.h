@@ -165,6 +165,25 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of hm_gemm for the W4A16 formats (HM_W4A16_INT4, HM_W4A16_MXFP4).
+ * The paper has no counterpart; this entry point exists for callers that cannot allocate
+ * device memory at all: for example code running inside another engine's fixed memory plan
+ * (a plugin that is handed no workspace), or code that must not call cudaMalloc because it
+ * synchronises the device. It runs the same kernel as hm_gemm, but the split-K partials and
+ * tile counters live in an 8 MiB array inside the library (held by every GPU that loads the
+ * library until the process exits), so the caller passes only X, the packed weight and Y.
+ * Arguments and layouts are those of hm_gemm. The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine); it clears the counters it needs with
+ * cudaMemsetAsync on `stream` at every call.
+ * Limits: problems whose split-K scratch exceeds 8 MiB (roughly M > 64 with stream-K on a
+ * 152-SM GB300, or very tall N) return HM_ERR_WORKSPACE; use hm_gemm with a workspace then.
+ * All calls share the one array: calls that overlap on the GPU (on different streams, or from
+ * several threads) race and must be serialised by the caller.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture. */
+hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, void* y,
+                                int64_t M, int64_t N, int64_t K, void* stream);
+
 /* ---------------------------------------------------------------- plan / diagnostics */
 
 /* The kernel configuration hm_gemm would use: token tile (MMA N), pipeline stages, split

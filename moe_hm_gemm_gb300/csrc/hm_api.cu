@@ -216,6 +216,27 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------- allocation-free W4A16 GEMM
+// Scratch for hm_gemm_w4a16_noalloc: a fixed array in the library's own device memory, so that
+// callers who may not allocate still get the split-K schedule. Every GPU that loads the library
+// holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the array's name is
+// only a stand-in for the symbol, never a usable pointer, so the address is looked up once per
+// device (with that device current) and cached.
+uint8_t* noalloc_scratch(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  return g_noalloc_ptr[dev];
+}
+
 }  // namespace
 }  // namespace hm
 
@@ -461,6 +482,44 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
   prm.timeout_ns = timeout_ns();
   return cuda_status(launch_f16_gemm(prm, tile_m, true, cudaStream_t(stream)));
+}
+
+hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, void* y, int64_t M, int64_t N,
+                                int64_t K, void* stream) {
+  if ((fmt != kW4A16Int4 && fmt != kW4A16Mx) || M < 0 || N <= 0 || !valid_k(fmt, K)) return HM_ERR_INVALID_ARG;
+  if (M == 0) return HM_OK;
+  if (x == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 4) || (N % 2) != 0) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  uint8_t* scratch = noalloc_scratch(di.dev);
+  if (scratch == nullptr) return HM_ERR_CUDA;
+  const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  // Partials for the CTAs of this launch, then the per-tile arrival counters.
+  const size_t partial_bytes = align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float));
+  const size_t counter_bytes = align_up(static_cast<size_t>(p.tiles) * 4 * sizeof(uint32_t));
+  if (partial_bytes + counter_bytes > kNoAllocScratchBytes) return HM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The counters must start at zero; clear them on every call (cheap, and safe even after a
+  // call that stopped early on a device error).
+  if (p.stream_k && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
+  F16Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, p.tile_m)) return HM_ERR_CUDA;
+  prm.packed = static_cast<const uint8_t*>(packed);
+  prm.y = static_cast<__nv_bfloat16*>(y);
+  prm.partial = reinterpret_cast<float*>(scratch);
+  prm.counters = reinterpret_cast<uint32_t*>(scratch + partial_bytes);
+  prm.err = di.err;
+  prm.m = M;
+  prm.n = N;
+  prm.k = K;
+  prm.fmt = fmt;
+  prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
+  prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
+  prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
+  prm.timeout_ns = timeout_ns();
+  return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
 }
 
 uint32_t hm_get_device_error(void* stream) {

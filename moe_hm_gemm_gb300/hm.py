@@ -53,6 +53,7 @@ def _load():
         "hm_workspace_size": (SZ, [I32, I64, I64, I64]),
         "hm_gemm": (I32, [I32, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "hm_moe_gemm": (I32, [I32, P, P, I32, P, P, I64, I64, I64, P, SZ, P]),
+        "hm_gemm_w4a16_noalloc": (I32, [I32, P, P, P, I64, I64, I64, P]),
         "hm_plan": (I32, [I32, I64, I64, I64, I32, ctypes.POINTER(PlanInfo)]),
         "hm_get_device_error": (ctypes.c_uint32, [P]),
         "hm_debug_wait_timeout": (I32, [ctypes.c_uint64, P]),
@@ -170,6 +171,15 @@ def gemm(fmt, x, packed, n, k, x_scale=None, x_global=None, ws=None, out=None):
         ws = alloc_workspace(fmt, m, n, k, x.device)
     _check(_lib.hm_gemm(int(fmt), _ptr(x), _ptr(x_scale), _ptr(x_global), _ptr(packed), _ptr(y), m, n, k,
                         _ptr(ws), ws.numel(), _stream()), "hm_gemm")
+    return y
+
+
+def gemm_noalloc(fmt, x, packed, n, k, out=None):
+    """W4A16 GEMM through the allocation-free entry point (scratch inside the library)."""
+    m = x.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _check(_lib.hm_gemm_w4a16_noalloc(int(fmt), _ptr(x), _ptr(packed), _ptr(y), m, n, k, _stream()),
+           "hm_gemm_w4a16_noalloc")
     return y
 
 
