@@ -37,22 +37,34 @@ constexpr int kDqWarps = 8;                     // dequant warps (2 per schedule
 constexpr int kThreads = 32 * (2 + kDqWarps + 4);  // producer, MMA, dequant, epilogue
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
+// Two variants of the A (restored weight) path:
+//  * tile_m <= 128: the dequant warps store bf16 A straight into TMEM (tcgen05.st) and the MMA
+//    reads A from TMEM, so shared memory carries only the packed weights and X; TMEM holds the
+//    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns;
+//  * tile_m = 256: the accumulator pair fills TMEM, so A goes through shared memory in the
+//    128-byte-swizzled K-major layout.
 template <int BT>
 struct F16Shape {
-  static constexpr int kSL = BT <= 32 ? 8 : (BT == 64 ? 6 : (BT == 128 ? 3 : 2));  // load stages
-  static constexpr int kSA = BT <= 16 ? 3 : 2;                                      // A stages
+  static constexpr bool kATmem = BT <= 128;
   static constexpr int kXStage = BT * 128 * 2;
-  static constexpr int kAOff = 0;
-  static constexpr int kXOff = kSA * kAStage;
-  static constexpr int kWOff = kXOff + kSL * kXStage;
   static constexpr int kWStage = kUnitMx;  // room for the largest unit
+  static constexpr int kSA = kATmem ? ((512 - 2 * BT) / 64 > 6 ? 6 : (512 - 2 * BT) / 64) : 2;
+  static constexpr int kAOff = 0;
+  static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
+  static constexpr int kXOff = kASmem;
+  static constexpr int kSLFit = ((kATmem ? 208 : 216) * 1024 - kASmem) / (kXStage + kWStage);
+  static constexpr int kSL = kSLFit > 16 ? 16 : kSLFit;
+  static constexpr int kWOff = kXOff + kSL * kXStage;
   static constexpr int kBarOff = kWOff + kSL * kWStage;
   static constexpr int kNumBars = 3 * kSL + 2 * kSA + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kLutOff = kMiscOff + 32;
   static constexpr int kMoeOff = kLutOff + 64;
-  static constexpr uint32_t kTmemCols = 2 * BT < 32 ? 32 : 2 * BT;
+  static constexpr uint32_t kTmemCols = kATmem ? 512u : (2 * BT < 32 ? 32u : 2u * BT);
+  static constexpr uint32_t kACol0 = 2 * BT;  // first TMEM column of the A stages
   static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
+  static_assert(kSL >= 2, "load pipeline depth");
+  static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
 };
 
 struct TileInfo {
@@ -301,13 +313,22 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           if (!mbar_wait(&full_x[ls], lph, wc) || !mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
           tc_fence_after();
           if (acc_i == 0 && kb == seg.kb0) trace_mark(p.trace, 6);
-          const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
           const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
+          if constexpr (S::kATmem) {
+            const uint32_t a_t = tmem + S::kACol0 + as * 64;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
-            const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
-            mma_bf16(d, ad, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+              mma_bf16_ta(d, a_t + 8 * k, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
+              const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+              mma_bf16(d, ad, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty_l[ls]);
           tc_commit(&empty_a[as]);
@@ -327,8 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   } else if (warp < 2 + kDqWarps) {
     // ------------------------------------------------------------ dequant warps
     // two threads per weight row, each restoring 64 of the stage's 128 K
+    // Thread -> (row, K half). With A in TMEM a warp may only touch its own 32-lane quarter
+    // (warp index % 4), so rows follow the quarter; otherwise rows follow the thread index.
     const int dq = threadIdx.x - 64;
-    const int r = dq & 127;          // weight row within the tile
+    const int r = S::kATmem ? 32 * (warp & 3) + lane : (dq & 127);  // weight row within the tile
     const int half = dq >> 7;        // K half: 16-byte code groups c4 in {2*half, 2*half+1}
     int ls = 0, as = 0;
     uint32_t lph = 0, aph = 0;
@@ -361,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_l[ls]);
-        const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+        uint32_t a_regs[32];  // TMEM path: this row's 64 restored K as bf16x2, in K order
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int c4 = 2 * half + i;
@@ -373,13 +396,25 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             uint32_t o[4];
             if (WK == 2) dq_mx_word(words[j], lut, scale, o);
             else dq_int4_word(words[j], zz, ss, o);
-            const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
-            const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
-                                 ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
-            st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+            if constexpr (S::kATmem) {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
+            } else {
+              const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
+              const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+              const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
+                                   ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
+              st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+            }
           }
         }
-        fence_proxy_async_smem();
+        if constexpr (S::kATmem) {
+          tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          fence_proxy_async_smem();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[as]);
         if (++ls == SL) { ls = 0; lph ^= 1u; }
