@@ -213,12 +213,14 @@ uint32_t hm_get_device_error(void* stream);
 hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /* Diagnostics: install (or, with NULL/0, remove) a device buffer of `bytes` bytes on the current
- * device. While installed, each dense W4A16 GEMM launch whose grid fits (16 uint64 per CTA) writes
+ * device. While installed, each dense W4A16 GEMM launch (grid <= 256 CTAs) writes
  * global-timer stamps of its pipeline milestones per CTA: 0 entry, 1 set-up done, 2 first load
  * issued, 3 last load issued, 4 first weight stage seen by the dequant warps, 6 first MMA,
  * 7 last MMA commit, 8 first accumulator seen by the epilogue, 9 last tile stored, 10 stream-K
- * arrival counted, 11 fix-up done, 12 exit; slot 13 holds the SM id. The buffer stays owned by
- * the caller; concurrent launches overwrite each other's rows. */
+ * arrival counted, 11 fix-up done, 12 exit; slot 13 holds the SM id. The buffer must hold
+ * 256*16 + 5*64 uint64: after the 256 per-CTA rows, CTA 0 stamps its first 64 pipeline stages
+ * (five rows of 64: load issued, dequant start, dequant done, MMA start, MMA committed). The
+ * buffer stays owned by the caller; concurrent launches overwrite each other's stamps. */
 hm_status hm_set_trace_buffer(void* trace, size_t bytes);
 
 const char* hm_status_string(hm_status s);

@@ -77,7 +77,8 @@ bool device_info(DeviceInfo* out) {
 
 // Trace buffer of the current device if it holds one 16-slot row per CTA of this launch.
 uint64_t* trace_for(const DeviceInfo& di, int grid) {
-  return g_trace_bytes[di.dev] >= static_cast<size_t>(grid) * 16 * sizeof(uint64_t) ? g_trace[di.dev] : nullptr;
+  (void)grid;
+  return g_trace_bytes[di.dev] >= static_cast<size_t>(256 * 16 + 5 * 64) * sizeof(uint64_t) ? g_trace[di.dev] : nullptr;
 }
 
 uint64_t timeout_ns() {
@@ -237,6 +238,21 @@ uint8_t* noalloc_scratch(int dev) {
   return g_noalloc_ptr[dev];
 }
 
+// X (bf16 [rows][K]) as the W4A16 kernel loads it: box {64, tile_m} when a stage holds one
+// 128-K block, else the K axis split into 64-element chunks as a third dimension (stride 128
+// bytes) so that one load covers the 2*group chunks of a stage.
+bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int tile_m) {
+  const int g = f16_group(tile_m);
+  if (g == 1) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, rows, k * 2, 64, tile_m);
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k * 2), 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tile_m), static_cast<cuuint32_t>(2 * g)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace hm
 
@@ -369,7 +385,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
     F16Params prm;
     std::memset(&prm, 0, sizeof(prm));
-    if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, p.tile_m))
+    if (!encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
       return HM_ERR_CUDA;
     prm.packed = static_cast<const uint8_t*>(packed);
     prm.y = static_cast<__nv_bfloat16*>(y);
@@ -467,7 +483,7 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) tile_m = forced;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, rows, K * 2, 64, tile_m)) return HM_ERR_CUDA;
+  if (!encode_x_f16(&prm.tmap_x, x, K, rows, tile_m)) return HM_ERR_CUDA;
   prm.packed_list = reinterpret_cast<const uint8_t* const*>(packed);
   prm.offsets = expert_offsets;
   prm.y = static_cast<__nv_bfloat16*>(y);
@@ -505,7 +521,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (p.stream_k && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (!encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, p.tile_m)) return HM_ERR_CUDA;
+  if (!encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m)) return HM_ERR_CUDA;
   prm.packed = static_cast<const uint8_t*>(packed);
   prm.y = static_cast<__nv_bfloat16*>(y);
   prm.partial = reinterpret_cast<float*>(scratch);

@@ -16,14 +16,19 @@
 
 namespace hm {
 
-// One 32-bit word of the unit layout -> 8 consecutive bf16 (as 4 bf16x2 registers).
+// One 32-bit word of the unit layout -> 8 consecutive bf16 (as 4 bf16x2 registers). Written as
+// explicit PTX so that each pair costs one shift, one lop3 (mask | magic), one bf16x2 subtract
+// (exact: both operands are integers in [128, 143]) and one bf16x2 multiply (one rounding).
 __device__ __forceinline__ void dq_int4_word(uint32_t w, __nv_bfloat162 zz, __nv_bfloat162 ss,
                                              uint32_t (&o)[4]) {
+  const uint32_t z2 = bf16x2_bits(zz), s2 = bf16x2_bits(ss);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-    const __nv_bfloat162 v = __hsub2(bits_bf16x2(t), zz);
-    o[i] = bf16x2_bits(__hmul2(v, ss));
+    uint32_t t, v;
+    const uint32_t sh = w >> (4 * i);
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(sh));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(t), "r"(z2));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(v), "r"(s2));
   }
 }
 
@@ -59,6 +64,29 @@ __device__ __forceinline__ void dq_mx_word(uint32_t w, const float* lut, float s
     const float lo = lut[(w >> (4 * i)) & 0xFu] * scale;
     const float hi = lut[(w >> (16 + 4 * i)) & 0xFu] * scale;
     o[i] = pack_bf16x2_rn(lo, hi);
+  }
+}
+
+// MXFP4 restore without a table. The three magnitude bits of an e2m1 code (exponent e1 e0,
+// mantissa m) placed at bf16 bits [8:6], with the sign at bit 15, form the bf16 number
+// code * 2^-126: codes with e = 0 land on bf16 subnormals (m * 2^-127), the others on normals
+// 2^(e-127) * (1 + m/2). One bf16 multiply by 2^(E-1) then gives code * 2^(E-127) with a
+// single rounding, the restored weight of the OCP MX definition. sc2 holds 2^(E-1) in both
+// halves, which bf16 can represent for E <= 128; callers take dq_mx_word above otherwise.
+// Nibble pairing is that of dq_mx_word: nibble i of w goes to the low half, nibble i + 4 to the
+// high half of o[i].
+__device__ __forceinline__ uint32_t mx_pow2_pair(uint32_t e) {
+  return ((e + 126u) << 7) * 0x00010001u;
+}
+
+__device__ __forceinline__ void dq_mx_word_bits(uint32_t w, uint32_t sc2, uint32_t (&o)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = (6 - 4 * i) >= 0 ? (w << (6 - 4 * i)) : (w >> (4 * i - 6));
+    const uint32_t b = w << (12 - 4 * i);
+    uint32_t v;
+    asm("lop3.b32 %0, %1, 0x01C001C0, %2, 0xEA;" : "=r"(v) : "r"(a), "r"(b & 0x80008000u));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(v), "r"(sc2));
   }
 }
 

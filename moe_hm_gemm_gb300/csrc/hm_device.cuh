@@ -30,6 +30,12 @@ __device__ __forceinline__ void trace_mark(uint64_t* trace, int i) {
   if (trace != nullptr) trace[blockIdx.x * 16 + i] = globaltimer();
 }
 
+// Diagnostics: per-stage stamps of CTA 0 (role r in 0..4, stage index i < 64) after the
+// per-CTA rows.
+__device__ __forceinline__ void trace_stage(uint64_t* trace, int r, int i) {
+  if (trace != nullptr && blockIdx.x == 0 && i < 64) trace[256 * 16 + r * 64 + i] = globaltimer();
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 __device__ __forceinline__ bool elect_one() {
@@ -57,6 +63,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
+               : "memory");
+}
+
+// Raise the expected transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
 
@@ -132,6 +144,16 @@ __device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, in
       : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tma_3d_g2s(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                           uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -141,6 +163,20 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its prologue, and
+// wait until every kernel this one depends on has finished and its writes are visible.
+// Both are no-ops when the launch did not ask for programmatic serialization.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

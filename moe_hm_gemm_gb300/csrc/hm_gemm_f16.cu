@@ -33,7 +33,12 @@
 namespace hm {
 namespace {
 
-constexpr int kDqWarps = 8;                     // dequant warps (2 per scheduler)
+// Dequant warps: two groups of four that take alternate 128-K blocks, so that two blocks are
+// being restored at any time (one block's chain of shared loads, conversion, TMEM store and
+// barrier signalling is latency-bound); inside a group each warp owns one 32-row TMEM quarter
+// and each thread restores its row's whole 128-K block.
+constexpr int kDqGroup = 4;
+constexpr int kDqWarps = 2 * kDqGroup;
 constexpr int kThreads = 32 * (2 + kDqWarps + 4);  // producer, MMA, dequant, epilogue
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
@@ -43,11 +48,15 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 //    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns;
 //  * tile_m = 256: the accumulator pair fills TMEM, so A goes through shared memory in the
 //    128-byte-swizzled K-major layout.
+// A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
+// activation load), so that small token tiles move many bytes per TMA instruction; the dequant
+// warps and the MMA still step through it one 128-K block (one TMEM A slot) at a time.
 template <int BT>
 struct F16Shape {
   static constexpr bool kATmem = BT <= 128;
-  static constexpr int kXStage = BT * 128 * 2;
-  static constexpr int kWStage = kUnitMx;  // room for the largest unit
+  static constexpr int kG = f16_group_of(BT);
+  static constexpr int kXStage = kG * BT * 128 * 2;
+  static constexpr int kWStage = kG * kUnitMx;  // room for the largest units
   static constexpr int kSA = kATmem ? ((512 - 2 * BT) / 64 > 6 ? 6 : (512 - 2 * BT) / 64) : 2;
   static constexpr int kAOff = 0;
   static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
@@ -159,13 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     trace_mark(p.trace, 0);
+    // Read the (first) weight header before initialising the barriers so that its memory
+    // latency overlaps the set-up. MoE offsets (and thus expert pointers) may come from the
+    // previous kernel, so the MoE variant waits for it first.
+    if (MOE) pdl_wait();
+    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
+    const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first);
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
       mbar_init(&empty_l[s], 1 + kDqWarps);
     }
     for (int s = 0; s < SA; ++s) {
-      mbar_init(&full_a[s], kDqWarps);
+      mbar_init(&full_a[s], kDqGroup);
       mbar_init(&empty_a[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -177,16 +192,16 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     *abort_flag = 0u;
     // The first weight's header decides whether INT4 units carry zero-points; every weight
     // used must agree with it and with the call's (fmt, N, K).
-    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
-    const uint32_t hz = reinterpret_cast<const PackedHeader*>(first)->has_zero;
+    const uint32_t hz = hdr.has_zero;
     *hz_sh = (WK == 0 && hz == 1u) ? 1u : 0u;
-    if (!header_ok(first, p, hz)) {
+    if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
       atomicOr(p.err, kErrHeader);
       *abort_flag = 1u;
     }
   }
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
   if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (MOE && warp == 2) pdl_wait();   // the offsets below may be written by the previous kernel
 
   int32_t num_tiles = p.sched.num_tiles;
   if (MOE) {
@@ -242,8 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   const int kb_total = p.sched.kb_total;
   const bool aborted_early = *abort_flag != 0u;
   const uint32_t has_zero = *hz_sh;
-  if (threadIdx.x == 0) trace_mark(p.trace, 1);
+  if (threadIdx.x == 0) {
+    trace_mark(p.trace, 1);
+    pdl_launch_dependents();
+  }
   const uint32_t kUnit = WK == 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  // Weights are streamed once when a single token tile covers M; with several token tiles the
+  // same weight tiles are read again by other CTAs, so keep them in L2.
+  const bool reuse_w = MOE || p.num_m_tiles > 1;
 
   if (aborted_early) {
     // nothing to do: fall through to teardown
@@ -251,14 +272,31 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&p.tmap_x);
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
+      const uint64_t pol_w = reuse_w ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_x = reuse_w ? policy_evict_normal() : policy_evict_last();
       int ls = 0;
       uint32_t lph = 0;
       int issued = 0;
       const uint8_t* last_checked = nullptr;
       Segment seg;
       bool ok = true;
+      // Weights do not depend on the previous kernel: stream the first pipeline stages of them
+      // before waiting for it (dense path), then issue the activation loads.
+      int pre = 0;
+      if (!MOE) {
+        SchedIter pf = sched;
+        Segment ps;
+        while (pre < SL && pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          for (int kb = ps.kb0; kb < ps.kb1 && pre < SL; kb += S::kG, ++pre) {
+            const uint32_t bytes = static_cast<uint32_t>(min(S::kG, ps.kb1 - kb)) * kUnit;
+            mbar_arrive_expect_tx(&full_w[pre], bytes);
+            bulk_g2s(smem + S::kWOff + pre * S::kWStage, t.wbase + static_cast<size_t>(kb) * kUnit, bytes,
+                     &full_w[pre], pol_w);
+          }
+        }
+      }
+      pdl_wait();
       while (ok && sched.next(seg)) {
         const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
         if (MOE) {
@@ -271,15 +309,23 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             last_checked = t.base;
           }
         }
-        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-          if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
-          uint8_t* ws = smem + S::kWOff + ls * S::kWStage;
+        for (int kb = seg.kb0; kb < seg.kb1; kb += S::kG) {
+          if (issued >= pre) {   // the first `pre` stages are free and already hold their weights
+            if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
+            uint8_t* ws = smem + S::kWOff + ls * S::kWStage;
+            const uint32_t bytes = static_cast<uint32_t>(min(S::kG, seg.kb1 - kb)) * kUnit;
+            mbar_arrive_expect_tx(&full_w[ls], bytes);
+            bulk_g2s(ws, t.wbase + static_cast<size_t>(kb) * kUnit, bytes, &full_w[ls], pol_w);
+          }
+          trace_stage(p.trace, 0, issued);
           uint8_t* xs = smem + S::kXOff + ls * S::kXStage;
-          mbar_arrive_expect_tx(&full_w[ls], kUnit);
-          bulk_g2s(ws, t.wbase + static_cast<size_t>(kb) * kUnit, kUnit, &full_w[ls], pol_w);
-          mbar_arrive_expect_tx(&full_x[ls], S::kXStage);
-          tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[ls], pol_x);
-          tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[ls], pol_x);
+          mbar_arrive_expect_tx(&full_x[ls], S::kXStage);   // the whole box lands (zero-filled past K)
+          if constexpr (S::kG == 1) {
+            tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[ls], pol_x);
+            tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[ls], pol_x);
+          } else {
+            tma_3d_g2s(xs, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[ls], pol_x);
+          }
           if (issued == 0) trace_mark(p.trace, 2);
           ++issued;
           if (++ls == SL) { ls = 0; lph ^= 1u; }
@@ -301,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(128, BT);
       int ls = 0, as = 0;
-      uint32_t lph = 0, aph = 0, acc_i = 0;
+      uint32_t lph = 0, aph = 0, acc_i = 0;   // A slot `as` / parity `aph` follow the block sequence
+      int mma_count = 0;
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
@@ -309,11 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + b * BT;
-        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-          if (!mbar_wait(&full_x[ls], lph, wc) || !mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
+        for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+          if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
+          const int g = min(S::kG, seg.kb1 - kb0);
+          for (int j = 0; j < g; ++j) {
+          const int kb = kb0 + j;
+          if (!mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
           tc_fence_after();
           if (acc_i == 0 && kb == seg.kb0) trace_mark(p.trace, 6);
-          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
+          trace_stage(p.trace, 3, mma_count);
+          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
           if constexpr (S::kATmem) {
             const uint32_t a_t = tmem + S::kACol0 + as * 64;
 #pragma unroll
@@ -330,10 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
               mma_bf16(d, ad, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty_l[ls]);
           tc_commit(&empty_a[as]);
-          if (++ls == SL) { ls = 0; lph ^= 1u; }
+          trace_stage(p.trace, 4, mma_count++);
           if (++as == SA) { as = 0; aph ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit(&empty_l[ls]);
+          if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
         if (!ok) break;
         tc_commit(&acc_full[b]);
@@ -347,25 +402,45 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     __syncwarp();
   } else if (warp < 2 + kDqWarps) {
     // ------------------------------------------------------------ dequant warps
-    // two threads per weight row, each restoring 64 of the stage's 128 K
-    // Thread -> (row, K half). With A in TMEM a warp may only touch its own 32-lane quarter
-    // (warp index % 4), so rows follow the quarter; otherwise rows follow the thread index.
-    const int dq = threadIdx.x - 64;
-    const int r = S::kATmem ? 32 * (warp & 3) + lane : (dq & 127);  // weight row within the tile
-    const int half = dq >> 7;        // K half: 16-byte code groups c4 in {2*half, 2*half+1}
-    int ls = 0, as = 0;
-    uint32_t lph = 0, aph = 0;
+    // Warp -> (group, row, K half). With A in TMEM a warp may only touch its own 32-lane
+    // quarter (warp index % 4), so rows follow the quarter; otherwise rows follow the thread.
+    const int dw = warp - 2;
+    const int grp = dw / kDqGroup;                 // takes the blocks with sequence index % 2 == grp
+    const int r = 32 * (warp & 3) + lane;          // weight row within the tile (TMEM lane)
+    int ls = 0;
+    uint32_t lph = 0;
+    int seq = 0;                                   // running 128-K block index over all segments
     bool first_dq = true;
     Segment seg;
     bool ok = true;
     while (ok && sched.next(seg)) {
-      for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-        if (!mbar_wait(&full_w[ls], lph, wc) || !mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
-        if (dq == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
-        const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage);
-        uint4 c[2];
+      for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+        const int g = min(S::kG, seg.kb1 - kb0);
+        // blocks j of this stage that belong to this group
+        const int j0 = ((seq & 1) == grp) ? 0 : 1;
+        // Every group waits for the stage to fill, even one with no block in it: its release
+        // must not reach the ring slot's empty barrier before the slot's previous use is over,
+        // or it would count towards the wrong phase.
+        if (!mbar_wait(&full_w[ls], lph, wc)) {
+          ok = false;
+          break;
+        }
+        if (j0 >= g) {                             // none of the blocks: release the stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_l[ls]);
+        }
+        for (int jb = j0; jb < g; jb += 2) {
+        const int bi = seq + jb;
+        const int as = bi % SA;
+        const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
+        if (!mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
+        if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
+        const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
+        // INT4 takes the whole 128-K row into registers at once; MXFP4 (whose scale and
+        // conversion need more registers) takes the second half after converting the first.
+        uint4 c[4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) c[i] = ld_shared_v4(wsa + (2 * half + i) * 2048 + r * 16);
+        for (int i = 0; i < (WK == 2 ? 2 : 4); ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
         __nv_bfloat162 zz, ss;
         uint32_t e4 = 0;
         if (WK == 2) {
@@ -382,34 +457,52 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           }
           zz = int4_zero_pair(z);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_l[ls]);
-        uint32_t a_regs[32];  // TMEM path: this row's 64 restored K as bf16x2, in K order
+        const bool last_of_stage = jb + 2 >= g;
+        if (WK != 2 && last_of_stage) {   // the stage's last block of this group is in registers
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_l[ls]);
+        }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c4 = 2 * half + i;
-          const uint32_t words[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
-          float scale = 0.f;
-          if (WK == 2) scale = pow2f(static_cast<int>((e4 >> (8 * c4)) & 0xFFu) - 127);
+        for (int half = 0; half < 2; ++half) {
+          if (WK == 2 && half == 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t o[4];
-            if (WK == 2) dq_mx_word(words[j], lut, scale, o);
-            else dq_int4_word(words[j], zz, ss, o);
-            if constexpr (S::kATmem) {
-#pragma unroll
-              for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
-            } else {
-              const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
-              const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
-              const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
-                                   ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
-              st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+            for (int i = 2; i < 4; ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
+            if (last_of_stage) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&empty_l[ls]);
             }
           }
+          uint32_t a_regs[32];  // TMEM path: 64 restored K of this row as bf16x2, in K order
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c4 = 2 * half + i;
+            const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
+            const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
+            const bool mx_bits = WK == 2 && ex <= 128u;
+            const uint32_t sc2 = mx_pow2_pair(ex);
+            const float scale = WK == 2 ? pow2f(static_cast<int>(ex) - 127) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t o[4];
+              if (WK != 2) dq_int4_word(words[j], zz, ss, o);
+              else if (mx_bits) dq_mx_word_bits(words[j], sc2, o);
+              else dq_mx_word(words[j], lut, scale, o);
+              if constexpr (S::kATmem) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
+              } else {
+                const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
+                const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+                const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
+                                     ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
+                st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+              }
+            }
+          }
+          if constexpr (S::kATmem)
+            tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
         }
         if constexpr (S::kATmem) {
-          tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
           tmem_wait_st();
           tc_fence_before();
         } else {
@@ -417,12 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[as]);
+        }
+        seq += g;
         if (++ls == SL) { ls = 0; lph ^= 1u; }
-        if (++as == SA) { as = 0; aph ^= 1u; }
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps (10..13)
+    // ------------------------------------------------------------ epilogue warps (last four)
+    pdl_wait();                          // Y, partials and counters may be in use by the previous kernel
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;       // weight row within the tile
     const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
@@ -525,8 +620,7 @@ cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  kern<<<p.sched.grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, p.sched.grid, kThreads, smem, st, p);
 }
 
 template <int WK, bool MOE>
@@ -542,6 +636,8 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
 }
 
 }  // namespace
+
+int f16_group(int tile_m) { return f16_group_of(tile_m); }
 
 int f16_stages(int tile_m) {
   switch (tile_m) {

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       atomicOr(p.err, kErrHeader);
       *abort_flag = 1u;
     }
-    *gw_sh = NV ? h->tensor_scale * (*p.x_global) : 1.0f;
+    *gw_sh = NV ? h->tensor_scale : 1.0f;   // gX is applied by the epilogue (after its wait)
   }
   if (!NV) {
     // unit activation scales (E8M0 127 = 1.0) for every row
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
   }
   if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
   __syncthreads();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sf_col0 = 2 * BT;  // first scale-factor column
@@ -126,38 +127,58 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
     if (lane == 0) {
       prefetch_tmap(&p.tmap_w);
       prefetch_tmap(&p.tmap_x);
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
+      // Weights are streamed once when one token tile covers M; otherwise other CTAs re-read them.
+      const bool reuse_w = p.num_m_tiles > 1;
+      const uint64_t pol_w = reuse_w ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_x = reuse_w ? policy_evict_normal() : policy_evict_last();
       // The W4A8 weight load reads 8 KB of packed codes and spreads them over 16 KB of shared
       // memory (16U4_ALIGN16B); its transaction count is the 8 KB read.
-      const uint32_t w_tx = NV ? kWTile : kWTile / 2;
-      const uint32_t tx = static_cast<uint32_t>(w_tx + S::kXStage + S::kSfaBytes + S::kSfbBytes);
+      const uint32_t w_tx = static_cast<uint32_t>((NV ? kWTile : kWTile / 2) + S::kSfaBytes);
+      const uint32_t x_tx = static_cast<uint32_t>(S::kXStage + S::kSfbBytes);
+      auto load_w = [&](int slot, int nt, int kb) {
+        tma_2d_g2s(smem + S::kWOff + slot * kWTile, &p.tmap_w, kb * 128, nt * 128, &full[slot], pol_w);
+        const size_t atom = NV ? static_cast<size_t>(nt) * (kb_total * 4) + static_cast<size_t>(kb) * 4
+                               : static_cast<size_t>(nt) * kb_total + kb;
+        bulk_g2s(smem + S::kSfaOff + slot * S::kSfaBytes, p.w_atoms + atom * kAtomBytes, S::kSfaBytes, &full[slot],
+                 pol_w);
+      };
       int ls = 0;
       uint32_t ph = 0;
       int issued = 0;
       Segment seg;
       bool ok = true;
+      // Weights and their scales do not depend on the previous kernel: start streaming the first
+      // pipeline stages before waiting for it. Their bytes are announced with expect_tx (no
+      // arrive), so a stage cannot complete before its activation part is issued below.
+      int pre = 0;
+      {
+        SchedIter pf = sched;
+        Segment ps;
+        while (pre < SL && pf.next(ps)) {
+          const int nt = ps.tile % p.num_n_tiles;
+          for (int kb = ps.kb0; kb < ps.kb1 && pre < SL; ++kb, ++pre) {
+            mbar_expect_tx(&full[pre], w_tx);
+            load_w(pre, nt, kb);
+          }
+        }
+      }
+      pdl_wait();
       while (ok && sched.next(seg)) {
         const int nt = seg.tile % p.num_n_tiles;  // m-major tile order
         const int mt = seg.tile / p.num_n_tiles;
         const int m0 = mt * BT;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-          if (!mbar_wait(&empty[ls], ph ^ 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[ls], tx);
-          tma_2d_g2s(smem + S::kWOff + ls * kWTile, &p.tmap_w, NV ? kb * 128 : kb * 128, nt * 128, &full[ls], pol_w);
+          if (issued >= pre) {
+            if (!mbar_wait(&empty[ls], ph ^ 1u, wc)) { ok = false; break; }
+            mbar_expect_tx(&full[ls], w_tx);
+            load_w(ls, nt, kb);
+          }
+          mbar_arrive_expect_tx(&full[ls], x_tx);
           tma_2d_g2s(smem + S::kXOff + ls * S::kXStage, &p.tmap_x, kb * 128, m0, &full[ls], pol_x);
           if (NV) {
-            const size_t kc = static_cast<size_t>(kb) * 4;  // 64-K chunks
-            bulk_g2s(smem + S::kSfaOff + ls * S::kSfaBytes,
-                     p.w_atoms + (static_cast<size_t>(nt) * (kb_total * 4) + kc) * kAtomBytes, S::kSfaBytes,
-                     &full[ls], pol_w);
             bulk_g2s(smem + S::kSfbOff + ls * S::kSfbBytes,
-                     p.x_atoms + (static_cast<size_t>(m0 / 128) * (p.k / 64) + kc) * kAtomBytes, S::kSfbBytes,
-                     &full[ls], pol_x);
-          } else {
-            bulk_g2s(smem + S::kSfaOff + ls * S::kSfaBytes,
-                     p.w_atoms + (static_cast<size_t>(nt) * kb_total + kb) * kAtomBytes, S::kSfaBytes, &full[ls],
-                     pol_w);
+                     p.x_atoms + (static_cast<size_t>(m0 / 128) * (p.k / 64) + static_cast<size_t>(kb) * 4) * kAtomBytes,
+                     S::kSfbBytes, &full[ls], pol_x);
           }
           ++issued;
           if (++ls == SL) { ls = 0; ph ^= 1u; }
@@ -230,10 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue warps (2..5)
+    pdl_wait();   // Y, s_tok, partials and counters: wait for the previous kernel
     const int q = warp & 3;
     const int row = 32 * q + lane;
     const int64_t total_it = static_cast<int64_t>(p.sched.num_tiles) * kb_total;
-    const float gscale = *gw_sh;
+    const float gscale = NV ? *gw_sh * (*p.x_global) : 1.0f;
     uint32_t acc_i = 0;
     bool first_seg = true;
     Segment seg;
@@ -325,8 +347,7 @@ cudaError_t launch_one(const MxParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  kern<<<p.sched.grid, kThreads, S::kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, p.sched.grid, kThreads, S::kSmem, st, p);
 }
 
 template <bool NV>

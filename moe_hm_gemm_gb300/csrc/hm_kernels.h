@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "hm_sched.cuh"
 
 namespace hm {
@@ -53,8 +55,36 @@ struct MxParams {
   uint64_t* trace;
 };
 
+// Launch a GEMM kernel with programmatic stream serialization (PDL), so that its prologue and
+// weight prefetch overlap the tail of the previous kernel in the stream; the kernel itself
+// waits (griddepcontrol.wait) before touching anything the previous kernel may produce or use.
+// HM_PDL=0 in the environment launches without the attribute.
+template <typename Params>
+inline cudaError_t launch_pdl(void (*kern)(Params), int grid, int threads, int smem, cudaStream_t st,
+                              const Params& p) {
+  static const bool enabled = [] {
+    const char* e = std::getenv("HM_PDL");
+    return !(e && e[0] == '0');
+  }();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = enabled ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 // Launchers (return a cudaError_t of the launch). `tile_m` and `stages` select an instantiation.
 cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+// 128-K blocks per W4A16 load stage for a token tile: the X tensor map for that tile is 2-D
+// (box {64, tile_m}) when this is 1 and 3-D (box {64, tile_m, 2*group}) otherwise.
+constexpr int f16_group_of(int tile_m) { return tile_m <= 32 ? 4 : (tile_m == 64 ? 2 : 1); }
+int f16_group(int tile_m);
 cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st);
 int f16_stages(int tile_m);
 int mx_stages(int fmt, int tile_m);

@@ -117,3 +117,19 @@ def test_full_size_sampled(hm):
         ok = og.tolerance_ok(got, ref)
         assert ok.all(), f"M={m}: {int((~ok).sum())} sampled outputs outside tolerance"
     assert hm.device_error() == 0
+
+
+@pytest.mark.parametrize("log2_gain", [-100, 14])
+def test_mxfp4_extreme_scales(hm, log2_gain):
+    """MXFP4 blocks whose E8M0 exponent is far from 127: E > 128 takes the table path,
+    small E restores through bf16 subnormal codes; both must match the oracle."""
+    n, k, m = 256, 512, 16
+    w = synth.weights(n, k, seed=17) * np.float32(2.0 ** log2_gain)
+    qw = QuantWeight(2, w)
+    _, packed = qw.transform(hm)
+    e = oq.quant_mxfp4(w)[1]
+    assert (e > 128).any() if log2_gain > 0 else (e < 40).all()
+    x = synth.activations(m, k, seed=18)
+    y = hm.gemm(2, x.cuda(), packed, n, k)
+    torch.cuda.synchronize()
+    assert_close(y, og.gemm(bf16_np(x), qw.what), f"mxfp4 gain 2^{log2_gain}")
