@@ -78,7 +78,7 @@ bool device_info(DeviceInfo* out) {
 // Trace buffer of the current device if it holds one 16-slot row per CTA of this launch.
 uint64_t* trace_for(const DeviceInfo& di, int grid) {
   (void)grid;
-  return g_trace_bytes[di.dev] >= static_cast<size_t>(256 * 16 + 5 * 64) * sizeof(uint64_t) ? g_trace[di.dev] : nullptr;
+  return g_trace_bytes[di.dev] >= static_cast<size_t>(256 * 16 + 8 * 64) * sizeof(uint64_t) ? g_trace[di.dev] : nullptr;
 }
 
 uint64_t timeout_ns() {
@@ -150,7 +150,7 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.bucket = bucket_of(m);
   p.tile_m = tile_m_for(fmt, m, n, num_sms);
   p.tile_k = fmt == kW4A4Nv ? 256 : 128;
-  p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(p.tile_m) : mx_stages(fmt, p.tile_m);
+  p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(fmt, p.tile_m) : mx_stages(fmt, p.tile_m);
   p.num_m_tiles = ceil_div(m > 0 ? m : 1, p.tile_m);
   p.num_n_tiles = pad_n(n) / 128;
   p.kb_total = pad_k(fmt, k) / p.tile_k;

@@ -32,6 +32,18 @@ __device__ __forceinline__ void dq_int4_word(uint32_t w, __nv_bfloat162 zz, __nv
   }
 }
 
+// One word -> 8 consecutive bf16 holding u - z exactly (integers in [-15, 15]), for kernels
+// that apply the group scale to the fp32 partial sum of the group instead of to each weight.
+__device__ __forceinline__ void dq_int4_word_unscaled(uint32_t w, uint32_t z2, uint32_t (&o)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t t;
+    const uint32_t sh = w >> (4 * i);
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(sh));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(z2));
+  }
+}
+
 // bf16x2 holding (128 + z, 128 + z).
 __device__ __forceinline__ __nv_bfloat162 int4_zero_pair(uint32_t z) {
   const uint32_t b = 0x4300u | (z & 0xFu);

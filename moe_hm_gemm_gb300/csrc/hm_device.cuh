@@ -30,7 +30,7 @@ __device__ __forceinline__ void trace_mark(uint64_t* trace, int i) {
   if (trace != nullptr) trace[blockIdx.x * 16 + i] = globaltimer();
 }
 
-// Diagnostics: per-stage stamps of CTA 0 (role r in 0..4, stage index i < 64) after the
+// Diagnostics: per-stage / per-block stamps of CTA 0 (row r in 0..7, index i < 64) after the
 // per-CTA rows.
 __device__ __forceinline__ void trace_stage(uint64_t* trace, int r, int i) {
   if (trace != nullptr && blockIdx.x == 0 && i < 64) trace[256 * 16 + r * 64 + i] = globaltimer();

@@ -24,8 +24,11 @@
 //  * every wait is bounded (hm_device.cuh).
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "hm_dequant.cuh"
 #include "hm_device.cuh"
+#include "hm_f16_common.cuh"
 #include "hm_kernels.h"
 #include "hm_layout.h"
 #include "hm_sched.cuh"
@@ -39,7 +42,11 @@ namespace {
 // and each thread restores its row's whole 128-K block.
 constexpr int kDqGroup = 4;
 constexpr int kDqWarps = 2 * kDqGroup;
-constexpr int kThreads = 32 * (2 + kDqWarps + 4);  // producer, MMA, dequant, epilogue
+// Warp roles: 0 producer, 1-2 MMA issuers (warp 1 also owns TMEM), 3-10 dequant, 11-14 epilogue.
+constexpr int kMmaWarp0 = 1;
+constexpr int kDqWarp0 = 3;
+constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
 // Two variants of the A (restored weight) path:
@@ -51,13 +58,20 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 // A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
 // activation load), so that small token tiles move many bytes per TMA instruction; the dequant
 // warps and the MMA still step through it one 128-K block (one TMEM A slot) at a time.
+// One thread issuing tcgen05.mma waits about 46 cycles per instruction whatever N, while the
+// tensor core accepts M = 128 / K = 16 MMAs with A in TMEM several times faster from several
+// threads. Small token tiles (N <= 64, where one MMA is far below that wait) therefore use two
+// issuing warps that take alternate 128-K blocks into separate accumulators, which the epilogue
+// adds (issuer 0 first, so the sum is deterministic).
 template <int BT>
 struct F16Shape {
   static constexpr bool kATmem = BT <= 128;
+  static constexpr int kIss = BT <= 64 ? 2 : 1;
+  static constexpr int kAccCols = 2 * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
   static constexpr int kG = f16_group_of(BT);
   static constexpr int kXStage = kG * BT * 128 * 2;
   static constexpr int kWStage = kG * kUnitMx;  // room for the largest units
-  static constexpr int kSA = kATmem ? ((512 - 2 * BT) / 64 > 6 ? 6 : (512 - 2 * BT) / 64) : 2;
+  static constexpr int kSA = kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2;
   static constexpr int kAOff = 0;
   static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
   static constexpr int kXOff = kASmem;
@@ -70,72 +84,12 @@ struct F16Shape {
   static constexpr int kLutOff = kMiscOff + 32;
   static constexpr int kMoeOff = kLutOff + 64;
   static constexpr uint32_t kTmemCols = kATmem ? 512u : (2 * BT < 32 ? 32u : 2u * BT);
-  static constexpr uint32_t kACol0 = 2 * BT;  // first TMEM column of the A stages
+  static constexpr uint32_t kACol0 = kAccCols;  // first TMEM column of the A stages
   static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
   static_assert(kSL >= 2, "load pipeline depth");
   static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
+  static_assert(kATmem || kIss == 1, "two issuers only with A in TMEM");
 };
-
-struct TileInfo {
-  int32_t m0, m_end, n0;
-  const uint8_t* base;   // packed weight (header) of this tile's matrix
-  const uint8_t* wbase;  // first unit of this n-tile
-};
-
-// Largest e with prefix[e] <= tile (prefix[0] = 0 <= tile < prefix[E]).
-__device__ __forceinline__ int find_expert(const int32_t* prefix, int experts, int tile) {
-  int lo = 0, hi = experts;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= tile) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-template <int BT, bool MOE>
-__device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, const int32_t* prefix,
-                                                const int32_t* offs, uint32_t unit) {
-  TileInfo t;
-  const int64_t kb_total = p.k / 128;
-  if (!MOE) {
-    // m-major: concurrent CTAs share one X tile and stream different weight tiles
-    const int nt = tile % p.num_n_tiles;
-    const int mt = tile / p.num_n_tiles;
-    t.m0 = mt * BT;
-    t.m_end = static_cast<int32_t>(p.m < t.m0 + BT ? p.m : t.m0 + BT);
-    t.n0 = nt * 128;
-    t.base = p.packed;
-    t.wbase = p.packed + kHeaderBytes + static_cast<size_t>(nt) * kb_total * unit;
-  } else {
-    const int e = find_expert(prefix, p.num_experts, tile);
-    const int local = tile - prefix[e];
-    const int cnt = offs[e + 1] - offs[e];
-    const int mte = (cnt + BT - 1) / BT;
-    const int nt = local / mte;
-    const int mt = local - nt * mte;
-    t.m0 = offs[e] + mt * BT;
-    t.m_end = min(offs[e + 1], t.m0 + BT);
-    t.n0 = nt * 128;
-    t.base = p.packed_list[e];
-    t.wbase = t.base + kHeaderBytes + static_cast<size_t>(nt) * kb_total * unit;
-  }
-  return t;
-}
-
-__device__ __forceinline__ bool header_ok(const uint8_t* packed, const F16Params& p, uint32_t has_zero) {
-  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
-  return h->magic == kMagic && static_cast<int32_t>(h->fmt) == p.fmt && h->n == p.n &&
-         h->k == p.k && h->has_zero == has_zero;
-}
-
-// Wait without looking at the abort flag (used to drain in-flight work before exit).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(a, parity)) {
-    if (globaltimer() - t0 > limit_ns) return;
-  }
-}
 
 // WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4.
 template <int BT, int WK, bool MOE>
@@ -177,17 +131,17 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
-      mbar_init(&empty_l[s], 1 + kDqWarps);
+      mbar_init(&empty_l[s], S::kIss + kDqWarps);
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&full_a[s], kDqGroup);
       mbar_init(&empty_a[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], S::kIss);
       mbar_init(&acc_empty[b], 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, S::kIss);
     fence_barrier_init();
     *abort_flag = 0u;
     // The first weight's header decides whether INT4 units carry zero-points; every weight
@@ -200,52 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     }
   }
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
-  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
-  if (MOE && warp == 2) pdl_wait();   // the offsets below may be written by the previous kernel
+  if (warp == kMmaWarp0) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (MOE && warp == kDqWarp0) pdl_wait();   // the offsets below may be written by the previous kernel
 
   int32_t num_tiles = p.sched.num_tiles;
   if (MOE) {
-    // Per-expert tile counts and their exclusive prefix (warp 2), offsets copied to shared.
-    if (warp == 2) {
-      const int E = p.num_experts;
-      const int per = (E + 31) / 32;
-      const int e0 = lane * per;
-      int local = 0;
-      bool bad = false;
-      for (int i = 0; i < per; ++i) {
-        const int e = e0 + i;
-        if (e < E) {
-          const int a = p.offsets[e], b = p.offsets[e + 1];
-          bad |= (b < a) || (a < 0) || (b > p.m);
-          offs[e] = a;
-          local += b > a ? ((b - a + BT - 1) / BT) * p.num_n_tiles : 0;
-        }
-      }
-      if (lane == 0) {
-        offs[E] = p.offsets[E];
-        bad |= p.offsets[0] != 0;
-      }
-      int incl = local;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += v;
-      }
-      int run = incl - local;
-      for (int i = 0; i < per; ++i) {
-        const int e = e0 + i;
-        if (e < E) {
-          prefix[e] = run;
-          const int a = p.offsets[e], b = p.offsets[e + 1];
-          run += b > a ? ((b - a + BT - 1) / BT) * p.num_n_tiles : 0;
-        }
-      }
-      if (lane == 31) prefix[E] = incl;
-      if (__any_sync(0xffffffffu, bad) && lane == 0) {
-        atomicOr(p.err, kErrOffsets);
-        *abort_flag = 1u;
-      }
-    }
+    // Per-expert tile counts and their exclusive prefix (first dequant warp), offsets copied to shared.
+    if (warp == kDqWarp0) moe_tile_prefix<BT>(p, offs, prefix, abort_flag, lane);
   }
   __syncthreads();
   tc_fence_after();
@@ -274,137 +189,179 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       prefetch_tmap(&p.tmap_x);
       const uint64_t pol_w = reuse_w ? policy_evict_last() : policy_evict_first();
       const uint64_t pol_x = reuse_w ? policy_evict_normal() : policy_evict_last();
-      int ls = 0;
-      uint32_t lph = 0;
-      int issued = 0;
       const uint8_t* last_checked = nullptr;
-      Segment seg;
+      // A weight buffer is read only after its header matched the call (MoE: each expert's).
+      auto checked = [&](const TileInfo& t) -> bool {
+        if (!MOE || t.base == last_checked) return true;
+        if (!header_ok(t.base, p, has_zero)) {
+          atomicOr(p.err, kErrHeader);
+          *abort_flag = 1u;
+          return false;
+        }
+        last_checked = t.base;
+        return true;
+      };
+      // Stage `idx` (ring slot idx % SL) covers k-blocks [kb, kb + g) of tile t.
+      auto issue_w = [&](int idx, const TileInfo& t, int kb, int g) {
+        const int slot = idx % SL;
+        const uint32_t bytes = static_cast<uint32_t>(g) * kUnit;
+        mbar_arrive_expect_tx(&full_w[slot], bytes);
+        bulk_g2s(smem + S::kWOff + slot * S::kWStage, t.wbase + static_cast<size_t>(kb) * kUnit, bytes,
+                 &full_w[slot], pol_w);
+      };
+      auto issue_x = [&](int idx, const TileInfo& t, int kb) {
+        const int slot = idx % SL;
+        uint8_t* xs = smem + S::kXOff + slot * S::kXStage;
+        trace_stage(p.trace, 0, idx);
+        mbar_arrive_expect_tx(&full_x[slot], S::kXStage);   // the whole box lands (zero-filled past K)
+        if constexpr (S::kG == 1) {
+          tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[slot], pol_x);
+          tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[slot], pol_x);
+        } else {
+          tma_3d_g2s(xs, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[slot], pol_x);
+        }
+        if (idx == 0) trace_mark(p.trace, 2);
+      };
+      // Start-up order. The weights of stage 0 do not depend on the previous kernel, so the
+      // dense path streams them before waiting for it. Then the activation tiles of the first SL
+      // stages go out before the rest of their weights: an SM's copies complete roughly in issue
+      // order, and an activation tile queued behind ~100 KB of weights would hold back the first
+      // MMA by microseconds.
+      int issued_w = 0, issued_x = 0;
       bool ok = true;
-      // Weights do not depend on the previous kernel: stream the first pipeline stages of them
-      // before waiting for it (dense path), then issue the activation loads.
-      int pre = 0;
       if (!MOE) {
         SchedIter pf = sched;
         Segment ps;
-        while (pre < SL && pf.next(ps)) {
+        if (pf.next(ps)) {
           const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
-          for (int kb = ps.kb0; kb < ps.kb1 && pre < SL; kb += S::kG, ++pre) {
-            const uint32_t bytes = static_cast<uint32_t>(min(S::kG, ps.kb1 - kb)) * kUnit;
-            mbar_arrive_expect_tx(&full_w[pre], bytes);
-            bulk_g2s(smem + S::kWOff + pre * S::kWStage, t.wbase + static_cast<size_t>(kb) * kUnit, bytes,
-                     &full_w[pre], pol_w);
-          }
+          issue_w(0, t, ps.kb0, min(S::kG, ps.kb1 - ps.kb0));
+          issued_w = 1;
         }
       }
       pdl_wait();
+      {
+        SchedIter pf = sched;
+        Segment ps;
+        int idx = 0;
+        while (idx < SL && pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          for (int kb = ps.kb0; kb < ps.kb1 && idx < SL; kb += S::kG, ++idx) issue_x(idx, t, kb);
+        }
+        issued_x = idx;
+        pf = sched;
+        idx = 0;
+        while (idx < issued_x && pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          if (!checked(t)) { ok = false; break; }
+          for (int kb = ps.kb0; kb < ps.kb1 && idx < issued_x; kb += S::kG, ++idx)
+            if (idx >= issued_w) issue_w(idx, t, kb, min(S::kG, ps.kb1 - kb));
+        }
+        if (ok) issued_w = issued_x;
+      }
+      // Steady state: a stage is refilled once every consumer released it.
+      int idx = 0;
+      int ls = 0;
+      uint32_t lph = 0;
+      Segment seg;
       while (ok && sched.next(seg)) {
         const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
-        if (MOE) {
-          if (t.base != last_checked) {
-            if (!header_ok(t.base, p, has_zero)) {
-              atomicOr(p.err, kErrHeader);
-              *abort_flag = 1u;
-              break;
-            }
-            last_checked = t.base;
-          }
-        }
-        for (int kb = seg.kb0; kb < seg.kb1; kb += S::kG) {
-          if (issued >= pre) {   // the first `pre` stages are free and already hold their weights
+        if (!checked(t)) break;
+        for (int kb = seg.kb0; kb < seg.kb1; kb += S::kG, ++idx) {
+          if (idx >= issued_x) {
             if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
-            uint8_t* ws = smem + S::kWOff + ls * S::kWStage;
-            const uint32_t bytes = static_cast<uint32_t>(min(S::kG, seg.kb1 - kb)) * kUnit;
-            mbar_arrive_expect_tx(&full_w[ls], bytes);
-            bulk_g2s(ws, t.wbase + static_cast<size_t>(kb) * kUnit, bytes, &full_w[ls], pol_w);
+            issue_w(idx, t, kb, min(S::kG, seg.kb1 - kb));   // weights first: the dequant needs them first
+            issue_x(idx, t, kb);
+            issued_x = issued_w = idx + 1;
           }
-          trace_stage(p.trace, 0, issued);
-          uint8_t* xs = smem + S::kXOff + ls * S::kXStage;
-          mbar_arrive_expect_tx(&full_x[ls], S::kXStage);   // the whole box lands (zero-filled past K)
-          if constexpr (S::kG == 1) {
-            tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[ls], pol_x);
-            tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[ls], pol_x);
-          } else {
-            tma_3d_g2s(xs, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[ls], pol_x);
-          }
-          if (issued == 0) trace_mark(p.trace, 2);
-          ++issued;
           if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
       }
       trace_mark(p.trace, 3);
       if (*abort_flag) {
-        // Let copies already in flight land before the CTA's shared memory goes away.
-        const int n = issued < SL ? issued : SL;
-        for (int i = 0; i < n; ++i) {
-          if (--ls < 0) { ls = SL - 1; lph ^= 1u; }
-          drain_wait(&full_w[ls], lph, 100000000ull);
-          drain_wait(&full_x[ls], lph, 100000000ull);
-        }
+        // Let copies already in flight (at most the last SL stages issued) land before the
+        // CTA's shared memory goes away.
+        for (int i = issued_x > SL ? issued_x - SL : 0; i < issued_x; ++i)
+          drain_wait(&full_x[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
+        for (int i = issued_w > SL ? issued_w - SL : 0; i < issued_w; ++i)
+          drain_wait(&full_w[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < kMmaWarp0 + S::kIss) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `is` takes the 128-K blocks whose running sequence index bi has bi % kIss == is,
+    // accumulating into its own TMEM accumulator; A slot bi % SA holds block bi.
     if (lane == 0) {
+      const int is = warp - kMmaWarp0;
       constexpr uint32_t idesc = idesc_bf16(128, BT);
-      int ls = 0, as = 0;
-      uint32_t lph = 0, aph = 0, acc_i = 0;   // A slot `as` / parity `aph` follow the block sequence
-      int mma_count = 0;
+      int ls = 0;
+      uint32_t lph = 0, acc_i = 0;
+      int seq = 0;
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
         const uint32_t b = acc_i & 1u;
         if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t d = tmem + b * BT;
+        const uint32_t d = tmem + (b * S::kIss + is) * BT;
+        bool first = true;
         for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+          // Wait for the stage even without a block in it: the release below must not reach
+          // the slot's empty barrier before the slot's previous use is over.
           if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
+          if (is == 0) trace_stage(p.trace, 7, seq / S::kG);
           const int g = min(S::kG, seg.kb1 - kb0);
           for (int j = 0; j < g; ++j) {
-          const int kb = kb0 + j;
-          if (!mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
-          tc_fence_after();
-          if (acc_i == 0 && kb == seg.kb0) trace_mark(p.trace, 6);
-          trace_stage(p.trace, 3, mma_count);
-          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
-          if constexpr (S::kATmem) {
-            const uint32_t a_t = tmem + S::kACol0 + as * 64;
+            const int bi = seq + j;
+            if (S::kIss > 1 && bi % S::kIss != is) continue;
+            const int as = bi % SA;
+            const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
+            if (!mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
+            trace_stage(p.trace, 3, bi);
+            tc_fence_after();
+            if (is == 0 && acc_i == 0 && first) trace_mark(p.trace, 6);
+            trace_stage(p.trace, 4, bi);
+            const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
+            if constexpr (S::kATmem) {
+              const uint32_t a_t = tmem + S::kACol0 + as * 64;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
-              mma_bf16_ta(d, a_t + 8 * k, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
-            }
-          } else {
-            const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+                mma_bf16_ta(d, a_t + 8 * k, bd, idesc, (!first || k > 0) ? 1u : 0u);
+              }
+            } else {
+              const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
-              const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
-              mma_bf16(d, ad, bd, idesc, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+                mma_bf16(d, ad, bd, idesc, (!first || k > 0) ? 1u : 0u);
+              }
             }
-          }
-          tc_commit(&empty_a[as]);
-          trace_stage(p.trace, 4, mma_count++);
-          if (++as == SA) { as = 0; aph ^= 1u; }
+            first = false;
+            trace_stage(p.trace, 5, bi);
+            tc_commit(&empty_a[as]);
+            trace_stage(p.trace, 6, bi);
           }
           if (!ok) break;
           tc_commit(&empty_l[ls]);
+          seq += g;
           if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[b]);
+        tc_commit(&acc_full[b]);   // also when this issuer had no block in the tile
         ++acc_i;
       }
-      trace_mark(p.trace, 7);
-      // All tcgen05 work of this thread has completed once `drain` flips.
+      if (is == 0) trace_mark(p.trace, 7);
+      // All tcgen05 work of this thread has completed once `drain` flips (one arrival per issuer).
       tc_commit(drain);
       drain_wait(drain, 0, 1000000000ull);
     }
     __syncwarp();
-  } else if (warp < 2 + kDqWarps) {
+  } else if (warp >= kDqWarp0 && warp < kEpiWarp0) {
     // ------------------------------------------------------------ dequant warps
     // Warp -> (group, row, K half). With A in TMEM a warp may only touch its own 32-lane
     // quarter (warp index % 4), so rows follow the quarter; otherwise rows follow the thread.
-    const int dw = warp - 2;
+    const int dw = warp - kDqWarp0;
     const int grp = dw / kDqGroup;                 // takes the blocks with sequence index % 2 == grp
     const int r = 32 * (warp & 3) + lane;          // weight row within the tile (TMEM lane)
     int ls = 0;
@@ -435,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
         if (!mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
         if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
+        if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 1, bi);
         const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
         // INT4 takes the whole 128-K row into registers at once; MXFP4 (whose scale and
         // conversion need more registers) takes the second half after converting the first.
@@ -509,13 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           fence_proxy_async_smem();
         }
         __syncwarp();
+        if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 2, bi);
         if (lane == 0) mbar_arrive(&full_a[as]);
         }
         seq += g;
         if (++ls == SL) { ls = 0; lph ^= 1u; }
       }
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue warps (last four)
     pdl_wait();                          // Y, partials and counters may be in use by the previous kernel
     const int q = warp & 3;              // TMEM lane quarter this warp may access
@@ -523,29 +482,59 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
     uint32_t acc_i = 0;
     bool first_seg = true;
+    int seq = 0;                         // running 128-K block index, as the issuers count it
     Segment seg;
     while (sched.next(seg)) {
       const uint32_t b = acc_i & 1u;
+      // Issuer i wrote its accumulator iff the segment has a block with sequence index % 2 == i.
+      const int nb = seg.kb1 - seg.kb0;
+      const bool use1 = S::kIss > 1 && (nb >= 2 || (seq & 1) == 1);
+      const bool use0 = S::kIss == 1 || nb >= 2 || (seq & 1) == 0;
+      seq += nb;
       if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
       tc_fence_after();
       if (row == 0 && acc_i == 0) trace_mark(p.trace, 8);
       const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
       const int64_t n = static_cast<int64_t>(t.n0) + row;
       const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
+      // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
+      // others' published partials and adds them to its own accumulator; the others publish.
+      const bool owner = !full && seg.kb0 == 0;
+      uint32_t* flag = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+      int64_t c_hi = 0;
+      bool have = true;
+      if (owner) {
+        c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
+        if (row == 0) trace_mark(p.trace, 10);
+      }
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * S::kIss * BT;
       float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                     static_cast<size_t>(row) * BT;
 #pragma unroll 1
-      for (int j0 = 0; j0 < BT; j0 += 16) {
+      for (int j0 = 0; j0 < BT && have; j0 += 16) {
         uint32_t v[16];
-        tmem_ld16(tbase + j0, v);
-        tmem_wait_ld();
-        if (full) {
+        tmem_ld16(tbase + (use0 ? 0 : BT) + j0, v);
+        if (S::kIss > 1 && use0 && use1) {
+          uint32_t v1[16];
+          tmem_ld16(tbase + BT + j0, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(v1[jj]));
+        } else {
+          tmem_wait_ld();
+        }
+        if (full || owner) {
+          float a[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
+          if (owner)
+            sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
           if (n < p.n) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
-              if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(__uint_as_float(v[jj]));
+              if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(a[jj]);
             }
           }
         } else {
@@ -561,28 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++acc_i;
       if (row == 0) trace_mark(p.trace, 9);
-      if (!full) {
-        // Stream-K fix-up, per warp (32 rows): publish the partial, count arrivals; the last
-        // CTA to arrive sums every CTA's partial for these rows in k order.
-        __threadfence();
+      if (!full && !owner) sk_publish(flag, lane);
+      if (owner && have) {
         __syncwarp();
-        uint32_t old = 0;
-        uint32_t* ctr = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
-        if (lane == 0) old = atomicAdd(ctr, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (row == 0) trace_mark(p.trace, 10);
-        const int64_t c_lo = sk_owner(static_cast<int64_t>(seg.tile) * kb_total, total_it, p.sched.grid);
-        const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
-        if (old == static_cast<uint32_t>(c_hi - c_lo)) {
-          __threadfence();
-          streamk_fixup<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, c_lo, c_hi, row,
-                            [&](int j, float acc) {
-                              const int64_t m = static_cast<int64_t>(t.m0) + j;
-                              if (m < t.m_end && n < p.n) p.y[m * p.n + n] = __float2bfloat16_rn(acc);
-                            });
-          if (lane == 0) *ctr = 0u;
-          if (row == 0) trace_mark(p.trace, 11);
-        }
+        if (lane == 0) *flag = 0u;
+        if (row == 0) trace_mark(p.trace, 11);
       }
       first_seg = false;
     }
@@ -590,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 
   __syncwarp();  // reconverge lanes that skipped a single-thread role before the CTA barrier
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, S::kTmemCols);
     if (lane == 0) {
@@ -639,7 +611,14 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
 
 int f16_group(int tile_m) { return f16_group_of(tile_m); }
 
-int f16_stages(int tile_m) {
+bool f16s_serves(int fmt, int tile_m) {
+  if (fmt != kW4A16Int4 || (tile_m != 16 && tile_m != 32)) return false;
+  const char* e = std::getenv("HM_F16_SMALL");
+  return !(e && e[0] == '0');
+}
+
+int f16_stages(int fmt, int tile_m) {
+  if (f16s_serves(fmt, tile_m)) return f16s_stages(tile_m);
   switch (tile_m) {
     case 16: return F16Shape<16>::kSL;
     case 32: return F16Shape<32>::kSL;
@@ -650,6 +629,7 @@ int f16_stages(int tile_m) {
 }
 
 cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st) {
+  if (f16s_serves(p.fmt, tile_m)) return launch_f16s_gemm(p, tile_m, moe, st);
   if (p.fmt == kW4A16Mx) return moe ? launch_bt<2, true>(p, tile_m, st) : launch_bt<2, false>(p, tile_m, st);
   return moe ? launch_bt<0, true>(p, tile_m, st) : launch_bt<0, false>(p, tile_m, st);
 }

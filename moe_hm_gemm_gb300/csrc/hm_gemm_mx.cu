@@ -269,22 +269,37 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       const int64_t m_end = p.m < m0 + BT ? p.m : m0 + BT;
       const int64_t n = static_cast<int64_t>(nt) * 128 + row;
       const bool full_seg = seg.kb0 == 0 && seg.kb1 == kb_total;
+      // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
+      // others' published partials and adds them to its own accumulator; the others publish.
+      const bool owner = !full_seg && seg.kb0 == 0;
+      uint32_t* flag = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+      int64_t c_hi = 0;
+      bool have = true;
+      if (owner) {
+        c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
+      }
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
       float* slotp = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                      static_cast<size_t>(row) * BT;
 #pragma unroll 1
-      for (int j0 = 0; j0 < BT; j0 += 16) {
+      for (int j0 = 0; j0 < BT && have; j0 += 16) {
         uint32_t v[16];
         tmem_ld16(tbase + j0, v);
         tmem_wait_ld();
-        if (full_seg) {
+        if (full_seg || owner) {
+          float a[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
+          if (owner)
+            sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
           if (n < p.n) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int64_t m = m0 + j0 + jj;
               if (m < m_end) {
                 const float sc = NV ? gscale : p.s_tok[m];
-                p.y[m * p.n + n] = __float2bfloat16_rn(__uint_as_float(v[jj]) * sc);
+                p.y[m * p.n + n] = __float2bfloat16_rn(a[jj] * sc);
               }
             }
           }
@@ -300,27 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++acc_i;
-      if (!full_seg) {
-        __threadfence();
+      if (!full_seg && !owner) sk_publish(flag, lane);
+      if (owner && have) {
         __syncwarp();
-        uint32_t old = 0;
-        uint32_t* ctr = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
-        if (lane == 0) old = atomicAdd(ctr, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        const int64_t c_lo = sk_owner(static_cast<int64_t>(seg.tile) * kb_total, total_it, p.sched.grid);
-        const int64_t c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
-        if (old == static_cast<uint32_t>(c_hi - c_lo)) {
-          __threadfence();
-          streamk_fixup<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, c_lo, c_hi, row,
-                            [&](int j, float acc) {
-                              const int64_t m = m0 + j;
-                              if (m < m_end && n < p.n) {
-                                const float sc = NV ? gscale : p.s_tok[m];
-                                p.y[m * p.n + n] = __float2bfloat16_rn(acc * sc);
-                              }
-                            });
-          if (lane == 0) *ctr = 0u;
-        }
+        if (lane == 0) *flag = 0u;
       }
       first_seg = false;
     }

@@ -86,7 +86,13 @@ cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream
 constexpr int f16_group_of(int tile_m) { return tile_m <= 32 ? 4 : (tile_m == 64 ? 2 : 1); }
 int f16_group(int tile_m);
 cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st);
-int f16_stages(int tile_m);
+// Load stages of the W4A16 kernel that serves (fmt, tile_m).
+int f16_stages(int fmt, int tile_m);
+// Small-token INT4 kernel (tile_m 16 or 32; hm_gemm_f16s.cu), chosen by launch_f16_gemm unless
+// HM_F16_SMALL=0 in the environment.
+cudaError_t launch_f16s_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+int f16s_stages(int tile_m);
+bool f16s_serves(int fmt, int tile_m);
 int mx_stages(int fmt, int tile_m);
 
 // Weight preprocessing and activation quantization launchers (hm_weights.cu, hm_act.cu).

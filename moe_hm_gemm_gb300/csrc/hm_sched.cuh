@@ -5,11 +5,13 @@
 //  * stream-K (small M, fewer tiles than SMs): the flattened (tile, k-block) space of
 //    num_tiles*kb_total iterations is cut into G contiguous ranges, start(c) =
 //    floor(c*total/G); a CTA's range crosses tile boundaries, so a tile may be shared by
-//    several CTAs, each producing an fp32 partial that one of them (the last to finish,
-//    found with an atomic counter) sums in k order. G <= total guarantees every range is
-//    non-empty, so the number of CTAs sharing a tile is exactly c_hi - c_lo + 1.
+//    several CTAs, each producing an fp32 partial that the tile's owner (the CTA holding its
+//    first k-block) sums in k order (fixed-owner hand-off below). G <= total guarantees every
+//    range is non-empty, so the number of CTAs sharing a tile is exactly c_hi - c_lo + 1.
 #pragma once
 #include <cstdint>
+
+#include "hm_device.cuh"
 
 namespace hm {
 
@@ -76,61 +78,92 @@ struct SchedIter {
   }
 };
 
-// Sum the stream-K partials of one tile for one accumulator row, in k order (CTA c_lo first),
-// and hand each column's total to `emit(j, value)`. Partials are laid out
-// [cta][first/last segment][row][tile_m] (fp32), so each lane reads its row's columns with
-// 16-byte loads; four contributors' loads are issued before any of them is summed, which keeps
-// many independent L2 reads in flight instead of one dependent read per column.
-template <int BT, typename Emit>
-__device__ __forceinline__ void streamk_fixup(const float* partial, int64_t total_it, int32_t grid,
-                                              int32_t kb_total, int32_t tile, int64_t c_lo, int64_t c_hi,
-                                              int row, Emit emit) {
+// ---------------------------------------------------------------------------------------
+// Fixed-owner hand-off of a stream-K tile. The owner is the CTA whose range holds the tile's
+// first k-block (segment with kb0 == 0). In forward stream-K order that is the last segment of
+// its range, while every other contributor holds the tile in the first segment of its own range,
+// so by the time the owner finishes, the others have long published. Non-owners store their
+// fp32 partial rows ([cta][first/last segment][row][tile_m]) and add 1 to the tile's per-warp
+// flag with release semantics, without waiting for anything; the owner waits (bounded) until the
+// flag shows all of them, adds their partials to its own in k order (CTA c_lo = itself first,
+// so the sum is deterministic), writes Y and clears the flag for the next call.
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Non-owner: publish this warp's partial rows (already stored by every lane).
+__device__ __forceinline__ void sk_publish(uint32_t* flag, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(flag) : "memory");
+}
+
+// Owner: wait until `expect` contributors have published. Every lane polls with an acquire load,
+// so its later loads of the partials are ordered after the flag. False when the CTA is aborting
+// or the wait ran out (then kErrTimeout and the abort flag are set).
+__device__ __forceinline__ bool sk_wait(const uint32_t* flag, uint32_t expect, const WaitCtx& ctx) {
+  if (ld_acquire_gpu(flag) >= expect) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (ld_acquire_gpu(flag) >= expect) return true;
+    if (*ctx.abort) return false;
+    if (globaltimer() - t0 > ctx.timeout_ns) {
+      *ctx.abort = 1u;
+      atomicOr(ctx.err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Owner: add columns [j0, j0 + 16) of the other contributors' partial rows (CTAs c_lo+1 .. c_hi,
+// in that order) to `acc`, which holds the owner's own values. Loads of up to four contributors
+// are in flight together.
+template <int BT>
+__device__ __forceinline__ void sk_add_partials(const float* partial, int64_t total_it, int32_t grid,
+                                                int32_t kb_total, int32_t tile, int64_t c_lo, int64_t c_hi,
+                                                int row, int j0, float (&acc)[16]) {
   auto src = [&](int64_t c) {
     const int which = (sk_start(c, total_it, grid) / kb_total == tile) ? 0 : 1;
-    return partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 + static_cast<size_t>(row) * BT;
+    return reinterpret_cast<const float4*>(partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 +
+                                           static_cast<size_t>(row) * BT + j0);
   };
+  int64_t c = c_lo + 1;
 #pragma unroll 1
-  for (int j0 = 0; j0 < BT; j0 += 16) {
-    float acc[16];
+  for (; c + 3 <= c_hi; c += 4) {
+    float4 v[4][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    int64_t c = c_lo;
-#pragma unroll 1
-    for (; c + 3 <= c_hi; c += 4) {
-      float4 v[4][4];
+    for (int u = 0; u < 4; ++u) {
+      const float4* s4 = src(c + u);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4* s4 = reinterpret_cast<const float4*>(src(c + u) + j0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[u][i] = __ldcg(s4 + i);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[4 * i] += v[u][i].x;
-          acc[4 * i + 1] += v[u][i].y;
-          acc[4 * i + 2] += v[u][i].z;
-          acc[4 * i + 3] += v[u][i].w;
-        }
-      }
+      for (int i = 0; i < 4; ++i) v[u][i] = __ldcg(s4 + i);
     }
-#pragma unroll 1
-    for (; c <= c_hi; ++c) {
-      const float4* s4 = reinterpret_cast<const float4*>(src(c) + j0);
-      float4 v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = __ldcg(s4 + i);
+    for (int u = 0; u < 4; ++u) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc[4 * i] += v[i].x;
-        acc[4 * i + 1] += v[i].y;
-        acc[4 * i + 2] += v[i].z;
-        acc[4 * i + 3] += v[i].w;
+        acc[4 * i] += v[u][i].x;
+        acc[4 * i + 1] += v[u][i].y;
+        acc[4 * i + 2] += v[u][i].z;
+        acc[4 * i + 3] += v[u][i].w;
       }
     }
+  }
+#pragma unroll 1
+  for (; c <= c_hi; ++c) {
+    const float4* s4 = src(c);
+    float4 v[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) emit(j0 + i, acc[i]);
+    for (int i = 0; i < 4; ++i) v[i] = __ldcg(s4 + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[4 * i] += v[i].x;
+      acc[4 * i + 1] += v[i].y;
+      acc[4 * i + 2] += v[i].z;
+      acc[4 * i + 3] += v[i].w;
+    }
   }
 }
 

@@ -133,3 +133,21 @@ def test_mxfp4_extreme_scales(hm, log2_gain):
     y = hm.gemm(2, x.cuda(), packed, n, k)
     torch.cuda.synchronize()
     assert_close(y, og.gemm(bf16_np(x), qw.what), f"mxfp4 gain 2^{log2_gain}")
+
+
+@pytest.mark.parametrize("small", ["0", "1"])
+@pytest.mark.parametrize("m", [1, 5, 16, 17, 32])
+def test_small_token_kernel_and_general_kernel(hm, env, small, m):
+    """INT4 token tiles of 16 and 32 go to the small-token kernel (group scale applied to each
+    block's fp32 partial sum); HM_F16_SMALL=0 keeps the general kernel. Both must match the oracle,
+    with stream-K splitting tiles (grid > tiles) and without."""
+    env["HM_F16_SMALL"] = small
+    run_case(hm, 1, m, 640, 3072, True, seed=40 + m)
+    run_case(hm, 1, m, 256, 1024, False, seed=60 + m)
+
+
+@pytest.mark.parametrize("stream_k", ["0", "1"])
+def test_small_token_kernel_long_k(hm, env, stream_k):
+    """Many 128-K blocks per tile: the block-accumulator ring and A slots wrap many times."""
+    env["HM_STREAM_K"] = stream_k
+    run_case(hm, 1, 9, 384, 14336, True, seed=77)

@@ -74,3 +74,12 @@ def test_bad_offsets_set_device_error(hm):
     offs = torch.tensor([0, 6, 3], dtype=torch.int32, device="cuda")   # decreasing
     hm.moe_gemm(1, x, offs, ptrs, n, k)
     assert hm.device_error() & 4
+
+
+@pytest.mark.parametrize("small", ["0", "1"])
+def test_small_tiles_both_kernels(hm, small, monkeypatch):
+    monkeypatch.setenv("HM_F16_SMALL", small)
+    monkeypatch.setenv("HM_MOE_TILE_M", "16")
+    moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=True, seed=11)
+    monkeypatch.setenv("HM_MOE_TILE_M", "32")
+    moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=False, seed=12)
