@@ -219,9 +219,10 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
  * 7 last MMA commit, 8 first accumulator seen by the epilogue, 9 last tile stored, 10 stream-K
  * arrival counted, 11 fix-up done, 12 exit; slot 13 holds the SM id. The buffer must hold
  * 256*16 + 8*64 uint64: after the 256 per-CTA rows, CTA 0 stamps its first 64 load stages and
- * 128-K blocks in eight rows of 64 (load issued; dequant start, dequant done; then per block
- * on its MMA issuer: A ready seen, fence passed, MMAs issued, commit issued; last row: the
- * accumulator slot seen free (small-token kernel) or the stage's activation tile seen). The
+ * 128-K blocks in eight rows of 64 (row 0: load issued, or in the small-token kernel the block's
+ * accumulator seen by the epilogue; dequant start, dequant done; then per block on its MMA
+ * issuer: A ready seen, fence passed, MMAs issued, commit issued; last row: the accumulator slot
+ * seen free (small-token kernel) or the stage's activation tile seen). The
  * buffer stays owned by the caller; concurrent launches overwrite each other's stamps. */
 hm_status hm_set_trace_buffer(void* trace, size_t bytes);
 

@@ -12,10 +12,14 @@
 //    one bf16x2 subtract per pair of weights), and each block accumulates into its own TMEM
 //    accumulator taken from a ring; the epilogue warps add s * P_block in fp32, block by block,
 //    in k order (deterministic);
-//  * a single thread issuing tcgen05.mma waits ~50 cycles per instruction, while the tensor core
-//    takes small-N MMAs from several threads far faster, so three warps issue MMAs (block i goes
-//    to issuer i % 3; a fourth would put a fifth warp on one SM sub-partition and cut every
-//    thread's registers to 96);
+//  * a thread that issues tcgen05.mma waits ~50 cycles per instruction and then stalls at its next
+//    shared-memory access until its MMAs drain, while the tensor core takes small-N MMAs from
+//    several threads far faster. So the two 128-K blocks of each half load stage form a pair,
+//    pairs go round-robin to NI issuing warps (3 for tile_m 16, 2 for 32, as TMEM allows), and an
+//    issuer waits once per pair and then issues its 16 MMAs back to back;
+//  * every TMEM slot (restored weights, block accumulator) and its barriers belong to one
+//    (issuer, dequant group) pair, so each barrier has one producer and one consumer that use it
+//    strictly in turn: every wait is for the next phase of that slot, never one further ahead;
 //  * everything else (persistent CTA per SM, TMA bulk loads of packed 128x128 units, weights
 //    restored into TMEM as the MMA's A operand, stream-K for tiles fewer than SMs, PDL, bounded
 //    waits) follows the general kernel.
@@ -31,46 +35,59 @@
 namespace hm {
 namespace {
 
-constexpr int kSIss = 3;                     // MMA issuing warps
+constexpr int kSIssMax = 3;                  // MMA issuing warps (tile_m 32 uses two of them)
 constexpr int kSDqGroup = 4;                 // warps per dequant group (one per TMEM lane quarter)
 constexpr int kSDqWarps = 2 * kSDqGroup;     // two groups take alternate 128-K blocks
 constexpr int kSMma0 = 1;                    // warps: 0 producer, 1-3 MMA, 4-11 dequant, 12-15 epilogue
-constexpr int kSDq0 = kSMma0 + kSIss;
+constexpr int kSDq0 = kSMma0 + kSIssMax;
 constexpr int kSEpi0 = kSDq0 + kSDqWarps;
 constexpr int kSThreads = 32 * (kSEpi0 + 4);   // 16 warps: 4 per SM sub-partition, 128 registers each
 
 template <int BT>
 struct SShape {
-  static constexpr int kG = f16_group_of(BT);       // 128-K blocks per load stage
-  static constexpr int kRA = 128 / BT;              // block accumulators: TMEM columns [0, 128)
-  static constexpr int kSA = 6;                     // restored-weight slots: 64 columns each from 128
-  static constexpr uint32_t kACol0 = 128;
-  static constexpr int kMeta = kSA + kRA;           // scale ring (see the dequant warps)
+  static constexpr int kG = f16_group_of(BT);       // 128-K blocks per load stage (4)
+  static constexpr int kNI = BT == 16 ? 3 : 2;      // issuing warps
+  static constexpr int kNS = 2 * kNI;               // slots: (issuer, dequant group)
+  static constexpr uint32_t kACol0 = kNS * BT;      // block accumulators at [0, kNS*BT), then A slots
   static constexpr int kXStage = kG * BT * 128 * 2;
   static constexpr int kWStage = kG * kUnitInt4Zp;
-  static constexpr int kMetaBytes = kMeta * 128 * 4;
+  static constexpr int kMetaBytes = kNS * 2 * 128 * 4;   // group scales: [slot][use parity][row]
   static constexpr int kSLFit = (212 * 1024 - kMetaBytes) / (kXStage + kWStage);
   static constexpr int kSL = kSLFit > 16 ? 16 : kSLFit;
   static constexpr int kXOff = 0;
   static constexpr int kWOff = kXOff + kSL * kXStage;
   static constexpr int kMetaOff = kWOff + kSL * kWStage;
   static constexpr int kBarOff = kMetaOff + kMetaBytes;
-  static constexpr int kNumBars = 3 * kSL + 2 * kSA + 2 * kRA + kMeta + 1;
+  static constexpr int kNumBars = 3 * kSL + 6 * kNS + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kMoeOff = kMiscOff + 32;
   static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
   static_assert(BT == 16 || BT == 32, "small token tiles only");
-  static_assert(kSL >= 2, "load pipeline depth");
-  static_assert(kRA * BT == 128 && kACol0 + kSA * 64 <= 512, "TMEM budget");
+  static_assert(kSL >= 3, "load pipeline depth (the issuers' skipped stages rely on it)");
+  static_assert(kACol0 + kNS * 64 <= 512, "TMEM budget");
+  static_assert(kNI <= kSIssMax, "issuing warps");
+};
+
+// Walks the block sequence of a CTA's schedule the way every role does: segments, load stages of
+// up to kG blocks, and pairs of blocks (j, j + 1) within a stage; pair index `pair` runs over the
+// whole range. Block j of the current stage belongs to dequant group (seq + j) & 1 and to issuer
+// pair % NI.
+struct PairWalk {
+  int seq = 0;       // running block index at the current stage's start
+  int pair0 = 0;     // pair index of the current stage's first pair
+  __device__ __forceinline__ int pair_of(int j) const { return pair0 + (j >> 1); }
+  __device__ __forceinline__ void next_stage(int g) {
+    seq += g;
+    pair0 += (g + 1) >> 1;
+  }
 };
 
 template <int BT, bool MOE>
 __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_constant__ F16Params p) {
   using S = SShape<BT>;
   constexpr int SL = S::kSL;
-  constexpr int SA = S::kSA;
-  constexpr int RA = S::kRA;
-  constexpr int MT = S::kMeta;
+  constexpr int NI = S::kNI;
+  constexpr int NS = S::kNS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -79,13 +96,13 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
   uint64_t* full_w = bars;
   uint64_t* full_x = full_w + SL;
   uint64_t* empty_l = full_x + SL;
-  uint64_t* full_a = empty_l + SL;
-  uint64_t* empty_a = full_a + SA;
-  uint64_t* acc_full = empty_a + SA;
-  uint64_t* acc_empty = acc_full + RA;
-  uint64_t* meta_full = acc_empty + RA;
-  uint64_t* drain = meta_full + MT;
-  float* meta = reinterpret_cast<float*>(smem + S::kMetaOff);   // [MT][128] group scales
+  uint64_t* full_a = empty_l + SL;       // [slot] restored weights in TMEM (4 dequant warps)
+  uint64_t* empty_a = full_a + NS;       // [slot] their MMAs done (commit)
+  uint64_t* acc_full = empty_a + NS;     // [slot] block accumulator ready (commit)
+  uint64_t* acc_empty = acc_full + NS;   // [slot] drained by the epilogue (4 warps)
+  uint64_t* meta_full = acc_empty + NS;  // [slot][use parity] group scale written (4 dequant warps)
+  uint64_t* drain = meta_full + 2 * NS;
+  float* meta = reinterpret_cast<float*>(smem + S::kMetaOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 4);
   volatile uint32_t* hz_sh = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 8);
@@ -103,18 +120,17 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
-      mbar_init(&empty_l[s], kSIss + kSDqWarps);
+      mbar_init(&empty_l[s], 4 + kSDqWarps);   // epilogue warps (X read by the MMAs) + dequant warps (W)
     }
-    for (int s = 0; s < SA; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full_a[s], kSDqGroup);
       mbar_init(&empty_a[s], 1);
-    }
-    for (int s = 0; s < RA; ++s) {
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], 4);
+      mbar_init(&meta_full[2 * s], kSDqGroup);
+      mbar_init(&meta_full[2 * s + 1], kSDqGroup);
     }
-    for (int s = 0; s < MT; ++s) mbar_init(&meta_full[s], kSDqGroup);
-    mbar_init(drain, kSIss);
+    mbar_init(drain, NI);
     fence_barrier_init();
     *abort_flag = 0u;
     *hz_sh = hdr.has_zero == 1u ? 1u : 0u;
@@ -173,7 +189,6 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
       };
       auto issue_x = [&](int idx, const TileInfo& t, int kb) {
         const int slot = idx % SL;
-        trace_stage(p.trace, 0, idx);
         mbar_arrive_expect_tx(&full_x[slot], S::kXStage);   // the whole box lands (zero-filled past M, K)
         tma_3d_g2s(smem + S::kXOff + slot * S::kXStage, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[slot], pol_x);
         if (idx == 0) trace_mark(p.trace, 2);
@@ -238,52 +253,63 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
     }
   } else if (warp < kSDq0) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer `is` takes the blocks whose running sequence index bi has bi % 3 == is: block bi
-    // reads restored weights from A slot bi % SA and accumulates (from zero) into ring slot bi % RA.
-    if (lane == 0) {
+    // Issuer `is` takes pairs pair % NI == is. For each block of the pair (dequant group g =
+    // block & 1, slot is*2 + g): wait until the slot's accumulator was drained and its restored
+    // weights are in TMEM; then one fence and all of the pair's MMAs (each block into its own
+    // accumulator, from zero); then the commits. The issuers do not release load stages: the
+    // epilogue does, once it has seen the MMAs of a stage's last block complete.
+    if (lane == 0 && warp - kSMma0 < NI) {
       const int is = warp - kSMma0;
       constexpr uint32_t idesc = idesc_bf16(128, BT);
+      uint32_t par = 0u;   // bit g: parity of the number of uses of slot (is, g) so far
       int ls = 0;
       uint32_t lph = 0;
-      int seq = 0;
+      PairWalk pw;
       bool first = true;
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
         for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
-          // Wait for the stage even without a block in it: the release below must not reach the
-          // slot's empty barrier before the slot's previous use is over.
-          if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
           const int g = min(S::kG, seg.kb1 - kb0);
-          for (int j = 0; j < g; ++j) {
-            const int bi = seq + j;
-            if (bi % kSIss != is) continue;
-            const int ra = bi % RA;
-            if (!mbar_wait(&acc_empty[ra], (static_cast<uint32_t>(bi / RA) & 1u) ^ 1u, wc)) { ok = false; break; }
-            trace_stage(p.trace, 7, bi);
-            const int as = bi % SA;
-            if (!mbar_wait(&full_a[as], static_cast<uint32_t>(bi / SA) & 1u, wc)) { ok = false; break; }
-            trace_stage(p.trace, 3, bi);
+          bool have_x = false;
+          for (int j0 = 0; j0 < g && ok; j0 += 2) {
+            if (pw.pair_of(j0) % NI != is) continue;
+            if (!have_x) {
+              if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
+              have_x = true;
+            }
+            const int nb = min(2, g - j0);
+            for (int u = 0; u < nb && ok; ++u) {
+              const int gr = (pw.seq + j0 + u) & 1;
+              const int sl = 2 * is + gr;
+              const uint32_t ph = (par >> gr) & 1u;
+              ok = mbar_wait(&acc_empty[sl], ph ^ 1u, wc) && mbar_wait(&full_a[sl], ph, wc);
+              if (ok) trace_stage(p.trace, 3, pw.seq + j0 + u);
+            }
+            if (!ok) break;
             tc_fence_after();
             if (first && is == 0) trace_mark(p.trace, 6);
             first = false;
-            trace_stage(p.trace, 4, bi);
-            const uint32_t d = tmem + ra * BT;
-            const uint32_t a_t = tmem + S::kACol0 + as * 64;
-            const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
+            for (int u = 0; u < nb; ++u) {
+              const int sl = 2 * is + ((pw.seq + j0 + u) & 1);
+              const uint32_t d = tmem + sl * BT;
+              const uint32_t a_t = tmem + S::kACol0 + sl * 64;
+              const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + (j0 + u) * (2 * BT * 128);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
-              mma_bf16_ta(d, a_t + 8 * k, bd, idesc, k > 0 ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+                mma_bf16_ta(d, a_t + 8 * k, bd, idesc, k > 0 ? 1u : 0u);
+              }
+              trace_stage(p.trace, 5, pw.seq + j0 + u);
             }
-            trace_stage(p.trace, 5, bi);
-            tc_commit(&empty_a[as]);
-            tc_commit(&acc_full[ra]);
-            trace_stage(p.trace, 6, bi);
+            for (int u = 0; u < nb; ++u) {
+              const int gr = (pw.seq + j0 + u) & 1;
+              tc_commit(&empty_a[2 * is + gr]);
+              tc_commit(&acc_full[2 * is + gr]);
+              par ^= 1u << gr;
+            }
           }
-          if (!ok) break;
-          tc_commit(&empty_l[ls]);
-          seq += g;
+          pw.next_stage(g);
           if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
       }
@@ -296,31 +322,36 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
   } else if (warp < kSEpi0) {
     // ------------------------------------------------------------ dequant warps
     // Group grp restores the blocks with sequence index % 2 == grp; its warp for TMEM lane
-    // quarter warp % 4 handles weight rows 32*(warp % 4) .. +31, one row per thread. The row's
-    // group scale goes to meta[bi % MT] (published through meta_full) for the epilogue.
+    // quarter warp % 4 handles weight rows 32*(warp % 4) .. +31, one row per thread. A block goes
+    // to the slot of its pair's issuer; the row's group scale goes to that slot's scale entry for
+    // the use parity (published through meta_full) for the epilogue.
     const int dw = warp - kSDq0;
     const int grp = dw / kSDqGroup;
     const int r = 32 * (warp & 3) + lane;
+    uint32_t par = 0u;   // bit i: parity of the number of uses of slot (issuer i, grp) so far
     int ls = 0;
     uint32_t lph = 0;
-    int seq = 0;
+    PairWalk pw;
     bool first_dq = true;
     Segment seg;
     bool ok = true;
     while (ok && sched.next(seg)) {
       for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
         const int g = min(S::kG, seg.kb1 - kb0);
-        const int j0 = ((seq & 1) == grp) ? 0 : 1;
-        // Every group waits for the stage to fill, even one with no block in it (see the issuers).
+        const int j0 = ((pw.seq & 1) == grp) ? 0 : 1;
+        // Every group waits for the stage to fill, even one with no block in it: its release must
+        // not reach the slot's empty barrier before the slot's previous use is over.
         if (!mbar_wait(&full_w[ls], lph, wc)) { ok = false; break; }
         if (j0 >= g) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_l[ls]);
         }
         for (int jb = j0; jb < g; jb += 2) {
-          const int bi = seq + jb;
-          const int as = bi % SA;
-          if (!mbar_wait(&empty_a[as], (static_cast<uint32_t>(bi / SA) & 1u) ^ 1u, wc)) { ok = false; break; }
+          const int bi = pw.seq + jb;
+          const int iss = pw.pair_of(jb) % NI;
+          const int sl = 2 * iss + grp;
+          const uint32_t u = (par >> iss) & 1u;
+          if (!mbar_wait(&empty_a[sl], u ^ 1u, wc)) { ok = false; break; }
           if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
           if (dw % kSDqGroup == 0 && lane == 0) trace_stage(p.trace, 1, bi);
           const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
@@ -336,9 +367,9 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
             z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
           }
           const uint32_t z2 = bf16x2_bits(int4_zero_pair(z));
-          meta[(bi % MT) * 128 + r] = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+          meta[(sl * 2 + u) * 128 + r] = __uint_as_float(static_cast<uint32_t>(sb) << 16);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&meta_full[bi % MT]);
+          if (lane == 0) mbar_arrive(&meta_full[2 * sl + u]);
           if (jb + 2 >= g) {   // the stage's last block of this group is in registers: release it
             if (lane == 0) mbar_arrive(&empty_l[ls]);
           }
@@ -357,16 +388,17 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
                 for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
               }
             }
-            tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32,
+            tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + sl * 64 + half * 32,
                       a_regs);
           }
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (dw % kSDqGroup == 0 && lane == 0) trace_stage(p.trace, 2, bi);
-          if (lane == 0) mbar_arrive(&full_a[as]);
+          if (lane == 0) mbar_arrive(&full_a[sl]);
+          par ^= 1u << iss;
         }
-        seq += g;
+        pw.next_stage(g);
         if (++ls == SL) { ls = 0; lph ^= 1u; }
       }
     }
@@ -374,12 +406,16 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
     // ------------------------------------------------------------ epilogue warps
     // Drain each block's accumulator as soon as its MMAs complete, scale it by the row's group
     // scale and add it to the segment's running fp32 sum (k order); store the segment at its end.
+    // After a stage's last block, release the stage (its activation tile was read by the MMAs).
     pdl_wait();                          // Y, partials and counters may be in use by the previous kernel
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;
     const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    int seq = 0;
+    uint32_t par = 0u;        // bit sl: parity of the number of uses of slot sl so far
+    uint32_t uses_meta = 0u;  // bit sl: parity of the number of uses of meta_full[sl][u] (every other use)
+    int ls = 0;
+    PairWalk pw;
     bool first_seg = true;
     bool ok = true;
     Segment seg;
@@ -387,24 +423,37 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
       float acc[BT];
 #pragma unroll
       for (int j = 0; j < BT; ++j) acc[j] = 0.f;
-      for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++seq) {
-        const int ra = seq % RA;
-        if (!mbar_wait(&acc_full[ra], static_cast<uint32_t>(seq / RA) & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        if (row == 0 && first_seg && kb == seg.kb0) trace_mark(p.trace, 8);
-        uint32_t v[BT];
+      for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+        const int g = min(S::kG, seg.kb1 - kb0);
+        for (int j = 0; j < g; ++j) {
+          const int bi = pw.seq + j;
+          const int sl = 2 * (pw.pair_of(j) % NI) + (bi & 1);
+          const uint32_t u = (par >> sl) & 1u;
+          if (!mbar_wait(&acc_full[sl], u, wc)) { ok = false; break; }
+          tc_fence_after();
+          if (row == 0 && first_seg && kb0 == seg.kb0 && j == 0) trace_mark(p.trace, 8);
+          if (row == 0) trace_stage(p.trace, 0, bi);
+          uint32_t v[BT];
 #pragma unroll
-        for (int j0 = 0; j0 < BT; j0 += 16)
-          tmem_ld16(tmem + lane_base + ra * BT + j0, *reinterpret_cast<uint32_t(*)[16]>(v + j0));
-        tmem_wait_ld();
-        const int mi = seq % MT;
-        if (!mbar_wait(&meta_full[mi], static_cast<uint32_t>(seq / MT) & 1u, wc)) { ok = false; break; }
-        const float s = meta[mi * 128 + row];
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ra]);
+          for (int j0 = 0; j0 < BT; j0 += 16)
+            tmem_ld16(tmem + lane_base + sl * BT + j0, *reinterpret_cast<uint32_t(*)[16]>(v + j0));
+          tmem_wait_ld();
+          // Scale entries and their barriers are kept per use parity: the dequant warps may write
+          // the slot's next scale before this one is read.
+          if (!mbar_wait(&meta_full[2 * sl + u], (uses_meta >> sl) & 1u, wc)) { ok = false; break; }
+          const float s = meta[(sl * 2 + u) * 128 + row];
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[sl]);
+          par ^= 1u << sl;
+          if (u) uses_meta ^= 1u << sl;   // both parity barriers of the slot have now been used once more
 #pragma unroll
-        for (int j = 0; j < BT; ++j) acc[j] = fmaf(s, __uint_as_float(v[j]), acc[j]);
+          for (int jj = 0; jj < BT; ++jj) acc[jj] = fmaf(s, __uint_as_float(v[jj]), acc[jj]);
+        }
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(&empty_l[ls]);
+        if (++ls == SL) ls = 0;
+        pw.next_stage(g);
       }
       if (!ok) break;
       const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
