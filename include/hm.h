@@ -101,9 +101,16 @@ hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const u
  * 256-byte aligned). Inputs (device): q [N][K/2] packed codes as above; scales [N][K/g];
  * zeros [N][K/128] one u4 value per byte (HM_W4A16_INT4 with has_zero, else NULL).
  * For HM_W4A4_NVFP4 the header records desc->tensor_scale as gW.
- * Layout (tiles of 128 rows; the order the GEMM kernels stream): see README of the packed
- * layout in DESIGN; INT4/MXFP4-W4A16 use 128x128 "units" holding interleaved nibbles plus
- * per-row scales (and zero-points); W4A8/W4A4 use row-major codes plus 512-byte scale atoms. */
+ * Layout: a 256-byte header (magic, fmt, N, K, padded N and K, has_zero, tensor scale, payload
+ * bytes), then the payload, N padded to 128 and K to 128 (W4A4: 256):
+ *  - INT4 and MXFP4-W4A16: 128x128 "units", n-tile major, each one contiguous block: 8192 bytes
+ *    of codes (code (r, kk) in the little-endian word at (kk/32)*2048 + r*16 + ((kk%32)/8)*4,
+ *    bits 4*((kk%8)/2) + 16*(kk%2)), then the per-row scales (INT4: 128 bf16; MXFP4: 128 x 4
+ *    E8M0) and, for INT4 with zero-points, 64 bytes of u4 zero-points (row r in the low nibble
+ *    of byte r/2 when r is even). Units are 8448 / 8512 / 8704 bytes.
+ *  - W4A8 / W4A4: codes row-major [N_pad][K_pad/2], then 512-byte scale atoms
+ *    [N_pad/128][K_pad/chunk] (chunk = 128 K for E8M0 per 32, 64 K for e4m3 per 16), the scale
+ *    of (row r, sub-block j) at byte (r%32)*16 + (r/32)*4 + j of its atom. */
 hm_status hm_transform(const hm_weight_desc* desc, const void* q, const void* scales,
                        const void* zeros, void* packed, void* stream);
 
