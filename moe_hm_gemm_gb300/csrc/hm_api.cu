@@ -155,11 +155,21 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.num_n_tiles = pad_n(n) / 128;
   p.kb_total = pad_k(fmt, k) / p.tile_k;
   p.tiles = p.num_m_tiles * p.num_n_tiles;
+  // Block-scaled formats run two CTAs per SM; with fewer than four waves of tiles they use
+  // stream-K so that every CTA gets the same share (a partial last wave would idle SMs).
+  // When there are fewer tiles than SMs and the token tile is wider than 16, twice the CTAs
+  // would split each tile among twice the contributors, and the stream-K partials (tile_m x 128
+  // fp32 each) cost more than the second issuer gains: one CTA per SM then.
+  const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int sk_env = env_int("HM_STREAM_K", -1);
-  p.stream_k = sk_env >= 0 ? (sk_env != 0) : (p.tiles < num_sms ? 1 : 0);
+  const bool sk_auto = block_scaled ? p.tiles < 4 * static_cast<int64_t>(num_sms) * kMxCtasPerSm
+                                    : p.tiles < num_sms;
+  p.stream_k = sk_env >= 0 ? (sk_env != 0) : (sk_auto ? 1 : 0);
+  const bool one_per_sm = !block_scaled || (p.stream_k && p.tiles < num_sms && p.tile_m > 16);
+  const int64_t ctas = static_cast<int64_t>(num_sms) * (one_per_sm ? 1 : kMxCtasPerSm);
   const int64_t total = p.tiles * p.kb_total;
   const int64_t units = p.stream_k ? total : p.tiles;
-  p.grid = static_cast<int>(units < num_sms ? units : num_sms);
+  p.grid = static_cast<int>(units < ctas ? units : ctas);
   if (p.grid < 1) p.grid = 1;
   return p;
 }
@@ -181,7 +191,8 @@ WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_a
   WsLayout w{};
   size_t off = 0;
   w.partial = off;
-  off += align_up(static_cast<size_t>(kMaxSmsForSizing) * 2 * widest * 128 * sizeof(float));
+  const size_t max_ctas = static_cast<size_t>(kMaxSmsForSizing) * ((fmt == kW4A8Mx || fmt == kW4A4Nv) ? kMxCtasPerSm : 1);
+  off += align_up(max_ctas * 2 * widest * 128 * sizeof(float));
   w.counters = off;
   off += align_up(static_cast<size_t>(max_tiles) * 4 * sizeof(uint32_t));
   w.act_q = w.act_s = w.act_g = w.act_amax = off;

@@ -16,8 +16,8 @@
 // scales, row r at byte (r%32)*16 + (r/32)*4) and moved to TMEM with
 // tcgen05.cp.32x128b.warpx4, which puts row r's four scales in lane r%32 (every 32-lane
 // group) of column r/32 of a 4-column slot; the MMA picks the byte with the scale-factor id
-// (1X) or uses all four (4X). Same persistent structure as the W4A16 kernel: warp 0 loads,
-// warp 1 issues MMAs (and the scale copies), warps 2-5 drain TMEM.
+// (1X) or uses all four (4X). Persistent, two CTAs per SM (see MxShape): warp 0 loads, warp 1
+// issues MMAs (and the scale copies), warps 2-5 drain TMEM.
 #include <cuda_bf16.h>
 
 #include "hm_device.cuh"
@@ -28,31 +28,42 @@
 namespace hm {
 namespace {
 
-constexpr int kThreads = 192;
+// Warps: 0 loads, 1 issues MMAs, 2-5 drain TMEM; W4A4 adds warp 6, which copies the eight
+// scale atoms of each 256-K block to TMEM (W4A8 has one copy per block, kept on the MMA thread).
+template <bool NV>
+constexpr int threads_of() { return NV ? 224 : 192; }
+constexpr int kSfWarp = 6;
 constexpr int kWTile = 128 * 128;  // weight stage: 128 rows x 128 bytes (swizzled)
 
+// Two CTAs share each SM (kMxCtasPerSm): each has its own MMA-issuing thread, which a single
+// thread per SM cannot keep up with at FP8/FP4 rates (it issues every scale copy and MMA and
+// stalls at its next shared-memory access until its MMAs are under way), and while one CTA
+// drains its accumulator the other keeps the tensor pipe busy. So each CTA takes half of the
+// shared memory and at most 256 TMEM columns with a single accumulator.
 template <int BT, bool NV>
 struct MxShape {
   static constexpr int kXStage = BT * 128;                          // 128 bytes of K per row
   static constexpr int kSfaBytes = NV ? 4 * kAtomBytes : kAtomBytes;  // per stage
   static constexpr int kSfbBytes = NV ? 4 * kAtomBytes : 0;
   static constexpr int kStageBytes = kWTile + kXStage + kSfaBytes + kSfbBytes;
-  static constexpr int kSL = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  static constexpr int kBudget = 108 * 1024;
+  static constexpr int kSL = kBudget / kStageBytes > 8 ? 8 : kBudget / kStageBytes;
   static constexpr int kWOff = 0;
   static constexpr int kXOff = kWOff + kSL * kWTile;
   static constexpr int kSfaOff = kXOff + kSL * kXStage;
   static constexpr int kSfbOff = kSfaOff + kSL * kSfaBytes;
   static constexpr int kUnitSfOff = kSfbOff + kSL * kSfbBytes;     // W4A8: atom of 1.0 scales
   static constexpr int kBarOff = kUnitSfOff + kAtomBytes;
-  static constexpr int kNumBars = 2 * kSL + 5;
+  static constexpr int kNumBars = 3 * kSL + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmem = 1024 + kMiscOff + 64;
-  // TMEM: accumulators [0, 2*BT), then scale-factor slots
+  // TMEM: accumulator [0, BT), then scale-factor slots
   static constexpr int kSfCols = NV ? kSL * 32 : kSL * 4 + 4;
-  static constexpr int kColsNeeded = 2 * BT + kSfCols;
+  static constexpr int kColsNeeded = BT + kSfCols;
   static constexpr uint32_t kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
-                                        : kColsNeeded <= 256 ? 256 : 512;
-  static_assert(kColsNeeded <= 512, "TMEM budget");
+                                        : 256;
+  static_assert(kColsNeeded <= 256, "TMEM budget: two CTAs per SM");
+  static_assert(kSmem <= 113 * 1024, "shared memory: two CTAs per SM");
   static_assert(kSL >= 2, "pipeline depth");
 };
 
@@ -65,7 +76,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 }
 
 template <int BT, bool NV>
-__global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_constant__ MxParams p) {
+__global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel(const __grid_constant__ MxParams p) {
   using S = MxShape<BT, NV>;
   constexpr int SL = S::kSL;
   extern __shared__ uint8_t smem_raw[];
@@ -74,9 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   uint64_t* full = bars;
   uint64_t* empty = bars + SL;
-  uint64_t* acc_full = bars + 2 * SL;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* sf_full = bars + 2 * SL;     // [stage] its scale factors are in TMEM (commit)
+  uint64_t* acc_full = sf_full + SL;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 4);
   float* gw_sh = reinterpret_cast<float*>(smem + S::kMiscOff + 8);
@@ -88,12 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
-    }
-    mbar_init(drain, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, NV ? 2 : 1);   // the MMA thread's (and W4A4's scale-copy thread's) last commits
     fence_barrier_init();
     *abort_flag = 0u;
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
@@ -105,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
   }
   if (!NV) {
     // unit activation scales (E8M0 127 = 1.0) for every row
-    for (int i = threadIdx.x; i < kAtomBytes / 4; i += kThreads)
+    for (int i = threadIdx.x; i < kAtomBytes / 4; i += threads_of<NV>())
       reinterpret_cast<uint32_t*>(smem + S::kUnitSfOff)[i] = 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
@@ -114,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
   if (threadIdx.x == 0) pdl_launch_dependents();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sf_col0 = 2 * BT;  // first scale-factor column
+  const uint32_t sf_col0 = BT;  // first scale-factor column
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   SchedIter sched;
   sched.init(p.sched, p.sched.num_tiles, blockIdx.x);
@@ -194,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per k-block: wait for the stage (W4A4: until its scale factors are in TMEM, which implies
+    // its operands have landed), copy its weight scales (W4A8), then its MMAs. W4A4's eight scale
+    // copies per block run on their own warp: a thread that issues tcgen05 work stalls at its
+    // next shared-memory access until that work is under way, so they would otherwise lengthen
+    // every k-block of this thread.
     if (lane == 0) {
       const uint32_t unit_sfb = tmem + sf_col0 + (NV ? 0 : SL * 4);
       if (!NV) tc_cp_32x128b_x4(unit_sfb, sdesc_sf(smem_u32(smem + S::kUnitSfOff)));
@@ -202,24 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
-        const uint32_t b = acc_i & 1u;
-        if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
+        if (!mbar_wait(acc_empty, (acc_i & 1u) ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t d = tmem + b * BT;
+        const uint32_t d = tmem;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-          if (!mbar_wait(&full[ls], ph, wc)) { ok = false; break; }
+          if (!mbar_wait(NV ? &sf_full[ls] : &full[ls], ph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t w_base = smem_u32(smem + S::kWOff + ls * kWTile);
           const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
-          const uint32_t sfa_base = smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes);
           if (NV) {
-            const uint32_t sfb_base = smem_u32(smem + S::kSfbOff + ls * S::kSfbBytes);
             const uint32_t slot = tmem + sf_col0 + ls * 32;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_cp_32x128b_x4(slot + 4 * j, sdesc_sf(sfa_base + j * kAtomBytes));
-              tc_cp_32x128b_x4(slot + 16 + 4 * j, sdesc_sf(sfb_base + j * kAtomBytes));
-            }
             constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
             }
           } else {
             const uint32_t slot = tmem + sf_col0 + ls * 4;
-            tc_cp_32x128b_x4(slot, sdesc_sf(sfa_base));
+            tc_cp_32x128b_x4(slot, sdesc_sf(smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes)));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, k, k);
@@ -242,14 +250,44 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
           if (++ls == SL) { ls = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[b]);
+        tc_commit(acc_full);
         ++acc_i;
       }
       tc_commit(drain);
       drain_wait(drain, 0, 1000000000ull);
     }
     __syncwarp();
-  } else {
+  } else if (NV && warp == kSfWarp) {
+    // ------------------------------------------------------------ scale-factor copies
+    // For every k-block in order: once the stage has landed, copy its scale atoms from shared
+    // memory to the stage's TMEM slot (tcgen05.cp.32x128b.warpx4 puts row r's four scales in lane
+    // r%32 of column r/32 of a 4-column slot) and commit to sf_full. A slot is rewritten only
+    // after the producer refilled its stage, i.e. after the MMAs that read it completed.
+    if (lane == 0) {
+      int ls = 0;
+      uint32_t ph = 0;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(&full[ls], ph, wc)) { ok = false; break; }
+          const uint32_t sfa_base = smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes);
+          const uint32_t sfb_base = smem_u32(smem + S::kSfbOff + ls * S::kSfbBytes);
+          const uint32_t slot = tmem + sf_col0 + ls * 32;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_32x128b_x4(slot + 4 * j, sdesc_sf(sfa_base + j * kAtomBytes));
+            tc_cp_32x128b_x4(slot + 16 + 4 * j, sdesc_sf(sfb_base + j * kAtomBytes));
+          }
+          tc_commit(&sf_full[ls]);
+          if (++ls == SL) { ls = 0; ph ^= 1u; }
+        }
+      }
+      tc_commit(drain);
+      drain_wait(drain, 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue warps (2..5)
     pdl_wait();   // Y, s_tok, partials and counters: wait for the previous kernel
     const int q = warp & 3;
@@ -260,8 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
     bool first_seg = true;
     Segment seg;
     while (sched.next(seg)) {
-      const uint32_t b = acc_i & 1u;
-      if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
+      if (!mbar_wait(acc_full, acc_i & 1u, wc)) break;
       tc_fence_after();
       const int nt = seg.tile % p.num_n_tiles;
       const int mt = seg.tile / p.num_n_tiles;
@@ -279,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
         c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
         have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
       }
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * BT;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
       float* slotp = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                      static_cast<size_t>(row) * BT;
 #pragma unroll 1
@@ -313,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gemm_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (lane == 0) mbar_arrive(acc_empty);
       ++acc_i;
       if (!full_seg && !owner) sk_publish(flag, lane);
       if (owner && have) {
@@ -345,7 +382,7 @@ cudaError_t launch_one(const MxParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  return launch_pdl(kern, p.sched.grid, kThreads, S::kSmem, st, p);
+  return launch_pdl(kern, p.sched.grid, threads_of<NV>(), S::kSmem, st, p);
 }
 
 template <bool NV>

@@ -86,6 +86,8 @@ cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream
 constexpr int f16_group_of(int tile_m) { return tile_m <= 32 ? 4 : (tile_m == 64 ? 2 : 1); }
 int f16_group(int tile_m);
 cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st);
+// The block-scaled kernel runs two CTAs per SM (the plan's grid counts CTAs, not SMs).
+constexpr int kMxCtasPerSm = 2;
 // Load stages of the W4A16 kernel that serves (fmt, tile_m).
 int f16_stages(int fmt, int tile_m);
 // Small-token INT4 kernel (tile_m 16 or 32; hm_gemm_f16s.cu), chosen by launch_f16_gemm unless
