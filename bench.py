@@ -51,6 +51,27 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
+def measured_traffic(workload, label):
+    """DRAM bytes per launch of the point's kernel from an ncu capture recorded under profiles/,
+    or None when there is none or the kernel's sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    entry = json.load(open(path))["points"].get(f"{workload}:{label}")
+    if entry is None:
+        return None
+    h = hashlib.sha256()
+    for f in entry["sources"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != entry["sources_sha256"]:
+        return None
+    return entry["read_bytes"] + entry["write_bytes"]
+
+
 # nominal dense ratios of the MMA kinds to kind::f16 (bf16): fp8 x2, fp4 x4
 KIND_RATIO = {"kind::f16": 1.0, "kind::mxf8f6f4": 2.0, "kind::mxf4nvf4": 4.0}
 
@@ -360,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         ach, peak, unit = dom.bytes / t / 1e9, pk["hbm"], "GB/s"
     roofline = {"bound": dom_bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
-                "frac": round(ach / peak, 4), "traffic": None, "kernel": dom.label,
+                "frac": round(ach / peak, 4), "traffic": measured_traffic(args.workload, dom.label), "kernel": dom.label,
                 "peak_source": f"{pk['source']} ({'bf16 sustained' if dom_bound == 'tensor' else 'hbm copy'}"
                                f"{' x nominal ' + str(KIND_RATIO[dom.kind]) + ' for ' + dom.kind if dom.kind != 'kind::f16' and dom_bound == 'tensor' else ''})"}
 
