@@ -487,9 +487,11 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   (void)ws_bytes;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
-  // Token tile from the mean rows per expert (per-expert counts stay on the device).
+  // Token tile from the mean rows per expert (per-expert counts stay on the device); past 256 rows
+  // per expert the 256-token tile's halved dequant work per FLOP outweighs its padding of the
+  // smaller experts (measured: T=16384, E=256, top-8 runs 20 % faster than with 128).
   const int64_t mean = rows / E;
-  int tile_m = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : 128));
+  int tile_m = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : (mean <= 256 ? 128 : 256)));
   const int forced = env_int("HM_MOE_TILE_M", 0);
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) tile_m = forced;
   F16Params prm;

@@ -28,10 +28,11 @@
 namespace hm {
 namespace {
 
-// Warps: 0 loads, 1 issues MMAs, 2-5 drain TMEM; W4A4 adds warp 6, which copies the eight
-// scale atoms of each 256-K block to TMEM (W4A8 has one copy per block, kept on the MMA thread).
+// Warps: 0 loads, 1 issues MMAs, 2-5 drain TMEM; W4A4 adds warps 6 and 7, which copy the four
+// weight and the four activation scale atoms of each 256-K block to TMEM (W4A8 has one copy per
+// block, kept on the MMA thread).
 template <bool NV>
-constexpr int threads_of() { return NV ? 224 : 192; }
+constexpr int threads_of() { return NV ? 256 : 192; }
 constexpr int kSfWarp = 6;
 constexpr int kWTile = 128 * 128;  // weight stage: 128 rows x 128 bytes (swizzled)
 
@@ -100,11 +101,11 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_full[s], NV ? 2 : 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
-    mbar_init(drain, NV ? 2 : 1);   // the MMA thread's (and W4A4's scale-copy thread's) last commits
+    mbar_init(drain, NV ? 3 : 1);   // the MMA thread's (and W4A4's scale-copy threads') last commits
     fence_barrier_init();
     *abort_flag = 0u;
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
@@ -257,13 +258,14 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
       drain_wait(drain, 0, 1000000000ull);
     }
     __syncwarp();
-  } else if (NV && warp == kSfWarp) {
+  } else if (NV && (warp == kSfWarp || warp == kSfWarp + 1)) {
     // ------------------------------------------------------------ scale-factor copies
     // For every k-block in order: once the stage has landed, copy its scale atoms from shared
     // memory to the stage's TMEM slot (tcgen05.cp.32x128b.warpx4 puts row r's four scales in lane
     // r%32 of column r/32 of a 4-column slot) and commit to sf_full. A slot is rewritten only
     // after the producer refilled its stage, i.e. after the MMAs that read it completed.
     if (lane == 0) {
+      const bool act = warp == kSfWarp + 1;   // warp 6: weight scales, warp 7: activation scales
       int ls = 0;
       uint32_t ph = 0;
       Segment seg;
@@ -271,14 +273,11 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
       while (ok && sched.next(seg)) {
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!mbar_wait(&full[ls], ph, wc)) { ok = false; break; }
-          const uint32_t sfa_base = smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes);
-          const uint32_t sfb_base = smem_u32(smem + S::kSfbOff + ls * S::kSfbBytes);
-          const uint32_t slot = tmem + sf_col0 + ls * 32;
+          const uint32_t src = act ? smem_u32(smem + S::kSfbOff + ls * S::kSfbBytes)
+                                   : smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes);
+          const uint32_t slot = tmem + sf_col0 + ls * 32 + (act ? 16 : 0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_x4(slot + 4 * j, sdesc_sf(sfa_base + j * kAtomBytes));
-            tc_cp_32x128b_x4(slot + 16 + 4 * j, sdesc_sf(sfb_base + j * kAtomBytes));
-          }
+          for (int j = 0; j < 4; ++j) tc_cp_32x128b_x4(slot + 4 * j, sdesc_sf(src + j * kAtomBytes));
           tc_commit(&sf_full[ls]);
           if (++ls == SL) { ls = 0; ph ^= 1u; }
         }

@@ -83,3 +83,12 @@ def test_small_tiles_both_kernels(hm, small, monkeypatch):
     moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=True, seed=11)
     monkeypatch.setenv("HM_MOE_TILE_M", "32")
     moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=False, seed=12)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("tile", ["64", "128", "256"])
+def test_forced_token_tiles(hm, fmt, tile, monkeypatch):
+    """Every token tile of the grouped path, including the 256-row tile with restored weights in
+    shared memory, on skewed counts with empty experts and experts larger than the tile."""
+    monkeypatch.setenv("HM_MOE_TILE_M", tile)
+    moe_case(hm, fmt, [300, 0, 1, 17, 0, 129, 256, 3], 256, 512, has_zero=(fmt == 1), seed=21)
