@@ -72,8 +72,9 @@ def measured_traffic(workload, label):
     return entry["read_bytes"] + entry["write_bytes"]
 
 
-# nominal dense ratios of the MMA kinds to kind::f16 (bf16): fp8 x2, fp4 x4
-KIND_RATIO = {"kind::f16": 1.0, "kind::mxf8f6f4": 2.0, "kind::mxf4nvf4": 4.0}
+# nominal dense ratios of the MMA kinds to kind::f16 (bf16) on GB300: 2.25 (bf16), 4.5 (fp8) and
+# 13.5 (fp4) PFLOP/s dense, i.e. fp8 x2 and fp4 x6
+KIND_RATIO = {"kind::f16": 1.0, "kind::mxf8f6f4": 2.0, "kind::mxf4nvf4": 6.0}
 
 
 class Clocks:

@@ -12,16 +12,21 @@
 // Design (GB300-first; the pages give no kernel design):
 //  * weights are the MMA's A operand (M = 128 weight rows), tokens its B operand (N =
 //    tile_m in 16..256), so even M = 1 fills the 128-row side of the tensor core;
-//  * one persistent CTA per SM, 10 warps: warp 0 issues the TMA loads (one bulk copy of a
-//    packed 128x128 unit with its scales, two 2-D tensor loads of the X tile), warp 1 owns
-//    TMEM and issues tcgen05.mma from one thread, warps 2-5 restore the unit to bf16 into the
-//    128-byte-swizzled K-major layout the MMA reads, warps 6-9 drain TMEM (tcgen05.ld), round
-//    to bf16 and store Y;
-//  * the accumulator is double-buffered in TMEM so the epilogue of one tile overlaps the
-//    main loop of the next;
-//  * small M uses stream-K (see hm_sched.cuh) so that every SM streams weights; partial tiles
-//    are summed in k order by the last CTA to finish (deterministic, no spinning);
-//  * every wait is bounded (hm_device.cuh).
+//  * one persistent CTA per SM, 15 warps: warp 0 issues the TMA loads (one bulk copy of g
+//    contiguous packed 128x128 units with their scales, and the matching X tile), warps 1-2
+//    issue tcgen05.mma (two issuers with separate accumulators for tile_m <= 64, warp 1 also
+//    owns TMEM), warps 3-10 restore the weights to bf16 (two groups taking alternate 128-K
+//    blocks) into TMEM (tile_m <= 128, the MMA reads A from TMEM) or into the 128-byte-swizzled
+//    K-major shared layout (tile_m = 256), warps 11-14 drain TMEM (tcgen05.ld), round to bf16
+//    and store Y;
+//  * INT4 with tile_m 16 or 32 runs the small-token kernel instead (hm_gemm_f16s.cu);
+//  * accumulators are double-buffered in TMEM so the epilogue of one tile overlaps the main
+//    loop of the next;
+//  * small M uses stream-K (hm_sched.cuh) so that every SM streams weights; the CTA holding a
+//    tile's first k-block sums the other CTAs' published partials in k order (deterministic;
+//    no contributor waits);
+//  * programmatic dependent launch: the first weight stages stream before the wait for the
+//    previous kernel; every wait is bounded (hm_device.cuh).
 #include <cuda_bf16.h>
 
 #include <cstdlib>

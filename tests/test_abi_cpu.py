@@ -98,3 +98,32 @@ def test_status_strings(hm):
     assert lib.hm_status_string(0) == b"ok"
     assert b"workspace" in lib.hm_status_string(3)
     assert hm.version().startswith("hm ")
+
+
+def test_plan_block_scaled_two_ctas_per_sm(hm):
+    """W4A8/W4A4 run two CTAs per SM: tile-parallel from four waves of tiles up, stream-K below
+    (balanced CTAs), and one CTA per SM when tiles are fewer than SMs with tiles wider than 16."""
+    for fmt in (3, 4):
+        big = hm.plan(fmt, 8192, 8192, 8192, 152)          # 64 x 64 tiles
+        assert big["stream_k"] == 0 and big["grid"] == 2 * 152 and big["tile_m"] == 128
+        mid = hm.plan(fmt, 1024, 8192, 8192, 152)          # 8 x 64 = 512 tiles < 4 waves
+        assert mid["stream_k"] == 1 and mid["grid"] == 2 * 152
+        few = hm.plan(fmt, 128, 8192, 8192, 152)           # 64 tiles of 128 tokens < 152 SMs
+        assert few["stream_k"] == 1 and few["grid"] == 152
+        tiny = hm.plan(fmt, 16, 8192, 8192, 152)           # 64 tiles of 16 tokens
+        assert tiny["stream_k"] == 1 and tiny["grid"] == 2 * 152 and tiny["tile_m"] == 16
+    # W4A16 keeps one CTA per SM
+    assert hm.plan(1, 8192, 8192, 8192, 152)["grid"] == 152
+    # stream-K partials are sized for the widest grid the planner can choose
+    assert hm.workspace_size(3, 16, 8192, 8192) >= 2 * 256 * 2 * 16 * 128 * 4
+
+
+def test_plan_small_token_stages(hm):
+    """INT4 token tiles 16/32 report the small-token kernel's load stages; HM_F16_SMALL=0 the general kernel's."""
+    a = hm.plan(1, 8, 4096, 4096, 152)["stages"]
+    os.environ["HM_F16_SMALL"] = "0"
+    try:
+        b = hm.plan(1, 8, 4096, 4096, 152)["stages"]
+    finally:
+        del os.environ["HM_F16_SMALL"]
+    assert a >= 3 and b >= 2
