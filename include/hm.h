@@ -40,7 +40,8 @@ extern "C" {
 typedef enum hm_status {
   HM_OK = 0,
   HM_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad offsets length */
-  HM_ERR_UNSUPPORTED = 2,   /* format/shape combination not implemented */
+  HM_ERR_UNSUPPORTED = 2,   /* format/shape combination not implemented, or a problem whose
+                               (tile, 128-K block) space has 2^31 or more iterations */
   HM_ERR_WORKSPACE = 3,     /* workspace smaller than hm_workspace_size() */
   HM_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
   HM_ERR_DEVICE = 5         /* device error word was set (see hm_get_device_error) */

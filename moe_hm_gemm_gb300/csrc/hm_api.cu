@@ -174,6 +174,9 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   return p;
 }
 
+// The kernels walk the (tile, k-block) space in 32-bit indices.
+bool plan_fits(const Plan& p) { return p.tiles * p.kb_total < (int64_t{1} << 31); }
+
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -365,6 +368,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
       num_sms > kMaxSmsForSizing)
     return HM_ERR_INVALID_ARG;
   const Plan p = make_plan(fmt, M, N, K, num_sms);
+  if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   out->bucket = p.bucket;
   out->tile_m = p.tile_m;
   out->tile_n = 128;
@@ -391,6 +395,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (!device_info(&di)) return HM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
   if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
@@ -487,6 +492,8 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   (void)ws_bytes;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
+  // The device-side tile count is at most ceil(rows/16) + E tiles of 16 per n-tile.
+  if ((rows / 16 + 1 + E) * (pad_n(N) / 128) * (K / 128) >= (int64_t{1} << 31)) return HM_ERR_UNSUPPORTED;
   // Token tile from the mean rows per expert (per-expert counts stay on the device); past 256 rows
   // per expert the 256-token tile's halved dequant work per FLOP outweighs its padding of the
   // smaller experts (measured: T=16384, E=256, top-8 runs 20 % faster than with 128).
@@ -524,6 +531,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   uint8_t* scratch = noalloc_scratch(di.dev);
   if (scratch == nullptr) return HM_ERR_CUDA;
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   // Partials for the CTAs of this launch, then the per-tile arrival counters.
   const size_t partial_bytes = align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float));
   const size_t counter_bytes = align_up(static_cast<size_t>(p.tiles) * 4 * sizeof(uint32_t));

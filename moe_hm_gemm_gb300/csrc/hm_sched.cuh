@@ -40,8 +40,12 @@ struct Segment {
   int32_t kb1;
 };
 
+// Cursor over a CTA's segments. The (tile, k-block) space has fewer than 2^31 iterations (the
+// API bounds M, N and K), so the per-segment steps divide in 32 bits; only the range ends, whose
+// products c * total can exceed 2^31, are computed in 64 bits, once. (A 64-bit division is a
+// long instruction sequence, and every role walks the schedule at start-up.)
 struct SchedIter {
-  int64_t it, it_end;     // stream-K cursor
+  int32_t it, it_end;     // stream-K cursor
   int32_t next_tile;      // tile-parallel cursor
   int32_t stride;
   int32_t num_tiles;
@@ -54,18 +58,23 @@ struct SchedIter {
     stream_k = s.stream_k != 0;
     stride = s.grid;
     next_tile = b;
-    const int64_t total = static_cast<int64_t>(num_tiles) * kb_total;
-    it = sk_start(b, total, s.grid);
-    it_end = sk_start(b + 1, total, s.grid);
+    if (stream_k) {
+      const int64_t total = static_cast<int64_t>(num_tiles) * kb_total;
+      it = static_cast<int32_t>(sk_start(b, total, s.grid));
+      it_end = static_cast<int32_t>(sk_start(b + 1, total, s.grid));
+    } else {
+      it = it_end = 0;
+    }
   }
 
   __device__ __forceinline__ bool next(Segment& seg) {
     if (stream_k) {
       if (it >= it_end) return false;
-      seg.tile = static_cast<int32_t>(it / kb_total);
-      seg.kb0 = static_cast<int32_t>(it % kb_total);
-      const int64_t left = it_end - it;
-      seg.kb1 = static_cast<int32_t>(seg.kb0 + left < kb_total ? seg.kb0 + left : kb_total);
+      const uint32_t q = static_cast<uint32_t>(it) / static_cast<uint32_t>(kb_total);
+      seg.tile = static_cast<int32_t>(q);
+      seg.kb0 = it - static_cast<int32_t>(q) * kb_total;
+      const int32_t left = it_end - it;
+      seg.kb1 = seg.kb0 + left < kb_total ? seg.kb0 + left : kb_total;
       it += seg.kb1 - seg.kb0;
       return true;
     }

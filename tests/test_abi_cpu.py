@@ -127,3 +127,11 @@ def test_plan_small_token_stages(hm):
     finally:
         del os.environ["HM_F16_SMALL"]
     assert a >= 3 and b >= 2
+
+
+def test_oversized_schedule_rejected(hm):
+    """Problems whose (tile, k-block) space reaches 2^31 iterations are refused before any launch
+    (the kernels index it in 32 bits)."""
+    with pytest.raises(hm.HmError) as e:
+        hm.plan(1, 1 << 22, 1 << 20, 1 << 16, 152)
+    assert e.value.status == 2
