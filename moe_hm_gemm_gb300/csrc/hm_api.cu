@@ -141,8 +141,10 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
   if (m <= 32) return 32;
   if (m <= 64) return 64;
   if (m <= 128 || block_scaled) return 128;
+  // The 256-token tile halves the dequant work and X traffic per FLOP; it wins (measured on
+  // 4096x4096, 14336x4096, 4096x14336) once its tiles cover about 70 % of the SMs.
   const int64_t n_tiles = pad_n(n) / 128;
-  return ceil_div(m, 256) * n_tiles >= num_sms ? 256 : 128;
+  return ceil_div(m, 256) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 7 ? 256 : 128;
 }
 
 Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
@@ -162,8 +164,12 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   // fp32 each) cost more than the second issuer gains: one CTA per SM then.
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int sk_env = env_int("HM_STREAM_K", -1);
-  const bool sk_auto = block_scaled ? p.tiles < 4 * static_cast<int64_t>(num_sms) * kMxCtasPerSm
-                                    : p.tiles < num_sms;
+  // W4A16 with tiles of 128 or 256 tokens: stream-K pays for its partial hand-offs only when a
+  // tile's whole K loop is much longer than the balanced share (measured break-even about 30
+  // k-blocks); token tiles up to 64 always split.
+  const int64_t share = ceil_div(p.tiles * p.kb_total, num_sms);
+  const bool sk_f16 = p.tiles < num_sms && (p.tile_m <= 64 || p.kb_total > share + 30);
+  const bool sk_auto = block_scaled ? p.tiles < 4 * static_cast<int64_t>(num_sms) * kMxCtasPerSm : sk_f16;
   p.stream_k = sk_env >= 0 ? (sk_env != 0) : (sk_auto ? 1 : 0);
   const bool one_per_sm = !block_scaled || (p.stream_k && p.tiles < num_sms && p.tile_m > 16);
   const int64_t ctas = static_cast<int64_t>(num_sms) * (one_per_sm ? 1 : kMxCtasPerSm);

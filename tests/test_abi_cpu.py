@@ -79,7 +79,11 @@ def test_plan_buckets(hm):
     assert [seen[m]["bucket"] for m in (1, 16, 17, 64, 65, 256, 257, 1024, 1025)] == [0, 0, 1, 1, 2, 2, 3, 3, 4]
     assert seen[1]["stream_k"] == 1 and seen[1]["grid"] == 152   # 32 tiles < 152 SMs
     assert seen[8192]["stream_k"] == 0 and seen[8192]["tile_m"] == 256 and seen[8192]["tiles"] == 32 * 32
-    assert seen[1024]["tile_m"] == 128 and seen[1024]["stream_k"] == 0   # 256 would leave SMs idle
+    assert seen[1024]["tile_m"] == 256 and seen[1024]["stream_k"] == 0   # 128 tiles cover 84 % of the SMs
+    assert seen[256]["tile_m"] == 128 and seen[256]["stream_k"] == 0     # short K: no split
+    # long K: stream-K; wide N: the 256-token tile from M = 256 on
+    assert hm.plan(1, 128, 4096, 14336, 152)["stream_k"] == 1
+    assert hm.plan(1, 256, 14336, 4096, 152)["tile_m"] == 256
     # every stream-K CTA gets at least one k-block
     p = hm.plan(1, 1, 128, 256, 152)
     assert p["grid"] == 2
