@@ -130,6 +130,24 @@ int bucket_of(int64_t m) {
 // gives every SM a tile. The block-scaled kernels stop at 128 (TMEM also holds their scale
 // factors), and a W4A4 tile narrower than 128 must cover all of M (its activation scale atoms
 // hold 128 rows).
+// Block-scaled formats above 16 tokens (measured on the W4A8 7168x7168 / 18432x7168 and W4A4
+// 8192x8192 layers, M = 32..1024): run tile-parallel with the widest token tile whose tiles fill
+// 1.4x the SMs (two CTAs per SM take them); if even 32-token tiles give fewer, run them
+// tile-parallel when they still cover 0.9x the SMs, else stream-K. A W4A4 tile narrower than 128
+// must cover all of M (its activation scale atoms hold 128 rows), so W4A4 keeps 128, tile-parallel.
+struct MxChoice {
+  int tile_m;
+  bool stream_k;
+};
+MxChoice mx_choice(int32_t fmt, int64_t m, int64_t n, int num_sms) {
+  if (m <= 16) return {16, true};
+  if (fmt == kW4A4Nv) return {128, false};
+  const int64_t n_tiles = pad_n(n) / 128;
+  for (int t : {128, 64, 32})
+    if (ceil_div(m, t) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 14) return {t, false};
+  return {32, ceil_div(m, 32) * n_tiles * 10 < static_cast<int64_t>(num_sms) * 9};
+}
+
 int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
@@ -137,10 +155,11 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
     if (fmt == kW4A4Nv && forced < 128 && m > forced) return 128;
     return forced;
   }
+  if (block_scaled) return mx_choice(fmt, m, n, num_sms).tile_m;
   if (m <= 16) return 16;
   if (m <= 32) return 32;
   if (m <= 64) return 64;
-  if (m <= 128 || block_scaled) return 128;
+  if (m <= 128) return 128;
   // The 256-token tile halves the dequant work and X traffic per FLOP; it wins (measured on
   // 4096x4096, 14336x4096, 4096x14336) once its tiles cover about 70 % of the SMs.
   const int64_t n_tiles = pad_n(n) / 128;
@@ -157,11 +176,10 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.num_n_tiles = pad_n(n) / 128;
   p.kb_total = pad_k(fmt, k) / p.tile_k;
   p.tiles = p.num_m_tiles * p.num_n_tiles;
-  // Block-scaled formats run two CTAs per SM; with fewer than four waves of tiles they use
-  // stream-K so that every CTA gets the same share (a partial last wave would idle SMs).
-  // When there are fewer tiles than SMs and the token tile is wider than 16, twice the CTAs
-  // would split each tile among twice the contributors, and the stream-K partials (tile_m x 128
-  // fp32 each) cost more than the second issuer gains: one CTA per SM then.
+  // Block-scaled formats run two CTAs per SM, stream-K as mx_choice says. With stream-K over
+  // fewer tiles than SMs and tiles wider than 16 tokens, twice the CTAs would split each tile
+  // among twice the contributors, and the partials (tile_m x 128 fp32 each) cost more than the
+  // second issuer gains: one CTA per SM then.
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int sk_env = env_int("HM_STREAM_K", -1);
   // W4A16 with tiles of 128 or 256 tokens: stream-K pays for its partial hand-offs only when a
@@ -169,9 +187,14 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   // k-blocks); token tiles up to 64 always split.
   const int64_t share = ceil_div(p.tiles * p.kb_total, num_sms);
   const bool sk_f16 = p.tiles < num_sms && (p.tile_m <= 64 || p.kb_total > share + 30);
-  const bool sk_auto = block_scaled ? p.tiles < 4 * static_cast<int64_t>(num_sms) * kMxCtasPerSm : sk_f16;
+  const bool sk_auto = block_scaled ? (p.tile_m == mx_choice(fmt, m, n, num_sms).tile_m
+                                         ? mx_choice(fmt, m, n, num_sms).stream_k
+                                         : p.tiles < num_sms)
+                                    : sk_f16;
   p.stream_k = sk_env >= 0 ? (sk_env != 0) : (sk_auto ? 1 : 0);
-  const bool one_per_sm = !block_scaled || (p.stream_k && p.tiles < num_sms && p.tile_m > 16);
+  const int ctas_env = env_int("HM_MX_CTAS_PER_SM", 0);
+  const bool one_per_sm = !block_scaled || (ctas_env == 1) ||
+                          (ctas_env != 2 && p.stream_k && p.tiles < num_sms && p.tile_m > 16);
   const int64_t ctas = static_cast<int64_t>(num_sms) * (one_per_sm ? 1 : kMxCtasPerSm);
   const int64_t total = p.tiles * p.kb_total;
   const int64_t units = p.stream_k ? total : p.tiles;

@@ -110,12 +110,19 @@ def test_plan_block_scaled_two_ctas_per_sm(hm):
     for fmt in (3, 4):
         big = hm.plan(fmt, 8192, 8192, 8192, 152)          # 64 x 64 tiles
         assert big["stream_k"] == 0 and big["grid"] == 2 * 152 and big["tile_m"] == 128
-        mid = hm.plan(fmt, 1024, 8192, 8192, 152)          # 8 x 64 = 512 tiles < 4 waves
-        assert mid["stream_k"] == 1 and mid["grid"] == 2 * 152
-        few = hm.plan(fmt, 128, 8192, 8192, 152)           # 64 tiles of 128 tokens < 152 SMs
-        assert few["stream_k"] == 1 and few["grid"] == 152
-        tiny = hm.plan(fmt, 16, 8192, 8192, 152)           # 64 tiles of 16 tokens
+        mid = hm.plan(fmt, 1024, 8192, 8192, 152)          # 8 x 64 = 512 tiles: tile-parallel
+        assert mid["stream_k"] == 0 and mid["grid"] == 2 * 152
+        tiny = hm.plan(fmt, 16, 8192, 8192, 152)           # 64 tiles of 16 tokens: stream-K
         assert tiny["stream_k"] == 1 and tiny["grid"] == 2 * 152 and tiny["tile_m"] == 16
+    # W4A8 at M = 128: the widest tile giving >= 1.4x SMs tiles (32 tokens: 4 x 64 = 256 tiles)
+    p = hm.plan(3, 128, 8192, 8192, 152)
+    assert p["tile_m"] == 32 and p["stream_k"] == 0 and p["grid"] == 256
+    # W4A4 keeps 128-token tiles (its activation scale atoms hold 128 rows), tile-parallel
+    p = hm.plan(4, 128, 8192, 8192, 152)
+    assert p["tile_m"] == 128 and p["stream_k"] == 0 and p["grid"] == 64
+    # too few tiles even at 32 tokens: stream-K, one CTA per SM
+    p = hm.plan(3, 64, 7168, 7168, 152)
+    assert p["tile_m"] == 32 and p["stream_k"] == 1 and p["grid"] == 152
     # W4A16 keeps one CTA per SM
     assert hm.plan(1, 8192, 8192, 8192, 152)["grid"] == 152
     # stream-K partials are sized for the widest grid the planner can choose
