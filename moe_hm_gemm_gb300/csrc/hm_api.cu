@@ -148,7 +148,35 @@ MxChoice mx_choice(int32_t fmt, int64_t m, int64_t n, int num_sms) {
   return {32, ceil_div(m, 32) * n_tiles * 10 < static_cast<int64_t>(num_sms) * 9};
 }
 
-int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
+// INT4 W4A16 for 16 < M <= 512: pick (token tile, stream-K) by a cost model fitted to measured
+// times on the 4096x4096, 14336x4096 and 4096x14336 layers (within ~10 %): time ~ 5 us + blocks
+// per CTA x c(tile), where a 128-K block costs c = 0.47 / 0.55 / 0.85 / 1.3 us for tiles of
+// 32 / 64 / 128 / 256 tokens, a tile-parallel CTA runs ceil(tiles / SMs) x kb blocks, and a
+// stream-K CTA runs ceil(tiles x kb / SMs) blocks plus a hand-off cost of 15 / 18 / 35 / 60
+// blocks. Narrow tiles stream weights faster per block; wide tiles do more tokens per block.
+struct F16Choice {
+  int tile_m;
+  bool stream_k;
+};
+F16Choice f16_choice(int64_t m, int64_t n, int64_t k, int num_sms) {
+  const int64_t n_tiles = pad_n(n) / 128, kb = k / 128;
+  const int tiles_m[4] = {32, 64, 128, 256};
+  const double cost[4] = {0.47, 0.55, 0.85, 1.3}, handoff[4] = {15, 18, 35, 60};
+  F16Choice best{32, true};
+  double best_t = 1e30;
+  for (int i = 0; i < 4; ++i) {
+    const int t = tiles_m[i];
+    if (t > 32 && t / 2 >= m) continue;   // no wider than the next power of two covering M
+    const int64_t tiles = ceil_div(m, t) * n_tiles;
+    const double tp = static_cast<double>(ceil_div(tiles, num_sms) * kb) * cost[i];
+    const double sk = (static_cast<double>(ceil_div(tiles * kb, num_sms)) + handoff[i]) * cost[i];
+    if (tp < best_t) { best_t = tp; best = {t, false}; }
+    if (sk < best_t) { best_t = sk; best = {t, true}; }
+  }
+  return best;
+}
+
+int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !block_scaled)) {
@@ -156,6 +184,7 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
     return forced;
   }
   if (block_scaled) return mx_choice(fmt, m, n, num_sms).tile_m;
+  if (fmt == kW4A16Int4 && m > 16 && m <= 512 && k > 0) return f16_choice(m, n, k, num_sms).tile_m;
   if (m <= 16) return 16;
   if (m <= 32) return 32;
   if (m <= 64) return 64;
@@ -169,7 +198,7 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms) {
 Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   Plan p{};
   p.bucket = bucket_of(m);
-  p.tile_m = tile_m_for(fmt, m, n, num_sms);
+  p.tile_m = tile_m_for(fmt, m, n, num_sms, k);
   p.tile_k = fmt == kW4A4Nv ? 256 : 128;
   p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(fmt, p.tile_m) : mx_stages(fmt, p.tile_m);
   p.num_m_tiles = ceil_div(m > 0 ? m : 1, p.tile_m);
@@ -186,7 +215,9 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   // tile's whole K loop is much longer than the balanced share (measured break-even about 30
   // k-blocks); token tiles up to 64 always split.
   const int64_t share = ceil_div(p.tiles * p.kb_total, num_sms);
-  const bool sk_f16 = p.tiles < num_sms && (p.tile_m <= 64 || p.kb_total > share + 30);
+  const bool modelled = fmt == kW4A16Int4 && m > 16 && m <= 512 && p.tile_m == f16_choice(m, n, k, num_sms).tile_m;
+  const bool sk_f16 = modelled ? f16_choice(m, n, k, num_sms).stream_k
+                               : p.tiles < num_sms && (p.tile_m <= 64 || p.kb_total > share + 30);
   const bool sk_auto = block_scaled ? (p.tile_m == mx_choice(fmt, m, n, num_sms).tile_m
                                          ? mx_choice(fmt, m, n, num_sms).stream_k
                                          : p.tiles < num_sms)
@@ -217,7 +248,12 @@ struct WsLayout {
 // widest token tile and the counters for the most tiles the planner can choose for this M.
 WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_act) {
   int widest = tile_m_for(fmt, m, n, 1);          // one SM: the widest choice
-  const int narrowest = tile_m_for(fmt, m, n, 1 << 30);
+  int narrowest = tile_m_for(fmt, m, n, 1 << 30);
+  if (fmt == kW4A16Int4 && m > 16 && m <= 512) {  // f16_choice may pick any tile from 32 up to the cover
+    narrowest = 32;
+    const int cover = m > 128 ? 256 : (m > 64 ? 128 : (m > 32 ? 64 : 32));
+    if (cover > widest) widest = cover;
+  }
   if (narrowest > widest) widest = narrowest;
   const int64_t max_tiles = ceil_div(m > 0 ? m : 1, narrowest < widest ? narrowest : widest) * (pad_n(n) / 128);
   WsLayout w{};

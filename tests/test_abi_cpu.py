@@ -80,10 +80,16 @@ def test_plan_buckets(hm):
     assert seen[1]["stream_k"] == 1 and seen[1]["grid"] == 152   # 32 tiles < 152 SMs
     assert seen[8192]["stream_k"] == 0 and seen[8192]["tile_m"] == 256 and seen[8192]["tiles"] == 32 * 32
     assert seen[1024]["tile_m"] == 256 and seen[1024]["stream_k"] == 0   # 128 tiles cover 84 % of the SMs
-    assert seen[256]["tile_m"] == 128 and seen[256]["stream_k"] == 0     # short K: no split
+    # 16 < M <= 512 (INT4): the cost model picks the measured-best (tile, stream-K) pair
+    assert (seen[256]["tile_m"], seen[256]["stream_k"]) == (64, 0)     # 256 tiles cover the SMs
+    assert (seen[64]["tile_m"], seen[64]["stream_k"]) == (32, 1)       # 64 tiles: split K
+    p = hm.plan(1, 128, 4096, 4096, 152)
+    assert (p["tile_m"], p["stream_k"], p["grid"]) == (32, 0, 128)
     # long K: stream-K; wide N: the 256-token tile from M = 256 on
-    assert hm.plan(1, 128, 4096, 14336, 152)["stream_k"] == 1
+    p = hm.plan(1, 128, 4096, 14336, 152)
+    assert (p["tile_m"], p["stream_k"]) == (64, 1)
     assert hm.plan(1, 256, 14336, 4096, 152)["tile_m"] == 256
+    assert hm.plan(1, 64, 14336, 4096, 152)["stream_k"] == 0           # 112 tiles of 64 tokens
     # every stream-K CTA gets at least one k-block
     p = hm.plan(1, 1, 128, 256, 152)
     assert p["grid"] == 2
