@@ -46,10 +46,11 @@ __device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, co
   } else {
     const int e = find_expert(prefix, p.num_experts, tile);
     const int local = tile - prefix[e];
-    const int cnt = offs[e + 1] - offs[e];
-    const int mte = (cnt + BT - 1) / BT;
-    const int nt = local / mte;
-    const int mt = local - nt * mte;
+    // m-major within the expert, as in the dense order: the CTAs of one wave share an X tile and
+    // stream the expert's weight tiles, which stay in L2 while its token tiles are processed (the
+    // other order re-reads a heavy expert's X rows, hundreds of MB, once per weight tile)
+    const int nt = local % p.num_n_tiles;
+    const int mt = local / p.num_n_tiles;
     t.m0 = offs[e] + mt * BT;
     t.m_end = min(offs[e + 1], t.m0 + BT);
     t.n0 = nt * 128;
