@@ -194,18 +194,21 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
 
 /* ---------------------------------------------------------------- plan / diagnostics */
 
-/* The kernel configuration hm_gemm would use: token tile (MMA N), pipeline stages, split
- * (number of CTAs sharing one output tile along K; 1 = none) and grid size, for a device
- * with `num_sms` SMs. Host-only, no CUDA call. */
+/* The kernel configuration hm_gemm would use: kernel, token tile, pipeline stages, split
+ * (whether CTAs share one output tile along K) and grid size, for a device with `num_sms` SMs.
+ * Host-only, no CUDA call. */
 typedef struct hm_plan_info {
   int32_t bucket;      /* M bucket index: 0: M<=16, 1: <=64, 2: <=256, 3: <=1024, 4: >1024 */
-  int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension) */
+  int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension); CUDA-core kernel: tokens
+                          it is instantiated for (1, 2, 4 or 8, >= M) */
   int32_t tile_n;      /* weight rows per tile (tcgen05 MMA M dimension, 128) */
   int32_t tile_k;      /* K per pipeline stage */
   int32_t stages;      /* load-pipeline depth */
   int32_t stream_k;    /* 1 if the K loop is split across CTAs (stream-K) */
   int32_t grid;        /* CTAs launched */
   int32_t tiles;       /* output tiles */
+  int32_t kernel;      /* 0: tcgen05 tensor-core kernel; 1: CUDA-core kernel for decode-sized M
+                          (W4A16 formats, M <= 8: a matrix-vector product bound by HBM) */
 } hm_plan_info;
 hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
                   hm_plan_info* out);

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -114,6 +115,7 @@ struct Plan {
   int64_t num_m_tiles;
   int64_t num_n_tiles;
   int64_t kb_total;
+  int gemv;   // 1: the CUDA-core decode kernel (tile_m = tokens it is built for)
 };
 
 int bucket_of(int64_t m) {
@@ -195,9 +197,33 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   return ceil_div(m, 256) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 7 ? 256 : 128;
 }
 
+// W4A16 formats at decode-sized M run the CUDA-core kernel: with M <= 8 tokens per weight the
+// product is a matrix-vector one bound by HBM, which the tcgen05 pipeline (dequant into the MMA's
+// operand, one MMA per 128-K block, accumulator hand-offs) cannot keep up with.
+// HM_GEMV=0 in the environment keeps the tensor-core kernels for every M.
+bool use_gemv(int32_t fmt, int64_t m) {
+  if (fmt != kW4A16Int4 && fmt != kW4A16Mx) return false;
+  if (m < 1 || m > kGemvMaxTokens) return false;
+  return env_int("HM_GEMV", 1) != 0;
+}
+
 Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   Plan p{};
   p.bucket = bucket_of(m);
+  if (use_gemv(fmt, m)) {
+    p.gemv = 1;
+    p.tile_m = gemv_tokens(m);
+    p.tile_k = 128;
+    p.stages = gemv_stages(m);
+    p.num_m_tiles = 1;
+    p.num_n_tiles = pad_n(n) / 128;
+    p.kb_total = k / 128;
+    p.tiles = p.num_n_tiles;
+    const int64_t units = p.tiles * p.kb_total;
+    p.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    p.stream_k = (p.grid > p.tiles || p.tiles % p.grid != 0) ? 1 : 0;   // some tile shared by CTAs
+    return p;
+  }
   p.tile_m = tile_m_for(fmt, m, n, num_sms, k);
   p.tile_k = fmt == kW4A4Nv ? 256 : 128;
   p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(fmt, p.tile_m) : mx_stages(fmt, p.tile_m);
@@ -262,7 +288,9 @@ WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_a
   const size_t max_ctas = static_cast<size_t>(kMaxSmsForSizing) * ((fmt == kW4A8Mx || fmt == kW4A4Nv) ? kMxCtasPerSm : 1);
   off += align_up(max_ctas * 2 * widest * 128 * sizeof(float));
   w.counters = off;
-  off += align_up(static_cast<size_t>(max_tiles) * 4 * sizeof(uint32_t));
+  const int64_t counters = m <= kGemvMaxTokens ? std::max<int64_t>(max_tiles * 4, (pad_n(n) / 128) * kGemvCounters)
+                                               : max_tiles * 4;
+  off += align_up(static_cast<size_t>(counters) * sizeof(uint32_t));
   w.act_q = w.act_s = w.act_g = w.act_amax = off;
   if (internal_act && fmt == kW4A8Mx) {
     w.act_q = off;
@@ -329,6 +357,18 @@ bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int 
   const cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// X (bf16 [M][K]) as the decode kernel loads it: one box of 160 columns x `tokens` rows per 128-K
+// block, unswizzled (rows past M and columns past K read as zeros).
+bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int tokens) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k * 2)};
+  const cuuint32_t box[2] = {160, static_cast<cuuint32_t>(tokens)};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -442,6 +482,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
   out->stream_k = p.stream_k;
   out->grid = p.grid;
   out->tiles = static_cast<int32_t>(p.tiles);
+  out->kernel = p.gemv;
   return HM_OK;
 }
 
@@ -466,7 +507,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
     F16Params prm;
     std::memset(&prm, 0, sizeof(prm));
-    if (!encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
+    if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
       return HM_ERR_CUDA;
     prm.packed = static_cast<const uint8_t*>(packed);
     prm.y = static_cast<__nv_bfloat16*>(y);
@@ -483,6 +524,10 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
     prm.timeout_ns = timeout_ns();
     prm.trace = trace_for(di, p.grid);
+    if (p.gemv) {
+      prm.trace = nullptr;
+      return cuda_status(launch_gemv(prm, st));
+    }
     return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
   }
 
@@ -599,7 +644,8 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   // Partials for the CTAs of this launch, then the per-tile arrival counters.
   const size_t partial_bytes = align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float));
-  const size_t counter_bytes = align_up(static_cast<size_t>(p.tiles) * 4 * sizeof(uint32_t));
+  const size_t counter_bytes =
+      align_up(static_cast<size_t>(p.tiles) * (p.gemv ? kGemvCounters : 4) * sizeof(uint32_t));
   if (partial_bytes + counter_bytes > kNoAllocScratchBytes) return HM_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The counters must start at zero; clear them on every call (cheap, and safe even after a
@@ -607,7 +653,8 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (p.stream_k && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (!encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m)) return HM_ERR_CUDA;
+  if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
+    return HM_ERR_CUDA;
   prm.packed = static_cast<const uint8_t*>(packed);
   prm.y = static_cast<__nv_bfloat16*>(y);
   prm.partial = reinterpret_cast<float*>(scratch);
@@ -621,7 +668,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
   prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
   prm.timeout_ns = timeout_ns();
-  return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
+  return cuda_status(p.gemv ? launch_gemv(prm, st) : launch_f16_gemm(prm, p.tile_m, false, st));
 }
 
 uint32_t hm_get_device_error(void* stream) {

@@ -1,0 +1,477 @@
+// W4A16 GEMM for decode-sized M (up to 16 tokens): Y[M,N] = X[M,K] * dequant(W)^T, with
+// warp-level bf16 MMA (mma.sync m16n8k16, fp32 accumulation) as the multiply engine.
+//
+// Same product and restore rule as the tcgen05 W4A16 kernels (the explainer page "vLLM
+// Humming은 4비트를 어떻게 계산하나", sections "4비트 값에는 스케일이라는 해석 규칙이 붙는다" and
+// "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다"). With at most 16 tokens every weight byte
+// feeds at most 32 multiply-adds: the product is bound by streaming the packed weights from HBM,
+// and what limits a kernel is the work per weight on the SM (dequant, operand staging, hand-offs
+// between roles), not MMA throughput. The tcgen05 path spends that on restoring weights into
+// TMEM, single-thread MMA issue and accumulator hand-offs per 128-K block; here each warp restores
+// its weights in registers straight into the MMA's A fragment and keeps its accumulators in
+// registers, so the only hand-off per unit is the shared-memory stage itself.
+//
+//  * Work: the packed 128x128 units (n-tile major: unit u is tile u / kb, k-block u % kb) are cut
+//    into one contiguous range per CTA, start(c) = floor(c * U / G), G = min(U, SMs). A range may
+//    cover the tail of one tile, whole tiles and the head of another.
+//  * Roles (persistent CTA per SM): one producer lane loads each unit with a bulk copy and the
+//    activation block X[0:MT, k-block] with one 2-D TMA load (token rows past M read as zeros) into
+//    a ring of stages; 16 consumer warps, warp (p, c, r) taking rows 32p..32p+31 (two 16-row MMA
+//    tiles), the 32-K chunks 2c, 2c+1, and the units of parity r (every other unit, so that four
+//    warps per SM sub-partition hide each other's load and MMA latencies). The walk over units,
+//    slots and phases advances by counting (no division per unit).
+//  * Fragments: for m16n8k16, lane (g = lane/4, t = lane%4) holds A pairs at MMA k-slots
+//    {2t, 2t+1} and {2t+8, 2t+9}, B pairs at the same slots for token g. A contraction may number
+//    its k in any order as long as A and B agree, so lane t takes the 32-bit code word t of its
+//    rows (8 consecutive k) and the 8 matching activations: one 32-bit load per weight row, one
+//    16-byte load of activations per 8 tokens, no shuffles. Two MMAs per word (k-slots 0-7 from
+//    the word's columns 0-3, then columns 4-7).
+//  * INT4: the word is restored to exact bf16 (u - z) pairs (one shift, one lop3, one bf16x2
+//    subtract per pair); each unit's MMAs accumulate sum (u - z) x over the unit's 128 K in fp32,
+//    and the group scale multiplies that sum (s * sum (u - z) x, as in the small-token tcgen05
+//    kernel). MXFP4: the word is restored with its E8M0 scale (exact) and the MMAs accumulate
+//    straight into the running sums.
+//  * Segment end: the four warps of a row pair add their sums in a fixed order through shared
+//    memory (mbarrier hand-off, bounded); every warp closes every segment of its CTA's range, even
+//    one that holds no unit of its parity. A tile owned whole by the CTA is written to Y. A tile
+//    shared by several CTAs has a fixed owner, the CTA holding its first k-block: it reaches the
+//    tile at the end of its range, while for every other contributor the tile is the first
+//    segment. Those store fp32 partials ([CTA][token][row]) and add 1 to a per-(tile, row pair)
+//    counter with a release (no waiting); the owner waits (bounded, acquire) for the count, adds
+//    the partials in CTA order to its own (deterministic), writes Y and clears the counter.
+//  * Every mbarrier wait is bounded (device error word + CTA abort flag); the producer drains its
+//    copies in flight before the CTA exits; PDL as in the other kernels (weights are loaded before
+//    griddepcontrol.wait, activations and outputs only after it).
+#include <cuda_bf16.h>
+
+#include "hm_dequant.cuh"
+#include "hm_device.cuh"
+#include "hm_f16_common.cuh"
+#include "hm_kernels.h"
+#include "hm_layout.h"
+#include "hm_sched.cuh"
+
+namespace hm {
+namespace {
+
+constexpr int kVConsumers = 16;   // consumer warps: 4 row pairs x 2 chunk pairs x 2 unit parities
+constexpr int kVCons0 = 1;        // warps: 0 producer, 1-16 consumers
+constexpr int kVThreads = 32 * (kVCons0 + kVConsumers);
+
+template <int MT>
+struct VShape {
+  static constexpr int kNQ = MT / 8;                // token groups of 8 (MMA N)
+  static constexpr int kWBytes = 8704;              // one unit (the largest, MXFP4)
+  // activations: MT token rows of 160 bf16 (the unit's 128 K + 32 unused), a 320-byte pitch that
+  // puts the two token rows each quarter-warp reads into opposite halves of the banks
+  static constexpr int kXPitch = 320;
+  static constexpr int kXBytes = MT * kXPitch;
+  static constexpr int kStage = kWBytes + kXBytes;
+  static constexpr int kSFit = (192 * 1024) / kStage;
+  static constexpr int kS = kSFit > 16 ? 16 : kSFit;
+  static_assert(kS % 2 == 0, "a stage always holds units of one parity");
+  // segment-end exchange: [row pair][3 other warps][lane][2 tiles x 4 x kNQ floats]
+  static constexpr int kXchgFloats = 8 * kNQ;
+  static constexpr int kXchgOff = kS * kStage;
+  static constexpr int kXchgBytes = 4 * 3 * 32 * kXchgFloats * 4;
+  static constexpr int kBarOff = kXchgOff + kXchgBytes;
+  static constexpr int kNumBars = 2 * kS + 2 * 4;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmem = kMiscOff + 64 + 16 * 4 + 128;   // + e2m1 table, alignment slack
+  static_assert(kS >= 4, "pipeline depth");
+  static_assert(kWBytes % 128 == 0 && kStage % 128 == 0, "TMA destinations 128-byte aligned");
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+template <int MT, bool MX>
+__global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constant__ F16Params p) {
+  using S = VShape<MT>;
+  constexpr int SL = S::kS;
+  constexpr int NQ = S::kNQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);   // unit + activations landed
+  uint64_t* empty = full + SL;                                        // stage consumed (8 warps)
+  uint64_t* xfull = empty + SL;                                       // [row pair] 3 warps stored
+  uint64_t* xfree = xfull + 4;                                        // [row pair] the 4th read them
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff);
+  volatile uint32_t* hz_sh = abort_flag + 1;
+  float* lut = reinterpret_cast<float*>(smem + S::kMiscOff + 64);
+  float* xchg = reinterpret_cast<float*>(smem + S::kXchgOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t kb_total = p.sched.kb_total;
+  const int64_t total = static_cast<int64_t>(p.sched.num_tiles) * kb_total;
+  const int32_t grid = p.sched.grid;
+  const int32_t u0 = static_cast<int32_t>(sk_start(blockIdx.x, total, grid));
+  const int32_t u1 = static_cast<int32_t>(sk_start(blockIdx.x + 1, total, grid));
+  const int32_t n_units = u1 - u0;
+  const int32_t tile0 = u0 / kb_total, kb0 = u0 - tile0 * kb_total;
+  const int m_rows = static_cast<int>(p.m);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kVConsumers / 2);   // the 8 warps of the stage's unit parity
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&xfull[q], 3);
+      mbar_init(&xfree[q], 1);
+    }
+    fence_barrier_init();
+    const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(p.packed);
+    *abort_flag = 0u;
+    *hz_sh = hdr.has_zero == 1u ? 1u : 0u;
+    if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
+      atomicOr(p.err, kErrHeader);
+      *abort_flag = 1u;
+    }
+  }
+  if (MX && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
+  __syncthreads();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const bool aborted_early = *abort_flag != 0u;
+  const uint32_t has_zero = *hz_sh;
+  const uint32_t kUnit = MX ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+
+  if (aborted_early) {
+    // header mismatch: nothing was issued
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_x);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint8_t* wsrc = p.packed + kHeaderBytes + static_cast<size_t>(u0) * kUnit;
+      const uint32_t stage_bytes = kUnit + static_cast<uint32_t>(S::kXBytes);
+      // start-up: the weights of the first stages before waiting for the previous kernel (they are
+      // never written by another kernel), then their activation blocks
+      const int first = n_units < SL ? n_units : SL;
+      for (int i = 0; i < first; ++i) {
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        bulk_g2s(smem + i * S::kStage, wsrc + static_cast<size_t>(i) * kUnit, kUnit, &full[i], pol_w);
+      }
+      pdl_wait();
+      int kb = kb0;
+      for (int i = 0; i < first; ++i) {
+        tma_2d_g2s(smem + i * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, 0, &full[i], pol_x);
+        if (++kb == kb_total) kb = 0;
+      }
+      int issued = first, s = 0;
+      uint32_t ph = 0;
+      for (int i = first; i < n_units; ++i) {
+        if (!mbar_wait(&empty[s], ph, wc)) break;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        bulk_g2s(smem + s * S::kStage, wsrc + static_cast<size_t>(i) * kUnit, kUnit, &full[s], pol_w);
+        tma_2d_g2s(smem + s * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, 0, &full[s], pol_x);
+        if (++kb == kb_total) kb = 0;
+        issued = i + 1;
+        if (++s == SL) { s = 0; ph ^= 1u; }
+      }
+      // nothing may still be landing in shared memory when the CTA exits
+      for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
+        drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - kVCons0;
+    const int par = cw >> 3;                 // units u0 + par, u0 + par + 2, ...
+    const int pr = (cw >> 1) & 3;            // row pair: rows 32pr .. 32pr + 31
+    const int cp = cw & 1;                   // 32-K chunks 2cp and 2cp + 1 of every unit
+    const int slot_id = cp + 2 * par;        // 0 reads the other three at a segment end
+    const int g = lane >> 2, t = lane & 3;
+    // fragment rows: tile j (0, 1) of the pair, rows g and g + 8 of the tile
+    int rows[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      rows[j][0] = 32 * pr + 16 * j + g;
+      rows[j][1] = rows[j][0] + 8;
+    }
+    // shared-memory offsets within a stage: code words (tile j, row g / g+8, chunk 2cp + cc),
+    // activation fragments (token 8q + g, columns 32(2cp + cc) + 8t .. +7)
+    uint32_t woff[2][2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) woff[j][hl][cc] = (2 * cp + cc) * 2048 + rows[j][hl] * 16 + 4 * t;
+    const uint32_t xoff = static_cast<uint32_t>(S::kWBytes + g * S::kXPitch + (2 * cp) * 64 + t * 16);
+    const uint32_t smem0 = smem_u32(smem);
+
+    float yacc[2][NQ][4];   // [tile][token group][c0..c3]: rows g / g+8 x tokens 2t, 2t+1
+    int seg_kb0 = kb0, seg_count = 0;
+    bool first_seg = true;
+
+    // The segment [seg_kb0, seg_kb1) of `tile` is complete in yacc (this warp's units and chunks):
+    // add the other three warps' sums of the row pair, then write Y or hand off.
+    auto finish = [&](int tile, int seg_kb1, bool first) -> bool {
+      const uint32_t ph_x = static_cast<uint32_t>(seg_count) & 1u;
+      float* xb = xchg + (static_cast<size_t>(pr) * 3 * 32 + lane) * S::kXchgFloats;
+      if (slot_id != 0) {
+        // wait until the reader has taken the previous segment's values, then store ours
+        if (seg_count > 0 && !mbar_wait(&xfree[pr], ph_x ^ 1u, wc)) return false;
+        float* mine = xb + (slot_id - 1) * 32 * S::kXchgFloats;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mine[(j * NQ + q) * 4 + e] = yacc[j][q][e];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfull[pr]);
+        return true;
+      }
+      if (!mbar_wait(&xfull[pr], ph_x, wc)) return false;
+      float v[2][NQ][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int f = (j * NQ + q) * 4 + e;
+            v[j][q][e] = ((yacc[j][q][e] + xb[f]) + xb[32 * S::kXchgFloats + f]) + xb[64 * S::kXchgFloats + f];
+          }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xfree[pr]);
+      const int64_t n0 = static_cast<int64_t>(tile) * 128;
+      auto store_y = [&](int j, int q, int e, float val) {
+        const int tok = 8 * q + 2 * t + (e & 1);
+        const int64_t row = n0 + rows[j][e >> 1];
+        if (tok < m_rows && row < p.n) p.y[static_cast<size_t>(tok) * p.n + row] = __float2bfloat16_rn(val);
+      };
+      if (seg_kb0 == 0 && seg_kb1 == kb_total) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) store_y(j, q, e, v[j][q][e]);
+        return true;
+      }
+      // Shared tile, fixed owner: the CTA holding the tile's first k-block (c_lo), which reaches
+      // the tile at the end of its range, long after the others (c_lo+1 .. c_hi, for whom it is the
+      // first segment) have published their fp32 partials [CTA][token][row].
+      const int64_t it0 = static_cast<int64_t>(tile) * kb_total;
+      const int64_t c_lo = sk_owner(it0, total, grid), c_hi = sk_owner(it0 + kb_total - 1, total, grid);
+      uint32_t* ctr = p.counters + static_cast<size_t>(tile) * kGemvCounters + pr;
+      auto pidx = [&](int64_t c, int j, int q, int e) {
+        const int tok = 8 * q + 2 * t + (e & 1);
+        return static_cast<size_t>(c) * MT * 128 + static_cast<size_t>(tok) * 128 + rows[j][e >> 1];
+      };
+      if (static_cast<int64_t>(blockIdx.x) != c_lo) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) __stcg(p.partial + pidx(blockIdx.x, j, q, e), v[j][q][e]);
+        // the warp's stores are ordered before lane 0's release add (warp barrier, then release)
+        __syncwarp();
+        if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+        return true;
+      }
+      (void)first;
+      if (!sk_wait(ctr, static_cast<uint32_t>(c_hi - c_lo), wc)) return false;
+      // own values first, then the other contributors in CTA order, CU of them in flight at a time
+      constexpr int CU = NQ == 1 ? 4 : 2;
+      for (int64_t c = c_lo + 1; c <= c_hi; c += CU) {
+        float pv[CU][2][NQ][4];
+#pragma unroll
+        for (int uu = 0; uu < CU; ++uu) {
+          const int64_t cc = c + uu <= c_hi ? c + uu : c_hi;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) pv[uu][j][q][e] = __ldcg(p.partial + pidx(cc, j, q, e));
+        }
+#pragma unroll
+        for (int uu = 0; uu < CU; ++uu) {
+          if (c + uu > c_hi) break;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) v[j][q][e] += pv[uu][j][q][e];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) store_y(j, q, e, v[j][q][e]);
+      __syncwarp();
+      if (lane == 0) *ctr = 0u;   // for the next call (no contributor touches it again in this one)
+      return true;
+    };
+
+    // Segments (the parts of tiles in this CTA's range) in order; within each, this warp's units.
+    int i = par, s = par;                      // unit ordinal in the range, its stage
+    uint32_t ph = 0;
+    int tile = tile0;
+    for (int seg_end = 0; seg_end < n_units; ++tile) {
+      const int seg_begin = seg_end;
+      seg_end = seg_begin + (kb_total - seg_kb0 < n_units - seg_begin ? kb_total - seg_kb0 : n_units - seg_begin);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yacc[j][q][e] = 0.f;
+      bool ok = true;
+      for (; i < seg_end; i += 2) {
+        if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+        const uint32_t base = smem0 + s * S::kStage;
+        uint32_t bx[NQ][2][4];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint4 v = ld_shared_v4(base + xoff + q * 8 * S::kXPitch + cc * 64);
+            bx[q][cc][0] = v.x; bx[q][cc][1] = v.y; bx[q][cc][2] = v.z; bx[q][cc][3] = v.w;
+          }
+        uint32_t wd[2][2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff[j][hl][cc]);
+        if constexpr (!MX) {
+          float sc[2][2];
+          uint32_t z2[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+              const int r = rows[j][hl];
+              uint16_t sb;
+              asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(base + kUnitCodes + 2 * r));
+              sc[j][hl] = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+              uint32_t z = 8u;
+              if (has_zero) {
+                uint16_t zb;
+                asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(base + kUnitInt4 + (r >> 1)));
+                z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
+              }
+              z2[j][hl] = (0x43004300u | z) | (z << 16);
+            }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float d[2][NQ][4];   // per chunk: two short MMA chains instead of one long one
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t lo[4], hi[4];
+              dq_int4_word_unscaled(wd[j][0][cc], z2[j][0], lo);
+              dq_int4_word_unscaled(wd[j][1][cc], z2[j][1], hi);
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[cc][q][e] = 0.f;
+                mma_bf16_16816(d[cc][q], lo[0], hi[0], lo[1], hi[1], bx[q][cc][0], bx[q][cc][1]);
+                mma_bf16_16816(d[cc][q], lo[2], hi[2], lo[3], hi[3], bx[q][cc][2], bx[q][cc][3]);
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              yacc[j][q][0] = fmaf(sc[j][0], d[0][q][0] + d[1][q][0], yacc[j][q][0]);
+              yacc[j][q][1] = fmaf(sc[j][0], d[0][q][1] + d[1][q][1], yacc[j][q][1]);
+              yacc[j][q][2] = fmaf(sc[j][1], d[0][q][2] + d[1][q][2], yacc[j][q][2]);
+              yacc[j][q][3] = fmaf(sc[j][1], d[0][q][3] + d[1][q][3], yacc[j][q][3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint32_t e4[2];
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) e4[hl] = lds32(base + kUnitCodes + 4 * rows[j][hl]);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t a[2][4];
+#pragma unroll
+              for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t ex = (e4[hl] >> (8 * (2 * cp + cc))) & 0xFFu;
+                if (ex <= 128u) {
+                  dq_mx_word_bits(wd[j][hl][cc], mx_pow2_pair(ex), a[hl]);
+                } else {
+                  dq_mx_word(wd[j][hl][cc], lut, pow2f(static_cast<int>(ex) - 127), a[hl]);
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+                mma_bf16_16816(yacc[j][q], a[0][0], a[1][0], a[0][1], a[1][1], bx[q][cc][0], bx[q][cc][1]);
+                mma_bf16_16816(yacc[j][q], a[0][2], a[1][2], a[0][3], a[1][3], bx[q][cc][2], bx[q][cc][3]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        s += 2;
+        if (s >= SL) { s -= SL; ph ^= 1u; }
+      }
+      if (!ok) break;
+      // every warp closes every segment, even one without a unit of its parity
+      if (!finish(tile, seg_kb0 + (seg_end - seg_begin), first_seg)) break;
+      first_seg = false;
+      ++seg_count;
+      seg_kb0 = 0;
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+}
+
+template <int MT, bool MX>
+cudaError_t launch_v(const F16Params& p, cudaStream_t st) {
+  using S = VShape<MT>;
+  auto kern = gemv_kernel<MT, MX>;
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  return launch_pdl(kern, p.sched.grid, kVThreads, S::kSmem, st, p);
+}
+
+}  // namespace
+
+int gemv_tokens(int64_t m) { return m <= 8 ? 8 : 16; }
+
+int gemv_stages(int64_t m) { return gemv_tokens(m) == 8 ? VShape<8>::kS : VShape<16>::kS; }
+
+cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
+  if (p.m < 1 || p.m > kGemvMaxTokens) return cudaErrorInvalidValue;
+  const bool mx = p.fmt == kW4A16Mx;
+  if (gemv_tokens(p.m) == 8) return mx ? launch_v<8, true>(p, st) : launch_v<8, false>(p, st);
+  return mx ? launch_v<16, true>(p, st) : launch_v<16, false>(p, st);
+}
+
+}  // namespace hm

@@ -31,7 +31,7 @@ class WeightDesc(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("bucket", "tile_m", "tile_n", "tile_k", "stages", "stream_k", "grid", "tiles")]
+                ("bucket", "tile_m", "tile_n", "tile_k", "stages", "stream_k", "grid", "tiles", "kernel")]
 
 
 def _load():

@@ -74,10 +74,15 @@ def test_plan_buckets(hm):
         p = hm.plan(1, m, 4096, 4096, 152)
         seen[m] = p
         assert p["tile_n"] == 128 and p["tile_k"] == 128
-        assert p["tile_m"] >= min(m, 16) and p["tile_m"] in (16, 32, 64, 128, 256)
+        if m <= 16:   # decode-sized M: the warp-MMA decode kernel, built for 8 or 16 tokens
+            assert p["kernel"] == 1 and p["tile_m"] in (8, 16) and p["tile_m"] >= m
+        else:
+            assert p["kernel"] == 0 and p["tile_m"] >= min(m, 16) and p["tile_m"] in (16, 32, 64, 128, 256)
         assert 1 <= p["grid"] <= 152
     assert [seen[m]["bucket"] for m in (1, 16, 17, 64, 65, 256, 257, 1024, 1025)] == [0, 0, 1, 1, 2, 2, 3, 3, 4]
-    assert seen[1]["stream_k"] == 1 and seen[1]["grid"] == 152   # 32 tiles < 152 SMs
+    # M = 1: 1024 units over 152 CTAs, tiles shared
+    assert (seen[1]["stream_k"], seen[1]["grid"], seen[1]["tiles"]) == (1, 152, 32)
+    assert seen[16]["stream_k"] == 1 and seen[16]["grid"] == 152   # 32 tiles < 152 SMs
     assert seen[8192]["stream_k"] == 0 and seen[8192]["tile_m"] == 256 and seen[8192]["tiles"] == 32 * 32
     assert seen[1024]["tile_m"] == 256 and seen[1024]["stream_k"] == 0   # 128 tiles cover 84 % of the SMs
     # 16 < M <= 512 (INT4): the cost model picks the measured-best (tile, stream-K) pair
@@ -137,10 +142,10 @@ def test_plan_block_scaled_two_ctas_per_sm(hm):
 
 def test_plan_small_token_stages(hm):
     """INT4 token tiles 16/32 report the small-token kernel's load stages; HM_F16_SMALL=0 the general kernel's."""
-    a = hm.plan(1, 8, 4096, 4096, 152)["stages"]
+    a = hm.plan(1, 24, 4096, 4096, 152)["stages"]
     os.environ["HM_F16_SMALL"] = "0"
     try:
-        b = hm.plan(1, 8, 4096, 4096, 152)["stages"]
+        b = hm.plan(1, 24, 4096, 4096, 152)["stages"]
     finally:
         del os.environ["HM_F16_SMALL"]
     assert a >= 3 and b >= 2
@@ -152,3 +157,31 @@ def test_oversized_schedule_rejected(hm):
     with pytest.raises(hm.HmError) as e:
         hm.plan(1, 1 << 22, 1 << 20, 1 << 16, 152)
     assert e.value.status == 2
+
+
+def test_plan_decode_kernel(hm, monkeypatch):
+    """W4A16 formats at M <= 16 take the warp-MMA decode kernel (built for 8 or 16 tokens); the
+    block-scaled formats and M > 16 keep tcgen05; HM_GEMV=0 keeps tcgen05 for every M."""
+    for fmt in (1, 2):
+        tiles = [hm.plan(fmt, m, 4096, 4096, 152)["tile_m"] for m in range(1, 17)]
+        assert tiles == [8] * 8 + [16] * 8
+        assert all(hm.plan(fmt, m, 4096, 4096, 152)["kernel"] == 1 for m in range(1, 17))
+        assert hm.plan(fmt, 17, 4096, 4096, 152)["kernel"] == 0
+    for fmt in (3, 4):
+        assert hm.plan(fmt, 1, 4096, 4096, 152)["kernel"] == 0
+    # 152 tiles of two 128-K blocks on 152 SMs: one whole tile per CTA, no split
+    p = hm.plan(1, 1, 152 * 128, 256, 152)
+    assert (p["grid"], p["stream_k"]) == (152, 0)
+    # two units: two CTAs
+    p = hm.plan(1, 3, 200, 128, 152)
+    assert (p["grid"], p["tiles"], p["stream_k"]) == (2, 2, 0)
+    monkeypatch.setenv("HM_GEMV", "0")
+    assert hm.plan(1, 1, 4096, 4096, 152)["kernel"] == 0
+    assert hm.plan(1, 1, 4096, 4096, 152)["tile_m"] == 16
+
+
+def test_workspace_holds_decode_counters(hm):
+    """The decode kernel keeps 8 arrival counters per 128-row tile and 2 x 16 x 128 fp32 partials
+    per CTA; the workspace for M <= 16 has room for both on any device up to the sizing limit."""
+    n, k = 19456, 4096
+    assert hm.workspace_size(1, 16, n, k) >= (n // 128) * 8 * 4 + 148 * 2 * 16 * 128 * 4

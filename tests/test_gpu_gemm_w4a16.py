@@ -142,6 +142,7 @@ def test_small_token_kernel_and_general_kernel(hm, env, small, m):
     block's fp32 partial sum); HM_F16_SMALL=0 keeps the general kernel. Both must match the oracle,
     with stream-K splitting tiles (grid > tiles) and without."""
     env["HM_F16_SMALL"] = small
+    env["HM_GEMV"] = "0"          # M <= 16 would otherwise take the warp-MMA decode kernel
     run_case(hm, 1, m, 640, 3072, True, seed=40 + m)
     run_case(hm, 1, m, 256, 1024, False, seed=60 + m)
 
@@ -150,4 +151,5 @@ def test_small_token_kernel_and_general_kernel(hm, env, small, m):
 def test_small_token_kernel_long_k(hm, env, stream_k):
     """Many 128-K blocks per tile: the block-accumulator ring and A slots wrap many times."""
     env["HM_STREAM_K"] = stream_k
+    env["HM_GEMV"] = "0"
     run_case(hm, 1, 9, 384, 14336, True, seed=77)
