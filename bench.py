@@ -367,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
         plan = None
         if not p.label.startswith("moe"):
             plan = hm.plan(p.fmt, p.m, p.n, p.k, torch.cuda.get_device_properties(local_rank).multi_processor_count)
-            plan = {k: plan[k] for k in ("tile_m", "stages", "stream_k", "grid")}
+            plan = {k: plan[k] for k in ("kernel", "tile_m", "stages", "stream_k", "grid")}
         sweep.append({"point": p.label, "plan": plan, "us": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
                       "weight_gbs": round(wgbs, 1), "bound": bound,
                       "frac_hbm": round(gbs / pk["hbm"], 3), "frac_tensor": round(tf / peak_t, 3),
