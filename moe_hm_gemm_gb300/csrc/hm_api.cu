@@ -219,8 +219,16 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.num_n_tiles = pad_n(n) / 128;
     p.kb_total = k / 128;
     p.tiles = p.num_n_tiles;
-    const int64_t units = p.tiles * p.kb_total;
-    p.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    // With no more tiles than SMs, each tile is cut into the same number of K ranges, so every CTA
+    // holds one range of one tile: no CTA publishes a shared tile in the middle of its work, and a
+    // tile's contributors all finish together. With more tiles than SMs the ranges run across
+    // tile boundaries (one range per SM).
+    if (p.tiles <= num_sms) {
+      const int64_t per = std::min<int64_t>(num_sms / p.tiles, p.kb_total);
+      p.grid = static_cast<int>(p.tiles * per);
+    } else {
+      p.grid = num_sms;
+    }
     p.stream_k = (p.grid > p.tiles || p.tiles % p.grid != 0) ? 1 : 0;   // some tile shared by CTAs
     return p;
   }
@@ -360,12 +368,12 @@ bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// X (bf16 [M][K]) as the decode kernel loads it: one box of 160 columns x `tokens` rows per 128-K
-// block, unswizzled (rows past M and columns past K read as zeros).
+// X (bf16 [M][K]) as the decode kernel loads it: one box of 128 columns x `tokens` rows per 128-K
+// block, unswizzled (rows past M read as zeros).
 bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int tokens) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k * 2)};
-  const cuuint32_t box[2] = {160, static_cast<cuuint32_t>(tokens)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(tokens)};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

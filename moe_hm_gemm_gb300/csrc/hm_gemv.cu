@@ -55,27 +55,33 @@ namespace hm {
 namespace {
 
 constexpr int kVConsumers = 16;   // consumer warps: 4 row pairs x 2 chunk pairs x 2 unit parities
-constexpr int kVCons0 = 1;        // warps: 0 producer, 1-16 consumers
-constexpr int kVThreads = 32 * (kVCons0 + kVConsumers);
+constexpr int kVCons0 = 1;        // warps: 0 producer, 1-16 consumers, 17 row metadata (INT4)
+constexpr int kVMeta = kVCons0 + kVConsumers;
+constexpr int kVThreads = 32 * (kVMeta + 1);
 
 template <int MT>
 struct VShape {
   static constexpr int kNQ = MT / 8;                // token groups of 8 (MMA N)
   static constexpr int kWBytes = 8704;              // one unit (the largest, MXFP4)
-  // activations: MT token rows of 160 bf16 (the unit's 128 K + 32 unused), a 320-byte pitch that
-  // puts the two token rows each quarter-warp reads into opposite halves of the banks
-  static constexpr int kXPitch = 320;
+  // activations: MT token rows of 128 bf16, as one TMA box lands them. The two token rows a
+  // quarter-warp reads then share banks (a 2-way conflict on two loads per warp and unit), which
+  // costs less than a wider, padded box: the activation box is a TMA operation per unit, and a
+  // 160-column box with a 320-byte pitch made the load pipeline ~25 % slower (measured)
+  static constexpr int kXPitch = 256;
   static constexpr int kXBytes = MT * kXPitch;
-  static constexpr int kStage = kWBytes + kXBytes;
+  // INT4 row metadata of the unit, written by the metadata warp: [128 rows] {fp32 scale, bf16x2
+  // (128 + z, 128 + z)}
+  static constexpr int kMetaOff = kWBytes + kXBytes;
+  static constexpr int kStage = kMetaOff + 128 * 8;
   static constexpr int kSFit = (192 * 1024) / kStage;
-  static constexpr int kS = kSFit > 16 ? 16 : kSFit;
+  static constexpr int kS = (kSFit > 16 ? 16 : kSFit) & ~1;
   static_assert(kS % 2 == 0, "a stage always holds units of one parity");
   // segment-end exchange: [row pair][3 other warps][lane][2 tiles x 4 x kNQ floats]
   static constexpr int kXchgFloats = 8 * kNQ;
   static constexpr int kXchgOff = kS * kStage;
   static constexpr int kXchgBytes = 4 * 3 * 32 * kXchgFloats * 4;
   static constexpr int kBarOff = kXchgOff + kXchgBytes;
-  static constexpr int kNumBars = 2 * kS + 2 * 4;
+  static constexpr int kNumBars = 3 * kS + 2 * 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmem = kMiscOff + 64 + 16 * 4 + 128;   // + e2m1 table, alignment slack
   static_assert(kS >= 4, "pipeline depth");
@@ -89,6 +95,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same with a zero accumulator (the first MMA of a chain).
+__device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -107,7 +123,8 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
                                              ~static_cast<uintptr_t>(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);   // unit + activations landed
   uint64_t* empty = full + SL;                                        // stage consumed (8 warps)
-  uint64_t* xfull = empty + SL;                                       // [row pair] 3 warps stored
+  uint64_t* meta_full = empty + SL;                                   // INT4 row metadata written
+  uint64_t* xfull = meta_full + SL;                                   // [row pair] 3 warps stored
   uint64_t* xfree = xfull + 4;                                        // [row pair] the 4th read them
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff);
   volatile uint32_t* hz_sh = abort_flag + 1;
@@ -129,6 +146,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kVConsumers / 2);   // the 8 warps of the stage's unit parity
+      mbar_init(&meta_full[s], 1);
     }
     for (int q = 0; q < 4; ++q) {
       mbar_init(&xfull[q], 3);
@@ -155,19 +173,21 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
     // header mismatch: nothing was issued
   } else if (warp == 0) {
     // ---------------------------------------------------------------- producer
+    const uint64_t pol_w = policy_evict_first();
+    const uint8_t* wsrc = p.packed + kHeaderBytes + static_cast<size_t>(u0) * kUnit;
+    const uint32_t stage_bytes = kUnit + static_cast<uint32_t>(S::kXBytes);
+    const int first = n_units < SL ? n_units : SL;
+    // start-up: the weights of the first stages, one stage per lane (a single thread takes ~70 ns
+    // per bulk copy issue), before waiting for the previous kernel (weights are never written by
+    // another kernel); their activation blocks follow from lane 0 after the wait
+    if (lane < first) {
+      mbar_arrive_expect_tx(&full[lane], stage_bytes);
+      bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
+    }
+    __syncwarp();
     if (lane == 0) {
       prefetch_tmap(&p.tmap_x);
-      const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const uint8_t* wsrc = p.packed + kHeaderBytes + static_cast<size_t>(u0) * kUnit;
-      const uint32_t stage_bytes = kUnit + static_cast<uint32_t>(S::kXBytes);
-      // start-up: the weights of the first stages before waiting for the previous kernel (they are
-      // never written by another kernel), then their activation blocks
-      const int first = n_units < SL ? n_units : SL;
-      for (int i = 0; i < first; ++i) {
-        mbar_arrive_expect_tx(&full[i], stage_bytes);
-        bulk_g2s(smem + i * S::kStage, wsrc + static_cast<size_t>(i) * kUnit, kUnit, &full[i], pol_w);
-      }
       pdl_wait();
       int kb = kb0;
       for (int i = 0; i < first; ++i) {
@@ -189,6 +209,38 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
       for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
         drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
     }
+  } else if (warp == kVMeta) {
+    // ---------------------------------------------------------------- INT4 row metadata
+    // Each unit's 128 scales and zero-points, once per unit instead of once per consumer warp:
+    // lane l converts rows 4l .. 4l+3 (bf16 scale -> fp32, u4 zero-point -> bf16x2 128 + z).
+    if constexpr (!MX) {
+      const uint32_t smem0 = smem_u32(smem);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < n_units; ++i) {
+        if (!mbar_wait(&full[s], ph, wc)) break;
+        const uint32_t base = smem0 + s * S::kStage;
+        uint32_t sc01, sc23, zz = 0x8888u;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc01), "=r"(sc23) : "r"(base + kUnitCodes + 8 * lane));
+        if (has_zero) {
+          uint16_t zb;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(base + kUnitInt4 + 2 * lane));
+          zz = zb;
+        }
+        uint32_t z2[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t z = (zz >> (4 * r)) & 0xFu;
+          z2[r] = (0x43004300u | z) | (z << 16);
+        }
+        const uint32_t mb = base + S::kMetaOff + 32 * lane;
+        st_shared_v4(mb, sc01 << 16, z2[0], sc01 & 0xFFFF0000u, z2[1]);
+        st_shared_v4(mb + 16, sc23 << 16, z2[2], sc23 & 0xFFFF0000u, z2[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_full[s]);
+        if (++s == SL) { s = 0; ph ^= 1u; }
+      }
+    }
   } else {
     // ---------------------------------------------------------------- consumers
     const int cw = warp - kVCons0;
@@ -204,16 +256,12 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
       rows[j][0] = 32 * pr + 16 * j + g;
       rows[j][1] = rows[j][0] + 8;
     }
-    // shared-memory offsets within a stage: code words (tile j, row g / g+8, chunk 2cp + cc),
-    // activation fragments (token 8q + g, columns 32(2cp + cc) + 8t .. +7)
-    uint32_t woff[2][2][2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) woff[j][hl][cc] = (2 * cp + cc) * 2048 + rows[j][hl] * 16 + 4 * t;
+    // shared-memory offsets within a stage (the per-(tile, row, chunk) parts are immediates):
+    // code word t of row 32pr + g (+16j, +8hl) in chunk 2cp (+cc); activation fragment of token g
+    // (+8q), columns 64cp + 8t (+32cc); the row's metadata (INT4) or E8M0 scale word (MXFP4)
+    const uint32_t woff = static_cast<uint32_t>((2 * cp) * 2048 + (32 * pr + g) * 16 + 4 * t);
     const uint32_t xoff = static_cast<uint32_t>(S::kWBytes + g * S::kXPitch + (2 * cp) * 64 + t * 16);
+    const uint32_t moff = static_cast<uint32_t>(MX ? kUnitCodes + (32 * pr + g) * 4 : S::kMetaOff + (32 * pr + g) * 8);
     const uint32_t smem0 = smem_u32(smem);
 
     float yacc[2][NQ][4];   // [tile][token group][c0..c3]: rows g / g+8 x tokens 2t, 2t+1
@@ -342,7 +390,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
           for (int e = 0; e < 4; ++e) yacc[j][q][e] = 0.f;
       bool ok = true;
       for (; i < seg_end; i += 2) {
-        if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+        if (!mbar_wait(&full[s], ph, wc) || (!MX && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
         const uint32_t base = smem0 + s * S::kStage;
         uint32_t bx[NQ][2][4];
 #pragma unroll
@@ -358,7 +406,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
 #pragma unroll
           for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff[j][hl][cc]);
+            for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff + cc * 2048 + j * 256 + hl * 128);
         if constexpr (!MX) {
           float sc[2][2];
           uint32_t z2[2][2];
@@ -366,17 +414,10 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
           for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl) {
-              const int r = rows[j][hl];
-              uint16_t sb;
-              asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(base + kUnitCodes + 2 * r));
-              sc[j][hl] = __uint_as_float(static_cast<uint32_t>(sb) << 16);
-              uint32_t z = 8u;
-              if (has_zero) {
-                uint16_t zb;
-                asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(base + kUnitInt4 + (r >> 1)));
-                z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
-              }
-              z2[j][hl] = (0x43004300u | z) | (z << 16);
+              uint32_t sb, zb;
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sb), "=r"(zb) : "r"(base + moff + j * 128 + hl * 64));
+              sc[j][hl] = __uint_as_float(sb);
+              z2[j][hl] = zb;
             }
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -388,9 +429,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
               dq_int4_word_unscaled(wd[j][1][cc], z2[j][1], hi);
 #pragma unroll
               for (int q = 0; q < NQ; ++q) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[cc][q][e] = 0.f;
-                mma_bf16_16816(d[cc][q], lo[0], hi[0], lo[1], hi[1], bx[q][cc][0], bx[q][cc][1]);
+                mma_bf16_16816_z(d[cc][q], lo[0], hi[0], lo[1], hi[1], bx[q][cc][0], bx[q][cc][1]);
                 mma_bf16_16816(d[cc][q], lo[2], hi[2], lo[3], hi[3], bx[q][cc][2], bx[q][cc][3]);
               }
             }
@@ -407,7 +446,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
           for (int j = 0; j < 2; ++j) {
             uint32_t e4[2];
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl) e4[hl] = lds32(base + kUnitCodes + 4 * rows[j][hl]);
+            for (int hl = 0; hl < 2; ++hl) e4[hl] = lds32(base + moff + j * 64 + hl * 32);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               uint32_t a[2][4];

@@ -80,9 +80,9 @@ def test_plan_buckets(hm):
             assert p["kernel"] == 0 and p["tile_m"] >= min(m, 16) and p["tile_m"] in (16, 32, 64, 128, 256)
         assert 1 <= p["grid"] <= 152
     assert [seen[m]["bucket"] for m in (1, 16, 17, 64, 65, 256, 257, 1024, 1025)] == [0, 0, 1, 1, 2, 2, 3, 3, 4]
-    # M = 1: 1024 units over 152 CTAs, tiles shared
-    assert (seen[1]["stream_k"], seen[1]["grid"], seen[1]["tiles"]) == (1, 152, 32)
-    assert seen[16]["stream_k"] == 1 and seen[16]["grid"] == 152   # 32 tiles < 152 SMs
+    # M = 1: 32 tiles of 32 k-blocks, each cut into 4 K ranges (one per CTA)
+    assert (seen[1]["stream_k"], seen[1]["grid"], seen[1]["tiles"]) == (1, 128, 32)
+    assert seen[16]["stream_k"] == 1 and seen[16]["grid"] == 128   # M = 16 too: the decode kernel
     assert seen[8192]["stream_k"] == 0 and seen[8192]["tile_m"] == 256 and seen[8192]["tiles"] == 32 * 32
     assert seen[1024]["tile_m"] == 256 and seen[1024]["stream_k"] == 0   # 128 tiles cover 84 % of the SMs
     # 16 < M <= 512 (INT4): the cost model picks the measured-best (tile, stream-K) pair
@@ -175,6 +175,12 @@ def test_plan_decode_kernel(hm, monkeypatch):
     # two units: two CTAs
     p = hm.plan(1, 3, 200, 128, 152)
     assert (p["grid"], p["tiles"], p["stream_k"]) == (2, 2, 0)
+    # tiles <= SMs: every tile cut into the same number of K ranges, one per CTA
+    for n, k, grid, sk in ((14336, 4096, 112, 0), (4096, 14336, 128, 1), (1024, 1024, 64, 1), (640, 3072, 120, 1)):
+        p = hm.plan(1, 1, n, k, 152)
+        assert (p["grid"], p["stream_k"]) == (grid, sk), (n, k, p)
+    # more tiles than SMs: one range per SM
+    assert hm.plan(1, 1, 304 * 128, 256, 152)["grid"] == 152
     monkeypatch.setenv("HM_GEMV", "0")
     assert hm.plan(1, 1, 4096, 4096, 152)["kernel"] == 0
     assert hm.plan(1, 1, 4096, 4096, 152)["tile_m"] == 16
