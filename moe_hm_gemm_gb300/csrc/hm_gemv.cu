@@ -39,10 +39,18 @@
 //    segment. Those store fp32 partials ([CTA][token][row]) and add 1 to a per-(tile, row pair)
 //    counter with a release (no waiting); the owner waits (bounded, acquire) for the count, adds
 //    the partials in CTA order to its own (deterministic), writes Y and clears the counter.
+//    When every tile is cut into 2-4 K ranges, one per CTA, the ranges of a tile form a thread-block
+//    cluster instead: ranks 1.. store their sums straight into rank 0's shared memory and arrive on
+//    its barrier (release at cluster scope), rank 0 waits (bounded) and adds them in rank order,
+//    the same order as the global path, so both give identical bits. A cluster barrier after set-up
+//    and one before exit keep every remote access inside the lifetime of the CTA it targets; the
+//    launcher uses clusters only when the device can hold all of them at once.
 //  * Every mbarrier wait is bounded (device error word + CTA abort flag); the producer drains its
 //    copies in flight before the CTA exits; PDL as in the other kernels (weights are loaded before
 //    griddepcontrol.wait, activations and outputs only after it).
 #include <cuda_bf16.h>
+
+#include <cstdlib>
 
 #include "hm_dequant.cuh"
 #include "hm_device.cuh"
@@ -73,20 +81,29 @@ struct VShape {
   // (128 + z, 128 + z)}
   static constexpr int kMetaOff = kWBytes + kXBytes;
   static constexpr int kStage = kMetaOff + 128 * 8;
-  static constexpr int kSFit = (192 * 1024) / kStage;
-  static constexpr int kS = (kSFit > 16 ? 16 : kSFit) & ~1;
-  static_assert(kS % 2 == 0, "a stage always holds units of one parity");
   // segment-end exchange: [row pair][3 other warps][lane][2 tiles x 4 x kNQ floats]
   static constexpr int kXchgFloats = 8 * kNQ;
-  static constexpr int kXchgOff = kS * kStage;
   static constexpr int kXchgBytes = 4 * 3 * 32 * kXchgFloats * 4;
-  static constexpr int kBarOff = kXchgOff + kXchgBytes;
-  static constexpr int kNumBars = 3 * kS + 2 * 4;
+  // cluster hand-off of a shared tile: [rank 1..3][row pair][lane][2 tiles x 4 x kNQ floats] in
+  // the owner CTA (rank 0)
+  static constexpr int kRedBytes = 3 * 4 * 32 * kXchgFloats * 4;
+  // as many stages (even, at most 16) as the 227 KB per CTA leave beside the fixed parts
+  static constexpr int kFixed = kXchgBytes + kRedBytes + (3 * 16 + 3 * 4) * 8 + 64 + 16 * 4 + 128;
+  static constexpr int kSFit = (232448 - kFixed) / kStage;
+  static constexpr int kS = (kSFit > 16 ? 16 : kSFit) & ~1;
+  static_assert(kS % 2 == 0, "a stage always holds units of one parity");
+  static constexpr int kXchgOff = kS * kStage;
+  static constexpr int kRedOff = kXchgOff + kXchgBytes;
+  static constexpr int kBarOff = kRedOff + kRedBytes;
+  static constexpr int kNumBars = 3 * kS + 3 * 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmem = kMiscOff + 64 + 16 * 4 + 128;   // + e2m1 table, alignment slack
   static_assert(kS >= 4, "pipeline depth");
   static_assert(kWBytes % 128 == 0 && kStage % 128 == 0, "TMA destinations 128-byte aligned");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
+
+constexpr int kVMaxCluster = 4;   // CTAs per cluster for the shared-memory hand-off (ranks 1..3 publish)
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -105,6 +122,49 @@ __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uin
       "{%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Cluster-scope helpers for the hand-off of a shared tile between the CTAs of one cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Bounded wait for a phase completed by arrivals from other CTAs of the cluster (acquire at
+// cluster scope, so their stores into this CTA's shared memory are visible afterwards).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
+  const uint32_t a = smem_u32(bar);
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (try_wait()) return true;
+    if (*ctx.abort) return false;
+    if (globaltimer() - t0 > ctx.timeout_ns) {
+      *ctx.abort = 1u;
+      atomicOr(ctx.err, kErrTimeout);
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -126,10 +186,13 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
   uint64_t* meta_full = empty + SL;                                   // INT4 row metadata written
   uint64_t* xfull = meta_full + SL;                                   // [row pair] 3 warps stored
   uint64_t* xfree = xfull + 4;                                        // [row pair] the 4th read them
+  uint64_t* red_full = xfree + 4;                                     // [row pair] cluster ranks 1.. stored
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff);
   volatile uint32_t* hz_sh = abort_flag + 1;
   float* lut = reinterpret_cast<float*>(smem + S::kMiscOff + 64);
   float* xchg = reinterpret_cast<float*>(smem + S::kXchgOff);
+  float* red = reinterpret_cast<float*>(smem + S::kRedOff);
+  const int csize = p.cluster > 1 ? p.cluster : 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,6 +214,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
     for (int q = 0; q < 4; ++q) {
       mbar_init(&xfull[q], 3);
       mbar_init(&xfree[q], 1);
+      mbar_init(&red_full[q], csize > 1 ? csize - 1 : 1);
     }
     fence_barrier_init();
     const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(p.packed);
@@ -163,6 +227,8 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
   }
   if (MX && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
   __syncthreads();
+  // the owner's barriers must be initialised before another CTA of its cluster arrives on them
+  if (csize > 1) cluster_sync_all();
   if (threadIdx.x == 0) pdl_launch_dependents();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const bool aborted_early = *abort_flag != 0u;
@@ -307,6 +373,41 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
         if (tok < m_rows && row < p.n) p.y[static_cast<size_t>(tok) * p.n + row] = __float2bfloat16_rn(val);
       };
       if (seg_kb0 == 0 && seg_kb1 == kb_total) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) store_y(j, q, e, v[j][q][e]);
+        return true;
+      }
+      if (csize > 1) {
+        // Cluster hand-off: the cluster's CTAs are the tile's K ranges in order (rank 0 holds the
+        // first k-block); ranks 1.. store their sums into rank 0's shared memory and arrive on its
+        // barrier; rank 0 adds them in rank order (deterministic) and writes Y. One use per launch.
+        constexpr int F = S::kXchgFloats;
+        const uint32_t rank = blockIdx.x % static_cast<uint32_t>(csize);
+        if (rank != 0) {
+          const uint32_t dst = map_to_rank(smem_u32(red + ((static_cast<size_t>(rank - 1) * 4 + pr) * 32 + lane) * F), 0);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+              st_cluster_v4(dst + ((j * NQ + q) * 4) * 4, v[j][q][0], v[j][q][1], v[j][q][2], v[j][q][3]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&red_full[pr]), 0));
+          return true;
+        }
+        if (!mbar_wait_cluster(&red_full[pr], 0u, wc)) return false;
+        for (int r = 1; r < csize; ++r) {
+          const float* src = red + ((static_cast<size_t>(r - 1) * 4 + pr) * 32 + lane) * F;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) v[j][q][e] += src[(j * NQ + q) * 4 + e];
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -482,13 +583,16 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
   }
   __syncwarp();
   __syncthreads();
+  // no CTA leaves while another of its cluster may still write into its shared memory
+  if (csize > 1) cluster_sync_all();
 }
 
 template <int MT, bool MX>
-cudaError_t launch_v(const F16Params& p, cudaStream_t st) {
+cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   using S = VShape<MT>;
   auto kern = gemv_kernel<MT, MX>;
   static int configured[64] = {};
+  static int cluster_max[64][kVMaxCluster + 1] = {};   // active clusters the device holds, +1 (0 unknown)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
@@ -497,7 +601,49 @@ cudaError_t launch_v(const F16Params& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  return launch_pdl(kern, p.sched.grid, kVThreads, S::kSmem, st, p);
+  F16Params p = p_in;
+  // Cluster hand-off when every tile is cut into 2..4 K ranges, one per CTA (grid = tiles x ranges),
+  // and the device can hold all the clusters at once (they wait on each other).
+  const int32_t tiles = p.sched.num_tiles, grid = p.sched.grid;
+  const int ranges = tiles > 0 && grid % tiles == 0 ? grid / tiles : 0;
+  int cs = ranges >= 2 && ranges <= kVMaxCluster && ranges <= p.sched.kb_total ? ranges : 1;
+  static const bool clusters_on = [] {   // HM_GEMV_CLUSTER=0: the global-memory hand-off everywhere
+    const char* v = std::getenv("HM_GEMV_CLUSTER");
+    return !(v && v[0] == '0');
+  }();
+  if (!clusters_on) cs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(kVThreads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(S::kSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  if (cs > 1 && cluster_max[dev][cs] == 0) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cluster_max[dev][cs] = n + 1;
+  }
+  if (cs > 1 && (cluster_max[dev][cs] - 1) * cs < grid) cs = 1;   // not all clusters fit at once
+  p.cluster = cs;
+  if (cs <= 1) return launch_pdl(kern, grid, kVThreads, S::kSmem, st, p);
+  static const bool pdl = [] {
+    const char* v = std::getenv("HM_PDL");
+    return !(v && v[0] == '0');
+  }();
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace

@@ -30,6 +30,7 @@ struct F16Params {
   SchedParams sched;
   uint64_t timeout_ns;
   uint64_t* trace;                    // optional per-CTA timestamps [grid][16] (diagnostics)
+  int32_t cluster;                    // decode kernel: CTAs per cluster (each tile's K ranges), 0/1 = none
 };
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).

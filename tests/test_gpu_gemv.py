@@ -55,10 +55,10 @@ def check(hm, fmt, m, n, k, has_zero, seed):
     return p
 
 
-# (n, k): 120 units on 120 CTAs, each tile split 24 ways | 2 units, no split, ragged N |
-# 152 tiles of 2 blocks: one whole tile per CTA | 1024 units: ranges of 6-7 units across tiles |
-# 2 tiles x 112 blocks: 76 CTAs per tile
-SHAPES = [(640, 3072), (200, 128), (19456, 256), (4096, 4096), (256, 14336)]
+# (n, k): 5 tiles each cut into 24 K ranges (global hand-off) | 2 units, no split, ragged N |
+# 152 tiles of 2 blocks: one whole tile per CTA | 32 tiles cut into 4 ranges (clusters of 4) |
+# 2 tiles x 112 blocks cut into 76 ranges | 64 tiles cut in 2 (clusters of 2) | 40 tiles cut in 3
+SHAPES = [(640, 3072), (200, 128), (19456, 256), (4096, 4096), (256, 14336), (8192, 1024), (5120, 1024)]
 
 
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 15, 16])
@@ -154,4 +154,33 @@ def test_full_size_sampled(hm):
         got = bf16_np(y.cpu()[torch.from_numpy(ms), torch.from_numpy(ns)])
         ok = og.tolerance_ok(got, ref)
         assert ok.all(), f"M={m}: {int((~ok).sum())} sampled outputs outside tolerance"
+    assert hm.device_error() == 0
+
+
+@pytest.mark.parametrize("n,k,m", [(4096, 4096, 1), (8192, 1024, 8), (5120, 1024, 16), (4096, 14336, 3)])
+def test_cluster_and_global_handoff_agree(hm, n, k, m):
+    """Tiles cut into 2-4 K ranges are summed through a thread-block cluster's shared memory, or
+    (HM_GEMV_CLUSTER=0, read once per process: run in a child) through global memory; both add the
+    ranges in the same order, so the outputs are bit-identical."""
+    import subprocess, sys, tempfile, textwrap
+    qw, packed = quantized(hm, 1, n, k, True, seed=600 + m)
+    x = synth.activations(m, k, seed=601)
+    y = hm.gemm(1, x.cuda(), packed, n, k)
+    torch.cuda.synchronize()
+    assert_close(y, og.gemm(bf16_np(x), qw.what), "cluster hand-off")
+    with tempfile.TemporaryDirectory() as d:
+        torch.save({"packed": packed.cpu(), "x": x}, d + "/in.pt")
+        code = textwrap.dedent(f"""
+            import torch, __graft_entry__
+            from moe_hm_gemm_gb300 import hm
+            t = torch.load("{d}/in.pt")
+            y = hm.gemm(1, t["x"].cuda(), t["packed"].cuda(), {n}, {k})
+            torch.cuda.synchronize()
+            assert hm.device_error() == 0
+            torch.save(y.cpu(), "{d}/y.pt")
+        """)
+        env = dict(os.environ, HM_GEMV_CLUSTER="0")
+        subprocess.run([sys.executable, "-c", code], check=True, env=env, cwd=os.getcwd())
+        y_global = torch.load(d + "/y.pt")
+    assert torch.equal(y.cpu(), y_global)
     assert hm.device_error() == 0
