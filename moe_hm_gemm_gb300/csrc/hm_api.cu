@@ -197,20 +197,26 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   return ceil_div(m, 256) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 7 ? 256 : 128;
 }
 
-// W4A16 formats at decode-sized M run the CUDA-core kernel: with M <= 8 tokens per weight the
-// product is a matrix-vector one bound by HBM, which the tcgen05 pipeline (dequant into the MMA's
-// operand, one MMA per 128-K block, accumulator hand-offs) cannot keep up with.
-// HM_GEMV=0 in the environment keeps the tensor-core kernels for every M.
-bool use_gemv(int32_t fmt, int64_t m) {
+// W4A16 formats at decode-sized M run the warp-MMA decode kernel: with few tokens per weight the
+// product is bound by streaming the weights, which the tcgen05 pipeline (restore into TMEM, one
+// MMA batch per 128-K block, accumulator hand-offs) does not keep up with (measured on the 4096 and
+// 14336 layers). Up to 16 tokens always; for 17..32 tokens MXFP4 always, INT4 when the tcgen05
+// plan would split tiles along K (the decode kernel's K ranges are cheaper there; with a whole tile
+// per CTA the tcgen05 small-token kernel is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2
+// takes the decode kernel for every M it serves (tests, sweeps).
+bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (fmt != kW4A16Int4 && fmt != kW4A16Mx) return false;
   if (m < 1 || m > kGemvMaxTokens) return false;
-  return env_int("HM_GEMV", 1) != 0;
+  const int mode = env_int("HM_GEMV", 1);
+  if (mode == 0) return false;
+  if (mode == 2 || m <= 16 || fmt == kW4A16Mx) return true;
+  return f16_choice(m, n, k, num_sms).stream_k;
 }
 
 Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   Plan p{};
   p.bucket = bucket_of(m);
-  if (use_gemv(fmt, m)) {
+  if (use_gemv(fmt, m, n, k, num_sms)) {
     p.gemv = 1;
     p.tile_m = gemv_tokens(m);
     p.tile_k = 128;

@@ -62,10 +62,15 @@
 namespace hm {
 namespace {
 
-constexpr int kVConsumers = 16;   // consumer warps: 4 row pairs x 2 chunk pairs x 2 unit parities
-constexpr int kVCons0 = 1;        // warps: 0 producer, 1-16 consumers, 17 row metadata (INT4)
-constexpr int kVMeta = kVCons0 + kVConsumers;
-constexpr int kVThreads = 32 * (kVMeta + 1);
+// Warps: 0 producer, then the consumers, then the INT4 row-metadata warp. Consumer warp (row pair,
+// chunk pair, unit parity): 4 x 2 x kPar. Up to 16 tokens two parities take alternate units (16
+// consumers, four per sub-partition, to hide load and MMA latency); with 32 tokens a warp holds four
+// token groups of sums and there is one parity (8 consumers, twice the registers each).
+constexpr int kVCons0 = 1;
+__host__ __device__ constexpr int v_par(int mt) { return mt <= 16 ? 2 : 1; }
+__host__ __device__ constexpr int v_consumers(int mt) { return 8 * v_par(mt); }
+__host__ __device__ constexpr int v_meta_warp(int mt) { return kVCons0 + v_consumers(mt); }
+__host__ __device__ constexpr int v_threads(int mt) { return 32 * (v_meta_warp(mt) + 1); }
 
 template <int MT>
 struct VShape {
@@ -81,9 +86,10 @@ struct VShape {
   // (128 + z, 128 + z)}
   static constexpr int kMetaOff = kWBytes + kXBytes;
   static constexpr int kStage = kMetaOff + 128 * 8;
-  // segment-end exchange: [row pair][3 other warps][lane][2 tiles x 4 x kNQ floats]
+  static constexpr int kPar = v_par(MT);
+  // segment-end exchange: [row pair][the 2 kPar - 1 other warps][lane][2 tiles x 4 x kNQ floats]
   static constexpr int kXchgFloats = 8 * kNQ;
-  static constexpr int kXchgBytes = 4 * 3 * 32 * kXchgFloats * 4;
+  static constexpr int kXchgBytes = 4 * (2 * kPar - 1) * 32 * kXchgFloats * 4;
   // cluster hand-off of a shared tile: [rank 1..3][row pair][lane][2 tiles x 4 x kNQ floats] in
   // the owner CTA (rank 0)
   static constexpr int kRedBytes = 3 * 4 * 32 * kXchgFloats * 4;
@@ -91,7 +97,7 @@ struct VShape {
   static constexpr int kFixed = kXchgBytes + kRedBytes + (3 * 16 + 3 * 4) * 8 + 64 + 16 * 4 + 128;
   static constexpr int kSFit = (232448 - kFixed) / kStage;
   static constexpr int kS = (kSFit > 16 ? 16 : kSFit) & ~1;
-  static_assert(kS % 2 == 0, "a stage always holds units of one parity");
+  static_assert(kS % kPar == 0, "a stage always holds units of one parity");
   static constexpr int kXchgOff = kS * kStage;
   static constexpr int kRedOff = kXchgOff + kXchgBytes;
   static constexpr int kBarOff = kRedOff + kRedBytes;
@@ -174,7 +180,7 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 template <int MT, bool MX>
-__global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constant__ F16Params p) {
+__global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_constant__ F16Params p) {
   using S = VShape<MT>;
   constexpr int SL = S::kS;
   constexpr int NQ = S::kNQ;
@@ -208,11 +214,11 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kVConsumers / 2);   // the 8 warps of the stage's unit parity
+      mbar_init(&empty[s], 8);   // the 8 consumer warps of the stage's unit parity
       mbar_init(&meta_full[s], 1);
     }
     for (int q = 0; q < 4; ++q) {
-      mbar_init(&xfull[q], 3);
+      mbar_init(&xfull[q], 2 * S::kPar - 1);
       mbar_init(&xfree[q], 1);
       mbar_init(&red_full[q], csize > 1 ? csize - 1 : 1);
     }
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
       for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
         drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
     }
-  } else if (warp == kVMeta) {
+  } else if (warp == v_meta_warp(MT)) {
     // ---------------------------------------------------------------- INT4 row metadata
     // Each unit's 128 scales and zero-points, once per unit instead of once per consumer warp:
     // lane l converts rows 4l .. 4l+3 (bf16 scale -> fp32, u4 zero-point -> bf16x2 128 + z).
@@ -310,10 +316,10 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
   } else {
     // ---------------------------------------------------------------- consumers
     const int cw = warp - kVCons0;
-    const int par = cw >> 3;                 // units u0 + par, u0 + par + 2, ...
+    const int par = cw >> 3;                 // units u0 + par, u0 + par + kPar, ...
     const int pr = (cw >> 1) & 3;            // row pair: rows 32pr .. 32pr + 31
     const int cp = cw & 1;                   // 32-K chunks 2cp and 2cp + 1 of every unit
-    const int slot_id = cp + 2 * par;        // 0 reads the other three at a segment end
+    const int slot_id = cp + 2 * par;        // 0 reads the others of its row pair at a segment end
     const int g = lane >> 2, t = lane & 3;
     // fragment rows: tile j (0, 1) of the pair, rows g and g + 8 of the tile
     int rows[2][2];
@@ -338,7 +344,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
     // add the other three warps' sums of the row pair, then write Y or hand off.
     auto finish = [&](int tile, int seg_kb1, bool first) -> bool {
       const uint32_t ph_x = static_cast<uint32_t>(seg_count) & 1u;
-      float* xb = xchg + (static_cast<size_t>(pr) * 3 * 32 + lane) * S::kXchgFloats;
+      float* xb = xchg + (static_cast<size_t>(pr) * (2 * S::kPar - 1) * 32 + lane) * S::kXchgFloats;
       if (slot_id != 0) {
         // wait until the reader has taken the previous segment's values, then store ours
         if (seg_count > 0 && !mbar_wait(&xfree[pr], ph_x ^ 1u, wc)) return false;
@@ -362,7 +368,10 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int f = (j * NQ + q) * 4 + e;
-            v[j][q][e] = ((yacc[j][q][e] + xb[f]) + xb[32 * S::kXchgFloats + f]) + xb[64 * S::kXchgFloats + f];
+            float a = yacc[j][q][e];
+#pragma unroll
+            for (int o = 0; o < 2 * S::kPar - 1; ++o) a += xb[o * 32 * S::kXchgFloats + f];
+            v[j][q][e] = a;
           }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xfree[pr]);
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
 #pragma unroll
           for (int e = 0; e < 4; ++e) yacc[j][q][e] = 0.f;
       bool ok = true;
-      for (; i < seg_end; i += 2) {
+      for (; i < seg_end; i += S::kPar) {
         if (!mbar_wait(&full[s], ph, wc) || (!MX && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
         const uint32_t base = smem0 + s * S::kStage;
         uint32_t bx[NQ][2][4];
@@ -570,7 +579,7 @@ __global__ void __launch_bounds__(kVThreads, 1) gemv_kernel(const __grid_constan
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        s += 2;
+        s += S::kPar;
         if (s >= SL) { s -= SL; ph ^= 1u; }
       }
       if (!ok) break;
@@ -614,7 +623,7 @@ cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   if (!clusters_on) cs = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(static_cast<unsigned>(kVThreads));
+  cfg.blockDim = dim3(static_cast<unsigned>(v_threads(MT)));
   cfg.dynamicSmemBytes = static_cast<size_t>(S::kSmem);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -634,7 +643,7 @@ cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   }
   if (cs > 1 && (cluster_max[dev][cs] - 1) * cs < grid) cs = 1;   // not all clusters fit at once
   p.cluster = cs;
-  if (cs <= 1) return launch_pdl(kern, grid, kVThreads, S::kSmem, st, p);
+  if (cs <= 1) return launch_pdl(kern, grid, v_threads(MT), S::kSmem, st, p);
   static const bool pdl = [] {
     const char* v = std::getenv("HM_PDL");
     return !(v && v[0] == '0');
@@ -648,15 +657,21 @@ cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
 
 }  // namespace
 
-int gemv_tokens(int64_t m) { return m <= 8 ? 8 : 16; }
+int gemv_tokens(int64_t m) { return m <= 8 ? 8 : (m <= 16 ? 16 : 32); }
 
-int gemv_stages(int64_t m) { return gemv_tokens(m) == 8 ? VShape<8>::kS : VShape<16>::kS; }
+int gemv_stages(int64_t m) {
+  const int t = gemv_tokens(m);
+  return t == 8 ? VShape<8>::kS : (t == 16 ? VShape<16>::kS : VShape<32>::kS);
+}
 
 cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
   if (p.m < 1 || p.m > kGemvMaxTokens) return cudaErrorInvalidValue;
   const bool mx = p.fmt == kW4A16Mx;
-  if (gemv_tokens(p.m) == 8) return mx ? launch_v<8, true>(p, st) : launch_v<8, false>(p, st);
-  return mx ? launch_v<16, true>(p, st) : launch_v<16, false>(p, st);
+  switch (gemv_tokens(p.m)) {
+    case 8: return mx ? launch_v<8, true>(p, st) : launch_v<8, false>(p, st);
+    case 16: return mx ? launch_v<16, true>(p, st) : launch_v<16, false>(p, st);
+  }
+  return mx ? launch_v<32, true>(p, st) : launch_v<32, false>(p, st);
 }
 
 }  // namespace hm

@@ -100,7 +100,7 @@ int mx_stages(int fmt, int tile_m);
 // W4A16 kernel for decode-sized M (hm_gemv.cu): INT4 or MXFP4 weights, up to 16 tokens, warp-level
 // bf16 MMA on registers, split over the packed units with a last-arriver hand-off of shared tiles.
 // X comes as tmap_x, a 2-D map with box {128, gemv_tokens(M)} and no swizzle.
-constexpr int kGemvMaxTokens = 16;
+constexpr int kGemvMaxTokens = 32;
 constexpr int kGemvCounters = 8;   // arrival counters per output tile (one per consumer warp)
 cudaError_t launch_gemv(const F16Params& p, cudaStream_t st);
 int gemv_tokens(int64_t m);

@@ -74,8 +74,8 @@ def test_plan_buckets(hm):
         p = hm.plan(1, m, 4096, 4096, 152)
         seen[m] = p
         assert p["tile_n"] == 128 and p["tile_k"] == 128
-        if m <= 16:   # decode-sized M: the warp-MMA decode kernel, built for 8 or 16 tokens
-            assert p["kernel"] == 1 and p["tile_m"] in (8, 16) and p["tile_m"] >= m
+        if m <= 32:   # decode-sized M: the warp-MMA decode kernel, built for 8, 16 or 32 tokens
+            assert p["kernel"] == 1 and p["tile_m"] in (8, 16, 32) and p["tile_m"] >= m
         else:
             assert p["kernel"] == 0 and p["tile_m"] >= min(m, 16) and p["tile_m"] in (16, 32, 64, 128, 256)
         assert 1 <= p["grid"] <= 152
@@ -160,13 +160,20 @@ def test_oversized_schedule_rejected(hm):
 
 
 def test_plan_decode_kernel(hm, monkeypatch):
-    """W4A16 formats at M <= 16 take the warp-MMA decode kernel (built for 8 or 16 tokens); the
-    block-scaled formats and M > 16 keep tcgen05; HM_GEMV=0 keeps tcgen05 for every M."""
+    """W4A16 formats at M <= 32 take the warp-MMA decode kernel (built for 8, 16 or 32 tokens);
+    the block-scaled formats and M > 32 keep tcgen05; HM_GEMV=0 keeps tcgen05 for every M."""
     for fmt in (1, 2):
-        tiles = [hm.plan(fmt, m, 4096, 4096, 152)["tile_m"] for m in range(1, 17)]
-        assert tiles == [8] * 8 + [16] * 8
-        assert all(hm.plan(fmt, m, 4096, 4096, 152)["kernel"] == 1 for m in range(1, 17))
-        assert hm.plan(fmt, 17, 4096, 4096, 152)["kernel"] == 0
+        tiles = [hm.plan(fmt, m, 4096, 4096, 152)["tile_m"] for m in range(1, 33)]
+        assert tiles == [8] * 8 + [16] * 8 + [32] * 16
+        assert all(hm.plan(fmt, m, 4096, 4096, 152)["kernel"] == 1 for m in range(1, 33))
+        assert hm.plan(fmt, 33, 4096, 4096, 152)["kernel"] == 0
+    # 17..32 tokens on the 14336-wide layer: 112 whole tiles for tcgen05, which INT4 keeps;
+    # MXFP4 always takes the decode kernel up to 32 tokens
+    assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 0
+    assert hm.plan(1, 16, 14336, 4096, 152)["kernel"] == 1
+    assert hm.plan(2, 32, 14336, 4096, 152)["kernel"] == 1
+    monkeypatch.setenv("HM_GEMV", "2")
+    assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 1
     for fmt in (3, 4):
         assert hm.plan(fmt, 1, 4096, 4096, 152)["kernel"] == 0
     # 152 tiles of two 128-K blocks on 152 SMs: one whole tile per CTA, no split
@@ -187,7 +194,8 @@ def test_plan_decode_kernel(hm, monkeypatch):
 
 
 def test_workspace_holds_decode_counters(hm):
-    """The decode kernel keeps 8 arrival counters per 128-row tile and 2 x 16 x 128 fp32 partials
-    per CTA; the workspace for M <= 16 has room for both on any device up to the sizing limit."""
+    """The decode kernel keeps 8 arrival counters per 128-row tile and tokens x 128 fp32 partials
+    per CTA; the workspace for M <= 32 has room for both on any device up to the sizing limit."""
     n, k = 19456, 4096
-    assert hm.workspace_size(1, 16, n, k) >= (n // 128) * 8 * 4 + 148 * 2 * 16 * 128 * 4
+    for m in (16, 32):
+        assert hm.workspace_size(1, m, n, k) >= (n // 128) * 8 * 4 + 148 * m * 128 * 4

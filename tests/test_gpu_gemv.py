@@ -1,4 +1,4 @@
-"""GPU parity of the warp-MMA W4A16 kernel for decode-sized M (1..16 tokens), through the C ABI,
+"""GPU parity of the warp-MMA W4A16 kernel for decode-sized M (1..32 tokens), through the C ABI,
 against the fp64 oracle with the tolerance |Y - Yref| <= 1e-2*|Yref| + 1e-2*rms(Yref).
 
 The kernel splits the packed 128x128 units over the CTAs; the shapes below cover tiles shared by
@@ -46,10 +46,19 @@ def quantized(hm, fmt, n, k, has_zero, seed):
 def check(hm, fmt, m, n, k, has_zero, seed):
     qw, packed = quantized(hm, fmt, n, k, has_zero, seed)
     x = synth.activations(m, k, seed=seed + 2)
-    p = hm.plan(fmt, m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert p["kernel"] == 1 and p["tile_m"] >= m
-    y = hm.gemm(fmt, x.cuda(), packed, n, k)
-    torch.cuda.synchronize()
+    # INT4 at 17..32 tokens takes the decode kernel only where tcgen05 would split tiles; force it
+    saved = os.environ.get("HM_GEMV")
+    os.environ["HM_GEMV"] = "2"
+    try:
+        p = hm.plan(fmt, m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)
+        assert p["kernel"] == 1 and p["tile_m"] >= m
+        y = hm.gemm(fmt, x.cuda(), packed, n, k)
+        torch.cuda.synchronize()
+    finally:
+        if saved is None:
+            del os.environ["HM_GEMV"]
+        else:
+            os.environ["HM_GEMV"] = saved
     assert_close(y, og.gemm(bf16_np(x), qw.what), f"fmt={fmt} m={m} n={n} k={k} zp={has_zero}")
     assert hm.device_error() == 0
     return p
@@ -61,26 +70,26 @@ def check(hm, fmt, m, n, k, has_zero, seed):
 SHAPES = [(640, 3072), (200, 128), (19456, 256), (4096, 4096), (256, 14336), (8192, 1024), (5120, 1024)]
 
 
-@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 15, 16])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 15, 16, 17, 24, 31, 32])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_int4_zero_point(hm, m, n, k):
     check(hm, 1, m, n, k, True, seed=100 + m)
 
 
-@pytest.mark.parametrize("m", [1, 3, 8, 11, 16])
+@pytest.mark.parametrize("m", [1, 3, 8, 11, 16, 20, 32])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_int4_symmetric(hm, m, n, k):
     check(hm, 1, m, n, k, False, seed=200 + m)
 
 
-@pytest.mark.parametrize("m", [1, 2, 4, 6, 8, 10, 16])
+@pytest.mark.parametrize("m", [1, 2, 4, 6, 8, 10, 16, 25, 32])
 @pytest.mark.parametrize("n,k", SHAPES)
 def test_mxfp4(hm, m, n, k):
     check(hm, 2, m, n, k, False, seed=300 + m)
 
 
 @pytest.mark.parametrize("log2_gain", [-100, 14])
-@pytest.mark.parametrize("m", [1, 5, 13])
+@pytest.mark.parametrize("m", [1, 5, 13, 29])
 def test_mxfp4_extreme_scales(hm, m, log2_gain):
     """E8M0 exponents above 128 take the fp32 restore, tiny ones bf16 subnormal codes."""
     n, k = 256, 512
@@ -96,7 +105,7 @@ def test_mxfp4_extreme_scales(hm, m, log2_gain):
     assert hm.device_error() == 0
 
 
-@pytest.mark.parametrize("m", [1, 8, 16])
+@pytest.mark.parametrize("m", [1, 8, 16, 32])
 def test_deterministic_and_workspace_reuse(hm, m):
     """The last-arriver hand-off sums partials in CTA order and clears its counters: repeated calls
     on one workspace, and a fresh workspace, give bit-identical outputs."""
@@ -113,9 +122,9 @@ def test_deterministic_and_workspace_reuse(hm, m):
     assert hm.device_error() == 0
 
 
-@pytest.mark.parametrize("m", [1, 3, 8, 16])
+@pytest.mark.parametrize("m", [1, 3, 8, 16, 32])
 def test_tensor_core_path_still_matches(hm, env, m):
-    """HM_GEMV=0 keeps the tcgen05 kernels for M <= 16: both paths agree with the oracle."""
+    """HM_GEMV=0 keeps the tcgen05 kernels for M <= 32: both paths agree with the oracle."""
     n, k = 640, 3072
     qw, packed = quantized(hm, 1, n, k, True, seed=500 + m)
     x = synth.activations(m, k, seed=501)
@@ -133,7 +142,7 @@ def test_tensor_core_path_still_matches(hm, env, m):
 
 
 def test_full_size_sampled(hm):
-    """The 14336 x 4096 layer at M = 1, 8 and 16, checked on sampled outputs."""
+    """The 14336 x 4096 layer at M = 1, 8, 16 and 32, checked on sampled outputs."""
     n, k = 14336, 4096
     w = synth.weights(n, k, seed=1)
     z = synth.zero_points(n, k // 128, seed=2)
@@ -143,7 +152,7 @@ def test_full_size_sampled(hm):
     packed = hm.transform(d, torch.from_numpy(pack_nibbles(q)).cuda(), to_bf16(s).cuda(),
                           torch.from_numpy(z).cuda())
     rng = np.random.default_rng(0)
-    for m in (1, 8, 16):
+    for m in (1, 8, 16, 32):
         x = synth.activations(m, k, seed=3)
         y = hm.gemm(1, x.cuda(), packed, n, k)
         torch.cuda.synchronize()
@@ -157,7 +166,7 @@ def test_full_size_sampled(hm):
     assert hm.device_error() == 0
 
 
-@pytest.mark.parametrize("n,k,m", [(4096, 4096, 1), (8192, 1024, 8), (5120, 1024, 16), (4096, 14336, 3)])
+@pytest.mark.parametrize("n,k,m", [(4096, 4096, 1), (8192, 1024, 8), (5120, 1024, 16), (4096, 14336, 3), (4096, 4096, 32)])
 def test_cluster_and_global_handoff_agree(hm, n, k, m):
     """Tiles cut into 2-4 K ranges are summed through a thread-block cluster's shared memory, or
     (HM_GEMV_CLUSTER=0, read once per process: run in a child) through global memory; both add the
