@@ -158,7 +158,11 @@ size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
  *                  when x_scale is NULL, x = bf16 [M][K] quantized internally.
  *                  Y = gX*gW*sum(blocks) sbX*sbW*sum e2m1X*e2m1W.
  * M >= 0 (M = 0 is a no-op), N and K must match the packed header (checked on the device).
- * x must be 16-byte aligned, packed 256-byte aligned. ws: hm_workspace_size bytes. */
+ * x must be 16-byte aligned, packed 256-byte aligned. ws: hm_workspace_size bytes.
+ * Kernel per call (hm_plan reports it): tcgen05 tensor-core kernels, except the W4A16 formats at
+ * decode sizes (M <= 16; 17..32 with MXFP4, or with INT4 where tcgen05 would split tiles along K),
+ * which run on warp-level bf16 MMA with fp32 accumulation. Output tiles split along K are summed
+ * in a fixed order, so a call is deterministic. */
 hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* x_global,
                   const void* packed, void* y, int64_t M, int64_t N, int64_t K, void* ws,
                   size_t ws_bytes, void* stream);
@@ -199,16 +203,17 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
  * Host-only, no CUDA call. */
 typedef struct hm_plan_info {
   int32_t bucket;      /* M bucket index: 0: M<=16, 1: <=64, 2: <=256, 3: <=1024, 4: >1024 */
-  int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension); CUDA-core kernel: tokens
-                          it is instantiated for (1, 2, 4 or 8, >= M) */
+  int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension); decode kernel: tokens it
+                          is instantiated for (8, 16 or 32, >= M) */
   int32_t tile_n;      /* weight rows per tile (tcgen05 MMA M dimension, 128) */
   int32_t tile_k;      /* K per pipeline stage */
   int32_t stages;      /* load-pipeline depth */
   int32_t stream_k;    /* 1 if the K loop is split across CTAs (stream-K) */
   int32_t grid;        /* CTAs launched */
   int32_t tiles;       /* output tiles */
-  int32_t kernel;      /* 0: tcgen05 tensor-core kernel; 1: CUDA-core kernel for decode-sized M
-                          (W4A16 formats, M <= 8: a matrix-vector product bound by HBM) */
+  int32_t kernel;      /* 0: tcgen05 tensor-core kernel; 1: decode kernel (W4A16 formats; warp-level
+                          bf16 MMA with fp32 accumulation in registers) for M <= 16, and for
+                          17 <= M <= 32 with MXFP4 or where tcgen05 would split tiles along K */
 } hm_plan_info;
 hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
                   hm_plan_info* out);

@@ -1,10 +1,10 @@
-// W4A16 GEMM for decode-sized M (up to 16 tokens): Y[M,N] = X[M,K] * dequant(W)^T, with
+// W4A16 GEMM for decode-sized M (up to 32 tokens): Y[M,N] = X[M,K] * dequant(W)^T, with
 // warp-level bf16 MMA (mma.sync m16n8k16, fp32 accumulation) as the multiply engine.
 //
 // Same product and restore rule as the tcgen05 W4A16 kernels (the explainer page "vLLM
 // Humming은 4비트를 어떻게 계산하나", sections "4비트 값에는 스케일이라는 해석 규칙이 붙는다" and
-// "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다"). With at most 16 tokens every weight byte
-// feeds at most 32 multiply-adds: the product is bound by streaming the packed weights from HBM,
+// "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다"). With at most 32 tokens every weight byte
+// feeds at most 64 multiply-adds: the product is bound by streaming the packed weights from HBM,
 // and what limits a kernel is the work per weight on the SM (dequant, operand staging, hand-offs
 // between roles), not MMA throughput. The tcgen05 path spends that on restoring weights into
 // TMEM, single-thread MMA issue and accumulator hand-offs per 128-K block; here each warp restores
@@ -12,14 +12,18 @@
 // registers, so the only hand-off per unit is the shared-memory stage itself.
 //
 //  * Work: the packed 128x128 units (n-tile major: unit u is tile u / kb, k-block u % kb) are cut
-//    into one contiguous range per CTA, start(c) = floor(c * U / G), G = min(U, SMs). A range may
-//    cover the tail of one tile, whole tiles and the head of another.
-//  * Roles (persistent CTA per SM): one producer lane loads each unit with a bulk copy and the
-//    activation block X[0:MT, k-block] with one 2-D TMA load (token rows past M read as zeros) into
-//    a ring of stages; 16 consumer warps, warp (p, c, r) taking rows 32p..32p+31 (two 16-row MMA
-//    tiles), the 32-K chunks 2c, 2c+1, and the units of parity r (every other unit, so that four
-//    warps per SM sub-partition hide each other's load and MMA latencies). The walk over units,
-//    slots and phases advances by counting (no division per unit).
+//    into one contiguous range per CTA, start(c) = floor(c * U / G). The planner takes G = tiles x
+//    floor(SMs / tiles) when tiles <= SMs (every CTA then holds one K range of one tile), else
+//    G = SMs (a range may cover the tail of one tile, whole tiles and the head of another).
+//  * Roles (persistent CTA per SM): a producer warp loads each unit with a bulk copy (the first
+//    stages from one lane each) and the activation block X[0:MT, k-block] with one 2-D TMA load
+//    (token rows past M read as zeros) into a ring of stages; consumer warp (p, c, r) takes rows
+//    32p..32p+31 (two 16-row MMA tiles) and the 32-K chunks 2c, 2c+1 of the units of parity r: for
+//    up to 16 tokens two parities take alternate units (16 consumer warps, four per SM
+//    sub-partition, hiding each other's load and MMA latencies), for 32 tokens one parity (8 warps,
+//    each holding four token groups of sums). An INT4 metadata warp turns each unit's 128 scales
+//    and zero-points into fp32 scales and bf16x2 (128 + z) pairs once. The walk over units, slots
+//    and phases advances by counting (no division per unit).
 //  * Fragments: for m16n8k16, lane (g = lane/4, t = lane%4) holds A pairs at MMA k-slots
 //    {2t, 2t+1} and {2t+8, 2t+9}, B pairs at the same slots for token g. A contraction may number
 //    its k in any order as long as A and B agree, so lane t takes the 32-bit code word t of its
@@ -31,7 +35,7 @@
 //    and the group scale multiplies that sum (s * sum (u - z) x, as in the small-token tcgen05
 //    kernel). MXFP4: the word is restored with its E8M0 scale (exact) and the MMAs accumulate
 //    straight into the running sums.
-//  * Segment end: the four warps of a row pair add their sums in a fixed order through shared
+//  * Segment end: the warps of a row pair (two or four) add their sums in a fixed order through shared
 //    memory (mbarrier hand-off, bounded); every warp closes every segment of its CTA's range, even
 //    one that holds no unit of its parity. A tile owned whole by the CTA is written to Y. A tile
 //    shared by several CTAs has a fixed owner, the CTA holding its first k-block: it reaches the
