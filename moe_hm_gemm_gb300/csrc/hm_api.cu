@@ -270,6 +270,12 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   const int64_t total = p.tiles * p.kb_total;
   const int64_t units = p.stream_k ? total : p.tiles;
   p.grid = static_cast<int>(units < ctas ? units : ctas);
+  // Stream-K with no more tiles than CTAs: cut every tile into the same number of K ranges, one
+  // per CTA, instead of ranges that run across tile boundaries (HM_SK_ALIGN=0 keeps the latter)
+  if (p.stream_k && p.tiles <= ctas && env_int("HM_SK_ALIGN", 1) != 0) {
+    const int64_t per = std::min<int64_t>(ctas / p.tiles, p.kb_total);
+    p.grid = static_cast<int>(p.tiles * per);
+  }
   if (p.grid < 1) p.grid = 1;
   return p;
 }

@@ -123,17 +123,17 @@ def test_plan_block_scaled_two_ctas_per_sm(hm):
         assert big["stream_k"] == 0 and big["grid"] == 2 * 152 and big["tile_m"] == 128
         mid = hm.plan(fmt, 1024, 8192, 8192, 152)          # 8 x 64 = 512 tiles: tile-parallel
         assert mid["stream_k"] == 0 and mid["grid"] == 2 * 152
-        tiny = hm.plan(fmt, 16, 8192, 8192, 152)           # 64 tiles of 16 tokens: stream-K
-        assert tiny["stream_k"] == 1 and tiny["grid"] == 2 * 152 and tiny["tile_m"] == 16
+        tiny = hm.plan(fmt, 16, 8192, 8192, 152)           # 64 tiles of 16 tokens: stream-K,
+        assert tiny["stream_k"] == 1 and tiny["grid"] == 64 * 4 and tiny["tile_m"] == 16   # 4 K ranges each
     # W4A8 at M = 128: the widest tile giving >= 1.4x SMs tiles (32 tokens: 4 x 64 = 256 tiles)
     p = hm.plan(3, 128, 8192, 8192, 152)
     assert p["tile_m"] == 32 and p["stream_k"] == 0 and p["grid"] == 256
     # W4A4 keeps 128-token tiles (its activation scale atoms hold 128 rows), tile-parallel
     p = hm.plan(4, 128, 8192, 8192, 152)
     assert p["tile_m"] == 128 and p["stream_k"] == 0 and p["grid"] == 64
-    # too few tiles even at 32 tokens: stream-K, one CTA per SM
+    # too few tiles even at 32 tokens: stream-K, one CTA per SM (112 tiles: one K range each)
     p = hm.plan(3, 64, 7168, 7168, 152)
-    assert p["tile_m"] == 32 and p["stream_k"] == 1 and p["grid"] == 152
+    assert p["tile_m"] == 32 and p["stream_k"] == 1 and p["grid"] == 112
     # W4A16 keeps one CTA per SM
     assert hm.plan(1, 8192, 8192, 8192, 152)["grid"] == 152
     # stream-K partials are sized for the widest grid the planner can choose
@@ -199,3 +199,15 @@ def test_workspace_holds_decode_counters(hm):
     n, k = 19456, 4096
     for m in (16, 32):
         assert hm.workspace_size(1, m, n, k) >= (n // 128) * 8 * 4 + 148 * m * 128 * 4
+
+
+def test_plan_stream_k_equal_ranges(hm, monkeypatch):
+    """tcgen05 stream-K with no more tiles than CTAs cuts every tile into the same number of K
+    ranges (one per CTA); HM_SK_ALIGN=0 keeps ranges that run across tile boundaries."""
+    p = hm.plan(3, 1, 7168, 7168, 152)              # 56 tiles, 304 CTA slots: 5 ranges per tile
+    assert (p["stream_k"], p["grid"]) == (1, 280)
+    p = hm.plan(1, 64, 4096, 4096, 152)             # 64 tiles of 32 tokens: 2 ranges per tile
+    assert (p["tile_m"], p["stream_k"], p["grid"]) == (32, 1, 128)
+    monkeypatch.setenv("HM_SK_ALIGN", "0")
+    assert hm.plan(3, 1, 7168, 7168, 152)["grid"] == 304
+    assert hm.plan(1, 64, 4096, 4096, 152)["grid"] == 152
