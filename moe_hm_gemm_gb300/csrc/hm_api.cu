@@ -155,7 +155,9 @@ MxChoice mx_choice(int32_t fmt, int64_t m, int64_t n, int num_sms) {
 // per CTA x c(tile), where a 128-K block costs c = 0.47 / 0.55 / 0.85 / 1.3 us for tiles of
 // 32 / 64 / 128 / 256 tokens, a tile-parallel CTA runs ceil(tiles / SMs) x kb blocks, and a
 // stream-K CTA runs ceil(tiles x kb / SMs) blocks plus a hand-off cost of 15 / 18 / 35 / 60
-// blocks. Narrow tiles stream weights faster per block; wide tiles do more tokens per block.
+// blocks. Narrow tiles stream weights faster per block; wide tiles do more tokens per block. (The
+// costs were fitted with stream-K ranges running across tile boundaries; with the equal K ranges
+// per tile used now the chosen configurations measured the same or up to 8 % faster.)
 struct F16Choice {
   int tile_m;
   bool stream_k;
