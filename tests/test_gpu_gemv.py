@@ -66,8 +66,11 @@ def check(hm, fmt, m, n, k, has_zero, seed):
 
 # (n, k): 5 tiles each cut into 24 K ranges (global hand-off) | 2 units, no split, ragged N |
 # 152 tiles of 2 blocks: one whole tile per CTA | 32 tiles cut into 4 ranges (clusters of 4) |
-# 2 tiles x 112 blocks cut into 76 ranges | 64 tiles cut in 2 (clusters of 2) | 40 tiles cut in 3
-SHAPES = [(640, 3072), (200, 128), (19456, 256), (4096, 4096), (256, 14336), (8192, 1024), (5120, 1024)]
+# 2 tiles x 112 blocks cut into 76 ranges | 64 tiles cut in 2 (clusters of 2) | 40 tiles cut in 3 |
+# 160 tiles > 152 SMs: ranges of ~8.4 units run across tiles (a CTA publishes one shared tile and
+# owns another, several segment ends per CTA)
+SHAPES = [(640, 3072), (200, 128), (19456, 256), (4096, 4096), (256, 14336), (8192, 1024), (5120, 1024),
+          (20480, 1024)]
 
 
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 15, 16, 17, 24, 31, 32])
