@@ -211,3 +211,25 @@ def test_plan_stream_k_equal_ranges(hm, monkeypatch):
     monkeypatch.setenv("HM_SK_ALIGN", "0")
     assert hm.plan(3, 1, 7168, 7168, 152)["grid"] == 304
     assert hm.plan(1, 64, 4096, 4096, 152)["grid"] == 152
+
+
+def test_workspace_covers_every_plan(hm):
+    """For any device up to the sizing limit, the workspace hm_workspace_size asks for holds the
+    split partials and arrival counters of the plan hm_plan chooses (decode kernel: grid x tokens x
+    128 fp32 partials and 8 counters per tile; tcgen05, including the block-scaled kernels' two CTAs
+    per SM: grid x 2 x tile_m x 128 and 4 per tile)."""
+    import random
+    rng = random.Random(7)
+    shapes = [(1, m, n, k) for m in (1, 8, 16, 17, 32, 33, 64, 200) for n, k in ((4096, 4096), (20480, 1024), (200, 128))]
+    for _ in range(80):
+        fmt = rng.choice((1, 2, 3, 4))
+        shapes.append((fmt, rng.randint(1, 300), 128 * rng.randint(1, 200) - rng.choice((0, 2, 64)), 256 * rng.randint(1, 30)))
+    for fmt, m, n, k in shapes:
+        ws = hm.workspace_size(fmt, m, n, k)
+        for sms in (1, 2, 7, 64, 148, 152, 160, 256):
+            p = hm.plan(fmt, m, n, k, sms)
+            if p["kernel"] == 1:
+                need = p["grid"] * p["tile_m"] * 128 * 4 + p["tiles"] * 8 * 4
+            else:
+                need = (p["grid"] * 2 * p["tile_m"] * 128 * 4 if p["stream_k"] else 0) + p["tiles"] * 4 * 4
+            assert ws >= need, (fmt, m, n, k, sms, p, ws, need)
