@@ -20,7 +20,7 @@ def hm():
     return mod
 
 
-def moe_case(hm, fmt, counts, n, k, has_zero=False, seed=0):
+def moe_case(hm, fmt, counts, n, k, has_zero=False, seed=0, gain=1.0):
     e = len(counts)
     offsets = np.zeros(e + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
@@ -28,7 +28,7 @@ def moe_case(hm, fmt, counts, n, k, has_zero=False, seed=0):
     qws, packs = [], []
     for i in range(e):
         z = synth.zero_points(n, k // 128, seed=seed + 100 + i) if has_zero else None
-        qw = QuantWeight(fmt, synth.weights(n, k, seed=seed + i), z)
+        qw = QuantWeight(fmt, synth.weights(n, k, seed=seed + i) * np.float32(gain), z)
         qws.append(qw)
         packs.append(qw.transform(hm)[1])
     ptrs = torch.tensor([p.data_ptr() for p in packs], dtype=torch.int64, device="cuda")
@@ -76,13 +76,24 @@ def test_bad_offsets_set_device_error(hm):
     assert hm.device_error() & 4
 
 
+@pytest.mark.parametrize("fmt", [1, 2])
 @pytest.mark.parametrize("small", ["0", "1"])
-def test_small_tiles_both_kernels(hm, small, monkeypatch):
+def test_small_tiles_both_kernels(hm, fmt, small, monkeypatch):
+    """Token tiles of 16 and 32: INT4 runs the small-token kernel (the general kernel with
+    HM_F16_SMALL=0), MXFP4 the general kernel (its restore is heavier than the small-token kernel's
+    dequant warps keep up with: measured slower there)."""
     monkeypatch.setenv("HM_F16_SMALL", small)
     monkeypatch.setenv("HM_MOE_TILE_M", "16")
-    moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=True, seed=11)
+    moe_case(hm, fmt, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=(fmt == 1), seed=11)
     monkeypatch.setenv("HM_MOE_TILE_M", "32")
-    moe_case(hm, 1, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=False, seed=12)
+    moe_case(hm, fmt, [3, 0, 17, 40, 1, 0, 9], 256, 1024, has_zero=False, seed=12)
+
+
+@pytest.mark.parametrize("tile", ["16", "32"])
+def test_small_tiles_mxfp4_large_scales(hm, tile, monkeypatch):
+    """MXFP4 blocks with E8M0 exponents above 128 (fp32 restore) at token tiles of 16 and 32."""
+    monkeypatch.setenv("HM_MOE_TILE_M", tile)
+    moe_case(hm, 2, [5, 0, 12, 30], 256, 512, seed=31, gain=2.0 ** 14)
 
 
 @pytest.mark.parametrize("fmt", [1, 2])
