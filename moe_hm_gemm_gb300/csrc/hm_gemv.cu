@@ -342,11 +342,10 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
 
     float yacc[2][NQ][4];   // [tile][token group][c0..c3]: rows g / g+8 x tokens 2t, 2t+1
     int seg_kb0 = kb0, seg_count = 0;
-    bool first_seg = true;
 
     // The segment [seg_kb0, seg_kb1) of `tile` is complete in yacc (this warp's units and chunks):
-    // add the other three warps' sums of the row pair, then write Y or hand off.
-    auto finish = [&](int tile, int seg_kb1, bool first) -> bool {
+    // add the sums of the row pair's other warps (one or three), then write Y or hand off.
+    auto finish = [&](int tile, int seg_kb1) -> bool {
       const uint32_t ph_x = static_cast<uint32_t>(seg_count) & 1u;
       float* xb = xchg + (static_cast<size_t>(pr) * (2 * S::kPar - 1) * 32 + lane) * S::kXchgFloats;
       if (slot_id != 0) {
@@ -451,7 +450,6 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
         if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
         return true;
       }
-      (void)first;
       if (!sk_wait(ctr, static_cast<uint32_t>(c_hi - c_lo), wc)) return false;
       // own values first, then the other contributors in CTA order, CU of them in flight at a time
       constexpr int CU = NQ == 1 ? 4 : 2;
@@ -588,8 +586,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
       }
       if (!ok) break;
       // every warp closes every segment, even one without a unit of its parity
-      if (!finish(tile, seg_kb0 + (seg_end - seg_begin), first_seg)) break;
-      first_seg = false;
+      if (!finish(tile, seg_kb0 + (seg_end - seg_begin))) break;
       ++seg_count;
       seg_kb0 = 0;
     }
