@@ -229,6 +229,30 @@ def moe_points(hm, synth, fmt, quick):
     return points
 
 
+def silu_points(hm, synth, quick):
+    """MoE expert activation on the gate-up output of the MoE layers above: rows = 8 T,
+    gate | up of 2 x 2048 columns in, 2048 out; inputs rotated over copies covering 4x L2."""
+    inter = 2048
+    tokens = [16, 256, 4096, 16384] if not quick else [16, 4096]
+    points = []
+    for t in tokens:
+        rows = 8 * t
+        gu = synth.device_activations(rows, 2 * inter, seed=40000 + t)
+        h = torch.empty((rows, inter), dtype=torch.bfloat16, device="cuda")
+        in_bytes, out_bytes = rows * 2 * inter * 2, rows * inter * 2
+        # ~4 fp32 operations for SiLU and one multiply per output (no tensor-core work)
+        p = Point(f"moe silu_mul T={t}", 0, rows, inter, 2 * inter, 5.0 * rows * inter, 0, in_bytes, out_bytes,
+                  "kind::f16", 1)
+        copies = [gu] + [gu.clone() for _ in range(rotations(in_bytes) - 1)]
+        for c in copies:
+            p.calls.append(lambda c=c, h=h: hm.silu_mul(c, inter, out=h))
+        p.e2e = (gu.cpu().pin_memory(), gu, torch.empty((rows, inter), dtype=torch.bfloat16).pin_memory(), h,
+                 p.calls[0])
+        points.append(p)
+    torch.cuda.synchronize()
+    return points
+
+
 def build_points(args, hm, synth):
     pts = _build_points(args, hm, synth)
     if args.m:
@@ -256,6 +280,8 @@ def _build_points(args, hm, synth):
         return moe_points(hm, synth, hm.W4A16_INT4, args.quick)
     if w == "moe_mxfp4":
         return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick)
+    if w == "moe_silu_mul":
+        return silu_points(hm, synth, args.quick)
     raise SystemExit(f"unknown workload {w}")
 
 
@@ -269,6 +295,9 @@ WORKLOAD_NAMES = {
                  "T in {16,256,4096,16384}",
     "moe_mxfp4": "MoE grouped MXFP4-W4A16: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
                  "T in {16,256,4096,16384}",
+    "moe_silu_mul": "MoE expert activation h = SiLU(gate) * up between the grouped GEMMs: rows = 8 T, "
+                    "gate | up 2 x 2048 bf16 in, 2048 bf16 out, T in {16,256,4096,16384} (HBM-bound; "
+                    "value in TFLOP/s of ~5 operations per output, roofline in GB/s)",
 }
 
 
@@ -393,7 +422,8 @@ def run_ours(args, rank, world, local_rank):
                                        "kind::mxf4nvf4": "fp4"}[points[0].kind],
         "data": "synthetic (seeded, generated on the device)",
         "config": {"workload": WORKLOAD_NAMES[args.workload], "parallelism": f"replicas x{world}",
-                   "l2": "packed weights rotated over copies covering 4x L2 per shape"},
+                   "l2": ("gate-up inputs" if args.workload == "moe_silu_mul" else "packed weights")
+                         + " rotated over copies covering 4x L2 per shape"},
         "roofline": roofline, "gpu_launches": launches, "clocks": clocks, "device_error": err,
         "sweep": sweep,
     }
@@ -441,6 +471,12 @@ def oracle_sample(workload):
         x = synth.activations(m, k, seed=3).float().numpy().astype(np.float64)
         desc = f"oracle W4A16 INT4+zp dequant + fp64 GEMM, N=K=4096, M={m} rows"
         return desc, 2.0 * m * n * k, lambda: og.gemm_w4a16_int4(x, q, s, z)
+    if workload == "moe_silu_mul":
+        from oracle import act as oa
+        rows, inter = 4096, 2048
+        gu = synth.activations(rows, 2 * inter, seed=3).float().numpy().astype(np.float64)
+        return (f"oracle SiLU(gate) * up in fp64 + bf16 rounding, {rows} rows x {inter}", 5.0 * rows * inter,
+                lambda: oa.silu_mul(gu, inter))
     if workload == "w4a8":
         n, k, m = 7168, 7168, 64
         codes, e = oq.quant_mxfp4(synth.weights(n, k, seed=1))

@@ -140,6 +140,15 @@ size_t hm_act_workspace_size(int64_t M, int64_t K);
 hm_status hm_quant_act_nvfp4(const void* x, int64_t M, int64_t K, const float* g_in, void* xq,
                              void* xs, float* g_out, void* ws, size_t ws_bytes, void* stream);
 
+/* MoE expert activation between the gate-up and down grouped GEMMs:
+ * out[r][c] = bf16(SiLU(gate_up[r][c]) * gate_up[r][inter + c]), SiLU(v) = v / (1 + exp(-v))
+ * evaluated in fp32 and rounded once to bf16 (round to nearest even). gate_up: device bf16
+ * [rows][2*inter] (gate in the first half of each row, up in the second, as a gate-up GEMM with
+ * N = 2*inter writes them); out: device bf16 [rows][inter]. inter % 8 == 0; both pointers
+ * 16-byte aligned. rows = 0 is a no-op. Caller owns both buffers; nothing is allocated.
+ * Returns HM_ERR_INVALID_ARG for bad sizes or pointers, HM_ERR_CUDA for a launch failure. */
+hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inter, void* stream);
+
 /* ---------------------------------------------------------------- GEMM */
 
 /* Workspace bytes hm_gemm / hm_moe_gemm need for this problem (split-K partials and tile

@@ -11,6 +11,12 @@
 // Both are HBM-bound streaming kernels: each input byte is read once (twice for the
 // two-pass NVFP4 tensor scale) and the outputs are written once with 16-byte or 8-byte
 // stores.
+//
+// MoE expert activation between the grouped GEMMs (the MoE layer of the explainer page, MoE
+// paragraph of the section "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다"; the activation
+// itself is not printed on the pages, the usual gated SiLU is taken): h = bf16(SiLU(gate) * up)
+// with SiLU(v) = v / (1 + exp(-v)) in fp32 (evaluated as v * logistic(v) from exp(-|v|)), gate
+// the first and up the second half of each gate-up row. Streaming: 8 columns per thread and step (two 16-byte loads, one 16-byte store).
 #include <cuda_bf16.h>
 
 #include "hm_dequant.cuh"
@@ -200,10 +206,51 @@ __global__ void wait_probe_kernel(uint32_t* err, uint64_t timeout_ns) {
 
 int act_amax_blocks(int64_t, int64_t) { return kAmaxBlocks; }
 
+__global__ void __launch_bounds__(256) silu_mul_kernel(const __nv_bfloat16* __restrict__ gu,
+                                                       __nv_bfloat16* __restrict__ h, int64_t rows,
+                                                       int64_t inter) {
+  const int64_t per_row = inter / 8;
+  const int64_t total = rows * per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row, c8 = i - r * per_row;
+    const uint4* row = reinterpret_cast<const uint4*>(gu + r * 2 * inter);
+    const uint4 g4 = __ldcs(row + c8);
+    const uint4 u4 = __ldcs(row + per_row + c8);
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float g = __uint_as_float(hh ? (gw[q] & 0xFFFF0000u) : (gw[q] << 16));
+        const float u = __uint_as_float(hh ? (uw[q] & 0xFFFF0000u) : (uw[q] << 16));
+        // logistic(g) from e = exp(-|g|) in (0, 1]: no overflow for very negative gates
+        const float e = expf(-fabsf(g));
+        v[hh] = g * ((g >= 0.0f ? 1.0f : e) / (1.0f + e)) * u;
+      }
+      o[q] = pack_bf16x2_rn(v[0], v[1]);
+    }
+    __stcs(reinterpret_cast<uint4*>(h + r * inter) + c8, make_uint4(o[0], o[1], o[2], o[3]));
+  }
+}
+
 cudaError_t launch_act_fp8(const __nv_bfloat16* x, int64_t m, int64_t k, uint8_t* xq, float* s_tok,
                            cudaStream_t st) {
   if (m == 0) return cudaSuccess;
   act_fp8_kernel<<<static_cast<unsigned>(m), kFp8Threads, 0, st>>>(x, k, xq, s_tok);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul(const __nv_bfloat16* gu, __nv_bfloat16* h, int64_t rows, int64_t inter, int num_sms,
+                            cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t work = rows * (inter / 8);
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 blocks of 256 per SM, grid-stride
+  if (blocks > cap) blocks = cap;
+  silu_mul_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(gu, h, rows, inter);
   return cudaGetLastError();
 }
 

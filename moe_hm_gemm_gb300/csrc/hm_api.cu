@@ -462,6 +462,16 @@ hm_status hm_quant_act_fp8(const void* x, int64_t M, int64_t K, void* xq, float*
                                     static_cast<cudaStream_t>(stream)));
 }
 
+hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inter, void* stream) {
+  if (rows < 0 || inter <= 0 || inter % 8 != 0) return HM_ERR_INVALID_ARG;
+  if (rows == 0) return HM_OK;
+  if (gate_up == nullptr || out == nullptr || !aligned(gate_up, 16) || !aligned(out, 16)) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_silu_mul(static_cast<const __nv_bfloat16*>(gate_up), static_cast<__nv_bfloat16*>(out),
+                                     rows, inter, di.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 size_t hm_act_scale_size(int64_t M, int64_t K) {
   if (M < 0 || K <= 0 || K % 64 != 0) return 0;
   return static_cast<size_t>(ceil_div(M, 128)) * (K / 64) * kAtomBytes;

@@ -120,6 +120,9 @@ cudaError_t launch_act_fp8(const __nv_bfloat16* x, int64_t m, int64_t k, uint8_t
 cudaError_t launch_act_nvfp4(const __nv_bfloat16* x, int64_t m, int64_t k, const float* g_in,
                              uint8_t* xq, uint8_t* xs, float* g_out, float* ws, cudaStream_t st);
 int act_amax_blocks(int64_t m, int64_t k);
+// MoE expert activation: h[rows][inter] = bf16(SiLU(gate) * up) from gate_up[rows][2*inter].
+cudaError_t launch_silu_mul(const __nv_bfloat16* gu, __nv_bfloat16* h, int64_t rows, int64_t inter, int num_sms,
+                            cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace hm

@@ -47,6 +47,7 @@ def _load():
         "hm_transform": (I32, [D, P, P, P, P, P]),
         "hm_dequant": (I32, [D, P, P, P]),
         "hm_quant_act_fp8": (I32, [P, I64, I64, P, P, P]),
+        "hm_silu_mul": (I32, [P, P, I64, I64, P]),
         "hm_act_scale_size": (SZ, [I64, I64]),
         "hm_act_workspace_size": (SZ, [I64, I64]),
         "hm_quant_act_nvfp4": (I32, [P, I64, I64, P, P, P, P, P, SZ, P]),
@@ -141,6 +142,17 @@ def quant_act_fp8(x):
     s = torch.empty((m,), dtype=torch.float32, device=x.device)
     _check(_lib.hm_quant_act_fp8(_ptr(x), m, k, _ptr(xq), _ptr(s), _stream()), "hm_quant_act_fp8")
     return xq, s
+
+
+def silu_mul(gate_up, inter, out=None):
+    """bf16 [rows][2*inter] (gate | up) -> bf16 SiLU(gate) * up [rows][inter] (hm_silu_mul)."""
+    assert gate_up.dtype == torch.bfloat16 and gate_up.is_contiguous() and gate_up.shape[1] == 2 * inter
+    rows = gate_up.shape[0]
+    if out is None:
+        out = torch.empty((rows, inter), dtype=torch.bfloat16, device=gate_up.device)
+    assert out.dtype == torch.bfloat16 and out.is_contiguous() and tuple(out.shape) == (rows, inter)
+    _check(_lib.hm_silu_mul(_ptr(gate_up), _ptr(out), int(rows), int(inter), _stream()), "hm_silu_mul")
+    return out
 
 
 def quant_act_nvfp4(x, g_in=None):

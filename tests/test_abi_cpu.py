@@ -64,6 +64,12 @@ def test_invalid_arguments_fail_before_any_launch(hm):
     assert lib.hm_moe_gemm(3, P(16), P(16), 4, P(16), P(16), 8, 256, 512, None, 0, None) == 2
     assert lib.hm_moe_gemm(1, P(16), P(16), 0, P(16), P(16), 8, 256, 512, None, 0, None) == 1
     assert lib.hm_quant_act_fp8(P(16), 4, 100, P(16), P(16), None) == 1
+    # SiLU-mul: inter a multiple of 8, rows >= 0, aligned non-null buffers; rows = 0 is a no-op
+    assert lib.hm_silu_mul(P(16), P(16), 4, 12, None) == 1
+    assert lib.hm_silu_mul(P(16), P(16), -1, 16, None) == 1
+    assert lib.hm_silu_mul(None, P(16), 4, 16, None) == 1
+    assert lib.hm_silu_mul(P(18), P(16), 4, 16, None) == 1
+    assert lib.hm_silu_mul(None, None, 0, 16, None) == 0
     assert lib.hm_quant_act_nvfp4(P(16), 4, 96, None, P(16), P(16), P(16), None, 0, None) == 1
     assert lib.hm_quant_act_nvfp4(P(16), 4, 128, None, P(16), P(16), P(16), None, 0, None) == 3
 
