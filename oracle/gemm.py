@@ -34,6 +34,10 @@ def gemm_w4a16_mxfp4(x, codes, e):
     return gemm(x, quant.dequant_mxfp4(codes, e))
 
 
+def gemm_w4a16_mxint4(x, q, e):
+    return gemm(x, quant.dequant_mxint4(q, e))
+
+
 def gemm_w4a8_mxfp4(xq, s_tok, codes, e):
     """Y[m,n] = s_tok[m] * sum_k e4m3(xq[m,k]) * what[n,k] (per-token scale outside the sum)."""
     from .formats import decode_e4m3

@@ -13,9 +13,10 @@ Header (little endian): u32 magic 0x31574D48, u32 fmt, i64 N, i64 K, i64 N_pad, 
 u32 has_zero, f32 tensor_scale, u64 payload_bytes, zeros up to 256 bytes.
 
 Formats: 1 = W4A16 INT4 (group 128, bf16 scales, optional u4 zero-points),
-2 = W4A16 MXFP4 (e2m1 + E8M0/32, bf16 activations), 3 = W4A8 MXFP4, 4 = W4A4 NVFP4.
+2 = W4A16 MXFP4 (e2m1 + E8M0/32, bf16 activations), 3 = W4A8 MXFP4, 4 = W4A4 NVFP4,
+5 = W4A16 MXINT4 (signed int4 + E8M0/32, bf16 activations).
 
-Tiled payload (formats 1, 2): one "unit" per (n_tile of 128 rows, k_block of 128),
+Tiled payload (formats 1, 2, 5): one "unit" per (n_tile of 128 rows, k_block of 128),
 n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
   * nibble of (r, kk) lives in the 32-bit little-endian word at byte
     (kk//32)*2048 + r*16 + ((kk%32)//8)*4, at bit 4*((kk%8)//2) + 16*(kk%2);
@@ -23,14 +24,15 @@ n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
     row r at byte 8192 + 2r; zero-point of row r (if any) at byte 8448 + r//2, bit 4*(r%2);
     unit = 8448 bytes, or 8512 with zero-points;
   * format 2: nibble = e2m1 code; E8M0 code of (r, kk//32) at byte 8192 + 4r + kk//32;
-    unit = 8704 bytes.
+    unit = 8704 bytes;
+  * format 5: nibble u = q + 8; E8M0 codes as format 2; unit = 8704 bytes.
 
 Row-major payload (formats 3, 4): codes as bytes [N_pad][K_pad/2] (even k in the low
 nibble), then scale-factor atoms of 512 bytes, atom (n_tile, kc) n_tile-major, where kc
 counts chunks of 128 K (format 3, E8M0 per 32) or 64 K (format 4, e4m3 per 16); inside an
 atom the scale of (row r, sub-block j in 0..3) is at byte (r%32)*16 + (r//32)*4 + j.
 
-Padding: N_pad = ceil(N/128)*128; K_pad = K (formats 1-3, K % 128 == 0) or
+Padding: N_pad = ceil(N/128)*128; K_pad = K (formats 1-3 and 5, K % 128 == 0) or
 ceil(K/256)*256 (format 4, K % 64 == 0); padded codes, scales and zero-points are zero.
 
 Quantized activations: FP8 per token is e4m3 bytes [M][K] plus fp32 s_tok [M]; NVFP4 is
@@ -49,7 +51,8 @@ from .formats import bf16_bits
 
 MAGIC = 0x31574D48
 HEADER = 256
-FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A8_MXFP4, FMT_W4A4_NVFP4 = 1, 2, 3, 4
+FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A8_MXFP4, FMT_W4A4_NVFP4, FMT_W4A16_MXINT4 = 1, 2, 3, 4, 5
+TILED = (FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A16_MXINT4)
 TILE_N = 128
 ATOM = 512
 
@@ -66,14 +69,14 @@ def padded_dims(fmt, n, k):
 def unit_bytes(fmt, has_zero):
     if fmt == FMT_W4A16_INT4:
         return 8512 if has_zero else 8448
-    if fmt == FMT_W4A16_MXFP4:
+    if fmt in (FMT_W4A16_MXFP4, FMT_W4A16_MXINT4):
         return 8704
     raise ValueError(fmt)
 
 
 def payload_bytes(fmt, n, k, has_zero=False):
     n_pad, k_pad = padded_dims(fmt, n, k)
-    if fmt in (FMT_W4A16_INT4, FMT_W4A16_MXFP4):
+    if fmt in TILED:
         return (n_pad // 128) * (k_pad // 128) * unit_bytes(fmt, has_zero)
     chunk = 128 if fmt == FMT_W4A8_MXFP4 else 64
     return n_pad * k_pad // 2 + (n_pad // 128) * (k_pad // chunk) * ATOM
@@ -90,7 +93,7 @@ def header(fmt, n, k, has_zero, tensor_scale):
     return np.frombuffer(h + bytes(HEADER - len(h)), dtype=np.uint8).copy()
 
 
-# ------------------------------------------------------------------ tiled units (formats 1, 2)
+# ------------------------------------------------------------------ tiled units (formats 1, 2, 5)
 
 def nibble_position(kk):
     """(byte offset within the nibble region for row 0, bit shift) of column kk in a unit."""
@@ -147,12 +150,13 @@ def pack_w4a16_int4(q, s, zeros=None):
     return np.concatenate([header(FMT_W4A16_INT4, n, k, has_zero, 1.0), pay])
 
 
-def pack_w4a16_mxfp4(codes, e):
-    codes = np.asarray(codes)
-    n, k = codes.shape
-    n_pad, k_pad = padded_dims(FMT_W4A16_MXFP4, n, k)
+def _pack_e8_units(fmt, nibbles, e):
+    """Units of 4-bit nibbles [N,K] (0..15) with E8M0 codes [N,K/32] (formats 2 and 5)."""
+    nibbles = np.asarray(nibbles)
+    n, k = nibbles.shape
+    n_pad, k_pad = padded_dims(fmt, n, k)
     nib = np.zeros((n_pad, k_pad), dtype=np.int64)
-    nib[:n, :k] = codes
+    nib[:n, :k] = nibbles
     ecodes = np.zeros((n_pad, k_pad // 32), dtype=np.int64)
     ecodes[:n] = e
 
@@ -160,8 +164,18 @@ def pack_w4a16_mxfp4(codes, e):
         blk = ecodes[t * 128:(t + 1) * 128, b * 4:(b + 1) * 4]      # [128, 4]
         unit[8192 + 4 * np.arange(128)[:, None] + np.arange(4)[None, :]] = blk
 
-    pay = _pack_units(FMT_W4A16_MXFP4, nib, scales, None, n, k, False)
-    return np.concatenate([header(FMT_W4A16_MXFP4, n, k, False, 1.0), pay])
+    pay = _pack_units(fmt, nib, scales, None, n, k, False)
+    return np.concatenate([header(fmt, n, k, False, 1.0), pay])
+
+
+def pack_w4a16_mxfp4(codes, e):
+    """e2m1 codes [N,K] and E8M0 codes [N,K/32] -> packed buffer (uint8)."""
+    return _pack_e8_units(FMT_W4A16_MXFP4, codes, e)
+
+
+def pack_w4a16_mxint4(q, e):
+    """Signed codes q [N,K] in [-8, 7] (stored as q + 8) and E8M0 codes [N,K/32] -> packed buffer."""
+    return _pack_e8_units(FMT_W4A16_MXINT4, np.asarray(q, dtype=np.int64) + 8, e)
 
 
 # ------------------------------------------------------------------ row-major codes + atoms (3, 4)

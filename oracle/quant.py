@@ -19,6 +19,15 @@ exponent is floor(log2(amax)) - 2 (2 = largest exponent of e2m1), biased by 127 
 clamped to [0, 254]; elements are RNE(w / 2^(e-127)) saturated to +-6. An all-zero
 block has scale code 0 and zero elements.
 
+MXINT4 (named in the news pages' format list, section "하나의 라이브러리로 긴 포맷 목록을
+포괄", without a definition): read as the MX scheme of OCP Microscaling v1.0 (one E8M0 shared
+exponent per 32 along K) with a signed 4-bit integer element, q in [-8, 7], restored q * X with
+X = 2^(e-127). The largest power of two inside the element range is 4 = 2^2, so the shared
+exponent takes the same rule as MXFP4: e = clamp(floor(log2 amax) - 2 + 127, 0, 254), which
+puts amax / X in [4, 8); elements are clamp(RNE(w / X), -8, 7) (the quotient by a power of two
+is exact). This equals OCP's fixed-point reading (MXINT8 style: one integer and two fraction
+bits, X' = 2^floor(log2 amax), element q/4) with X = X'/4. An all-zero block has e = 0, q = 0.
+
 FP8 per-token activations (the W4A8 path named on the explainer page, section "가중치
 형식, 활성값, 백엔드를 한 줄에 적는다", "BF16 -> per-token FP8"): per row amax;
 s_tok = fp32(amax/448); inv = fp32(448/amax); xq = e4m3(RNE, satfinite)(fp32(x*inv)).
@@ -121,6 +130,22 @@ def quant_mxfp4(w, group=GROUP_MX):
 def dequant_mxfp4(codes, e, group=GROUP_MX):
     """e2m1(code) * 2^(e-127), float64 [N,K] (exact in bf16 for these ranges)."""
     return decode_e2m1(codes) * np.repeat(decode_e8m0(e), group, axis=1)
+
+
+# ------------------------------------------------------------------ MXINT4 (int4 + E8M0 / 32)
+
+def quant_mxint4(w, group=GROUP_MX):
+    """Returns (q int64 [N,K] in [-8, 7], scale codes int64 [N,K/32] E8M0)."""
+    w = f32(w)
+    e = mx_scale_codes(w, group)
+    scale = np.repeat(decode_e8m0(e), group, axis=1)
+    q = np.clip(np.rint(w / scale), -8, 7)          # exact quotient, round half to even
+    return q.astype(np.int64), e
+
+
+def dequant_mxint4(q, e, group=GROUP_MX):
+    """q * 2^(e-127), float64 [N,K] (exact in bf16: q has at most four significant bits)."""
+    return np.asarray(q, dtype=np.float64) * np.repeat(decode_e8m0(e), group, axis=1)
 
 
 # ------------------------------------------------------------------ FP8 per token

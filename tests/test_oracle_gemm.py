@@ -98,3 +98,17 @@ def test_tolerance_rule():
     rms = np.sqrt(np.mean(yref ** 2))
     ok = G.tolerance_ok(yref + np.array([0.0, 0.02, 0.01 * rms, 2.0]), yref)
     np.testing.assert_array_equal(ok, [True, True, True, False])
+
+
+def test_w4a16_mxint4_exact_integer_case_and_brute_force():
+    # E8M0 code 127 is scale 1: the product is numpy's integer matmul of q; other codes scale
+    # each 32-block of K by its power of two, checked against explicit loops
+    rng = np.random.default_rng(7)
+    m, n, k = 3, 5, 128
+    q = rng.integers(-8, 8, size=(n, k))
+    x = rng.integers(-4, 5, size=(m, k))
+    e = np.full((n, k // 32), 127)
+    np.testing.assert_array_equal(G.gemm_w4a16_mxint4(x.astype(np.float64), q, e), (x @ q.T).astype(np.float64))
+    e = rng.integers(120, 131, size=(n, k // 32))
+    w = np.array([[q[j, t] * 2.0 ** (int(e[j, t // 32]) - 127) for t in range(k)] for j in range(n)])
+    np.testing.assert_array_equal(G.gemm_w4a16_mxint4(x.astype(np.float64), q, e), _brute(x, w))

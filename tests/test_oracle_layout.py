@@ -91,6 +91,26 @@ def test_mxfp4_tiled_round_trip():
     np.testing.assert_array_equal(eb, e)
 
 
+def test_mxint4_tiled_round_trip():
+    # signed codes are stored biased by 8 (nibble 0 = -8, 8 = 0, 15 = 7); scales as MXFP4
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((130, 256)) * 0.02
+    q, e = Q.quant_mxint4(w)
+    buf = L.pack_w4a16_mxint4(q, e)
+    assert len(buf) == L.packed_size(L.FMT_W4A16_MXINT4, 130, 256) == 256 + 2 * 2 * 8704
+    nib, units = L.unpack_units(buf)
+    np.testing.assert_array_equal(nib, q + 8)
+    eb = units[:, :, 8192:8704].reshape(2, 2, 128, 4).transpose(0, 2, 1, 3).reshape(256, 8)[:130]
+    np.testing.assert_array_equal(eb, e)
+    # one hand-placed code: (row 0, k 33) = -8 -> nibble 0 in the word at byte 2048, bits 16..19
+    q2 = np.zeros((1, 128), dtype=np.int64)
+    q2[0, 33] = -8
+    buf2 = L.pack_w4a16_mxint4(q2, np.zeros((1, 4), dtype=np.int64))
+    unit = buf2[256:256 + 8704]
+    assert unit[2048 + 2] == 0x80      # low nibble k 33 (q -8 -> 0), high nibble k 35 (q 0 -> 8)
+    assert unit[2048 + 3] == 0x88 and unit[2048] == 0x88 and unit[0] == 0x88
+
+
 @pytest.mark.parametrize("fmt", [3, 4])
 def test_rowmajor_round_trip(fmt):
     rng = np.random.default_rng(2)

@@ -182,3 +182,70 @@ def test_nvfp4_invariants_random():
     back = Q.dequant_nvfp4(codes, sb, g)
     scale = np.repeat(F.decode_e4m3(sb), 16, axis=1) * g
     assert np.all(np.abs(back - v) <= scale * 1.0 + 1e-12)  # half of the widest e2m1 gap (2)
+
+
+# ------------------------------------------------------------------ MXINT4
+
+def test_mxint4_scale_rule_closed_forms():
+    def one(amax_val, probe):
+        w = np.zeros((1, 32))
+        w[0, 0] = amax_val
+        w[0, 1] = probe
+        q, e = Q.quant_mxint4(w)
+        return int(e[0, 0]), int(q[0, 0]), int(q[0, 1])
+    assert one(1.0, 0.3) == (125, 4, 1)          # X = 1/4: 1 -> 4, 0.3 -> rne(1.2) = 1
+    assert one(7.0, -2.0) == (127, 7, -2)        # floor(log2 7) = 2: X = 1
+    assert one(8.0, 3.0) == (128, 4, 2)          # X = 2: 3/2 = 1.5 is a tie -> 2
+    assert one(0.3, 0.03125) == (123, 5, 0)      # X = 1/16: 4.8 -> 5; 0.5 is a tie -> 0
+    assert one(-1.875, 1.875) == (125, -8, 7)    # -7.5 -> -8 (even); +7.5 -> 8 clamps to 7
+    assert one(1.9375, -1.9375) == (125, 7, -8)  # 7.75 -> 8 clamps to 7; -7.75 -> -8
+    q, e = Q.quant_mxint4(np.zeros((1, 32)))
+    assert e[0, 0] == 0 and np.all(q == 0) and np.all(Q.dequant_mxint4(q, e) == 0)
+
+
+def test_mxint4_codes_brute_force():
+    # each code is the integer in [-8, 7] nearest to w / X, ties to the even one, found by
+    # scanning all sixteen candidates
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal((6, 128)) * rng.choice([0.01, 1.0, 300.0], size=(6, 1))).astype(np.float32)
+    w[0, :32] = np.array([(c + 0.5) / 4 for c in range(-8, 8)] * 2, dtype=np.float32)   # exact ties
+    q, e = Q.quant_mxint4(w)
+    x = F.decode_e8m0(e)
+    cand = np.arange(-8, 8)
+    for r in range(w.shape[0]):
+        for c in range(w.shape[1]):
+            v = float(w[r, c]) / float(x[r, c // 32])
+            d = np.abs(v - cand)
+            best = cand[d == d.min()]
+            want = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+            assert q[r, c] == want, (r, c, v)
+
+
+def test_mxint4_invariants_random():
+    rng = np.random.default_rng(12)
+    w = (rng.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    q, e = Q.quant_mxint4(w)
+    what = Q.dequant_mxint4(q, e)
+    scale = np.repeat(F.decode_e8m0(e), 32, axis=1)
+    assert q.min() >= -8 and q.max() <= 7
+    # the block maximum lands on a magnitude in [4, 8] (amax / X is in [4, 8))
+    top = np.abs(q).reshape(16, 8, 32).max(axis=2)
+    assert top.min() >= 4 and top.max() <= 8
+    # round-to-nearest error, plus the clamp of values above 7.5 X to 7 X
+    r = w / scale
+    assert np.all(np.abs(w - what) <= scale / 2 + scale * np.maximum(r - 7.5, 0) + 1e-12)
+    # restored values are bf16 numbers (at most four significant bits times a power of two)
+    np.testing.assert_array_equal(F.bf16r(what), what)
+
+
+def test_mxint4_exact_on_its_own_grid():
+    # weights that are q * 2^j with the block's largest |q| in [4, 7] come back unchanged
+    rng = np.random.default_rng(13)
+    q0 = rng.integers(-7, 8, size=(4, 64))
+    q0[:, 0], q0[:, 32] = 7, -5
+    j = np.array([[-20, 3], [0, -1], [10, -7], [-3, 5]])
+    w = q0 * np.ldexp(1.0, np.repeat(j, 32, axis=1))
+    q, e = Q.quant_mxint4(w)
+    np.testing.assert_array_equal(q, q0)
+    np.testing.assert_array_equal(e, j + 127)
+    np.testing.assert_array_equal(Q.dequant_mxint4(q, e), w)
