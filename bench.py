@@ -172,7 +172,7 @@ def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick):
                                          outlier_frac=0.01 if fmt == hm.W4A8_MXFP4 else 0.0)
             y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
             ws = hm.alloc_workspace(fmt, m, n, k)
-            if fmt == hm.W4A16_INT4 or fmt == hm.W4A16_MXFP4:
+            if fmt in (hm.W4A16_INT4, hm.W4A16_MXFP4, hm.W4A16_MXINT4):
                 act = 2 * m * k
                 launches = 1
             elif fmt == hm.W4A8_MXFP4:
@@ -280,6 +280,11 @@ def _build_points(args, hm, synth):
         return moe_points(hm, synth, hm.W4A16_INT4, args.quick)
     if w == "moe_mxfp4":
         return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick)
+    if w == "w4a16_mxint4":
+        return dense_points(hm, synth, hm.W4A16_MXINT4, [(4096, 4096), (14336, 4096), (4096, 14336)], MS, 4,
+                            "kind::f16", args.quick)
+    if w == "moe_mxint4":
+        return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick)
     if w == "moe_silu_mul":
         return silu_points(hm, synth, args.quick)
     raise SystemExit(f"unknown workload {w}")
@@ -295,6 +300,10 @@ WORKLOAD_NAMES = {
                  "T in {16,256,4096,16384}",
     "moe_mxfp4": "MoE grouped MXFP4-W4A16: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
                  "T in {16,256,4096,16384}",
+    "w4a16_mxint4": "MXINT4-W4A16 dense LLM layer: (N,K) in {(4096,4096),(14336,4096),(4096,14336)} x M in "
+                    "{1,2,4,8,16,32,64,128,256,1024,4096,8192}; signed int4 + E8M0 scale per 32",
+    "moe_mxint4": "MoE grouped MXINT4-W4A16: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
+                  "T in {16,256,4096,16384}",
     "moe_silu_mul": "MoE expert activation h = SiLU(gate) * up between the grouped GEMMs: rows = 8 T, "
                     "gate | up 2 x 2048 bf16 in, 2048 bf16 out, T in {16,256,4096,16384} (HBM-bound; "
                     "value in TFLOP/s of ~5 operations per output, roofline in GB/s)",
@@ -463,7 +472,18 @@ def oracle_sample(workload):
     from moe_hm_gemm_gb300 import synth
     from oracle import gemm as og
     from oracle import quant as oq
-    if workload in ("w4a16", "moe_w4a16", "moe_mxfp4"):
+    if workload in ("w4a16_mxint4", "moe_mxint4", "moe_mxfp4"):
+        n, k, m = 4096, 4096, 64
+        w = synth.weights(n, k, seed=1)
+        x = synth.activations(m, k, seed=3).float().numpy().astype(np.float64)
+        if workload == "moe_mxfp4":
+            codes, e = oq.quant_mxfp4(w)
+            return (f"oracle MXFP4-W4A16 dequant + fp64 GEMM, N=K=4096, M={m} rows", 2.0 * m * n * k,
+                    lambda: og.gemm_w4a16_mxfp4(x, codes, e))
+        q, e = oq.quant_mxint4(w)
+        return (f"oracle MXINT4-W4A16 dequant + fp64 GEMM, N=K=4096, M={m} rows", 2.0 * m * n * k,
+                lambda: og.gemm_w4a16_mxint4(x, q, e))
+    if workload in ("w4a16", "moe_w4a16"):
         n, k, m = 4096, 4096, 64
         w = synth.weights(n, k, seed=1)
         z = synth.zero_points(n, k // 128, seed=2)

@@ -10,7 +10,7 @@
  * 흐름"). The linear layer is X*W^T with W stored [N,K] (section "같은 가중치도 한
  * 토큰과 많은 토큰에서 비용이 다르다"); MoE splits tokens by expert (same section, MoE
  * paragraph). Formats named on the news pages (news.cocoloop.cn, "하나의 라이브러리로 긴
- * 포맷 목록을 포괄"): W4A16, W4A8, W4A4, MXFP4, NVFP4.
+ * 포맷 목록을 포괄"): W4A16, W4A8, W4A4, MXFP4, MXINT4, NVFP4.
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller, unless stated otherwise.
@@ -55,18 +55,23 @@ typedef enum hm_status {
  *                   e2m1 * 2^(e-127); bf16 activations (the MoE "MXFP4 W4A16" path).
  *  HM_W4A8_MXFP4  : same weights; activations FP8 e4m3 with one fp32 scale per token.
  *  HM_W4A4_NVFP4  : e2m1 codes, e4m3 scale per 16 along K and one fp32 tensor scale, for
- *                   both weights and activations. */
+ *                   both weights and activations.
+ *  HM_W4A16_MXINT4: signed 4-bit integer codes q in [-8, 7] with an E8M0 scale per 32 along K
+ *                   (the MX scheme with integer elements, named on the news pages' format
+ *                   list, section "하나의 라이브러리로 긴 포맷 목록을 포괄"); restored
+ *                   q * 2^(e-127), exact in bf16; bf16 activations. */
 typedef enum hm_format {
   HM_W4A16_INT4 = 1,
   HM_W4A16_MXFP4 = 2,
   HM_W4A8_MXFP4 = 3,
-  HM_W4A4_NVFP4 = 4
+  HM_W4A4_NVFP4 = 4,
+  HM_W4A16_MXINT4 = 5
 } hm_format;
 
 /* Description of one quantized weight matrix W[N,K] in the common ("standard") format.
  *  has_zero     : HM_W4A16_INT4 only; 1 = zero-points present.
  *  tensor_scale : HM_W4A4_NVFP4 only; the fp32 per-tensor scale gW (ignored otherwise).
- * Shape rules: N >= 1; K % 128 == 0 for formats 1-3, K % 64 == 0 for format 4. */
+ * Shape rules: N >= 1; K % 128 == 0 for formats 1-3 and 5, K % 64 == 0 for format 4. */
 typedef struct hm_weight_desc {
   int32_t fmt;
   int32_t has_zero;
@@ -87,11 +92,13 @@ size_t hm_packed_size(const hm_weight_desc* desc);
  *   HM_W4A16_INT4 : s = bf16(fp32(max|w| over 128)/7); q = clamp(rne(fp32(w/s)) [+z]) into
  *                   [-8,7] (or [0,15] with the zero-points read from `zeros_in`).
  *   MXFP4 formats : E8M0 e = clamp(floor(log2 amax32) - 2 + 127, 0, 254); code = e2m1(w/2^(e-127)).
+ *   HM_W4A16_MXINT4 : the same e (an all-zero block: e = 0); q = clamp(rne(w/2^(e-127)), -8, 7).
  *   HM_W4A4_NVFP4 : g = fp32(amax/2688) computed on the device and written to *g_out;
  *                   sb = e4m3(fp32(fp32(amax16/6)/g)); code = e2m1(fp32(w/fp32(sb*g))).
- * Outputs (device): q_out packed codes [N][K/2] (even k in the low nibble; INT4 nibbles are
- * two's complement without zero-points, unsigned with them); scales_out [N][K/g] (bf16 for
- * INT4 g=128; one byte per code for MXFP4 g=32 and NVFP4 g=16); g_out (NVFP4 only, fp32).
+ * Outputs (device): q_out packed codes [N][K/2] (even k in the low nibble; INT4 and MXINT4
+ * nibbles are two's complement, INT4 ones unsigned with zero-points); scales_out [N][K/g]
+ * (bf16 for INT4 g=128; one byte per code for MXFP4 and MXINT4 g=32 and NVFP4 g=16); g_out
+ * (NVFP4 only, fp32).
  * `ws` needs hm_quantize_workspace_size() bytes (NVFP4 amax partials; may be NULL otherwise). */
 size_t hm_quantize_workspace_size(const hm_weight_desc* desc);
 hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const uint8_t* zeros_in,
@@ -104,11 +111,12 @@ hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const u
  * For HM_W4A4_NVFP4 the header records desc->tensor_scale as gW.
  * Layout: a 256-byte header (magic, fmt, N, K, padded N and K, has_zero, tensor scale, payload
  * bytes), then the payload, N padded to 128 and K to 128 (W4A4: 256):
- *  - INT4 and MXFP4-W4A16: 128x128 "units", n-tile major, each one contiguous block: 8192 bytes
- *    of codes (code (r, kk) in the little-endian word at (kk/32)*2048 + r*16 + ((kk%32)/8)*4,
- *    bits 4*((kk%8)/2) + 16*(kk%2)), then the per-row scales (INT4: 128 bf16; MXFP4: 128 x 4
- *    E8M0) and, for INT4 with zero-points, 64 bytes of u4 zero-points (row r in the low nibble
- *    of byte r/2 when r is even). Units are 8448 / 8512 / 8704 bytes.
+ *  - INT4, MXFP4-W4A16 and MXINT4: 128x128 "units", n-tile major, each one contiguous block:
+ *    8192 bytes of codes (code (r, kk) in the little-endian word at (kk/32)*2048 + r*16 +
+ *    ((kk%32)/8)*4, bits 4*((kk%8)/2) + 16*(kk%2); signed codes stored as q + 8), then the
+ *    per-row scales (INT4: 128 bf16; MXFP4 and MXINT4: 128 x 4 E8M0) and, for INT4 with
+ *    zero-points, 64 bytes of u4 zero-points (row r in the low nibble of byte r/2 when r is
+ *    even). Units are 8448 / 8512 / 8704 bytes.
  *  - W4A8 / W4A4: codes row-major [N_pad][K_pad/2], then 512-byte scale atoms
  *    [N_pad/128][K_pad/chunk] (chunk = 128 K for E8M0 per 32, 64 K for e4m3 per 16), the scale
  *    of (row r, sub-block j) at byte (r%32)*16 + (r/32)*4 + j of its atom. */
@@ -159,7 +167,7 @@ size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
  * the counters it uses back at zero after every call, so it can be reused across calls. */
 
 /* Y[M,N] (bf16) = X[M,K] * dequant(W)^T.
- *  HM_W4A16_INT4 / HM_W4A16_MXFP4 : x = bf16 [M][K]; x_scale, x_global ignored.
+ *  HM_W4A16_INT4 / HM_W4A16_MXFP4 / HM_W4A16_MXINT4 : x = bf16 [M][K]; x_scale, x_global ignored.
  *  HM_W4A8_MXFP4 : x = e4m3 [M][K] with x_scale = s_tok fp32 [M]; or, when x_scale is NULL,
  *                  x = bf16 [M][K] quantized internally (hm_quant_act_fp8) into `ws`.
  *                  Y = s_tok[m] * sum_k e4m3(x)*what.
@@ -169,7 +177,8 @@ size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
  * M >= 0 (M = 0 is a no-op), N and K must match the packed header (checked on the device).
  * x must be 16-byte aligned, packed 256-byte aligned. ws: hm_workspace_size bytes.
  * Kernel per call (hm_plan reports it): tcgen05 tensor-core kernels, except the W4A16 formats at
- * decode sizes (M <= 16; 17..32 with MXFP4, or with INT4 where tcgen05 would split tiles along K),
+ * decode sizes (M <= 16; 17..32 with MXFP4 and MXINT4, or with INT4 where tcgen05 would split
+ * tiles along K),
  * which run on warp-level bf16 MMA with fp32 accumulation. Output tiles split along K are summed
  * in a fixed order, so a call is deterministic. */
 hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* x_global,
@@ -180,13 +189,14 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
  * [expert_offsets[e], expert_offsets[e+1]) of x are multiplied by expert e's weight:
  * y[r,:] = x[r,:] * dequant(W_e)^T. expert_offsets: device int32 [E+1], non-decreasing,
  * offsets[0] = 0, offsets[E] = rows (read on the device only). packed: device array of E
- * device pointers, each a packed weight of the same (fmt, N, K). Formats HM_W4A16_INT4 and
- * HM_W4A16_MXFP4. Experts with no rows cost nothing. */
+ * device pointers, each a packed weight of the same (fmt, N, K). Formats HM_W4A16_INT4,
+ * HM_W4A16_MXFP4 and HM_W4A16_MXINT4. Experts with no rows cost nothing. */
 hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
                       void* ws, size_t ws_bytes, void* stream);
 
-/* Allocation-free variant of hm_gemm for the W4A16 formats (HM_W4A16_INT4, HM_W4A16_MXFP4).
+/* Allocation-free variant of hm_gemm for the W4A16 formats (HM_W4A16_INT4, HM_W4A16_MXFP4,
+ * HM_W4A16_MXINT4).
  * The paper has no counterpart; this entry point exists for callers that cannot allocate
  * device memory at all: for example code running inside another engine's fixed memory plan
  * (a plugin that is handed no workspace), or code that must not call cudaMalloc because it
@@ -222,7 +232,8 @@ typedef struct hm_plan_info {
   int32_t tiles;       /* output tiles */
   int32_t kernel;      /* 0: tcgen05 tensor-core kernel; 1: decode kernel (W4A16 formats; warp-level
                           bf16 MMA with fp32 accumulation in registers) for M <= 16, and for
-                          17 <= M <= 32 with MXFP4 or where tcgen05 would split tiles along K */
+                          17 <= M <= 32 with MXFP4 / MXINT4 or where tcgen05 would split tiles
+                          along K */
 } hm_plan_info;
 hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
                   hm_plan_info* out);

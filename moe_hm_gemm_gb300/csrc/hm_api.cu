@@ -95,7 +95,7 @@ int env_int(const char* name, int dflt) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A4Nv; }
+bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A16MxInt; }
 
 bool valid_k(int32_t fmt, int64_t k) {
   if (k <= 0) return false;
@@ -202,16 +202,17 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
 // W4A16 formats at decode-sized M run the warp-MMA decode kernel: with few tokens per weight the
 // product is bound by streaming the weights, which the tcgen05 pipeline (restore into TMEM, one
 // MMA batch per 128-K block, accumulator hand-offs) does not keep up with (measured on the 4096 and
-// 14336 layers). Up to 16 tokens always; for 17..32 tokens MXFP4 always, INT4 when the tcgen05
-// plan would split tiles along K (the decode kernel's K ranges are cheaper there; with a whole tile
-// per CTA the tcgen05 small-token kernel is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2
+// 14336 layers). Up to 16 tokens always; for 17..32 tokens MXFP4 and MXINT4 (no small-token
+// tcgen05 kernel) always, INT4 when the tcgen05 plan would split tiles along K (the decode
+// kernel's K ranges are cheaper there; with a whole tile per CTA the tcgen05 small-token kernel
+// is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2
 // takes the decode kernel for every M it serves (tests, sweeps).
 bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
-  if (fmt != kW4A16Int4 && fmt != kW4A16Mx) return false;
+  if (!unit_fmt(fmt)) return false;
   if (m < 1 || m > kGemvMaxTokens) return false;
   const int mode = env_int("HM_GEMV", 1);
   if (mode == 0) return false;
-  if (mode == 2 || m <= 16 || fmt == kW4A16Mx) return true;
+  if (mode == 2 || m <= 16 || e8_unit_fmt(fmt)) return true;
   return f16_choice(m, n, k, num_sms).stream_k;
 }
 
@@ -242,7 +243,7 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   }
   p.tile_m = tile_m_for(fmt, m, n, num_sms, k);
   p.tile_k = fmt == kW4A4Nv ? 256 : 128;
-  p.stages = (fmt == kW4A16Int4 || fmt == kW4A16Mx) ? f16_stages(fmt, p.tile_m) : mx_stages(fmt, p.tile_m);
+  p.stages = unit_fmt(fmt) ? f16_stages(fmt, p.tile_m) : mx_stages(fmt, p.tile_m);
   p.num_m_tiles = ceil_div(m > 0 ? m : 1, p.tile_m);
   p.num_n_tiles = pad_n(n) / 128;
   p.kb_total = pad_k(fmt, k) / p.tile_k;
@@ -536,7 +537,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
-  if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
+  if (unit_fmt(fmt)) {
     F16Params prm;
     std::memset(&prm, 0, sizeof(prm));
     if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
@@ -625,7 +626,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
 hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K, void* ws,
                       size_t ws_bytes, void* stream) {
-  if (fmt != kW4A16Int4 && fmt != kW4A16Mx) return valid_fmt(fmt) ? HM_ERR_UNSUPPORTED : HM_ERR_INVALID_ARG;
+  if (!unit_fmt(fmt)) return valid_fmt(fmt) ? HM_ERR_UNSUPPORTED : HM_ERR_INVALID_ARG;
   if (rows < 0 || N <= 0 || !valid_k(fmt, K) || E < 1 || E > 1024) return HM_ERR_INVALID_ARG;
   if (rows == 0) return HM_OK;
   if (x == nullptr || expert_offsets == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
@@ -664,7 +665,7 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
 
 hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, void* y, int64_t M, int64_t N,
                                 int64_t K, void* stream) {
-  if ((fmt != kW4A16Int4 && fmt != kW4A16Mx) || M < 0 || N <= 0 || !valid_k(fmt, K)) return HM_ERR_INVALID_ARG;
+  if (!unit_fmt(fmt) || M < 0 || N <= 0 || !valid_k(fmt, K)) return HM_ERR_INVALID_ARG;
   if (M == 0) return HM_OK;
   if (x == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(packed, 256) || !aligned(y, 4) || (N % 2) != 0) return HM_ERR_INVALID_ARG;

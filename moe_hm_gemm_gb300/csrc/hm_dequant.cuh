@@ -9,6 +9,10 @@
 //
 // MXFP4 (OCP MX v1.0): w = e2m1(code) * 2^(e-127), formed in fp32 (exact) and converted to
 // bf16 with round-to-nearest-even (exact in the normal range).
+//
+// MXINT4 (signed 4-bit integers q in [-8, 7] with an E8M0 scale per 32): w = q * 2^(e-127).
+// Units hold u = q + 8, so the INT4 restore with z = 8 gives q exactly and one bf16 multiply
+// by 2^(e-127) scales it; q has at most four significant bits, so that product is exact.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -100,6 +104,14 @@ __device__ __forceinline__ void dq_mx_word_bits(uint32_t w, uint32_t sc2, uint32
     asm("lop3.b32 %0, %1, 0x01C001C0, %2, 0xEA;" : "=r"(v) : "r"(a), "r"(b & 0x80008000u));
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(v), "r"(sc2));
   }
+}
+
+// bf16x2 holding 2^(e-127) in both halves, for an E8M0 code e: the normal 2^(e-127) for
+// e = 1..254 (exponent field e, zero mantissa) and the subnormal 2^-127 for e = 0. The NaN code
+// 255 gives infinity, so a block marked NaN restores to non-finite values.
+__device__ __forceinline__ uint32_t mxint_scale_pair(uint32_t e) {
+  const uint32_t b = e == 0u ? 0x0040u : (e << 7);
+  return b * 0x00010001u;
 }
 
 }  // namespace hm

@@ -1,0 +1,629 @@
+// W4A16 GEMM on tcgen05: Y[M,N] = X[M,K] * dequant(W)^T with 4-bit weights restored to bf16
+// in registers and multiplied on the 5th-generation tensor cores (kind::f16, fp32 accumulate
+// in TMEM). Dense and grouped-MoE variants.
+//
+// The computation is the explainer page's linear layer ("vLLM Humming은 4비트를 어떻게
+// 계산하나", section "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다": Y = X * W^T, W
+// stored [N,K], read once and reused over the M rows) with W replaced by its restored value
+// (section "4비트 값에는 스케일이라는 해석 규칙이 붙는다"); the MoE variant is the same
+// product per expert over that expert's contiguous token rows (MoE paragraph of the first
+// section).
+//
+// Design (GB300-first; the pages give no kernel design):
+//  * weights are the MMA's A operand (M = 128 weight rows), tokens its B operand (N =
+//    tile_m in 16..256), so even M = 1 fills the 128-row side of the tensor core;
+//  * one persistent CTA per SM, 15 warps: warp 0 issues the TMA loads (one bulk copy of g
+//    contiguous packed 128x128 units with their scales, and the matching X tile), warps 1-2
+//    issue tcgen05.mma (two issuers with separate accumulators for tile_m <= 64, warp 1 also
+//    owns TMEM), warps 3-10 restore the weights to bf16 (two groups taking alternate 128-K
+//    blocks) into TMEM (tile_m <= 128, the MMA reads A from TMEM) or into the 128-byte-swizzled
+//    K-major shared layout (tile_m = 256), warps 11-14 drain TMEM (tcgen05.ld), round to bf16
+//    and store Y;
+//  * INT4 with tile_m 16 or 32 runs the small-token kernel instead (hm_gemm_f16s.cu);
+//  * accumulators are double-buffered in TMEM so the epilogue of one tile overlaps the main
+//    loop of the next;
+//  * small M uses stream-K (hm_sched.cuh) so that every SM streams weights; the CTA holding a
+//    tile's first k-block sums the other CTAs' published partials in k order (deterministic;
+//    no contributor waits);
+//  * programmatic dependent launch: the first weight stages stream before the wait for the
+//    previous kernel; every wait is bounded (hm_device.cuh).
+//
+// This header holds the kernel template; hm_gemm_f16.cu (INT4 and the dispatch),
+// hm_gemm_f16_mxfp4.cu and hm_gemm_f16_mxint4.cu instantiate it, one weight format each.
+#pragma once
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+
+#include "hm_dequant.cuh"
+#include "hm_device.cuh"
+#include "hm_f16_common.cuh"
+#include "hm_kernels.h"
+#include "hm_layout.h"
+#include "hm_sched.cuh"
+
+namespace hm {
+namespace {
+
+// Dequant warps: two groups of four that take alternate 128-K blocks, so that two blocks are
+// being restored at any time (one block's chain of shared loads, conversion, TMEM store and
+// barrier signalling is latency-bound); inside a group each warp owns one 32-row TMEM quarter
+// and each thread restores its row's whole 128-K block.
+constexpr int kDqGroup = 4;
+constexpr int kDqWarps = 2 * kDqGroup;
+// Warp roles: 0 producer, 1-2 MMA issuers (warp 1 also owns TMEM), 3-10 dequant, 11-14 epilogue.
+constexpr int kMmaWarp0 = 1;
+constexpr int kDqWarp0 = 3;
+constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
+
+// Two variants of the A (restored weight) path:
+//  * tile_m <= 128: the dequant warps store bf16 A straight into TMEM (tcgen05.st) and the MMA
+//    reads A from TMEM, so shared memory carries only the packed weights and X; TMEM holds the
+//    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns;
+//  * tile_m = 256: the accumulator pair fills TMEM, so A goes through shared memory in the
+//    128-byte-swizzled K-major layout.
+// A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
+// activation load), so that small token tiles move many bytes per TMA instruction; the dequant
+// warps and the MMA still step through it one 128-K block (one TMEM A slot) at a time.
+// One thread issuing tcgen05.mma waits about 46 cycles per instruction whatever N, while the
+// tensor core accepts M = 128 / K = 16 MMAs with A in TMEM several times faster from several
+// threads. Small token tiles (N <= 64, where one MMA is far below that wait) therefore use two
+// issuing warps that take alternate 128-K blocks into separate accumulators, which the epilogue
+// adds (issuer 0 first, so the sum is deterministic).
+template <int BT>
+struct F16Shape {
+  static constexpr bool kATmem = BT <= 128;
+  static constexpr int kIss = BT <= 64 ? 2 : 1;
+  static constexpr int kAccCols = 2 * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
+  static constexpr int kG = f16_group_of(BT);
+  static constexpr int kXStage = kG * BT * 128 * 2;
+  static constexpr int kWStage = kG * kUnitMx;  // room for the largest units
+  static constexpr int kSA = kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2;
+  static constexpr int kAOff = 0;
+  static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
+  static constexpr int kXOff = kASmem;
+  static constexpr int kSLFit = ((kATmem ? 208 : 216) * 1024 - kASmem) / (kXStage + kWStage);
+  static constexpr int kSL = kSLFit > 16 ? 16 : kSLFit;
+  static constexpr int kWOff = kXOff + kSL * kXStage;
+  static constexpr int kBarOff = kWOff + kSL * kWStage;
+  static constexpr int kNumBars = 3 * kSL + 2 * kSA + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kLutOff = kMiscOff + 32;
+  static constexpr int kMoeOff = kLutOff + 64;
+  static constexpr uint32_t kTmemCols = kATmem ? 512u : (2 * BT < 32 ? 32u : 2u * BT);
+  static constexpr uint32_t kACol0 = kAccCols;  // first TMEM column of the A stages
+  static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
+  static_assert(kSL >= 2, "load pipeline depth");
+  static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
+  static_assert(kATmem || kIss == 1, "two issuers only with A in TMEM");
+};
+
+// WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4.
+template <int BT, int WK, bool MOE>
+__global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
+  using S = F16Shape<BT>;
+  constexpr int SL = S::kSL;
+  constexpr int SA = S::kSA;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* full_w = bars;
+  uint64_t* full_x = bars + SL;
+  uint64_t* empty_l = bars + 2 * SL;
+  uint64_t* full_a = bars + 3 * SL;
+  uint64_t* empty_a = full_a + SA;
+  uint64_t* acc_full = empty_a + SA;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 4);
+  float* lut = reinterpret_cast<float*>(smem + S::kLutOff);
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + S::kMoeOff);
+  int32_t* offs = prefix + (MOE ? p.num_experts + 1 : 0);
+  volatile uint32_t* hz_sh = reinterpret_cast<volatile uint32_t*>(smem + S::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    trace_mark(p.trace, 0);
+    // Read the (first) weight header before initialising the barriers so that its memory
+    // latency overlaps the set-up. MoE offsets (and thus expert pointers) may come from the
+    // previous kernel, so the MoE variant waits for it first.
+    if (MOE) pdl_wait();
+    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
+    const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first);
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(&full_w[s], 1);
+      mbar_init(&full_x[s], 1);
+      mbar_init(&empty_l[s], S::kIss + kDqWarps);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&full_a[s], kDqGroup);
+      mbar_init(&empty_a[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], S::kIss);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, S::kIss);
+    fence_barrier_init();
+    *abort_flag = 0u;
+    // The first weight's header decides whether INT4 units carry zero-points; every weight
+    // used must agree with it and with the call's (fmt, N, K).
+    const uint32_t hz = hdr.has_zero;
+    *hz_sh = (WK == 0 && hz == 1u) ? 1u : 0u;
+    if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
+      atomicOr(p.err, kErrHeader);
+      *abort_flag = 1u;
+    }
+  }
+  if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
+  if (warp == kMmaWarp0) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (MOE && warp == kDqWarp0) pdl_wait();   // the offsets below may be written by the previous kernel
+
+  int32_t num_tiles = p.sched.num_tiles;
+  if (MOE) {
+    // Per-expert tile counts and their exclusive prefix (first dequant warp), offsets copied to shared.
+    if (warp == kDqWarp0) moe_tile_prefix<BT>(p, offs, prefix, abort_flag, lane);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (MOE) num_tiles = prefix[p.num_experts];
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  SchedIter sched;
+  sched.init(p.sched, num_tiles, blockIdx.x);
+  const int kb_total = p.sched.kb_total;
+  const bool aborted_early = *abort_flag != 0u;
+  const uint32_t has_zero = *hz_sh;
+  if (threadIdx.x == 0) {
+    trace_mark(p.trace, 1);
+    pdl_launch_dependents();
+  }
+  const uint32_t kUnit = WK >= 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  // Weights are streamed once when a single token tile covers M; with several token tiles the
+  // same weight tiles are read again by other CTAs, so keep them in L2.
+  const bool reuse_w = MOE || p.num_m_tiles > 1;
+
+  if (aborted_early) {
+    // nothing to do: fall through to teardown
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_x);
+      const uint64_t pol_w = reuse_w ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_x = reuse_w ? policy_evict_normal() : policy_evict_last();
+      const uint8_t* last_checked = nullptr;
+      // A weight buffer is read only after its header matched the call (MoE: each expert's).
+      auto checked = [&](const TileInfo& t) -> bool {
+        if (!MOE || t.base == last_checked) return true;
+        if (!header_ok(t.base, p, has_zero)) {
+          atomicOr(p.err, kErrHeader);
+          *abort_flag = 1u;
+          return false;
+        }
+        last_checked = t.base;
+        return true;
+      };
+      // Stage `idx` (ring slot idx % SL) covers k-blocks [kb, kb + g) of tile t.
+      auto issue_w = [&](int idx, const TileInfo& t, int kb, int g) {
+        const int slot = idx % SL;
+        const uint32_t bytes = static_cast<uint32_t>(g) * kUnit;
+        mbar_arrive_expect_tx(&full_w[slot], bytes);
+        bulk_g2s(smem + S::kWOff + slot * S::kWStage, t.wbase + static_cast<size_t>(kb) * kUnit, bytes,
+                 &full_w[slot], pol_w);
+      };
+      auto issue_x = [&](int idx, const TileInfo& t, int kb) {
+        const int slot = idx % SL;
+        uint8_t* xs = smem + S::kXOff + slot * S::kXStage;
+        trace_stage(p.trace, 0, idx);
+        mbar_arrive_expect_tx(&full_x[slot], S::kXStage);   // the whole box lands (zero-filled past K)
+        if constexpr (S::kG == 1) {
+          tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[slot], pol_x);
+          tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[slot], pol_x);
+        } else {
+          tma_3d_g2s(xs, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[slot], pol_x);
+        }
+        if (idx == 0) trace_mark(p.trace, 2);
+      };
+      // Start-up order. The weights of stage 0 do not depend on the previous kernel, so the
+      // dense path streams them before waiting for it. Then the activation tiles of the first SL
+      // stages go out before the rest of their weights: an SM's copies complete roughly in issue
+      // order, and an activation tile queued behind ~100 KB of weights would hold back the first
+      // MMA by microseconds.
+      int issued_w = 0, issued_x = 0;
+      bool ok = true;
+      if (!MOE) {
+        SchedIter pf = sched;
+        Segment ps;
+        if (pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          issue_w(0, t, ps.kb0, min(S::kG, ps.kb1 - ps.kb0));
+          issued_w = 1;
+        }
+      }
+      pdl_wait();
+      {
+        SchedIter pf = sched;
+        Segment ps;
+        int idx = 0;
+        while (idx < SL && pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          for (int kb = ps.kb0; kb < ps.kb1 && idx < SL; kb += S::kG, ++idx) issue_x(idx, t, kb);
+        }
+        issued_x = idx;
+        pf = sched;
+        idx = 0;
+        while (idx < issued_x && pf.next(ps)) {
+          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          if (!checked(t)) { ok = false; break; }
+          for (int kb = ps.kb0; kb < ps.kb1 && idx < issued_x; kb += S::kG, ++idx)
+            if (idx >= issued_w) issue_w(idx, t, kb, min(S::kG, ps.kb1 - kb));
+        }
+        if (ok) issued_w = issued_x;
+      }
+      // Steady state: a stage is refilled once every consumer released it.
+      int idx = 0;
+      int ls = 0;
+      uint32_t lph = 0;
+      Segment seg;
+      while (ok && sched.next(seg)) {
+        const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+        if (!checked(t)) break;
+        for (int kb = seg.kb0; kb < seg.kb1; kb += S::kG, ++idx) {
+          if (idx >= issued_x) {
+            if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
+            issue_w(idx, t, kb, min(S::kG, seg.kb1 - kb));   // weights first: the dequant needs them first
+            issue_x(idx, t, kb);
+            issued_x = issued_w = idx + 1;
+          }
+          if (++ls == SL) { ls = 0; lph ^= 1u; }
+        }
+      }
+      trace_mark(p.trace, 3);
+      if (*abort_flag) {
+        // Let copies already in flight (at most the last SL stages issued) land before the
+        // CTA's shared memory goes away.
+        for (int i = issued_x > SL ? issued_x - SL : 0; i < issued_x; ++i)
+          drain_wait(&full_x[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
+        for (int i = issued_w > SL ? issued_w - SL : 0; i < issued_w; ++i)
+          drain_wait(&full_w[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp < kMmaWarp0 + S::kIss) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `is` takes the 128-K blocks whose running sequence index bi has bi % kIss == is,
+    // accumulating into its own TMEM accumulator; A slot bi % SA holds block bi.
+    if (lane == 0) {
+      const int is = warp - kMmaWarp0;
+      constexpr uint32_t idesc = idesc_bf16(128, BT);
+      int ls = 0;
+      uint32_t lph = 0, acc_i = 0;
+      int seq = 0;
+      Segment seg;
+      bool ok = true;
+      while (ok && sched.next(seg)) {
+        const uint32_t b = acc_i & 1u;
+        if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (b * S::kIss + is) * BT;
+        bool first = true;
+        for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+          // Wait for the stage even without a block in it: the release below must not reach
+          // the slot's empty barrier before the slot's previous use is over.
+          if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
+          if (is == 0) trace_stage(p.trace, 7, seq / S::kG);
+          const int g = min(S::kG, seg.kb1 - kb0);
+          for (int j = 0; j < g; ++j) {
+            const int bi = seq + j;
+            if (S::kIss > 1 && bi % S::kIss != is) continue;
+            const int as = bi % SA;
+            const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
+            if (!mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
+            trace_stage(p.trace, 3, bi);
+            tc_fence_after();
+            if (is == 0 && acc_i == 0 && first) trace_mark(p.trace, 6);
+            trace_stage(p.trace, 4, bi);
+            const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
+            if constexpr (S::kATmem) {
+              const uint32_t a_t = tmem + S::kACol0 + as * 64;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+                mma_bf16_ta(d, a_t + 8 * k, bd, idesc, (!first || k > 0) ? 1u : 0u);
+              }
+            } else {
+              const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * (kAStage / 2) + (k & 3) * 32);
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (BT * 128) + (k & 3) * 32);
+                mma_bf16(d, ad, bd, idesc, (!first || k > 0) ? 1u : 0u);
+              }
+            }
+            first = false;
+            trace_stage(p.trace, 5, bi);
+            tc_commit(&empty_a[as]);
+            trace_stage(p.trace, 6, bi);
+          }
+          if (!ok) break;
+          tc_commit(&empty_l[ls]);
+          seq += g;
+          if (++ls == SL) { ls = 0; lph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[b]);   // also when this issuer had no block in the tile
+        ++acc_i;
+      }
+      if (is == 0) trace_mark(p.trace, 7);
+      // All tcgen05 work of this thread has completed once `drain` flips (one arrival per issuer).
+      tc_commit(drain);
+      drain_wait(drain, 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= kDqWarp0 && warp < kEpiWarp0) {
+    // ------------------------------------------------------------ dequant warps
+    // Warp -> (group, row, K half). With A in TMEM a warp may only touch its own 32-lane
+    // quarter (warp index % 4), so rows follow the quarter; otherwise rows follow the thread.
+    const int dw = warp - kDqWarp0;
+    const int grp = dw / kDqGroup;                 // takes the blocks with sequence index % 2 == grp
+    const int r = 32 * (warp & 3) + lane;          // weight row within the tile (TMEM lane)
+    int ls = 0;
+    uint32_t lph = 0;
+    int seq = 0;                                   // running 128-K block index over all segments
+    bool first_dq = true;
+    Segment seg;
+    bool ok = true;
+    while (ok && sched.next(seg)) {
+      for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
+        const int g = min(S::kG, seg.kb1 - kb0);
+        // blocks j of this stage that belong to this group
+        const int j0 = ((seq & 1) == grp) ? 0 : 1;
+        // Every group waits for the stage to fill, even one with no block in it: its release
+        // must not reach the ring slot's empty barrier before the slot's previous use is over,
+        // or it would count towards the wrong phase.
+        if (!mbar_wait(&full_w[ls], lph, wc)) {
+          ok = false;
+          break;
+        }
+        if (j0 >= g) {                             // none of the blocks: release the stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_l[ls]);
+        }
+        for (int jb = j0; jb < g; jb += 2) {
+        const int bi = seq + jb;
+        const int as = bi % SA;
+        const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
+        if (!mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
+        if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
+        if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 1, bi);
+        const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
+        // INT4 and MXINT4 take the whole 128-K row into registers at once; MXFP4 (whose scale
+        // and conversion need more registers) takes the second half after converting the first.
+        uint4 c[4];
+#pragma unroll
+        for (int i = 0; i < (WK == 2 ? 2 : 4); ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
+        __nv_bfloat162 zz, ss;
+        uint32_t e4 = 0;
+        if (WK >= 2) {
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e4) : "r"(wsa + kUnitCodes + 4 * r));
+          zz = int4_zero_pair(8);   // MXINT4 nibbles are q + 8
+        } else {
+          uint16_t sb;
+          asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(wsa + kUnitCodes + 2 * r));
+          ss = bf16_pair(sb);
+          uint32_t z = 8u;
+          if (has_zero) {
+            uint16_t zb;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitInt4 + (r >> 1)));
+            z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
+          }
+          zz = int4_zero_pair(z);
+        }
+        const bool last_of_stage = jb + 2 >= g;
+        if (WK != 2 && last_of_stage) {   // the stage's last block of this group is in registers
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_l[ls]);
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (WK == 2 && half == 1) {
+#pragma unroll
+            for (int i = 2; i < 4; ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
+            if (last_of_stage) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&empty_l[ls]);
+            }
+          }
+          uint32_t a_regs[32];  // TMEM path: 64 restored K of this row as bf16x2, in K order
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c4 = 2 * half + i;
+            const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
+            const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
+            const bool mx_bits = WK == 2 && ex <= 128u;
+            const uint32_t sc2 = mx_pow2_pair(ex);
+            const float scale = WK == 2 ? pow2f(static_cast<int>(ex) - 127) : 0.f;
+            const __nv_bfloat162 si = bits_bf16x2(mxint_scale_pair(ex));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t o[4];
+              if (WK == 0) dq_int4_word(words[j], zz, ss, o);
+              else if (WK == 3) dq_int4_word(words[j], zz, si, o);
+              else if (mx_bits) dq_mx_word_bits(words[j], sc2, o);
+              else dq_mx_word(words[j], lut, scale, o);
+              if constexpr (S::kATmem) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
+              } else {
+                const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
+                const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+                const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
+                                     ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
+                st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+              }
+            }
+          }
+          if constexpr (S::kATmem)
+            tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
+        }
+        if constexpr (S::kATmem) {
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 2, bi);
+        if (lane == 0) mbar_arrive(&full_a[as]);
+        }
+        seq += g;
+        if (++ls == SL) { ls = 0; lph ^= 1u; }
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue warps (last four)
+    pdl_wait();                          // Y, partials and counters may be in use by the previous kernel
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int row = 32 * q + lane;       // weight row within the tile
+    const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
+    uint32_t acc_i = 0;
+    bool first_seg = true;
+    int seq = 0;                         // running 128-K block index, as the issuers count it
+    Segment seg;
+    while (sched.next(seg)) {
+      const uint32_t b = acc_i & 1u;
+      // Issuer i wrote its accumulator iff the segment has a block with sequence index % 2 == i.
+      const int nb = seg.kb1 - seg.kb0;
+      const bool use1 = S::kIss > 1 && (nb >= 2 || (seq & 1) == 1);
+      const bool use0 = S::kIss == 1 || nb >= 2 || (seq & 1) == 0;
+      seq += nb;
+      if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
+      tc_fence_after();
+      if (row == 0 && acc_i == 0) trace_mark(p.trace, 8);
+      const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+      const int64_t n = static_cast<int64_t>(t.n0) + row;
+      const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
+      // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
+      // others' published partials and adds them to its own accumulator; the others publish.
+      const bool owner = !full && seg.kb0 == 0;
+      uint32_t* flag = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+      int64_t c_hi = 0;
+      bool have = true;
+      if (owner) {
+        c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
+        if (row == 0) trace_mark(p.trace, 10);
+      }
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * S::kIss * BT;
+      float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
+                    static_cast<size_t>(row) * BT;
+#pragma unroll 1
+      for (int j0 = 0; j0 < BT && have; j0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + (use0 ? 0 : BT) + j0, v);
+        if (S::kIss > 1 && use0 && use1) {
+          uint32_t v1[16];
+          tmem_ld16(tbase + BT + j0, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(v1[jj]));
+        } else {
+          tmem_wait_ld();
+        }
+        if (full || owner) {
+          float a[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
+          if (owner)
+            sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
+          if (n < p.n) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
+              if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(a[jj]);
+            }
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(slot + j0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++acc_i;
+      if (row == 0) trace_mark(p.trace, 9);
+      if (!full && !owner) sk_publish(flag, lane);
+      if (owner && have) {
+        __syncwarp();
+        if (lane == 0) *flag = 0u;
+        if (row == 0) trace_mark(p.trace, 11);
+      }
+      first_seg = false;
+    }
+  }
+
+  __syncwarp();  // reconverge lanes that skipped a single-thread role before the CTA barrier
+  __syncthreads();
+  if (warp == kMmaWarp0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::kTmemCols);
+    if (lane == 0) {
+      trace_mark(p.trace, 12);
+      if (p.trace) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[blockIdx.x * 16 + 13] = smid;
+      }
+    }
+  }
+}
+
+template <int BT, int WK, bool MOE>
+cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
+  using S = F16Shape<BT>;
+  auto kern = f16_gemm_kernel<BT, WK, MOE>;
+  const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
+  // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
+  // instantiation can ask for), so that later calls, including ones under stream capture, only launch.
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::smem_bytes(1024));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  return launch_pdl(kern, p.sched.grid, kThreads, smem, st, p);
+}
+
+template <int WK, bool MOE>
+cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
+  switch (tile_m) {
+    case 16: return launch_one<16, WK, MOE>(p, st);
+    case 32: return launch_one<32, WK, MOE>(p, st);
+    case 64: return launch_one<64, WK, MOE>(p, st);
+    case 128: return launch_one<128, WK, MOE>(p, st);
+    case 256: return launch_one<256, WK, MOE>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+// Per-format entry points, each defined in its own translation unit so that the three sets of
+// kernel instantiations compile in parallel.
+cudaError_t launch_f16_mxfp4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+cudaError_t launch_f16_mxint4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+
+}  // namespace hm

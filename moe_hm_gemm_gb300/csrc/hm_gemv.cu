@@ -33,7 +33,8 @@
 //  * INT4: the word is restored to exact bf16 (u - z) pairs (one shift, one lop3, one bf16x2
 //    subtract per pair); each unit's MMAs accumulate sum (u - z) x over the unit's 128 K in fp32,
 //    and the group scale multiplies that sum (s * sum (u - z) x, as in the small-token tcgen05
-//    kernel). MXFP4: the word is restored with its E8M0 scale (exact) and the MMAs accumulate
+//    kernel). MXFP4 and MXINT4: the word is restored with its E8M0 scale (exact; MXINT4 through
+//    the INT4 restore with z = 8 and a bf16 power-of-two scale) and the MMAs accumulate
 //    straight into the running sums.
 //  * Segment end: the warps of a row pair (two or four) add their sums in a fixed order through shared
 //    memory (mbarrier hand-off, bounded); every warp closes every segment of its CTA's range, even
@@ -183,9 +184,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-template <int MT, bool MX>
+// WK: 0 = INT4, 2 = MXFP4, 3 = MXINT4 (the last two carry E8M0 scales per 32 in their units).
+template <int MT, int WK>
 __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_constant__ F16Params p) {
   using S = VShape<MT>;
+  constexpr bool MX = WK >= 2;
   constexpr int SL = S::kS;
   constexpr int NQ = S::kNQ;
   extern __shared__ uint8_t smem_raw[];
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
       *abort_flag = 1u;
     }
   }
-  if (MX && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
+  if (WK == 2 && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
   __syncthreads();
   // the owner's barriers must be initialised before another CTA of its cluster arrives on them
   if (csize > 1) cluster_sync_all();
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     }
     // shared-memory offsets within a stage (the per-(tile, row, chunk) parts are immediates):
     // code word t of row 32pr + g (+16j, +8hl) in chunk 2cp (+cc); activation fragment of token g
-    // (+8q), columns 64cp + 8t (+32cc); the row's metadata (INT4) or E8M0 scale word (MXFP4)
+    // (+8q), columns 64cp + 8t (+32cc); the row's metadata (INT4) or E8M0 scale word (MXFP4, MXINT4)
     const uint32_t woff = static_cast<uint32_t>((2 * cp) * 2048 + (32 * pr + g) * 16 + 4 * t);
     const uint32_t xoff = static_cast<uint32_t>(S::kWBytes + g * S::kXPitch + (2 * cp) * 64 + t * 16);
     const uint32_t moff = static_cast<uint32_t>(MX ? kUnitCodes + (32 * pr + g) * 4 : S::kMetaOff + (32 * pr + g) * 8);
@@ -565,7 +568,9 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
 #pragma unroll
               for (int hl = 0; hl < 2; ++hl) {
                 const uint32_t ex = (e4[hl] >> (8 * (2 * cp + cc))) & 0xFFu;
-                if (ex <= 128u) {
+                if constexpr (WK == 3) {
+                  dq_int4_word(wd[j][hl][cc], int4_zero_pair(8), bits_bf16x2(mxint_scale_pair(ex)), a[hl]);
+                } else if (ex <= 128u) {
                   dq_mx_word_bits(wd[j][hl][cc], mx_pow2_pair(ex), a[hl]);
                 } else {
                   dq_mx_word(wd[j][hl][cc], lut, pow2f(static_cast<int>(ex) - 127), a[hl]);
@@ -597,10 +602,10 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   if (csize > 1) cluster_sync_all();
 }
 
-template <int MT, bool MX>
+template <int MT, int WK>
 cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   using S = VShape<MT>;
-  auto kern = gemv_kernel<MT, MX>;
+  auto kern = gemv_kernel<MT, WK>;
   static int configured[64] = {};
   static int cluster_max[64][kVMaxCluster + 1] = {};   // active clusters the device holds, +1 (0 unknown)
   int dev = 0;
@@ -667,12 +672,12 @@ int gemv_stages(int64_t m) {
 
 cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
   if (p.m < 1 || p.m > kGemvMaxTokens) return cudaErrorInvalidValue;
-  const bool mx = p.fmt == kW4A16Mx;
-  switch (gemv_tokens(p.m)) {
-    case 8: return mx ? launch_v<8, true>(p, st) : launch_v<8, false>(p, st);
-    case 16: return mx ? launch_v<16, true>(p, st) : launch_v<16, false>(p, st);
-  }
-  return mx ? launch_v<32, true>(p, st) : launch_v<32, false>(p, st);
+  const int t = gemv_tokens(p.m);
+  if (p.fmt == kW4A16Mx)
+    return t == 8 ? launch_v<8, 2>(p, st) : (t == 16 ? launch_v<16, 2>(p, st) : launch_v<32, 2>(p, st));
+  if (p.fmt == kW4A16MxInt)
+    return t == 8 ? launch_v<8, 3>(p, st) : (t == 16 ? launch_v<16, 3>(p, st) : launch_v<32, 3>(p, st));
+  return t == 8 ? launch_v<8, 0>(p, st) : (t == 16 ? launch_v<16, 0>(p, st) : launch_v<32, 0>(p, st));
 }
 
 }  // namespace hm

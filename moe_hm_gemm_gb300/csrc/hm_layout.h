@@ -8,7 +8,8 @@
 // word at byte (kk/32)*2048 + r*16 + ((kk%32)/8)*4, bit 4*((kk%8)/2) + 16*(kk%2): even
 // columns fill the low half-word and odd columns the high one, so a mask of 0x000F000F
 // after a shift yields a bf16x2 pair of consecutive columns. INT4 nibbles are stored offset
-// by 8 when there is no zero-point (u = q + 8), so every INT4 unit restores (u - z) * s.
+// by 8 when there is no zero-point (u = q + 8), so every INT4 unit restores (u - z) * s. MXINT4
+// units hold the same biased nibbles (u = q + 8) with the 128 x 4 E8M0 scales of MXFP4 units.
 #pragma once
 #include <cstdint>
 
@@ -37,18 +38,25 @@ struct PackedHeader {
 };
 static_assert(sizeof(PackedHeader) == 56, "header layout");
 
-enum Fmt : int32_t { kW4A16Int4 = 1, kW4A16Mx = 2, kW4A8Mx = 3, kW4A4Nv = 4 };
+enum Fmt : int32_t { kW4A16Int4 = 1, kW4A16Mx = 2, kW4A8Mx = 3, kW4A4Nv = 4, kW4A16MxInt = 5 };
+
+// Formats stored as 128x128 units and multiplied with bf16 activations on kind::f16.
+__host__ __device__ inline bool unit_fmt(int32_t fmt) {
+  return fmt == kW4A16Int4 || fmt == kW4A16Mx || fmt == kW4A16MxInt;
+}
+// Unit formats whose scales are E8M0 per 32 along K (128 rows x 4 bytes after the codes).
+__host__ __device__ inline bool e8_unit_fmt(int32_t fmt) { return fmt == kW4A16Mx || fmt == kW4A16MxInt; }
 
 inline int64_t pad_n(int64_t n) { return (n + kTileN - 1) / kTileN * kTileN; }
 inline int64_t pad_k(int32_t fmt, int64_t k) { return fmt == kW4A4Nv ? (k + 255) / 256 * 256 : k; }
 
-inline uint32_t unit_bytes(int32_t fmt, bool has_zero) {
-  return fmt == kW4A16Mx ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+__host__ __device__ inline uint32_t unit_bytes(int32_t fmt, bool has_zero) {
+  return e8_unit_fmt(fmt) ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
 }
 
 inline uint64_t payload_bytes(int32_t fmt, int64_t n, int64_t k, bool has_zero) {
   const int64_t np = pad_n(n), kp = pad_k(fmt, k);
-  if (fmt == kW4A16Int4 || fmt == kW4A16Mx)
+  if (unit_fmt(fmt))
     return static_cast<uint64_t>(np / 128) * (kp / 128) * unit_bytes(fmt, has_zero);
   const int64_t chunk = fmt == kW4A8Mx ? 128 : 64;
   return static_cast<uint64_t>(np) * kp / 2 + static_cast<uint64_t>(np / 128) * (kp / chunk) * kAtomBytes;

@@ -6,7 +6,8 @@
 // "4비트 값에는 스케일이라는 해석 규칙이 붙는다" (q = round(w/s) in [-8, 7], restored s*q, one
 // 16-bit scale per 128 weights) and section "표현을 맞춘 다음 GPU가 읽기 좋은 배치로 바꾼다"
 // (weights, scales and zero-points are padded and rearranged once for the device). MXFP4
-// follows OCP Microscaling v1.0; NVFP4 the two-level (e4m3 per 16, fp32 per tensor) recipe.
+// follows OCP Microscaling v1.0; MXINT4 takes the same shared exponent with signed 4-bit integer
+// elements; NVFP4 the two-level (e4m3 per 16, fp32 per tensor) recipe.
 #include <cuda_bf16.h>
 
 #include "hm_dequant.cuh"
@@ -98,6 +99,35 @@ __global__ void quant_mx_kernel(const float* __restrict__ w, int64_t n, int64_t 
   if ((lane & 7) == 0) e8[row * (k / 32) + c * 4 + (lane >> 3)] = static_cast<uint8_t>(code);
 }
 
+// MXINT4, one warp per (row, 128 K); 8 lanes per 32-block. Shared exponent as for MXFP4
+// (floor(log2 amax) - 2, 2 being the largest power of two in the int4 range), elements
+// clamp(RNE(w / 2^(e-127)), -8, 7) stored as two's-complement nibbles, even K in the low nibble.
+__global__ void quant_mxint_kernel(const float* __restrict__ w, int64_t n, int64_t k,
+                                   uint8_t* __restrict__ q, uint8_t* __restrict__ e8) {
+  const int64_t chunks = k / 128;
+  const int64_t gid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gid >= n * chunks) return;
+  const int64_t row = gid / chunks, c = gid % chunks;
+  const float4 v = *reinterpret_cast<const float4*>(w + row * k + c * 128 + 4 * lane);
+  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  const int be = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int code = amax == 0.f ? 0 : min(max(be - 2, 0), 254);
+  const float mul = pow2f(127 - code);   // exact: a power of two, |w * mul| < 8
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int qi = min(max(__float2int_rn(__fmul_rn(x[i], mul)), -8), 7);
+    packed |= (static_cast<uint32_t>(qi) & 0xFu) << (4 * i);
+  }
+  *reinterpret_cast<uint16_t*>(q + row * (k / 2) + c * 64 + 2 * lane) = static_cast<uint16_t>(packed);
+  if ((lane & 7) == 0) e8[row * (k / 32) + c * 4 + (lane >> 3)] = static_cast<uint8_t>(code);
+}
+
 // Max |x| over a float array into per-block partials.
 __global__ void amax_f32_kernel(const float* __restrict__ x, int64_t count, float* __restrict__ partial) {
   float m = 0.f;
@@ -172,9 +202,8 @@ __device__ void write_header(uint8_t* packed, int32_t fmt, int64_t n, int64_t k,
     h.has_zero = static_cast<uint32_t>(has_zero);
     h.tensor_scale = gw;
     const int64_t np = h.n_pad, kp = h.k_pad;
-    if (fmt == kW4A16Int4 || fmt == kW4A16Mx)
-      h.payload_bytes = static_cast<uint64_t>(np / 128) * (kp / 128) *
-                        (fmt == kW4A16Mx ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4));
+    if (unit_fmt(fmt))
+      h.payload_bytes = static_cast<uint64_t>(np / 128) * (kp / 128) * unit_bytes(fmt, has_zero != 0);
     else
       h.payload_bytes = static_cast<uint64_t>(np) * kp / 2 +
                         static_cast<uint64_t>(np / 128) * (kp / (fmt == kW4A8Mx ? 128 : 64)) * kAtomBytes;
@@ -202,11 +231,12 @@ __global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n,
   const int64_t nt = blockIdx.x / kbt, kb = blockIdx.x % kbt;
   const int r = threadIdx.x;
   const int64_t row = nt * 128 + r;
-  const uint32_t ub = fmt == kW4A16Mx ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  const uint32_t ub = unit_bytes(fmt, has_zero != 0);
   uint8_t* unit = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * ub;
   if (blockIdx.x == 0 && threadIdx.x < 64) write_header(packed, fmt, n, k, has_zero, 1.0f);
   const bool valid = row < n;
-  const uint32_t flip = (fmt == kW4A16Int4 && !has_zero) ? 0x88888888u : 0u;
+  // signed nibbles (INT4 without zero-points, MXINT4) are stored as q + 8 = q ^ 8
+  const uint32_t flip = ((fmt == kW4A16Int4 && !has_zero) || fmt == kW4A16MxInt) ? 0x88888888u : 0u;
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
     uint4 src = make_uint4(0, 0, 0, 0);
@@ -218,7 +248,7 @@ __global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n,
     dst.w = valid ? interleave_word(src.w ^ flip) : 0u;
     *reinterpret_cast<uint4*>(unit + c4 * 2048 + r * 16) = dst;
   }
-  if (fmt == kW4A16Mx) {
+  if (e8_unit_fmt(fmt)) {
     uint32_t e4 = 0;
     if (valid) e4 = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(scales) + row * (k / 32) + kb * 4);
     *reinterpret_cast<uint32_t*>(unit + kUnitCodes + 4 * r) = e4;
@@ -277,11 +307,11 @@ __global__ void dequant_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, i
   const int r = threadIdx.x;
   const int64_t row = nt * 128 + r;
   if (row >= n) return;
-  const uint32_t ub = fmt == kW4A16Mx ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  const uint32_t ub = unit_bytes(fmt, has_zero != 0);
   const uint8_t* unit = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * ub;
   __nv_bfloat162 zz = int4_zero_pair(8), ss = bf16_pair(0);
   uint32_t e4 = 0;
-  if (fmt == kW4A16Mx) {
+  if (e8_unit_fmt(fmt)) {
     e4 = *reinterpret_cast<const uint32_t*>(unit + kUnitCodes + 4 * r);
   } else {
     ss = bf16_pair(*reinterpret_cast<const uint16_t*>(unit + kUnitCodes + 2 * r));
@@ -290,10 +320,13 @@ __global__ void dequant_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, i
   for (int c4 = 0; c4 < 4; ++c4) {
     const uint4 c = *reinterpret_cast<const uint4*>(unit + c4 * 2048 + r * 16);
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-    const float scale = pow2f(static_cast<int>((e4 >> (8 * c4)) & 0xFFu) - 127);
+    const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
+    const float scale = pow2f(static_cast<int>(ex) - 127);
+    const __nv_bfloat162 si = bits_bf16x2(mxint_scale_pair(ex));
     for (int j = 0; j < 4; ++j) {
       uint32_t o[4];
       if (fmt == kW4A16Mx) dq_mx_word(words[j], lut, scale, o);
+      else if (fmt == kW4A16MxInt) dq_int4_word(words[j], zz, si, o);
       else dq_int4_word(words[j], zz, ss, o);
       *reinterpret_cast<uint4*>(w + row * k + kb * 128 + (4 * c4 + j) * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -339,6 +372,9 @@ cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int
   } else if (fmt == kW4A16Mx || fmt == kW4A8Mx) {
     quant_mx_kernel<<<blocks_for(n * (k / 128) * 32, 256), 256, 0, st>>>(
         w, n, k, q_out, static_cast<uint8_t*>(scales_out));
+  } else if (fmt == kW4A16MxInt) {
+    quant_mxint_kernel<<<blocks_for(n * (k / 128) * 32, 256), 256, 0, st>>>(
+        w, n, k, q_out, static_cast<uint8_t*>(scales_out));
   } else {
     amax_f32_kernel<<<kAmaxBlocks, 256, 0, st>>>(w, n * k, ws);
     quant_nv_kernel<<<blocks_for(n * k / 4, 256), 256, 0, st>>>(
@@ -353,7 +389,7 @@ cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k
                              const uint8_t* q, const void* scales, const uint8_t* zeros, uint8_t* packed,
                              cudaStream_t st) {
   const int64_t n_pad = (n + 127) / 128 * 128;
-  if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
+  if (unit_fmt(fmt)) {
     transform_units_kernel<<<static_cast<unsigned>((n_pad / 128) * (k / 128)), 128, 0, st>>>(
         fmt, has_zero, n, k, q, scales, zeros, packed);
     return cudaGetLastError();
@@ -372,7 +408,7 @@ cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k
 cudaError_t launch_dequant(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, const uint8_t* packed,
                            __nv_bfloat16* w, cudaStream_t st) {
   const int64_t n_pad = (n + 127) / 128 * 128;
-  if (fmt == kW4A16Int4 || fmt == kW4A16Mx) {
+  if (unit_fmt(fmt)) {
     dequant_units_kernel<<<static_cast<unsigned>((n_pad / 128) * (k / 128)), 128, 0, st>>>(
         fmt, has_zero, n, k, packed, w);
     return cudaGetLastError();

@@ -13,9 +13,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libhm.so")
 
-W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4 = 1, 2, 3, 4
+W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4, W4A16_MXINT4 = 1, 2, 3, 4, 5
 FORMATS = {"w4a16_int4": W4A16_INT4, "w4a16_mxfp4": W4A16_MXFP4,
-           "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4}
+           "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4, "w4a16_mxint4": W4A16_MXINT4}
 
 
 class HmError(RuntimeError):
@@ -104,7 +104,7 @@ def quantize_weight(d, w, zeros=None):
     q = torch.empty((d.N, d.K // 2), dtype=torch.uint8, device=dev)
     if d.fmt == W4A16_INT4:
         scales = torch.empty((d.N, d.K // 128), dtype=torch.bfloat16, device=dev)
-    elif d.fmt in (W4A16_MXFP4, W4A8_MXFP4):
+    elif d.fmt in (W4A16_MXFP4, W4A8_MXFP4, W4A16_MXINT4):
         scales = torch.empty((d.N, d.K // 32), dtype=torch.uint8, device=dev)
     else:
         scales = torch.empty((d.N, d.K // 16), dtype=torch.uint8, device=dev)

@@ -40,6 +40,12 @@ class QuantWeight:
             self.std_s = torch.from_numpy(self.s.astype(np.uint8))
             pack = ol.pack_w4a16_mxfp4 if fmt == ol.FMT_W4A16_MXFP4 else ol.pack_w4a8_mxfp4
             self.packed_ref = pack(self.q, self.s)
+        elif fmt == ol.FMT_W4A16_MXINT4:
+            self.q, self.s = oq.quant_mxint4(w)
+            self.what = oq.dequant_mxint4(self.q, self.s)
+            self.std_q = pack_nibbles(self.q)            # two's-complement nibbles
+            self.std_s = torch.from_numpy(self.s.astype(np.uint8))
+            self.packed_ref = ol.pack_w4a16_mxint4(self.q, self.s)
         else:
             self.q, self.s, self.g = oq.quant_nvfp4(w)
             self.what = oq.dequant_nvfp4(self.q, self.s, self.g)

@@ -34,7 +34,8 @@ def test_exports_every_declared_symbol(hm):
 
 
 @pytest.mark.parametrize("fmt,n,k,hz", [(1, 4096, 4096, False), (1, 130, 256, True), (2, 256, 512, False),
-                                        (3, 7168, 7168, False), (4, 8192, 8192, False), (4, 100, 64, False)])
+                                        (3, 7168, 7168, False), (4, 8192, 8192, False), (4, 100, 64, False),
+                                        (5, 4096, 14336, False), (5, 130, 128, False)])
 def test_packed_size_matches_layout_spec(hm, fmt, n, k, hz):
     assert hm.packed_size(hm.desc(fmt, n, k, hz)) == L.packed_size(fmt, n, k, hz)
 
@@ -43,6 +44,9 @@ def test_packed_size_rejects_bad_shapes(hm):
     assert hm.packed_size(hm.desc(1, 128, 100)) == 0      # K not a multiple of 128
     assert hm.packed_size(hm.desc(4, 128, 96)) == 0       # NVFP4 K % 64
     assert hm.packed_size(hm.desc(2, 128, 128, True)) == 0  # zero-points only for INT4
+    assert hm.packed_size(hm.desc(5, 128, 128, True)) == 0
+    assert hm.packed_size(hm.desc(5, 128, 64)) == 0       # MXINT4 K % 128
+    assert hm.packed_size(hm.desc(6, 128, 128)) == 0
     assert hm.packed_size(hm.desc(9, 128, 128)) == 0
     assert hm.packed_size(hm.desc(1, 0, 128)) == 0
 
@@ -168,7 +172,7 @@ def test_oversized_schedule_rejected(hm):
 def test_plan_decode_kernel(hm, monkeypatch):
     """W4A16 formats at M <= 32 take the warp-MMA decode kernel (built for 8, 16 or 32 tokens);
     the block-scaled formats and M > 32 keep tcgen05; HM_GEMV=0 keeps tcgen05 for every M."""
-    for fmt in (1, 2):
+    for fmt in (1, 2, 5):
         tiles = [hm.plan(fmt, m, 4096, 4096, 152)["tile_m"] for m in range(1, 33)]
         assert tiles == [8] * 8 + [16] * 8 + [32] * 16
         assert all(hm.plan(fmt, m, 4096, 4096, 152)["kernel"] == 1 for m in range(1, 33))
@@ -178,6 +182,7 @@ def test_plan_decode_kernel(hm, monkeypatch):
     assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 0
     assert hm.plan(1, 16, 14336, 4096, 152)["kernel"] == 1
     assert hm.plan(2, 32, 14336, 4096, 152)["kernel"] == 1
+    assert hm.plan(5, 32, 14336, 4096, 152)["kernel"] == 1   # MXINT4 as MXFP4
     monkeypatch.setenv("HM_GEMV", "2")
     assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 1
     for fmt in (3, 4):
@@ -228,7 +233,7 @@ def test_workspace_covers_every_plan(hm):
     rng = random.Random(7)
     shapes = [(1, m, n, k) for m in (1, 8, 16, 17, 32, 33, 64, 200) for n, k in ((4096, 4096), (20480, 1024), (200, 128))]
     for _ in range(80):
-        fmt = rng.choice((1, 2, 3, 4))
+        fmt = rng.choice((1, 2, 3, 4, 5))
         shapes.append((fmt, rng.randint(1, 300), 128 * rng.randint(1, 200) - rng.choice((0, 2, 64)), 256 * rng.randint(1, 30)))
     for fmt, m, n, k in shapes:
         ws = hm.workspace_size(fmt, m, n, k)
