@@ -152,9 +152,13 @@ hm_status hm_quant_act_nvfp4(const void* x, int64_t M, int64_t K, const float* g
  * out[r][c] = bf16(SiLU(gate_up[r][c]) * gate_up[r][inter + c]), SiLU(v) = v / (1 + exp(-v))
  * evaluated in fp32 and rounded once to bf16 (round to nearest even). gate_up: device bf16
  * [rows][2*inter] (gate in the first half of each row, up in the second, as a gate-up GEMM with
- * N = 2*inter writes them); out: device bf16 [rows][inter]. inter % 8 == 0; both pointers
- * 16-byte aligned. rows = 0 is a no-op. Caller owns both buffers; nothing is allocated.
- * Returns HM_ERR_INVALID_ARG for bad sizes or pointers, HM_ERR_CUDA for a launch failure. */
+ * N = 2*inter writes them); out: device bf16 [rows][inter], not overlapping gate_up.
+ * inter % 8 == 0; both pointers 16-byte aligned. rows = 0 is a no-op. Caller owns both buffers;
+ * nothing is allocated. (The pages run expert MLPs of the DeepSeek models, the MoE paragraph of
+ * the explainer page's section "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다", without
+ * printing the activation; the gated SiLU of such experts is the reading taken.)
+ * Returns HM_ERR_INVALID_ARG for bad sizes, misaligned or overlapping buffers, HM_ERR_CUDA for a
+ * launch failure. */
 hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inter, void* stream);
 
 /* ---------------------------------------------------------------- GEMM */

@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <cstdlib>
 #include <algorithm>
 #include <cstring>
@@ -467,6 +468,11 @@ hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inte
   if (rows < 0 || inter <= 0 || inter % 8 != 0) return HM_ERR_INVALID_ARG;
   if (rows == 0) return HM_OK;
   if (gate_up == nullptr || out == nullptr || !aligned(gate_up, 16) || !aligned(out, 16)) return HM_ERR_INVALID_ARG;
+  if (rows > INT64_MAX / (4 * inter)) return HM_ERR_INVALID_ARG;
+  // out's rows are half as long as gate_up's, so an overlapping out would overwrite rows not yet read
+  const uintptr_t a = reinterpret_cast<uintptr_t>(gate_up), b = reinterpret_cast<uintptr_t>(out);
+  if (a < b + static_cast<uintptr_t>(rows * 2 * inter) && b < a + static_cast<uintptr_t>(rows * 4 * inter))
+    return HM_ERR_INVALID_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
   return cuda_status(launch_silu_mul(static_cast<const __nv_bfloat16*>(gate_up), static_cast<__nv_bfloat16*>(out),

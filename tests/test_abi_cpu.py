@@ -74,6 +74,10 @@ def test_invalid_arguments_fail_before_any_launch(hm):
     assert lib.hm_silu_mul(None, P(16), 4, 16, None) == 1
     assert lib.hm_silu_mul(P(18), P(16), 4, 16, None) == 1
     assert lib.hm_silu_mul(None, None, 0, 16, None) == 0
+    # 4 rows x (16 | 16) bf16 = 256 bytes in, 128 out: any overlap is refused before a CUDA call
+    assert lib.hm_silu_mul(P(4096), P(4096), 4, 16, None) == 1
+    assert lib.hm_silu_mul(P(4096), P(4096 + 240), 4, 16, None) == 1
+    assert lib.hm_silu_mul(P(4096 + 112), P(4096), 4, 16, None) == 1
     assert lib.hm_quant_act_nvfp4(P(16), 4, 96, None, P(16), P(16), P(16), None, 0, None) == 1
     assert lib.hm_quant_act_nvfp4(P(16), 4, 128, None, P(16), P(16), P(16), None, 0, None) == 3
 
