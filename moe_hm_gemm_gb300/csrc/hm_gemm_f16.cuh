@@ -129,6 +129,12 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if (MOE) {
+    // The MoE prefix warp may raise the abort flag while thread 0 is still setting up: clear the
+    // flag before any role runs, so that a raised flag is never overwritten.
+    if (threadIdx.x == 0) *abort_flag = 0u;
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     trace_mark(p.trace, 0);
     // Read the (first) weight header before initialising the barriers so that its memory
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     }
     mbar_init(drain, S::kIss);
     fence_barrier_init();
-    *abort_flag = 0u;
+    if (!MOE) *abort_flag = 0u;
     // The first weight's header decides whether INT4 units carry zero-points; every weight
     // used must agree with it and with the call's (fmt, N, K).
     const uint32_t hz = hdr.has_zero;

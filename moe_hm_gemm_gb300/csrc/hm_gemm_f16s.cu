@@ -112,6 +112,12 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if (MOE) {
+    // The MoE prefix warp may raise the abort flag while thread 0 is still setting up: clear the
+    // flag before any role runs, so that a raised flag is never overwritten.
+    if (threadIdx.x == 0) *abort_flag = 0u;
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     trace_mark(p.trace, 0);
     if (MOE) pdl_wait();   // expert pointers may come from the previous kernel
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
     }
     mbar_init(drain, NI);
     fence_barrier_init();
-    *abort_flag = 0u;
+    if (!MOE) *abort_flag = 0u;
     *hz_sh = hdr.has_zero == 1u ? 1u : 0u;
     if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
       atomicOr(p.err, kErrHeader);

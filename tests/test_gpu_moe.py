@@ -77,6 +77,24 @@ def test_bad_offsets_set_device_error(hm):
 
 
 @pytest.mark.parametrize("fmt", [1, 2])
+def test_offsets_past_rows_abort_before_any_store(hm, fmt):
+    """Offsets that run past the rows (here 100 > 8) set the offsets error and stop the kernel
+    before any tile is stored: the rows after Y keep their contents. INT4 runs the small-token
+    kernel at this size, MXFP4 the general one."""
+    n, k = 128, 256
+    qw = QuantWeight(fmt, synth.weights(n, k, seed=1))
+    _, packed = qw.transform(hm)
+    ptrs = torch.tensor([packed.data_ptr()], dtype=torch.int64, device="cuda")
+    x = synth.activations(8, k, seed=2).cuda()
+    y = torch.full((128, n), 7.0, dtype=torch.bfloat16, device="cuda")
+    offs = torch.tensor([0, 100], dtype=torch.int32, device="cuda")
+    hm.moe_gemm(fmt, x, offs, ptrs, n, k, out=y[:8])
+    torch.cuda.synchronize()
+    assert hm.device_error() & 4
+    assert (y[8:] == 7.0).all()
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
 @pytest.mark.parametrize("small", ["0", "1"])
 def test_small_tiles_both_kernels(hm, fmt, small, monkeypatch):
     """Token tiles of 16 and 32: INT4 runs the small-token kernel (the general kernel with
