@@ -192,9 +192,11 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
 /* Grouped GEMM over expert-sorted rows: for each expert e, rows
  * [expert_offsets[e], expert_offsets[e+1]) of x are multiplied by expert e's weight:
  * y[r,:] = x[r,:] * dequant(W_e)^T. expert_offsets: device int32 [E+1], non-decreasing,
- * offsets[0] = 0, offsets[E] = rows (read on the device only). packed: device array of E
- * device pointers, each a packed weight of the same (fmt, N, K). Formats HM_W4A16_INT4,
- * HM_W4A16_MXFP4 and HM_W4A16_MXINT4. Experts with no rows cost nothing. */
+ * offsets[0] = 0, offsets[E] <= rows (read on the device only; rows from offsets[E] on, e.g.
+ * padding, belong to no expert and their y rows are not written). Offsets that decrease, are
+ * negative, exceed rows or do not start at 0 set device error bit 2 and nothing is stored.
+ * packed: device array of E device pointers, each a packed weight of the same (fmt, N, K).
+ * Formats HM_W4A16_INT4, HM_W4A16_MXFP4 and HM_W4A16_MXINT4. Experts with no rows cost nothing. */
 hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
                       void* ws, size_t ws_bytes, void* stream);
