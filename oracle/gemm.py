@@ -64,11 +64,6 @@ def moe_gemm(x, offsets, what_per_expert):
     return y
 
 
-def gemm_entry(x, w, m, n):
-    """One output element sum_k x[m,k]*w[n,k] in fp64, for sampled checks at full size."""
-    return float(np.dot(np.asarray(x[m], dtype=np.float64), np.asarray(w[n], dtype=np.float64)))
-
-
 def tolerance_ok(y, yref, rel=1e-2, abs_rms=1e-2):
     """|Y - Yref| <= rel*|Yref| + abs_rms*rms(Yref), element-wise."""
     y = np.asarray(y, dtype=np.float64)

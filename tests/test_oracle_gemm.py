@@ -112,3 +112,16 @@ def test_w4a16_mxint4_exact_integer_case_and_brute_force():
     e = rng.integers(120, 131, size=(n, k // 32))
     w = np.array([[q[j, t] * 2.0 ** (int(e[j, t // 32]) - 127) for t in range(k)] for j in range(n)])
     np.testing.assert_array_equal(G.gemm_w4a16_mxint4(x.astype(np.float64), q, e), _brute(x, w))
+
+
+def test_w4a16_mxfp4_against_typed_e2m1_values():
+    # the e2m1 code table written out from the format definition (sign bit 3, then
+    # 0, 0.5, 1, 1.5, 2, 3, 4, 6), independent of the oracle's decoder, and a loop GEMM
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    rng = np.random.default_rng(8)
+    m, n, k = 2, 3, 64
+    codes = rng.integers(0, 16, size=(n, k))
+    e = rng.integers(124, 131, size=(n, k // 32))
+    x = rng.integers(-3, 4, size=(m, k)).astype(np.float64)
+    w = np.array([[table[codes[j, t]] * 2.0 ** (int(e[j, t // 32]) - 127) for t in range(k)] for j in range(n)])
+    np.testing.assert_array_equal(G.gemm_w4a16_mxfp4(x, codes, e), _brute(x, w))
