@@ -225,7 +225,9 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
 
 /* The kernel configuration hm_gemm would use: kernel, token tile, pipeline stages, split
  * (whether CTAs share one output tile along K) and grid size, for a device with `num_sms` SMs.
- * Host-only, no CUDA call. */
+ * Host-only, no CUDA call. With HM_LOG=1 in the environment, hm_plan, hm_gemm,
+ * hm_gemm_w4a16_noalloc and hm_moe_gemm print the configuration they take as one "[hm] ..." line
+ * on stderr. */
 typedef struct hm_plan_info {
   int32_t bucket;      /* M bucket index: 0: M<=16, 1: <=64, 2: <=256, 3: <=1024, 4: >1024 */
   int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension); decode kernel: tokens it

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <algorithm>
 #include <cstring>
@@ -287,6 +288,23 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
 // The kernels walk the (tile, k-block) space in 32-bit indices.
 bool plan_fits(const Plan& p) { return p.tiles * p.kb_total < (int64_t{1} << 31); }
 
+// HM_LOG=1: one line on stderr per planned call with the configuration it runs (for sweeps and
+// for checking which kernel a layer takes); off by default.
+bool log_on() {
+  static const bool on = env_int("HM_LOG", 0) != 0;
+  return on;
+}
+
+void log_plan(const char* entry, int32_t fmt, int64_t m, int64_t n, int64_t k, const Plan& p) {
+  if (!log_on()) return;
+  std::fprintf(stderr,
+               "[hm] %s fmt=%d M=%lld N=%lld K=%lld kernel=%s tile_m=%d tile_k=%d stages=%d stream_k=%d grid=%d "
+               "tiles=%lld\n",
+               entry, fmt, static_cast<long long>(m), static_cast<long long>(n), static_cast<long long>(k),
+               p.gemv ? "decode" : "tcgen05", p.tile_m, p.tile_k, p.stages, p.stream_k, p.grid,
+               static_cast<long long>(p.tiles));
+}
+
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -512,6 +530,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
       num_sms > kMaxSmsForSizing)
     return HM_ERR_INVALID_ARG;
   const Plan p = make_plan(fmt, M, N, K, num_sms);
+  log_plan("hm_plan", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   out->bucket = p.bucket;
   out->tile_m = p.tile_m;
@@ -540,6 +559,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (!device_info(&di)) return HM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  log_plan("hm_gemm", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
 
@@ -650,6 +670,9 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   int tile_m = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : (mean <= 256 ? 128 : 256)));
   const int forced = env_int("HM_MOE_TILE_M", 0);
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) tile_m = forced;
+  if (log_on())
+    std::fprintf(stderr, "[hm] hm_moe_gemm fmt=%d E=%d rows=%lld N=%lld K=%lld kernel=tcgen05 tile_m=%d grid=%d\n", fmt, E,
+                 static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K), tile_m, di.num_sms);
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
   if (!encode_x_f16(&prm.tmap_x, x, K, rows, tile_m)) return HM_ERR_CUDA;
@@ -680,6 +703,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   uint8_t* scratch = noalloc_scratch(di.dev);
   if (scratch == nullptr) return HM_ERR_CUDA;
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  log_plan("hm_gemm_w4a16_noalloc", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   // Partials for the CTAs of this launch, then the per-tile arrival counters.
   const size_t partial_bytes = align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float));

@@ -248,3 +248,21 @@ def test_workspace_covers_every_plan(hm):
             else:
                 need = (p["grid"] * 2 * p["tile_m"] * 128 * 4 if p["stream_k"] else 0) + p["tiles"] * 4 * 4
             assert ws >= need, (fmt, m, n, k, sms, p, ws, need)
+
+
+def test_plan_log_line(hm):
+    """HM_LOG=1 prints the configuration each planned call takes (stderr), nothing otherwise."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = "from moe_hm_gemm_gb300 import hm; hm.plan(1, 1, 14336, 4096, 152); hm.plan(4, 8192, 8192, 8192, 152)"
+    env = dict(os.environ, HM_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, check=True)
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[hm] ")]
+    assert len(lines) == 2
+    assert "fmt=1 M=1 N=14336 K=4096 kernel=decode tile_m=8" in lines[0]
+    assert "fmt=4 M=8192 N=8192 K=8192 kernel=tcgen05 tile_m=128 tile_k=256" in lines[1]
+    env.pop("HM_LOG")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, check=True)
+    assert "[hm]" not in r.stderr
