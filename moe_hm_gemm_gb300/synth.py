@@ -55,6 +55,29 @@ def moe_routing(tokens, experts=256, topk=8, alpha=1.1, seed=0):
     return tok[order], exp[order], offsets
 
 
+def moe_routing_slots(tokens, experts=256, topk=8, alpha=1.1, seed=0):
+    """moe_routing plus, for the combine after the grouped GEMMs, pos [T][topk] int32 (the sorted row
+    holding token t's j-th routing choice) and weights [T][topk] float32 (a softmax of N(0,1) logits
+    per token)."""
+    rng = np.random.default_rng(seed)
+    p = np.arange(1, experts + 1, dtype=np.float64) ** (-alpha)
+    p /= p.sum()
+    choice = np.stack([rng.choice(experts, topk, replace=False, p=p) for _ in range(tokens)]) \
+        if tokens else np.zeros((0, topk), dtype=np.int64)
+    tok = np.repeat(np.arange(tokens), topk)
+    exp = choice.reshape(-1).astype(np.int64)
+    order = np.argsort(exp, kind="stable")
+    counts = np.bincount(exp, minlength=experts)
+    offsets = np.zeros(experts + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    pos = np.empty(tokens * topk, dtype=np.int32)
+    pos[order] = np.arange(tokens * topk, dtype=np.int32)
+    logits = rng.standard_normal((tokens, topk))
+    wts = np.exp(logits - logits.max(axis=1, keepdims=True)) if tokens else logits
+    wts = (wts / wts.sum(axis=1, keepdims=True)).astype(np.float32) if tokens else wts.astype(np.float32)
+    return tok[order], exp[order], offsets, pos.reshape(tokens, topk), wts
+
+
 def device_weights(n, k, seed, device="cuda", std=0.02):
     g = torch.Generator(device=device)
     g.manual_seed(seed)
