@@ -233,12 +233,13 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     // With no more tiles than SMs, each tile is cut into the same number of K ranges, so every CTA
     // holds one range of one tile: no CTA publishes a shared tile in the middle of its work, and a
     // tile's contributors all finish together. With more tiles than SMs the ranges run across
-    // tile boundaries (one range per SM).
-    if (p.tiles <= num_sms) {
+    // tile boundaries (one range per SM). HM_SK_ALIGN=0 takes the latter everywhere (for sweeps:
+    // 112 whole tiles leave 40 of 152 SMs idle).
+    if (p.tiles <= num_sms && env_int("HM_SK_ALIGN", 1) != 0) {
       const int64_t per = std::min<int64_t>(num_sms / p.tiles, p.kb_total);
       p.grid = static_cast<int>(p.tiles * per);
     } else {
-      p.grid = num_sms;
+      p.grid = static_cast<int>(std::min<int64_t>(num_sms, p.tiles * p.kb_total));
     }
     p.stream_k = (p.grid > p.tiles || p.tiles % p.grid != 0) ? 1 : 0;   // some tile shared by CTAs
     return p;

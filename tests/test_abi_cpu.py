@@ -189,6 +189,12 @@ def test_plan_decode_kernel(hm, monkeypatch):
     assert hm.plan(5, 32, 14336, 4096, 152)["kernel"] == 1   # MXINT4 as MXFP4
     monkeypatch.setenv("HM_GEMV", "2")
     assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 1
+    # HM_SK_ALIGN=0: ranges across tile boundaries, one per SM (never more CTAs than units)
+    monkeypatch.setenv("HM_SK_ALIGN", "0")
+    p = hm.plan(1, 1, 14336, 4096, 152)
+    assert (p["grid"], p["stream_k"]) == (152, 1)
+    assert hm.plan(1, 1, 128, 256, 152)["grid"] == 2
+    monkeypatch.delenv("HM_SK_ALIGN")
     for fmt in (3, 4):
         assert hm.plan(fmt, 1, 4096, 4096, 152)["kernel"] == 0
     # 152 tiles of two 128-K blocks on 152 SMs: one whole tile per CTA, no split
