@@ -14,9 +14,10 @@ u32 has_zero, f32 tensor_scale, u64 payload_bytes, zeros up to 256 bytes.
 
 Formats: 1 = W4A16 INT4 (group 128, bf16 scales, optional u4 zero-points),
 2 = W4A16 MXFP4 (e2m1 + E8M0/32, bf16 activations), 3 = W4A8 MXFP4, 4 = W4A4 NVFP4,
-5 = W4A16 MXINT4 (signed int4 + E8M0/32, bf16 activations).
+5 = W4A16 MXINT4 (signed int4 + E8M0/32, bf16 activations), 6 = W4A16 INT4 with bf16 scales (and
+optional u4 zero-points) per 32 along K (inputs grouped by 32 or 64).
 
-Tiled payload (formats 1, 2, 5): one "unit" per (n_tile of 128 rows, k_block of 128),
+Tiled payload (formats 1, 2, 5, 6): one "unit" per (n_tile of 128 rows, k_block of 128),
 n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
   * nibble of (r, kk) lives in the 32-bit little-endian word at byte
     (kk//32)*2048 + r*16 + ((kk%32)//8)*4, at bit 4*((kk%8)//2) + 16*(kk%2);
@@ -25,7 +26,10 @@ n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
     unit = 8448 bytes, or 8512 with zero-points;
   * format 2: nibble = e2m1 code; E8M0 code of (r, kk//32) at byte 8192 + 4r + kk//32;
     unit = 8704 bytes;
-  * format 5: nibble u = q + 8; E8M0 codes as format 2; unit = 8704 bytes.
+  * format 5: nibble u = q + 8; E8M0 codes as format 2; unit = 8704 bytes;
+  * format 6: nibbles as format 1; bf16 scale of (r, kk//32) at byte 8192 + 8r + 2(kk//32); zero-point
+    of (r, kk//32) (if any) at byte 9216 + 2r + (kk//32)//2, bit 4((kk//32)%2); unit = 9216 bytes, or
+    9472 with zero-points.
 
 Row-major payload (formats 3, 4): codes as bytes [N_pad][K_pad/2] (even k in the low
 nibble), then scale-factor atoms of 512 bytes, atom (n_tile, kc) n_tile-major, where kc
@@ -52,7 +56,8 @@ from .formats import bf16_bits
 MAGIC = 0x31574D48
 HEADER = 256
 FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A8_MXFP4, FMT_W4A4_NVFP4, FMT_W4A16_MXINT4 = 1, 2, 3, 4, 5
-TILED = (FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A16_MXINT4)
+FMT_W4A16_INT4_G32 = 6
+TILED = (FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A16_MXINT4, FMT_W4A16_INT4_G32)
 TILE_N = 128
 ATOM = 512
 
@@ -71,6 +76,8 @@ def unit_bytes(fmt, has_zero):
         return 8512 if has_zero else 8448
     if fmt in (FMT_W4A16_MXFP4, FMT_W4A16_MXINT4):
         return 8704
+    if fmt == FMT_W4A16_INT4_G32:
+        return 9472 if has_zero else 9216
     raise ValueError(fmt)
 
 
@@ -119,7 +126,7 @@ def _pack_units(fmt, nibbles, scale_bytes_fn, zeros, n, k, has_zero):
             unit = np.zeros(ub, dtype=np.uint16)
             np.add.at(unit, off.ravel(), (tile << shift).ravel())
             scale_bytes_fn(unit, t, b)
-            if has_zero:
+            if has_zero and fmt == FMT_W4A16_INT4:
                 zr = zeros[t * 128:(t + 1) * 128, b].astype(np.uint16)
                 np.add.at(unit, 8448 + np.arange(128) // 2, zr << (4 * (np.arange(128) % 2)))
             out[t, b] = unit.astype(np.uint8)
@@ -148,6 +155,40 @@ def pack_w4a16_int4(q, s, zeros=None):
 
     pay = _pack_units(FMT_W4A16_INT4, nib, scales, z, n, k, has_zero)
     return np.concatenate([header(FMT_W4A16_INT4, n, k, has_zero, 1.0), pay])
+
+
+def pack_w4a16_int4_g32(q, s, zeros=None, group=32):
+    """q int [N,K] (signed without zero-points, unsigned with), s bf16 values [N,K/group], zeros ints
+    [N,K/group] or None, group 32 or 64 (a group of 64 fills two 32-K chunks). Returns the packed
+    buffer (uint8)."""
+    q = np.asarray(q)
+    n, k = q.shape
+    has_zero = zeros is not None
+    rep = group // 32
+    n_pad, k_pad = padded_dims(FMT_W4A16_INT4_G32, n, k)
+    nib = np.zeros((n_pad, k_pad), dtype=np.int64)
+    nib[:n, :k] = q if has_zero else q + 8
+    sbits = np.zeros((n_pad, k_pad // 32), dtype=np.uint16)
+    sbits[:n] = np.repeat(bf16_bits(s), rep, axis=1)
+    z = np.zeros((n_pad, k_pad // 32), dtype=np.int64)
+    if has_zero:
+        z[:n] = np.repeat(np.asarray(zeros, dtype=np.int64), rep, axis=1)
+    ub = unit_bytes(FMT_W4A16_INT4_G32, has_zero)
+    r = np.arange(128)
+
+    def scales(unit, t, b):
+        blk = sbits[t * 128:(t + 1) * 128, b * 4:(b + 1) * 4]        # [128, 4]
+        off = 8192 + 8 * r[:, None] + 2 * np.arange(4)[None, :]
+        unit[off] = blk & 0xFF
+        unit[off + 1] = blk >> 8
+        if has_zero:
+            zb = z[t * 128:(t + 1) * 128, b * 4:(b + 1) * 4]          # [128, 4]
+            unit[9216 + 2 * r] = zb[:, 0] | (zb[:, 1] << 4)
+            unit[9216 + 2 * r + 1] = zb[:, 2] | (zb[:, 3] << 4)
+
+    pay = _pack_units(FMT_W4A16_INT4_G32, nib, scales, None, n, k, has_zero)
+    assert pay.size == (n_pad // 128) * (k_pad // 128) * ub
+    return np.concatenate([header(FMT_W4A16_INT4_G32, n, k, has_zero, 1.0), pay])
 
 
 def _pack_e8_units(fmt, nibbles, e):

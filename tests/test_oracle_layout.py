@@ -140,3 +140,28 @@ def test_act_nvfp4_layout():
     assert body.shape == (70, 64) and atoms.size == L.act_scale_bytes(70, 128) == 2 * 512
     np.testing.assert_array_equal(L.unpack_codes_rowmajor(body, 70, 128), codes)
     np.testing.assert_array_equal(L.unpack_atoms(atoms, 70, 2), sb)
+
+
+@pytest.mark.parametrize("group,has_zero", [(32, True), (64, True), (32, False)])
+def test_int4_g32_units(group, has_zero):
+    """Per-32 INT4 units: nibbles as INT4, the bf16 scale of (r, chunk c) at 8192 + 8r + 2c and its
+    zero-point nibble at 9216 + 2r + c // 2, bit 4 (c % 2); a group of 64 fills two chunks."""
+    from oracle.formats import bf16_bits
+    rng = np.random.default_rng(9)
+    w = rng.standard_normal((130, 256)) * 0.02
+    z = rng.integers(0, 16, size=(130, 256 // group)) if has_zero else None
+    q, s = Q.quant_int4(w, zeros=z, group=group)
+    buf = L.pack_w4a16_int4_g32(q, s, z, group=group)
+    assert len(buf) == L.packed_size(L.FMT_W4A16_INT4_G32, 130, 256, has_zero) == 256 + 2 * 2 * (9472 if has_zero else 9216)
+    nib, units = L.unpack_units(buf)
+    np.testing.assert_array_equal(nib, q if has_zero else q + 8)
+    ub = 9472 if has_zero else 9216
+    units = units.reshape(2, 2, ub)
+    row, kk = 129, 200                       # n-tile 1, k-block 1, chunk (200 % 128) // 32 = 2
+    unit = units[1, 1]
+    rr, c = row - 128, (kk % 128) // 32
+    sb = int(unit[8192 + 8 * rr + 2 * c]) | (int(unit[8192 + 8 * rr + 2 * c + 1]) << 8)
+    assert sb == int(bf16_bits(s[row, kk // group]))
+    if has_zero:
+        zn = (int(unit[9216 + 2 * rr + c // 2]) >> (4 * (c % 2))) & 0xF
+        assert zn == z[row, kk // group]
