@@ -81,6 +81,22 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _dev(*named):
+    """The C ABI takes raw device pointers: every tensor passed must be a contiguous CUDA tensor
+    (None is passed through as NULL). Raises ValueError otherwise."""
+    for name, t in named:
+        if t is not None and (not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name}: expected a contiguous CUDA tensor")
+
+
+def _out(y, shape, name="out"):
+    """An output tensor given by the caller: contiguous CUDA bf16 of exactly `shape`."""
+    _dev((name, y))
+    if y.dtype != torch.bfloat16 or tuple(y.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected bf16 {tuple(shape)}, got {y.dtype} {tuple(y.shape)}")
+    return y
+
+
 def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
@@ -100,6 +116,9 @@ def packed_size(d):
 
 def quantize_weight(d, w, zeros=None):
     """fp32 W [N,K] (device) -> (q [N,K/2] uint8, scales, g) in the standard format."""
+    _dev(("w", w), ("zeros", zeros))
+    if w.dtype != torch.float32:
+        raise ValueError("w: expected float32")
     dev = w.device
     q = torch.empty((d.N, d.K // 2), dtype=torch.uint8, device=dev)
     if d.fmt == W4A16_INT4:
@@ -124,6 +143,7 @@ def alloc_packed(d, device="cuda"):
 
 
 def transform(d, q, scales, zeros=None, out=None):
+    _dev(("q", q), ("scales", scales), ("zeros", zeros), ("out", out))
     packed = alloc_packed(d, q.device) if out is None else out
     _check(_lib.hm_transform(ctypes.byref(d), _ptr(q), _ptr(scales), _ptr(zeros), _ptr(packed), _stream()),
            "hm_transform")
@@ -131,12 +151,14 @@ def transform(d, q, scales, zeros=None, out=None):
 
 
 def dequant(d, packed):
+    _dev(("packed", packed))
     w = torch.empty((d.N, d.K), dtype=torch.bfloat16, device=packed.device)
     _check(_lib.hm_dequant(ctypes.byref(d), _ptr(packed), _ptr(w), _stream()), "hm_dequant")
     return w
 
 
 def quant_act_fp8(x):
+    _dev(("x", x))
     m, k = x.shape
     xq = torch.empty((m, k), dtype=torch.uint8, device=x.device)
     s = torch.empty((m,), dtype=torch.float32, device=x.device)
@@ -156,6 +178,7 @@ def silu_mul(gate_up, inter, out=None):
 
 
 def quant_act_nvfp4(x, g_in=None):
+    _dev(("x", x), ("g_in", g_in))
     m, k = x.shape
     xq = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
     xs = torch.empty((max(_lib.hm_act_scale_size(m, k), 1),), dtype=torch.uint8, device=x.device)
@@ -177,8 +200,9 @@ def alloc_workspace(fmt, m, n, k, device="cuda"):
 
 
 def gemm(fmt, x, packed, n, k, x_scale=None, x_global=None, ws=None, out=None):
+    _dev(("x", x), ("packed", packed), ("x_scale", x_scale), ("x_global", x_global), ("ws", ws))
     m = x.shape[0]
-    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (m, n))
     if ws is None:
         ws = alloc_workspace(fmt, m, n, k, x.device)
     _check(_lib.hm_gemm(int(fmt), _ptr(x), _ptr(x_scale), _ptr(x_global), _ptr(packed), _ptr(y), m, n, k,
@@ -188,8 +212,9 @@ def gemm(fmt, x, packed, n, k, x_scale=None, x_global=None, ws=None, out=None):
 
 def gemm_noalloc(fmt, x, packed, n, k, out=None):
     """W4A16 GEMM through the allocation-free entry point (scratch inside the library)."""
+    _dev(("x", x), ("packed", packed))
     m = x.shape[0]
-    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (m, n))
     _check(_lib.hm_gemm_w4a16_noalloc(int(fmt), _ptr(x), _ptr(packed), _ptr(y), m, n, k, _stream()),
            "hm_gemm_w4a16_noalloc")
     return y
@@ -197,9 +222,12 @@ def gemm_noalloc(fmt, x, packed, n, k, out=None):
 
 def moe_gemm(fmt, x, offsets, packed_ptrs, n, k, out=None, ws=None):
     """x: expert-sorted rows [R,K] bf16; offsets int32 [E+1] (device); packed_ptrs int64 [E] (device)."""
+    _dev(("x", x), ("offsets", offsets), ("packed_ptrs", packed_ptrs), ("ws", ws))
+    if offsets.dtype != torch.int32 or packed_ptrs.dtype != torch.int64 or packed_ptrs.numel() != offsets.numel() - 1:
+        raise ValueError("offsets: int32 [E+1]; packed_ptrs: int64 [E]")
     rows = x.shape[0]
     e = offsets.numel() - 1
-    y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (rows, n))
     wsz = 0 if ws is None else ws.numel()
     _check(_lib.hm_moe_gemm(int(fmt), _ptr(x), _ptr(offsets), e, _ptr(packed_ptrs), _ptr(y), rows, n, k,
                             _ptr(ws), wsz, _stream()), "hm_moe_gemm")

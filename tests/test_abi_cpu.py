@@ -272,3 +272,27 @@ def test_plan_log_line(hm):
     env.pop("HM_LOG")
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, check=True)
     assert "[hm]" not in r.stderr
+
+
+def test_binding_rejects_host_and_strided_tensors(hm):
+    """The binding hands raw pointers to the C ABI, so it refuses host tensors, strided views and
+    mis-shaped outputs before any call."""
+    import torch
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    packed = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        hm.gemm(1, x, packed, 128, 256)
+    with pytest.raises(ValueError):
+        hm.gemm_noalloc(1, x, packed, 128, 256)
+    with pytest.raises(ValueError):
+        hm.moe_gemm(1, x, torch.zeros(3, dtype=torch.int32), torch.zeros(2, dtype=torch.int64), 128, 256)
+    with pytest.raises(ValueError):
+        hm.quant_act_fp8(x)
+    with pytest.raises(ValueError):
+        hm.quant_act_nvfp4(x[:, ::2])
+    with pytest.raises(ValueError):
+        hm.quantize_weight(hm.desc(1, 128, 256), torch.zeros((128, 256)))
+    with pytest.raises(ValueError):
+        hm.transform(hm.desc(1, 128, 256), packed, packed)
+    with pytest.raises(ValueError):
+        hm.dequant(hm.desc(1, 128, 256), packed)
