@@ -63,6 +63,21 @@ class QuantWeight:
         return d, hm.transform(d, q, s, z)
 
 
+CANARY = -3.0
+CANARY_ROWS = 3
+
+
+def canary_out(m, n):
+    """An output of m bf16 rows followed by CANARY_ROWS rows of CANARY in one buffer; returns
+    (buffer, its first m rows). A kernel that stores past row m - 1 overwrites the canary."""
+    full = torch.full((m + CANARY_ROWS, n), CANARY, dtype=torch.bfloat16, device="cuda")
+    return full, full[:m]
+
+
+def check_canary(full, m, what=""):
+    assert bool((full[m:] == CANARY).all()), f"{what}: a kernel wrote past the {m} output rows"
+
+
 def assert_close(y_gpu, yref, what=""):
     y = y_gpu.float().cpu().numpy().astype(np.float64)
     ok = og.tolerance_ok(y, yref)

@@ -10,7 +10,7 @@ from moe_hm_gemm_gb300 import synth
 from oracle import gemm as og
 from oracle import quant as oq
 
-from .gpu_util import QuantWeight, assert_close, bf16_np
+from .gpu_util import QuantWeight, assert_close, bf16_np, canary_out, check_canary
 
 pytestmark = pytest.mark.gpu
 
@@ -37,13 +37,15 @@ def w4a8_case(hm, m, n, k, seed=0, explicit=False):
     x = synth.activations(m, k, seed=seed + 1, outlier_frac=0.01)
     xq, st = oq.quant_fp8_per_token(bf16_np(x))
     yref = og.gemm_w4a8_mxfp4(xq, st, qw.q, qw.s)
+    full, y = canary_out(m, n)
     if explicit:
         gq, gs = hm.quant_act_fp8(x.cuda())
-        y = hm.gemm(3, gq, packed, n, k, x_scale=gs)
+        hm.gemm(3, gq, packed, n, k, x_scale=gs, out=y)
     else:
-        y = hm.gemm(3, x.cuda(), packed, n, k)
+        hm.gemm(3, x.cuda(), packed, n, k, out=y)
     torch.cuda.synchronize()
     assert_close(y, yref, f"w4a8 m={m} n={n} k={k}")
+    check_canary(full, m, f"w4a8 m={m} n={n} k={k}")
     assert hm.device_error() == 0
 
 
@@ -53,13 +55,15 @@ def w4a4_case(hm, m, n, k, seed=0, explicit=False):
     x = synth.activations(m, k, seed=seed + 1)
     xc, xsb, gx = oq.quant_nvfp4(bf16_np(x))
     yref = og.gemm_w4a4_nvfp4(xc, xsb, gx, qw.q, qw.s, qw.g)
+    full, y = canary_out(m, n)
     if explicit:
         gq, gs, gg = hm.quant_act_nvfp4(x.cuda())
-        y = hm.gemm(4, gq, packed, n, k, x_scale=gs, x_global=gg)
+        hm.gemm(4, gq, packed, n, k, x_scale=gs, x_global=gg, out=y)
     else:
-        y = hm.gemm(4, x.cuda(), packed, n, k)
+        hm.gemm(4, x.cuda(), packed, n, k, out=y)
     torch.cuda.synchronize()
     assert_close(y, yref, f"w4a4 m={m} n={n} k={k}")
+    check_canary(full, m, f"w4a4 m={m} n={n} k={k}")
     assert hm.device_error() == 0
 
 

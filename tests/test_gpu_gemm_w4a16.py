@@ -11,7 +11,7 @@ from moe_hm_gemm_gb300 import synth
 from oracle import gemm as og
 from oracle import quant as oq
 
-from .gpu_util import QuantWeight, assert_close, bf16_np
+from .gpu_util import QuantWeight, assert_close, bf16_np, canary_out, check_canary
 
 pytestmark = pytest.mark.gpu
 
@@ -38,10 +38,12 @@ def run_case(hm, fmt, m, n, k, has_zero, seed=0):
     qw = QuantWeight(fmt, w, z)
     _, packed = qw.transform(hm)
     x = synth.activations(m, k, seed=seed + 2)
-    y = hm.gemm(fmt, x.cuda(), packed, n, k)
+    full, y = canary_out(m, n)
+    hm.gemm(fmt, x.cuda(), packed, n, k, out=y)
     torch.cuda.synchronize()
     yref = og.gemm(bf16_np(x), qw.what)
     assert_close(y, yref, f"fmt={fmt} m={m} n={n} k={k} zp={has_zero}")
+    check_canary(full, m, f"fmt={fmt} m={m} n={n} k={k}")
     assert hm.device_error() == 0
 
 

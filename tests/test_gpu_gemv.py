@@ -14,7 +14,7 @@ from moe_hm_gemm_gb300 import synth
 from oracle import gemm as og
 from oracle import quant as oq
 
-from .gpu_util import QuantWeight, assert_close, bf16_np
+from .gpu_util import QuantWeight, assert_close, bf16_np, canary_out, check_canary
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,8 @@ def check(hm, fmt, m, n, k, has_zero, seed):
     try:
         p = hm.plan(fmt, m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)
         assert p["kernel"] == 1 and p["tile_m"] >= m
-        y = hm.gemm(fmt, x.cuda(), packed, n, k)
+        full, y = canary_out(m, n)
+        hm.gemm(fmt, x.cuda(), packed, n, k, out=y)
         torch.cuda.synchronize()
     finally:
         if saved is None:
@@ -60,6 +61,7 @@ def check(hm, fmt, m, n, k, has_zero, seed):
         else:
             os.environ["HM_GEMV"] = saved
     assert_close(y, og.gemm(bf16_np(x), qw.what), f"fmt={fmt} m={m} n={n} k={k} zp={has_zero}")
+    check_canary(full, m, f"decode m={m} n={n} k={k}")
     assert hm.device_error() == 0
     return p
 

@@ -7,7 +7,7 @@ import torch
 from moe_hm_gemm_gb300 import synth
 from oracle import gemm as og
 
-from .gpu_util import QuantWeight, assert_close, bf16_np
+from .gpu_util import QuantWeight, assert_close, bf16_np, canary_out, check_canary
 
 pytestmark = pytest.mark.gpu
 
@@ -33,10 +33,12 @@ def moe_case(hm, fmt, counts, n, k, has_zero=False, seed=0, gain=1.0):
         packs.append(qw.transform(hm)[1])
     ptrs = torch.tensor([p.data_ptr() for p in packs], dtype=torch.int64, device="cuda")
     x = synth.activations(rows, k, seed=seed + 999)
-    y = hm.moe_gemm(fmt, x.cuda(), torch.from_numpy(offsets).cuda(), ptrs, n, k)
+    full, y = canary_out(rows, n)
+    hm.moe_gemm(fmt, x.cuda(), torch.from_numpy(offsets).cuda(), ptrs, n, k, out=y)
     torch.cuda.synchronize()
     yref = og.moe_gemm(bf16_np(x), offsets, [q.what for q in qws])
     assert_close(y, yref, f"moe fmt={fmt} counts={counts}")
+    check_canary(full, rows, f"moe fmt={fmt} counts={counts}")
     assert hm.device_error() == 0
     return y
 

@@ -11,7 +11,7 @@ from moe_hm_gemm_gb300 import synth
 from oracle import gemm as og
 from oracle import quant as oq
 
-from .gpu_util import QuantWeight, assert_close, bf16_np, pack_nibbles
+from .gpu_util import QuantWeight, assert_close, bf16_np, canary_out, check_canary, pack_nibbles
 
 pytestmark = pytest.mark.gpu
 
@@ -38,9 +38,11 @@ def weight(hm, n, k, seed, gain=1.0):
 def gemm_case(hm, m, n, k, seed=0, gain=1.0, what=""):
     qw, packed = weight(hm, n, k, seed, gain)
     x = synth.activations(m, k, seed=seed + 2)
-    y = hm.gemm(FMT, x.cuda(), packed, n, k)
+    full, y = canary_out(m, n)
+    hm.gemm(FMT, x.cuda(), packed, n, k, out=y)
     torch.cuda.synchronize()
     assert_close(y, og.gemm(bf16_np(x), qw.what), f"mxint4 m={m} n={n} k={k} {what}")
+    check_canary(full, m, f"mxint4 m={m} n={n} k={k}")
     assert hm.device_error() == 0
 
 
