@@ -207,8 +207,8 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
 // 14336 layers). Up to 16 tokens always; for 17..32 tokens MXFP4 and MXINT4 (no small-token
 // tcgen05 kernel) always, INT4 when the tcgen05 plan would split tiles along K (the decode
 // kernel's K ranges are cheaper there; with a whole tile per CTA the tcgen05 small-token kernel
-// is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2
-// takes the decode kernel for every M it serves (tests, sweeps).
+// is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2 takes the decode kernel for every M
+// it serves (tests, sweeps).
 bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (!unit_fmt(fmt)) return false;
   if (m < 1 || m > kGemvMaxTokens) return false;
