@@ -296,3 +296,37 @@ def test_binding_rejects_host_and_strided_tensors(hm):
         hm.transform(hm.desc(1, 128, 256), packed, packed)
     with pytest.raises(ValueError):
         hm.dequant(hm.desc(1, 128, 256), packed)
+
+
+def test_plan_invariants_random(hm):
+    """For random formats, shapes and SM counts the plan satisfies what the kernels rely on: every
+    CTA holds at least one k-block (grid <= tiles x k-blocks), at most one CTA per SM for W4A16 and
+    two for the block-scaled kernels, tiles = token tiles x 128-row tiles, the decode kernel only for
+    W4A16 formats at M <= 32 with a token tile covering M, token tiles the kernels are built for, a
+    split flag whenever CTAs share a tile, and at least two pipeline stages."""
+    import random
+    rng = random.Random(11)
+    for _ in range(3000):
+        fmt = rng.choice((1, 2, 3, 4, 5))
+        m = rng.choice((1, 2, 8, 15, 16, 17, 31, 32, 33, 64, 100, 256, 1000, 4096, 9000))
+        n = 128 * rng.randint(1, 160) - rng.choice((0, 2, 64))
+        k = (256 if fmt == 4 else 128) * rng.randint(1, 60)
+        sms = rng.choice((1, 2, 7, 64, 148, 152, 160, 256))
+        p = hm.plan(fmt, m, n, k, sms)
+        n_tiles = -(-n // 128)
+        kb_total = k // p["tile_k"]
+        assert p["tile_k"] == (256 if fmt == 4 else 128)
+        assert p["stages"] >= 2
+        if p["kernel"] == 1:
+            assert fmt in (1, 2, 5) and m <= 32 and p["tile_m"] in (8, 16, 32) and p["tile_m"] >= m
+            assert p["tiles"] == n_tiles
+        else:
+            assert p["tile_m"] in ((16, 32, 64, 128) if fmt in (3, 4) else (16, 32, 64, 128, 256))
+            assert p["tiles"] == -(-m // p["tile_m"]) * n_tiles
+            if fmt == 4 and m > 16:
+                assert p["tile_m"] == 128          # its activation scale atoms hold 128 rows
+        per_sm = 2 if fmt in (3, 4) and p["kernel"] == 0 else 1
+        assert 1 <= p["grid"] <= sms * per_sm
+        assert p["grid"] <= p["tiles"] * kb_total, (fmt, m, n, k, sms, p)
+        if p["grid"] > p["tiles"]:
+            assert p["stream_k"] == 1
