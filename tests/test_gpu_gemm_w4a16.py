@@ -95,9 +95,9 @@ def test_repeated_calls_reuse_workspace(hm):
             assert torch.equal(first, y)      # deterministic split-K reduction
 
 
-def test_full_size_sampled(hm):
-    """The 14336 x 4096 layer at M = 8192 and M = 1, checked on sampled outputs."""
-    n, k = 14336, 4096
+@pytest.mark.parametrize("n,k", [(14336, 4096), (4096, 4096), (4096, 14336)])
+def test_full_size_sampled(hm, n, k):
+    """The benchmark's three W4A16 layers at M = 8192 and M = 1, checked on sampled outputs."""
     w = synth.weights(n, k, seed=1)
     z = synth.zero_points(n, k // 128, seed=2)
     q, s = oq.quant_int4(w, zeros=z)
