@@ -100,14 +100,14 @@ def test_forced_stream_k(hm, env, stream_k):
     w4a4_case(hm, 20, 256, 2048, seed=9)
 
 
-@pytest.mark.parametrize("fmt", [3, 4])
-def test_full_size_sampled(hm, fmt):
-    n, k = (18432, 7168) if fmt == 3 else (8192, 8192)
+@pytest.mark.parametrize("fmt,n,k", [(3, 18432, 7168), (3, 7168, 7168), (4, 8192, 8192)])
+def test_full_size_sampled(hm, fmt, n, k):
+    """The benchmark's block-scaled layers at M = 1, 1024 and 8192, checked on sampled outputs."""
     w = synth.weights(n, k, seed=2)
     qw = QuantWeight(fmt, w)
     _, packed = qw.transform(hm)
     rng = np.random.default_rng(1)
-    for m in (1, 1024):
+    for m in (1, 1024, 8192):
         x = synth.activations(m, k, seed=3, outlier_frac=0.01 if fmt == 3 else 0.0)
         y = hm.gemm(fmt, x.cuda(), packed, n, k)
         torch.cuda.synchronize()
@@ -119,8 +119,9 @@ def test_full_size_sampled(hm, fmt):
             from oracle.formats import decode_e4m3
             xhat = decode_e4m3(xq) * st[:, None]
         else:
-            xc, xsb, gx = oq.quant_nvfp4(xv)            # the tensor scale needs all of X
-            xhat = oq.dequant_nvfp4(xc[ms], xsb[ms], gx)
+            gx = oq.nvfp4_global_scale(xv)              # the tensor scale needs all of X
+            xc, xsb, _ = oq.quant_nvfp4(xv[ms], g=gx)   # the 16-blocks are row-local
+            xhat = oq.dequant_nvfp4(xc, xsb, gx)
         ref = np.einsum("ik,ik->i", xhat, qw.what[ns])
         got = bf16_np(y.cpu()[torch.from_numpy(ms), torch.from_numpy(ns)])
         ok = og.tolerance_ok(got, ref)
