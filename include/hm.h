@@ -83,7 +83,11 @@ typedef struct hm_weight_desc {
 /* ---------------------------------------------------------------- preprocessing (once) */
 
 /* Bytes of the packed weight buffer for `desc` (256-byte header + padded payload), or 0 if
- * the description is invalid. Host-only, no CUDA call. */
+ * the description is invalid. Host-only, no CUDA call. The payload keeps the byte accounting of
+ * the explainer page, section "4비트 값에는 스케일이라는 해석 규칙이 붙는다" (128 INT4 values
+ * and one 16-bit scale take 66 bytes), plus one byte per 128 values for INT4 zero-points and one
+ * scale byte per 32 (MX) or 16 (NVFP4) values, with N padded to 128 and K to the kernel block as
+ * the preprocessing step of section "표현을 맞춘 다음 GPU가 읽기 좋은 배치로 바꾼다" pads them. */
 size_t hm_packed_size(const hm_weight_desc* desc);
 
 /* Quantize an fp32 weight W[N,K] (device) into the standard format by round-to-nearest
@@ -125,7 +129,11 @@ hm_status hm_transform(const hm_weight_desc* desc, const void* q, const void* sc
 
 /* Test hook: restore the packed weight to bf16 W[N,K] (device). Bit-exact definition of the
  * restored values used by the GEMM (bf16((q-z)*s), e2m1*2^(e-127), or, for NVFP4,
- * bf16(e2m1*sb) without the tensor scale, exact). */
+ * bf16(e2m1*sb) without the tensor scale, exact): the "restore s*q" step of the explainer page,
+ * section "4비트 값에는 스케일이라는 해석 규칙이 붙는다", which the GEMM kernels perform in
+ * registers ("read and unpack", section "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다").
+ * w_bf16 must be 16-byte aligned, packed 256-byte aligned; HM_ERR_INVALID_ARG otherwise. A header
+ * that does not match `desc` sets device error bit 0 and leaves w_bf16 unwritten. */
 hm_status hm_dequant(const hm_weight_desc* desc, const void* packed, void* w_bf16, void* stream);
 
 /* ---------------------------------------------------------------- activations (per call) */
@@ -164,13 +172,20 @@ hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inte
 /* ---------------------------------------------------------------- GEMM */
 
 /* Workspace bytes hm_gemm / hm_moe_gemm need for this problem (split-K partials and tile
- * counters, internal activation quantization). Host-only. `M` is rows for MoE. */
+ * counters, internal activation quantization). Host-only. `M` is rows for MoE. The split of K
+ * across CTAs for decode-sized M has no passage on the pages (they name only the M-dependent
+ * choice of tile shape and stages, aihaber.org, section "Mimari", "Tuning Config"); the
+ * workspace holds its fp32 partial tiles. Returns 0 for an invalid format or shape. */
 size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
 
 /* The workspace must be zero-filled once after allocation (cudaMemset); the library leaves
  * the counters it uses back at zero after every call, so it can be reused across calls. */
 
-/* Y[M,N] (bf16) = X[M,K] * dequant(W)^T.
+/* Y[M,N] (bf16) = X[M,K] * dequant(W)^T: the linear layer of the explainer page, section
+ * "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다" (weights W[N,K] read once and reused
+ * over the M rows), with the per-call activations of section "표현을 맞춘 다음 GPU가 읽기 좋은
+ * 배치로 바꾼다" (layer(inputs) after transform()) and the A16 / A8 / A4 activation formats of
+ * section "가중치 형식, 활성값, 백엔드를 한 줄에 적는다" and the news pages' format list.
  *  HM_W4A16_INT4 / HM_W4A16_MXFP4 / HM_W4A16_MXINT4 : x = bf16 [M][K]; x_scale, x_global ignored.
  *  HM_W4A8_MXFP4 : x = e4m3 [M][K] with x_scale = s_tok fp32 [M]; or, when x_scale is NULL,
  *                  x = bf16 [M][K] quantized internally (hm_quant_act_fp8) into `ws`.
@@ -189,7 +204,10 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
                   const void* packed, void* y, int64_t M, int64_t N, int64_t K, void* ws,
                   size_t ws_bytes, void* stream);
 
-/* Grouped GEMM over expert-sorted rows: for each expert e, rows
+/* Grouped GEMM over expert-sorted rows (the MoE paragraph of the explainer page, section
+ * "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다": tokens are split by expert, so each
+ * expert multiplies its own number of rows; the grouped kernel of aihaber.org, section
+ * "Performans"): for each expert e, rows
  * [expert_offsets[e], expert_offsets[e+1]) of x are multiplied by expert e's weight:
  * y[r,:] = x[r,:] * dequant(W_e)^T. expert_offsets: device int32 [E+1], non-decreasing,
  * offsets[0] = 0, offsets[E] <= rows (read on the device only; rows from offsets[E] on, e.g.
@@ -207,13 +225,16 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
  * device memory at all: for example code running inside another engine's fixed memory plan
  * (a plugin that is handed no workspace), or code that must not call cudaMalloc because it
  * synchronises the device. It runs the same kernel as hm_gemm, but the split-K partials and
- * tile counters live in an 8 MiB array inside the library (held by every GPU that loads the
+ * tile counters live in a 20 MiB array inside the library (held by every GPU that loads the
  * library until the process exits), so the caller passes only X, the packed weight and Y.
  * Arguments and layouts are those of hm_gemm. The call allocates nothing (no cudaMalloc,
- * cudaFree or allocating library routine); it clears the counters it needs with
- * cudaMemsetAsync on `stream` at every call.
- * Limits: problems whose split-K scratch exceeds 8 MiB (roughly M > 64 with stream-K on a
- * 152-SM GB300, or very tall N) return HM_ERR_WORKSPACE; use hm_gemm with a workspace then.
+ * cudaFree or allocating library routine). A plan that shares output tiles between CTAs clears
+ * its counters with cudaMemsetAsync on `stream` at every call; a plan in which every CTA owns
+ * whole tiles (no stream-K, or stream-K ranges that are whole tiles) uses no scratch at all.
+ * Limits: a split plan whose partials (CTAs x 2 x token tile x 128 fp32) and counters exceed
+ * 20 MiB returns HM_ERR_WORKSPACE; use hm_gemm with a workspace then. On a 152-SM GB300 the
+ * planner's own splits need at most 19 MiB (152 CTAs sharing 128-token tiles), so every M is
+ * accepted there; only splits forced through HM_TILE_M / HM_STREAM_K can exceed the array.
  * All calls share the one array: calls that overlap on the GPU (on different streams, or from
  * several threads) race and must be serialised by the caller.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with

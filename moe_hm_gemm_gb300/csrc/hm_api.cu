@@ -371,7 +371,9 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 // Scratch for hm_gemm_w4a16_noalloc: a fixed array in the library's own device memory, so that
 // callers who may not allocate still get the split-K schedule. Every GPU that loads the library
 // holds these bytes until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+// 20 MiB: the largest split the planner makes on a 152-SM GB300 (152 CTAs sharing tiles of 128
+// tokens) needs 19 MiB of partials plus its counters.
+constexpr size_t kNoAllocScratchBytes = size_t(20) << 20;
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 uint8_t* g_noalloc_ptr[kMaxDevices] = {};
 
@@ -706,15 +708,20 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
   log_plan("hm_gemm_w4a16_noalloc", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
-  // Partials for the CTAs of this launch, then the per-tile arrival counters.
-  const size_t partial_bytes = align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float));
+  // Partials for the CTAs of this launch, then the per-tile arrival counters. Only a plan that
+  // shares tiles between CTAs touches them: without stream-K, or with stream-K ranges that cover
+  // whole tiles (as many CTAs as tiles, or a whole number of tiles per CTA), every CTA owns its
+  // tiles outright and the call needs no scratch at all.
+  const bool shared = p.stream_k && (p.grid > p.tiles || p.tiles % p.grid != 0);
+  const size_t partial_bytes =
+      shared ? align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float)) : 0;
   const size_t counter_bytes =
-      align_up(static_cast<size_t>(p.tiles) * (p.gemv ? kGemvCounters : 4) * sizeof(uint32_t));
+      shared ? align_up(static_cast<size_t>(p.tiles) * (p.gemv ? kGemvCounters : 4) * sizeof(uint32_t)) : 0;
   if (partial_bytes + counter_bytes > kNoAllocScratchBytes) return HM_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The counters must start at zero; clear them on every call (cheap, and safe even after a
   // call that stopped early on a device error).
-  if (p.stream_k && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
+  if (shared && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
   if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))

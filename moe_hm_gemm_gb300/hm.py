@@ -199,12 +199,29 @@ def alloc_workspace(fmt, m, n, k, device="cuda"):
     return torch.zeros((max(workspace_size(fmt, m, n, k), 256),), dtype=torch.uint8, device=device)
 
 
+_WS_CACHE = {}
+
+
+def cached_workspace(fmt, m, n, k, device):
+    """A zero-initialised workspace kept per (device, current stream) and grown on demand, so that
+    calls without `ws` allocate only when a problem needs more than any earlier one did (the
+    library leaves its counters at zero after every call, so the buffer is reused as it is).
+    Calls on one stream are ordered, so they may share it; other streams get their own."""
+    need = max(workspace_size(fmt, m, n, k), 256)
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _WS_CACHE.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros((need,), dtype=torch.uint8, device=device)
+        _WS_CACHE[key] = ws
+    return ws
+
+
 def gemm(fmt, x, packed, n, k, x_scale=None, x_global=None, ws=None, out=None):
     _dev(("x", x), ("packed", packed), ("x_scale", x_scale), ("x_global", x_global), ("ws", ws))
     m = x.shape[0]
     y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (m, n))
     if ws is None:
-        ws = alloc_workspace(fmt, m, n, k, x.device)
+        ws = cached_workspace(fmt, m, n, k, x.device)
     _check(_lib.hm_gemm(int(fmt), _ptr(x), _ptr(x_scale), _ptr(x_global), _ptr(packed), _ptr(y), m, n, k,
                         _ptr(ws), ws.numel(), _stream()), "hm_gemm")
     return y
@@ -241,7 +258,12 @@ def plan(fmt, m, n, k, num_sms):
 
 
 def device_error():
-    return int(_lib.hm_get_device_error(_stream()))
+    """Returns and clears the device error word. A call that stopped early may leave arrival
+    counters raised in its workspace, so a non-zero word also drops the cached workspaces."""
+    v = int(_lib.hm_get_device_error(_stream()))
+    if v:
+        _WS_CACHE.clear()
+    return v
 
 
 def debug_wait_timeout(ns):

@@ -60,6 +60,19 @@ def test_nvfp4_act_given_scale(hm):
     np.testing.assert_array_equal(gs.cpu().numpy(), atoms)
 
 
+def test_nvfp4_act_all_zero(hm):
+    """An all-zero X: the tensor scale is 1 by the reading taken, every block scale and code 0."""
+    m, k = 3, 128
+    x = torch.zeros((m, k), dtype=torch.bfloat16)
+    codes, sb, g = oq.quant_nvfp4(x.float().numpy())
+    assert g == 1.0 and not codes.any() and not sb.any()
+    gq, gs, gg = hm.quant_act_nvfp4(x.cuda())
+    torch.cuda.synchronize()
+    assert float(gg.item()) == 1.0
+    assert not gq.cpu().numpy().any()
+    np.testing.assert_array_equal(gs.cpu().numpy(), ol.pack_act_nvfp4(codes, sb)[1])
+
+
 def _bf16_ulp(v):
     """Spacing of bf16 numbers at |v| (normal range)."""
     e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))

@@ -51,6 +51,30 @@ def test_quantize_mxfp4(hm, n, k):
     np.testing.assert_array_equal(qg.cpu().numpy(), pack_nibbles(codes))
 
 
+def test_quantize_nvfp4_tensor_scale_not_one(hm):
+    """The hand-computed NVFP4 row of the oracle's tests (tensor amax 1, g = fp32(1/2688)), every
+    value at a rounding boundary of one step of the recipe, quantized on the GPU: the codes and
+    scales written out there by hand."""
+    def f(h):
+        return float(np.array([h], dtype=np.uint32).view(np.float32)[0])
+    w = np.zeros((2, 64), dtype=np.float32)
+    w[0, 0] = 1.0
+    w[0, 16:21] = [f(0x3B76DB6D), f(0x392AAAAB), f(0x3A955555), f(0x3A000000), -f(0x3A955555)]
+    w[0, 32:36] = [f(0x3B400001), f(0x39C92492), f(0x3A279E7B), -f(0x3A279E7B)]
+    w[0, 48:50] = [f(0x3B2DB6DB), -f(0x3B2DB6DB)]
+    qg, sg, gg = hm.quantize_weight(hm.desc(4, 2, 64), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert gg.cpu().view(torch.int32).item() == 0x39C30C31
+    expect = np.zeros((2, 64), dtype=np.int64)
+    expect[0, 0] = 7
+    expect[0, 16:21] = [7, 0, 3, 2, 11]
+    expect[0, 32:36] = [7, 1, 2, 10]
+    expect[0, 48:50] = [7, 15]
+    np.testing.assert_array_equal(qg.cpu().numpy(), pack_nibbles(expect))
+    np.testing.assert_array_equal(sg.cpu().numpy()[0], [0x7E, 0x3E, 0x3B, 0x39])
+    assert not sg.cpu().numpy()[1].any()        # an all-zero row: sb = 0, codes 0
+
+
 @pytest.mark.parametrize("n,k", [(256, 512), (100, 64), (130, 1024)])
 def test_quantize_nvfp4(hm, n, k):
     w = synth.weights(n, k, seed=14)

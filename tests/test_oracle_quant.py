@@ -249,3 +249,51 @@ def test_mxint4_exact_on_its_own_grid():
     np.testing.assert_array_equal(q, q0)
     np.testing.assert_array_equal(e, j + 127)
     np.testing.assert_array_equal(Q.dequant_mxint4(q, e), w)
+
+
+def test_nvfp4_hand_computed_tensor_scale_not_one():
+    """A row with tensor amax 1, so g = fp32(1/2688) = 0x39C30C31 (3.7202382e-4), not 1.
+
+    Every value is an fp32 bit pattern chosen at a rounding boundary, so that another order of
+    the recipe's fp32 steps gives other codes: sb from the exact amax/(6g), or from
+    amax/fp32(6g), or amax*fp32(1/(6g)); elements divided by the exact sb*g instead of its fp32
+    rounding, or by g then sb, or by sb then g, or multiplied by the fp32 reciprocal of fp32(sb*g).
+    The steps, worked by hand in exact arithmetic (fp32 rounding after each operation):
+
+    block 0: amax 1: fp32(1/6) = 0.16666667163, /g -> 448.0 (e4m3 0x7E); d = fp32(448*g) =
+             0.16666667163; 1/d = 6.0 -> e2m1 6 (code 7).
+    block 1: amax 0x3B76DB6D = 0.0037667409: fp32(amax/6) = 6.2779017e-4, /g = 1.6875 exactly, the
+             e4m3 midpoint of 1.625 and 1.75, ties to even -> 1.75 (0x3E) (the exact quotient is
+             just below 1.6875 -> 1.625); d = fp32(1.75*g) = 6.5104169e-4 (rounded up).
+             0x392AAAAB = d/4 exactly: v/d = 0.25, tie -> 0 (code 0) (exact sb*g < d: 0.5);
+             0x3A955555: v/d = 1.7499999 -> 1.5 (code 3) (times fp32(1/d): 1.75 -> 2);
+             0x3A000000: v/d rounds to 0.75 in fp32, a tie -> 1.0 (code 2) (the exact quotient
+             by sb*g is just below 0.75 -> 0.5); -0x3A955555 -> code 11; amax/d = 5.79 -> 6
+             (code 7).
+    block 2: amax 0x3B400001 = 0.0029296877: fp32(amax/6)/g = 1.3125001 -> 1.375 (0x3B)
+             (amax/fp32(6g) = 1.3124999 -> 1.25); d = 5.1153277e-4.
+             0x39C92492: v/d = 0.74999994 -> 0.5 (code 1) (fp32(v/g)/sb: 0.75 -> 1.0);
+             0x3A279E7B: v/d = 1.25, tie -> 1.0 (code 2) (exact, v/g/sb and v/sb/g: 1.5);
+             its negative -> code 10.
+    block 3: amax 0x3B2DB6DB = 0.0026506695: fp32(amax/6)/g = 1.1874999 -> 1.125 (0x39)
+             (amax*fp32(1/(6g)): 1.1875 -> 1.25); +-amax/d = +-6.333 -> +-6 (codes 7, 15).
+    """
+    def f(h):
+        return float(np.array([h], dtype=np.uint32).view(np.float32)[0])
+    v = np.zeros((1, 64))
+    v[0, 0] = 1.0
+    v[0, 16:21] = [f(0x3B76DB6D), f(0x392AAAAB), f(0x3A955555), f(0x3A000000), -f(0x3A955555)]
+    v[0, 32:36] = [f(0x3B400001), f(0x39C92492), f(0x3A279E7B), -f(0x3A279E7B)]
+    v[0, 48:50] = [f(0x3B2DB6DB), -f(0x3B2DB6DB)]
+    codes, sb, g = Q.quant_nvfp4(v)
+    assert np.float32(g).view(np.uint32) == 0x39C30C31
+    assert list(sb[0]) == [0x7E, 0x3E, 0x3B, 0x39]
+    expect = np.zeros(64, dtype=np.int64)
+    expect[0] = 7
+    expect[16:21] = [7, 0, 3, 2, 11]
+    expect[32:36] = [7, 1, 2, 10]
+    expect[48:50] = [7, 15]
+    np.testing.assert_array_equal(codes[0], expect)
+    # restored values: e2m1 * sb * g
+    back = Q.dequant_nvfp4(codes, sb, g)
+    assert back[0, 18] == 1.5 * 1.75 * g and back[0, 49] == -6.0 * 1.125 * g
