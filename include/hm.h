@@ -169,6 +169,33 @@ hm_status hm_quant_act_nvfp4(const void* x, int64_t M, int64_t K, const float* g
  * launch failure. */
 hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inter, void* stream);
 
+/* MoE token gather before the gate-up grouped GEMM: xs[r][:] = x[token_of_row[r]][:] for
+ * r in [0, rows), an exact copy. x: device bf16 [T][K] (one row per token); token_of_row: device
+ * int32 [rows] (the token of each expert-sorted row, rows = T * top-k for a full routing); xs:
+ * device bf16 [rows][K], not overlapping x. K % 8 == 0; x and xs 16-byte aligned. rows = 0 is a
+ * no-op. A token index outside [0, T) sets device error bit 3 and that row of xs is written as
+ * zeros. (The MoE paragraph of the explainer page, section "같은 가중치도 한 토큰과 많은 토큰에서
+ * 비용이 다르다": each token goes to the experts it is routed to, and each expert multiplies its
+ * own rows; the pages do not print the gather, the plain row copy is the reading taken.)
+ * Returns HM_ERR_INVALID_ARG for bad sizes or misaligned pointers, HM_ERR_CUDA for a launch
+ * failure. Caller owns every buffer; nothing is allocated. */
+hm_status hm_moe_gather(const void* x, const int32_t* token_of_row, void* xs, int64_t T, int64_t rows,
+                        int64_t K, void* stream);
+
+/* MoE top-k combine after the down grouped GEMM:
+ * out[t][c] = bf16( sum over j = 0 .. topk-1 with pos[t][j] >= 0 of w[t][j] * y[pos[t][j]][c] ),
+ * summed in fp32 by one fused multiply-add per slot in slot order, then rounded once to bf16
+ * (nearest even); a call is deterministic. y: device bf16 [rows][N] (the expert-sorted outputs);
+ * pos: device int32 [T][topk] (the sorted row of token t's j-th routing slot, < 0 = empty slot);
+ * w: device fp32 [T][topk] routing weights; out: device bf16 [T][N], not overlapping y.
+ * N % 8 == 0; y and out 16-byte aligned. T = 0 is a no-op. A pos >= rows sets device error bit 3
+ * and that slot is skipped. (Same passage as hm_moe_gather: the tokens' expert outputs are brought
+ * back to the token; the weighted sum of the usual top-k layer is the reading taken.)
+ * Returns HM_ERR_INVALID_ARG for bad sizes or misaligned pointers, HM_ERR_CUDA for a launch
+ * failure. Caller owns every buffer; nothing is allocated. */
+hm_status hm_moe_combine(const void* y, const int32_t* pos, const float* w, void* out, int64_t T,
+                         int32_t topk, int64_t rows, int64_t N, void* stream);
+
 /* ---------------------------------------------------------------- GEMM */
 
 /* Workspace bytes hm_gemm / hm_moe_gemm need for this problem (split-K partials and tile
@@ -269,7 +296,8 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
 
 /* Returns and clears the device error word on the current device (synchronises `stream`).
  * 0 = no error; bit 0: packed header mismatch; bit 1: pipeline wait timed out;
- * bit 2: bad expert offsets. */
+ * bit 2: bad expert offsets; bit 3: a token or row index of hm_moe_gather / hm_moe_combine out of
+ * range. */
 uint32_t hm_get_device_error(void* stream);
 
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on an mbarrier

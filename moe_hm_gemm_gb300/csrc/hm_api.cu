@@ -500,6 +500,35 @@ hm_status hm_silu_mul(const void* gate_up, void* out, int64_t rows, int64_t inte
                                      rows, inter, di.num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+hm_status hm_moe_gather(const void* x, const int32_t* token_of_row, void* xs, int64_t T, int64_t rows, int64_t K,
+                        void* stream) {
+  if (T < 0 || rows < 0 || K <= 0 || K % 8 != 0) return HM_ERR_INVALID_ARG;
+  if (rows == 0) return HM_OK;
+  if (x == nullptr || token_of_row == nullptr || xs == nullptr || !aligned(x, 16) || !aligned(xs, 16) ||
+      !aligned(token_of_row, 4))
+    return HM_ERR_INVALID_ARG;
+  if (rows > INT64_MAX / (2 * K)) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_moe_gather(static_cast<const __nv_bfloat16*>(x), token_of_row,
+                                       static_cast<__nv_bfloat16*>(xs), T, rows, K, di.err, di.num_sms,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+hm_status hm_moe_combine(const void* y, const int32_t* pos, const float* w, void* out, int64_t T, int32_t topk,
+                         int64_t rows, int64_t N, void* stream) {
+  if (T < 0 || topk < 1 || rows < 0 || N <= 0 || N % 8 != 0) return HM_ERR_INVALID_ARG;
+  if (T == 0) return HM_OK;
+  if (y == nullptr || pos == nullptr || w == nullptr || out == nullptr || !aligned(y, 16) || !aligned(out, 16) ||
+      !aligned(pos, 4) || !aligned(w, 4))
+    return HM_ERR_INVALID_ARG;
+  if (T > INT64_MAX / (2 * N) || rows > INT64_MAX / (2 * N)) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_moe_combine(static_cast<const __nv_bfloat16*>(y), pos, w, static_cast<__nv_bfloat16*>(out),
+                                        T, topk, rows, N, di.err, di.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 size_t hm_act_scale_size(int64_t M, int64_t K) {
   if (M < 0 || K <= 0 || K % 64 != 0) return 0;
   return static_cast<size_t>(ceil_div(M, 128)) * (K / 64) * kAtomBytes;

@@ -123,6 +123,13 @@ int act_amax_blocks(int64_t m, int64_t k);
 // MoE expert activation: h[rows][inter] = bf16(SiLU(gate) * up) from gate_up[rows][2*inter].
 cudaError_t launch_silu_mul(const __nv_bfloat16* gu, __nv_bfloat16* h, int64_t rows, int64_t inter, int num_sms,
                             cudaStream_t st);
+// MoE token gather (xs[r] = x[token_of_row[r]]) and weighted top-k combine (hm_moe.cu).
+cudaError_t launch_moe_gather(const __nv_bfloat16* x, const int32_t* token_of_row, __nv_bfloat16* xs,
+                              int64_t tokens, int64_t rows, int64_t k, uint32_t* err, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_moe_combine(const __nv_bfloat16* y, const int32_t* pos, const float* w, __nv_bfloat16* out,
+                               int64_t tokens, int32_t topk, int64_t rows, int64_t n, uint32_t* err, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace hm

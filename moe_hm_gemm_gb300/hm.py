@@ -48,6 +48,8 @@ def _load():
         "hm_dequant": (I32, [D, P, P, P]),
         "hm_quant_act_fp8": (I32, [P, I64, I64, P, P, P]),
         "hm_silu_mul": (I32, [P, P, I64, I64, P]),
+        "hm_moe_gather": (I32, [P, P, P, I64, I64, I64, P]),
+        "hm_moe_combine": (I32, [P, P, P, P, I64, I32, I64, I64, P]),
         "hm_act_scale_size": (SZ, [I64, I64]),
         "hm_act_workspace_size": (SZ, [I64, I64]),
         "hm_quant_act_nvfp4": (I32, [P, I64, I64, P, P, P, P, P, SZ, P]),
@@ -175,6 +177,31 @@ def silu_mul(gate_up, inter, out=None):
     assert out.dtype == torch.bfloat16 and out.is_contiguous() and tuple(out.shape) == (rows, inter)
     _check(_lib.hm_silu_mul(_ptr(gate_up), _ptr(out), int(rows), int(inter), _stream()), "hm_silu_mul")
     return out
+
+
+def moe_gather(x, token_of_row, out=None):
+    """bf16 x [T,K], int32 token_of_row [rows] (device) -> bf16 xs [rows,K] (hm_moe_gather)."""
+    _dev(("x", x), ("token_of_row", token_of_row))
+    if x.dtype != torch.bfloat16 or token_of_row.dtype != torch.int32:
+        raise ValueError("x: bf16 [T,K]; token_of_row: int32 [rows]")
+    t, k = x.shape
+    rows = token_of_row.numel()
+    xs = torch.empty((rows, k), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (rows, k))
+    _check(_lib.hm_moe_gather(_ptr(x), _ptr(token_of_row), _ptr(xs), t, rows, k, _stream()), "hm_moe_gather")
+    return xs
+
+
+def moe_combine(y, pos, w, out=None):
+    """bf16 y [rows,N], int32 pos [T,topk], fp32 w [T,topk] (device) -> bf16 [T,N] (hm_moe_combine)."""
+    _dev(("y", y), ("pos", pos), ("w", w))
+    if y.dtype != torch.bfloat16 or pos.dtype != torch.int32 or w.dtype != torch.float32 or pos.shape != w.shape:
+        raise ValueError("y: bf16 [rows,N]; pos: int32 [T,topk]; w: float32 [T,topk]")
+    rows, n = y.shape
+    t, topk = pos.shape
+    o = torch.empty((t, n), dtype=torch.bfloat16, device=y.device) if out is None else _out(out, (t, n))
+    _check(_lib.hm_moe_combine(_ptr(y), _ptr(pos), _ptr(w), _ptr(o), t, topk, rows, n, _stream()),
+           "hm_moe_combine")
+    return o
 
 
 def quant_act_nvfp4(x, g_in=None):

@@ -330,3 +330,22 @@ def test_plan_invariants_random(hm):
         assert p["grid"] <= p["tiles"] * kb_total, (fmt, m, n, k, sms, p)
         if p["grid"] > p["tiles"]:
             assert p["stream_k"] == 1
+
+
+def test_moe_gather_combine_argument_checks(hm):
+    lib = hm.lib()
+    P = ctypes.c_void_p
+    # gather: K % 8, negative sizes, null or misaligned pointers -> HM_ERR_INVALID_ARG; rows = 0 no-op
+    assert lib.hm_moe_gather(P(16), P(16), P(4096), 4, 8, 12, None) == 1
+    assert lib.hm_moe_gather(P(16), P(16), P(4096), -1, 8, 16, None) == 1
+    assert lib.hm_moe_gather(None, P(16), P(4096), 4, 8, 16, None) == 1
+    assert lib.hm_moe_gather(P(24), P(16), P(4096), 4, 8, 16, None) == 1
+    assert lib.hm_moe_gather(P(16), P(18), P(4096), 4, 8, 16, None) == 1
+    assert lib.hm_moe_gather(None, None, None, 4, 0, 16, None) == 0
+    # combine: N % 8, topk < 1, misaligned y / out / pos / w -> HM_ERR_INVALID_ARG; T = 0 no-op
+    assert lib.hm_moe_combine(P(16), P(16), P(16), P(4096), 4, 8, 32, 12, None) == 1
+    assert lib.hm_moe_combine(P(16), P(16), P(16), P(4096), 4, 0, 32, 16, None) == 1
+    assert lib.hm_moe_combine(P(24), P(16), P(16), P(4096), 4, 8, 32, 16, None) == 1
+    assert lib.hm_moe_combine(P(16), P(16), P(18), P(4096), 4, 8, 32, 16, None) == 1
+    assert lib.hm_moe_combine(P(16), None, P(16), P(4096), 4, 8, 32, 16, None) == 1
+    assert lib.hm_moe_combine(None, None, None, None, 0, 8, 32, 16, None) == 0

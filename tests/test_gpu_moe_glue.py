@@ -1,0 +1,135 @@
+"""GPU parity of the MoE token movement around the grouped GEMMs, through the C ABI: the gather
+(bit-exact against the oracle's row copy) and the weighted top-k combine (within one bf16 step of
+the oracle's single rounding of the exact fp64 sum, almost always equal), and a whole MoE block
+(gather, gate-up grouped GEMM, SiLU-mul, down grouped GEMM, combine) against the oracle's chain."""
+import numpy as np
+import pytest
+import torch
+
+from moe_hm_gemm_gb300 import synth
+from oracle import act as oa
+from oracle import gemm as og
+from oracle import moe as om
+
+from .gpu_util import QuantWeight, assert_close, bf16_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hm():
+    import __graft_entry__
+    __graft_entry__.build()
+    from moe_hm_gemm_gb300 import hm as mod
+    return mod
+
+
+def _bf16_step(v):
+    """Spacing of bf16 numbers at |v| (normal range)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def _within_one_step(out, ref):
+    out = np.asarray(out, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    step = _bf16_step(np.maximum(np.abs(out), np.abs(ref)))
+    bad = np.abs(out - ref) > step
+    assert not bad.any(), f"{int(bad.sum())} outputs more than one bf16 step from the oracle"
+    return float(np.mean(out == ref))
+
+
+@pytest.mark.parametrize("t,experts,topk,k", [(1, 8, 1, 8), (40, 16, 4, 7168), (257, 64, 8, 520), (16, 256, 8, 2048)])
+def test_gather_bit_exact(hm, t, experts, topk, k):
+    tok, _, _ = synth.moe_routing(t, experts=experts, topk=topk, seed=t)
+    x = synth.activations(t, k, seed=t + 1)
+    ref = om.gather_rows(x.view(torch.int16).numpy(), tok)        # exact row copy, compared as bits
+    xs = hm.moe_gather(x.cuda(), torch.from_numpy(tok.astype(np.int32)).cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(xs.view(torch.int16).cpu().numpy(), ref)
+    assert hm.device_error() == 0
+
+
+def test_gather_bad_token_sets_error_and_zero_row(hm):
+    x = synth.activations(4, 64, seed=3).cuda()
+    tok = torch.tensor([0, 3, 4, -1, 2], dtype=torch.int32, device="cuda")
+    xs = hm.moe_gather(x, tok)
+    torch.cuda.synchronize()
+    assert hm.device_error() & 8
+    assert (xs[2] == 0).all() and (xs[3] == 0).all()
+    assert torch.equal(xs[1], x[3]) and torch.equal(xs[4], x[2])
+
+
+@pytest.mark.parametrize("t,experts,topk,n", [(1, 8, 1, 8), (40, 16, 4, 7168), (257, 64, 8, 56), (100, 256, 8, 2048)])
+def test_combine_within_one_bf16_step(hm, t, experts, topk, n):
+    _, _, _, pos, w = synth.moe_routing_slots(t, experts=experts, topk=topk, seed=t + 5)
+    rows = t * topk
+    y = synth.activations(rows, n, seed=t + 6)
+    pos = pos.copy()
+    if t > 3:
+        pos[1, 0] = -1                     # empty slots: first, last, and a whole token
+        pos[2, topk - 1] = -1
+        pos[3, :] = -1
+    ref = om.combine(bf16_np(y), pos, w)
+    out = hm.moe_combine(y.cuda(), torch.from_numpy(pos.astype(np.int32)).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    exact = _within_one_step(bf16_np(out), ref)
+    assert exact >= 0.99, f"only {exact:.4f} of outputs equal the oracle's rounding"
+    if t > 3:
+        assert (out[3] == 0).all()
+    assert hm.device_error() == 0
+
+
+def test_combine_row_past_end_sets_error(hm):
+    y = synth.activations(8, 16, seed=1).cuda()
+    pos = torch.tensor([[0, 8], [1, 2]], dtype=torch.int32, device="cuda")
+    w = torch.tensor([[0.5, 0.5], [1.0, 0.25]], dtype=torch.float32, device="cuda")
+    out = hm.moe_combine(y, pos, w)
+    torch.cuda.synchronize()
+    assert hm.device_error() & 8
+    # the bad slot is skipped: token 0 is 0.5 * y[0] exactly
+    assert torch.equal(out[0], (y[0].float() * 0.5).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_moe_block_end_to_end(hm, fmt):
+    """gather -> gate-up grouped GEMM -> SiLU-mul -> down grouped GEMM -> combine, all on the GPU,
+    against the same chain in the oracle with bf16 roundings at the same points (each GEMM output,
+    the activation, the combine). Each step is also checked on the GPU's own input."""
+    t, experts, topk, hidden, inter = 48, 8, 4, 512, 256
+    tok, _, offsets, pos, w = synth.moe_routing_slots(t, experts=experts, topk=topk, seed=7)
+    x = synth.activations(t, hidden, seed=8)
+    up_w = [QuantWeight(fmt, synth.weights(2 * inter, hidden, seed=100 + e),
+                        synth.zero_points(2 * inter, hidden // 128, seed=200 + e) if fmt == 1 else None)
+            for e in range(experts)]
+    dn_w = [QuantWeight(fmt, synth.weights(hidden, inter, seed=300 + e),
+                        synth.zero_points(hidden, inter // 128, seed=400 + e) if fmt == 1 else None)
+            for e in range(experts)]
+    up_p = [q.transform(hm)[1] for q in up_w]
+    dn_p = [q.transform(hm)[1] for q in dn_w]
+    up_ptr = torch.tensor([p.data_ptr() for p in up_p], dtype=torch.int64, device="cuda")
+    dn_ptr = torch.tensor([p.data_ptr() for p in dn_p], dtype=torch.int64, device="cuda")
+    offs = torch.from_numpy(offsets).cuda()
+
+    xs = hm.moe_gather(x.cuda(), torch.from_numpy(tok.astype(np.int32)).cuda())
+    gu = hm.moe_gemm(fmt, xs, offs, up_ptr, 2 * inter, hidden)
+    h = hm.silu_mul(gu, inter)
+    yd = hm.moe_gemm(fmt, h, offs, dn_ptr, hidden, inter)
+    out = hm.moe_combine(yd, torch.from_numpy(pos.astype(np.int32)).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert hm.device_error() == 0
+
+    # step by step on the GPU's own inputs
+    np.testing.assert_array_equal(xs.view(torch.int16).cpu().numpy(), om.gather_rows(x.view(torch.int16).numpy(), tok))
+    assert_close(gu, og.moe_gemm(bf16_np(xs), offsets, [q.what for q in up_w]), "gate-up")
+    assert_close(yd, og.moe_gemm(bf16_np(h), offsets, [q.what for q in dn_w]), "down")
+    _within_one_step(bf16_np(out), om.combine(bf16_np(yd), pos, w))
+
+    # the whole block in the oracle
+    from oracle.formats import bf16r
+    r_xs = om.gather_rows(bf16_np(x), tok)
+    r_gu = bf16r(og.moe_gemm(r_xs, offsets, [q.what for q in up_w]))
+    r_h = oa.silu_mul(r_gu, inter)
+    r_yd = bf16r(og.moe_gemm(r_h, offsets, [q.what for q in dn_w]))
+    r_out = om.combine(r_yd, pos, w)
+    assert_close(out, r_out, "MoE block")
