@@ -46,9 +46,15 @@ def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
-                    source="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+        pk = dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"], source="measured")
+    else:
+        pk = dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+    kp = os.path.join(ROOT, "profiles", "tcgen05_peaks.json")
+    if os.path.exists(kp):
+        d = json.load(open(kp))
+        pk["kinds"] = {k: v["tflops"] for k, v in d["kinds"].items()}
+        pk["kinds_note"] = d.get("note", "")
+    return pk
 
 
 def measured_traffic(workload, label):
@@ -73,8 +79,27 @@ def measured_traffic(workload, label):
 
 
 # nominal dense ratios of the MMA kinds to kind::f16 (bf16) on GB300: 2.25 (bf16), 4.5 (fp8) and
-# 13.5 (fp4) PFLOP/s dense, i.e. fp8 x2 and fp4 x6
+# 13.5 (fp4) PFLOP/s dense, i.e. fp8 x2 and fp4 x6; used only when no measured peak of the kind
+# is recorded (profiles/tcgen05_peaks.json, written from the tcgen05 microbenchmark)
 KIND_RATIO = {"kind::f16": 1.0, "kind::mxf8f6f4": 2.0, "kind::mxf4nvf4": 6.0}
+
+
+def tensor_peak(pk, kind):
+    """Dense TFLOP/s of an MMA kind: the measured tcgen05 peak of that kind when recorded, else the
+    measured cuBLAS bf16 figure times the nominal ratio."""
+    kinds = pk.get("kinds") or {}
+    if kind in kinds:
+        return kinds[kind]
+    return pk["bf16_sus"] * KIND_RATIO[kind]
+
+
+def peak_source(pk, kind, bound):
+    if bound != "tensor":
+        return f"{pk['source']} (hbm copy)"
+    if kind in (pk.get("kinds") or {}):
+        return f"measured tcgen05 {kind} microbenchmark ({pk.get('kinds_note', '')})"
+    extra = f" x nominal {KIND_RATIO[kind]} for {kind}" if kind != "kind::f16" else ""
+    return f"{pk['source']} (bf16 sustained{extra})"
 
 
 class Clocks:
@@ -140,9 +165,14 @@ class Point:
         self.flops, self.weight_bytes, self.act_bytes, self.out_bytes = flops, weight_bytes, act_bytes, out_bytes
         self.kind, self.launches_per_call = kind, launches
         self.calls = []        # list of zero-arg callables, one per rotation copy
+        self.reps = 1          # passes over the copies captured in the point's graph
         self.e2e = None        # (host_in, dev_in, host_out, dev_out, call)
         self.graph = None
-        self.times_ms = []
+        self.times_ms = []     # per launch, one value per timed step
+
+    @property
+    def launches(self):
+        return self.reps * len(self.calls)
 
     @property
     def bytes(self):
@@ -153,10 +183,11 @@ def rotations(weight_bytes):
     return max(2, math.ceil(4 * L2_BYTES / max(weight_bytes, 1)))
 
 
-def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick):
+def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick, has_zero=None):
     points = []
     for si, (n, k) in enumerate(shapes):
-        has_zero = fmt == hm.W4A16_INT4
+        if has_zero is None:
+            has_zero = fmt == hm.W4A16_INT4
         d = hm.desc(fmt, n, k, has_zero)
         w = synth.device_weights(n, k, seed=seed0 + si)
         z = synth.device_zero_points(n, k // 128, seed=seed0 + 100 + si) if has_zero else None
@@ -253,6 +284,48 @@ def silu_points(hm, synth, quick):
     return points
 
 
+def glue_points(hm, synth, quick):
+    """MoE token gather (x[T, 7168] -> xs[8T, 7168] by the routing) and top-8 combine of the down
+    layer's outputs (y[8T, 7168] -> out[T, 7168]) for the Zipf(1.1) routing of T tokens; inputs
+    rotated over copies covering 4x L2. Bytes: the gather reads T x 7168 x 2 (every token row once)
+    plus the row indices and writes 8T x 7168 x 2; the combine reads 8T x 7168 x 2 (+ routing) and
+    writes T x 7168 x 2."""
+    hidden, topk = 7168, 8
+    tokens = [16, 256, 4096, 16384] if not quick else [16, 4096]
+    points = []
+    for t in tokens:
+        tok, _, _, pos, wts = synth.moe_routing_slots(t, experts=256, topk=topk, seed=0)
+        rows = t * topk
+        x = synth.device_activations(t, hidden, seed=50000 + t)
+        tok_d = torch.from_numpy(tok.astype(np.int32)).cuda()
+        xs = torch.empty((rows, hidden), dtype=torch.bfloat16, device="cuda")
+        # each token row is read from HBM once (its other copies come from L2) and written top-k times
+        p = Point(f"moe gather T={t}", 0, rows, hidden, hidden, 0.0, 0, t * hidden * 2 + rows * 4, rows * hidden * 2,
+                  "kind::f16", 1)
+        copies = [x] + [x.clone() for _ in range(rotations(t * hidden * 2) - 1)]
+        for c in copies:
+            p.calls.append(lambda c=c, xs=xs, tok_d=tok_d: hm.moe_gather(c, tok_d, out=xs))
+        p.e2e = (x.cpu().pin_memory(), x, torch.empty((rows, hidden), dtype=torch.bfloat16).pin_memory(), xs,
+                 p.calls[0])
+        points.append(p)
+        y = synth.device_activations(rows, hidden, seed=60000 + t)
+        pos_d = torch.from_numpy(pos.astype(np.int32)).cuda()
+        w_d = torch.from_numpy(wts).cuda()
+        out = torch.empty((t, hidden), dtype=torch.bfloat16, device="cuda")
+        c_in = rows * hidden * 2 + t * topk * 8
+        # one multiply-add per slot and output element
+        p = Point(f"moe combine T={t}", 0, t, hidden, topk, 2.0 * t * topk * hidden, 0, c_in, t * hidden * 2,
+                  "kind::f16", 1)
+        copies = [y] + [y.clone() for _ in range(rotations(rows * hidden * 2) - 1)]
+        for c in copies:
+            p.calls.append(lambda c=c, out=out, pos_d=pos_d, w_d=w_d: hm.moe_combine(c, pos_d, w_d, out=out))
+        p.e2e = (y.cpu().pin_memory(), y, torch.empty((t, hidden), dtype=torch.bfloat16).pin_memory(), out,
+                 p.calls[0])
+        points.append(p)
+    torch.cuda.synchronize()
+    return points
+
+
 def build_points(args, hm, synth):
     pts = _build_points(args, hm, synth)
     if args.m:
@@ -287,8 +360,19 @@ def _build_points(args, hm, synth):
         return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick)
     if w == "moe_silu_mul":
         return silu_points(hm, synth, args.quick)
+    if w == "moe_glue":
+        return glue_points(hm, synth, args.quick)
+    if w == "w4a16_tiny":
+        return dense_points(hm, synth, hm.W4A16_INT4, [(256, 512)], [4], 0, "kind::f16", False, has_zero=False)
     raise SystemExit(f"unknown workload {w}")
 
+
+EXTRA_WORKLOADS = ["w4a16_tiny", "w4a8", "w4a4", "moe_w4a16", "moe_mxfp4", "w4a16_mxint4", "moe_mxint4",
+                   "moe_silu_mul", "moe_glue"]
+DTYPE = {"w4a8": "fp8xfp4", "w4a4": "fp4"}
+L2_NOTE = {"moe_silu_mul": "gate-up inputs rotated over copies covering 4x L2",
+           "moe_glue": "token activations / expert outputs rotated over copies covering 4x L2",
+           "w4a16_tiny": "packed weight rotated over copies covering 4x L2"}
 
 WORKLOAD_NAMES = {
     "w4a16": "W4A16 dense LLM layer: (N,K) in {(4096,4096),(14336,4096),(4096,14336)} x M in "
@@ -304,6 +388,9 @@ WORKLOAD_NAMES = {
                     "{1,2,4,8,16,32,64,128,256,1024,4096,8192}; signed int4 + E8M0 scale per 32",
     "moe_mxint4": "MoE grouped MXINT4-W4A16: E=256, gate-up 4096x7168 and down 7168x2048, top-8 Zipf(1.1), "
                   "T in {16,256,4096,16384}",
+    "w4a16_tiny": "W4A16 dense tiny: M=4, K=512, N=256, INT4 symmetric g128 bf16 scales",
+    "moe_glue": "MoE token gather (T x 7168 -> 8T rows) and top-8 weighted combine (8T x 7168 -> T rows), "
+                "Zipf(1.1) routing over 256 experts, T in {16,256,4096,16384} (HBM-bound; roofline in GB/s)",
     "moe_silu_mul": "MoE expert activation h = SiLU(gate) * up between the grouped GEMMs: rows = 8 T, "
                     "gate | up 2 x 2048 bf16 in, 2048 bf16 out, T in {16,256,4096,16384} (HBM-bound; "
                     "value in TFLOP/s of ~5 operations per output, roofline in GB/s)",
@@ -312,6 +399,117 @@ WORKLOAD_NAMES = {
 
 # ----------------------------------------------------------------------------- our arm
 
+MIN_LAUNCHES = 200          # launches per point and timed step (CUDA graph of back-to-back calls)
+SLOW_LAUNCH_MS = 0.5        # points slower than this per launch: >= 20 launches and >= 100 ms per step
+
+
+def set_reps(points, stream):
+    """Passes over the rotation copies per graph: at least MIN_LAUNCHES launches, or for slow
+    points (> SLOW_LAUNCH_MS per launch, from one timed warm-up pass) at least 20 launches and
+    100 ms."""
+    for p in points:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for c in p.calls:
+            c()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per = a.elapsed_time(b) / len(p.calls)
+        want = MIN_LAUNCHES if per <= SLOW_LAUNCH_MS else max(20, math.ceil(100.0 / per))
+        p.reps = max(1, math.ceil(want / len(p.calls)))
+
+
+def measure(points, steps, warmup, stream, hm, world=1, clocks_index=None):
+    """Capture one graph per point (reps x copies launches), replay each once per step; returns
+    (total ms of the timed steps, clocks summary). Per-launch times per step land in p.times_ms."""
+    for p in points:
+        for c in p.calls:
+            c()
+    torch.cuda.synchronize()
+    set_reps(points, stream)
+    for p in points:
+        p.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(p.graph, stream=stream):
+            for _ in range(p.reps):
+                for c in p.calls:
+                    c()
+    torch.cuda.synchronize()
+    if hm.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    def step(events=None):
+        for i, p in enumerate(points):
+            if events is not None:
+                events[i][0].record(stream)
+            p.graph.replay()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in points] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = Clocks(clocks_index) if clocks_index is not None else None
+    if clk is not None:
+        clk.__enter__()
+    try:
+        t0.record(stream)
+        for s in range(steps):
+            step(evs[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        if clk is not None:
+            clk.__exit__()
+    barrier(world)
+    for s in range(steps):
+        for i, p in enumerate(points):
+            p.times_ms.append(evs[s][i][0].elapsed_time(evs[s][i][1]) / p.launches)
+    return t0.elapsed_time(t1), (clk.summary() if clk is not None else None)
+
+
+def summarize(points, pk, workload, hm, local_rank):
+    """Per-point sweep (median over the timed steps of the per-launch time) and the roofline of
+    the point that takes the largest share of the step."""
+    sweep = []
+    dom, dom_share = None, -1.0
+    total_pt = sum(statistics.median(p.times_ms) * p.launches for p in points)
+    sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+    for p in points:
+        t = statistics.median(p.times_ms) * 1e-3
+        peak_t = tensor_peak(pk, p.kind)
+        tf = p.flops / t / 1e12
+        gbs = p.bytes / t / 1e9
+        share = t * 1e3 * p.launches / total_pt
+        bound = "hbm" if (p.flops == 0 or p.bytes / (pk["hbm"] * 1e9) > p.flops / (peak_t * 1e12)) else "tensor"
+        plan = None
+        if p.fmt and not p.label.startswith("moe"):
+            plan = hm.plan(p.fmt, p.m, p.n, p.k, sms)
+            plan = {k: plan[k] for k in ("kernel", "tile_m", "stages", "stream_k", "grid")}
+        sweep.append({"point": p.label, "plan": plan, "us": round(t * 1e6, 2), "launches": p.launches,
+                      "tflops": round(tf, 2), "gbs": round(gbs, 1),
+                      "weight_gbs": round(p.weight_bytes / t / 1e9, 1), "bound": bound,
+                      "frac_hbm": round(gbs / pk["hbm"], 3), "frac_tensor": round(tf / peak_t, 3),
+                      "share": round(share, 4)})
+        if share > dom_share:
+            dom, dom_share = p, share
+    t = statistics.median(dom.times_ms) * 1e-3
+    peak_t = tensor_peak(pk, dom.kind)
+    dom_bound = "hbm" if (dom.flops == 0 or dom.bytes / (pk["hbm"] * 1e9) > dom.flops / (peak_t * 1e12)) else "tensor"
+    if dom_bound == "tensor":
+        ach, peak, unit = dom.flops / t / 1e12, peak_t, "TFLOP/s"
+    else:
+        ach, peak, unit = dom.bytes / t / 1e9, pk["hbm"], "GB/s"
+    roofline = {"bound": dom_bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
+                "frac": round(ach / peak, 4), "traffic": measured_traffic(workload, dom.label), "kernel": dom.label,
+                "peak_source": peak_source(pk, dom.kind, dom_bound)}
+    return sweep, roofline
+
+
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     from moe_hm_gemm_gb300 import hm, synth
@@ -319,48 +517,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         points = build_points(args, hm, synth)
-        # warm-up calls (sets kernel attributes) and graph capture, one graph per point
-        for p in points:
-            for c in p.calls:
-                c()
-        torch.cuda.synchronize()
-        for p in points:
-            p.graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(p.graph, stream=stream):
-                for c in p.calls:
-                    c()
-        torch.cuda.synchronize()
-        if hm.device_error() != 0:
-            raise SystemExit("device error during warm-up")
-
-        def step(events=None):
-            for i, p in enumerate(points):
-                if events is not None:
-                    events[i][0].record(stream)
-                p.graph.replay()
-                if events is not None:
-                    events[i][1].record(stream)
-
-        for _ in range(args.warmup):
-            step()
-        torch.cuda.synchronize()
-        evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in points] for _ in range(args.steps)]
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize()
-        with Clocks(local_rank) as clk:
-            t0.record(stream)
-            for s in range(args.steps):
-                step(evs[s])
-            t1.record(stream)
-            torch.cuda.synchronize()
-        barrier(world)
-        total_ms = t0.elapsed_time(t1)
-        for s in range(args.steps):
-            for i, p in enumerate(points):
-                p.times_ms.append(evs[s][i][0].elapsed_time(evs[s][i][1]) / len(p.calls))
-        clocks = clk.summary()
+        total_ms, clocks = measure(points, args.steps, args.warmup, stream, hm, world, local_rank)
         err = hm.device_error()
 
         # end-to-end pass through the public API with host buffers
@@ -385,59 +542,55 @@ def run_ours(args, rank, world, local_rank):
             e2e_ms = a.elapsed_time(b) / reps
             h2d = sum(p.e2e[0].numel() * p.e2e[0].element_size() for p in points)
             d2h = sum(p.e2e[2].numel() * p.e2e[2].element_size() for p in points)
+        sweep, roofline = summarize(points, pk, args.workload, hm, local_rank)
+        flops_step = sum(p.flops * p.launches for p in points)
+        flops_e2e_pass = sum(p.flops for p in points)
+        launches = args.steps * sum(p.launches_per_call * p.launches for p in points)
+        for p in points:
+            p.graph = None
+        del points
+        torch.cuda.empty_cache()
+
+        # the other configurations, each measured the same way and reported under "configs"
+        configs = {}
+        if not args.no_extra and args.workload == "w4a16" and not args.m and not args.shape:
+            for w in EXTRA_WORKLOADS:
+                sub = argparse.Namespace(**vars(args))
+                sub.workload, sub.quick = w, False
+                pts = _build_points(sub, hm, synth)
+                ms_total, _ = measure(pts, args.extra_steps, 2, stream, hm, world)
+                sw, rf = summarize(pts, pk, w, hm, local_rank)
+                fl = sum(p.flops * p.launches for p in pts)
+                configs[w] = {"workload": WORKLOAD_NAMES[w], "value": round(fl / (ms_total / args.extra_steps * 1e-3) / 1e12, 3),
+                              "unit": "TFLOP/s", "steps": args.extra_steps, "roofline": rf, "sweep": sw}
+                launches += args.extra_steps * sum(p.launches_per_call * p.launches for p in pts)
+                for p in pts:
+                    p.graph = None
+                del pts
+                torch.cuda.empty_cache()
+            err |= hm.device_error()
 
     step_ms = total_ms / args.steps
-    flops_step = sum(p.flops * len(p.calls) for p in points)
     value, step_ms_max = aggregate_tflops(flops_step, step_ms, world)
-    launches = args.steps * sum(p.launches_per_call * len(p.calls) for p in points)
-
-    sweep = []
-    dom, dom_share = None, -1.0
-    total_pt = sum(sum(p.times_ms) * len(p.calls) for p in points)
-    for p in points:
-        t = statistics.mean(p.times_ms) * 1e-3
-        peak_t = pk["bf16_sus"] * KIND_RATIO[p.kind]
-        tf = p.flops / t / 1e12
-        gbs = p.bytes / t / 1e9
-        wgbs = p.weight_bytes / t / 1e9
-        share = sum(p.times_ms) * len(p.calls) / total_pt
-        bound = "hbm" if p.bytes / (pk["hbm"] * 1e9) > p.flops / (peak_t * 1e12) else "tensor"
-        plan = None
-        if not p.label.startswith("moe"):
-            plan = hm.plan(p.fmt, p.m, p.n, p.k, torch.cuda.get_device_properties(local_rank).multi_processor_count)
-            plan = {k: plan[k] for k in ("kernel", "tile_m", "stages", "stream_k", "grid")}
-        sweep.append({"point": p.label, "plan": plan, "us": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
-                      "weight_gbs": round(wgbs, 1), "bound": bound,
-                      "frac_hbm": round(gbs / pk["hbm"], 3), "frac_tensor": round(tf / peak_t, 3),
-                      "share": round(share, 4)})
-        if share > dom_share:
-            dom, dom_share = p, share
-    t = statistics.mean(dom.times_ms) * 1e-3
-    peak_t = pk["bf16_sus"] * KIND_RATIO[dom.kind]
-    dom_bound = "hbm" if dom.bytes / (pk["hbm"] * 1e9) > dom.flops / (peak_t * 1e12) else "tensor"
-    if dom_bound == "tensor":
-        ach, peak, unit = dom.flops / t / 1e12, peak_t, "TFLOP/s"
-    else:
-        ach, peak, unit = dom.bytes / t / 1e9, pk["hbm"], "GB/s"
-    roofline = {"bound": dom_bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
-                "frac": round(ach / peak, 4), "traffic": measured_traffic(args.workload, dom.label), "kernel": dom.label,
-                "peak_source": f"{pk['source']} ({'bf16 sustained' if dom_bound == 'tensor' else 'hbm copy'}"
-                               f"{' x nominal ' + str(KIND_RATIO[dom.kind]) + ' for ' + dom.kind if dom.kind != 'kind::f16' and dom_bound == 'tensor' else ''})"}
-
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"kind::f16": "bf16", "kind::mxf8f6f4": "fp8xfp4",
-                                       "kind::mxf4nvf4": "fp4"}[points[0].kind],
+        "vs_baseline": None, "dtype": DTYPE.get(args.workload, "bf16"),
         "data": "synthetic (seeded, generated on the device)",
         "config": {"workload": WORKLOAD_NAMES[args.workload], "parallelism": f"replicas x{world}",
-                   "l2": ("gate-up inputs" if args.workload == "moe_silu_mul" else "packed weights")
-                         + " rotated over copies covering 4x L2 per shape"},
+                   "l2": L2_NOTE.get(args.workload, "packed weights rotated over copies covering 4x L2 per shape"),
+                   "timing": f"per point: one CUDA graph of >= {MIN_LAUNCHES} back-to-back launches "
+                             f"(>= 20 launches and >= 100 ms for launches above {SLOW_LAUNCH_MS} ms), replayed once "
+                             f"per step; per-point time = median over the timed steps"},
         "roofline": roofline, "gpu_launches": launches, "clocks": clocks, "device_error": err,
+        "peaks": {"hbm_gbs": pk["hbm"], "bf16_tflops": pk["bf16"], "bf16_tflops_sustained": pk["bf16_sus"],
+                  "tensor_kind_tflops": pk.get("kinds"), "source": pk["source"]},
         "sweep": sweep,
     }
+    if configs:
+        out["configs"] = configs
     if e2e_ms is not None:
-        out["e2e"] = {"value": round(world * sum(p.flops for p in points) / (max_over_ranks(e2e_ms, world) * 1e-3) / 1e12, 3),
+        out["e2e"] = {"value": round(world * flops_e2e_pass / (max_over_ranks(e2e_ms, world) * 1e-3) / 1e12, 3),
                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0:
         if not args.no_cpu_baseline:
@@ -491,6 +644,20 @@ def oracle_sample(workload):
         x = synth.activations(m, k, seed=3).float().numpy().astype(np.float64)
         desc = f"oracle W4A16 INT4+zp dequant + fp64 GEMM, N=K=4096, M={m} rows"
         return desc, 2.0 * m * n * k, lambda: og.gemm_w4a16_int4(x, q, s, z)
+    if workload == "w4a16_tiny":
+        n, k, m = 256, 512, 4
+        q, s_ = oq.quant_int4(synth.weights(n, k, seed=0))
+        x = synth.activations(m, k, seed=0).float().numpy().astype(np.float64)
+        return (f"oracle W4A16 INT4 dequant + fp64 GEMM, N=256, K=512, M={m}", 2.0 * m * n * k,
+                lambda: og.gemm_w4a16_int4(x, q, s_))
+    if workload == "moe_glue":
+        from oracle import moe as om
+        t, hidden = 256, 7168
+        tok, _, _, pos, wts = synth.moe_routing_slots(t, experts=256, topk=8, seed=0)
+        x = synth.activations(t, hidden, seed=1).float().numpy().astype(np.float64)
+        y = synth.activations(8 * t, hidden, seed=2).float().numpy().astype(np.float64)
+        return (f"oracle MoE gather + top-8 combine in fp64, T={t}, hidden {hidden}", 2.0 * t * 8 * hidden,
+                lambda: (om.gather_rows(x, tok), om.combine(y, pos, wts)))
     if workload == "moe_silu_mul":
         from oracle import act as oa
         rows, inter = 4096, 2048
@@ -563,6 +730,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads the default run reports under 'configs'")
+    ap.add_argument("--extra-steps", type=int, default=5)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -305,6 +305,16 @@ uint32_t hm_get_device_error(void* stream);
  * sets bit 1 of the device error word and returns. */
 hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/* Diagnostics: tensor-core throughput probe. Launches one CTA per SM that issues `iters` rounds
+ * of MMAs of one tcgen05 kind from shared-memory operands into TMEM accumulators (no memory
+ * traffic in the loop): kind 0 = kind::f16 (bf16, M=128, N=256, K=16), 1 = kind::mxf8f6f4
+ * block-scaled 1X (e4m3 x e4m3, UE8M0 scales, M=N=128, K=32), 2 = kind::mxf4nvf4 block-scaled 4X
+ * (e2m1 x e2m1, UE4M3 scales, M=N=128, K=64), several issuing warps each. *flops_out receives the
+ * FLOPs (2*M*N*K per MMA) the launch issues; the caller times it on `stream` (events) to get the
+ * dense peak of that kind on this device. iters in [1, 2^24]. A completion wait that runs out (2 s)
+ * sets device error bit 1. Allocates nothing; the launch holds all of TMEM on each SM. */
+hm_status hm_mma_peak_probe(int32_t kind, int32_t iters, double* flops_out, void* stream);
+
 /* Diagnostics: install (or, with NULL/0, remove) a device buffer of `bytes` bytes on the current
  * device. While installed, each dense W4A16 GEMM launch (grid <= 256 CTAs) writes
  * global-timer stamps of its pipeline milestones per CTA: 0 entry, 1 set-up done, 2 first load

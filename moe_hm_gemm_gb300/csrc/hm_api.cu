@@ -791,6 +791,14 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns_, void* stream) {
   return cuda_status(launch_wait_timeout_probe(di.err, timeout_ns_, static_cast<cudaStream_t>(stream)));
 }
 
+hm_status hm_mma_peak_probe(int32_t kind, int32_t iters, double* flops_out, void* stream) {
+  if (kind < 0 || kind > 2 || iters < 1 || iters > (1 << 24) || flops_out == nullptr) return HM_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  return cuda_status(launch_mma_peak(kind, iters, di.num_sms, di.err, kDefaultTimeoutNs,
+                                     static_cast<cudaStream_t>(stream), flops_out));
+}
+
 const char* hm_status_string(hm_status s) {
   switch (s) {
     case HM_OK: return "ok";

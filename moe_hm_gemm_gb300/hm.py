@@ -60,6 +60,7 @@ def _load():
         "hm_plan": (I32, [I32, I64, I64, I64, I32, ctypes.POINTER(PlanInfo)]),
         "hm_get_device_error": (ctypes.c_uint32, [P]),
         "hm_debug_wait_timeout": (I32, [ctypes.c_uint64, P]),
+        "hm_mma_peak_probe": (I32, [I32, I32, ctypes.POINTER(ctypes.c_double), P]),
         "hm_set_trace_buffer": (I32, [P, SZ]),
         "hm_status_string": (ctypes.c_char_p, [I32]),
         "hm_version": (ctypes.c_char_p, []),
@@ -291,6 +292,23 @@ def device_error():
     if v:
         _WS_CACHE.clear()
     return v
+
+
+def mma_peak(kind, iters, repeats=3):
+    """Dense TFLOP/s of a tcgen05 MMA kind (0 f16, 1 mxf8f6f4, 2 mxf4nvf4) from hm_mma_peak_probe,
+    timed with CUDA events on the current stream: the best of `repeats` launches after one warm-up."""
+    fl = ctypes.c_double(0.0)
+    _check(_lib.hm_mma_peak_probe(int(kind), int(iters), ctypes.byref(fl), _stream()), "hm_mma_peak_probe")
+    best = None
+    for _ in range(repeats):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        _check(_lib.hm_mma_peak_probe(int(kind), int(iters), ctypes.byref(fl), _stream()), "hm_mma_peak_probe")
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    return fl.value / (best * 1e-3) / 1e12, best
 
 
 def debug_wait_timeout(ns):

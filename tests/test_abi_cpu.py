@@ -349,3 +349,11 @@ def test_moe_gather_combine_argument_checks(hm):
     assert lib.hm_moe_combine(P(16), P(16), P(18), P(4096), 4, 8, 32, 16, None) == 1
     assert lib.hm_moe_combine(P(16), None, P(16), P(4096), 4, 8, 32, 16, None) == 1
     assert lib.hm_moe_combine(None, None, None, None, 0, 8, 32, 16, None) == 0
+
+
+def test_mma_peak_probe_argument_checks(hm):
+    lib = hm.lib()
+    fl = ctypes.c_double(0.0)
+    assert lib.hm_mma_peak_probe(3, 10, ctypes.byref(fl), None) == 1
+    assert lib.hm_mma_peak_probe(0, 0, ctypes.byref(fl), None) == 1
+    assert lib.hm_mma_peak_probe(0, 10, None, None) == 1

@@ -102,12 +102,13 @@ def test_forced_stream_k(hm, env, stream_k):
 
 @pytest.mark.parametrize("fmt,n,k", [(3, 18432, 7168), (3, 7168, 7168), (4, 8192, 8192)])
 def test_full_size_sampled(hm, fmt, n, k):
-    """The benchmark's block-scaled layers at M = 1, 1024 and 8192, checked on sampled outputs."""
+    """The benchmark's block-scaled layers, checked on sampled outputs: W4A8 at M = 1, 16, 1024 and
+    8192, W4A4 at the benchmark's M = 16, 128, 1024 and 8192."""
     w = synth.weights(n, k, seed=2)
     qw = QuantWeight(fmt, w)
     _, packed = qw.transform(hm)
     rng = np.random.default_rng(1)
-    for m in (1, 1024, 8192):
+    for m in ((1, 16, 1024, 8192) if fmt == 3 else (16, 128, 1024, 8192)):
         x = synth.activations(m, k, seed=3, outlier_frac=0.01 if fmt == 3 else 0.0)
         y = hm.gemm(fmt, x.cuda(), packed, n, k)
         torch.cuda.synchronize()
