@@ -59,25 +59,45 @@ typedef enum hm_status {
  *  HM_W4A16_MXINT4: signed 4-bit integer codes q in [-8, 7] with an E8M0 scale per 32 along K
  *                   (the MX scheme with integer elements, named on the news pages' format
  *                   list, section "하나의 라이브러리로 긴 포맷 목록을 포괄"); restored
- *                   q * 2^(e-127), exact in bf16; bf16 activations. */
+ *                   q * 2^(e-127), exact in bf16; bf16 activations.
+ *  HM_W4A16_INT4_G32: INT4 as HM_W4A16_INT4 but with a bf16 scale (and optional u4 zero-point)
+ *                   per group of 32 or 64 along K (desc.group), the small groups other
+ *                   quantization tools produce (aihaber.org, section "Mimari": weights from
+ *                   different tools are brought into one standard format); restored
+ *                   bf16((q - z) * s) with the group's s and z. */
 typedef enum hm_format {
   HM_W4A16_INT4 = 1,
   HM_W4A16_MXFP4 = 2,
   HM_W4A8_MXFP4 = 3,
   HM_W4A4_NVFP4 = 4,
-  HM_W4A16_MXINT4 = 5
+  HM_W4A16_MXINT4 = 5,
+  HM_W4A16_INT4_G32 = 6
 } hm_format;
 
+/* How zero-points are stored in the standard format handed to hm_transform (INT4 formats with
+ * has_zero). HM_ZP_INT: the u4 zero-point z itself, restored (q - z) * s (the convention of
+ * AWQ-style checkpoints and of this library). HM_ZP_GPTQ: the value (z - 1) mod 16, as GPTQ-style
+ * checkpoints store it; the transform restores z = (stored + 1) mod 16. The packed weight always
+ * holds z. hm_quantize_weight takes z itself in either case. */
+typedef enum hm_zero_convention { HM_ZP_INT = 0, HM_ZP_GPTQ = 1 } hm_zero_convention;
+
 /* Description of one quantized weight matrix W[N,K] in the common ("standard") format.
- *  has_zero     : HM_W4A16_INT4 only; 1 = zero-points present.
- *  tensor_scale : HM_W4A4_NVFP4 only; the fp32 per-tensor scale gW (ignored otherwise).
- * Shape rules: N >= 1; K % 128 == 0 for formats 1-3 and 5, K % 64 == 0 for format 4. */
+ *  has_zero       : INT4 formats (1 and 6) only; 1 = zero-points present.
+ *  tensor_scale   : HM_W4A4_NVFP4 only; the fp32 per-tensor scale gW (ignored otherwise).
+ *  group          : K values per scale. HM_W4A16_INT4: 0 (= 128) or any multiple of 128 that
+ *                   divides K, or -1 for one scale per row (per channel, = K); these pack into
+ *                   the same units as 128 (each unit carries its group's scale). HM_W4A16_INT4_G32:
+ *                   0 (= 32), 32 or 64. Others: 0 or the format's own (32 MX, 16 NVFP4).
+ *  zero_convention: hm_zero_convention of the zero-points handed to hm_transform.
+ * Shape rules: N >= 1; K % 128 == 0 for formats 1-3, 5 and 6, K % 64 == 0 for format 4. */
 typedef struct hm_weight_desc {
   int32_t fmt;
   int32_t has_zero;
   int64_t N;
   int64_t K;
   float tensor_scale;
+  int32_t group;
+  int32_t zero_convention;
 } hm_weight_desc;
 
 /* ---------------------------------------------------------------- preprocessing (once) */
@@ -101,8 +121,8 @@ size_t hm_packed_size(const hm_weight_desc* desc);
  *                   sb = e4m3(fp32(fp32(amax16/6)/g)); code = e2m1(fp32(w/fp32(sb*g))).
  * Outputs (device): q_out packed codes [N][K/2] (even k in the low nibble; INT4 and MXINT4
  * nibbles are two's complement, INT4 ones unsigned with zero-points); scales_out [N][K/g]
- * (bf16 for INT4 g=128; one byte per code for MXFP4 and MXINT4 g=32 and NVFP4 g=16); g_out
- * (NVFP4 only, fp32).
+ * (bf16 for the INT4 formats with g = desc.group; one byte per code for MXFP4 and MXINT4 g=32 and
+ * NVFP4 g=16); g_out (NVFP4 only, fp32). INT4 zero-points zeros_in are [N][K/g], one u4 per byte.
  * `ws` needs hm_quantize_workspace_size() bytes (NVFP4 amax partials; may be NULL otherwise). */
 size_t hm_quantize_workspace_size(const hm_weight_desc* desc);
 hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const uint8_t* zeros_in,
@@ -111,7 +131,8 @@ hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const u
 
 /* Pad and relayout the standard-format weight into `packed` (device, hm_packed_size bytes,
  * 256-byte aligned). Inputs (device): q [N][K/2] packed codes as above; scales [N][K/g];
- * zeros [N][K/128] one u4 value per byte (HM_W4A16_INT4 with has_zero, else NULL).
+ * zeros [N][K/g] one u4 value per byte in desc.zero_convention (INT4 formats with has_zero, else
+ * NULL), g = desc.group (INT4: a group of 128 j fills j consecutive units with its scale).
  * For HM_W4A4_NVFP4 the header records desc->tensor_scale as gW.
  * Layout: a 256-byte header (magic, fmt, N, K, padded N and K, has_zero, tensor scale, payload
  * bytes), then the payload, N padded to 128 and K to 128 (W4A4: 256):
@@ -120,7 +141,9 @@ hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const u
  *    ((kk%32)/8)*4, bits 4*((kk%8)/2) + 16*(kk%2); signed codes stored as q + 8), then the
  *    per-row scales (INT4: 128 bf16; MXFP4 and MXINT4: 128 x 4 E8M0) and, for INT4 with
  *    zero-points, 64 bytes of u4 zero-points (row r in the low nibble of byte r/2 when r is
- *    even). Units are 8448 / 8512 / 8704 bytes.
+ *    even). Units are 8448 / 8512 / 8704 bytes. HM_W4A16_INT4_G32 units: the same codes, then the
+ *    bf16 scale of (row r, 32-K chunk c) at 8192 + 8r + 2c and the u4 zero-point of (r, c) at
+ *    9216 + 2r + c/2, bit 4 (c % 2) (a group of 64 fills two chunks); 9216 / 9472 bytes.
  *  - W4A8 / W4A4: codes row-major [N_pad][K_pad/2], then 512-byte scale atoms
  *    [N_pad/128][K_pad/chunk] (chunk = 128 K for E8M0 per 32, 64 K for e4m3 per 16), the scale
  *    of (row r, sub-block j) at byte (r%32)*16 + (r/32)*4 + j of its atom. */
@@ -241,10 +264,38 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
  * padding, belong to no expert and their y rows are not written). Offsets that decrease, are
  * negative, exceed rows or do not start at 0 set device error bit 2 and nothing is stored.
  * packed: device array of E device pointers, each a packed weight of the same (fmt, N, K).
- * Formats HM_W4A16_INT4, HM_W4A16_MXFP4 and HM_W4A16_MXINT4. Experts with no rows cost nothing. */
+ * Formats HM_W4A16_INT4, HM_W4A16_MXFP4 and HM_W4A16_MXINT4 (HM_ERR_UNSUPPORTED otherwise: the
+ * block-scaled formats take their experts at a fixed stride, hm_moe_gemm_strided). Experts with no
+ * rows cost nothing. */
 hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
                       void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped GEMM over expert-sorted rows with the E experts' packed weights back to back in one
+ * buffer: expert e's packed weight (header first, as hm_transform writes it) starts at
+ * packed + e * expert_stride. Every format, including the block-scaled ones, which need one tensor
+ * map over all experts (the explainer page's MoE paragraph, section "같은 가중치도 한 토큰과 많은
+ * 토큰에서 비용이 다르다"; the W4A8 MoE of section "가중치 형식, 활성값, 백엔드를 한 줄에 적는다";
+ * the grouped NVFP4 path of aihaber.org, section "Performans").
+ *  packed: device, 256-byte aligned; expert_stride: a multiple of 256 and at least hm_packed_size()
+ *          of one expert's description; every expert's header must match (fmt, N, K), else device
+ *          error bit 0 and nothing is stored.
+ *  x, x_scale: HM_W4A16_*: x = bf16 [rows][K], x_scale = NULL.
+ *          HM_W4A8_MXFP4: x = e4m3 [rows][K] with x_scale = s_tok fp32 [rows]; or x = bf16 and
+ *          x_scale = NULL (quantized per token inside the call, into ws).
+ *          HM_W4A4_NVFP4: x = bf16 [rows][K], x_scale = NULL; quantized inside the call with one
+ *          tensor scale gX = fp32(amax(x)/2688) over all rows and e4m3 scales per 16, the scale atoms
+ *          laid out per expert token tile; Y = gX * gW_e * sum ... with gW_e from expert e's header.
+ *  expert_offsets, rows, y: as hm_moe_gemm. E <= 1024 (W4A16), <= 256 (W4A8, W4A4).
+ *  ws: hm_moe_workspace_size(fmt, rows, E, N, K) bytes (0 for the W4A16 formats and for W4A8 with
+ *      x_scale given); need not be zeroed.
+ * Returns HM_ERR_INVALID_ARG for bad sizes, strides or pointers, HM_ERR_UNSUPPORTED for W4A4 with
+ * x_scale or K % 256 != 0, HM_ERR_WORKSPACE, HM_ERR_CUDA. One launch (plus the activation
+ * quantization); tiles m-major within each expert; experts with no rows cost nothing. */
+size_t hm_moe_workspace_size(int32_t fmt, int64_t rows, int32_t E, int64_t N, int64_t K);
+hm_status hm_moe_gemm_strided(int32_t fmt, const void* x, const void* x_scale, const int32_t* expert_offsets,
+                              int32_t E, const void* packed, int64_t expert_stride, void* y, int64_t rows,
+                              int64_t N, int64_t K, void* ws, size_t ws_bytes, void* stream);
 
 /* Allocation-free variant of hm_gemm for the W4A16 formats (HM_W4A16_INT4, HM_W4A16_MXFP4,
  * HM_W4A16_MXINT4).
@@ -309,7 +360,8 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
  * of MMAs of one tcgen05 kind from shared-memory operands into TMEM accumulators (no memory
  * traffic in the loop): kind 0 = kind::f16 (bf16, M=128, N=256, K=16), 1 = kind::mxf8f6f4
  * block-scaled 1X (e4m3 x e4m3, UE8M0 scales, M=N=128, K=32), 2 = kind::mxf4nvf4 block-scaled 4X
- * (e2m1 x e2m1, UE4M3 scales, M=N=128, K=64), several issuing warps each. *flops_out receives the
+ * (e2m1 x e2m1, UE4M3 scales, M=N=128, K=64), several issuing warps each; kinds 3 and 4 = kinds 1
+ * and 2 with N=256 and one issuing warp. *flops_out receives the
  * FLOPs (2*M*N*K per MMA) the launch issues; the caller times it on `stream` (events) to get the
  * dense peak of that kind on this device. iters in [1, 2^24]. A completion wait that runs out (2 s)
  * sets device error bit 1. Allocates nothing; the launch holds all of TMEM on each SM. */

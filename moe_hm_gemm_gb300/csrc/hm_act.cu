@@ -121,11 +121,70 @@ __global__ void amax_bf16_kernel(const __nv_bfloat16* __restrict__ x, int64_t co
   }
 }
 
+// MoE W4A4 activations: the scale atoms of expert-sorted rows are laid out per expert token tile
+// (an expert's rows need not start on a 128-row boundary): row r of expert e (rows offs[e] ..
+// offs[e+1]-1) is row i % bt of atom block tpre[e] + i / bt, i = r - offs[e], where tpre[e] is the
+// number of token tiles of bt rows of the experts before e. row_slot[r] = block * 128 + row within
+// the block, or -1 for a row of no expert (r >= offs[E]) or a block past `max_blocks`.
+constexpr int kSlotMaxExperts = 1024;
+__global__ void __launch_bounds__(1024) moe_row_slots_kernel(const int32_t* __restrict__ offsets, int E, int64_t rows,
+                                                             int bt, int64_t max_blocks, int32_t* __restrict__ row_slot) {
+  __shared__ int32_t offs[kSlotMaxExperts + 1];
+  __shared__ int32_t tpre[kSlotMaxExperts + 1];
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        const int a = offsets[e], b = offsets[e + 1];
+        offs[e] = a;
+        local += b > a ? (b - a + bt - 1) / bt : 0;
+      }
+    }
+    if (lane == 0) offs[E] = offsets[E];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) {
+        tpre[e] = run;
+        const int a = offsets[e], b = offsets[e + 1];
+        run += b > a ? (b - a + bt - 1) / bt : 0;
+      }
+    }
+  }
+  __syncthreads();
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < rows;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int32_t slot = -1;
+    if (r >= offs[0] && r < offs[E]) {
+      int lo = 0, hi = E;   // largest e with offs[e] <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offs[mid] <= r) lo = mid; else hi = mid;
+      }
+      const int64_t i = r - offs[lo];
+      const int64_t blk = static_cast<int64_t>(tpre[lo]) + i / bt;
+      if (i >= 0 && blk >= 0 && blk < max_blocks) slot = static_cast<int32_t>(blk * 128 + i % bt);
+    }
+    row_slot[r] = slot;
+  }
+}
+
 // One thread per (row, 16-block) over ceil(M/128)*128 rows; rows >= M only zero their
-// scale-atom bytes.
+// scale-atom bytes. With row_slot (MoE), the threads cover the M rows only and row r's scales go
+// to the atom row row_slot[r] (none when it is negative); the caller zeroes the atoms first.
 __global__ void act_nvfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t m, int64_t k,
                                  const float* __restrict__ g_in, const float* __restrict__ partial, int nparts,
-                                 uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float* __restrict__ g_out) {
+                                 const int32_t* __restrict__ row_slot, uint8_t* __restrict__ xq,
+                                 uint8_t* __restrict__ xs, float* __restrict__ g_out) {
   __shared__ float red[32];
   __shared__ float g_sh;
   if (g_in == nullptr) {
@@ -146,7 +205,7 @@ __global__ void act_nvfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t m,
   const float g = g_sh;
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   const int64_t blocks_per_row = k / 16;
-  const int64_t m_pad = (m + 127) / 128 * 128;
+  const int64_t m_pad = row_slot != nullptr ? m : (m + 127) / 128 * 128;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= m_pad * blocks_per_row) return;
   const int64_t row = i / blocks_per_row, b16 = i % blocks_per_row;
@@ -179,10 +238,12 @@ __global__ void act_nvfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t m,
     out.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
     *reinterpret_cast<uint2*>(xq + row * (k / 2) + b16 * 8) = out;
   }
+  const int64_t arow = row_slot != nullptr ? static_cast<int64_t>(row_slot[row]) : row;
+  if (arow < 0) return;
   const int64_t kc = (b16 * 16) / 64;
-  const int r = static_cast<int>(row % 128);
+  const int r = static_cast<int>(arow % 128);
   const int j = static_cast<int>(((b16 * 16) % 64) / 16);
-  xs[((row / 128) * (k / 64) + kc) * kAtomBytes + (r % 32) * 16 + (r / 32) * 4 + j] = static_cast<uint8_t>(sb);
+  xs[((arow / 128) * (k / 64) + kc) * kAtomBytes + (r % 32) * 16 + (r / 32) * 4 + j] = static_cast<uint8_t>(sb);
 }
 
 __global__ void wait_probe_kernel(uint32_t* err, uint64_t timeout_ns) {
@@ -261,7 +322,24 @@ cudaError_t launch_act_nvfp4(const __nv_bfloat16* x, int64_t m, int64_t k, const
   const int64_t m_pad = (m + 127) / 128 * 128;
   const int64_t threads = m_pad * (k / 16);
   act_nvfp4_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(x, m, k, g_in, ws, kAmaxBlocks,
-                                                                               xq, xs, g_out);
+                                                                               nullptr, xq, xs, g_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_nvfp4_moe(const __nv_bfloat16* x, int64_t rows, int64_t k, const int32_t* offsets, int E,
+                                 int bt, int64_t max_blocks, int32_t* row_slot, uint8_t* xq, uint8_t* xs,
+                                 float* g_out, float* ws, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  if (E < 1 || E > kSlotMaxExperts) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(xs, 0, static_cast<size_t>(max_blocks) * (k / 64) * kAtomBytes, st);
+  if (e != cudaSuccess) return e;
+  const int64_t sb = (rows + 1023) / 1024;
+  moe_row_slots_kernel<<<static_cast<unsigned>(sb < 1024 ? sb : 1024), 1024, 0, st>>>(offsets, E, rows, bt, max_blocks,
+                                                                                      row_slot);
+  amax_bf16_kernel<<<kAmaxBlocks, 256, 0, st>>>(x, rows * k / 8, ws);
+  const int64_t threads = rows * (k / 16);
+  act_nvfp4_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(x, rows, k, nullptr, ws, kAmaxBlocks,
+                                                                               row_slot, xq, xs, g_out);
   return cudaGetLastError();
 }
 

@@ -97,7 +97,26 @@ int env_int(const char* name, int dflt) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A16MxInt; }
+bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A16Int4G; }
+
+// The K values per scale a description stands for (0 stands for the format's own), or 0 when the
+// group, zero-point and convention fields do not fit the format.
+int64_t desc_group(const hm_weight_desc* d) {
+  const bool int4 = d->fmt == kW4A16Int4 || d->fmt == kW4A16Int4G;
+  if (d->has_zero != 0 && d->has_zero != 1) return 0;
+  if (d->has_zero && !int4) return 0;
+  if (d->zero_convention != HM_ZP_INT && !(d->zero_convention == HM_ZP_GPTQ && int4 && d->has_zero)) return 0;
+  if (d->fmt == kW4A16Int4) {
+    const int64_t g = d->group == 0 ? 128 : (d->group == -1 ? d->K : d->group);
+    return (g >= 128 && g % 128 == 0 && d->K % g == 0) ? g : 0;
+  }
+  if (d->fmt == kW4A16Int4G) {
+    const int64_t g = d->group == 0 ? 32 : d->group;
+    return (g == 32 || g == 64) ? g : 0;
+  }
+  const int64_t own = d->fmt == kW4A4Nv ? 16 : 32;
+  return (d->group == 0 || d->group == own) ? own : 0;
+}
 
 bool valid_k(int32_t fmt, int64_t k) {
   if (k <= 0) return false;
@@ -214,7 +233,7 @@ bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (m < 1 || m > kGemvMaxTokens) return false;
   const int mode = env_int("HM_GEMV", 1);
   if (mode == 0) return false;
-  if (mode == 2 || m <= 16 || e8_unit_fmt(fmt)) return true;
+  if (mode == 2 || m <= 16 || chunk_scaled_fmt(fmt)) return true;
   return f16_choice(m, n, k, num_sms).stream_k;
 }
 
@@ -225,7 +244,7 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.gemv = 1;
     p.tile_m = gemv_tokens(m);
     p.tile_k = 128;
-    p.stages = gemv_stages(m);
+    p.stages = gemv_stages(m, fmt);
     p.num_m_tiles = 1;
     p.num_n_tiles = pad_n(n) / 128;
     p.kb_total = k / 128;
@@ -417,6 +436,49 @@ bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int to
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token tile of the grouped GEMM from the mean rows per expert (per-expert counts stay on the
+// device); HM_MOE_TILE_M overrides. Block-scaled formats stop at 128.
+int moe_tile_m(int32_t fmt, int64_t rows, int32_t E) {
+  const int64_t mean = rows / E;
+  int t = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : (mean <= 256 ? 128 : 256)));
+  const bool bs = fmt == kW4A8Mx || fmt == kW4A4Nv;
+  const int forced = env_int("HM_MOE_TILE_M", 0);
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !bs)) t = forced;
+  if (bs && t > 128) t = 128;
+  return t;
+}
+
+// Workspace of the grouped block-scaled GEMM with bf16 activations quantized inside the call.
+struct MoeWs {
+  size_t act_q, act_s, act_g, act_amax, slots, total;
+  int64_t max_blocks;
+};
+MoeWs moe_ws_layout(int32_t fmt, int64_t rows, int32_t E, int64_t k) {
+  MoeWs w{};
+  size_t off = 0;
+  if (fmt == kW4A8Mx) {
+    w.act_q = off;
+    off += align_up(static_cast<size_t>(rows) * k);
+    w.act_s = off;
+    off += align_up(static_cast<size_t>(rows) * sizeof(float));
+  } else if (fmt == kW4A4Nv) {
+    const int bt = moe_tile_m(fmt, rows, E);
+    w.max_blocks = ceil_div(rows, bt) + E;
+    w.act_q = off;
+    off += align_up(static_cast<size_t>(rows) * k / 2);
+    w.act_s = off;
+    off += align_up(static_cast<size_t>(w.max_blocks) * (k / 64) * kAtomBytes);
+    w.act_g = off;
+    off += align_up(sizeof(float));
+    w.act_amax = off;
+    off += align_up(static_cast<size_t>(act_amax_blocks(rows, k)) * sizeof(float));
+    w.slots = off;
+    off += align_up(static_cast<size_t>(rows) * sizeof(int32_t));
+  }
+  w.total = off;
+  return w;
+}
+
 }  // namespace
 }  // namespace hm
 
@@ -426,7 +488,7 @@ extern "C" {
 
 size_t hm_packed_size(const hm_weight_desc* d) {
   if (d == nullptr || !valid_fmt(d->fmt) || d->N <= 0 || !valid_k(d->fmt, d->K)) return 0;
-  if (d->has_zero && d->fmt != kW4A16Int4) return 0;
+  if (desc_group(d) == 0) return 0;
   return kHeaderBytes + payload_bytes(d->fmt, d->N, d->K, d->has_zero != 0);
 }
 
@@ -448,7 +510,7 @@ hm_status hm_quantize_weight(const hm_weight_desc* d, const float* w, const uint
   if (d->fmt != kW4A4Nv && d->K % 128 != 0) return HM_ERR_INVALID_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
-  return cuda_status(launch_quantize_weight(d->fmt, d->has_zero, d->N, d->K, w, zeros_in,
+  return cuda_status(launch_quantize_weight(d->fmt, d->has_zero, d->N, d->K, desc_group(d), w, zeros_in,
                                             static_cast<uint8_t*>(q_out), scales_out, g_out,
                                             static_cast<float*>(ws), static_cast<cudaStream_t>(stream)));
 }
@@ -460,7 +522,8 @@ hm_status hm_transform(const hm_weight_desc* d, const void* q, const void* scale
   if (!aligned(packed, 256) || !aligned(q, 16) || !aligned(scales, 4)) return HM_ERR_INVALID_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
-  return cuda_status(launch_transform(d->fmt, d->has_zero, d->N, d->K, d->tensor_scale,
+  return cuda_status(launch_transform(d->fmt, d->has_zero, d->N, d->K, d->tensor_scale, desc_group(d),
+                                      d->zero_convention,
                                       static_cast<const uint8_t*>(q), scales, static_cast<const uint8_t*>(zeros),
                                       static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream)));
 }
@@ -615,10 +678,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
     prm.timeout_ns = timeout_ns();
     prm.trace = trace_for(di, p.grid);
-    if (p.gemv) {
-      prm.trace = nullptr;
-      return cuda_status(launch_gemv(prm, st));
-    }
+    if (p.gemv) return cuda_status(launch_gemv(prm, st));
     return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
   }
 
@@ -698,10 +758,7 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   // Token tile from the mean rows per expert (per-expert counts stay on the device); past 256 rows
   // per expert the 256-token tile's halved dequant work per FLOP outweighs its padding of the
   // smaller experts (measured: T=16384, E=256, top-8 runs 20 % faster than with 128).
-  const int64_t mean = rows / E;
-  int tile_m = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : (mean <= 256 ? 128 : 256)));
-  const int forced = env_int("HM_MOE_TILE_M", 0);
-  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || forced == 256) tile_m = forced;
+  const int tile_m = moe_tile_m(fmt, rows, E);
   if (log_on())
     std::fprintf(stderr, "[hm] hm_moe_gemm fmt=%d E=%d rows=%lld N=%lld K=%lld kernel=tcgen05 tile_m=%d grid=%d\n", fmt, E,
                  static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K), tile_m, di.num_sms);
@@ -722,6 +779,124 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
   prm.timeout_ns = timeout_ns();
   return cuda_status(launch_f16_gemm(prm, tile_m, true, cudaStream_t(stream)));
+}
+
+size_t hm_moe_workspace_size(int32_t fmt, int64_t rows, int32_t E, int64_t N, int64_t K) {
+  if (!valid_fmt(fmt) || rows < 0 || E < 1 || N <= 0 || !valid_k(fmt, K)) return 0;
+  return moe_ws_layout(fmt, rows, E, K).total;
+}
+
+hm_status hm_moe_gemm_strided(int32_t fmt, const void* x, const void* x_scale, const int32_t* expert_offsets, int32_t E,
+                              const void* packed, int64_t expert_stride, void* y, int64_t rows, int64_t N, int64_t K,
+                              void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_fmt(fmt) || rows < 0 || N <= 0 || !valid_k(fmt, K) || E < 1 || E > 1024) return HM_ERR_INVALID_ARG;
+  if (rows == 0) return HM_OK;
+  if (x == nullptr || expert_offsets == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 4) || (N % 2) != 0 || !aligned(packed, 256) || !aligned(expert_offsets, 4))
+    return HM_ERR_INVALID_ARG;
+  // (INT4 without zero-points packs smaller; either size may be passed as the stride, and every
+  // expert's header is checked on the device)
+  hm_weight_desc d0{fmt, 0, N, K, 1.0f, 0, 0};
+  if (expert_stride < static_cast<int64_t>(hm_packed_size(&d0)) || expert_stride % 256 != 0) return HM_ERR_INVALID_ARG;
+  const bool bs = fmt == kW4A8Mx || fmt == kW4A4Nv;
+  if (fmt == kW4A4Nv && (x_scale != nullptr || K % 256 != 0)) return HM_ERR_UNSUPPORTED;
+  if (bs && E > kMxMoeMaxExperts) return HM_ERR_UNSUPPORTED;
+  const MoeWs wl = moe_ws_layout(fmt, rows, E, K);
+  if (bs && x_scale == nullptr && (ws == nullptr || ws_bytes < wl.total)) return HM_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (!device_info(&di)) return HM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int tile_m = moe_tile_m(fmt, rows, E);
+  if (log_on())
+    std::fprintf(stderr, "[hm] hm_moe_gemm_strided fmt=%d E=%d rows=%lld N=%lld K=%lld tile_m=%d\n", fmt, E,
+                 static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K), tile_m);
+  if (!bs) {
+    if ((rows / 16 + 1 + E) * (pad_n(N) / 128) * (K / 128) >= (int64_t{1} << 31)) return HM_ERR_UNSUPPORTED;
+    F16Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    if (!encode_x_f16(&prm.tmap_x, x, K, rows, tile_m)) return HM_ERR_CUDA;
+    prm.packed = static_cast<const uint8_t*>(packed);
+    prm.packed_list = nullptr;
+    prm.expert_stride = expert_stride;
+    prm.offsets = expert_offsets;
+    prm.y = static_cast<__nv_bfloat16*>(y);
+    prm.err = di.err;
+    prm.m = rows;
+    prm.n = N;
+    prm.k = K;
+    prm.fmt = fmt;
+    prm.num_experts = E;
+    prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
+    prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
+    prm.timeout_ns = timeout_ns();
+    return cuda_status(launch_f16_gemm(prm, tile_m, true, st));
+  }
+  const int64_t n_pad = pad_n(N), k_pad = pad_k(fmt, K);
+  if ((rows / 16 + 1 + E) * (n_pad / 128) * (k_pad / (fmt == kW4A4Nv ? 256 : 128)) >= (int64_t{1} << 31))
+    return HM_ERR_UNSUPPORTED;
+  const bool internal_act = x_scale == nullptr;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const uint8_t* xq = static_cast<const uint8_t*>(x);
+  const void* xs = x_scale;
+  const float* xg = nullptr;
+  if (internal_act) {
+    uint8_t* q = wsb + wl.act_q;
+    if (fmt == kW4A8Mx) {
+      float* sp = reinterpret_cast<float*>(wsb + wl.act_s);
+      if (launch_act_fp8(static_cast<const __nv_bfloat16*>(x), rows, K, q, sp, st) != cudaSuccess) return HM_ERR_CUDA;
+      xs = sp;
+    } else {
+      float* g = reinterpret_cast<float*>(wsb + wl.act_g);
+      if (launch_act_nvfp4_moe(static_cast<const __nv_bfloat16*>(x), rows, K, expert_offsets, E, tile_m, wl.max_blocks,
+                               reinterpret_cast<int32_t*>(wsb + wl.slots), q, wsb + wl.act_s, g,
+                               reinterpret_cast<float*>(wsb + wl.act_amax), st) != cudaSuccess)
+        return HM_ERR_CUDA;
+      xs = wsb + wl.act_s;
+      xg = g;
+    }
+    xq = q;
+  }
+  MxParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const uint8_t* body = static_cast<const uint8_t*>(packed) + kHeaderBytes;
+  {
+    const bool w8 = fmt == kW4A8Mx;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(w8 ? k_pad : k_pad / 2), static_cast<cuuint64_t>(n_pad),
+                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k_pad / 2), static_cast<cuuint64_t>(expert_stride)};
+    const cuuint32_t box[3] = {128, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (g_encode(&prm.tmap_w, w8 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                 const_cast<uint8_t*>(body), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return HM_ERR_CUDA;
+    const bool ok = w8 ? encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K, rows, K, 128, tile_m)
+                       : encode_2d(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K / 2, rows, K / 2, 128, tile_m);
+    if (!ok) return HM_ERR_CUDA;
+  }
+  prm.packed = static_cast<const uint8_t*>(packed);
+  prm.w_atoms = body + static_cast<size_t>(n_pad) * k_pad / 2;
+  prm.offsets = expert_offsets;
+  prm.num_experts = E;
+  prm.expert_stride = expert_stride;
+  prm.x_atoms = static_cast<const uint8_t*>(xs);
+  prm.s_tok = static_cast<const float*>(xs);
+  prm.x_global = xg;
+  prm.y = static_cast<__nv_bfloat16*>(y);
+  prm.err = di.err;
+  prm.m = rows;
+  prm.n = N;
+  prm.k = K;
+  prm.fmt = fmt;
+  prm.num_m_tiles = 0;
+  prm.num_n_tiles = static_cast<int32_t>(n_pad / 128);
+  prm.k_blocks = static_cast<int32_t>(k_pad / (fmt == kW4A4Nv ? 256 : 128));
+  prm.sched = SchedParams{0, prm.k_blocks, di.num_sms * kMxCtasPerSm, 0};
+  prm.timeout_ns = timeout_ns();
+  const cudaError_t e = launch_mx_moe_gemm(prm, tile_m, st);
+  if (e == cudaErrorNotSupported) return HM_ERR_UNSUPPORTED;
+  return cuda_status(e);
 }
 
 hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, void* y, int64_t M, int64_t N,
@@ -792,7 +967,7 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns_, void* stream) {
 }
 
 hm_status hm_mma_peak_probe(int32_t kind, int32_t iters, double* flops_out, void* stream) {
-  if (kind < 0 || kind > 2 || iters < 1 || iters > (1 << 24) || flops_out == nullptr) return HM_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 4 || iters < 1 || iters > (1 << 24) || flops_out == nullptr) return HM_ERR_INVALID_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
   return cuda_status(launch_mma_peak(kind, iters, di.num_sms, di.err, kDefaultTimeoutNs,

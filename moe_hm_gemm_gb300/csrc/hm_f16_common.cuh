@@ -54,7 +54,7 @@ __device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, co
     t.m0 = offs[e] + mt * BT;
     t.m_end = min(offs[e + 1], t.m0 + BT);
     t.n0 = nt * 128;
-    t.base = p.packed_list[e];
+    t.base = p.packed_list != nullptr ? p.packed_list[e] : p.packed + static_cast<size_t>(e) * p.expert_stride;
     t.wbase = t.base + kHeaderBytes + static_cast<size_t>(nt) * kb_total * unit;
   }
   return t;

@@ -72,14 +72,14 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 // threads. Small token tiles (N <= 64, where one MMA is far below that wait) therefore use two
 // issuing warps that take alternate 128-K blocks into separate accumulators, which the epilogue
 // adds (issuer 0 first, so the sum is deterministic).
-template <int BT>
+template <int BT, int UB = kUnitMx>
 struct F16Shape {
   static constexpr bool kATmem = BT <= 128;
   static constexpr int kIss = BT <= 64 ? 2 : 1;
   static constexpr int kAccCols = 2 * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
   static constexpr int kG = f16_group_of(BT);
   static constexpr int kXStage = kG * BT * 128 * 2;
-  static constexpr int kWStage = kG * kUnitMx;  // room for the largest units
+  static constexpr int kWStage = kG * UB;  // room for the largest units of the formats served
   static constexpr int kSA = kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2;
   static constexpr int kAOff = 0;
   static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
@@ -100,10 +100,14 @@ struct F16Shape {
   static_assert(kATmem || kIss == 1, "two issuers only with A in TMEM");
 };
 
-// WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4.
+// Unit bytes a load stage must hold per 128-K block for a weight format (WK).
+constexpr int f16_unit_room(int wk) { return wk == 6 ? static_cast<int>(kUnitG32Zp) : static_cast<int>(kUnitMx); }
+
+// WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4,
+// 6 = INT4 with a bf16 scale and u4 zero-point per 32-K chunk.
 template <int BT, int WK, bool MOE>
 __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
-  using S = F16Shape<BT>;
+  using S = F16Shape<BT, f16_unit_room(WK)>;
   constexpr int SL = S::kSL;
   constexpr int SA = S::kSA;
 
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // latency overlaps the set-up. MoE offsets (and thus expert pointers) may come from the
     // previous kernel, so the MoE variant waits for it first.
     if (MOE) pdl_wait();
-    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
+    const uint8_t* first = (MOE && p.packed_list != nullptr) ? p.packed_list[0] : p.packed;
     const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first);
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // The first weight's header decides whether INT4 units carry zero-points; every weight
     // used must agree with it and with the call's (fmt, N, K).
     const uint32_t hz = hdr.has_zero;
-    *hz_sh = (WK == 0 && hz == 1u) ? 1u : 0u;
+    *hz_sh = ((WK == 0 || WK == 6) && hz == 1u) ? 1u : 0u;
     if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
       atomicOr(p.err, kErrHeader);
       *abort_flag = 1u;
@@ -191,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     trace_mark(p.trace, 1);
     pdl_launch_dependents();
   }
-  const uint32_t kUnit = WK >= 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  const uint32_t kUnit = WK == 6 ? (has_zero ? kUnitG32Zp : kUnitG32)
+                                  : (WK >= 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4));
   // Weights are streamed once when a single token tile covers M; with several token tiles the
   // same weight tiles are read again by other CTAs, so keep them in L2.
   const bool reuse_w = MOE || p.num_m_tiles > 1;
@@ -416,7 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         for (int i = 0; i < (WK == 2 ? 2 : 4); ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
         __nv_bfloat162 zz, ss;
         uint32_t e4 = 0;
-        if (WK >= 2) {
+        uint32_t s4[2] = {0u, 0u}, z4 = 0x8888u;   // WK 6: the four chunks' bf16 scales and zero-points
+        if (WK == 6) {
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(s4[0]), "=r"(s4[1]) : "r"(wsa + kUnitCodes + 8 * r));
+          if (has_zero) {
+            uint16_t zb;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitG32 + 2 * r));
+            z4 = zb;
+          }
+          zz = int4_zero_pair(8);
+          ss = bf16_pair(0);
+        } else if (WK >= 2) {
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e4) : "r"(wsa + kUnitCodes + 4 * r));
           zz = int4_zero_pair(8);   // MXINT4 nibbles are q + 8
         } else {
@@ -459,7 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t o[4];
-              if (WK == 0) dq_int4_word(words[j], zz, ss, o);
+              if (WK == 6)
+                dq_int4_word(words[j], int4_zero_pair((z4 >> (4 * c4)) & 0xFu),
+                             bf16_pair(static_cast<uint16_t>(s4[c4 >> 1] >> (16 * (c4 & 1)))), o);
+              else if (WK == 0) dq_int4_word(words[j], zz, ss, o);
               else if (WK == 3) dq_int4_word(words[j], zz, si, o);
               else if (mx_bits) dq_mx_word_bits(words[j], sc2, o);
               else dq_mx_word(words[j], lut, scale, o);
@@ -596,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 
 template <int BT, int WK, bool MOE>
 cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
-  using S = F16Shape<BT>;
+  using S = F16Shape<BT, f16_unit_room(WK)>;
   auto kern = f16_gemm_kernel<BT, WK, MOE>;
   const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
   // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
@@ -631,5 +649,6 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
 // kernel instantiations compile in parallel.
 cudaError_t launch_f16_mxfp4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
 cudaError_t launch_f16_mxint4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+cudaError_t launch_f16_int4g(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
 
 }  // namespace hm

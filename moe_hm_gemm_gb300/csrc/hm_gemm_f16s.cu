@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kSThreads, 1) f16s_gemm_kernel(const __grid_co
   if (threadIdx.x == 0) {
     trace_mark(p.trace, 0);
     if (MOE) pdl_wait();   // expert pointers may come from the previous kernel
-    const uint8_t* first = MOE ? p.packed_list[0] : p.packed;
+    const uint8_t* first = (MOE && p.packed_list != nullptr) ? p.packed_list[0] : p.packed;
     const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first);
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);

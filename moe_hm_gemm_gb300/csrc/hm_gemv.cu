@@ -77,10 +77,10 @@ __host__ __device__ constexpr int v_consumers(int mt) { return 8 * v_par(mt); }
 __host__ __device__ constexpr int v_meta_warp(int mt) { return kVCons0 + v_consumers(mt); }
 __host__ __device__ constexpr int v_threads(int mt) { return 32 * (v_meta_warp(mt) + 1); }
 
-template <int MT>
+template <int MT, int WB = 8704>
 struct VShape {
   static constexpr int kNQ = MT / 8;                // token groups of 8 (MMA N)
-  static constexpr int kWBytes = 8704;              // one unit (the largest, MXFP4)
+  static constexpr int kWBytes = WB;                // one unit (the largest of the formats served)
   // activations: MT token rows of 128 bf16, as one TMA box lands them. The two token rows a
   // quarter-warp reads then share banks (a 2-way conflict on two loads per warp and unit), which
   // costs less than a wider, padded box: the activation box is a TMA operation per unit, and a
@@ -184,11 +184,16 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-// WK: 0 = INT4, 2 = MXFP4, 3 = MXINT4 (the last two carry E8M0 scales per 32 in their units).
+// Unit bytes a stage holds for a weight format (WK).
+__host__ __device__ constexpr int v_wbytes(int wk) { return wk == 6 ? 9472 : 8704; }
+
+// WK: 0 = INT4, 2 = MXFP4, 3 = MXINT4 (the last two carry E8M0 scales per 32 in their units),
+// 6 = INT4 with a bf16 scale (and zero-point) per 32-K chunk, applied to each chunk's sum.
 template <int MT, int WK>
 __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_constant__ F16Params p) {
-  using S = VShape<MT>;
-  constexpr bool MX = WK >= 2;
+  using S = VShape<MT, v_wbytes(WK)>;
+  constexpr bool MX = WK == 2 || WK == 3;
+  constexpr bool G32 = WK == 6;
   constexpr int SL = S::kS;
   constexpr int NQ = S::kNQ;
   extern __shared__ uint8_t smem_raw[];
@@ -219,6 +224,12 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   const int m_rows = static_cast<int>(p.m);
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, 0);
+    if (p.trace != nullptr) {
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      p.trace[blockIdx.x * 16 + 13] = smid;
+    }
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 8);   // the 8 consumer warps of the stage's unit parity
@@ -242,11 +253,14 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   __syncthreads();
   // the owner's barriers must be initialised before another CTA of its cluster arrives on them
   if (csize > 1) cluster_sync_all();
-  if (threadIdx.x == 0) pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    pdl_launch_dependents();
+    trace_mark(p.trace, 1);
+  }
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const bool aborted_early = *abort_flag != 0u;
   const uint32_t has_zero = *hz_sh;
-  const uint32_t kUnit = MX ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
+  const uint32_t kUnit = MX ? kUnitMx : (G32 ? (has_zero ? kUnitG32Zp : kUnitG32) : (has_zero ? kUnitInt4Zp : kUnitInt4));
 
   if (aborted_early) {
     // header mismatch: nothing was issued
@@ -256,23 +270,35 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     const uint8_t* wsrc = p.packed + kHeaderBytes + static_cast<size_t>(u0) * kUnit;
     const uint32_t stage_bytes = kUnit + static_cast<uint32_t>(S::kXBytes);
     const int first = n_units < SL ? n_units : SL;
-    // start-up: the weights of the first stages, one stage per lane (a single thread takes ~70 ns
-    // per bulk copy issue), before waiting for the previous kernel (weights are never written by
-    // another kernel); their activation blocks follow from lane 0 after the wait
-    if (lane < first) {
+    // Start-up, one stage per lane (a single thread takes ~70 ns per bulk-copy issue): the weights
+    // of the first few stages before waiting for the previous kernel (weights are never written
+    // by another kernel), then, after the wait, their activation blocks, and only then the rest of
+    // the first stages, weights and activations. The TMA unit works through its copies roughly in
+    // issue order, so the first stages complete without queueing behind the whole ring's weights.
+    constexpr int kEarly = 4;
+    const int early = first < kEarly ? first : kEarly;
+    if (lane < early) {
       mbar_arrive_expect_tx(&full[lane], stage_bytes);
       bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
     }
+    if (lane == 0) {
+      trace_mark(p.trace, 2);
+      prefetch_tmap(&p.tmap_x);
+    }
+    const uint64_t pol_x = policy_evict_last();
+    pdl_wait();
+    if (lane == 0) trace_mark(p.trace, 5);
+    const int kb_lane = (kb0 + lane) % kb_total;   // k-block of stage `lane`
+    if (lane < early) tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
+    __syncwarp();
+    if (lane >= early && lane < first) {
+      mbar_arrive_expect_tx(&full[lane], stage_bytes);
+      bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
+      tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
+    }
     __syncwarp();
     if (lane == 0) {
-      prefetch_tmap(&p.tmap_x);
-      const uint64_t pol_x = policy_evict_last();
-      pdl_wait();
-      int kb = kb0;
-      for (int i = 0; i < first; ++i) {
-        tma_2d_g2s(smem + i * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, 0, &full[i], pol_x);
-        if (++kb == kb_total) kb = 0;
-      }
+      int kb = (kb0 + first) % kb_total;
       int issued = first, s = 0;
       uint32_t ph = 0;
       for (int i = first; i < n_units; ++i) {
@@ -284,6 +310,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
         issued = i + 1;
         if (++s == SL) { s = 0; ph ^= 1u; }
       }
+      trace_mark(p.trace, 3);
       // nothing may still be landing in shared memory when the CTA exits
       for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
         drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
@@ -292,7 +319,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     // ---------------------------------------------------------------- INT4 row metadata
     // Each unit's 128 scales and zero-points, once per unit instead of once per consumer warp:
     // lane l converts rows 4l .. 4l+3 (bf16 scale -> fp32, u4 zero-point -> bf16x2 128 + z).
-    if constexpr (!MX) {
+    if constexpr (WK == 0) {
       const uint32_t smem0 = smem_u32(smem);
       int s = 0;
       uint32_t ph = 0;
@@ -505,7 +532,8 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
           for (int e = 0; e < 4; ++e) yacc[j][q][e] = 0.f;
       bool ok = true;
       for (; i < seg_end; i += S::kPar) {
-        if (!mbar_wait(&full[s], ph, wc) || (!MX && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
+        if (!mbar_wait(&full[s], ph, wc) || (WK == 0 && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
+        if (cw == 0 && lane == 0 && i == 0) trace_mark(p.trace, 4);
         const uint32_t base = smem0 + s * S::kStage;
         uint32_t bx[NQ][2][4];
 #pragma unroll
@@ -522,7 +550,50 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
           for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff + cc * 2048 + j * 256 + hl * 128);
-        if constexpr (!MX) {
+        if constexpr (G32) {
+          // per (row, 32-K chunk): bf16 scales of chunks 2cp, 2cp + 1 in one word, u4 zero-points
+          // of the row's four chunks in one half-word
+          uint32_t sw[2][2], zw[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+              const uint32_t rr = static_cast<uint32_t>(32 * pr + g + 16 * j + 8 * hl);
+              sw[j][hl] = lds32(base + kUnitCodes + rr * 8 + 4 * cp);
+              uint32_t zb = 0x8888u;
+              if (has_zero) {
+                uint16_t h16;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h16) : "r"(base + kUnitG32 + rr * 2));
+                zb = h16;
+              }
+              zw[j][hl] = zb >> (8 * cp);   // chunks 2cp, 2cp + 1 in the low byte
+            }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float d[2][NQ][4];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t lo[4], hi[4];
+              const uint32_t zl = (zw[j][0] >> (4 * cc)) & 0xFu, zh = (zw[j][1] >> (4 * cc)) & 0xFu;
+              dq_int4_word_unscaled(wd[j][0][cc], 0x43004300u | zl | (zl << 16), lo);
+              dq_int4_word_unscaled(wd[j][1][cc], 0x43004300u | zh | (zh << 16), hi);
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+                mma_bf16_16816_z(d[cc][q], lo[0], hi[0], lo[1], hi[1], bx[q][cc][0], bx[q][cc][1]);
+                mma_bf16_16816(d[cc][q], lo[2], hi[2], lo[3], hi[3], bx[q][cc][2], bx[q][cc][3]);
+              }
+            }
+            const float s00 = __uint_as_float(sw[j][0] << 16), s01 = __uint_as_float(sw[j][0] & 0xFFFF0000u);
+            const float s10 = __uint_as_float(sw[j][1] << 16), s11 = __uint_as_float(sw[j][1] & 0xFFFF0000u);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              yacc[j][q][0] = fmaf(s01, d[1][q][0], fmaf(s00, d[0][q][0], yacc[j][q][0]));
+              yacc[j][q][1] = fmaf(s01, d[1][q][1], fmaf(s00, d[0][q][1], yacc[j][q][1]));
+              yacc[j][q][2] = fmaf(s11, d[1][q][2], fmaf(s10, d[0][q][2], yacc[j][q][2]));
+              yacc[j][q][3] = fmaf(s11, d[1][q][3], fmaf(s10, d[0][q][3], yacc[j][q][3]));
+            }
+          }
+        } else if constexpr (!MX) {
           float sc[2][2];
           uint32_t z2[2][2];
 #pragma unroll
@@ -590,21 +661,25 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
         if (s >= SL) { s -= SL; ph ^= 1u; }
       }
       if (!ok) break;
+      if (cw == 0 && lane == 0 && seg_end == n_units) trace_mark(p.trace, 7);
       // every warp closes every segment, even one without a unit of its parity
       if (!finish(tile, seg_kb0 + (seg_end - seg_begin))) break;
+      if (cw == 0 && lane == 0 && seg_end == n_units) trace_mark(p.trace, 9);
       ++seg_count;
       seg_kb0 = 0;
     }
   }
+  if (lane == 0) trace_stage(p.trace, 0, warp);   // (diagnostics: when each warp finished its role)
   __syncwarp();
   __syncthreads();
   // no CTA leaves while another of its cluster may still write into its shared memory
   if (csize > 1) cluster_sync_all();
+  if (threadIdx.x == 0) trace_mark(p.trace, 12);
 }
 
 template <int MT, int WK>
 cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
-  using S = VShape<MT>;
+  using S = VShape<MT, v_wbytes(WK)>;
   auto kern = gemv_kernel<MT, WK>;
   static int configured[64] = {};
   static int cluster_max[64][kVMaxCluster + 1] = {};   // active clusters the device holds, +1 (0 unknown)
@@ -665,8 +740,10 @@ cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
 
 int gemv_tokens(int64_t m) { return m <= 8 ? 8 : (m <= 16 ? 16 : 32); }
 
-int gemv_stages(int64_t m) {
+int gemv_stages(int64_t m, int32_t fmt) {
   const int t = gemv_tokens(m);
+  if (fmt == kW4A16Int4G)
+    return t == 8 ? VShape<8, v_wbytes(6)>::kS : (t == 16 ? VShape<16, v_wbytes(6)>::kS : VShape<32, v_wbytes(6)>::kS);
   return t == 8 ? VShape<8>::kS : (t == 16 ? VShape<16>::kS : VShape<32>::kS);
 }
 
@@ -677,6 +754,8 @@ cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
     return t == 8 ? launch_v<8, 2>(p, st) : (t == 16 ? launch_v<16, 2>(p, st) : launch_v<32, 2>(p, st));
   if (p.fmt == kW4A16MxInt)
     return t == 8 ? launch_v<8, 3>(p, st) : (t == 16 ? launch_v<16, 3>(p, st) : launch_v<32, 3>(p, st));
+  if (p.fmt == kW4A16Int4G)
+    return t == 8 ? launch_v<8, 6>(p, st) : (t == 16 ? launch_v<16, 6>(p, st) : launch_v<32, 6>(p, st));
   return t == 8 ? launch_v<8, 0>(p, st) : (t == 16 ? launch_v<16, 0>(p, st) : launch_v<32, 0>(p, st));
 }
 

@@ -16,7 +16,9 @@ namespace hm {
 struct F16Params {
   CUtensorMap tmap_x;                 // X bf16 [rows][K], box {64, tile_m}, 128-byte swizzle
   const uint8_t* packed;              // dense: packed weight (header first)
-  const uint8_t* const* packed_list;  // MoE: device array of E packed weights
+  const uint8_t* const* packed_list;  // MoE: device array of E packed weights, or NULL when the
+                                      // experts lie at packed + e * expert_stride
+  int64_t expert_stride;              // MoE with packed_list == NULL: bytes between experts
   const int32_t* offsets;             // MoE: expert offsets [E+1]
   __nv_bfloat16* y;                   // [rows][N]
   float* partial;                     // stream-K partial tiles [grid][2][tile_m][128]
@@ -35,10 +37,13 @@ struct F16Params {
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
 struct MxParams {
-  CUtensorMap tmap_w;                 // weight codes
+  CUtensorMap tmap_w;                 // weight codes (MoE: 3-D, the experts as third dimension)
   CUtensorMap tmap_x;                 // activation codes
-  const uint8_t* packed;              // packed weight (header; scale atoms after the codes)
-  const uint8_t* w_atoms;             // first weight scale atom
+  const uint8_t* packed;              // packed weight (header; scale atoms after the codes); MoE: expert 0
+  const uint8_t* w_atoms;             // first weight scale atom (MoE: of expert 0)
+  const int32_t* offsets;             // MoE: expert offsets [E+1] (device)
+  int32_t num_experts;                // MoE: E (0 = dense)
+  int64_t expert_stride;              // MoE: bytes between consecutive experts' packed weights
   const uint8_t* x_atoms;             // NVFP4 activation scale atoms
   const float* s_tok;                 // W4A8 per-token scales [M]
   const float* x_global;              // W4A4 activation tensor scale (device scalar)
@@ -87,6 +92,9 @@ cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream
 constexpr int f16_group_of(int tile_m) { return tile_m <= 32 ? 4 : (tile_m == 64 ? 2 : 1); }
 int f16_group(int tile_m);
 cudaError_t launch_mx_gemm(const MxParams& p, int tile_m, cudaStream_t st);
+// Grouped (MoE) block-scaled GEMM: p.num_experts >= 1, at most kMxMoeMaxExperts.
+constexpr int kMxMoeMaxExperts = 256;
+cudaError_t launch_mx_moe_gemm(const MxParams& p, int tile_m, cudaStream_t st);
 // The block-scaled kernel runs two CTAs per SM (the plan's grid counts CTAs, not SMs).
 constexpr int kMxCtasPerSm = 2;
 // Load stages of the W4A16 kernel that serves (fmt, tile_m).
@@ -104,14 +112,14 @@ constexpr int kGemvMaxTokens = 32;
 constexpr int kGemvCounters = 8;   // arrival counters per output tile (one per consumer warp)
 cudaError_t launch_gemv(const F16Params& p, cudaStream_t st);
 int gemv_tokens(int64_t m);
-int gemv_stages(int64_t m);
+int gemv_stages(int64_t m, int32_t fmt);
 
 // Weight preprocessing and activation quantization launchers (hm_weights.cu, hm_act.cu).
-cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k,
+cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, int64_t group,
                                    const float* w, const uint8_t* zeros_in, uint8_t* q_out,
                                    void* scales_out, float* g_out, float* ws, cudaStream_t st);
-cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, float gw,
-                             const uint8_t* q, const void* scales, const uint8_t* zeros,
+cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, float gw, int64_t group,
+                             int32_t zconv, const uint8_t* q, const void* scales, const uint8_t* zeros,
                              uint8_t* packed, cudaStream_t st);
 cudaError_t launch_dequant(int32_t fmt, int32_t has_zero, int64_t n, int64_t k,
                            const uint8_t* packed, __nv_bfloat16* w, cudaStream_t st);
@@ -120,6 +128,12 @@ cudaError_t launch_act_fp8(const __nv_bfloat16* x, int64_t m, int64_t k, uint8_t
 cudaError_t launch_act_nvfp4(const __nv_bfloat16* x, int64_t m, int64_t k, const float* g_in,
                              uint8_t* xq, uint8_t* xs, float* g_out, float* ws, cudaStream_t st);
 int act_amax_blocks(int64_t m, int64_t k);
+// NVFP4 quantization of expert-sorted rows for the grouped W4A4 GEMM: codes as the dense layout,
+// scale atoms per expert token tile of `bt` rows (at most max_blocks blocks of 128 rows, zeroed
+// first); row_slot is [rows] int32 scratch; the tensor scale is computed over all rows.
+cudaError_t launch_act_nvfp4_moe(const __nv_bfloat16* x, int64_t rows, int64_t k, const int32_t* offsets, int E,
+                                 int bt, int64_t max_blocks, int32_t* row_slot, uint8_t* xq, uint8_t* xs,
+                                 float* g_out, float* ws, cudaStream_t st);
 // MoE expert activation: h[rows][inter] = bf16(SiLU(gate) * up) from gate_up[rows][2*inter].
 cudaError_t launch_silu_mul(const __nv_bfloat16* gu, __nv_bfloat16* h, int64_t rows, int64_t inter, int num_sms,
                             cudaStream_t st);

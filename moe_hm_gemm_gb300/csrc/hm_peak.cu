@@ -11,7 +11,8 @@
 //   kind 1: kind::mxf8f6f4.block_scale.scale_vec::1X, e4m3 x e4m3 with UE8M0 scales, M = N = 128,
 //           K = 32, three issuers;
 //   kind 2: kind::mxf4nvf4.block_scale.scale_vec::4X, e2m1 x e2m1 with UE4M3 scales, M = N = 128,
-//           K = 64, three issuers.
+//           K = 64, three issuers;
+//   kinds 3 and 4: kinds 1 and 2 with N = 256 and one issuer (the widest instruction of the kind).
 // The operand values are arbitrary finite numbers (the tensor pipe's rate does not depend on
 // them). The caller times the launch with events; hm_mma_peak_probe reports the FLOPs it issued.
 #include <cuda_bf16.h>
@@ -27,9 +28,11 @@ constexpr int kPeakSmem = 120 * 1024;   // keeps one CTA per SM (the probe alloc
 
 template <int KIND>
 struct PeakShape {
-  static constexpr int kN = KIND == 0 ? 256 : 128;
-  static constexpr int kK = KIND == 0 ? 16 : (KIND == 1 ? 32 : 64);   // K per instruction
-  static constexpr int kIssuers = KIND == 0 ? 2 : 3;
+  static constexpr int kN = (KIND == 0 || KIND >= 3) ? 256 : 128;
+  static constexpr int kK = KIND == 0 ? 16 : ((KIND == 1 || KIND == 3) ? 32 : 64);   // K per instruction
+  static constexpr int kIssuers = KIND == 0 ? 2 : (KIND >= 3 ? 1 : 3);
+  static constexpr int kBase = KIND >= 3 ? 1 : KIND;                                 // MMA kind of kinds 3, 4
+  static constexpr int kSfCol = KIND >= 3 ? 256 : 384;                               // first scale column
   static constexpr int kAOff = 0;                                     // 128 rows x 128 bytes
   static constexpr int kBOff = 128 * 128;                             // kN rows x 128 bytes
   static constexpr int kSfOff = kBOff + kN * 128;                     // 8 scale atoms of 512 bytes
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
     uint32_t v;
     if (KIND == 0) {
       v = (h & 0x807F807Fu) | 0x3C003C00u;   // bf16 values of magnitude in [2^-7, 2^-6)
-    } else if (KIND == 1) {
+    } else if (KIND == 1 || KIND == 3) {
       v = h & 0xF7F7F7F7u;                   // e4m3 without the NaN codes (exponent field <= 14)
     } else {
       v = h;                                 // e2m1: every code is finite
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
     words[i] = v;
   }
   // scale factors: 1.0 (UE8M0 127, UE4M3 0x38)
-  const uint32_t one4 = KIND == 1 ? 0x7F7F7F7Fu : 0x38383838u;
+  const uint32_t one4 = (KIND == 1 || KIND == 3) ? 0x7F7F7F7Fu : 0x38383838u;
   for (int i = threadIdx.x; i < 8 * 512 / 4; i += kPeakThreads) words[S::kSfOff / 4 + i] = one4;
   if (threadIdx.x == 0) {
     for (int w = 0; w < S::kIssuers; ++w) mbar_init(&done[w], 1);
@@ -90,12 +93,16 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
     const uint32_t a0 = smem_u32(smem + S::kAOff), b0 = smem_u32(smem + S::kBOff);
     const uint32_t d = tmem + static_cast<uint32_t>(issuer * S::kN);
     // this issuer's scale-factor columns (block-scaled kinds): after the accumulators
-    const uint32_t sf = tmem + 384u + static_cast<uint32_t>(issuer * 32);
-    if (KIND == 1) {
-      tc_cp_32x128b_x4(sf, sdesc_sf(smem_u32(smem + S::kSfOff)));
-      tc_cp_32x128b_x4(sf + 4, sdesc_sf(smem_u32(smem + S::kSfOff + 512)));
-    } else if (KIND == 2) {
+    const uint32_t sf = tmem + static_cast<uint32_t>(S::kSfCol) + static_cast<uint32_t>(issuer * 32);
+    // (kinds 3 and 4: the B scales of 256 rows span twice the columns of 128; all of them lie in
+    // the allocation and hold 1.0)
+    if (KIND == 1 || KIND == 3) {
+      for (int j = 0; j < (KIND == 3 ? 4 : 2); ++j)
+        tc_cp_32x128b_x4(sf + 4 * j, sdesc_sf(smem_u32(smem + S::kSfOff + 512 * j)));
+    } else if (KIND == 2 || KIND == 4) {
       for (int j = 0; j < 8; ++j) tc_cp_32x128b_x4(sf + 4 * j, sdesc_sf(smem_u32(smem + S::kSfOff + 512 * j)));
+      if (KIND == 4)
+        for (int j = 0; j < 8; ++j) tc_cp_32x128b_x4(sf + 32 + 4 * j, sdesc_sf(smem_u32(smem + S::kSfOff + 512 * j)));
     }
     for (int32_t it = 0; it < iters; ++it) {
 #pragma unroll
@@ -105,11 +112,11 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
         const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
         if constexpr (KIND == 0) {
           mma_bf16(d, ad, bd, idesc_bf16(128, S::kN), acc);
-        } else if constexpr (KIND == 1) {
+        } else if constexpr (KIND == 1 || KIND == 3) {
           mma_mxf8f6f4(d, ad, bd, idesc_block_scaled(128, S::kN, 0, 0, 1, k, k), sf, sf + 4, acc);
         } else {
-          mma_mxf4nvf4_4x(d, ad, bd, idesc_block_scaled(128, S::kN, 1, 1, 0, 0, 0), sf + 4 * k, sf + 16 + 4 * k,
-                          acc);
+          mma_mxf4nvf4_4x(d, ad, bd, idesc_block_scaled(128, S::kN, 1, 1, 0, 0, 0), sf + 4 * k,
+                          sf + (KIND == 4 ? 32 + 8 * k : 16 + 4 * k), acc);
         }
       }
     }
@@ -156,6 +163,8 @@ cudaError_t launch_mma_peak(int kind, int32_t iters, int num_sms, uint32_t* err,
   if (kind == 0) return launch_peak<0>(iters, num_sms, err, timeout_ns, st, flops);
   if (kind == 1) return launch_peak<1>(iters, num_sms, err, timeout_ns, st, flops);
   if (kind == 2) return launch_peak<2>(iters, num_sms, err, timeout_ns, st, flops);
+  if (kind == 3) return launch_peak<3>(iters, num_sms, err, timeout_ns, st, flops);
+  if (kind == 4) return launch_peak<4>(iters, num_sms, err, timeout_ns, st, flops);
   return cudaErrorInvalidValue;
 }
 

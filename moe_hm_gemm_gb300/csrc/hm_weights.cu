@@ -49,32 +49,47 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 
 // ------------------------------------------------------------------ quantization (standard format)
 
-// INT4, one warp per (row, group of 128); lane holds 4 consecutive K.
+// INT4 with a bf16 scale per group of `group` along K (32, 64, or a multiple of 128): one warp per
+// (row, group of max(group, 128) K); lane holds 4 consecutive K of each 128-K chunk. A group of 32
+// or 64 is the amax over its 8 or 16 lanes; a group of 128 j takes the amax over its j chunks
+// first, then quantizes them.
 __global__ void quant_int4_kernel(const float* __restrict__ w, const uint8_t* __restrict__ zeros,
-                                  int64_t n, int64_t k, int has_zero, uint8_t* __restrict__ q,
+                                  int64_t n, int64_t k, int has_zero, int64_t group, uint8_t* __restrict__ q,
                                   __nv_bfloat16* __restrict__ scales) {
-  const int64_t groups = k / 128;
+  const int64_t span = group < 128 ? 128 : group;        // K per warp
+  const int64_t spans = k / span;
   const int64_t gid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gid >= n * groups) return;
-  const int64_t row = gid / groups, g = gid % groups;
-  const float4 v = *reinterpret_cast<const float4*>(w + row * k + g * 128 + 4 * lane);
-  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-  amax = warp_max(amax, 32);
+  if (gid >= n * spans) return;
+  const int64_t row = gid / spans, sp = gid % spans;
+  const int64_t groups = k / group;
+  const int width = group < 128 ? static_cast<int>(group / 4) : 32;   // lanes per group within a chunk
+  float amax = 0.f;
+  for (int64_t c = 0; c < span / 128; ++c) {
+    const float4 v = *reinterpret_cast<const float4*>(w + row * k + sp * span + c * 128 + 4 * lane);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = warp_max(amax, width);
   const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(amax, 7.0f));
   const float s = __bfloat162float(sb);
-  const int z = has_zero ? zeros[row * groups + g] : 0;
-  const float x[4] = {v.x, v.y, v.z, v.w};
-  uint32_t nib[4];
+  // the group of this lane's values (the same for every chunk of a wide group)
+  const int64_t gi = group < 128 ? (sp * 128 + 4 * lane) / group : sp;
+  const int z = has_zero ? zeros[row * groups + gi] : 0;
+  for (int64_t c = 0; c < span / 128; ++c) {
+    const int64_t k0 = sp * span + c * 128;
+    const float4 v = *reinterpret_cast<const float4*>(w + row * k + k0 + 4 * lane);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    uint32_t nib[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = s == 0.f ? 0 : __float2int_rn(rintf(__fdiv_rn(x[i], s)));
-    const int qi = has_zero ? min(max(r + z, 0), 15) : min(max(r, -8), 7);
-    nib[i] = static_cast<uint32_t>(qi) & 0xFu;
+    for (int i = 0; i < 4; ++i) {
+      const int r = s == 0.f ? 0 : __float2int_rn(rintf(__fdiv_rn(x[i], s)));
+      const int qi = has_zero ? min(max(r + z, 0), 15) : min(max(r, -8), 7);
+      nib[i] = static_cast<uint32_t>(qi) & 0xFu;
+    }
+    const uint16_t packed = static_cast<uint16_t>(nib[0] | (nib[1] << 4) | (nib[2] << 8) | (nib[3] << 12));
+    *reinterpret_cast<uint16_t*>(q + row * (k / 2) + k0 / 2 + 2 * lane) = packed;
   }
-  const uint16_t packed = static_cast<uint16_t>(nib[0] | (nib[1] << 4) | (nib[2] << 8) | (nib[3] << 12));
-  *reinterpret_cast<uint16_t*>(q + row * (k / 2) + g * 64 + 2 * lane) = packed;
-  if (lane == 0) scales[row * groups + g] = sb;
+  if ((4 * lane) % (group < 128 ? group : 128) == 0) scales[row * groups + gi] = sb;
 }
 
 // MXFP4, one warp per (row, 128 K); 8 lanes per 32-block.
@@ -223,9 +238,18 @@ __device__ __forceinline__ uint32_t interleave_word(uint32_t s) {
   return lo | (hi << 16);
 }
 
-// One block (128 threads, thread = row) per 128x128 unit.
-__global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, int64_t k,
-                                       const uint8_t* __restrict__ q, const void* __restrict__ scales,
+// Zero-point as the packed weight holds it, from the standard-format value in `conv` (0: z itself;
+// 1: (z - 1) mod 16, GPTQ-style).
+__device__ __forceinline__ uint32_t zero_point(uint8_t stored, int32_t conv) {
+  const uint32_t v = stored & 0xFu;
+  return conv == 1 ? ((v + 1u) & 0xFu) : v;
+}
+
+// One block (128 threads, thread = row) per 128x128 unit. INT4 scales (and zero-points) come in
+// groups of `group` along K: a group of 128 j gives every unit of its j k-blocks its scale; groups
+// of 32 / 64 (format 6) give each 32-K chunk of a unit its own.
+__global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, int64_t group,
+                                       int32_t zconv, const uint8_t* __restrict__ q, const void* __restrict__ scales,
                                        const uint8_t* __restrict__ zeros, uint8_t* __restrict__ packed) {
   const int64_t kbt = k / 128;
   const int64_t nt = blockIdx.x / kbt, kb = blockIdx.x % kbt;
@@ -236,7 +260,8 @@ __global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n,
   if (blockIdx.x == 0 && threadIdx.x < 64) write_header(packed, fmt, n, k, has_zero, 1.0f);
   const bool valid = row < n;
   // signed nibbles (INT4 without zero-points, MXINT4) are stored as q + 8 = q ^ 8
-  const uint32_t flip = ((fmt == kW4A16Int4 && !has_zero) || fmt == kW4A16MxInt) ? 0x88888888u : 0u;
+  const bool int4 = fmt == kW4A16Int4 || fmt == kW4A16Int4G;
+  const uint32_t flip = ((int4 && !has_zero) || fmt == kW4A16MxInt) ? 0x88888888u : 0u;
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
     uint4 src = make_uint4(0, 0, 0, 0);
@@ -252,12 +277,30 @@ __global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n,
     uint32_t e4 = 0;
     if (valid) e4 = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(scales) + row * (k / 32) + kb * 4);
     *reinterpret_cast<uint32_t*>(unit + kUnitCodes + 4 * r) = e4;
+  } else if (fmt == kW4A16Int4G) {
+    const int64_t groups = k / group;
+    uint16_t sb[4] = {0, 0, 0, 0};
+    uint32_t z[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int64_t gi = (kb * 128 + 32 * c) / group;
+      if (valid) {
+        sb[c] = reinterpret_cast<const uint16_t*>(scales)[row * groups + gi];
+        if (has_zero) z[c] = zero_point(zeros[row * groups + gi], zconv);
+      }
+    }
+    *reinterpret_cast<uint2*>(unit + kUnitCodes + 8 * r) =
+        make_uint2(sb[0] | (static_cast<uint32_t>(sb[1]) << 16), sb[2] | (static_cast<uint32_t>(sb[3]) << 16));
+    if (has_zero)
+      *reinterpret_cast<uint16_t*>(unit + kUnitG32 + 2 * r) =
+          static_cast<uint16_t>(z[0] | (z[1] << 4) | (z[2] << 8) | (z[3] << 12));
   } else {
+    const int64_t groups = k / group, gi = (kb * 128) / group;
     uint16_t sb = 0;
-    if (valid) sb = reinterpret_cast<const uint16_t*>(scales)[row * kbt + kb];
+    if (valid) sb = reinterpret_cast<const uint16_t*>(scales)[row * groups + gi];
     *reinterpret_cast<uint16_t*>(unit + kUnitCodes + 2 * r) = sb;
     if (has_zero) {
-      uint32_t z = valid ? (zeros[row * kbt + kb] & 0xFu) : 0u;
+      uint32_t z = valid ? zero_point(zeros[row * groups + gi], zconv) : 0u;
       const uint32_t z_next = __shfl_down_sync(0xffffffffu, z, 1);
       if ((r & 1) == 0) unit[kUnitInt4 + r / 2] = static_cast<uint8_t>(z | (z_next << 4));
     }
@@ -311,8 +354,13 @@ __global__ void dequant_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, i
   const uint8_t* unit = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * ub;
   __nv_bfloat162 zz = int4_zero_pair(8), ss = bf16_pair(0);
   uint32_t e4 = 0;
+  uint2 s4 = make_uint2(0u, 0u);   // format 6: bf16 scales of the four 32-K chunks
+  uint32_t z4 = 0x8888u;           // format 6: their zero-points
   if (e8_unit_fmt(fmt)) {
     e4 = *reinterpret_cast<const uint32_t*>(unit + kUnitCodes + 4 * r);
+  } else if (fmt == kW4A16Int4G) {
+    s4 = *reinterpret_cast<const uint2*>(unit + kUnitCodes + 8 * r);
+    if (has_zero) z4 = *reinterpret_cast<const uint16_t*>(unit + kUnitG32 + 2 * r);
   } else {
     ss = bf16_pair(*reinterpret_cast<const uint16_t*>(unit + kUnitCodes + 2 * r));
     if (has_zero) zz = int4_zero_pair((unit[kUnitInt4 + r / 2] >> (4 * (r & 1))) & 0xFu);
@@ -323,6 +371,11 @@ __global__ void dequant_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, i
     const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
     const float scale = pow2f(static_cast<int>(ex) - 127);
     const __nv_bfloat162 si = bits_bf16x2(mxint_scale_pair(ex));
+    if (fmt == kW4A16Int4G) {
+      const uint32_t sw = c4 < 2 ? s4.x : s4.y;
+      ss = bf16_pair(static_cast<uint16_t>(sw >> (16 * (c4 & 1))));
+      zz = int4_zero_pair((z4 >> (4 * c4)) & 0xFu);
+    }
     for (int j = 0; j < 4; ++j) {
       uint32_t o[4];
       if (fmt == kW4A16Mx) dq_mx_word(words[j], lut, scale, o);
@@ -363,12 +416,13 @@ inline unsigned blocks_for(int64_t threads, int per_block) {
 
 }  // namespace
 
-cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, const float* w,
-                                   const uint8_t* zeros_in, uint8_t* q_out, void* scales_out,
+cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, int64_t group,
+                                   const float* w, const uint8_t* zeros_in, uint8_t* q_out, void* scales_out,
                                    float* g_out, float* ws, cudaStream_t st) {
-  if (fmt == kW4A16Int4) {
-    quant_int4_kernel<<<blocks_for(n * (k / 128) * 32, 256), 256, 0, st>>>(
-        w, zeros_in, n, k, has_zero, q_out, static_cast<__nv_bfloat16*>(scales_out));
+  if (fmt == kW4A16Int4 || fmt == kW4A16Int4G) {
+    const int64_t span = group < 128 ? 128 : group;
+    quant_int4_kernel<<<blocks_for(n * (k / span) * 32, 256), 256, 0, st>>>(
+        w, zeros_in, n, k, has_zero, group, q_out, static_cast<__nv_bfloat16*>(scales_out));
   } else if (fmt == kW4A16Mx || fmt == kW4A8Mx) {
     quant_mx_kernel<<<blocks_for(n * (k / 128) * 32, 256), 256, 0, st>>>(
         w, n, k, q_out, static_cast<uint8_t*>(scales_out));
@@ -385,13 +439,13 @@ cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int
 
 size_t quantize_ws_floats() { return kAmaxBlocks; }
 
-cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, float gw,
-                             const uint8_t* q, const void* scales, const uint8_t* zeros, uint8_t* packed,
-                             cudaStream_t st) {
+cudaError_t launch_transform(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, float gw, int64_t group,
+                             int32_t zconv, const uint8_t* q, const void* scales, const uint8_t* zeros,
+                             uint8_t* packed, cudaStream_t st) {
   const int64_t n_pad = (n + 127) / 128 * 128;
   if (unit_fmt(fmt)) {
     transform_units_kernel<<<static_cast<unsigned>((n_pad / 128) * (k / 128)), 128, 0, st>>>(
-        fmt, has_zero, n, k, q, scales, zeros, packed);
+        fmt, has_zero, n, k, group, zconv, q, scales, zeros, packed);
     return cudaGetLastError();
   }
   const int64_t k_pad = fmt == kW4A4Nv ? (k + 255) / 256 * 256 : k;

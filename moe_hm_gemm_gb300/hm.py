@@ -13,9 +13,11 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libhm.so")
 
-W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4, W4A16_MXINT4 = 1, 2, 3, 4, 5
+W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4, W4A16_MXINT4, W4A16_INT4_G32 = 1, 2, 3, 4, 5, 6
 FORMATS = {"w4a16_int4": W4A16_INT4, "w4a16_mxfp4": W4A16_MXFP4,
-           "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4, "w4a16_mxint4": W4A16_MXINT4}
+           "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4, "w4a16_mxint4": W4A16_MXINT4,
+           "w4a16_int4_g32": W4A16_INT4_G32}
+ZP_INT, ZP_GPTQ = 0, 1
 
 
 class HmError(RuntimeError):
@@ -26,7 +28,8 @@ class HmError(RuntimeError):
 
 class WeightDesc(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("has_zero", ctypes.c_int32), ("N", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("tensor_scale", ctypes.c_float)]
+                ("K", ctypes.c_int64), ("tensor_scale", ctypes.c_float), ("group", ctypes.c_int32),
+                ("zero_convention", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -56,6 +59,8 @@ def _load():
         "hm_workspace_size": (SZ, [I32, I64, I64, I64]),
         "hm_gemm": (I32, [I32, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "hm_moe_gemm": (I32, [I32, P, P, I32, P, P, I64, I64, I64, P, SZ, P]),
+        "hm_moe_workspace_size": (SZ, [I32, I64, I32, I64, I64]),
+        "hm_moe_gemm_strided": (I32, [I32, P, P, P, I32, P, I64, P, I64, I64, I64, P, SZ, P]),
         "hm_gemm_w4a16_noalloc": (I32, [I32, P, P, P, I64, I64, I64, P]),
         "hm_plan": (I32, [I32, I64, I64, I64, I32, ctypes.POINTER(PlanInfo)]),
         "hm_get_device_error": (ctypes.c_uint32, [P]),
@@ -109,8 +114,18 @@ def _check(status, where):
         raise HmError(status, where)
 
 
-def desc(fmt, n, k, has_zero=False, tensor_scale=1.0):
-    return WeightDesc(int(fmt), int(bool(has_zero)), int(n), int(k), float(tensor_scale))
+def desc(fmt, n, k, has_zero=False, tensor_scale=1.0, group=0, zero_convention=ZP_INT):
+    return WeightDesc(int(fmt), int(bool(has_zero)), int(n), int(k), float(tensor_scale), int(group),
+                      int(zero_convention))
+
+
+def group_of(d):
+    """K values per scale of a description (its `group`, or the format's own for 0; -1 = K)."""
+    if d.group == -1:
+        return d.K
+    if d.group:
+        return d.group
+    return {W4A16_INT4: 128, W4A16_INT4_G32: 32, W4A4_NVFP4: 16}.get(d.fmt, 32)
 
 
 def packed_size(d):
@@ -124,8 +139,8 @@ def quantize_weight(d, w, zeros=None):
         raise ValueError("w: expected float32")
     dev = w.device
     q = torch.empty((d.N, d.K // 2), dtype=torch.uint8, device=dev)
-    if d.fmt == W4A16_INT4:
-        scales = torch.empty((d.N, d.K // 128), dtype=torch.bfloat16, device=dev)
+    if d.fmt in (W4A16_INT4, W4A16_INT4_G32):
+        scales = torch.empty((d.N, d.K // group_of(d)), dtype=torch.bfloat16, device=dev)
     elif d.fmt in (W4A16_MXFP4, W4A8_MXFP4, W4A16_MXINT4):
         scales = torch.empty((d.N, d.K // 32), dtype=torch.uint8, device=dev)
     else:
@@ -262,6 +277,37 @@ def gemm_noalloc(fmt, x, packed, n, k, out=None):
     y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (m, n))
     _check(_lib.hm_gemm_w4a16_noalloc(int(fmt), _ptr(x), _ptr(packed), _ptr(y), m, n, k, _stream()),
            "hm_gemm_w4a16_noalloc")
+    return y
+
+
+def moe_stride(d):
+    """Bytes between experts in a strided MoE weight buffer: the packed size rounded up to 256."""
+    return (packed_size(d) + 255) // 256 * 256
+
+
+def alloc_moe_packed(d, experts, device="cuda"):
+    """One buffer for `experts` packed weights of description d at moe_stride(d)."""
+    return torch.empty((experts * moe_stride(d),), dtype=torch.uint8, device=device)
+
+
+def moe_expert_view(buf, d, e):
+    """Expert e's slot of a strided MoE weight buffer (to pass to transform(out=...))."""
+    st = moe_stride(d)
+    return buf[e * st:e * st + packed_size(d)]
+
+
+def moe_gemm_strided(fmt, x, offsets, packed, experts, stride, n, k, x_scale=None, out=None, ws=None):
+    """Grouped GEMM with the experts at packed + e * stride (hm_moe_gemm_strided). x: expert-sorted
+    rows (bf16, or e4m3 bytes with x_scale for W4A8); offsets int32 [E+1] (device)."""
+    _dev(("x", x), ("offsets", offsets), ("packed", packed), ("x_scale", x_scale), ("ws", ws))
+    rows = x.shape[0]
+    y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (rows, n))
+    if ws is None:
+        need = _lib.hm_moe_workspace_size(int(fmt), rows, int(experts), n, k)
+        ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=x.device)
+    _check(_lib.hm_moe_gemm_strided(int(fmt), _ptr(x), _ptr(x_scale), _ptr(offsets), int(experts), _ptr(packed),
+                                    int(stride), _ptr(y), rows, n, k, _ptr(ws), ws.numel(), _stream()),
+           "hm_moe_gemm_strided")
     return y
 
 

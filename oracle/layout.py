@@ -133,11 +133,16 @@ def _pack_units(fmt, nibbles, scale_bytes_fn, zeros, n, k, has_zero):
     return out.reshape(-1)
 
 
-def pack_w4a16_int4(q, s, zeros=None):
-    """q int [N,K] (signed without zero-points, unsigned with), s bf16 values [N,K/128],
-    zeros ints [N,K/128] or None. Returns the packed buffer (uint8)."""
+def pack_w4a16_int4(q, s, zeros=None, group=128):
+    """q int [N,K] (signed without zero-points, unsigned with), s bf16 values [N,K/group],
+    zeros ints [N,K/group] or None, group a multiple of 128 dividing K (a group of 128 j gives each
+    of its j units its scale and zero-point). Returns the packed buffer (uint8)."""
     q = np.asarray(q)
     n, k = q.shape
+    rep = group // 128
+    s = np.repeat(np.asarray(s), rep, axis=1)
+    if zeros is not None:
+        zeros = np.repeat(np.asarray(zeros), rep, axis=1)
     has_zero = zeros is not None
     n_pad, k_pad = padded_dims(FMT_W4A16_INT4, n, k)
     nib = np.zeros((n_pad, k_pad), dtype=np.int64)

@@ -108,6 +108,21 @@ def dequant_int4(q, s, zeros=None, group=GROUP_INT4):
     return bf16r(int4_restore(q, s_full, z_full))
 
 
+# ------------------------------------------------------------------ zero-point conventions
+
+def gptq_stored_zero(z):
+    """The value a GPTQ-style checkpoint stores for the u4 zero-point z: z - 1, kept in four bits
+    (so z = 0 is stored as 15). Reading taken for "zero-points from different quantization tools"
+    (aihaber.org, section "Mimari"): such tools keep z - 1 and add the 1 back when restoring."""
+    return (np.asarray(z, dtype=np.int64) - 1) % 16
+
+
+def zero_from_gptq(stored):
+    """The zero-point z of a GPTQ-style stored value: stored + 1, modulo 16 (inverse of
+    gptq_stored_zero for every z in [0, 15])."""
+    return (np.asarray(stored, dtype=np.int64) + 1) % 16
+
+
 # ------------------------------------------------------------------ MXFP4 (e2m1 + E8M0 / 32)
 
 def mx_scale_codes(w, group=GROUP_MX):

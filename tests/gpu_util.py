@@ -22,17 +22,26 @@ def to_bf16(values):
 class QuantWeight:
     """A weight quantized by the oracle, with its standard-format tensors."""
 
-    def __init__(self, fmt, w, zeros=None):
+    def __init__(self, fmt, w, zeros=None, group=0):
         self.fmt = fmt
         self.n, self.k = w.shape
         self.zeros = zeros
         self.g = 1.0
+        self.group = group
         if fmt == ol.FMT_W4A16_INT4:
-            self.q, self.s = oq.quant_int4(w, zeros=zeros)
-            self.what = oq.dequant_int4(self.q, self.s, zeros)
+            grp = self.k if group == -1 else (group or 128)
+            self.q, self.s = oq.quant_int4(w, zeros=zeros, group=grp)
+            self.what = oq.dequant_int4(self.q, self.s, zeros, group=grp)
             self.std_q = pack_nibbles(self.q)
             self.std_s = to_bf16(self.s)
-            self.packed_ref = ol.pack_w4a16_int4(self.q, self.s, zeros)
+            self.packed_ref = ol.pack_w4a16_int4(self.q, self.s, zeros, group=grp)
+        elif fmt == ol.FMT_W4A16_INT4_G32:
+            grp = group or 32
+            self.q, self.s = oq.quant_int4(w, zeros=zeros, group=grp)
+            self.what = oq.dequant_int4(self.q, self.s, zeros, group=grp)
+            self.std_q = pack_nibbles(self.q)
+            self.std_s = to_bf16(self.s)
+            self.packed_ref = ol.pack_w4a16_int4_g32(self.q, self.s, zeros, group=grp)
         elif fmt in (ol.FMT_W4A16_MXFP4, ol.FMT_W4A8_MXFP4):
             self.q, self.s = oq.quant_mxfp4(w)
             self.what = oq.dequant_mxfp4(self.q, self.s)
@@ -57,8 +66,12 @@ class QuantWeight:
         z = None if self.zeros is None else torch.from_numpy(np.asarray(self.zeros, np.uint8)).cuda()
         return torch.from_numpy(self.std_q).cuda(), self.std_s.cuda(), z
 
+    def desc(self, hm, zero_convention=0):
+        return hm.desc(self.fmt, self.n, self.k, self.zeros is not None, self.g, group=self.group,
+                       zero_convention=zero_convention)
+
     def transform(self, hm):
-        d = hm.desc(self.fmt, self.n, self.k, self.zeros is not None, self.g)
+        d = self.desc(hm)
         q, s, z = self.device_inputs()
         return d, hm.transform(d, q, s, z)
 

@@ -46,8 +46,22 @@ def test_packed_size_rejects_bad_shapes(hm):
     assert hm.packed_size(hm.desc(2, 128, 128, True)) == 0  # zero-points only for INT4
     assert hm.packed_size(hm.desc(5, 128, 128, True)) == 0
     assert hm.packed_size(hm.desc(5, 128, 64)) == 0       # MXINT4 K % 128
-    assert hm.packed_size(hm.desc(6, 128, 128)) == 0
+    assert hm.packed_size(hm.desc(7, 128, 128)) == 0
     assert hm.packed_size(hm.desc(9, 128, 128)) == 0
+    # group sizes: INT4 takes multiples of 128 dividing K (or -1 per channel), format 6 takes 32 / 64
+    assert hm.packed_size(hm.desc(1, 128, 512, group=256)) == L.packed_size(1, 128, 512, False)
+    assert hm.packed_size(hm.desc(1, 128, 512, group=-1)) == L.packed_size(1, 128, 512, False)
+    assert hm.packed_size(hm.desc(1, 128, 512, group=384)) == 0      # does not divide K
+    assert hm.packed_size(hm.desc(1, 128, 512, group=64)) == 0       # below 128: format 6
+    assert hm.packed_size(hm.desc(6, 128, 512, group=64)) == L.packed_size(6, 128, 512, False)
+    assert hm.packed_size(hm.desc(6, 128, 512, True, group=32)) == L.packed_size(6, 128, 512, True)
+    assert hm.packed_size(hm.desc(6, 128, 512, group=128)) == 0
+    assert hm.packed_size(hm.desc(2, 128, 512, group=64)) == 0       # MX groups are 32
+    # the GPTQ zero-point convention needs zero-points of an INT4 format
+    assert hm.packed_size(hm.desc(1, 128, 512, True, zero_convention=1)) == L.packed_size(1, 128, 512, True)
+    assert hm.packed_size(hm.desc(1, 128, 512, False, zero_convention=1)) == 0
+    assert hm.packed_size(hm.desc(5, 128, 512, False, zero_convention=1)) == 0
+    assert hm.packed_size(hm.desc(1, 128, 512, True, zero_convention=2)) == 0
     assert hm.packed_size(hm.desc(1, 0, 128)) == 0
 
 
@@ -354,6 +368,28 @@ def test_moe_gather_combine_argument_checks(hm):
 def test_mma_peak_probe_argument_checks(hm):
     lib = hm.lib()
     fl = ctypes.c_double(0.0)
-    assert lib.hm_mma_peak_probe(3, 10, ctypes.byref(fl), None) == 1
+    assert lib.hm_mma_peak_probe(5, 10, ctypes.byref(fl), None) == 1
     assert lib.hm_mma_peak_probe(0, 0, ctypes.byref(fl), None) == 1
     assert lib.hm_mma_peak_probe(0, 10, None, None) == 1
+
+
+def test_moe_strided_argument_checks(hm):
+    lib = hm.lib()
+    P = ctypes.c_void_p
+    st = hm.moe_stride(hm.desc(3, 256, 512))
+    # stride not a multiple of 256, or smaller than one packed weight
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 2, P(256), st + 16, P(256), 8, 256, 512, None, 0, None) == 1
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 2, P(256), 256, P(256), 8, 256, 512, None, 0, None) == 1
+    # misaligned packed buffer, zero experts
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 2, P(272), st, P(256), 8, 256, 512, None, 0, None) == 1
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 0, P(256), st, P(256), 8, 256, 512, None, 0, None) == 1
+    # W4A4 takes bf16 activations only; too many experts for the block-scaled kernel
+    st4 = hm.moe_stride(hm.desc(4, 256, 512))
+    assert lib.hm_moe_gemm_strided(4, P(256), P(256), P(256), 2, P(256), st4, P(256), 8, 256, 512, None, 0, None) == 2
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 300, P(256), st, P(256), 8, 256, 512, None, 0, None) == 2
+    # internal activation quantization needs the workspace
+    assert lib.hm_moe_workspace_size(3, 8, 2, 256, 512) >= 8 * 512 + 8 * 4
+    assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 2, P(256), st, P(256), 8, 256, 512, None, 0, None) == 3
+    assert lib.hm_moe_workspace_size(1, 8, 2, 256, 512) == 0
+    # rows = 0 is a no-op
+    assert lib.hm_moe_gemm_strided(3, None, None, None, 2, None, st, None, 0, 256, 512, None, 0, None) == 0

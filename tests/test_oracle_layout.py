@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 from oracle import layout as L
+from oracle import formats as F
 from oracle import quant as Q
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "int4_worked_example.json")
@@ -165,3 +166,24 @@ def test_int4_g32_units(group, has_zero):
     if has_zero:
         zn = (int(unit[9216 + 2 * rr + c // 2]) >> (4 * (c % 2))) & 0xF
         assert zn == z[row, kk // group]
+
+
+@pytest.mark.parametrize("group", [256, 512])
+def test_int4_wide_group_units_carry_their_group_scale(group):
+    """A group of 128 j along K fills j consecutive units: unit (t, b) holds the bf16 scale and
+    zero-point of group (b * 128) // group for every row, at the INT4 unit offsets."""
+    rng = np.random.default_rng(3)
+    n, k = 130, 1024
+    w = rng.standard_normal((n, k)).astype(np.float32)
+    z = rng.integers(0, 16, size=(n, k // group))
+    q, s = Q.quant_int4(w, zeros=z, group=group)
+    buf = L.pack_w4a16_int4(q, s, z, group=group)
+    assert len(buf) == L.packed_size(1, n, k, True)
+    kb = k // 128
+    for row, b in [(0, 0), (129, kb - 1), (77, 3), (5, 1)]:
+        unit = 256 + ((row // 128) * kb + b) * 8512
+        r = row % 128
+        sb = int(buf[unit + 8192 + 2 * r]) | (int(buf[unit + 8192 + 2 * r + 1]) << 8)
+        assert sb == int(F.bf16_bits(s[row, (b * 128) // group]))
+        zn = (int(buf[unit + 8448 + r // 2]) >> (4 * (r % 2))) & 0xF
+        assert zn == z[row, (b * 128) // group]

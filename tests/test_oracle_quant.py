@@ -297,3 +297,28 @@ def test_nvfp4_hand_computed_tensor_scale_not_one():
     # restored values: e2m1 * sb * g
     back = Q.dequant_nvfp4(codes, sb, g)
     assert back[0, 18] == 1.5 * 1.75 * g and back[0, 49] == -6.0 * 1.125 * g
+
+
+def test_gptq_zero_convention():
+    # symmetric 4-bit quantization has z = 8, which GPTQ-style checkpoints store as 7; z = 0 wraps to
+    # 15; every z in [0, 15] comes back from its stored value
+    assert int(Q.gptq_stored_zero(8)) == 7 and int(Q.gptq_stored_zero(0)) == 15 and int(Q.gptq_stored_zero(15)) == 14
+    z = np.arange(16)
+    np.testing.assert_array_equal(Q.zero_from_gptq(Q.gptq_stored_zero(z)), z)
+    assert sorted(Q.gptq_stored_zero(z).tolist()) == list(range(16))     # a bijection on four bits
+
+
+def test_int4_wide_groups_and_per_channel():
+    # a group of 256 is one scale over two 128-blocks: s = bf16(max|w| / 7) over all 256 values
+    rng = np.random.default_rng(12)
+    w = rng.standard_normal((3, 512)).astype(np.float32)
+    w[1, 300] = 9.0                                     # the second group of row 1
+    q, s = Q.quant_int4(w, group=256)
+    assert s.shape == (3, 2)
+    assert s[1, 1] == F.bf16r(np.float32(9.0) / np.float32(7.0)) and q[1, 300] == 7
+    # per channel: one scale per row
+    q1, s1 = Q.quant_int4(w, group=512)
+    assert s1.shape == (3, 1) and s1[1, 0] == s[1, 1]
+    back = Q.dequant_int4(q1, s1, group=512)
+    # half a step of the row's scale, plus the bf16 rounding of the restored value
+    assert np.all(np.abs(back - w) <= np.repeat(s1, 512, axis=1) * 0.5 + 2.0 ** -8 * np.abs(w) + 1e-6)
