@@ -510,10 +510,32 @@ def summarize(points, pk, workload, hm, local_rank):
     return sweep, roofline
 
 
+KIND_PROBES = {"kind::f16": (0,), "kind::mxf8f6f4": (1, 3), "kind::mxf4nvf4": (2, 4)}
+
+
+def live_kind_peaks(hm):
+    """Dense TFLOP/s of each tcgen05 MMA kind on this device, from the library's throughput probe
+    (the larger of its shapes per kind), or None when the probe fails."""
+    try:
+        out = {}
+        for kind, probes in KIND_PROBES.items():
+            out[kind] = round(max(hm.mma_peak(k, 20000 if k != 2 else 40000, repeats=3)[0] for k in probes), 1)
+        if hm.device_error() != 0:
+            return None
+        return out
+    except Exception:   # noqa: BLE001 - fall back to the recorded peaks
+        return None
+
+
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     from moe_hm_gemm_gb300 import hm, synth
     pk = peaks()
+    if not args.no_peak_probe:
+        live = live_kind_peaks(hm)
+        if live is not None:
+            pk["kinds"] = live
+            pk["kinds_note"] = "measured in this run by hm_mma_peak_probe"
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         points = build_points(args, hm, synth)
@@ -733,6 +755,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads the default run reports under 'configs'")
     ap.add_argument("--extra-steps", type=int, default=5)
+    ap.add_argument("--no-peak-probe", action="store_true",
+                    help="take the MMA-kind peaks from profiles/tcgen05_peaks.json instead of measuring them")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

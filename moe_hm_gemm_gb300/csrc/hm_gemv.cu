@@ -136,9 +136,9 @@ __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uin
 }
 
 // Cluster-scope helpers for the hand-off of a shared tile between the CTAs of one cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// Split cluster barrier (per thread, not warp-aligned, so a warp may reach it from any branch).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
@@ -251,8 +251,14 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   }
   if (WK == 2 && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
   __syncthreads();
-  // the owner's barriers must be initialised before another CTA of its cluster arrives on them
-  if (csize > 1) cluster_sync_all();
+  // Cluster barrier, two phases, each split into an arrive and a wait per thread: phase 1 makes the
+  // owner's barriers initialised before another CTA of its cluster arrives on them (every thread
+  // arrives here, a publishing warp waits just before its first remote access, the others at
+  // exit); phase 2 keeps every CTA alive until no other one may still write into its shared
+  // memory (a thread arrives once it has no remote access left: a publisher after its stores, the
+  // owner's readers once the publications they wait for have landed, the other roles at exit).
+  bool cl_waited1 = false, cl_arrived2 = false;
+  if (csize > 1) cluster_arrive();
   if (threadIdx.x == 0) {
     pdl_launch_dependents();
     trace_mark(p.trace, 1);
@@ -429,6 +435,10 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
         // barrier; rank 0 adds them in rank order (deterministic) and writes Y. One use per launch.
         constexpr int F = S::kXchgFloats;
         const uint32_t rank = blockIdx.x % static_cast<uint32_t>(csize);
+        if (!cl_waited1) {
+          cluster_wait();
+          cl_waited1 = true;
+        }
         if (rank != 0) {
           const uint32_t dst = map_to_rank(smem_u32(red + ((static_cast<size_t>(rank - 1) * 4 + pr) * 32 + lane) * F), 0);
 #pragma unroll
@@ -438,9 +448,13 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
               st_cluster_v4(dst + ((j * NQ + q) * 4) * 4, v[j][q][0], v[j][q][1], v[j][q][2], v[j][q][3]);
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&red_full[pr]), 0));
+          cluster_arrive();
+          cl_arrived2 = true;
           return true;
         }
         if (!mbar_wait_cluster(&red_full[pr], 0u, wc)) return false;
+        cluster_arrive();
+        cl_arrived2 = true;
         for (int r = 1; r < csize; ++r) {
           const float* src = red + ((static_cast<size_t>(r - 1) * 4 + pr) * 32 + lane) * F;
 #pragma unroll
@@ -670,10 +684,14 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     }
   }
   if (lane == 0) trace_stage(p.trace, 0, warp);   // (diagnostics: when each warp finished its role)
+  // no CTA leaves while another of its cluster may still write into its shared memory
+  if (csize > 1) {
+    if (!cl_waited1) cluster_wait();
+    if (!cl_arrived2) cluster_arrive();
+    cluster_wait();
+  }
   __syncwarp();
   __syncthreads();
-  // no CTA leaves while another of its cluster may still write into its shared memory
-  if (csize > 1) cluster_sync_all();
   if (threadIdx.x == 0) trace_mark(p.trace, 12);
 }
 
