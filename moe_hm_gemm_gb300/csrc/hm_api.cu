@@ -204,7 +204,7 @@ F16Choice f16_choice(int64_t m, int64_t n, int64_t k, int num_sms) {
 int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
-  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !block_scaled)) {
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || ((forced == 192 || forced == 256) && !block_scaled)) {
     if (fmt == kW4A4Nv && forced < 128 && m > forced) return 128;
     return forced;
   }

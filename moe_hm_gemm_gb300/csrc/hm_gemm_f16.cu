@@ -22,6 +22,7 @@ int f16_stages(int fmt, int tile_m) {
       case 32: return F16Shape<32, kUnitG32Zp>::kSL;
       case 64: return F16Shape<64, kUnitG32Zp>::kSL;
       case 128: return F16Shape<128, kUnitG32Zp>::kSL;
+      case 192: return F16Shape<192, kUnitG32Zp>::kSL;
       default: return F16Shape<256, kUnitG32Zp>::kSL;
     }
   }
@@ -30,6 +31,7 @@ int f16_stages(int fmt, int tile_m) {
     case 32: return F16Shape<32>::kSL;
     case 64: return F16Shape<64>::kSL;
     case 128: return F16Shape<128>::kSL;
+    case 192: return F16Shape<192>::kSL;
     default: return F16Shape<256>::kSL;
   }
 }

@@ -59,9 +59,10 @@ constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
 // Two variants of the A (restored weight) path:
-//  * tile_m <= 128: the dequant warps store bf16 A straight into TMEM (tcgen05.st) and the MMA
+//  * tile_m <= 192: the dequant warps store bf16 A straight into TMEM (tcgen05.st) and the MMA
 //    reads A from TMEM, so shared memory carries only the packed weights and X; TMEM holds the
-//    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns;
+//    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns (two at 192
+//    tokens, whose accumulator pair takes 384 of the 512 columns);
 //  * tile_m = 256: the accumulator pair fills TMEM, so A goes through shared memory in the
 //    128-byte-swizzled K-major layout.
 // A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
@@ -74,7 +75,7 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 // adds (issuer 0 first, so the sum is deterministic).
 template <int BT, int UB = kUnitMx>
 struct F16Shape {
-  static constexpr bool kATmem = BT <= 128;
+  static constexpr bool kATmem = BT <= 192;
   static constexpr int kIss = BT <= 64 ? 2 : 1;
   static constexpr int kAccCols = 2 * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
   static constexpr int kG = f16_group_of(BT);
@@ -638,6 +639,9 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
     case 32: return launch_one<32, WK, MOE>(p, st);
     case 64: return launch_one<64, WK, MOE>(p, st);
     case 128: return launch_one<128, WK, MOE>(p, st);
+    case 192:
+      if constexpr (!MOE) return launch_one<192, WK, MOE>(p, st);
+      return cudaErrorInvalidValue;
     case 256: return launch_one<256, WK, MOE>(p, st);
     default: return cudaErrorInvalidValue;
   }

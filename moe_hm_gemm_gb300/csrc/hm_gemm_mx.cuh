@@ -336,56 +336,33 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
         if (!mbar_wait(acc_empty, (acc_i & 1u) ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem;
-        // k-blocks in pairs when the pipeline is ahead: after waiting for a stage, the next one is
-        // taken into the same batch if it has already landed (checked without waiting), since the
-        // issuing thread stalls at its next shared-memory access (a barrier wait) until the MMAs it
-        // just issued are under way; one such stall per two k-blocks instead of one. When the loads
-        // are behind (small M), blocks go one at a time as they land.
-        for (int kb = seg.kb0; kb < seg.kb1;) {
-          int nb = 1;
-          int sl[2] = {ls, 0};
-          {
-            int l2 = ls;
-            uint32_t p2 = ph;
-            if (!mbar_wait(NV ? &sf_full[l2] : &full[l2], p2, wc)) { ok = false; break; }
-            if (++l2 == SL) { l2 = 0; p2 ^= 1u; }
-            if (kb + 1 < seg.kb1 && mbar_try_wait(smem_u32(NV ? &sf_full[l2] : &full[l2]), p2)) {
-              nb = 2;
-              sl[1] = l2;
-            }
-          }
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+          if (!mbar_wait(NV ? &sf_full[ls] : &full[ls], ph, wc)) { ok = false; break; }
           tc_fence_after();
-          for (int b = 0; b < nb; ++b) {
-            const int st = sl[b];
-            const uint32_t w_base = smem_u32(smem + S::kWOff + st * kWTile);
-            const uint32_t x_base = smem_u32(smem + S::kXOff + st * S::kXStage);
-            const bool first_blk = kb + b == seg.kb0;
-            if (NV) {
-              const uint32_t slot = tmem + sf_col0 + st * 32;
-              constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
+          const uint32_t w_base = smem_u32(smem + S::kWOff + ls * kWTile);
+          const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage);
+          if (NV) {
+            const uint32_t slot = tmem + sf_col0 + ls * 32;
+            constexpr uint32_t idesc = idesc_block_scaled(128, BT, 1, 1, 0, 0, 0);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = sdesc_sw128(w_base + k * 32);
-                const uint64_t bd = sdesc_sw128(x_base + k * 32);
-                mma_mxf4nvf4_4x(d, ad, bd, idesc, slot + 4 * k, slot + 16 + 4 * k, (!first_blk || k > 0) ? 1u : 0u);
-              }
-            } else {
-              const uint32_t slot = tmem + sf_col0 + st * 4;
-              tc_cp_32x128b_x4(slot, sdesc_sf(smem_u32(smem + S::kSfaOff + st * S::kSfaBytes)));
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(w_base + k * 32);
+              const uint64_t bd = sdesc_sw128(x_base + k * 32);
+              mma_mxf4nvf4_4x(d, ad, bd, idesc, slot + 4 * k, slot + 16 + 4 * k, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+            const uint32_t slot = tmem + sf_col0 + ls * 4;
+            tc_cp_32x128b_x4(slot, sdesc_sf(smem_u32(smem + S::kSfaOff + ls * S::kSfaBytes)));
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, k, k);
-                const uint64_t ad = sdesc_sw128(w_base + k * 32);
-                const uint64_t bd = sdesc_sw128(x_base + k * 32);
-                mma_mxf8f6f4(d, ad, bd, idesc, slot, unit_sfb, (!first_blk || k > 0) ? 1u : 0u);
-              }
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t idesc = idesc_block_scaled(128, BT, 5, 0, 1, k, k);
+              const uint64_t ad = sdesc_sw128(w_base + k * 32);
+              const uint64_t bd = sdesc_sw128(x_base + k * 32);
+              mma_mxf8f6f4(d, ad, bd, idesc, slot, unit_sfb, (kb > seg.kb0 || k > 0) ? 1u : 0u);
             }
           }
-          for (int b = 0; b < nb; ++b) {
-            tc_commit(&empty[ls]);
-            if (++ls == SL) { ls = 0; ph ^= 1u; }
-          }
-          kb += nb;
+          tc_commit(&empty[ls]);
+          if (++ls == SL) { ls = 0; ph ^= 1u; }
         }
         if (!ok) break;
         tc_commit(acc_full);

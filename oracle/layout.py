@@ -15,7 +15,8 @@ u32 has_zero, f32 tensor_scale, u64 payload_bytes, zeros up to 256 bytes.
 Formats: 1 = W4A16 INT4 (group 128, bf16 scales, optional u4 zero-points),
 2 = W4A16 MXFP4 (e2m1 + E8M0/32, bf16 activations), 3 = W4A8 MXFP4, 4 = W4A4 NVFP4,
 5 = W4A16 MXINT4 (signed int4 + E8M0/32, bf16 activations), 6 = W4A16 INT4 with bf16 scales (and
-optional u4 zero-points) per 32 along K (inputs grouped by 32 or 64).
+optional u4 zero-points) per 32 along K (inputs grouped by 32 or 64), 7 = W8A16 INT8 (8-bit codes,
+bf16 scale per 128, optional u8 zero-point).
 
 Tiled payload (formats 1, 2, 5, 6): one "unit" per (n_tile of 128 rows, k_block of 128),
 n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
@@ -30,6 +31,8 @@ n_tile-major. Inside a unit, row r in 0..127 and kk in 0..127:
   * format 6: nibbles as format 1; bf16 scale of (r, kk//32) at byte 8192 + 8r + 2(kk//32); zero-point
     of (r, kk//32) (if any) at byte 9216 + 2r + (kk//32)//2, bit 4((kk//32)%2); unit = 9216 bytes, or
     9472 with zero-points.
+  * format 7: one byte per code at (kk//16)*2048 + r*16 + kk%16 (stored q + 128 without zero-points);
+    bf16 scale of row r at 16384 + 2r; u8 zero-point at 16640 + r; unit = 16640 bytes, or 16768.
 
 Row-major payload (formats 3, 4): codes as bytes [N_pad][K_pad/2] (even k in the low
 nibble), then scale-factor atoms of 512 bytes, atom (n_tile, kc) n_tile-major, where kc
@@ -57,7 +60,8 @@ MAGIC = 0x31574D48
 HEADER = 256
 FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A8_MXFP4, FMT_W4A4_NVFP4, FMT_W4A16_MXINT4 = 1, 2, 3, 4, 5
 FMT_W4A16_INT4_G32 = 6
-TILED = (FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A16_MXINT4, FMT_W4A16_INT4_G32)
+FMT_W8A16_INT8 = 7
+TILED = (FMT_W4A16_INT4, FMT_W4A16_MXFP4, FMT_W4A16_MXINT4, FMT_W4A16_INT4_G32, FMT_W8A16_INT8)
 TILE_N = 128
 ATOM = 512
 
@@ -78,6 +82,8 @@ def unit_bytes(fmt, has_zero):
         return 8704
     if fmt == FMT_W4A16_INT4_G32:
         return 9472 if has_zero else 9216
+    if fmt == FMT_W8A16_INT8:
+        return 16768 if has_zero else 16640
     raise ValueError(fmt)
 
 
@@ -194,6 +200,46 @@ def pack_w4a16_int4_g32(q, s, zeros=None, group=32):
     pay = _pack_units(FMT_W4A16_INT4_G32, nib, scales, None, n, k, has_zero)
     assert pay.size == (n_pad // 128) * (k_pad // 128) * ub
     return np.concatenate([header(FMT_W4A16_INT4_G32, n, k, has_zero, 1.0), pay])
+
+
+def int8_position(kk):
+    """Byte offset, within a unit's code region for row 0, of column kk of an INT8 unit: 16-column
+    chunks, each chunk 16 contiguous bytes per row, rows 16 bytes apart."""
+    kk = np.asarray(kk)
+    return (kk // 16) * 2048 + kk % 16
+
+
+def pack_w8a16_int8(q, s, zeros=None):
+    """q int [N,K] (signed in [-128, 127] without zero-points, unsigned in [0, 255] with), s bf16
+    values [N,K/128], zeros ints [N,K/128] or None. Units of 128 rows x 128 K: code (r, kk) as a byte
+    at (kk//16)*2048 + r*16 + kk%16 (stored q + 128 without zero-points), the bf16 scale of row r at
+    16384 + 2r, its u8 zero-point (if any) at 16640 + r. Returns the packed buffer (uint8)."""
+    q = np.asarray(q)
+    n, k = q.shape
+    has_zero = zeros is not None
+    n_pad, k_pad = padded_dims(FMT_W8A16_INT8, n, k)
+    codes = np.zeros((n_pad, k_pad), dtype=np.int64)
+    codes[:n, :k] = q if has_zero else q + 128
+    sbits = np.zeros((n_pad, k_pad // 128), dtype=np.uint16)
+    sbits[:n] = bf16_bits(s)
+    z = np.zeros((n_pad, k_pad // 128), dtype=np.int64)
+    if has_zero:
+        z[:n] = zeros
+    ub = unit_bytes(FMT_W8A16_INT8, has_zero)
+    nt, kb = n_pad // 128, k_pad // 128
+    out = np.zeros((nt, kb, ub), dtype=np.uint8)
+    r = np.arange(128)
+    off = r[:, None] * 16 + int8_position(np.arange(128))[None, :]
+    for t in range(nt):
+        for b in range(kb):
+            unit = out[t, b]
+            unit[off.ravel()] = codes[t * 128:(t + 1) * 128, b * 128:(b + 1) * 128].ravel().astype(np.uint8)
+            v = sbits[t * 128:(t + 1) * 128, b]
+            unit[16384 + 2 * r] = v & 0xFF
+            unit[16384 + 2 * r + 1] = v >> 8
+            if has_zero:
+                unit[16640 + r] = z[t * 128:(t + 1) * 128, b]
+    return np.concatenate([header(FMT_W8A16_INT8, n, k, has_zero, 1.0), out.reshape(-1)])
 
 
 def _pack_e8_units(fmt, nibbles, e):

@@ -108,6 +108,35 @@ def dequant_int4(q, s, zeros=None, group=GROUP_INT4):
     return bf16r(int4_restore(q, s_full, z_full))
 
 
+# ------------------------------------------------------------------ INT8 (8-bit integer weights)
+
+def quant_int8(w, zeros=None, group=GROUP_INT4):
+    """The page's INT4 rule with the 8-bit integer range (the news pages list integer weights up to
+    8 bits, section "하나의 라이브러리로 긴 포맷 목록을 포괄"): s = bf16(fp32(max|w_g|) / 127) per
+    group, q = clamp(round(fp32(w / s)), -128, 127), or with an unsigned 8-bit zero-point z,
+    clamp(round(fp32(w / s)) + z, 0, 255). Returns (q int64 [N,K], s float64 [N,K/group])."""
+    w = f32(w)
+    amax = np.abs(_groups(w, group)).max(axis=2)
+    s = bf16r(f32(f32(amax) / 127.0))
+    s_full = np.repeat(s, group, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(f32(w / s_full))
+    r = np.where(s_full == 0, 0.0, r)
+    if zeros is None:
+        return np.clip(r, -128, 127).astype(np.int64), s
+    z_full = np.repeat(np.asarray(zeros, dtype=np.float64), group, axis=1)
+    return np.clip(r + z_full, 0, 255).astype(np.int64), s
+
+
+def dequant_int8(q, s, zeros=None, group=GROUP_INT4):
+    """Restored weight bf16((q - z) * s), float64 [N,K] (one rounding of the exact product)."""
+    s_full = np.repeat(np.asarray(s, dtype=np.float64), group, axis=1)
+    v = np.asarray(q, dtype=np.float64)
+    if zeros is not None:
+        v = v - np.repeat(np.asarray(zeros, dtype=np.float64), group, axis=1)
+    return bf16r(v * s_full)
+
+
 # ------------------------------------------------------------------ zero-point conventions
 
 def gptq_stored_zero(z):

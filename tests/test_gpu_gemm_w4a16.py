@@ -68,12 +68,14 @@ def test_mxfp4_w4a16(hm, m):
     run_case(hm, 2, m, 256, 1024, False, seed=7)
 
 
-@pytest.mark.parametrize("tile_m", ["16", "32", "64", "128", "256"])
+@pytest.mark.parametrize("tile_m", ["16", "32", "64", "128", "192", "256"])
 @pytest.mark.parametrize("stream_k", ["0", "1"])
 def test_forced_configs(hm, env, tile_m, stream_k):
     env["HM_TILE_M"] = tile_m
     env["HM_STREAM_K"] = stream_k
     run_case(hm, 1, 70, 512, 2048, True, seed=9)
+    if tile_m == "192":              # several token tiles, the last one ragged
+        run_case(hm, 1, 450, 384, 1024, True, seed=10)
 
 
 def test_repeated_calls_reuse_workspace(hm):

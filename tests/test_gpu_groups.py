@@ -89,7 +89,7 @@ def test_gemm_matches_oracle(hm, fmt, group, has_zero, m):
     assert hm.device_error() == 0
 
 
-@pytest.mark.parametrize("tile", ["16", "32", "64", "128", "256"])
+@pytest.mark.parametrize("tile", ["16", "32", "64", "128", "192", "256"])
 @pytest.mark.parametrize("stream_k", ["0", "1"])
 def test_g32_every_tcgen05_tile(hm, tile, stream_k, monkeypatch):
     monkeypatch.setenv("HM_GEMV", "0")

@@ -94,7 +94,7 @@ def test_tcgen05_m_sweep(hm, m):
     gemm_case(hm, m, 384, 1024, seed=410)
 
 
-@pytest.mark.parametrize("tile_m", ["16", "32", "64", "128", "256"])
+@pytest.mark.parametrize("tile_m", ["16", "32", "64", "128", "192", "256"])
 @pytest.mark.parametrize("stream_k", ["0", "1"])
 def test_tcgen05_forced_tiles(hm, monkeypatch, tile_m, stream_k):
     monkeypatch.setenv("HM_GEMV", "0")

@@ -187,3 +187,26 @@ def test_int4_wide_group_units_carry_their_group_scale(group):
         assert sb == int(F.bf16_bits(s[row, (b * 128) // group]))
         zn = (int(buf[unit + 8448 + r // 2]) >> (4 * (r % 2))) & 0xF
         assert zn == z[row, (b * 128) // group]
+
+
+@pytest.mark.parametrize("has_zero", [False, True])
+def test_int8_units(has_zero):
+    """Format 7 units: code bytes at (kk // 16) * 2048 + r * 16 + kk % 16 (q + 128 without zero-points),
+    the row's bf16 scale at 16384 + 2r, its zero-point at 16640 + r; a round trip through the offsets."""
+    rng = np.random.default_rng(5)
+    n, k = 130, 256
+    w = rng.standard_normal((n, k)).astype(np.float32)
+    z = rng.integers(0, 256, size=(n, k // 128)) if has_zero else None
+    q, s = Q.quant_int8(w, zeros=z)
+    buf = L.pack_w8a16_int8(q, s, z)
+    assert len(buf) == L.packed_size(7, n, k, has_zero) == 256 + 2 * 2 * (16768 if has_zero else 16640)
+    ub = L.unit_bytes(7, has_zero)
+    for row, kk in [(0, 0), (5, 17), (129, 255), (77, 130), (127, 127)]:
+        unit = 256 + ((row // 128) * (k // 128) + kk // 128) * ub
+        r, c = row % 128, kk % 128
+        code = int(buf[unit + (c // 16) * 2048 + r * 16 + c % 16])
+        assert code == (q[row, kk] if has_zero else q[row, kk] + 128)
+        sb = int(buf[unit + 16384 + 2 * r]) | (int(buf[unit + 16384 + 2 * r + 1]) << 8)
+        assert sb == int(F.bf16_bits(s[row, kk // 128]))
+        if has_zero:
+            assert int(buf[unit + 16640 + r]) == z[row, kk // 128]

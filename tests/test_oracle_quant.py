@@ -322,3 +322,40 @@ def test_int4_wide_groups_and_per_channel():
     back = Q.dequant_int4(q1, s1, group=512)
     # half a step of the row's scale, plus the bf16 rounding of the restored value
     assert np.all(np.abs(back - w) <= np.repeat(s1, 512, axis=1) * 0.5 + 2.0 ** -8 * np.abs(w) + 1e-6)
+
+
+def test_int8_closed_forms():
+    # one group of 128 with max |w| = 1.27: s = bf16(1.27 / 127) = bf16(0.01) = 0.010009765625
+    w = np.zeros((1, 128))
+    w[0, :4] = [1.27, -0.5, 0.005004882812, -1.3]
+    q, s = Q.quant_int8(w)
+    assert s[0, 0] == F.bf16r(np.float32(1.3) / np.float32(127.0))
+    sv = s[0, 0]
+    assert q[0, 3] == -127 and q[0, 0] == int(np.rint(np.float32(1.27) / np.float32(sv)))
+    # range: -128 appears only through clamping, +127 at the group maximum
+    assert q.min() >= -128 and q.max() <= 127
+    # zero-points: q + z, clamped into [0, 255]
+    qz, _ = Q.quant_int8(w, zeros=np.array([[200]]))
+    assert qz[0, 3] == 200 - 127 and qz[0, 0] == min(200 + q[0, 0], 255)
+    back = Q.dequant_int8(qz, s, np.array([[200]]))
+    assert back[0, 1] == F.bf16r((qz[0, 1] - 200) * sv)
+
+
+def test_int8_brute_force():
+    # every code is the integer in range nearest to fp32(w / s), ties to even, by scanning all candidates
+    rng = np.random.default_rng(13)
+    w = (rng.standard_normal((3, 256)) * 0.05).astype(np.float32)
+    z = np.array([[0, 255], [128, 7], [60, 200]])
+    for zeros in (None, z):
+        q, s = Q.quant_int8(w, zeros=zeros)
+        for r in range(3):
+            for c in range(0, 256, 7):
+                sv = float(s[r, c // 128])
+                quot = float(np.float32(np.float32(w[r, c]) / np.float32(sv)))
+                zz = 0 if zeros is None else int(zeros[r, c // 128])
+                lo, hi = (-128, 127) if zeros is None else (0, 255)
+                cands = np.arange(lo, hi + 1)
+                d = np.abs(cands - zz - quot)
+                best = cands[d == d.min()]
+                pick = best[0] if len(best) == 1 else [b for b in best if (b - zz) % 2 == 0][0]
+                assert q[r, c] == pick
