@@ -64,14 +64,20 @@ typedef enum hm_status {
  *                   per group of 32 or 64 along K (desc.group), the small groups other
  *                   quantization tools produce (aihaber.org, section "Mimari": weights from
  *                   different tools are brought into one standard format); restored
- *                   bf16((q - z) * s) with the group's s and z. */
+ *                   bf16((q - z) * s) with the group's s and z.
+ *  HM_W8A16_INT8  : 8-bit integer codes (signed in [-128, 127], or unsigned in [0, 255] with a u8
+ *                   zero-point per group), one bf16 scale per 128 along K, bf16 activations: the
+ *                   explainer page's INT4 rule with the 8-bit range (s = bf16(max|w|/127)), one of
+ *                   the integer widths of the news pages' format list (up to INT8); restored
+ *                   bf16((q - z) * s). */
 typedef enum hm_format {
   HM_W4A16_INT4 = 1,
   HM_W4A16_MXFP4 = 2,
   HM_W4A8_MXFP4 = 3,
   HM_W4A4_NVFP4 = 4,
   HM_W4A16_MXINT4 = 5,
-  HM_W4A16_INT4_G32 = 6
+  HM_W4A16_INT4_G32 = 6,
+  HM_W8A16_INT8 = 7
 } hm_format;
 
 /* How zero-points are stored in the standard format handed to hm_transform (INT4 formats with
@@ -82,14 +88,15 @@ typedef enum hm_format {
 typedef enum hm_zero_convention { HM_ZP_INT = 0, HM_ZP_GPTQ = 1 } hm_zero_convention;
 
 /* Description of one quantized weight matrix W[N,K] in the common ("standard") format.
- *  has_zero       : INT4 formats (1 and 6) only; 1 = zero-points present.
+ *  has_zero       : integer formats (1, 6 and 7) only; 1 = zero-points present (u4; u8 for 7).
  *  tensor_scale   : HM_W4A4_NVFP4 only; the fp32 per-tensor scale gW (ignored otherwise).
  *  group          : K values per scale. HM_W4A16_INT4: 0 (= 128) or any multiple of 128 that
  *                   divides K, or -1 for one scale per row (per channel, = K); these pack into
  *                   the same units as 128 (each unit carries its group's scale). HM_W4A16_INT4_G32:
- *                   0 (= 32), 32 or 64. Others: 0 or the format's own (32 MX, 16 NVFP4).
+ *                   0 (= 32), 32 or 64. HM_W8A16_INT8: 0 or 128. Others: 0 or the format's own
+ *                   (32 MX, 16 NVFP4).
  *  zero_convention: hm_zero_convention of the zero-points handed to hm_transform.
- * Shape rules: N >= 1; K % 128 == 0 for formats 1-3, 5 and 6, K % 64 == 0 for format 4. */
+ * Shape rules: N >= 1; K % 128 == 0 for formats 1-3 and 5-7, K % 64 == 0 for format 4. */
 typedef struct hm_weight_desc {
   int32_t fmt;
   int32_t has_zero;
@@ -119,7 +126,9 @@ size_t hm_packed_size(const hm_weight_desc* desc);
  *   HM_W4A16_MXINT4 : the same e (an all-zero block: e = 0); q = clamp(rne(w/2^(e-127)), -8, 7).
  *   HM_W4A4_NVFP4 : g = fp32(amax/2688) computed on the device and written to *g_out;
  *                   sb = e4m3(fp32(fp32(amax16/6)/g)); code = e2m1(fp32(w/fp32(sb*g))).
- * Outputs (device): q_out packed codes [N][K/2] (even k in the low nibble; INT4 and MXINT4
+ *   HM_W8A16_INT8 : s = bf16(fp32(max|w| over 128)/127); q = clamp(rne(fp32(w/s)) [+z]) into
+ *                   [-128,127] (or [0,255] with zero-points), one byte per code.
+ * Outputs (device): q_out packed codes [N][K/2] ([N][K] bytes for INT8; even k in the low nibble; INT4 and MXINT4
  * nibbles are two's complement, INT4 ones unsigned with zero-points); scales_out [N][K/g]
  * (bf16 for the INT4 formats with g = desc.group; one byte per code for MXFP4 and MXINT4 g=32 and
  * NVFP4 g=16); g_out (NVFP4 only, fp32). INT4 zero-points zeros_in are [N][K/g], one u4 per byte.
@@ -144,6 +153,8 @@ hm_status hm_quantize_weight(const hm_weight_desc* desc, const float* w, const u
  *    even). Units are 8448 / 8512 / 8704 bytes. HM_W4A16_INT4_G32 units: the same codes, then the
  *    bf16 scale of (row r, 32-K chunk c) at 8192 + 8r + 2c and the u4 zero-point of (r, c) at
  *    9216 + 2r + c/2, bit 4 (c % 2) (a group of 64 fills two chunks); 9216 / 9472 bytes.
+ *    HM_W8A16_INT8 units: code (r, kk) as a byte at (kk/16)*2048 + r*16 + kk%16 (q + 128 without
+ *    zero-points), 128 bf16 scales at 16384, 128 u8 zero-points at 16640; 16640 / 16768 bytes.
  *  - W4A8 / W4A4: codes row-major [N_pad][K_pad/2], then 512-byte scale atoms
  *    [N_pad/128][K_pad/chunk] (chunk = 128 K for E8M0 per 32, 64 K for e4m3 per 16), the scale
  *    of (row r, sub-block j) at byte (r%32)*16 + (r/32)*4 + j of its atom. */

@@ -97,14 +97,14 @@ int env_int(const char* name, int dflt) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW4A16Int4G; }
+bool valid_fmt(int32_t f) { return f >= kW4A16Int4 && f <= kW8A16Int8; }
 
 // The K values per scale a description stands for (0 stands for the format's own), or 0 when the
 // group, zero-point and convention fields do not fit the format.
 int64_t desc_group(const hm_weight_desc* d) {
   const bool int4 = d->fmt == kW4A16Int4 || d->fmt == kW4A16Int4G;
   if (d->has_zero != 0 && d->has_zero != 1) return 0;
-  if (d->has_zero && !int4) return 0;
+  if (d->has_zero && !int4 && d->fmt != kW8A16Int8) return 0;
   if (d->zero_convention != HM_ZP_INT && !(d->zero_convention == HM_ZP_GPTQ && int4 && d->has_zero)) return 0;
   if (d->fmt == kW4A16Int4) {
     const int64_t g = d->group == 0 ? 128 : (d->group == -1 ? d->K : d->group);
@@ -114,6 +114,7 @@ int64_t desc_group(const hm_weight_desc* d) {
     const int64_t g = d->group == 0 ? 32 : d->group;
     return (g == 32 || g == 64) ? g : 0;
   }
+  if (d->fmt == kW8A16Int8) return (d->group == 0 || d->group == 128) ? 128 : 0;
   const int64_t own = d->fmt == kW4A4Nv ? 16 : 32;
   return (d->group == 0 || d->group == own) ? own : 0;
 }
@@ -204,7 +205,8 @@ F16Choice f16_choice(int64_t m, int64_t n, int64_t k, int num_sms) {
 int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   const bool block_scaled = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_TILE_M", 0);
-  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || ((forced == 192 || forced == 256) && !block_scaled)) {
+  if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 192 && !block_scaled) ||
+      (forced == 256 && !block_scaled && fmt != kW8A16Int8)) {
     if (fmt == kW4A4Nv && forced < 128 && m > forced) return 128;
     return forced;
   }
@@ -215,8 +217,10 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
   if (m <= 64) return 64;
   if (m <= 128) return 128;
   // The 256-token tile halves the dequant work and X traffic per FLOP; it wins (measured on
-  // 4096x4096, 14336x4096, 4096x14336) once its tiles cover about 70 % of the SMs.
+  // 4096x4096, 14336x4096, 4096x14336) once its tiles cover about 70 % of the SMs. INT8 units are
+  // twice the size: its widest tile is 192 (A in TMEM, three load stages).
   const int64_t n_tiles = pad_n(n) / 128;
+  if (fmt == kW8A16Int8) return ceil_div(m, 192) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 7 ? 192 : 128;
   return ceil_div(m, 256) * n_tiles * 10 >= static_cast<int64_t>(num_sms) * 7 ? 256 : 128;
 }
 
@@ -233,7 +237,7 @@ bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (m < 1 || m > kGemvMaxTokens) return false;
   const int mode = env_int("HM_GEMV", 1);
   if (mode == 0) return false;
-  if (mode == 2 || m <= 16 || chunk_scaled_fmt(fmt)) return true;
+  if (mode == 2 || m <= 16 || fmt != kW4A16Int4) return true;   // no small-token tcgen05 kernel for the others
   return f16_choice(m, n, k, num_sms).stream_k;
 }
 
@@ -444,7 +448,7 @@ int moe_tile_m(int32_t fmt, int64_t rows, int32_t E) {
   const bool bs = fmt == kW4A8Mx || fmt == kW4A4Nv;
   const int forced = env_int("HM_MOE_TILE_M", 0);
   if (forced == 16 || forced == 32 || forced == 64 || forced == 128 || (forced == 256 && !bs)) t = forced;
-  if (bs && t > 128) t = 128;
+  if ((bs || fmt == kW8A16Int8) && t > 128) t = 128;
   return t;
 }
 

@@ -1,5 +1,5 @@
-// Restoring 4-bit weight codes to bf16 in registers. Shared by the W4A16 GEMM's dequant
-// warps and the hm_dequant test hook, so both restore exactly the same values.
+// Restoring 4-bit (and 8-bit) weight codes to bf16 in registers. Shared by the W4A16 GEMM's
+// dequant warps and the hm_dequant test hook, so both restore exactly the same values.
 //
 // INT4 (the explainer page's rule, restored weight = scale * code, with an optional
 // zero-point): w = bf16((u - z) * s). u and z are 4-bit unsigned; the pair (128 + u) is
@@ -46,6 +46,30 @@ __device__ __forceinline__ void dq_int4_word_unscaled(uint32_t w, uint32_t z2, u
     asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(t) : "r"(sh));
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(z2));
   }
+}
+
+// INT8: one 32-bit word of 4 codes (bytes, k order) -> 2 bf16x2 pairs holding u - z exactly
+// (integers in [-255, 255] need at most 8 significant bits). Each byte goes into the low mantissa
+// of the fp32 2^23 (a byte permute), the fp32 subtraction of 2^23 + z is exact, and the pair is
+// packed to bf16 (exact). zf = 2^23 + z as fp32.
+__device__ __forceinline__ void dq_int8_word_unscaled(uint32_t w, float zf, uint32_t (&o)[2]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(w), "r"(0x4B000000u), "r"(0x7540u | (2u * i)));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(w), "r"(0x4B000000u), "r"(0x7540u | (2u * i + 1u)));
+    o[i] = pack_bf16x2_rn(__uint_as_float(a) - zf, __uint_as_float(b) - zf);
+  }
+}
+
+// INT8 word -> 2 bf16x2 pairs of the restored weight bf16((u - z) * s): the exact pairs above times
+// the bf16 scale, rounded once.
+__device__ __forceinline__ void dq_int8_word(uint32_t w, float zf, __nv_bfloat162 ss, uint32_t (&o)[2]) {
+  uint32_t e[2];
+  dq_int8_word_unscaled(w, zf, e);
+  const uint32_t s2 = bf16x2_bits(ss);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(e[i]), "r"(s2));
 }
 
 // bf16x2 holding (128 + z, 128 + z).

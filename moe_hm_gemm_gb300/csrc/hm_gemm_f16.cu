@@ -16,6 +16,15 @@ bool f16s_serves(int fmt, int tile_m) {
 
 int f16_stages(int fmt, int tile_m) {
   if (f16s_serves(fmt, tile_m)) return f16s_stages(tile_m);
+  if (fmt == kW8A16Int8) {
+    switch (tile_m) {
+      case 16: return F16Shape<16, kUnitInt8Zp>::kSL;
+      case 32: return F16Shape<32, kUnitInt8Zp>::kSL;
+      case 64: return F16Shape<64, kUnitInt8Zp>::kSL;
+      case 128: return F16Shape<128, kUnitInt8Zp>::kSL;
+      default: return F16Shape<192, kUnitInt8Zp>::kSL;
+    }
+  }
   if (fmt == kW4A16Int4G) {
     switch (tile_m) {
       case 16: return F16Shape<16, kUnitG32Zp>::kSL;
@@ -41,6 +50,7 @@ cudaError_t launch_f16_gemm(const F16Params& p, int tile_m, bool moe, cudaStream
   if (p.fmt == kW4A16Mx) return launch_f16_mxfp4(p, tile_m, moe, st);
   if (p.fmt == kW4A16MxInt) return launch_f16_mxint4(p, tile_m, moe, st);
   if (p.fmt == kW4A16Int4G) return launch_f16_int4g(p, tile_m, moe, st);
+  if (p.fmt == kW8A16Int8) return launch_f16_int8(p, tile_m, moe, st);
   return moe ? launch_bt<0, true>(p, tile_m, st) : launch_bt<0, false>(p, tile_m, st);
 }
 

@@ -102,10 +102,12 @@ struct F16Shape {
 };
 
 // Unit bytes a load stage must hold per 128-K block for a weight format (WK).
-constexpr int f16_unit_room(int wk) { return wk == 6 ? static_cast<int>(kUnitG32Zp) : static_cast<int>(kUnitMx); }
+constexpr int f16_unit_room(int wk) {
+  return wk == 8 ? static_cast<int>(kUnitInt8Zp) : (wk == 6 ? static_cast<int>(kUnitG32Zp) : static_cast<int>(kUnitMx));
+}
 
 // WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4,
-// 6 = INT4 with a bf16 scale and u4 zero-point per 32-K chunk.
+// 6 = INT4 with a bf16 scale and u4 zero-point per 32-K chunk, 8 = INT8 (tiles up to 192 tokens).
 template <int BT, int WK, bool MOE>
 __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
   using S = F16Shape<BT, f16_unit_room(WK)>;
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // The first weight's header decides whether INT4 units carry zero-points; every weight
     // used must agree with it and with the call's (fmt, N, K).
     const uint32_t hz = hdr.has_zero;
-    *hz_sh = ((WK == 0 || WK == 6) && hz == 1u) ? 1u : 0u;
+    *hz_sh = ((WK == 0 || WK == 6 || WK == 8) && hz == 1u) ? 1u : 0u;
     if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
       atomicOr(p.err, kErrHeader);
       *abort_flag = 1u;
@@ -196,8 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     trace_mark(p.trace, 1);
     pdl_launch_dependents();
   }
-  const uint32_t kUnit = WK == 6 ? (has_zero ? kUnitG32Zp : kUnitG32)
-                                  : (WK >= 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4));
+  const uint32_t kUnit = WK == 8 ? (has_zero ? kUnitInt8Zp : kUnitInt8)
+                         : WK == 6 ? (has_zero ? kUnitG32Zp : kUnitG32)
+                                   : (WK >= 2 ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4));
   // Weights are streamed once when a single token tile covers M; with several token tiles the
   // same weight tiles are read again by other CTAs, so keep them in L2.
   const bool reuse_w = MOE || p.num_m_tiles > 1;
@@ -415,87 +418,127 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
         if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 1, bi);
         const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
-        // INT4 and MXINT4 take the whole 128-K row into registers at once; MXFP4 (whose scale
-        // and conversion need more registers) takes the second half after converting the first.
-        uint4 c[4];
-#pragma unroll
-        for (int i = 0; i < (WK == 2 ? 2 : 4); ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
-        __nv_bfloat162 zz, ss;
-        uint32_t e4 = 0;
-        uint32_t s4[2] = {0u, 0u}, z4 = 0x8888u;   // WK 6: the four chunks' bf16 scales and zero-points
-        if (WK == 6) {
-          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(s4[0]), "=r"(s4[1]) : "r"(wsa + kUnitCodes + 8 * r));
-          if (has_zero) {
-            uint16_t zb;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitG32 + 2 * r));
-            z4 = zb;
+        if constexpr (WK != 8) {
+          // INT4 and MXINT4 take the whole 128-K row into registers at once; MXFP4 (whose scale
+          // and conversion need more registers) takes the second half after converting the first.
+          uint4 c[4];
+  #pragma unroll
+          for (int i = 0; i < (WK == 2 ? 2 : 4); ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
+          __nv_bfloat162 zz, ss;
+          uint32_t e4 = 0;
+          uint32_t s4[2] = {0u, 0u}, z4 = 0x8888u;   // WK 6: the four chunks' bf16 scales and zero-points
+          if (WK == 6) {
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(s4[0]), "=r"(s4[1]) : "r"(wsa + kUnitCodes + 8 * r));
+            if (has_zero) {
+              uint16_t zb;
+              asm volatile("ld.shared.u16 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitG32 + 2 * r));
+              z4 = zb;
+            }
+            zz = int4_zero_pair(8);
+            ss = bf16_pair(0);
+          } else if (WK >= 2) {
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e4) : "r"(wsa + kUnitCodes + 4 * r));
+            zz = int4_zero_pair(8);   // MXINT4 nibbles are q + 8
+          } else {
+            uint16_t sb;
+            asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(wsa + kUnitCodes + 2 * r));
+            ss = bf16_pair(sb);
+            uint32_t z = 8u;
+            if (has_zero) {
+              uint16_t zb;
+              asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitInt4 + (r >> 1)));
+              z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
+            }
+            zz = int4_zero_pair(z);
           }
-          zz = int4_zero_pair(8);
-          ss = bf16_pair(0);
-        } else if (WK >= 2) {
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e4) : "r"(wsa + kUnitCodes + 4 * r));
-          zz = int4_zero_pair(8);   // MXINT4 nibbles are q + 8
+          const bool last_of_stage = jb + 2 >= g;
+          if (WK != 2 && last_of_stage) {   // the stage's last block of this group is in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_l[ls]);
+          }
+  #pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (WK == 2 && half == 1) {
+  #pragma unroll
+              for (int i = 2; i < 4; ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
+              if (last_of_stage) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_l[ls]);
+              }
+            }
+            uint32_t a_regs[32];  // TMEM path: 64 restored K of this row as bf16x2, in K order
+  #pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int c4 = 2 * half + i;
+              const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
+              const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
+              const bool mx_bits = WK == 2 && ex <= 128u;
+              const uint32_t sc2 = mx_pow2_pair(ex);
+              const float scale = WK == 2 ? pow2f(static_cast<int>(ex) - 127) : 0.f;
+              const __nv_bfloat162 si = bits_bf16x2(mxint_scale_pair(ex));
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t o[4];
+                if (WK == 6)
+                  dq_int4_word(words[j], int4_zero_pair((z4 >> (4 * c4)) & 0xFu),
+                               bf16_pair(static_cast<uint16_t>(s4[c4 >> 1] >> (16 * (c4 & 1)))), o);
+                else if (WK == 0) dq_int4_word(words[j], zz, ss, o);
+                else if (WK == 3) dq_int4_word(words[j], zz, si, o);
+                else if (mx_bits) dq_mx_word_bits(words[j], sc2, o);
+                else dq_mx_word(words[j], lut, scale, o);
+                if constexpr (S::kATmem) {
+  #pragma unroll
+                  for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
+                } else {
+                  const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
+                  const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
+                  const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
+                                       ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
+                  st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+                }
+              }
+            }
+            if constexpr (S::kATmem)
+              tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
+          }
         } else {
+          // INT8: one byte per code, the row's 128 codes in 8 chunks of 16; scale and zero-point per
+          // row; the two 64-K halves are loaded, restored and stored to TMEM in turn
+          static_assert(S::kATmem, "INT8 tiles keep the restored weights in TMEM");
           uint16_t sb;
-          asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(wsa + kUnitCodes + 2 * r));
-          ss = bf16_pair(sb);
-          uint32_t z = 8u;
+          asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sb) : "r"(wsa + kUnitInt8Codes + 2 * r));
+          const __nv_bfloat162 s8 = bf16_pair(sb);
+          uint32_t zb = 128u;
           if (has_zero) {
-            uint16_t zb;
-            asm volatile("ld.shared.u8 %0, [%1];" : "=h"(zb) : "r"(wsa + kUnitInt4 + (r >> 1)));
-            z = (static_cast<uint32_t>(zb) >> (4 * (r & 1))) & 0xFu;
+            uint16_t z16;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=h"(z16) : "r"(wsa + kUnitInt8 + r));
+            zb = z16;
           }
-          zz = int4_zero_pair(z);
-        }
-        const bool last_of_stage = jb + 2 >= g;
-        if (WK != 2 && last_of_stage) {   // the stage's last block of this group is in registers
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty_l[ls]);
-        }
+          const float zf = 8388608.0f + static_cast<float>(zb);
+          const bool last_of_stage = jb + 2 >= g;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (WK == 2 && half == 1) {
+          for (int half = 0; half < 2; ++half) {
+            uint4 c8[4];
 #pragma unroll
-            for (int i = 2; i < 4; ++i) c[i] = ld_shared_v4(wsa + i * 2048 + r * 16);
-            if (last_of_stage) {
+            for (int i = 0; i < 4; ++i) c8[i] = ld_shared_v4(wsa + (4 * half + i) * 2048 + r * 16);
+            if (half == 1 && last_of_stage) {   // the stage's last block of this group is in registers
               __syncwarp();
               if (lane == 0) mbar_arrive(&empty_l[ls]);
             }
-          }
-          uint32_t a_regs[32];  // TMEM path: 64 restored K of this row as bf16x2, in K order
+            uint32_t a_regs[32];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int c4 = 2 * half + i;
-            const uint32_t words[4] = {c[c4].x, c[c4].y, c[c4].z, c[c4].w};
-            const uint32_t ex = (e4 >> (8 * c4)) & 0xFFu;
-            const bool mx_bits = WK == 2 && ex <= 128u;
-            const uint32_t sc2 = mx_pow2_pair(ex);
-            const float scale = WK == 2 ? pow2f(static_cast<int>(ex) - 127) : 0.f;
-            const __nv_bfloat162 si = bits_bf16x2(mxint_scale_pair(ex));
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t words[4] = {c8[i].x, c8[i].y, c8[i].z, c8[i].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t o[4];
-              if (WK == 6)
-                dq_int4_word(words[j], int4_zero_pair((z4 >> (4 * c4)) & 0xFu),
-                             bf16_pair(static_cast<uint16_t>(s4[c4 >> 1] >> (16 * (c4 & 1)))), o);
-              else if (WK == 0) dq_int4_word(words[j], zz, ss, o);
-              else if (WK == 3) dq_int4_word(words[j], zz, si, o);
-              else if (mx_bits) dq_mx_word_bits(words[j], sc2, o);
-              else dq_mx_word(words[j], lut, scale, o);
-              if constexpr (S::kATmem) {
-#pragma unroll
-                for (int t = 0; t < 4; ++t) a_regs[16 * i + 4 * j + t] = o[t];
-              } else {
-                const int ch = 4 * c4 + j;  // 16-byte chunk (8 consecutive K) within the 128 K
-                const uint32_t a_base = smem_u32(smem + S::kAOff + as * kAStage);
-                const uint32_t dst = a_base + (ch >> 3) * (kAStage / 2) + r * 128 +
-                                     ((static_cast<uint32_t>(ch & 7) ^ static_cast<uint32_t>(r & 7)) << 4);
-                st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+              for (int j = 0; j < 4; ++j) {
+                uint32_t p2[2];
+                dq_int8_word(words[j], zf, s8, p2);
+                a_regs[8 * i + 2 * j] = p2[0];
+                a_regs[8 * i + 2 * j + 1] = p2[1];
               }
             }
-          }
-          if constexpr (S::kATmem)
             tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + S::kACol0 + as * 64 + half * 32, a_regs);
+          }
         }
         if constexpr (S::kATmem) {
           tmem_wait_st();
@@ -642,7 +685,9 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
     case 192:
       if constexpr (!MOE) return launch_one<192, WK, MOE>(p, st);
       return cudaErrorInvalidValue;
-    case 256: return launch_one<256, WK, MOE>(p, st);
+    case 256:
+      if constexpr (WK != 8) return launch_one<256, WK, MOE>(p, st);   // INT8 stops at 192
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -654,5 +699,6 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
 cudaError_t launch_f16_mxfp4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
 cudaError_t launch_f16_mxint4(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
 cudaError_t launch_f16_int4g(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
+cudaError_t launch_f16_int8(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
 
 }  // namespace hm

@@ -185,10 +185,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 // Unit bytes a stage holds for a weight format (WK).
-__host__ __device__ constexpr int v_wbytes(int wk) { return wk == 6 ? 9472 : 8704; }
+__host__ __device__ constexpr int v_wbytes(int wk) { return wk == 8 ? 16768 : (wk == 6 ? 9472 : 8704); }
 
 // WK: 0 = INT4, 2 = MXFP4, 3 = MXINT4 (the last two carry E8M0 scales per 32 in their units),
-// 6 = INT4 with a bf16 scale (and zero-point) per 32-K chunk, applied to each chunk's sum.
+// 6 = INT4 with a bf16 scale (and zero-point) per 32-K chunk, applied to each chunk's sum;
+// 8 = INT8 (one byte per code, bf16 scale and u8 zero-point per row and 128-K block), restored to the
+// exact integers u - z and scaled after the block's sum like INT4.
 template <int MT, int WK>
 __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_constant__ F16Params p) {
   using S = VShape<MT, v_wbytes(WK)>;
@@ -266,7 +268,8 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const bool aborted_early = *abort_flag != 0u;
   const uint32_t has_zero = *hz_sh;
-  const uint32_t kUnit = MX ? kUnitMx : (G32 ? (has_zero ? kUnitG32Zp : kUnitG32) : (has_zero ? kUnitInt4Zp : kUnitInt4));
+  const uint32_t kUnit = WK == 8 ? (has_zero ? kUnitInt8Zp : kUnitInt8)
+                         : (MX ? kUnitMx : (G32 ? (has_zero ? kUnitG32Zp : kUnitG32) : (has_zero ? kUnitInt4Zp : kUnitInt4)));
 
   if (aborted_early) {
     // header mismatch: nothing was issued
@@ -325,7 +328,28 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     // ---------------------------------------------------------------- INT4 row metadata
     // Each unit's 128 scales and zero-points, once per unit instead of once per consumer warp:
     // lane l converts rows 4l .. 4l+3 (bf16 scale -> fp32, u4 zero-point -> bf16x2 128 + z).
-    if constexpr (WK == 0) {
+    if constexpr (WK == 8) {
+      // INT8: per row {fp32 scale, fp32 2^23 + z} (z = 128 without zero-points: codes are q + 128)
+      const uint32_t smem0 = smem_u32(smem);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < n_units; ++i) {
+        if (!mbar_wait(&full[s], ph, wc)) break;
+        const uint32_t base = smem0 + s * S::kStage;
+        uint32_t sc01, sc23, z4 = 0x80808080u;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc01), "=r"(sc23) : "r"(base + kUnitInt8Codes + 8 * lane));
+        if (has_zero) z4 = lds32(base + kUnitInt8 + 4 * lane);
+        float zf[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) zf[r] = 8388608.0f + static_cast<float>((z4 >> (8 * r)) & 0xFFu);
+        const uint32_t mb = base + S::kMetaOff + 32 * lane;
+        st_shared_v4(mb, sc01 << 16, __float_as_uint(zf[0]), sc01 & 0xFFFF0000u, __float_as_uint(zf[1]));
+        st_shared_v4(mb + 16, sc23 << 16, __float_as_uint(zf[2]), sc23 & 0xFFFF0000u, __float_as_uint(zf[3]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_full[s]);
+        if (++s == SL) { s = 0; ph ^= 1u; }
+      }
+    } else if constexpr (WK == 0) {
       const uint32_t smem0 = smem_u32(smem);
       int s = 0;
       uint32_t ph = 0;
@@ -546,7 +570,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
           for (int e = 0; e < 4; ++e) yacc[j][q][e] = 0.f;
       bool ok = true;
       for (; i < seg_end; i += S::kPar) {
-        if (!mbar_wait(&full[s], ph, wc) || (WK == 0 && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
+        if (!mbar_wait(&full[s], ph, wc) || ((WK == 0 || WK == 8) && !mbar_wait(&meta_full[s], ph, wc))) { ok = false; break; }
         if (cw == 0 && lane == 0 && i == 0) trace_mark(p.trace, 4);
         const uint32_t base = smem0 + s * S::kStage;
         uint32_t bx[NQ][2][4];
@@ -558,13 +582,61 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
             bx[q][cc][0] = v.x; bx[q][cc][1] = v.y; bx[q][cc][2] = v.z; bx[q][cc][3] = v.w;
           }
         uint32_t wd[2][2][2];
+        if constexpr (WK != 8) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+          for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int hl = 0; hl < 2; ++hl)
+            for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff + cc * 2048 + j * 256 + hl * 128);
-        if constexpr (G32) {
+              for (int cc = 0; cc < 2; ++cc) wd[j][hl][cc] = lds32(base + woff + cc * 2048 + j * 256 + hl * 128);
+        }
+        if constexpr (WK == 8) {
+          // the lane's 8 codes of each row and 32-K chunk: bytes 8 (t % 2) .. of 16-column slot
+          // 2 (chunk) + t / 2; exact integers u - z, the block's scale applied to the sums
+          float sc[2][2], zf[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+              uint32_t sb, zb;
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sb), "=r"(zb) : "r"(base + moff + j * 128 + hl * 64));
+              sc[j][hl] = __uint_as_float(sb);
+              zf[j][hl] = __uint_as_float(zb);
+            }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float d[2][NQ][4];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t lo[4], hi[4];
+#pragma unroll
+              for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t rr = static_cast<uint32_t>(32 * pr + g + 16 * j + 8 * hl);
+                uint32_t w0, w1;
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(w0), "=r"(w1)
+                             : "r"(base + (2 * (2 * cp + cc) + (t >> 1)) * 2048 + rr * 16 + 8 * (t & 1)));
+                uint32_t e0[2], e1[2];
+                dq_int8_word_unscaled(w0, zf[j][hl], e0);
+                dq_int8_word_unscaled(w1, zf[j][hl], e1);
+                uint32_t* dst = hl ? hi : lo;
+                dst[0] = e0[0]; dst[1] = e0[1]; dst[2] = e1[0]; dst[3] = e1[1];
+              }
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+                mma_bf16_16816_z(d[cc][q], lo[0], hi[0], lo[1], hi[1], bx[q][cc][0], bx[q][cc][1]);
+                mma_bf16_16816(d[cc][q], lo[2], hi[2], lo[3], hi[3], bx[q][cc][2], bx[q][cc][3]);
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              yacc[j][q][0] = fmaf(sc[j][0], d[0][q][0] + d[1][q][0], yacc[j][q][0]);
+              yacc[j][q][1] = fmaf(sc[j][0], d[0][q][1] + d[1][q][1], yacc[j][q][1]);
+              yacc[j][q][2] = fmaf(sc[j][1], d[0][q][2] + d[1][q][2], yacc[j][q][2]);
+              yacc[j][q][3] = fmaf(sc[j][1], d[0][q][3] + d[1][q][3], yacc[j][q][3]);
+            }
+          }
+        } else if constexpr (G32) {
           // per (row, 32-K chunk): bf16 scales of chunks 2cp, 2cp + 1 in one word, u4 zero-points
           // of the row's four chunks in one half-word
           uint32_t sw[2][2], zw[2][2];
@@ -762,6 +834,8 @@ int gemv_stages(int64_t m, int32_t fmt) {
   const int t = gemv_tokens(m);
   if (fmt == kW4A16Int4G)
     return t == 8 ? VShape<8, v_wbytes(6)>::kS : (t == 16 ? VShape<16, v_wbytes(6)>::kS : VShape<32, v_wbytes(6)>::kS);
+  if (fmt == kW8A16Int8)
+    return t == 8 ? VShape<8, v_wbytes(8)>::kS : (t == 16 ? VShape<16, v_wbytes(8)>::kS : VShape<32, v_wbytes(8)>::kS);
   return t == 8 ? VShape<8>::kS : (t == 16 ? VShape<16>::kS : VShape<32>::kS);
 }
 
@@ -774,6 +848,8 @@ cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
     return t == 8 ? launch_v<8, 3>(p, st) : (t == 16 ? launch_v<16, 3>(p, st) : launch_v<32, 3>(p, st));
   if (p.fmt == kW4A16Int4G)
     return t == 8 ? launch_v<8, 6>(p, st) : (t == 16 ? launch_v<16, 6>(p, st) : launch_v<32, 6>(p, st));
+  if (p.fmt == kW8A16Int8)
+    return t == 8 ? launch_v<8, 8>(p, st) : (t == 16 ? launch_v<16, 8>(p, st) : launch_v<32, 8>(p, st));
   return t == 8 ? launch_v<8, 0>(p, st) : (t == 16 ? launch_v<16, 0>(p, st) : launch_v<32, 0>(p, st));
 }
 

@@ -12,7 +12,9 @@
 // units hold the same biased nibbles (u = q + 8) with the 128 x 4 E8M0 scales of MXFP4 units.
 // INT4 units with a bf16 scale per 32-K chunk (groups of 32 or 64) hold the INT4 nibbles, then the
 // scale of (row r, chunk c) at byte 8192 + 8r + 2c and, with zero-points, the u4 zero-point of
-// (r, c) at byte 9216 + 2r + c/2, bit 4 (c % 2).
+// (r, c) at byte 9216 + 2r + c/2, bit 4 (c % 2). INT8 units hold one byte per code, code (r, kk) at
+// (kk/16)*2048 + r*16 + kk%16 (q + 128 without zero-points), then 128 bf16 scales at 16384 and,
+// with zero-points, 128 u8 zero-points at 16640.
 #pragma once
 #include <cstdint>
 
@@ -28,6 +30,9 @@ constexpr uint32_t kUnitInt4Zp = 8512;    // + 64 bytes of u4 zero-points
 constexpr uint32_t kUnitMx = 8704;        // + 128 x 4 E8M0 scales
 constexpr uint32_t kUnitG32 = 9216;       // INT4 with a bf16 scale per 32-K chunk: + 128 x 4 bf16
 constexpr uint32_t kUnitG32Zp = 9472;     // + 128 x 4 u4 zero-points
+constexpr uint32_t kUnitInt8Codes = 16384; // INT8: 128 x 128 bytes of codes
+constexpr uint32_t kUnitInt8 = 16640;     // + 128 bf16 scales
+constexpr uint32_t kUnitInt8Zp = 16768;   // + 128 u8 zero-points
 constexpr uint32_t kAtomBytes = 512;      // scale-factor atom (128 rows x 4 scales)
 
 struct PackedHeader {
@@ -43,11 +48,13 @@ struct PackedHeader {
 };
 static_assert(sizeof(PackedHeader) == 56, "header layout");
 
-enum Fmt : int32_t { kW4A16Int4 = 1, kW4A16Mx = 2, kW4A8Mx = 3, kW4A4Nv = 4, kW4A16MxInt = 5, kW4A16Int4G = 6 };
+enum Fmt : int32_t {
+  kW4A16Int4 = 1, kW4A16Mx = 2, kW4A8Mx = 3, kW4A4Nv = 4, kW4A16MxInt = 5, kW4A16Int4G = 6, kW8A16Int8 = 7
+};
 
 // Formats stored as 128x128 units and multiplied with bf16 activations on kind::f16.
 __host__ __device__ inline bool unit_fmt(int32_t fmt) {
-  return fmt == kW4A16Int4 || fmt == kW4A16Mx || fmt == kW4A16MxInt || fmt == kW4A16Int4G;
+  return fmt == kW4A16Int4 || fmt == kW4A16Mx || fmt == kW4A16MxInt || fmt == kW4A16Int4G || fmt == kW8A16Int8;
 }
 // Unit formats whose scales are E8M0 per 32 along K (128 rows x 4 bytes after the codes).
 __host__ __device__ inline bool e8_unit_fmt(int32_t fmt) { return fmt == kW4A16Mx || fmt == kW4A16MxInt; }
@@ -59,6 +66,7 @@ inline int64_t pad_n(int64_t n) { return (n + kTileN - 1) / kTileN * kTileN; }
 inline int64_t pad_k(int32_t fmt, int64_t k) { return fmt == kW4A4Nv ? (k + 255) / 256 * 256 : k; }
 
 __host__ __device__ inline uint32_t unit_bytes(int32_t fmt, bool has_zero) {
+  if (fmt == kW8A16Int8) return has_zero ? kUnitInt8Zp : kUnitInt8;
   if (fmt == kW4A16Int4G) return has_zero ? kUnitG32Zp : kUnitG32;
   return e8_unit_fmt(fmt) ? kUnitMx : (has_zero ? kUnitInt4Zp : kUnitInt4);
 }

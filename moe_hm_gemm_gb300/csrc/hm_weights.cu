@@ -92,6 +92,33 @@ __global__ void quant_int4_kernel(const float* __restrict__ w, const uint8_t* __
   if ((4 * lane) % (group < 128 ? group : 128) == 0) scales[row * groups + gi] = sb;
 }
 
+// INT8, one warp per (row, group of 128); lane holds 4 consecutive K: s = bf16(fp32(amax)/127),
+// q = clamp(rne(fp32(w/s)) [+ z]) into [-128, 127] (or [0, 255] with a u8 zero-point), one byte each.
+__global__ void quant_int8_kernel(const float* __restrict__ w, const uint8_t* __restrict__ zeros, int64_t n,
+                                  int64_t k, int has_zero, uint8_t* __restrict__ q, __nv_bfloat16* __restrict__ scales) {
+  const int64_t groups = k / 128;
+  const int64_t gid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gid >= n * groups) return;
+  const int64_t row = gid / groups, g = gid % groups;
+  const float4 v = *reinterpret_cast<const float4*>(w + row * k + g * 128 + 4 * lane);
+  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  amax = warp_max(amax, 32);
+  const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(amax, 127.0f));
+  const float s = __bfloat162float(sb);
+  const int z = has_zero ? zeros[row * groups + g] : 0;
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = s == 0.f ? 0 : __float2int_rn(rintf(__fdiv_rn(x[i], s)));
+    const int qi = has_zero ? min(max(r + z, 0), 255) : min(max(r, -128), 127);
+    packed |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * i);
+  }
+  *reinterpret_cast<uint32_t*>(q + row * k + g * 128 + 4 * lane) = packed;
+  if (lane == 0) scales[row * groups + g] = sb;
+}
+
 // MXFP4, one warp per (row, 128 K); 8 lanes per 32-block.
 __global__ void quant_mx_kernel(const float* __restrict__ w, int64_t n, int64_t k,
                                 uint8_t* __restrict__ q, uint8_t* __restrict__ e8) {
@@ -259,6 +286,25 @@ __global__ void transform_units_kernel(int32_t fmt, int32_t has_zero, int64_t n,
   uint8_t* unit = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * ub;
   if (blockIdx.x == 0 && threadIdx.x < 64) write_header(packed, fmt, n, k, has_zero, 1.0f);
   const bool valid = row < n;
+  if (fmt == kW8A16Int8) {
+    // one byte per code: the row's 128 codes in 16-column chunks, 2048 bytes apart (signed codes
+    // stored as q + 128 = q ^ 0x80)
+    const uint32_t flip8 = has_zero ? 0u : 0x80808080u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (valid) {
+        v = *reinterpret_cast<const uint4*>(q + row * k + kb * 128 + c * 16);
+        v.x ^= flip8; v.y ^= flip8; v.z ^= flip8; v.w ^= flip8;
+      }
+      *reinterpret_cast<uint4*>(unit + c * 2048 + r * 16) = v;
+    }
+    uint16_t sb = 0;
+    if (valid) sb = reinterpret_cast<const uint16_t*>(scales)[row * kbt + kb];
+    *reinterpret_cast<uint16_t*>(unit + kUnitInt8Codes + 2 * r) = sb;
+    if (has_zero) unit[kUnitInt8 + r] = valid ? zeros[row * kbt + kb] : 0;
+    return;
+  }
   // signed nibbles (INT4 without zero-points, MXINT4) are stored as q + 8 = q ^ 8
   const bool int4 = fmt == kW4A16Int4 || fmt == kW4A16Int4G;
   const uint32_t flip = ((int4 && !has_zero) || fmt == kW4A16MxInt) ? 0x88888888u : 0u;
@@ -352,6 +398,26 @@ __global__ void dequant_units_kernel(int32_t fmt, int32_t has_zero, int64_t n, i
   if (row >= n) return;
   const uint32_t ub = unit_bytes(fmt, has_zero != 0);
   const uint8_t* unit = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * ub;
+  if (fmt == kW8A16Int8) {
+    const __nv_bfloat162 s8 = bf16_pair(*reinterpret_cast<const uint16_t*>(unit + kUnitInt8Codes + 2 * r));
+    const float zf = 8388608.0f + static_cast<float>(has_zero ? unit[kUnitInt8 + r] : 128u);
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(unit + c * 2048 + r * 16);
+      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t p2[2];
+        dq_int8_word(words[j], zf, s8, p2);
+        o[2 * j] = p2[0];
+        o[2 * j + 1] = p2[1];
+      }
+      uint4* dst = reinterpret_cast<uint4*>(w + row * k + kb * 128 + c * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    return;
+  }
   __nv_bfloat162 zz = int4_zero_pair(8), ss = bf16_pair(0);
   uint32_t e4 = 0;
   uint2 s4 = make_uint2(0u, 0u);   // format 6: bf16 scales of the four 32-K chunks
@@ -419,7 +485,10 @@ inline unsigned blocks_for(int64_t threads, int per_block) {
 cudaError_t launch_quantize_weight(int32_t fmt, int32_t has_zero, int64_t n, int64_t k, int64_t group,
                                    const float* w, const uint8_t* zeros_in, uint8_t* q_out, void* scales_out,
                                    float* g_out, float* ws, cudaStream_t st) {
-  if (fmt == kW4A16Int4 || fmt == kW4A16Int4G) {
+  if (fmt == kW8A16Int8) {
+    quant_int8_kernel<<<blocks_for(n * (k / 128) * 32, 256), 256, 0, st>>>(
+        w, zeros_in, n, k, has_zero, q_out, static_cast<__nv_bfloat16*>(scales_out));
+  } else if (fmt == kW4A16Int4 || fmt == kW4A16Int4G) {
     const int64_t span = group < 128 ? 128 : group;
     quant_int4_kernel<<<blocks_for(n * (k / span) * 32, 256), 256, 0, st>>>(
         w, zeros_in, n, k, has_zero, group, q_out, static_cast<__nv_bfloat16*>(scales_out));

@@ -13,10 +13,10 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libhm.so")
 
-W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4, W4A16_MXINT4, W4A16_INT4_G32 = 1, 2, 3, 4, 5, 6
+W4A16_INT4, W4A16_MXFP4, W4A8_MXFP4, W4A4_NVFP4, W4A16_MXINT4, W4A16_INT4_G32, W8A16_INT8 = 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"w4a16_int4": W4A16_INT4, "w4a16_mxfp4": W4A16_MXFP4,
            "w4a8_mxfp4": W4A8_MXFP4, "w4a4_nvfp4": W4A4_NVFP4, "w4a16_mxint4": W4A16_MXINT4,
-           "w4a16_int4_g32": W4A16_INT4_G32}
+           "w4a16_int4_g32": W4A16_INT4_G32, "w8a16_int8": W8A16_INT8}
 ZP_INT, ZP_GPTQ = 0, 1
 
 
@@ -125,7 +125,7 @@ def group_of(d):
         return d.K
     if d.group:
         return d.group
-    return {W4A16_INT4: 128, W4A16_INT4_G32: 32, W4A4_NVFP4: 16}.get(d.fmt, 32)
+    return {W4A16_INT4: 128, W4A16_INT4_G32: 32, W4A4_NVFP4: 16, W8A16_INT8: 128}.get(d.fmt, 32)
 
 
 def packed_size(d):
@@ -138,8 +138,8 @@ def quantize_weight(d, w, zeros=None):
     if w.dtype != torch.float32:
         raise ValueError("w: expected float32")
     dev = w.device
-    q = torch.empty((d.N, d.K // 2), dtype=torch.uint8, device=dev)
-    if d.fmt in (W4A16_INT4, W4A16_INT4_G32):
+    q = torch.empty((d.N, d.K if d.fmt == W8A16_INT8 else d.K // 2), dtype=torch.uint8, device=dev)
+    if d.fmt in (W4A16_INT4, W4A16_INT4_G32, W8A16_INT8):
         scales = torch.empty((d.N, d.K // group_of(d)), dtype=torch.bfloat16, device=dev)
     elif d.fmt in (W4A16_MXFP4, W4A8_MXFP4, W4A16_MXINT4):
         scales = torch.empty((d.N, d.K // 32), dtype=torch.uint8, device=dev)

@@ -42,6 +42,12 @@ class QuantWeight:
             self.std_q = pack_nibbles(self.q)
             self.std_s = to_bf16(self.s)
             self.packed_ref = ol.pack_w4a16_int4_g32(self.q, self.s, zeros, group=grp)
+        elif fmt == ol.FMT_W8A16_INT8:
+            self.q, self.s = oq.quant_int8(w, zeros=zeros)
+            self.what = oq.dequant_int8(self.q, self.s, zeros)
+            self.std_q = (np.asarray(self.q) & 0xFF).astype(np.uint8)      # one byte per code
+            self.std_s = to_bf16(self.s)
+            self.packed_ref = ol.pack_w8a16_int8(self.q, self.s, zeros)
         elif fmt in (ol.FMT_W4A16_MXFP4, ol.FMT_W4A8_MXFP4):
             self.q, self.s = oq.quant_mxfp4(w)
             self.what = oq.dequant_mxfp4(self.q, self.s)

@@ -46,8 +46,11 @@ def test_packed_size_rejects_bad_shapes(hm):
     assert hm.packed_size(hm.desc(2, 128, 128, True)) == 0  # zero-points only for INT4
     assert hm.packed_size(hm.desc(5, 128, 128, True)) == 0
     assert hm.packed_size(hm.desc(5, 128, 64)) == 0       # MXINT4 K % 128
-    assert hm.packed_size(hm.desc(7, 128, 128)) == 0
+    assert hm.packed_size(hm.desc(8, 128, 128)) == 0
     assert hm.packed_size(hm.desc(9, 128, 128)) == 0
+    assert hm.packed_size(hm.desc(7, 130, 256)) == L.packed_size(7, 130, 256, False)
+    assert hm.packed_size(hm.desc(7, 130, 256, True)) == L.packed_size(7, 130, 256, True)
+    assert hm.packed_size(hm.desc(7, 130, 256, group=64)) == 0        # INT8 groups are 128
     # group sizes: INT4 takes multiples of 128 dividing K (or -1 per channel), format 6 takes 32 / 64
     assert hm.packed_size(hm.desc(1, 128, 512, group=256)) == L.packed_size(1, 128, 512, False)
     assert hm.packed_size(hm.desc(1, 128, 512, group=-1)) == L.packed_size(1, 128, 512, False)
@@ -71,7 +74,7 @@ def test_invalid_arguments_fail_before_any_launch(hm):
     # null pointers / bad shapes are rejected on the host with HM_ERR_INVALID_ARG (1)
     assert lib.hm_gemm(1, None, None, None, None, None, 4, 256, 512, None, 0, None) == 1
     assert lib.hm_gemm(1, P(16), None, None, P(256), P(16), 4, 256, 100, P(256), 1 << 20, None) == 1
-    assert lib.hm_gemm(7, P(16), None, None, P(256), P(16), 4, 256, 512, P(256), 1 << 20, None) == 1
+    assert lib.hm_gemm(9, P(16), None, None, P(256), P(16), 4, 256, 512, P(256), 1 << 20, None) == 1
     # misaligned packed pointer
     assert lib.hm_gemm(1, P(16), None, None, P(272), P(16), 4, 256, 512, P(256), 1 << 20, None) == 1
     # too small a workspace -> HM_ERR_WORKSPACE (3)
