@@ -225,10 +225,11 @@ def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick, has_zero=None):
     return points
 
 
-def moe_points(hm, synth, fmt, quick):
+def moe_points(hm, synth, fmt, quick, only_t=None):
+    """only_t: the T values to build instead of the default sweep (from --m)."""
     e, topk = 256, 8
     layers = [("gate_up", 4096, 7168), ("down", 7168, 2048)]
-    tokens = [16, 256, 4096, 16384] if not quick else [16, 4096]
+    tokens = only_t or ([16, 256, 4096, 16384] if not quick else [16, 4096])
     points = []
     for li, (name, n, k) in enumerate(layers):
         d = hm.desc(fmt, n, k, fmt == hm.W4A16_INT4)
@@ -338,6 +339,10 @@ def build_points(args, hm, synth):
     return pts
 
 
+def moe_ts(args):
+    return sorted({int(v) for v in args.m.split(",")}) if args.m else None
+
+
 def _build_points(args, hm, synth):
     w = args.workload
     if w == "w4a16":
@@ -350,14 +355,14 @@ def _build_points(args, hm, synth):
         return dense_points(hm, synth, hm.W4A4_NVFP4, [(8192, 8192)], [16, 128, 1024, 8192], 3, "kind::mxf4nvf4",
                             args.quick)
     if w == "moe_w4a16":
-        return moe_points(hm, synth, hm.W4A16_INT4, args.quick)
+        return moe_points(hm, synth, hm.W4A16_INT4, args.quick, moe_ts(args))
     if w == "moe_mxfp4":
-        return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick)
+        return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick, moe_ts(args))
     if w == "w4a16_mxint4":
         return dense_points(hm, synth, hm.W4A16_MXINT4, [(4096, 4096), (14336, 4096), (4096, 14336)], MS, 4,
                             "kind::f16", args.quick)
     if w == "moe_mxint4":
-        return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick)
+        return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick, moe_ts(args))
     if w == "moe_silu_mul":
         return silu_points(hm, synth, args.quick)
     if w == "moe_glue":

@@ -240,7 +240,12 @@ hm_status hm_moe_combine(const void* y, const int32_t* pos, const float* w, void
 size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
 
 /* The workspace must be zero-filled once after allocation (cudaMemset); the library leaves
- * the counters it uses back at zero after every call, so it can be reused across calls. */
+ * the counters it uses back at zero after every call, so it can be reused across calls. The
+ * counters sit in one fixed block at the start of every workspace (per CTA that owns a tile split
+ * along K), which no call writes anything else into: one workspace, sized for the largest of them,
+ * may serve calls of every entry (hm_gemm, hm_moe_gemm, hm_moe_gemm_strided) and every size, in
+ * stream order. A call that stopped on a device error may leave counters raised: zero the
+ * workspace again before reusing it. */
 
 /* Y[M,N] (bf16) = X[M,K] * dequant(W)^T: the linear layer of the explainer page, section
  * "같은 가중치도 한 토큰과 많은 토큰에서 비용이 다르다" (weights W[N,K] read once and reused
@@ -275,9 +280,15 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
  * padding, belong to no expert and their y rows are not written). Offsets that decrease, are
  * negative, exceed rows or do not start at 0 set device error bit 2 and nothing is stored.
  * packed: device array of E device pointers, each a packed weight of the same (fmt, N, K).
- * Formats HM_W4A16_INT4, HM_W4A16_MXFP4 and HM_W4A16_MXINT4 (HM_ERR_UNSUPPORTED otherwise: the
- * block-scaled formats take their experts at a fixed stride, hm_moe_gemm_strided). Experts with no
- * rows cost nothing. */
+ * Formats HM_W4A16_INT4 (every group size), HM_W4A16_MXFP4, HM_W4A16_MXINT4 and HM_W8A16_INT8
+ * (HM_ERR_UNSUPPORTED otherwise: the block-scaled formats take their experts at a fixed stride,
+ * hm_moe_gemm_strided). Experts with no rows cost nothing.
+ * ws: hm_moe_workspace_size(fmt, rows, E, N, K) bytes, 16-byte aligned, zero-filled once after
+ * allocation (the library leaves it at zero after every call). With E <= 256 and at most 2 rows per
+ * expert on average (decode-sized batches) the call runs the grouped decode kernel: warp-level bf16
+ * MMA over every expert's (16-row token tile, weight tile, 128-K block) units cut into one range per
+ * SM, output tiles split along K summed in a fixed order through ws (deterministic). Otherwise, or
+ * when ws is NULL or smaller, the grouped tcgen05 kernel runs (it needs no workspace). */
 hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets, int32_t E,
                       const void* const* packed, void* y, int64_t rows, int64_t N, int64_t K,
                       void* ws, size_t ws_bytes, void* stream);
@@ -298,8 +309,10 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
  *          tensor scale gX = fp32(amax(x)/2688) over all rows and e4m3 scales per 16, the scale atoms
  *          laid out per expert token tile; Y = gX * gW_e * sum ... with gW_e from expert e's header.
  *  expert_offsets, rows, y: as hm_moe_gemm. E <= 1024 (W4A16), <= 256 (W4A8, W4A4).
- *  ws: hm_moe_workspace_size(fmt, rows, E, N, K) bytes (0 for the W4A16 formats and for W4A8 with
- *      x_scale given); need not be zeroed.
+ *  ws: hm_moe_workspace_size(fmt, rows, E, N, K) bytes. W4A16 formats: as hm_moe_gemm (the grouped
+ *      decode kernel's partials and counters; zero-filled once after allocation; NULL runs the
+ *      tcgen05 kernel). W4A8 and W4A4: the activations quantized inside the call (0 bytes for W4A8
+ *      with x_scale given); need not be zeroed.
  * Returns HM_ERR_INVALID_ARG for bad sizes, strides or pointers, HM_ERR_UNSUPPORTED for W4A4 with
  * x_scale or K % 256 != 0, HM_ERR_WORKSPACE, HM_ERR_CUDA. One launch (plus the activation
  * quantization); tiles m-major within each expert; experts with no rows cost nothing. */

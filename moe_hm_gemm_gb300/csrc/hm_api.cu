@@ -313,11 +313,9 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
 bool plan_fits(const Plan& p) { return p.tiles * p.kb_total < (int64_t{1} << 31); }
 
 // HM_LOG=1: one line on stderr per planned call with the configuration it runs (for sweeps and
-// for checking which kernel a layer takes); off by default.
-bool log_on() {
-  static const bool on = env_int("HM_LOG", 0) != 0;
-  return on;
-}
+// for checking which kernel a layer takes); off by default. Read at every call, so a process may
+// switch it on and off.
+bool log_on() { return env_int("HM_LOG", 0) != 0; }
 
 void log_plan(const char* entry, int32_t fmt, int64_t m, int64_t n, int64_t k, const Plan& p) {
   if (!log_on()) return;
@@ -336,8 +334,15 @@ struct WsLayout {
   size_t partial, counters, act_q, act_s, act_g, act_amax, total;
 };
 
+// Arrival counters of stream-K tiles, one block per owner CTA ([CTA][kCounterSlots]), at the
+// start of every workspace with the same size for every problem and entry: the partials and
+// activations of any call start after them, so calls of any size and entry may share a workspace
+// (each call leaves the counters at zero).
+constexpr size_t kCounterBytes =
+    (static_cast<size_t>(kMaxSmsForSizing) * kMxCtasPerSm * kCounterSlots * sizeof(uint32_t) + 255) / 256 * 256;
+
 // The workspace must fit whatever plan any device picks: size the stream-K partials for the
-// widest token tile and the counters for the most tiles the planner can choose for this M.
+// widest token tile the planner can choose for this M.
 WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_act) {
   int widest = tile_m_for(fmt, m, n, 1);          // one SM: the widest choice
   int narrowest = tile_m_for(fmt, m, n, 1 << 30);
@@ -347,16 +352,12 @@ WsLayout ws_layout(int32_t fmt, int64_t m, int64_t n, int64_t k, bool internal_a
     if (cover > widest) widest = cover;
   }
   if (narrowest > widest) widest = narrowest;
-  const int64_t max_tiles = ceil_div(m > 0 ? m : 1, narrowest < widest ? narrowest : widest) * (pad_n(n) / 128);
   WsLayout w{};
-  size_t off = 0;
+  w.counters = 0;
+  size_t off = kCounterBytes;
   w.partial = off;
   const size_t max_ctas = static_cast<size_t>(kMaxSmsForSizing) * ((fmt == kW4A8Mx || fmt == kW4A4Nv) ? kMxCtasPerSm : 1);
   off += align_up(max_ctas * 2 * widest * 128 * sizeof(float));
-  w.counters = off;
-  const int64_t counters = m <= kGemvMaxTokens ? std::max<int64_t>(max_tiles * 4, (pad_n(n) / 128) * kGemvCounters)
-                                               : max_tiles * 4;
-  off += align_up(static_cast<size_t>(counters) * sizeof(uint32_t));
   w.act_q = w.act_s = w.act_g = w.act_amax = off;
   if (internal_act && fmt == kW4A8Mx) {
     w.act_q = off;
@@ -441,7 +442,9 @@ bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int to
 }
 
 // Token tile of the grouped GEMM from the mean rows per expert (per-expert counts stay on the
-// device); HM_MOE_TILE_M overrides. Block-scaled formats stop at 128.
+// device); HM_MOE_TILE_M overrides. Block-scaled formats stop at 128. Past 256 rows per expert the
+// 256-token tile's halved dequant work per FLOP outweighs its padding of the smaller experts
+// (measured: T = 16384, E = 256, top-8 runs 20 % faster than with 128).
 int moe_tile_m(int32_t fmt, int64_t rows, int32_t E) {
   const int64_t mean = rows / E;
   int t = mean <= 16 ? 16 : (mean <= 32 ? 32 : (mean <= 64 ? 64 : (mean <= 256 ? 128 : 256)));
@@ -452,15 +455,41 @@ int moe_tile_m(int32_t fmt, int64_t rows, int32_t E) {
   return t;
 }
 
-// Workspace of the grouped block-scaled GEMM with bf16 activations quantized inside the call.
+// Grouped W4A16 layers with few rows per expert run on the grouped decode kernel: up to 8 rows per
+// expert on average it streams the experts' weights faster than the tcgen05 kernel's 16-row tile
+// (measured, E = 256 top-8 gate-up and down layers: 1.2-1.3x at T = 16, on par at T = 256).
+// HM_MOE_GEMV=0 / 1 forces the choice (given the workspace the decode kernel needs).
+bool moe_use_gemv(int32_t fmt, int64_t rows, int32_t E) {
+  if (!unit_fmt(fmt) || E > kGemvMoeMaxExperts) return false;
+  const int forced = env_int("HM_MOE_GEMV", -1);
+  if (forced == 0 || forced == 1) return forced == 1;
+  return rows <= 8 * static_cast<int64_t>(E);
+}
+
+// Token rows per tile of the grouped decode kernel: 8 halves the MMA work per weight unit, 16 reads
+// an expert's weights once for up to 16 rows; HM_MOE_GEMV_TOKENS=8 / 16 forces it.
+int moe_gemv_tokens(int64_t rows, int32_t E) {
+  const int forced = env_int("HM_MOE_GEMV_TOKENS", 0);
+  if (forced == 8 || forced == 16) return forced;
+  return rows <= 2 * static_cast<int64_t>(E) ? 8 : 16;
+}
+
+// Workspace of the grouped GEMM: the decode kernel's split partials and tile counters (W4A16
+// formats), or the block-scaled formats' activations quantized inside the call.
 struct MoeWs {
-  size_t act_q, act_s, act_g, act_amax, slots, total;
+  size_t partial, counters, act_q, act_s, act_g, act_amax, slots, total;
   int64_t max_blocks;
 };
-MoeWs moe_ws_layout(int32_t fmt, int64_t rows, int32_t E, int64_t k) {
+MoeWs moe_ws_layout(int32_t fmt, int64_t rows, int32_t E, int64_t n, int64_t k) {
   MoeWs w{};
-  size_t off = 0;
-  if (fmt == kW4A8Mx) {
+  w.counters = 0;
+  size_t off = kCounterBytes;   // (the counters' place in every workspace)
+  (void)n;
+  if (unit_fmt(fmt) && E <= kGemvMoeMaxExperts) {
+    // the decode kernel's [CTA][token][row] fp32 partials
+    w.partial = off;
+    off += align_up(static_cast<size_t>(kMaxSmsForSizing) * kGemvMoeTokens * 128 * sizeof(float));
+  } else if (fmt == kW4A8Mx) {
     w.act_q = off;
     off += align_up(static_cast<size_t>(rows) * k);
     w.act_s = off;
@@ -479,8 +508,53 @@ MoeWs moe_ws_layout(int32_t fmt, int64_t rows, int32_t E, int64_t k) {
     w.slots = off;
     off += align_up(static_cast<size_t>(rows) * sizeof(int32_t));
   }
-  w.total = off;
+  w.total = off == kCounterBytes ? 0 : off;   // (nothing needed: no workspace)
   return w;
+}
+
+// Grouped W4A16 GEMM over expert-sorted rows: the experts' packed weights from a device pointer
+// array (list) or at base + e * stride. The grouped decode kernel when moe_use_gemv says so and
+// the workspace holds its partials and counters, else the tcgen05 kernel with the token tile of
+// moe_tile_m.
+hm_status moe_w4a16(int32_t fmt, const void* x, const int32_t* offsets, int32_t E, const uint8_t* const* list,
+                    const uint8_t* base, int64_t stride, void* y, int64_t rows, int64_t N, int64_t K, void* ws,
+                    size_t ws_bytes, const DeviceInfo& di, cudaStream_t st, const char* entry) {
+  // The device-side tile count is at most rows/8 + 1 + E token tiles (of 8 rows or more) per weight tile.
+  if ((rows / 8 + 1 + E) * (pad_n(N) / 128) * (K / 128) >= (int64_t{1} << 31)) return HM_ERR_UNSUPPORTED;
+  const MoeWs wl = moe_ws_layout(fmt, rows, E, N, K);
+  const bool gemv = moe_use_gemv(fmt, rows, E) && ws != nullptr && ws_bytes >= wl.total && aligned(ws, 16) &&
+                    di.num_sms <= kMaxSmsForSizing;
+  const int tile_m = gemv ? moe_gemv_tokens(rows, E) : moe_tile_m(fmt, rows, E);
+  if (log_on())
+    std::fprintf(stderr, "[hm] %s fmt=%d E=%d rows=%lld N=%lld K=%lld kernel=%s tile_m=%d grid=%d\n", entry, fmt, E,
+                 static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K),
+                 gemv ? "decode" : "tcgen05", tile_m, di.num_sms);
+  F16Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (gemv ? !encode_x_gemv(&prm.tmap_x, x, K, rows, tile_m) : !encode_x_f16(&prm.tmap_x, x, K, rows, tile_m))
+    return HM_ERR_CUDA;
+  prm.packed = base;
+  prm.packed_list = list;
+  prm.expert_stride = stride;
+  prm.offsets = offsets;
+  prm.y = static_cast<__nv_bfloat16*>(y);
+  prm.err = di.err;
+  prm.m = rows;
+  prm.n = N;
+  prm.k = K;
+  prm.fmt = fmt;
+  prm.num_experts = E;
+  prm.num_m_tiles = 0;
+  prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
+  prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, gemv ? 1 : 0};
+  prm.timeout_ns = timeout_ns();
+  if (gemv) {
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    prm.partial = reinterpret_cast<float*>(wsb + wl.partial);
+    prm.counters = reinterpret_cast<uint32_t*>(wsb + wl.counters);
+    return cuda_status(launch_gemv_moe(prm, tile_m, st));
+  }
+  return cuda_status(launch_f16_gemm(prm, tile_m, true, st));
 }
 
 }  // namespace
@@ -753,41 +827,15 @@ hm_status hm_moe_gemm(int32_t fmt, const void* x, const int32_t* expert_offsets,
   if (rows == 0) return HM_OK;
   if (x == nullptr || expert_offsets == nullptr || packed == nullptr || y == nullptr) return HM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 4) || (N % 2) != 0 || !aligned(packed, 8)) return HM_ERR_INVALID_ARG;
-  (void)ws;
-  (void)ws_bytes;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
-  // The device-side tile count is at most ceil(rows/16) + E tiles of 16 per n-tile.
-  if ((rows / 16 + 1 + E) * (pad_n(N) / 128) * (K / 128) >= (int64_t{1} << 31)) return HM_ERR_UNSUPPORTED;
-  // Token tile from the mean rows per expert (per-expert counts stay on the device); past 256 rows
-  // per expert the 256-token tile's halved dequant work per FLOP outweighs its padding of the
-  // smaller experts (measured: T=16384, E=256, top-8 runs 20 % faster than with 128).
-  const int tile_m = moe_tile_m(fmt, rows, E);
-  if (log_on())
-    std::fprintf(stderr, "[hm] hm_moe_gemm fmt=%d E=%d rows=%lld N=%lld K=%lld kernel=tcgen05 tile_m=%d grid=%d\n", fmt, E,
-                 static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K), tile_m, di.num_sms);
-  F16Params prm;
-  std::memset(&prm, 0, sizeof(prm));
-  if (!encode_x_f16(&prm.tmap_x, x, K, rows, tile_m)) return HM_ERR_CUDA;
-  prm.packed_list = reinterpret_cast<const uint8_t* const*>(packed);
-  prm.offsets = expert_offsets;
-  prm.y = static_cast<__nv_bfloat16*>(y);
-  prm.err = di.err;
-  prm.m = rows;
-  prm.n = N;
-  prm.k = K;
-  prm.fmt = fmt;
-  prm.num_experts = E;
-  prm.num_m_tiles = 0;
-  prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
-  prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
-  prm.timeout_ns = timeout_ns();
-  return cuda_status(launch_f16_gemm(prm, tile_m, true, cudaStream_t(stream)));
+  return moe_w4a16(fmt, x, expert_offsets, E, reinterpret_cast<const uint8_t* const*>(packed), nullptr, 0, y, rows, N,
+                   K, ws, ws_bytes, di, cudaStream_t(stream), "hm_moe_gemm");
 }
 
 size_t hm_moe_workspace_size(int32_t fmt, int64_t rows, int32_t E, int64_t N, int64_t K) {
   if (!valid_fmt(fmt) || rows < 0 || E < 1 || N <= 0 || !valid_k(fmt, K)) return 0;
-  return moe_ws_layout(fmt, rows, E, K).total;
+  return moe_ws_layout(fmt, rows, E, N, K).total;
 }
 
 hm_status hm_moe_gemm_strided(int32_t fmt, const void* x, const void* x_scale, const int32_t* expert_offsets, int32_t E,
@@ -805,36 +853,18 @@ hm_status hm_moe_gemm_strided(int32_t fmt, const void* x, const void* x_scale, c
   const bool bs = fmt == kW4A8Mx || fmt == kW4A4Nv;
   if (fmt == kW4A4Nv && (x_scale != nullptr || K % 256 != 0)) return HM_ERR_UNSUPPORTED;
   if (bs && E > kMxMoeMaxExperts) return HM_ERR_UNSUPPORTED;
-  const MoeWs wl = moe_ws_layout(fmt, rows, E, K);
+  const MoeWs wl = moe_ws_layout(fmt, rows, E, N, K);
   if (bs && x_scale == nullptr && (ws == nullptr || ws_bytes < wl.total)) return HM_ERR_WORKSPACE;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!bs)
+    return moe_w4a16(fmt, x, expert_offsets, E, nullptr, static_cast<const uint8_t*>(packed), expert_stride, y, rows,
+                     N, K, ws, ws_bytes, di, st, "hm_moe_gemm_strided");
   const int tile_m = moe_tile_m(fmt, rows, E);
   if (log_on())
     std::fprintf(stderr, "[hm] hm_moe_gemm_strided fmt=%d E=%d rows=%lld N=%lld K=%lld tile_m=%d\n", fmt, E,
                  static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K), tile_m);
-  if (!bs) {
-    if ((rows / 16 + 1 + E) * (pad_n(N) / 128) * (K / 128) >= (int64_t{1} << 31)) return HM_ERR_UNSUPPORTED;
-    F16Params prm;
-    std::memset(&prm, 0, sizeof(prm));
-    if (!encode_x_f16(&prm.tmap_x, x, K, rows, tile_m)) return HM_ERR_CUDA;
-    prm.packed = static_cast<const uint8_t*>(packed);
-    prm.packed_list = nullptr;
-    prm.expert_stride = expert_stride;
-    prm.offsets = expert_offsets;
-    prm.y = static_cast<__nv_bfloat16*>(y);
-    prm.err = di.err;
-    prm.m = rows;
-    prm.n = N;
-    prm.k = K;
-    prm.fmt = fmt;
-    prm.num_experts = E;
-    prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
-    prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, 0};
-    prm.timeout_ns = timeout_ns();
-    return cuda_status(launch_f16_gemm(prm, tile_m, true, st));
-  }
   const int64_t n_pad = pad_n(N), k_pad = pad_k(fmt, K);
   if ((rows / 16 + 1 + E) * (n_pad / 128) * (k_pad / (fmt == kW4A4Nv ? 256 : 128)) >= (int64_t{1} << 31))
     return HM_ERR_UNSUPPORTED;
@@ -916,28 +946,27 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   const Plan p = make_plan(fmt, M, N, K, di.num_sms);
   log_plan("hm_gemm_w4a16_noalloc", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
-  // Partials for the CTAs of this launch, then the per-tile arrival counters. Only a plan that
-  // shares tiles between CTAs touches them: without stream-K, or with stream-K ranges that cover
-  // whole tiles (as many CTAs as tiles, or a whole number of tiles per CTA), every CTA owns its
-  // tiles outright and the call needs no scratch at all.
+  // The arrival counters of this launch's CTAs, then their partials. Only a plan that shares tiles
+  // between CTAs touches them: without stream-K, or with stream-K ranges that cover whole tiles (as
+  // many CTAs as tiles, or a whole number of tiles per CTA), every CTA owns its tiles outright and
+  // the call needs no scratch at all.
   const bool shared = p.stream_k && (p.grid > p.tiles || p.tiles % p.grid != 0);
+  const size_t counter_bytes = shared ? align_up(static_cast<size_t>(p.grid) * kCounterSlots * sizeof(uint32_t)) : 0;
   const size_t partial_bytes =
       shared ? align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float)) : 0;
-  const size_t counter_bytes =
-      shared ? align_up(static_cast<size_t>(p.tiles) * (p.gemv ? kGemvCounters : 4) * sizeof(uint32_t)) : 0;
   if (partial_bytes + counter_bytes > kNoAllocScratchBytes) return HM_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The counters must start at zero; clear them on every call (cheap, and safe even after a
   // call that stopped early on a device error).
-  if (shared && cudaMemsetAsync(scratch + partial_bytes, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
+  if (shared && cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
   if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
     return HM_ERR_CUDA;
   prm.packed = static_cast<const uint8_t*>(packed);
   prm.y = static_cast<__nv_bfloat16*>(y);
-  prm.partial = reinterpret_cast<float*>(scratch);
-  prm.counters = reinterpret_cast<uint32_t*>(scratch + partial_bytes);
+  prm.counters = reinterpret_cast<uint32_t*>(scratch);
+  prm.partial = reinterpret_cast<float*>(scratch + counter_bytes);
   prm.err = di.err;
   prm.m = M;
   prm.n = N;

@@ -142,7 +142,8 @@ __device__ __forceinline__ void store_segment(const F16Params& p, const TileInfo
     for (int j = 0; j < BT; ++j) emit(j, acc[j]);
     return;
   }
-  uint32_t* flag = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+  uint32_t* flag = sk_flag(p.counters, seg.kb0 == 0 ? blockIdx.x : sk_tile_owner(seg.tile, kb_total, total_it,
+                                                                                 p.sched.grid), q);
   if (seg.kb0 != 0) {
     float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                   static_cast<size_t>(row) * BT;

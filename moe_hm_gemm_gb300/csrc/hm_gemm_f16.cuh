@@ -580,7 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
       // others' published partials and adds them to its own accumulator; the others publish.
       const bool owner = !full && seg.kb0 == 0;
-      uint32_t* flag = p.counters + static_cast<size_t>(seg.tile) * 4 + q;
+      uint32_t* flag = full ? nullptr
+                            : sk_flag(p.counters, owner ? blockIdx.x
+                                                        : sk_tile_owner(seg.tile, kb_total, total_it, p.sched.grid), q);
       int64_t c_hi = 0;
       bool have = true;
       if (owner) {

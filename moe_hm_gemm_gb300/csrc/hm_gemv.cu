@@ -77,7 +77,7 @@ __host__ __device__ constexpr int v_consumers(int mt) { return 8 * v_par(mt); }
 __host__ __device__ constexpr int v_meta_warp(int mt) { return kVCons0 + v_consumers(mt); }
 __host__ __device__ constexpr int v_threads(int mt) { return 32 * (v_meta_warp(mt) + 1); }
 
-template <int MT, int WB = 8704>
+template <int MT, int WB = 8704, bool MOE = false>
 struct VShape {
   static constexpr int kNQ = MT / 8;                // token groups of 8 (MMA N)
   static constexpr int kWBytes = WB;                // one unit (the largest of the formats served)
@@ -97,9 +97,11 @@ struct VShape {
   static constexpr int kXchgBytes = 4 * (2 * kPar - 1) * 32 * kXchgFloats * 4;
   // cluster hand-off of a shared tile: [rank 1..3][row pair][lane][2 tiles x 4 x kNQ floats] in
   // the owner CTA (rank 0)
-  static constexpr int kRedBytes = 3 * 4 * 32 * kXchgFloats * 4;
+  static constexpr int kRedBytes = MOE ? 0 : 3 * 4 * 32 * kXchgFloats * 4;   // (no clusters when grouped)
   // as many stages (even, at most 16) as the 227 KB per CTA leave beside the fixed parts
-  static constexpr int kFixed = kXchgBytes + kRedBytes + (3 * 16 + 3 * 4) * 8 + 64 + 16 * 4 + 128;
+  // grouped (MoE) variant: expert offsets [E+1] and token-tile prefix [E+1]
+  static constexpr int kMoeBytes = MOE ? 2 * (kGemvMoeMaxExperts + 1) * 4 : 0;
+  static constexpr int kFixed = kXchgBytes + kRedBytes + (3 * 16 + 3 * 4) * 8 + 64 + 16 * 4 + 128 + kMoeBytes;
   static constexpr int kSFit = (232448 - kFixed) / kStage;
   static constexpr int kS = (kSFit > 16 ? 16 : kSFit) & ~1;
   static_assert(kS % kPar == 0, "a stage always holds units of one parity");
@@ -108,7 +110,8 @@ struct VShape {
   static constexpr int kBarOff = kRedOff + kRedBytes;
   static constexpr int kNumBars = 3 * kS + 3 * 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmem = kMiscOff + 64 + 16 * 4 + 128;   // + e2m1 table, alignment slack
+  static constexpr int kMoeOff = kMiscOff + 64 + 16 * 4;
+  static constexpr int kSmem = kMoeOff + kMoeBytes + 128;   // + e2m1 table, MoE arrays, alignment slack
   static_assert(kS >= 4, "pipeline depth");
   static_assert(kWBytes % 128 == 0 && kStage % 128 == 0, "TMA destinations 128-byte aligned");
   static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -191,9 +194,10 @@ __host__ __device__ constexpr int v_wbytes(int wk) { return wk == 8 ? 16768 : (w
 // 6 = INT4 with a bf16 scale (and zero-point) per 32-K chunk, applied to each chunk's sum;
 // 8 = INT8 (one byte per code, bf16 scale and u8 zero-point per row and 128-K block), restored to the
 // exact integers u - z and scaled after the block's sum like INT4.
-template <int MT, int WK>
+// MOE: the grouped variant over expert-sorted rows (token tiles of MT rows per expert).
+template <int MT, int WK, bool MOE>
 __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_constant__ F16Params p) {
-  using S = VShape<MT, v_wbytes(WK)>;
+  using S = VShape<MT, v_wbytes(WK), MOE>;
   constexpr bool MX = WK == 2 || WK == 3;
   constexpr bool G32 = WK == 6;
   constexpr int SL = S::kS;
@@ -212,19 +216,21 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
   float* lut = reinterpret_cast<float*>(smem + S::kMiscOff + 64);
   float* xchg = reinterpret_cast<float*>(smem + S::kXchgOff);
   float* red = reinterpret_cast<float*>(smem + S::kRedOff);
-  const int csize = p.cluster > 1 ? p.cluster : 1;
+  int32_t* mtpre = reinterpret_cast<int32_t*>(smem + S::kMoeOff);      // MoE: tile prefix [E+1]
+  int32_t* moffs = mtpre + kGemvMoeMaxExperts + 1;                      // MoE: expert offsets [E+1]
+  const int csize = (!MOE && p.cluster > 1) ? p.cluster : 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int32_t kb_total = p.sched.kb_total;
-  const int64_t total = static_cast<int64_t>(p.sched.num_tiles) * kb_total;
-  const int32_t grid = p.sched.grid;
-  const int32_t u0 = static_cast<int32_t>(sk_start(blockIdx.x, total, grid));
-  const int32_t u1 = static_cast<int32_t>(sk_start(blockIdx.x + 1, total, grid));
-  const int32_t n_units = u1 - u0;
-  const int32_t tile0 = u0 / kb_total, kb0 = u0 - tile0 * kb_total;
   const int m_rows = static_cast<int>(p.m);
 
+  if (MOE) {
+    // The MoE set-up warp may raise the abort flag while thread 0 is still setting up: clear the
+    // flag before any role runs, so that a raised flag is never overwritten.
+    if (threadIdx.x == 0) *abort_flag = 0u;
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     trace_mark(p.trace, 0);
     if (p.trace != nullptr) {
@@ -243,8 +249,13 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
       mbar_init(&red_full[q], csize > 1 ? csize - 1 : 1);
     }
     fence_barrier_init();
-    const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(p.packed);
-    *abort_flag = 0u;
+    // (MoE: the expert pointers may come from the previous kernel; the first expert's header
+    // decides whether the units carry zero-points, and the set-up warp checks every expert's
+    // header against it)
+    if (MOE) pdl_wait();
+    const uint8_t* first_w = (MOE && p.packed_list != nullptr) ? p.packed_list[0] : p.packed;
+    const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first_w);
+    if (!MOE) *abort_flag = 0u;
     *hz_sh = hdr.has_zero == 1u ? 1u : 0u;
     if (!(hdr.magic == kMagic && static_cast<int32_t>(hdr.fmt) == p.fmt && hdr.n == p.n && hdr.k == p.k)) {
       atomicOr(p.err, kErrHeader);
@@ -252,7 +263,39 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     }
   }
   if (WK == 2 && threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
+  if (MOE && warp == v_meta_warp(MT)) {
+    // Every expert's header against the call and the first expert's zero-point flag (strided
+    // weights before the wait for the previous kernel: they never depend on it; a pointer list
+    // after it), then the expert offsets (which the previous kernel may write) -> token tiles of
+    // MT rows per expert x weight tiles, exclusive prefix over the experts. A header that does not
+    // match or malformed offsets set the error word and abort every CTA before any weight is read.
+    const bool list = p.packed_list != nullptr;
+    if (list) pdl_wait();
+    const uint32_t hz0 = reinterpret_cast<const PackedHeader*>(list ? p.packed_list[0] : p.packed)->has_zero;
+    bool bad_hdr = false;
+    for (int e = lane; e < p.num_experts; e += 32) {
+      const uint8_t* w = list ? p.packed_list[e] : p.packed + static_cast<size_t>(e) * p.expert_stride;
+      bad_hdr |= !header_ok(w, p, hz0 == 1u ? 1u : 0u);
+    }
+    pdl_wait();
+    moe_tile_prefix<MT>(p, moffs, mtpre, abort_flag, lane);
+    if (__any_sync(0xffffffffu, bad_hdr) && lane == 0) {
+      atomicOr(p.err, kErrHeader);
+      *abort_flag = 1u;
+    }
+  }
   __syncthreads();
+  // this CTA's range of the (tile, k-block) space (MoE: the tile count comes from the offsets)
+  // (MoE: the launch has one CTA per SM whatever the offsets; with fewer units than CTAs only the
+  // first `total` CTAs take one each, so that every CTA between a shared tile's owner and its last
+  // contributor holds a part of it, which the owner's arrival count relies on)
+  const int64_t total = static_cast<int64_t>(MOE ? mtpre[p.num_experts] : p.sched.num_tiles) * kb_total;
+  const int32_t grid = MOE ? static_cast<int32_t>(total < p.sched.grid ? total : p.sched.grid) : p.sched.grid;
+  const bool idle = static_cast<int32_t>(blockIdx.x) >= grid;
+  const int32_t u0 = idle ? 0 : static_cast<int32_t>(sk_start(blockIdx.x, total, grid));
+  const int32_t u1 = idle ? 0 : static_cast<int32_t>(sk_start(blockIdx.x + 1, total, grid));
+  const int32_t n_units = u1 - u0;
+  const int32_t tile0 = u0 / kb_total, kb0 = u0 - tile0 * kb_total;
   // Cluster barrier, two phases, each split into an arrive and a wait per thread: phase 1 makes the
   // owner's barriers initialised before another CTA of its cluster arrives on them (every thread
   // arrives here, a publishing warp waits just before its first remote access, the others at
@@ -279,50 +322,93 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
     const uint8_t* wsrc = p.packed + kHeaderBytes + static_cast<size_t>(u0) * kUnit;
     const uint32_t stage_bytes = kUnit + static_cast<uint32_t>(S::kXBytes);
     const int first = n_units < SL ? n_units : SL;
-    // Start-up, one stage per lane (a single thread takes ~70 ns per bulk-copy issue): the weights
-    // of the first few stages before waiting for the previous kernel (weights are never written
-    // by another kernel), then, after the wait, their activation blocks, and only then the rest of
-    // the first stages, weights and activations. The TMA unit works through its copies roughly in
-    // issue order, so the first stages complete without queueing behind the whole ring's weights.
-    constexpr int kEarly = 4;
-    const int early = first < kEarly ? first : kEarly;
-    if (lane < early) {
-      mbar_arrive_expect_tx(&full[lane], stage_bytes);
-      bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
-    }
-    if (lane == 0) {
-      trace_mark(p.trace, 2);
-      prefetch_tmap(&p.tmap_x);
-    }
-    const uint64_t pol_x = policy_evict_last();
-    pdl_wait();
-    if (lane == 0) trace_mark(p.trace, 5);
-    const int kb_lane = (kb0 + lane) % kb_total;   // k-block of stage `lane`
-    if (lane < early) tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
-    __syncwarp();
-    if (lane >= early && lane < first) {
-      mbar_arrive_expect_tx(&full[lane], stage_bytes);
-      bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
-      tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      int kb = (kb0 + first) % kb_total;
-      int issued = first, s = 0;
-      uint32_t ph = 0;
-      for (int i = first; i < n_units; ++i) {
-        if (!mbar_wait(&empty[s], ph, wc)) break;
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        bulk_g2s(smem + s * S::kStage, wsrc + static_cast<size_t>(i) * kUnit, kUnit, &full[s], pol_w);
-        tma_2d_g2s(smem + s * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, 0, &full[s], pol_x);
-        if (++kb == kb_total) kb = 0;
-        issued = i + 1;
-        if (++s == SL) { s = 0; ph ^= 1u; }
+    if constexpr (MOE) {
+      // Grouped: unit i of the range is k-block (kb0 + i) % kb of tile tile0 + (kb0 + i) / kb, whose
+      // expert, weight tile and first token row come from the prefix (token rows of the box past the
+      // expert's end belong to the next expert or read as zeros; their sums are never stored). Every
+      // header was checked in the set-up. The first stages one per lane, then lane 0.
+      const uint64_t pol_x = policy_evict_last();
+      if (lane == 0) prefetch_tmap(&p.tmap_x);
+      if (lane < first) {
+        const int kb_l = (kb0 + lane) % kb_total;
+        const TileInfo t0 = decode_tile<MT, true>(p, tile0 + (kb0 + lane) / kb_total, mtpre, moffs, kUnit);
+        mbar_arrive_expect_tx(&full[lane], stage_bytes);
+        bulk_g2s(smem + lane * S::kStage, t0.wbase + static_cast<size_t>(kb_l) * kUnit, kUnit, &full[lane], pol_w);
+        tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_l * 128, t0.m0, &full[lane], pol_x);
       }
-      trace_mark(p.trace, 3);
-      // nothing may still be landing in shared memory when the CTA exits
-      for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
-        drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
+      __syncwarp();
+      if (lane == 0) {
+        int issued = first;
+        if (first < n_units) {
+          int32_t tl = tile0 + (kb0 + first) / kb_total;
+          int kb = (kb0 + first) % kb_total;
+          TileInfo t = decode_tile<MT, true>(p, tl, mtpre, moffs, kUnit);
+          int s = 0;
+          uint32_t ph = 0;
+          for (int i = first; i < n_units; ++i) {
+            if (!mbar_wait(&empty[s], ph, wc)) break;
+            mbar_arrive_expect_tx(&full[s], stage_bytes);
+            bulk_g2s(smem + s * S::kStage, t.wbase + static_cast<size_t>(kb) * kUnit, kUnit, &full[s], pol_w);
+            tma_2d_g2s(smem + s * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, t.m0, &full[s], pol_x);
+            issued = i + 1;
+            if (++kb == kb_total && issued < n_units) {
+              kb = 0;
+              t = decode_tile<MT, true>(p, ++tl, mtpre, moffs, kUnit);
+            }
+            if (++s == SL) { s = 0; ph ^= 1u; }
+          }
+        }
+        trace_mark(p.trace, 3);
+        // nothing may still be landing in shared memory when the CTA exits
+        for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
+          drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
+      }
+    } else {
+      // Start-up, one stage per lane (a single thread takes ~70 ns per bulk-copy issue): the weights
+      // of the first few stages before waiting for the previous kernel (weights are never written
+      // by another kernel), then, after the wait, their activation blocks, and only then the rest of
+      // the first stages, weights and activations. The TMA unit works through its copies roughly in
+      // issue order, so the first stages complete without queueing behind the whole ring's weights.
+      constexpr int kEarly = 4;
+      const int early = first < kEarly ? first : kEarly;
+      if (lane < early) {
+        mbar_arrive_expect_tx(&full[lane], stage_bytes);
+        bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
+      }
+      if (lane == 0) {
+        trace_mark(p.trace, 2);
+        prefetch_tmap(&p.tmap_x);
+      }
+      const uint64_t pol_x = policy_evict_last();
+      pdl_wait();
+      if (lane == 0) trace_mark(p.trace, 5);
+      const int kb_lane = (kb0 + lane) % kb_total;   // k-block of stage `lane`
+      if (lane < early) tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
+      __syncwarp();
+      if (lane >= early && lane < first) {
+        mbar_arrive_expect_tx(&full[lane], stage_bytes);
+        bulk_g2s(smem + lane * S::kStage, wsrc + static_cast<size_t>(lane) * kUnit, kUnit, &full[lane], pol_w);
+        tma_2d_g2s(smem + lane * S::kStage + S::kWBytes, &p.tmap_x, kb_lane * 128, 0, &full[lane], pol_x);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int kb = (kb0 + first) % kb_total;
+        int issued = first, s = 0;
+        uint32_t ph = 0;
+        for (int i = first; i < n_units; ++i) {
+          if (!mbar_wait(&empty[s], ph, wc)) break;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          bulk_g2s(smem + s * S::kStage, wsrc + static_cast<size_t>(i) * kUnit, kUnit, &full[s], pol_w);
+          tma_2d_g2s(smem + s * S::kStage + S::kWBytes, &p.tmap_x, kb * 128, 0, &full[s], pol_x);
+          if (++kb == kb_total) kb = 0;
+          issued = i + 1;
+          if (++s == SL) { s = 0; ph ^= 1u; }
+        }
+        trace_mark(p.trace, 3);
+        // nothing may still be landing in shared memory when the CTA exits
+        for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
+          drain_wait(&full[i % SL], static_cast<uint32_t>(i / SL) & 1u, p.timeout_ns);
+      }
     }
   } else if (warp == v_meta_warp(MT)) {
     // ---------------------------------------------------------------- INT4 row metadata
@@ -438,11 +524,19 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
           }
       __syncwarp();
       if (lane == 0) mbar_arrive(&xfree[pr]);
-      const int64_t n0 = static_cast<int64_t>(tile) * 128;
+      // the tile's first weight row, first token row and token count (grouped: the expert's rows)
+      int64_t n0 = static_cast<int64_t>(tile) * 128, y0 = 0;
+      int tok_end = m_rows;
+      if constexpr (MOE) {
+        const TileInfo ti = decode_tile<MT, true>(p, tile, mtpre, moffs, kUnit);
+        n0 = ti.n0;
+        y0 = ti.m0;
+        tok_end = ti.m_end - ti.m0;
+      }
       auto store_y = [&](int j, int q, int e, float val) {
         const int tok = 8 * q + 2 * t + (e & 1);
         const int64_t row = n0 + rows[j][e >> 1];
-        if (tok < m_rows && row < p.n) p.y[static_cast<size_t>(tok) * p.n + row] = __float2bfloat16_rn(val);
+        if (tok < tok_end && row < p.n) p.y[static_cast<size_t>(y0 + tok) * p.n + row] = __float2bfloat16_rn(val);
       };
       if (seg_kb0 == 0 && seg_kb1 == kb_total) {
 #pragma unroll
@@ -501,7 +595,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
       // first segment) have published their fp32 partials [CTA][token][row].
       const int64_t it0 = static_cast<int64_t>(tile) * kb_total;
       const int64_t c_lo = sk_owner(it0, total, grid), c_hi = sk_owner(it0 + kb_total - 1, total, grid);
-      uint32_t* ctr = p.counters + static_cast<size_t>(tile) * kGemvCounters + pr;
+      uint32_t* ctr = sk_flag(p.counters, c_lo, pr);
       auto pidx = [&](int64_t c, int j, int q, int e) {
         const int tok = 8 * q + 2 * t + (e & 1);
         return static_cast<size_t>(c) * MT * 128 + static_cast<size_t>(tok) * 128 + rows[j][e >> 1];
@@ -770,7 +864,7 @@ __global__ void __launch_bounds__(v_threads(MT), 1) gemv_kernel(const __grid_con
 template <int MT, int WK>
 cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   using S = VShape<MT, v_wbytes(WK)>;
-  auto kern = gemv_kernel<MT, WK>;
+  auto kern = gemv_kernel<MT, WK, false>;
   static int configured[64] = {};
   static int cluster_max[64][kVMaxCluster + 1] = {};   // active clusters the device holds, +1 (0 unknown)
   int dev = 0;
@@ -826,6 +920,24 @@ cudaError_t launch_v(const F16Params& p_in, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Grouped variant: persistent CTAs over the stream-K range of all experts' (token tile, weight
+// tile, k-block) units; no clusters (the tile count is known only on the device).
+template <int MT, int WK>
+cudaError_t launch_vm(const F16Params& p, cudaStream_t st) {
+  using S = VShape<MT, v_wbytes(WK), true>;
+  auto kern = gemv_kernel<MT, WK, true>;
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  return launch_pdl(kern, p.sched.grid, v_threads(MT), S::kSmem, st, p);
+}
+
 }  // namespace
 
 int gemv_tokens(int64_t m) { return m <= 8 ? 8 : (m <= 16 ? 16 : 32); }
@@ -851,6 +963,20 @@ cudaError_t launch_gemv(const F16Params& p, cudaStream_t st) {
   if (p.fmt == kW8A16Int8)
     return t == 8 ? launch_v<8, 8>(p, st) : (t == 16 ? launch_v<16, 8>(p, st) : launch_v<32, 8>(p, st));
   return t == 8 ? launch_v<8, 0>(p, st) : (t == 16 ? launch_v<16, 0>(p, st) : launch_v<32, 0>(p, st));
+}
+
+cudaError_t launch_gemv_moe(const F16Params& p, int tokens, cudaStream_t st) {
+  if (p.num_experts < 1 || p.num_experts > kGemvMoeMaxExperts || p.k % 128 != 0 || (tokens != 8 && tokens != 16))
+    return cudaErrorInvalidValue;
+  const bool t8 = tokens == 8;
+  switch (p.fmt) {
+    case kW4A16Int4: return t8 ? launch_vm<8, 0>(p, st) : launch_vm<16, 0>(p, st);
+    case kW4A16Mx: return t8 ? launch_vm<8, 2>(p, st) : launch_vm<16, 2>(p, st);
+    case kW4A16MxInt: return t8 ? launch_vm<8, 3>(p, st) : launch_vm<16, 3>(p, st);
+    case kW4A16Int4G: return t8 ? launch_vm<8, 6>(p, st) : launch_vm<16, 6>(p, st);
+    case kW8A16Int8: return t8 ? launch_vm<8, 8>(p, st) : launch_vm<16, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace hm

@@ -22,7 +22,7 @@ struct F16Params {
   const int32_t* offsets;             // MoE: expert offsets [E+1]
   __nv_bfloat16* y;                   // [rows][N]
   float* partial;                     // stream-K partial tiles [grid][2][tile_m][128]
-  uint32_t* counters;                 // stream-K arrival counters [num_tiles][4]
+  uint32_t* counters;                 // stream-K arrival counters [grid][kCounterSlots], by owner CTA
   uint32_t* err;                      // device error word
   int64_t m, n, k;                    // m = rows
   int32_t fmt;
@@ -105,12 +105,19 @@ cudaError_t launch_f16s_gemm(const F16Params& p, int tile_m, bool moe, cudaStrea
 int f16s_stages(int tile_m);
 bool f16s_serves(int fmt, int tile_m);
 int mx_stages(int fmt, int tile_m);
-// W4A16 kernel for decode-sized M (hm_gemv.cu): INT4 or MXFP4 weights, up to 16 tokens, warp-level
-// bf16 MMA on registers, split over the packed units with a last-arriver hand-off of shared tiles.
+// W4A16 kernel for decode-sized M (hm_gemv.cu): the unit formats (INT4, MXFP4, MXINT4, INT4 in
+// groups of 32/64, INT8), up to 32 tokens, warp-level bf16 MMA on registers, split over the packed
+// units with a fixed-owner hand-off of shared tiles.
 // X comes as tmap_x, a 2-D map with box {128, gemv_tokens(M)} and no swizzle.
 constexpr int kGemvMaxTokens = 32;
-constexpr int kGemvCounters = 8;   // arrival counters per output tile (one per consumer warp)
+constexpr int kGemvMoeMaxExperts = 256;   // grouped decode kernel: experts it holds offsets for
+constexpr int kGemvMoeTokens = 16;        // grouped decode kernel: the most token rows per tile (8 or 16)
 cudaError_t launch_gemv(const F16Params& p, cudaStream_t st);
+// Grouped (MoE) decode kernel: expert-sorted rows, token tiles of `tokens` (8 or 16) rows per
+// expert, the (tile, k-block) space over all experts cut into one range per CTA (p.sched.grid CTAs;
+// the tile count comes from the device offsets); shared tiles hand off through p.partial /
+// p.counters.
+cudaError_t launch_gemv_moe(const F16Params& p, int tokens, cudaStream_t st);
 int gemv_tokens(int64_t m);
 int gemv_stages(int64_t m, int32_t fmt);
 

@@ -34,6 +34,21 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t it, int64_t total, 
   return c;
 }
 
+// Arrival counters of a shared tile belong to its owner CTA: a CTA owns at most one shared tile
+// (the last segment of its contiguous range), so [grid][kCounterSlots] counters serve every problem
+// size, and a workspace's counters never move with the problem (calls of any size and entry may
+// share one workspace: no call's partials or activations land on another call's counters).
+constexpr int kCounterSlots = 8;
+
+__device__ __forceinline__ uint32_t* sk_flag(uint32_t* counters, int64_t owner_cta, int slot) {
+  return counters + static_cast<size_t>(owner_cta) * kCounterSlots + slot;
+}
+
+// Owner CTA of `tile` (the one whose range holds its first k-block).
+__host__ __device__ __forceinline__ int64_t sk_tile_owner(int32_t tile, int32_t kb_total, int64_t total, int64_t g) {
+  return sk_owner(static_cast<int64_t>(tile) * kb_total, total, g);
+}
+
 struct Segment {
   int32_t tile;
   int32_t kb0;
@@ -92,8 +107,8 @@ struct SchedIter {
 // first k-block (segment with kb0 == 0). In forward stream-K order that is the last segment of
 // its range, while every other contributor holds the tile in the first segment of its own range,
 // so by the time the owner finishes, the others have long published. Non-owners store their
-// fp32 partial rows ([cta][first/last segment][row][tile_m]) and add 1 to the tile's per-warp
-// flag with release semantics, without waiting for anything; the owner waits (bounded) until the
+// fp32 partial rows ([cta][first/last segment][row][tile_m]) and add 1 to the owner's per-warp
+// flag (sk_flag) with release semantics, without waiting for anything; the owner waits (bounded) until the
 // flag shows all of them, adds their partials to its own in k order (CTA c_lo = itself first,
 // so the sum is deterministic), writes Y and clears the flag for the next call.
 

@@ -245,12 +245,13 @@ def alloc_workspace(fmt, m, n, k, device="cuda"):
 _WS_CACHE = {}
 
 
-def cached_workspace(fmt, m, n, k, device):
+def cached_workspace(fmt, m, n, k, device, need=None):
     """A zero-initialised workspace kept per (device, current stream) and grown on demand, so that
     calls without `ws` allocate only when a problem needs more than any earlier one did (the
     library leaves its counters at zero after every call, so the buffer is reused as it is).
-    Calls on one stream are ordered, so they may share it; other streams get their own."""
-    need = max(workspace_size(fmt, m, n, k), 256)
+    Calls on one stream are ordered, so they may share it; other streams get their own.
+    `need` (bytes) replaces the dense GEMM's size, e.g. hm_moe_workspace_size for the grouped GEMM."""
+    need = max(workspace_size(fmt, m, n, k) if need is None else int(need), 256)
     key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
     ws = _WS_CACHE.get(key)
     if ws is None or ws.numel() < need:
@@ -303,8 +304,8 @@ def moe_gemm_strided(fmt, x, offsets, packed, experts, stride, n, k, x_scale=Non
     rows = x.shape[0]
     y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (rows, n))
     if ws is None:
-        need = _lib.hm_moe_workspace_size(int(fmt), rows, int(experts), n, k)
-        ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=x.device)
+        ws = cached_workspace(fmt, rows, n, k, x.device,
+                              need=_lib.hm_moe_workspace_size(int(fmt), rows, int(experts), n, k))
     _check(_lib.hm_moe_gemm_strided(int(fmt), _ptr(x), _ptr(x_scale), _ptr(offsets), int(experts), _ptr(packed),
                                     int(stride), _ptr(y), rows, n, k, _ptr(ws), ws.numel(), _stream()),
            "hm_moe_gemm_strided")
@@ -312,16 +313,18 @@ def moe_gemm_strided(fmt, x, offsets, packed, experts, stride, n, k, x_scale=Non
 
 
 def moe_gemm(fmt, x, offsets, packed_ptrs, n, k, out=None, ws=None):
-    """x: expert-sorted rows [R,K] bf16; offsets int32 [E+1] (device); packed_ptrs int64 [E] (device)."""
+    """x: expert-sorted rows [R,K] bf16; offsets int32 [E+1] (device); packed_ptrs int64 [E] (device).
+    ws: a zero-initialised workspace of hm_moe_workspace_size bytes, by default the cached one."""
     _dev(("x", x), ("offsets", offsets), ("packed_ptrs", packed_ptrs), ("ws", ws))
     if offsets.dtype != torch.int32 or packed_ptrs.dtype != torch.int64 or packed_ptrs.numel() != offsets.numel() - 1:
         raise ValueError("offsets: int32 [E+1]; packed_ptrs: int64 [E]")
     rows = x.shape[0]
     e = offsets.numel() - 1
     y = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device) if out is None else _out(out, (rows, n))
-    wsz = 0 if ws is None else ws.numel()
+    if ws is None:
+        ws = cached_workspace(fmt, rows, n, k, x.device, need=_lib.hm_moe_workspace_size(int(fmt), rows, e, n, k))
     _check(_lib.hm_moe_gemm(int(fmt), _ptr(x), _ptr(offsets), e, _ptr(packed_ptrs), _ptr(y), rows, n, k,
-                            _ptr(ws), wsz, _stream()), "hm_moe_gemm")
+                            _ptr(ws), ws.numel(), _stream()), "hm_moe_gemm")
     return y
 
 

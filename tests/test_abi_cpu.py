@@ -393,6 +393,11 @@ def test_moe_strided_argument_checks(hm):
     # internal activation quantization needs the workspace
     assert lib.hm_moe_workspace_size(3, 8, 2, 256, 512) >= 8 * 512 + 8 * 4
     assert lib.hm_moe_gemm_strided(3, P(256), None, P(256), 2, P(256), st, P(256), 8, 256, 512, None, 0, None) == 3
-    assert lib.hm_moe_workspace_size(1, 8, 2, 256, 512) == 0
+    # W4A16: the grouped decode kernel's fp32 partials (up to 256 CTAs x 16 tokens x 128 rows) and
+    # 8 counters per (token tile, weight tile), at most rows / 16 + 1 + min(E, rows) token tiles;
+    # more than 256 experts run the tcgen05 kernel only, which needs none
+    assert lib.hm_moe_workspace_size(1, 8, 2, 256, 512) >= 256 * 16 * 128 * 4 + (0 + 1 + 2) * 2 * 8 * 4
+    assert lib.hm_moe_workspace_size(7, 8, 2, 256, 512) == lib.hm_moe_workspace_size(1, 8, 2, 256, 512)
+    assert lib.hm_moe_workspace_size(1, 8, 300, 256, 512) == 0
     # rows = 0 is a no-op
     assert lib.hm_moe_gemm_strided(3, None, None, None, 2, None, st, None, 0, 256, 512, None, 0, None) == 0

@@ -1,6 +1,6 @@
 """GPU parity at the benchmarked full sizes, on sampled outputs the oracle computes one by one:
 the grouped MoE gate-up (N = 4096, K = 7168) and down (N = 7168, K = 2048) layers (E = 256,
-T = 16384 tokens with top-8 Zipf(1.1) routing) in the W4A16 formats, and the dense MXINT4 layer
+T = 16384 and 16 tokens with top-8 Zipf(1.1) routing) in the W4A16 formats, and the dense MXINT4 layer
 14336 x 4096 at M = 1 and 8192.
 
 The weights and activations come from the seeded device generators the benchmark uses; the
@@ -37,10 +37,13 @@ def restore_rows(fmt, w_rows, z_rows):
     return oq.dequant_mxint4(*oq.quant_mxint4(w_rows))
 
 
+@pytest.mark.parametrize("t", [16384, 16])
 @pytest.mark.parametrize("layer", ["gate_up", "down"])
 @pytest.mark.parametrize("fmt", [1, 2, 5])
-def test_moe_full_size_sampled(hm, fmt, layer):
-    e, t = 256, 16384
+def test_moe_full_size_sampled(hm, fmt, layer, t):
+    """T = 16384 runs the grouped tcgen05 kernel, T = 16 (128 rows over 256 experts) the grouped
+    decode kernel."""
+    e = 256
     n, k = (4096, 7168) if layer == "gate_up" else (7168, 2048)
     _, expert_of_row, offsets = synth.moe_routing(t, experts=e, topk=8, seed=0)
     rows = int(offsets[-1])
