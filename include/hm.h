@@ -264,8 +264,9 @@ size_t hm_workspace_size(int32_t fmt, int64_t M, int64_t N, int64_t K);
  * Kernel per call (hm_plan reports it): tcgen05 tensor-core kernels, except the W4A16 formats at
  * decode sizes (M <= 16; 17..32 with MXFP4 and MXINT4, or with INT4 where tcgen05 would split
  * tiles along K),
- * which run on warp-level bf16 MMA with fp32 accumulation. Output tiles split along K are summed
- * in a fixed order, so a call is deterministic. */
+ * which run on warp-level bf16 MMA with fp32 accumulation (or, with HM_DECODE_TC=1, INT4 up to 16
+ * tokens on the tensor-core decode kernel). Output tiles split along K are summed in a fixed
+ * order, so a call is deterministic. */
 hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* x_global,
                   const void* packed, void* y, int64_t M, int64_t N, int64_t K, void* ws,
                   size_t ws_bytes, void* stream);
@@ -364,7 +365,8 @@ typedef struct hm_plan_info {
   int32_t kernel;      /* 0: tcgen05 tensor-core kernel; 1: decode kernel (W4A16 formats; warp-level
                           bf16 MMA with fp32 accumulation in registers) for M <= 16, and for
                           17 <= M <= 32 with MXFP4 / MXINT4 or where tcgen05 would split tiles
-                          along K */
+                          along K; 2: tensor-core decode kernel (INT4, M <= 16, restored weights
+                          in TMEM), taken only with HM_DECODE_TC=1 in the environment */
 } hm_plan_info;
 hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
                   hm_plan_info* out);

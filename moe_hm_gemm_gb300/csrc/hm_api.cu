@@ -137,7 +137,9 @@ struct Plan {
   int64_t num_m_tiles;
   int64_t num_n_tiles;
   int64_t kb_total;
-  int gemv;   // 1: the CUDA-core decode kernel (tile_m = tokens it is built for)
+  int gemv;   // 1: a decode kernel (tile_m = tokens it is built for)
+  int tc;     // with gemv: the tensor-core decode kernel (else the warp-MMA one)
+  int a_tmem1;   // tcgen05 at 256 tokens: restored weights in TMEM beside one accumulator
 };
 
 int bucket_of(int64_t m) {
@@ -232,6 +234,15 @@ int tile_m_for(int32_t fmt, int64_t m, int64_t n, int num_sms, int64_t k = 0) {
 // kernel's K ranges are cheaper there; with a whole tile per CTA the tcgen05 small-token kernel
 // is as fast). HM_GEMV=0 keeps tcgen05 for every M; HM_GEMV=2 takes the decode kernel for every M
 // it serves (tests, sweeps).
+// Decode-sized INT4 layers (up to 16 tokens) may run on the tensor-core decode kernel instead of
+// the warp-MMA one (HM_DECODE_TC=1). Off by default: measured on the benchmark layers it is 17-25 %
+// slower up to 8 tokens and on par at 16 (a tcgen05.mma of 128 x 16 x 16 costs the issuing SM
+// ~40-80 cycles whatever its size, so a 128x128 unit costs ~8 of them as the warp-MMA kernel's 64
+// m16n8k16 instructions cost its four sub-partitions).
+bool use_tcdec(int32_t fmt, int64_t m) {
+  return tcdec_serves(fmt) && m >= 1 && m <= kGemvMoeTokens && env_int("HM_DECODE_TC", 0) == 1;
+}
+
 bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (!unit_fmt(fmt)) return false;
   if (m < 1 || m > kGemvMaxTokens) return false;
@@ -246,9 +257,10 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.bucket = bucket_of(m);
   if (use_gemv(fmt, m, n, k, num_sms)) {
     p.gemv = 1;
-    p.tile_m = gemv_tokens(m);
+    p.tc = use_tcdec(fmt, m) ? 1 : 0;
+    p.tile_m = p.tc ? kGemvMoeTokens : gemv_tokens(m);
     p.tile_k = 128;
-    p.stages = gemv_stages(m, fmt);
+    p.stages = p.tc ? tcdec_stages() : gemv_stages(m, fmt);
     p.num_m_tiles = 1;
     p.num_n_tiles = pad_n(n) / 128;
     p.kb_total = k / 128;
@@ -306,6 +318,14 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.grid = static_cast<int>(p.tiles * per);
   }
   if (p.grid < 1) p.grid = 1;
+  // 256-token tiles: restored weights in TMEM beside a single accumulator for long K loops or few
+  // tiles per CTA (the epilogue then delays only a few tile starts), else in shared memory with the
+  // accumulator pair (measured on the three benchmark layers; HM_A_TMEM1=0/1 forces it)
+  if (p.tile_m == 256 && fmt != kW8A16Int8) {
+    const int forced = env_int("HM_A_TMEM1", -1);
+    p.a_tmem1 = (forced == 0 || forced == 1) ? forced : ((p.kb_total >= 64 || ceil_div(p.tiles, p.grid) <= 3) ? 1 : 0);
+    p.stages = f16_stages(fmt, p.tile_m, p.a_tmem1 != 0);
+  }
   return p;
 }
 
@@ -321,10 +341,10 @@ void log_plan(const char* entry, int32_t fmt, int64_t m, int64_t n, int64_t k, c
   if (!log_on()) return;
   std::fprintf(stderr,
                "[hm] %s fmt=%d M=%lld N=%lld K=%lld kernel=%s tile_m=%d tile_k=%d stages=%d stream_k=%d grid=%d "
-               "tiles=%lld\n",
+               "tiles=%lld%s\n",
                entry, fmt, static_cast<long long>(m), static_cast<long long>(n), static_cast<long long>(k),
-               p.gemv ? "decode" : "tcgen05", p.tile_m, p.tile_k, p.stages, p.stream_k, p.grid,
-               static_cast<long long>(p.tiles));
+               p.gemv ? (p.tc ? "decode-tc" : "decode") : "tcgen05", p.tile_m, p.tile_k, p.stages, p.stream_k, p.grid,
+               static_cast<long long>(p.tiles), p.a_tmem1 ? " a=tmem" : "");
 }
 
 constexpr size_t kAlign = 256;
@@ -431,6 +451,18 @@ bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int 
 
 // X (bf16 [M][K]) as the decode kernel loads it: one box of 128 columns x `tokens` rows per 128-K
 // block, unswizzled (rows past M read as zeros).
+// Tensor-core decode kernel: X as [K/64 chunks][rows][64], box {64, 16, depth} (depth 2: one
+// 128-K block, 4: two), 128-byte swizzle (the MMA's K-major B operand).
+bool encode_x_tc(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int depth) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k * 2), 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kGemvMoeTokens), static_cast<cuuint32_t>(depth)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int tokens) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k * 2)};
@@ -439,6 +471,12 @@ bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int to
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// X tensor map(s) of a plan's kernel.
+bool encode_x_plan(F16Params* prm, const void* x, int64_t k, int64_t m, int gemv, int tc, int tile_m) {
+  if (gemv && tc) return encode_x_tc(&prm->tmap_x, x, k, m, 2) && encode_x_tc(&prm->tmap_x2, x, k, m, 4);
+  return gemv ? encode_x_gemv(&prm->tmap_x, x, k, m, tile_m) : encode_x_f16(&prm->tmap_x, x, k, m, tile_m);
 }
 
 // Token tile of the grouped GEMM from the mean rows per expert (per-expert counts stay on the
@@ -524,15 +562,15 @@ hm_status moe_w4a16(int32_t fmt, const void* x, const int32_t* offsets, int32_t 
   const MoeWs wl = moe_ws_layout(fmt, rows, E, N, K);
   const bool gemv = moe_use_gemv(fmt, rows, E) && ws != nullptr && ws_bytes >= wl.total && aligned(ws, 16) &&
                     di.num_sms <= kMaxSmsForSizing;
-  const int tile_m = gemv ? moe_gemv_tokens(rows, E) : moe_tile_m(fmt, rows, E);
+  const bool tc = gemv && use_tcdec(fmt, 1);
+  const int tile_m = tc ? kGemvMoeTokens : (gemv ? moe_gemv_tokens(rows, E) : moe_tile_m(fmt, rows, E));
   if (log_on())
     std::fprintf(stderr, "[hm] %s fmt=%d E=%d rows=%lld N=%lld K=%lld kernel=%s tile_m=%d grid=%d\n", entry, fmt, E,
                  static_cast<long long>(rows), static_cast<long long>(N), static_cast<long long>(K),
-                 gemv ? "decode" : "tcgen05", tile_m, di.num_sms);
+                 gemv ? (tc ? "decode-tc" : "decode") : "tcgen05", tile_m, di.num_sms);
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (gemv ? !encode_x_gemv(&prm.tmap_x, x, K, rows, tile_m) : !encode_x_f16(&prm.tmap_x, x, K, rows, tile_m))
-    return HM_ERR_CUDA;
+  if (!encode_x_plan(&prm, x, K, rows, gemv, tc, tile_m)) return HM_ERR_CUDA;
   prm.packed = base;
   prm.packed_list = list;
   prm.expert_stride = stride;
@@ -548,11 +586,13 @@ hm_status moe_w4a16(int32_t fmt, const void* x, const int32_t* offsets, int32_t 
   prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
   prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, gemv ? 1 : 0};
   prm.timeout_ns = timeout_ns();
+  prm.a_tmem1 = (tile_m == 256 && fmt != kW8A16Int8 && K / 128 >= 64 && env_int("HM_A_TMEM1", 1) != 0) ||
+                (tile_m == 256 && fmt != kW8A16Int8 && env_int("HM_A_TMEM1", -1) == 1) ? 1 : 0;
   if (gemv) {
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     prm.partial = reinterpret_cast<float*>(wsb + wl.partial);
     prm.counters = reinterpret_cast<uint32_t*>(wsb + wl.counters);
-    return cuda_status(launch_gemv_moe(prm, tile_m, st));
+    return cuda_status(tc ? launch_tcdec(prm, true, st) : launch_gemv_moe(prm, tile_m, st));
   }
   return cuda_status(launch_f16_gemm(prm, tile_m, true, st));
 }
@@ -713,7 +753,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
   out->stream_k = p.stream_k;
   out->grid = p.grid;
   out->tiles = static_cast<int32_t>(p.tiles);
-  out->kernel = p.gemv;
+  out->kernel = p.gemv ? (p.tc ? 2 : 1) : 0;
   return HM_OK;
 }
 
@@ -739,7 +779,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (unit_fmt(fmt)) {
     F16Params prm;
     std::memset(&prm, 0, sizeof(prm));
-    if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
+    if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m))
       return HM_ERR_CUDA;
     prm.packed = static_cast<const uint8_t*>(packed);
     prm.y = static_cast<__nv_bfloat16*>(y);
@@ -755,8 +795,9 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
     prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
     prm.timeout_ns = timeout_ns();
+    prm.a_tmem1 = p.a_tmem1;
     prm.trace = trace_for(di, p.grid);
-    if (p.gemv) return cuda_status(launch_gemv(prm, st));
+    if (p.gemv) return cuda_status(p.tc ? launch_tcdec(prm, false, st) : launch_gemv(prm, st));
     return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
   }
 
@@ -961,7 +1002,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (shared && cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (p.gemv ? !encode_x_gemv(&prm.tmap_x, x, K, M, p.tile_m) : !encode_x_f16(&prm.tmap_x, x, K, M, p.tile_m))
+  if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m))
     return HM_ERR_CUDA;
   prm.packed = static_cast<const uint8_t*>(packed);
   prm.y = static_cast<__nv_bfloat16*>(y);
@@ -976,7 +1017,9 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
   prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
   prm.timeout_ns = timeout_ns();
-  return cuda_status(p.gemv ? launch_gemv(prm, st) : launch_f16_gemm(prm, p.tile_m, false, st));
+  prm.a_tmem1 = p.a_tmem1;
+  return cuda_status(p.gemv ? (p.tc ? launch_tcdec(prm, false, st) : launch_gemv(prm, st))
+                            : launch_f16_gemm(prm, p.tile_m, false, st));
 }
 
 uint32_t hm_get_device_error(void* stream) {

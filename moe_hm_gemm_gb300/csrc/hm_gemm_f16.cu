@@ -14,7 +14,9 @@ bool f16s_serves(int fmt, int tile_m) {
   return !(e && e[0] == '0');
 }
 
-int f16_stages(int fmt, int tile_m) {
+int f16_stages(int fmt, int tile_m, bool a_tmem1) {
+  if (tile_m == 256 && a_tmem1 && fmt != kW8A16Int8)
+    return fmt == kW4A16Int4G ? F16Shape<256, kUnitG32Zp, true>::kSL : F16Shape<256, kUnitMx, true>::kSL;
   if (f16s_serves(fmt, tile_m)) return f16s_stages(tile_m);
   if (fmt == kW8A16Int8) {
     switch (tile_m) {

@@ -58,13 +58,18 @@ constexpr int kEpiWarp0 = kDqWarp0 + kDqWarps;
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle atoms of 64 K
 
-// Two variants of the A (restored weight) path:
+// Variants of the A (restored weight) path:
 //  * tile_m <= 192: the dequant warps store bf16 A straight into TMEM (tcgen05.st) and the MMA
 //    reads A from TMEM, so shared memory carries only the packed weights and X; TMEM holds the
 //    double-buffered accumulator (2 x tile_m columns) plus kSA A stages of 64 columns (two at 192
 //    tokens, whose accumulator pair takes 384 of the 512 columns);
-//  * tile_m = 256: the accumulator pair fills TMEM, so A goes through shared memory in the
-//    128-byte-swizzled K-major layout.
+//  * tile_m = 256 (T1 = false): the accumulator pair fills TMEM, so A goes through shared memory
+//    in the 128-byte-swizzled K-major layout (two A stages);
+//  * tile_m = 256, T1 = true: A in TMEM with four A stages beside a single accumulator; load
+//    stages gain the shared memory A left (three instead of two). Each 128-K block then waits less
+//    for its activations and restored weights (measured timelines: ~0.77 instead of ~1.0 us per
+//    block), but the next tile's first MMA waits for the epilogue, so the planner takes it for long
+//    K loops or few tiles per CTA.
 // A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
 // activation load), so that small token tiles move many bytes per TMA instruction; the dequant
 // warps and the MMA still step through it one 128-K block (one TMEM A slot) at a time.
@@ -73,11 +78,14 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 // threads. Small token tiles (N <= 64, where one MMA is far below that wait) therefore use two
 // issuing warps that take alternate 128-K blocks into separate accumulators, which the epilogue
 // adds (issuer 0 first, so the sum is deterministic).
-template <int BT, int UB = kUnitMx>
+template <int BT, int UB = kUnitMx, bool T1 = false>
 struct F16Shape {
-  static constexpr bool kATmem = BT <= 192;
+  static constexpr bool kATmem = BT <= 192 || T1;
   static constexpr int kIss = BT <= 64 ? 2 : 1;
-  static constexpr int kAccCols = 2 * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
+  // Accumulator buffers: two (the epilogue of one tile overlaps the next tile's main loop), or one
+  // (T1: TMEM room for four A stages at 256 tokens).
+  static constexpr int kAccBufs = T1 ? 1 : 2;
+  static constexpr int kAccCols = kAccBufs * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
   static constexpr int kG = f16_group_of(BT);
   static constexpr int kXStage = kG * BT * 128 * 2;
   static constexpr int kWStage = kG * UB;  // room for the largest units of the formats served
@@ -85,7 +93,12 @@ struct F16Shape {
   static constexpr int kAOff = 0;
   static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
   static constexpr int kXOff = kASmem;
-  static constexpr int kSLFit = ((kATmem ? 208 : 216) * 1024 - kASmem) / (kXStage + kWStage);
+  // load stages: as many as shared memory holds beside the A stages, the barriers (3 per load
+  // stage), the MoE arrays of up to 1024 experts and the alignment slack (smem_bytes(1024))
+  static constexpr int kSLFit =
+      (232448 - 1024 - kASmem - (2 * ((kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2)) + 5) * 8 -
+       96 - 8 * 1025) /
+      (kXStage + kWStage + 24);
   static constexpr int kSL = kSLFit > 16 ? 16 : kSLFit;
   static constexpr int kWOff = kXOff + kSL * kXStage;
   static constexpr int kBarOff = kWOff + kSL * kWStage;
@@ -97,6 +110,7 @@ struct F16Shape {
   static constexpr uint32_t kACol0 = kAccCols;  // first TMEM column of the A stages
   static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
   static_assert(kSL >= 2, "load pipeline depth");
+  static_assert(smem_bytes(1024) <= 232448, "shared memory per CTA");
   static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
   static_assert(kATmem || kIss == 1, "two issuers only with A in TMEM");
 };
@@ -108,9 +122,9 @@ constexpr int f16_unit_room(int wk) {
 
 // WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4,
 // 6 = INT4 with a bf16 scale and u4 zero-point per 32-K chunk, 8 = INT8 (tiles up to 192 tokens).
-template <int BT, int WK, bool MOE>
+template <int BT, int WK, bool MOE, bool T1>
 __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
-  using S = F16Shape<BT, f16_unit_room(WK)>;
+  using S = F16Shape<BT, f16_unit_room(WK), T1>;
   constexpr int SL = S::kSL;
   constexpr int SA = S::kSA;
 
@@ -323,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       Segment seg;
       bool ok = true;
       while (ok && sched.next(seg)) {
-        const uint32_t b = acc_i & 1u;
-        if (!mbar_wait(&acc_empty[b], ((acc_i >> 1) & 1u) ^ 1u, wc)) break;
+        const uint32_t b = acc_i % S::kAccBufs;
+        if (!mbar_wait(&acc_empty[b], ((acc_i / S::kAccBufs) & 1u) ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + (b * S::kIss + is) * BT;
         bool first = true;
@@ -565,13 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     int seq = 0;                         // running 128-K block index, as the issuers count it
     Segment seg;
     while (sched.next(seg)) {
-      const uint32_t b = acc_i & 1u;
+      const uint32_t b = acc_i % S::kAccBufs;
       // Issuer i wrote its accumulator iff the segment has a block with sequence index % 2 == i.
       const int nb = seg.kb1 - seg.kb0;
       const bool use1 = S::kIss > 1 && (nb >= 2 || (seq & 1) == 1);
       const bool use0 = S::kIss == 1 || nb >= 2 || (seq & 1) == 0;
       seq += nb;
-      if (!mbar_wait(&acc_full[b], (acc_i >> 1) & 1u, wc)) break;
+      if (!mbar_wait(&acc_full[b], (acc_i / S::kAccBufs) & 1u, wc)) break;
       tc_fence_after();
       if (row == 0 && acc_i == 0) trace_mark(p.trace, 8);
       const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
@@ -658,10 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   }
 }
 
-template <int BT, int WK, bool MOE>
+template <int BT, int WK, bool MOE, bool T1 = false>
 cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
-  using S = F16Shape<BT, f16_unit_room(WK)>;
-  auto kern = f16_gemm_kernel<BT, WK, MOE>;
+  using S = F16Shape<BT, f16_unit_room(WK), T1>;
+  auto kern = f16_gemm_kernel<BT, WK, MOE, T1>;
   const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
   // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
   // instantiation can ask for), so that later calls, including ones under stream capture, only launch.
@@ -688,7 +702,8 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
       if constexpr (!MOE) return launch_one<192, WK, MOE>(p, st);
       return cudaErrorInvalidValue;
     case 256:
-      if constexpr (WK != 8) return launch_one<256, WK, MOE>(p, st);   // INT8 stops at 192
+      if constexpr (WK != 8)   // INT8 stops at 192
+        return p.a_tmem1 ? launch_one<256, WK, MOE, true>(p, st) : launch_one<256, WK, MOE, false>(p, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }

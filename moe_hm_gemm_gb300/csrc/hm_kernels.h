@@ -15,6 +15,7 @@ namespace hm {
 // W4A16 GEMM (INT4 or MXFP4 weights restored to bf16, kind::f16 MMA), dense or MoE.
 struct F16Params {
   CUtensorMap tmap_x;                 // X bf16 [rows][K], box {64, tile_m}, 128-byte swizzle
+  CUtensorMap tmap_x2;                // tensor-core decode kernel: box of two k-blocks (else unused)
   const uint8_t* packed;              // dense: packed weight (header first)
   const uint8_t* const* packed_list;  // MoE: device array of E packed weights, or NULL when the
                                       // experts lie at packed + e * expert_stride
@@ -33,6 +34,8 @@ struct F16Params {
   uint64_t timeout_ns;
   uint64_t* trace;                    // optional per-CTA timestamps [grid][16] (diagnostics)
   int32_t cluster;                    // decode kernel: CTAs per cluster (each tile's K ranges), 0/1 = none
+  int32_t a_tmem1;                    // tcgen05 W4A16 kernel at 256 tokens: restored weights in TMEM
+                                      // beside one accumulator (else in shared memory, two accumulators)
 };
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
@@ -98,7 +101,7 @@ cudaError_t launch_mx_moe_gemm(const MxParams& p, int tile_m, cudaStream_t st);
 // The block-scaled kernel runs two CTAs per SM (the plan's grid counts CTAs, not SMs).
 constexpr int kMxCtasPerSm = 2;
 // Load stages of the W4A16 kernel that serves (fmt, tile_m).
-int f16_stages(int fmt, int tile_m);
+int f16_stages(int fmt, int tile_m, bool a_tmem1 = false);
 // Small-token INT4 kernel (tile_m 16 or 32; hm_gemm_f16s.cu), chosen by launch_f16_gemm unless
 // HM_F16_SMALL=0 in the environment.
 cudaError_t launch_f16s_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
@@ -118,6 +121,12 @@ cudaError_t launch_gemv(const F16Params& p, cudaStream_t st);
 // the tile count comes from the device offsets); shared tiles hand off through p.partial /
 // p.counters.
 cudaError_t launch_gemv_moe(const F16Params& p, int tokens, cudaStream_t st);
+// Tensor-core decode kernel (hm_gemv_tc.cu): INT4 weights (groups of 128), up to 16 tokens (MoE:
+// token tiles of 16 rows), the decode kernel's stream-K split (p.sched.grid CTAs); tmap_x is 3-D
+// with box {64, 16, 2} (one 128-K block) and tmap_x2 the same with box {64, 16, 4}.
+bool tcdec_serves(int32_t fmt);
+int tcdec_stages();
+cudaError_t launch_tcdec(const F16Params& p, bool moe, cudaStream_t st);
 int gemv_tokens(int64_t m);
 int gemv_stages(int64_t m, int32_t fmt);
 

@@ -192,12 +192,18 @@ def test_oversized_schedule_rejected(hm):
 
 def test_plan_decode_kernel(hm, monkeypatch):
     """W4A16 formats at M <= 32 take the warp-MMA decode kernel (built for 8, 16 or 32 tokens);
+    with HM_DECODE_TC=1, INT4 up to 16 tokens takes the tensor-core decode kernel (16-token tiles);
     the block-scaled formats and M > 32 keep tcgen05; HM_GEMV=0 keeps tcgen05 for every M."""
     for fmt in (1, 2, 5):
         tiles = [hm.plan(fmt, m, 4096, 4096, 152)["tile_m"] for m in range(1, 33)]
         assert tiles == [8] * 8 + [16] * 8 + [32] * 16
         assert all(hm.plan(fmt, m, 4096, 4096, 152)["kernel"] == 1 for m in range(1, 33))
         assert hm.plan(fmt, 33, 4096, 4096, 152)["kernel"] == 0
+    monkeypatch.setenv("HM_DECODE_TC", "1")
+    assert [hm.plan(1, m, 4096, 4096, 152)["tile_m"] for m in range(1, 33)] == [16] * 16 + [32] * 16
+    assert [hm.plan(1, m, 4096, 4096, 152)["kernel"] for m in range(1, 33)] == [2] * 16 + [1] * 16
+    assert hm.plan(2, 1, 4096, 4096, 152)["kernel"] == 1   # INT4 only
+    monkeypatch.delenv("HM_DECODE_TC")
     # 17..32 tokens on the 14336-wide layer: 112 whole tiles for tcgen05, which INT4 keeps;
     # MXFP4 always takes the decode kernel up to 32 tokens
     assert hm.plan(1, 32, 14336, 4096, 152)["kernel"] == 0
@@ -266,7 +272,7 @@ def test_workspace_covers_every_plan(hm):
         ws = hm.workspace_size(fmt, m, n, k)
         for sms in (1, 2, 7, 64, 148, 152, 160, 256):
             p = hm.plan(fmt, m, n, k, sms)
-            if p["kernel"] == 1:
+            if p["kernel"] in (1, 2):
                 need = p["grid"] * p["tile_m"] * 128 * 4 + p["tiles"] * 8 * 4
             else:
                 need = (p["grid"] * 2 * p["tile_m"] * 128 * 4 if p["stream_k"] else 0) + p["tiles"] * 4 * 4
@@ -337,6 +343,8 @@ def test_plan_invariants_random(hm):
         if p["kernel"] == 1:
             assert fmt in (1, 2, 5) and m <= 32 and p["tile_m"] in (8, 16, 32) and p["tile_m"] >= m
             assert p["tiles"] == n_tiles
+        elif p["kernel"] == 2:
+            assert fmt == 1 and m <= 16 and p["tile_m"] == 16 and p["tiles"] == n_tiles
         else:
             assert p["tile_m"] in ((16, 32, 64, 128) if fmt in (3, 4) else (16, 32, 64, 128, 256))
             assert p["tiles"] == -(-m // p["tile_m"]) * n_tiles

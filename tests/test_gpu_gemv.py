@@ -49,6 +49,7 @@ def check(hm, fmt, m, n, k, has_zero, seed):
     # INT4 at 17..32 tokens takes the decode kernel only where tcgen05 would split tiles; force it
     saved = os.environ.get("HM_GEMV")
     os.environ["HM_GEMV"] = "2"
+    os.environ["HM_DECODE_TC"] = "0"   # INT4 up to 16 tokens: the warp-MMA kernel, not the tensor-core one
     try:
         p = hm.plan(fmt, m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)
         assert p["kernel"] == 1 and p["tile_m"] >= m
@@ -56,6 +57,7 @@ def check(hm, fmt, m, n, k, has_zero, seed):
         hm.gemm(fmt, x.cuda(), packed, n, k, out=y)
         torch.cuda.synchronize()
     finally:
+        del os.environ["HM_DECODE_TC"]
         if saved is None:
             del os.environ["HM_GEMV"]
         else:

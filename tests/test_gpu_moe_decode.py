@@ -60,13 +60,17 @@ FORMATS = [(1, False, 0), (1, True, 0), (1, True, -1), (2, False, 0), (5, False,
            (7, True, 0), (7, False, 0)]
 
 
-@pytest.mark.parametrize("tokens", ["8", "16"])
+@pytest.mark.parametrize("tokens", ["8", "16", "tc"])
 @pytest.mark.parametrize("fmt,has_zero,group", FORMATS)
 def test_every_unit_format(hm, fmt, has_zero, group, tokens, monkeypatch):
-    """Token tiles of 8 and 16 rows; experts of 1 to 40 rows (up to five token tiles) and empty
-    ones; 216 or more units over the SMs, so most tiles are split along K between CTAs."""
+    """The warp-MMA decode kernel with token tiles of 8 and 16 rows, and the tensor-core decode
+    kernel (INT4; the other formats keep the warp-MMA kernel); experts of 1 to 40 rows (up to five
+    token tiles) and empty ones; 216 or more units over the SMs, so most tiles are split along K
+    between CTAs."""
     monkeypatch.setenv("HM_MOE_GEMV", "1")
-    monkeypatch.setenv("HM_MOE_GEMV_TOKENS", tokens)
+    monkeypatch.setenv("HM_DECODE_TC", "1" if tokens == "tc" else "0")
+    if tokens != "tc":
+        monkeypatch.setenv("HM_MOE_GEMV_TOKENS", tokens)
     decode_case(hm, fmt, [3, 0, 17, 40, 1, 0, 9, 16], 384, 1024, has_zero, group, seed=10 * fmt + 1)
 
 
@@ -77,13 +81,15 @@ def test_ragged_n_and_single_k_block(hm, fmt, monkeypatch):
     decode_case(hm, fmt, [2, 5, 0, 1], 200, 128, fmt == 1, seed=5)
 
 
-@pytest.mark.parametrize("tokens", ["8", "16"])
+@pytest.mark.parametrize("tokens", ["8", "16", "tc"])
 @pytest.mark.parametrize("fmt", [1, 7])
 def test_ranges_cross_experts(hm, fmt, tokens, monkeypatch):
     """64 experts with Zipf top-4 routing of 24 tokens (96 rows): about 180 tiles of 16 k-blocks,
     so each CTA's range runs over several tiles and experts."""
     monkeypatch.setenv("HM_MOE_GEMV", "1")
-    monkeypatch.setenv("HM_MOE_GEMV_TOKENS", tokens)
+    monkeypatch.setenv("HM_DECODE_TC", "1" if tokens == "tc" else "0")
+    if tokens != "tc":
+        monkeypatch.setenv("HM_MOE_GEMV_TOKENS", tokens)
     _, _, offsets = synth.moe_routing(tokens=24, experts=64, topk=4, seed=3)
     decode_case(hm, fmt, np.diff(offsets).tolist(), 512, 2048, fmt == 1, seed=7)
 
