@@ -318,12 +318,11 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.grid = static_cast<int>(p.tiles * per);
   }
   if (p.grid < 1) p.grid = 1;
-  // 256-token tiles: restored weights in TMEM beside a single accumulator for long K loops or few
-  // tiles per CTA (the epilogue then delays only a few tile starts), else in shared memory with the
-  // accumulator pair (measured on the three benchmark layers; HM_A_TMEM1=0/1 forces it)
+  // 256-token tiles: restored weights in TMEM beside a single accumulator (measured faster on all
+  // three benchmark layers from M = 256 on, 9-35 %, once the epilogue stores Y 16 bytes at a time);
+  // HM_A_TMEM1=0 keeps them in shared memory with the accumulator pair
   if (p.tile_m == 256 && fmt != kW8A16Int8) {
-    const int forced = env_int("HM_A_TMEM1", -1);
-    p.a_tmem1 = (forced == 0 || forced == 1) ? forced : ((p.kb_total >= 64 || ceil_div(p.tiles, p.grid) <= 3) ? 1 : 0);
+    p.a_tmem1 = env_int("HM_A_TMEM1", 1) != 0 ? 1 : 0;
     p.stages = f16_stages(fmt, p.tile_m, p.a_tmem1 != 0);
   }
   return p;
@@ -586,8 +585,8 @@ hm_status moe_w4a16(int32_t fmt, const void* x, const int32_t* offsets, int32_t 
   prm.num_n_tiles = static_cast<int32_t>(pad_n(N) / 128);
   prm.sched = SchedParams{0, static_cast<int32_t>(K / 128), di.num_sms, gemv ? 1 : 0};
   prm.timeout_ns = timeout_ns();
-  prm.a_tmem1 = (tile_m == 256 && fmt != kW8A16Int8 && K / 128 >= 64 && env_int("HM_A_TMEM1", 1) != 0) ||
-                (tile_m == 256 && fmt != kW8A16Int8 && env_int("HM_A_TMEM1", -1) == 1) ? 1 : 0;
+  // (256-token tiles: restored weights in TMEM where the epilogue's scratch fits beside the offsets)
+  prm.a_tmem1 = tile_m == 256 && fmt != kW8A16Int8 && E <= 512 && env_int("HM_A_TMEM1", 1) != 0 ? 1 : 0;
   if (gemv) {
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     prm.partial = reinterpret_cast<float*>(wsb + wl.partial);

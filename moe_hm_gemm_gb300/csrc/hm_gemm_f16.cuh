@@ -108,7 +108,16 @@ struct F16Shape {
   static constexpr int kMoeOff = kLutOff + 64;
   static constexpr uint32_t kTmemCols = kATmem ? 512u : (2 * BT < 32 ? 32u : 2u * BT);
   static constexpr uint32_t kACol0 = kAccCols;  // first TMEM column of the A stages
-  static constexpr int smem_bytes(int experts) { return 1024 + kMoeOff + 8 * (experts + 1); }
+  // MoE: offsets and tile prefix (8 (E + 1) bytes) at kMoeOff; then, where shared memory has room,
+  // the epilogue warps' transpose scratch ([warp][16 tokens][32 rows] bf16), 16-byte aligned for its
+  // vector loads
+  static constexpr int kEpiScratch = 4 * 16 * 32 * 2;
+  static constexpr __host__ __device__ int epi_off(int experts) {
+    return (kMoeOff + (experts > 0 ? 8 * (experts + 1) : 0) + 15) / 16 * 16;
+  }
+  static constexpr int smem_bytes(int experts, bool scratch = false) {
+    return 1024 + (scratch ? epi_off(experts) + kEpiScratch : kMoeOff + (experts > 0 ? 8 * (experts + 1) : 0));
+  }
   static_assert(kSL >= 2, "load pipeline depth");
   static_assert(smem_bytes(1024) <= 232448, "shared memory per CTA");
   static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
@@ -574,6 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;       // weight row within the tile
     const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
+    // 16-byte stores of Y through the transpose scratch (when the launch has one; Y 16-byte aligned,
+    // N % 8 == 0)
+    const bool vec_y = p.epi_scratch && (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && (p.n & 7) == 0;
     uint32_t acc_i = 0;
     bool first_seg = true;
     int seq = 0;                         // running 128-K block index, as the issuers count it
@@ -626,7 +638,35 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
           if (owner)
             sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
-          if (n < p.n) {
+          if (vec_y) {
+            // Transpose through shared memory so that each store moves 8 consecutive rows (16 bytes)
+            // of one token instead of one bf16 per thread: [16 tokens][32 rows] for this warp.
+            const uint32_t sc = smem_u32(smem + S::epi_off(MOE ? p.num_experts : 0)) + static_cast<uint32_t>(q) * (16 * 32 * 2);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const uint16_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(a[jj]));
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sc + (jj * 32 + lane) * 2), "h"(hb) : "memory");
+            }
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int piece = lane + 32 * h;   // token piece / 4, rows 8 (piece % 4) .. + 7
+              const int tt = piece >> 2, c8 = piece & 3;
+              const uint4 v8 = ld_shared_v4(sc + (tt * 32 + 8 * c8) * 2);
+              const int64_t m = static_cast<int64_t>(t.m0) + j0 + tt;
+              const int64_t n8 = static_cast<int64_t>(t.n0) + 32 * q + 8 * c8;
+              if (m < t.m_end) {
+                if (n8 + 8 <= p.n) {
+                  *reinterpret_cast<uint4*>(p.y + m * p.n + n8) = v8;
+                } else {
+                  const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
+                  for (int e = 0; e < 8 && n8 + e < p.n; ++e)
+                    p.y[m * p.n + n8 + e] = __ushort_as_bfloat16(static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1))));
+                }
+              }
+            }
+            __syncwarp();   // the scratch is rewritten by the next chunk
+          } else if (n < p.n) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
@@ -676,7 +716,12 @@ template <int BT, int WK, bool MOE, bool T1 = false>
 cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
   using S = F16Shape<BT, f16_unit_room(WK), T1>;
   auto kern = f16_gemm_kernel<BT, WK, MOE, T1>;
-  const int smem = S::smem_bytes(MOE ? p.num_experts : 0);
+  // with the epilogue's transpose scratch where it fits beside the MoE arrays
+  const int experts = MOE ? p.num_experts : 0;
+  const bool scratch = S::smem_bytes(experts, true) <= 232448;
+  const int smem = S::smem_bytes(experts, scratch);
+  F16Params q = p;
+  q.epi_scratch = scratch ? 1 : 0;
   // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
   // instantiation can ask for), so that later calls, including ones under stream capture, only launch.
   static int configured[64] = {};
@@ -684,11 +729,11 @@ cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? e : cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::smem_bytes(1024));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  return launch_pdl(kern, p.sched.grid, kThreads, smem, st, p);
+  return launch_pdl(kern, q.sched.grid, kThreads, smem, st, q);
 }
 
 template <int WK, bool MOE>

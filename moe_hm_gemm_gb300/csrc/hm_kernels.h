@@ -36,6 +36,8 @@ struct F16Params {
   int32_t cluster;                    // decode kernel: CTAs per cluster (each tile's K ranges), 0/1 = none
   int32_t a_tmem1;                    // tcgen05 W4A16 kernel at 256 tokens: restored weights in TMEM
                                       // beside one accumulator (else in shared memory, two accumulators)
+  int32_t epi_scratch;                // tcgen05 W4A16 kernel: the launch has the epilogue's transpose
+                                      // scratch (set by the launcher)
 };
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
