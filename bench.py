@@ -225,10 +225,12 @@ def dense_points(hm, synth, fmt, shapes, ms, seed0, kind, quick, has_zero=None):
     return points
 
 
-def moe_points(hm, synth, fmt, quick, only_t=None):
-    """only_t: the T values to build instead of the default sweep (from --m)."""
-    e, topk = 256, 8
-    layers = [("gate_up", 4096, 7168), ("down", 7168, 2048)]
+def moe_points(hm, synth, fmt, quick, only_t=None, experts=256, only_layer=None):
+    """only_t: the T values to build instead of the default sweep (from --m); experts: E (256 in the
+    benchmark, fewer for small profiling cases, --experts); only_layer: build one layer (--shape)."""
+    e, topk = experts, 8
+    layers = [(nm, n, k) for nm, n, k in (("gate_up", 4096, 7168), ("down", 7168, 2048))
+              if only_layer in (None, "", nm)]
     tokens = only_t or ([16, 256, 4096, 16384] if not quick else [16, 4096])
     points = []
     for li, (name, n, k) in enumerate(layers):
@@ -355,14 +357,14 @@ def _build_points(args, hm, synth):
         return dense_points(hm, synth, hm.W4A4_NVFP4, [(8192, 8192)], [16, 128, 1024, 8192], 3, "kind::mxf4nvf4",
                             args.quick)
     if w == "moe_w4a16":
-        return moe_points(hm, synth, hm.W4A16_INT4, args.quick, moe_ts(args))
+        return moe_points(hm, synth, hm.W4A16_INT4, args.quick, moe_ts(args), args.experts, args.shape)
     if w == "moe_mxfp4":
-        return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick, moe_ts(args))
+        return moe_points(hm, synth, hm.W4A16_MXFP4, args.quick, moe_ts(args), args.experts, args.shape)
     if w == "w4a16_mxint4":
         return dense_points(hm, synth, hm.W4A16_MXINT4, [(4096, 4096), (14336, 4096), (4096, 14336)], MS, 4,
                             "kind::f16", args.quick)
     if w == "moe_mxint4":
-        return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick, moe_ts(args))
+        return moe_points(hm, synth, hm.W4A16_MXINT4, args.quick, moe_ts(args), args.experts, args.shape)
     if w == "moe_silu_mul":
         return silu_points(hm, synth, args.quick)
     if w == "moe_glue":
@@ -757,6 +759,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--experts", type=int, default=256,
+                    help="MoE workloads: experts E (the benchmark's 256; fewer for small profiling cases)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads the default run reports under 'configs'")
     ap.add_argument("--extra-steps", type=int, default=5)

@@ -71,7 +71,12 @@ struct MxShape {
   // MoE: expert offsets [E+1], tile prefix [E+1] and each expert's weight tensor scale [E]
   static constexpr int kMoeOff = kMiscOff + 64;
   static constexpr int kMoeBytes = MOE ? (3 * kMxMoeMaxExperts + 2) * 4 : 0;
-  static constexpr int kSmem = 1024 + kMoeOff + kMoeBytes;
+  // the epilogue warps' transpose scratch ([warp][8 tokens][32 rows] bf16, 16-byte aligned) where
+  // two CTAs per SM still fit with it
+  static constexpr int kEpiOff = (kMoeOff + kMoeBytes + 15) / 16 * 16;
+  static constexpr int kEpiBytes = 4 * 8 * 32 * 2;
+  static constexpr bool kVecEpi = 1024 + kEpiOff + kEpiBytes <= 113 * 1024;
+  static constexpr int kSmem = 1024 + (kVecEpi ? kEpiOff + kEpiBytes : kMoeOff + kMoeBytes);
   // TMEM: accumulator [0, BT), then scale-factor slots
   static constexpr int kSfCols = NV ? kSL * 32 : kSL * 4 + 4;
   static constexpr int kColsNeeded = BT + kSfCols;
@@ -407,6 +412,8 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
     const int row = 32 * q + lane;
     const int64_t total_it = static_cast<int64_t>(p.sched.num_tiles) * kb_total;
     const float gscale = NV ? *gw_sh * (*p.x_global) : 1.0f;
+    // 16-byte stores of Y through the transpose scratch (Y 16-byte aligned, N % 8 == 0)
+    const bool vec_y = S::kVecEpi && (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && (p.n & 7) == 0;
     uint32_t acc_i = 0;
     bool first_seg = true;
     Segment seg;
@@ -445,7 +452,36 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
           for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
           if (owner)
             sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
-          if (n < p.n) {
+          if (vec_y) {
+            // Transpose 8 tokens at a time through shared memory, so that each store moves 8
+            // consecutive rows (16 bytes) of one token.
+            const uint32_t sc8 = smem_u32(smem + S::kEpiOff) + static_cast<uint32_t>(q) * (8 * 32 * 2);
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int64_t m = m0 + j0 + 8 * h8 + jj;
+                const float scl = m < m_end ? (NV ? gs : p.s_tok[m]) : 0.f;
+                const uint16_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(a[8 * h8 + jj] * scl));
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(sc8 + (jj * 32 + lane) * 2), "h"(hb) : "memory");
+              }
+              __syncwarp();
+              const int tt = lane >> 2, c8 = lane & 3;   // token, 8-row group
+              const uint4 v8 = ld_shared_v4(sc8 + (tt * 32 + 8 * c8) * 2);
+              const int64_t m = m0 + j0 + 8 * h8 + tt;
+              const int64_t n8 = static_cast<int64_t>(t.nt) * 128 + 32 * q + 8 * c8;
+              if (m < m_end) {
+                if (n8 + 8 <= p.n) {
+                  *reinterpret_cast<uint4*>(p.y + m * p.n + n8) = v8;
+                } else {
+                  const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
+                  for (int e = 0; e < 8 && n8 + e < p.n; ++e)
+                    p.y[m * p.n + n8 + e] = __ushort_as_bfloat16(static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1))));
+                }
+              }
+              __syncwarp();   // the scratch is rewritten by the next 8 tokens
+            }
+          } else if (n < p.n) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int64_t m = m0 + j0 + jj;
