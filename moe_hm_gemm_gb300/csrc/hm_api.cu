@@ -140,6 +140,8 @@ struct Plan {
   int gemv;   // 1: a decode kernel (tile_m = tokens it is built for)
   int tc;     // with gemv: the tensor-core decode kernel (else the warp-MMA one)
   int a_tmem1;   // tcgen05 at 256 tokens: restored weights in TMEM beside one accumulator
+  int pair;      // tcgen05, dense: clusters of two CTAs share each MMA (tiles of 256 weight rows;
+                 // grid counts CTAs, two per pair)
 };
 
 int bucket_of(int64_t m) {
@@ -325,6 +327,17 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.a_tmem1 = env_int("HM_A_TMEM1", 1) != 0 ? 1 : 0;
     p.stages = f16_stages(fmt, p.tile_m, p.a_tmem1 != 0);
   }
+  // CTA pairs (W4A16 formats, whole tiles, 128 or 256 tokens, N a multiple of 256): each pair's
+  // tile spans 256 weight rows, and each CTA loads half of the tile's activations.
+  const bool pair_ok = unit_fmt(fmt) && !p.stream_k && p.num_n_tiles % 2 == 0 &&
+                       (p.tile_m == 128 || (p.tile_m == 256 && fmt != kW8A16Int8)) && num_sms >= 2;
+  if (pair_ok && env_int("HM_PAIR", 0) == 1) {
+    p.pair = 1;
+    p.a_tmem1 = 0;
+    p.tiles = p.num_m_tiles * (p.num_n_tiles / 2);
+    p.grid = 2 * static_cast<int>(std::min<int64_t>(num_sms / 2, p.tiles));
+    p.stages = f16_stages(fmt, p.tile_m, false, true);
+  }
   return p;
 }
 
@@ -340,10 +353,10 @@ void log_plan(const char* entry, int32_t fmt, int64_t m, int64_t n, int64_t k, c
   if (!log_on()) return;
   std::fprintf(stderr,
                "[hm] %s fmt=%d M=%lld N=%lld K=%lld kernel=%s tile_m=%d tile_k=%d stages=%d stream_k=%d grid=%d "
-               "tiles=%lld%s\n",
+               "tiles=%lld%s%s\n",
                entry, fmt, static_cast<long long>(m), static_cast<long long>(n), static_cast<long long>(k),
                p.gemv ? (p.tc ? "decode-tc" : "decode") : "tcgen05", p.tile_m, p.tile_k, p.stages, p.stream_k, p.grid,
-               static_cast<long long>(p.tiles), p.a_tmem1 ? " a=tmem" : "");
+               static_cast<long long>(p.tiles), p.a_tmem1 ? " a=tmem" : "", p.pair ? " pair" : "");
 }
 
 constexpr size_t kAlign = 256;
@@ -436,9 +449,10 @@ uint8_t* noalloc_scratch(int dev) {
 // X (bf16 [rows][K]) as the W4A16 kernel loads it: box {64, tile_m} when a stage holds one
 // 128-K block, else the K axis split into 64-element chunks as a third dimension (stride 128
 // bytes) so that one load covers the 2*group chunks of a stage.
-bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int tile_m) {
+// CTA pairs load half of a tile's tokens per CTA: box {64, tile_m / 2}.
+bool encode_x_f16(CUtensorMap* map, const void* x, int64_t k, int64_t rows, int tile_m, int pair = 0) {
   const int g = f16_group(tile_m);
-  if (g == 1) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, rows, k * 2, 64, tile_m);
+  if (g == 1) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, k, rows, k * 2, 64, pair ? tile_m / 2 : tile_m);
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 64)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k * 2), 128};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tile_m), static_cast<cuuint32_t>(2 * g)};
@@ -473,9 +487,9 @@ bool encode_x_gemv(CUtensorMap* map, const void* x, int64_t k, int64_t m, int to
 }
 
 // X tensor map(s) of a plan's kernel.
-bool encode_x_plan(F16Params* prm, const void* x, int64_t k, int64_t m, int gemv, int tc, int tile_m) {
+bool encode_x_plan(F16Params* prm, const void* x, int64_t k, int64_t m, int gemv, int tc, int tile_m, int pair = 0) {
   if (gemv && tc) return encode_x_tc(&prm->tmap_x, x, k, m, 2) && encode_x_tc(&prm->tmap_x2, x, k, m, 4);
-  return gemv ? encode_x_gemv(&prm->tmap_x, x, k, m, tile_m) : encode_x_f16(&prm->tmap_x, x, k, m, tile_m);
+  return gemv ? encode_x_gemv(&prm->tmap_x, x, k, m, tile_m) : encode_x_f16(&prm->tmap_x, x, k, m, tile_m, pair);
 }
 
 // Token tile of the grouped GEMM from the mean rows per expert (per-expert counts stay on the
@@ -746,7 +760,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   out->bucket = p.bucket;
   out->tile_m = p.tile_m;
-  out->tile_n = 128;
+  out->tile_n = p.pair ? 256 : 128;
   out->tile_k = p.tile_k;
   out->stages = p.stages;
   out->stream_k = p.stream_k;
@@ -778,7 +792,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
   if (unit_fmt(fmt)) {
     F16Params prm;
     std::memset(&prm, 0, sizeof(prm));
-    if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m))
+    if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m, p.pair))
       return HM_ERR_CUDA;
     prm.packed = static_cast<const uint8_t*>(packed);
     prm.y = static_cast<__nv_bfloat16*>(y);
@@ -792,9 +806,11 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     prm.num_experts = 0;
     prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
     prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
-    prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
+    prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total),
+                            p.pair ? p.grid / 2 : p.grid, p.stream_k};
     prm.timeout_ns = timeout_ns();
     prm.a_tmem1 = p.a_tmem1;
+    prm.pair = p.pair;
     prm.trace = trace_for(di, p.grid);
     if (p.gemv) return cuda_status(p.tc ? launch_tcdec(prm, false, st) : launch_gemv(prm, st));
     return cuda_status(launch_f16_gemm(prm, p.tile_m, false, st));
@@ -1001,7 +1017,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (shared && cudaMemsetAsync(scratch, 0, counter_bytes, st) != cudaSuccess) return HM_ERR_CUDA;
   F16Params prm;
   std::memset(&prm, 0, sizeof(prm));
-  if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m))
+  if (!encode_x_plan(&prm, x, K, M, p.gemv, p.tc, p.tile_m, p.pair))
     return HM_ERR_CUDA;
   prm.packed = static_cast<const uint8_t*>(packed);
   prm.y = static_cast<__nv_bfloat16*>(y);
@@ -1014,9 +1030,11 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   prm.fmt = fmt;
   prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
   prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
-  prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total), p.grid, p.stream_k};
+  prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total),
+                          p.pair ? p.grid / 2 : p.grid, p.stream_k};
   prm.timeout_ns = timeout_ns();
   prm.a_tmem1 = p.a_tmem1;
+  prm.pair = p.pair;
   return cuda_status(p.gemv ? (p.tc ? launch_tcdec(prm, false, st) : launch_gemv(prm, st))
                             : launch_f16_gemm(prm, p.tile_m, false, st));
 }

@@ -72,10 +72,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// A thread whose phase has not completed is suspended until it completes or 20 us pass (the
+// suspend-time hint), instead of polling: waiting warps then leave the issue slots and the
+// shared-memory pipe to the warps doing work (measured 2-3 % on the 256-token W4A16 tiles). The
+// callers' bounded loops still check their time limits between calls.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, 20000;\n\t"
       "selp.u32 %0, 1, 0, P;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -101,6 +105,56 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
+    if (*ctx.abort) return false;
+    if (globaltimer() - t0 > ctx.timeout_ns) {
+      *ctx.abort = 1u;
+      atomicOr(ctx.err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+
+// Split cluster barrier (per thread, not warp-aligned, so a warp may reach it from any branch).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory object in the CTA of the cluster with the given rank.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Bounded wait for a phase completed by arrivals from other CTAs of the cluster (acquire at
+// cluster scope, so their stores into this CTA's shared memory are visible afterwards).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
+  const uint32_t a = smem_u32(bar);
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, 20000;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (try_wait()) return true;
     if (*ctx.abort) return false;
     if (globaltimer() - t0 > ctx.timeout_ns) {
       *ctx.abort = 1u;
@@ -141,6 +195,17 @@ __device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// CTA pairs: 2-D tiled copy into this CTA's shared memory whose completion is counted on a barrier
+// of the pair's other CTA (`bar_cluster`: a shared::cluster address, from map_to_rank).
+__device__ __forceinline__ void tma_2d_g2s_pair(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                uint32_t bar_cluster, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
       : "memory");
 }
 
@@ -198,6 +263,22 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// CTA pairs (a cluster of two CTAs whose tensor cores run one MMA together): the same
+// allocation is made, and later freed, collectively by one warp of each CTA of the pair; every
+// tcgen05 allocation, MMA and commit of such a kernel names the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
 
@@ -296,6 +377,29 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// CTA-pair MMA, issued by one thread of the pair's even CTA: M = 256 rows of A, rows 0-127 from
+// TMEM lanes 0-127 of the even CTA and rows 128-255 from the same TMEM address of the odd CTA; the
+// N columns of B are split between the two CTAs' shared memory at the same address (the even CTA
+// holds columns 0 .. N/2-1); each CTA's TMEM receives its 128 rows of D, all N columns.
+__device__ __forceinline__ void mma_bf16_ta_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pair version of tc_commit: arrive once on the barrier at the same shared-memory address in both
+// CTAs of the pair when all previously issued tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
       : "memory");
 }
 

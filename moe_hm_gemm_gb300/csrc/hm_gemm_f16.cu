@@ -14,7 +14,14 @@ bool f16s_serves(int fmt, int tile_m) {
   return !(e && e[0] == '0');
 }
 
-int f16_stages(int fmt, int tile_m, bool a_tmem1) {
+int f16_stages(int fmt, int tile_m, bool a_tmem1, bool pair) {
+  if (pair && (tile_m == 128 || tile_m == 256)) {
+    const bool g32 = fmt == kW4A16Int4G, i8 = fmt == kW8A16Int8;
+    if (tile_m == 128)
+      return i8 ? F16Shape<128, kUnitInt8Zp, false, true>::kSL
+                : (g32 ? F16Shape<128, kUnitG32Zp, false, true>::kSL : F16Shape<128, kUnitMx, false, true>::kSL);
+    return g32 ? F16Shape<256, kUnitG32Zp, false, true>::kSL : F16Shape<256, kUnitMx, false, true>::kSL;
+  }
   if (tile_m == 256 && a_tmem1 && fmt != kW8A16Int8)
     return fmt == kW4A16Int4G ? F16Shape<256, kUnitG32Zp, true>::kSL : F16Shape<256, kUnitMx, true>::kSL;
   if (f16s_serves(fmt, tile_m)) return f16s_stages(tile_m);

@@ -70,6 +70,10 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 //    for its activations and restored weights (measured timelines: ~0.77 instead of ~1.0 us per
 //    block), but the next tile's first MMA waits for the epilogue, so the planner takes it for long
 //    K loops or few tiles per CTA.
+//  * PAIR (dense): A in TMEM, and a cluster of two CTAs runs each MMA together (M = 256 weight
+//    rows, 128 restored in each CTA's TMEM; N = tile_m tokens, half of the activation tile in each
+//    CTA's shared memory), so a CTA loads half the activation bytes per weight row; tile_m 128 (two
+//    accumulators) or 256 (one).
 // A load stage holds kG consecutive 128-K blocks (one bulk copy of kG contiguous units and one
 // activation load), so that small token tiles move many bytes per TMA instruction; the dequant
 // warps and the MMA still step through it one 128-K block (one TMEM A slot) at a time.
@@ -78,31 +82,37 @@ constexpr int kAStage = 128 * 128 * 2;  // restored bf16 weight tile, 2 swizzle 
 // threads. Small token tiles (N <= 64, where one MMA is far below that wait) therefore use two
 // issuing warps that take alternate 128-K blocks into separate accumulators, which the epilogue
 // adds (issuer 0 first, so the sum is deterministic).
-template <int BT, int UB = kUnitMx, bool T1 = false>
+template <int BT, int UB = kUnitMx, bool T1 = false, bool PAIR = false>
 struct F16Shape {
-  static constexpr bool kATmem = BT <= 192 || T1;
+  static constexpr bool kATmem = BT <= 192 || T1 || PAIR;
   static constexpr int kIss = BT <= 64 ? 2 : 1;
   // Accumulator buffers: two (the epilogue of one tile overlaps the next tile's main loop), or one
-  // (T1: TMEM room for four A stages at 256 tokens).
-  static constexpr int kAccBufs = T1 ? 1 : 2;
+  // (T1, and pairs at 256 tokens: TMEM room for four A stages at 256 tokens).
+  static constexpr int kAccBufs = (T1 || (PAIR && BT == 256)) ? 1 : 2;
   static constexpr int kAccCols = kAccBufs * kIss * BT;  // accumulator (issuer i, buffer b) at (b*kIss + i)*BT
+  static constexpr int kXRows = PAIR ? BT / 2 : BT;      // activation rows (tokens) in this CTA's stages
   static constexpr int kG = f16_group_of(BT);
-  static constexpr int kXStage = kG * BT * 128 * 2;
+  static constexpr int kXStage = kG * kXRows * 128 * 2;
   static constexpr int kWStage = kG * UB;  // room for the largest units of the formats served
   static constexpr int kSA = kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2;
   static constexpr int kAOff = 0;
   static constexpr int kASmem = kATmem ? 0 : kSA * kAStage;
   static constexpr int kXOff = kASmem;
-  // load stages: as many as shared memory holds beside the A stages, the barriers (3 per load
-  // stage), the MoE arrays of up to 1024 experts and the alignment slack (smem_bytes(1024))
-  static constexpr int kSLFit =
-      (232448 - 1024 - kASmem - (2 * ((kATmem ? ((512 - kAccCols) / 64 > 6 ? 6 : (512 - kAccCols) / 64) : 2)) + 5) * 8 -
-       96 - 8 * 1025) /
-      (kXStage + kWStage + 24);
+  // One 128-K block per stage and a single issuer (tile_m >= 128): one commit per block signals
+  // both the block's A slot and its load stage free (mma_done ring of kSD barriers); the issuing
+  // thread spends about as long on a commit as on an MMA, so this saves an eighth of its work per
+  // block. Otherwise each stage and each A slot has its own release barrier.
+  static constexpr bool kMerged = kG == 1 && kIss == 1;
+  // load stages: as many as shared memory holds beside the A stages, the barriers (at most 4 per
+  // load stage and 2 per A slot), the MoE arrays of up to 1024 experts and the alignment slack
+  // (smem_bytes(1024))
+  static constexpr int kSLFit = (232448 - 1024 - kASmem - (2 * kSA + 5) * 8 - 96 - 8 * 1025) / (kXStage + kWStage + 32);
   static constexpr int kSL = kSLFit > 16 ? 16 : kSLFit;
+  static constexpr int kSD = kMerged ? (kSA > kSL ? kSA : kSL) : kSA;   // MMA release barriers
   static constexpr int kWOff = kXOff + kSL * kXStage;
   static constexpr int kBarOff = kWOff + kSL * kWStage;
-  static constexpr int kNumBars = 3 * kSL + 2 * kSA + 5;
+  // full_w, full_x, empty_l [kSL]; full_a [kSA]; empty_a / mma_done [kSD]; acc_full, acc_empty [2]; drain
+  static constexpr int kNumBars = 3 * kSL + kSA + kSD + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kLutOff = kMiscOff + 32;
   static constexpr int kMoeOff = kLutOff + 64;
@@ -111,14 +121,16 @@ struct F16Shape {
   // MoE: offsets and tile prefix (8 (E + 1) bytes) at kMoeOff; then, where shared memory has room,
   // the epilogue warps' transpose scratch ([warp][16 tokens][32 rows] bf16), 16-byte aligned for its
   // vector loads
-  static constexpr int kEpiScratch = 4 * 16 * 32 * 2;
+  static constexpr int kEpiScratch = 4 * 16 * 32 * 2;   // one 16-token chunk per warp (x2: two chunks)
   static constexpr __host__ __device__ int epi_off(int experts) {
     return (kMoeOff + (experts > 0 ? 8 * (experts + 1) : 0) + 15) / 16 * 16;
   }
-  static constexpr int smem_bytes(int experts, bool scratch = false) {
-    return 1024 + (scratch ? epi_off(experts) + kEpiScratch : kMoeOff + (experts > 0 ? 8 * (experts + 1) : 0));
+  static constexpr int smem_bytes(int experts, int scratch_chunks = 0) {
+    return 1024 + (scratch_chunks > 0 ? epi_off(experts) + scratch_chunks * kEpiScratch
+                                      : kMoeOff + (experts > 0 ? 8 * (experts + 1) : 0));
   }
   static_assert(kSL >= 2, "load pipeline depth");
+  static_assert(!PAIR || ((BT == 128 || BT == 256) && kMerged), "CTA pairs: 128 or 256 tokens");
   static_assert(smem_bytes(1024) <= 232448, "shared memory per CTA");
   static_assert(!kATmem || kACol0 + kSA * 64 <= 512, "TMEM budget");
   static_assert(kATmem || kIss == 1, "two issuers only with A in TMEM");
@@ -131,11 +143,13 @@ constexpr int f16_unit_room(int wk) {
 
 // WK: 0 = INT4 (zero-points read from the packed header at run time), 2 = MXFP4, 3 = MXINT4,
 // 6 = INT4 with a bf16 scale and u4 zero-point per 32-K chunk, 8 = INT8 (tiles up to 192 tokens).
-template <int BT, int WK, bool MOE, bool T1>
+template <int BT, int WK, bool MOE, bool T1, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_constant__ F16Params p) {
-  using S = F16Shape<BT, f16_unit_room(WK), T1>;
+  using S = F16Shape<BT, f16_unit_room(WK), T1, PAIR>;
+  static_assert(!(PAIR && MOE), "CTA pairs serve the dense product");
   constexpr int SL = S::kSL;
   constexpr int SA = S::kSA;
+  constexpr int SD = S::kSD;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -145,8 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   uint64_t* full_x = bars + SL;
   uint64_t* empty_l = bars + 2 * SL;
   uint64_t* full_a = bars + 3 * SL;
-  uint64_t* empty_a = full_a + SA;
-  uint64_t* acc_full = empty_a + SA;
+  uint64_t* empty_a = full_a + SA;   // merged releases: mma_done[SD], block bi completes on bi % SD
+  uint64_t* acc_full = empty_a + SD;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
@@ -158,6 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: rank 0 issues the pair's MMAs; the other CTA's arrivals on its barriers are remote
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
 
   if (MOE) {
     // The MoE prefix warp may raise the abort flag while thread 0 is still setting up: clear the
@@ -173,18 +190,18 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     if (MOE) pdl_wait();
     const uint8_t* first = (MOE && p.packed_list != nullptr) ? p.packed_list[0] : p.packed;
     const PackedHeader hdr = *reinterpret_cast<const PackedHeader*>(first);
+    // Pairs: both CTAs' activation copies of a stage complete on the even CTA's full_x (the odd
+    // CTA's stays unused); the even CTA's A slots and accumulators count both CTAs' warps.
     for (int s = 0; s < SL; ++s) {
       mbar_init(&full_w[s], 1);
       mbar_init(&full_x[s], 1);
-      mbar_init(&empty_l[s], S::kIss + kDqWarps);
+      mbar_init(&empty_l[s], (S::kMerged ? 0 : S::kIss) + kDqWarps);
     }
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(&full_a[s], kDqGroup);
-      mbar_init(&empty_a[s], 1);
-    }
+    for (int s = 0; s < SA; ++s) mbar_init(&full_a[s], kDqGroup * (PAIR ? 2 : 1));
+    for (int s = 0; s < SD; ++s) mbar_init(&empty_a[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], S::kIss);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], 4 * (PAIR ? 2 : 1));
     }
     mbar_init(drain, S::kIss);
     fence_barrier_init();
@@ -199,7 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     }
   }
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_value(threadIdx.x);
-  if (warp == kMmaWarp0) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (warp == kMmaWarp0) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, S::kTmemCols);
+    else tmem_alloc(tmem_slot, S::kTmemCols);
+  }
   if (MOE && warp == kDqWarp0) pdl_wait();   // the offsets below may be written by the previous kernel
 
   int32_t num_tiles = p.sched.num_tiles;
@@ -208,12 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     if (warp == kDqWarp0) moe_tile_prefix<BT>(p, offs, prefix, abort_flag, lane);
   }
   __syncthreads();
+  if (PAIR) {   // both CTAs' barriers are initialised before either signals the other's
+    cluster_arrive();
+    cluster_wait();
+  }
   tc_fence_after();
   if (MOE) num_tiles = prefix[p.num_experts];
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   SchedIter sched;
-  sched.init(p.sched, num_tiles, blockIdx.x);
+  sched.init(p.sched, num_tiles, PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x));
   const int kb_total = p.sched.kb_total;
   const bool aborted_early = *abort_flag != 0u;
   const uint32_t has_zero = *hz_sh;
@@ -227,6 +251,24 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   // Weights are streamed once when a single token tile covers M; with several token tiles the
   // same weight tiles are read again by other CTAs, so keep them in L2.
   const bool reuse_w = MOE || p.num_m_tiles > 1;
+  // Tile -> rows and weights. A pair's tile covers 256 weight rows (128 in each CTA) and BT tokens,
+  // of which each CTA loads the activations of BT / 2.
+  auto tile_info = [&](int tile) -> TileInfo {
+    if constexpr (PAIR) {
+      const int np = p.num_n_tiles >> 1;
+      const int nt = 2 * (tile % np) + static_cast<int>(rank);
+      TileInfo t;
+      t.m0 = (tile / np) * BT;
+      t.m_end = static_cast<int32_t>(p.m < t.m0 + BT ? p.m : t.m0 + BT);
+      t.n0 = nt * 128;
+      t.base = p.packed;
+      t.wbase = p.packed + kHeaderBytes + static_cast<size_t>(nt) * kb_total * kUnit;
+      return t;
+    } else {
+      return decode_tile<BT, MOE>(p, tile, prefix, offs, kUnit);
+    }
+  };
+  const int x_row0 = PAIR ? static_cast<int>(rank) * (BT / 2) : 0;   // this CTA's first token in a tile
 
   if (aborted_early) {
     // nothing to do: fall through to teardown
@@ -260,11 +302,23 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         const int slot = idx % SL;
         uint8_t* xs = smem + S::kXOff + slot * S::kXStage;
         trace_stage(p.trace, 0, idx);
-        mbar_arrive_expect_tx(&full_x[slot], S::kXStage);   // the whole box lands (zero-filled past K)
-        if constexpr (S::kG == 1) {
+        if constexpr (PAIR) {
+          // the even CTA expects both halves; the odd CTA's copies complete on the even CTA's barrier
+          if (!leader) {
+            const uint32_t bar = map_to_rank(smem_u32(&full_x[slot]), 0);
+            tma_2d_g2s_pair(xs, &p.tmap_x, kb * 128, t.m0 + x_row0, bar, pol_x);
+            tma_2d_g2s_pair(xs + S::kXRows * 128, &p.tmap_x, kb * 128 + 64, t.m0 + x_row0, bar, pol_x);
+          } else {
+            mbar_arrive_expect_tx(&full_x[slot], 2 * S::kXStage);
+            tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[slot], pol_x);
+            tma_2d_g2s(xs + S::kXRows * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[slot], pol_x);
+          }
+        } else if constexpr (S::kG == 1) {
+          mbar_arrive_expect_tx(&full_x[slot], S::kXStage);   // the whole box lands (zero-filled past K)
           tma_2d_g2s(xs, &p.tmap_x, kb * 128, t.m0, &full_x[slot], pol_x);
           tma_2d_g2s(xs + BT * 128, &p.tmap_x, kb * 128 + 64, t.m0, &full_x[slot], pol_x);
         } else {
+          mbar_arrive_expect_tx(&full_x[slot], S::kXStage);
           tma_3d_g2s(xs, &p.tmap_x, 0, t.m0, 2 * kb, &full_x[slot], pol_x);
         }
         if (idx == 0) trace_mark(p.trace, 2);
@@ -280,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         SchedIter pf = sched;
         Segment ps;
         if (pf.next(ps)) {
-          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          const TileInfo t = tile_info(ps.tile);
           issue_w(0, t, ps.kb0, min(S::kG, ps.kb1 - ps.kb0));
           issued_w = 1;
         }
@@ -291,31 +345,36 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         Segment ps;
         int idx = 0;
         while (idx < SL && pf.next(ps)) {
-          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          const TileInfo t = tile_info(ps.tile);
           for (int kb = ps.kb0; kb < ps.kb1 && idx < SL; kb += S::kG, ++idx) issue_x(idx, t, kb);
         }
         issued_x = idx;
         pf = sched;
         idx = 0;
         while (idx < issued_x && pf.next(ps)) {
-          const TileInfo t = decode_tile<BT, MOE>(p, ps.tile, prefix, offs, kUnit);
+          const TileInfo t = tile_info(ps.tile);
           if (!checked(t)) { ok = false; break; }
           for (int kb = ps.kb0; kb < ps.kb1 && idx < issued_x; kb += S::kG, ++idx)
             if (idx >= issued_w) issue_w(idx, t, kb, min(S::kG, ps.kb1 - kb));
         }
         if (ok) issued_w = issued_x;
       }
-      // Steady state: a stage is refilled once every consumer released it.
+      // Steady state: a stage is refilled once every consumer released it (merged releases: the
+      // dequant warps on empty_l, the MMAs of the stage's block on its mma_done barrier).
       int idx = 0;
       int ls = 0;
       uint32_t lph = 0;
       Segment seg;
       while (ok && sched.next(seg)) {
-        const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+        const TileInfo t = tile_info(seg.tile);
         if (!checked(t)) break;
         for (int kb = seg.kb0; kb < seg.kb1; kb += S::kG, ++idx) {
           if (idx >= issued_x) {
             if (!mbar_wait(&empty_l[ls], lph ^ 1u, wc)) { ok = false; break; }
+            if (S::kMerged) {
+              const int j = idx - SL;   // the block that last used this stage
+              if (!mbar_wait(&empty_a[j % SD], static_cast<uint32_t>(j / SD) & 1u, wc)) { ok = false; break; }
+            }
             issue_w(idx, t, kb, min(S::kG, seg.kb1 - kb));   // weights first: the dequant needs them first
             issue_x(idx, t, kb);
             issued_x = issued_w = idx + 1;
@@ -326,9 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       trace_mark(p.trace, 3);
       if (*abort_flag) {
         // Let copies already in flight (at most the last SL stages issued) land before the
-        // CTA's shared memory goes away.
-        for (int i = issued_x > SL ? issued_x - SL : 0; i < issued_x; ++i)
-          drain_wait(&full_x[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
+        // CTA's shared memory goes away. A pair's activation copies complete on the even CTA's
+        // barriers, whose phases also need the other CTA's copies, so pairs wait a fixed 200 us
+        // for them instead (at most SL stages from L2 or HBM land within microseconds).
+        if (PAIR) {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 200000ull) {
+          }
+        } else {
+          for (int i = issued_x > SL ? issued_x - SL : 0; i < issued_x; ++i)
+            drain_wait(&full_x[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
+        }
         for (int i = issued_w > SL ? issued_w - SL : 0; i < issued_w; ++i)
           drain_wait(&full_w[i % SL], static_cast<uint32_t>(i / SL) & 1u, 100000000ull);
       }
@@ -337,9 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // ------------------------------------------------------------ MMA issuers
     // Issuer `is` takes the 128-K blocks whose running sequence index bi has bi % kIss == is,
     // accumulating into its own TMEM accumulator; A slot bi % SA holds block bi.
-    if (lane == 0) {
+    // Pairs: the even CTA issues for both; barriers the odd CTA also arrives on (or whose copies
+    // complete there) are waited at cluster scope, and every commit signals both CTAs.
+    if (lane == 0 && leader) {
       const int is = warp - kMmaWarp0;
-      constexpr uint32_t idesc = idesc_bf16(128, BT);
+      constexpr uint32_t idesc = idesc_bf16(PAIR ? 256 : 128, BT);
+      auto wait_c = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if constexpr (PAIR) return mbar_wait_cluster(bar, parity, wc);
+        else return mbar_wait(bar, parity, wc);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (PAIR) tc_commit_pair(bar);
+        else tc_commit(bar);
+      };
       int ls = 0;
       uint32_t lph = 0, acc_i = 0;
       int seq = 0;
@@ -347,14 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       bool ok = true;
       while (ok && sched.next(seg)) {
         const uint32_t b = acc_i % S::kAccBufs;
-        if (!mbar_wait(&acc_empty[b], ((acc_i / S::kAccBufs) & 1u) ^ 1u, wc)) break;
+        if (!wait_c(&acc_empty[b], ((acc_i / S::kAccBufs) & 1u) ^ 1u)) break;
         tc_fence_after();
         const uint32_t d = tmem + (b * S::kIss + is) * BT;
         bool first = true;
         for (int kb0 = seg.kb0; kb0 < seg.kb1 && ok; kb0 += S::kG) {
           // Wait for the stage even without a block in it: the release below must not reach
-          // the slot's empty barrier before the slot's previous use is over.
-          if (!mbar_wait(&full_x[ls], lph, wc)) { ok = false; break; }
+          // the slot's empty barrier before the slot's previous use is over. (Merged releases: the
+          // dequant warps saw the activations land before they marked the block's A slot full.)
+          if (!S::kMerged && !wait_c(&full_x[ls], lph)) { ok = false; break; }
           if (is == 0) trace_stage(p.trace, 7, seq / S::kG);
           const int g = min(S::kG, seg.kb1 - kb0);
           for (int j = 0; j < g; ++j) {
@@ -362,13 +440,20 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             if (S::kIss > 1 && bi % S::kIss != is) continue;
             const int as = bi % SA;
             const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
-            if (!mbar_wait(&full_a[as], aph, wc)) { ok = false; break; }
+            if (!wait_c(&full_a[as], aph)) { ok = false; break; }
             trace_stage(p.trace, 3, bi);
             tc_fence_after();
             if (is == 0 && acc_i == 0 && first) trace_mark(p.trace, 6);
             trace_stage(p.trace, 4, bi);
-            const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * BT * 128);
-            if constexpr (S::kATmem) {
+            const uint32_t x_base = smem_u32(smem + S::kXOff + ls * S::kXStage) + j * (2 * S::kXRows * 128);
+            if constexpr (PAIR) {
+              const uint32_t a_t = tmem + S::kACol0 + as * 64;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint64_t bd = sdesc_sw128(x_base + (k >> 2) * (S::kXRows * 128) + (k & 3) * 32);
+                mma_bf16_ta_pair(d, a_t + 8 * k, bd, idesc, (!first || k > 0) ? 1u : 0u);
+              }
+            } else if constexpr (S::kATmem) {
               const uint32_t a_t = tmem + S::kACol0 + as * 64;
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
@@ -386,21 +471,22 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             }
             first = false;
             trace_stage(p.trace, 5, bi);
-            tc_commit(&empty_a[as]);
+            if (S::kMerged) commit(&empty_a[bi % SD]);   // the block's A slot and load stage
+            else commit(&empty_a[as]);
             trace_stage(p.trace, 6, bi);
           }
           if (!ok) break;
-          tc_commit(&empty_l[ls]);
+          if (!S::kMerged) commit(&empty_l[ls]);
           seq += g;
           if (++ls == SL) { ls = 0; lph ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[b]);   // also when this issuer had no block in the tile
+        commit(&acc_full[b]);   // also when this issuer had no block in the tile
         ++acc_i;
       }
       if (is == 0) trace_mark(p.trace, 7);
       // All tcgen05 work of this thread has completed once `drain` flips (one arrival per issuer).
-      tc_commit(drain);
+      commit(drain);
       drain_wait(drain, 0, 1000000000ull);
     }
     __syncwarp();
@@ -437,7 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         const int bi = seq + jb;
         const int as = bi % SA;
         const uint32_t aph = static_cast<uint32_t>(bi / SA) & 1u;
-        if (!mbar_wait(&empty_a[as], aph ^ 1u, wc)) { ok = false; break; }
+        if (S::kMerged) {   // A slot free once the MMAs of block bi - SA completed
+          const int jd = bi - SA;
+          if (jd >= 0 && !mbar_wait(&empty_a[jd % SD], static_cast<uint32_t>(jd / SD) & 1u, wc)) { ok = false; break; }
+        } else if (!mbar_wait(&empty_a[as], aph ^ 1u, wc)) {
+          ok = false;
+          break;
+        }
         if (dw == 0 && first_dq) { trace_mark(p.trace, 4); first_dq = false; }
         if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 1, bi);
         const uint32_t wsa = smem_u32(smem + S::kWOff + ls * S::kWStage) + jb * kUnit;
@@ -571,7 +663,21 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         }
         __syncwarp();
         if (dw % kDqGroup == 0 && lane == 0) trace_stage(p.trace, 2, bi);
-        if (lane == 0) mbar_arrive(&full_a[as]);
+        // Merged releases: the group's first warp also waits for the block's activations, so that
+        // the MMA issuer waits on one barrier per block (pairs: the even CTA's, which counts both
+        // halves).
+        if (S::kMerged && dw % kDqGroup == 0 && leader && lane == 0) {
+          const bool landed = PAIR ? mbar_wait_cluster(&full_x[ls], lph, wc) : mbar_wait(&full_x[ls], lph, wc);
+          if (!landed) ok = false;
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (PAIR && !leader) mbar_arrive_remote(map_to_rank(smem_u32(&full_a[as]), 0));
+          else mbar_arrive(&full_a[as]);
+        }
         }
         seq += g;
         if (++ls == SL) { ls = 0; lph ^= 1u; }
@@ -586,6 +692,38 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     // 16-byte stores of Y through the transpose scratch (when the launch has one; Y 16-byte aligned,
     // N % 8 == 0)
     const bool vec_y = p.epi_scratch && (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && (p.n & 7) == 0;
+    // This warp's transpose scratch: [16 tokens][32 rows] bf16 per chunk (the second chunk, where the
+    // launch has room for it, 4 KB further).
+    const uint32_t sc = smem_u32(smem + S::epi_off(MOE ? p.num_experts : 0)) + static_cast<uint32_t>(q) * (16 * 32 * 2);
+    // Transpose through shared memory so that each store moves 8 consecutive rows (16 bytes) of one
+    // token instead of one bf16 per thread: put() writes a thread's 16 tokens of its row, out() then
+    // has each lane store 8 rows of one token (after a __syncwarp between them).
+    auto put = [&](const uint32_t (&v)[16], uint32_t buf) {
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const uint16_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[jj])));
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(buf + (jj * 32 + lane) * 2), "h"(hb) : "memory");
+      }
+    };
+    auto out = [&](uint32_t buf, const TileInfo& t, int j0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int piece = lane + 32 * h;   // token piece / 4, rows 8 (piece % 4) .. + 7
+        const int tt = piece >> 2, c8 = piece & 3;
+        const uint4 v8 = ld_shared_v4(buf + (tt * 32 + 8 * c8) * 2);
+        const int64_t m = static_cast<int64_t>(t.m0) + j0 + tt;
+        const int64_t n8 = static_cast<int64_t>(t.n0) + 32 * q + 8 * c8;
+        if (m < t.m_end) {
+          if (n8 + 8 <= p.n) {
+            *reinterpret_cast<uint4*>(p.y + m * p.n + n8) = v8;
+          } else {
+            const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
+            for (int e = 0; e < 8 && n8 + e < p.n; ++e)
+              p.y[m * p.n + n8 + e] = __ushort_as_bfloat16(static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1))));
+          }
+        }
+      }
+    };
     uint32_t acc_i = 0;
     bool first_seg = true;
     int seq = 0;                         // running 128-K block index, as the issuers count it
@@ -600,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       if (!mbar_wait(&acc_full[b], (acc_i / S::kAccBufs) & 1u, wc)) break;
       tc_fence_after();
       if (row == 0 && acc_i == 0) trace_mark(p.trace, 8);
-      const TileInfo t = decode_tile<BT, MOE>(p, seg.tile, prefix, offs, kUnit);
+      const TileInfo t = tile_info(seg.tile);
       const int64_t n = static_cast<int64_t>(t.n0) + row;
       const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
       // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
@@ -619,8 +757,24 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * S::kIss * BT;
       float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                     static_cast<size_t>(row) * BT;
+      // Whole tiles with one issuer and room for two chunks of scratch: two chunks at a time, their
+      // loads, conversions and stores interleaved (each chunk alone is a chain of dependent steps).
+      const bool two = S::kIss == 1 && full && vec_y && p.epi_scratch == 2;
 #pragma unroll 1
-      for (int j0 = 0; j0 < BT && have; j0 += 16) {
+      for (int j0 = 0; two && j0 < BT; j0 += 32) {
+        uint32_t v0[16], v1[16];
+        tmem_ld16(tbase + j0, v0);
+        tmem_ld16(tbase + j0 + 16, v1);
+        tmem_wait_ld();
+        put(v0, sc);
+        put(v1, sc + S::kEpiScratch);
+        __syncwarp();
+        out(sc, t, j0);
+        out(sc + S::kEpiScratch, t, j0 + 16);
+        __syncwarp();   // the scratch is rewritten by the next pair of chunks
+      }
+#pragma unroll 1
+      for (int j0 = 0; !two && j0 < BT && have; j0 += 16) {
         uint32_t v[16];
         tmem_ld16(tbase + (use0 ? 0 : BT) + j0, v);
         if (S::kIss > 1 && use0 && use1) {
@@ -639,32 +793,12 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
           if (owner)
             sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
           if (vec_y) {
-            // Transpose through shared memory so that each store moves 8 consecutive rows (16 bytes)
-            // of one token instead of one bf16 per thread: [16 tokens][32 rows] for this warp.
-            const uint32_t sc = smem_u32(smem + S::epi_off(MOE ? p.num_experts : 0)) + static_cast<uint32_t>(q) * (16 * 32 * 2);
+            uint32_t va[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const uint16_t hb = __bfloat16_as_ushort(__float2bfloat16_rn(a[jj]));
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sc + (jj * 32 + lane) * 2), "h"(hb) : "memory");
-            }
+            for (int jj = 0; jj < 16; ++jj) va[jj] = __float_as_uint(a[jj]);
+            put(va, sc);
             __syncwarp();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int piece = lane + 32 * h;   // token piece / 4, rows 8 (piece % 4) .. + 7
-              const int tt = piece >> 2, c8 = piece & 3;
-              const uint4 v8 = ld_shared_v4(sc + (tt * 32 + 8 * c8) * 2);
-              const int64_t m = static_cast<int64_t>(t.m0) + j0 + tt;
-              const int64_t n8 = static_cast<int64_t>(t.n0) + 32 * q + 8 * c8;
-              if (m < t.m_end) {
-                if (n8 + 8 <= p.n) {
-                  *reinterpret_cast<uint4*>(p.y + m * p.n + n8) = v8;
-                } else {
-                  const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
-                  for (int e = 0; e < 8 && n8 + e < p.n; ++e)
-                    p.y[m * p.n + n8 + e] = __ushort_as_bfloat16(static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1))));
-                }
-              }
-            }
+            out(sc, t, j0);
             __syncwarp();   // the scratch is rewritten by the next chunk
           } else if (n < p.n) {
 #pragma unroll
@@ -683,7 +817,10 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (lane == 0) {
+        if (PAIR && !leader) mbar_arrive_remote(map_to_rank(smem_u32(&acc_empty[b]), 0));
+        else mbar_arrive(&acc_empty[b]);
+      }
       ++acc_i;
       if (row == 0) trace_mark(p.trace, 9);
       if (!full && !owner) sk_publish(flag, lane);
@@ -698,9 +835,14 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
 
   __syncwarp();  // reconverge lanes that skipped a single-thread role before the CTA barrier
   __syncthreads();
+  if (PAIR) {   // neither CTA frees its TMEM or shared memory while the other may still reach them
+    cluster_arrive();
+    cluster_wait();
+  }
   if (warp == kMmaWarp0) {
     tc_fence_after();
-    tmem_dealloc(tmem, S::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, S::kTmemCols);
+    else tmem_dealloc(tmem, S::kTmemCols);
     if (lane == 0) {
       trace_mark(p.trace, 12);
       if (p.trace) {
@@ -712,16 +854,17 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   }
 }
 
-template <int BT, int WK, bool MOE, bool T1 = false>
+template <int BT, int WK, bool MOE, bool T1 = false, bool PAIR = false>
 cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
-  using S = F16Shape<BT, f16_unit_room(WK), T1>;
-  auto kern = f16_gemm_kernel<BT, WK, MOE, T1>;
+  using S = F16Shape<BT, f16_unit_room(WK), T1, PAIR>;
+  auto kern = f16_gemm_kernel<BT, WK, MOE, T1, PAIR>;
   // with the epilogue's transpose scratch where it fits beside the MoE arrays
   const int experts = MOE ? p.num_experts : 0;
-  const bool scratch = S::smem_bytes(experts, true) <= 232448;
+  // two chunks of scratch where they fit (the epilogue then transposes two 16-token chunks at once)
+  const int scratch = S::smem_bytes(experts, 2) <= 232448 ? 2 : (S::smem_bytes(experts, 1) <= 232448 ? 1 : 0);
   const int smem = S::smem_bytes(experts, scratch);
   F16Params q = p;
-  q.epi_scratch = scratch ? 1 : 0;
+  q.epi_scratch = scratch;
   // Raise the dynamic shared-memory limit once per device (to the largest size any call of this
   // instantiation can ask for), so that later calls, including ones under stream capture, only launch.
   static int configured[64] = {};
@@ -733,7 +876,43 @@ cudaError_t launch_one(const F16Params& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  return launch_pdl(kern, q.sched.grid, kThreads, smem, st, q);
+  if constexpr (!PAIR) {
+    return launch_pdl(kern, q.sched.grid, kThreads, smem, st, q);
+  } else {
+    // q.sched.grid counts pairs: clusters of two CTAs, no more than the device holds at once
+    // (taken once per device; dense launches of one instantiation all ask for the same shared memory).
+    static int max_pairs[64] = {};
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(static_cast<unsigned>(kThreads));
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    if (max_pairs[dev] == 0) {
+      cfg.gridDim = dim3(2u * static_cast<unsigned>(q.sched.grid));
+      cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      max_pairs[dev] = n;
+    }
+    if (q.sched.grid > max_pairs[dev]) q.sched.grid = max_pairs[dev];
+    static const bool pdl = [] {
+      const char* v = std::getenv("HM_PDL");
+      return !(v && v[0] == '0');
+    }();
+    cfg.gridDim = dim3(2u * static_cast<unsigned>(q.sched.grid));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, q);
+  }
 }
 
 template <int WK, bool MOE>
@@ -742,13 +921,19 @@ cudaError_t launch_bt(const F16Params& p, int tile_m, cudaStream_t st) {
     case 16: return launch_one<16, WK, MOE>(p, st);
     case 32: return launch_one<32, WK, MOE>(p, st);
     case 64: return launch_one<64, WK, MOE>(p, st);
-    case 128: return launch_one<128, WK, MOE>(p, st);
+    case 128:
+      if constexpr (!MOE)
+        if (p.pair) return launch_one<128, WK, MOE, false, true>(p, st);
+      return launch_one<128, WK, MOE>(p, st);
     case 192:
       if constexpr (!MOE) return launch_one<192, WK, MOE>(p, st);
       return cudaErrorInvalidValue;
     case 256:
-      if constexpr (WK != 8)   // INT8 stops at 192
+      if constexpr (WK != 8) {   // INT8 stops at 192
+        if constexpr (!MOE)
+          if (p.pair) return launch_one<256, WK, MOE, false, true>(p, st);
         return p.a_tmem1 ? launch_one<256, WK, MOE, true>(p, st) : launch_one<256, WK, MOE, false>(p, st);
+      }
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }

@@ -138,49 +138,6 @@ __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-// Cluster-scope helpers for the hand-off of a shared tile between the CTAs of one cluster.
-// Split cluster barrier (per thread, not warp-aligned, so a warp may reach it from any branch).
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Bounded wait for a phase completed by arrivals from other CTAs of the cluster (acquire at
-// cluster scope, so their stores into this CTA's shared memory are visible afterwards).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
-  const uint32_t a = smem_u32(bar);
-  auto try_wait = [&]() {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    return ok != 0;
-  };
-  if (try_wait()) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (try_wait()) return true;
-    if (*ctx.abort) return false;
-    if (globaltimer() - t0 > ctx.timeout_ns) {
-      *ctx.abort = 1u;
-      atomicOr(ctx.err, kErrTimeout);
-      return false;
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));

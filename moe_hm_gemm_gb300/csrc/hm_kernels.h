@@ -38,6 +38,9 @@ struct F16Params {
                                       // beside one accumulator (else in shared memory, two accumulators)
   int32_t epi_scratch;                // tcgen05 W4A16 kernel: the launch has the epilogue's transpose
                                       // scratch (set by the launcher)
+  int32_t pair;                       // tcgen05 W4A16 kernel, dense, tile_m 128 or 256: clusters of two
+                                      // CTAs share each MMA (sched.grid counts pairs; tmap_x box
+                                      // {64, tile_m / 2}; N a multiple of 256)
 };
 
 // Block-scaled GEMM (W4A8 MXFP4 x FP8 with kind::mxf8f6f4, W4A4 NVFP4 with kind::mxf4nvf4).
@@ -103,7 +106,7 @@ cudaError_t launch_mx_moe_gemm(const MxParams& p, int tile_m, cudaStream_t st);
 // The block-scaled kernel runs two CTAs per SM (the plan's grid counts CTAs, not SMs).
 constexpr int kMxCtasPerSm = 2;
 // Load stages of the W4A16 kernel that serves (fmt, tile_m).
-int f16_stages(int fmt, int tile_m, bool a_tmem1 = false);
+int f16_stages(int fmt, int tile_m, bool a_tmem1 = false, bool pair = false);
 // Small-token INT4 kernel (tile_m 16 or 32; hm_gemm_f16s.cu), chosen by launch_f16_gemm unless
 // HM_F16_SMALL=0 in the environment.
 cudaError_t launch_f16s_gemm(const F16Params& p, int tile_m, bool moe, cudaStream_t st);
