@@ -72,11 +72,23 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// A thread whose phase has not completed is suspended until it completes or 20 us pass (the
-// suspend-time hint), instead of polling: waiting warps then leave the issue slots and the
-// shared-memory pipe to the warps doing work (measured 2-3 % on the 256-token W4A16 tiles). The
-// callers' bounded loops still check their time limits between calls.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Same, but a thread whose phase has not completed is suspended until it completes or 20 us pass
+// (the suspend-time hint) instead of returning at once, so that waiting warps leave the issue
+// slots and the shared-memory pipe to the warps doing work. Measured 2-3 % faster on the
+// 256-token W4A16 tiles (12 roles of 15 warps wait at any time) and 3-4 % slower on the
+// bandwidth-bound decode kernels, which therefore poll.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, 20000;\n\t"
@@ -94,6 +106,7 @@ struct WaitCtx {
   volatile uint32_t* abort;  // shared memory
   uint32_t* err;             // global device error word
   uint64_t timeout_ns;
+  bool suspend = false;      // wait with the suspend-time hint (mbar_try_wait_suspend)
 };
 
 // Waits until the barrier's phase with the given parity has completed. Returns false if the
@@ -101,10 +114,11 @@ struct WaitCtx {
 // flag). Never spins without a limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto try_wait = [&]() { return ctx.suspend ? mbar_try_wait_suspend(a, parity) : mbar_try_wait(a, parity); };
+  if (try_wait()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (try_wait()) return true;
     if (*ctx.abort) return false;
     if (globaltimer() - t0 > ctx.timeout_ns) {
       *ctx.abort = 1u;
@@ -143,12 +157,20 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   const uint32_t a = smem_u32(bar);
   auto try_wait = [&]() {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, 20000;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
+    if (ctx.suspend)
+      asm volatile(
+          "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, 20000;\n\t"
+          "selp.u32 %0, 1, 0, P;\n\t}"
+          : "=r"(ok)
+          : "r"(a), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, P;\n\t}"
+          : "=r"(ok)
+          : "r"(a), "r"(parity)
+          : "memory");
     return ok != 0;
   };
   if (try_wait()) return true;

@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
   tc_fence_after();
   if (MOE) num_tiles = prefix[p.num_experts];
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns, true};   // waiting roles suspend (mbar_try_wait_suspend)
   SchedIter sched;
   sched.init(p.sched, num_tiles, PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x));
   const int kb_total = p.sched.kb_total;

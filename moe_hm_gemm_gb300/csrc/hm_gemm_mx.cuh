@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sf_col0 = BT;  // first scale-factor column
-  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns, true};   // waiting roles suspend (mbar_try_wait_suspend)
   SchedIter sched;
   sched.init(p.sched, MOE ? prefix[p.num_experts] : p.sched.num_tiles, blockIdx.x);
   const int kb_total = p.sched.kb_total;
