@@ -35,9 +35,21 @@ __device__ __forceinline__ TileInfo decode_tile(const F16Params& p, int tile, co
   TileInfo t;
   const int64_t kb_total = p.k / 128;
   if (!MOE) {
-    // m-major: concurrent CTAs share one X tile and stream different weight tiles
-    const int nt = tile % p.num_n_tiles;
-    const int mt = tile / p.num_n_tiles;
+    // m-major: concurrent CTAs share one X tile and stream different weight tiles; or grouped
+    // (group_m > 1): within a group of group_m token tiles the token tile changes fastest, so a wave
+    // covers group_m token tiles and about CTAs / group_m weight tiles
+    int nt, mt;
+    if (p.group_m > 1) {
+      const int per = p.group_m * p.num_n_tiles;
+      const int g = tile / per, local = tile - g * per;
+      const int left = p.num_m_tiles - g * p.group_m;
+      const int rows = left < p.group_m ? left : p.group_m;
+      mt = g * p.group_m + local % rows;
+      nt = local / rows;
+    } else {
+      nt = tile % p.num_n_tiles;
+      mt = tile / p.num_n_tiles;
+    }
     t.m0 = mt * BT;
     t.m_end = static_cast<int32_t>(p.m < t.m0 + BT ? p.m : t.m0 + BT);
     t.n0 = nt * 128;

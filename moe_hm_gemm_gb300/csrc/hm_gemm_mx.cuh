@@ -112,12 +112,30 @@ struct MxTile {
   int64_t m0, m_end;
 };
 
+// Dense tile order: m-major (the CTAs of a wave share a token tile and stream different weight
+// tiles), or, with group_m > 1, grouped: within a group of group_m token tiles the token tile
+// changes fastest, so a wave covers group_m token tiles and ~CTAs / group_m weight tiles, and each
+// weight tile is read from DRAM once per group instead of once per wave.
+__device__ __forceinline__ void mx_dense_tile(const MxParams& p, int tile, int& mt, int& nt) {
+  if (p.group_m > 1) {
+    const int per = p.group_m * p.num_n_tiles;
+    const int g = tile / per, local = tile - g * per;
+    const int left = p.num_m_tiles - g * p.group_m;
+    const int rows = left < p.group_m ? left : p.group_m;
+    mt = g * p.group_m + local % rows;
+    nt = local / rows;
+  } else {
+    nt = tile % p.num_n_tiles;
+    mt = tile / p.num_n_tiles;
+  }
+}
+
 template <int BT, bool NV, bool MOE>
 __device__ __forceinline__ MxTile mx_decode(const MxParams& p, int tile, const int32_t* prefix, const int32_t* offs) {
   MxTile t;
   if (!MOE) {
-    t.nt = tile % p.num_n_tiles;   // m-major tile order
-    const int mt = tile / p.num_n_tiles;
+    int mt;
+    mx_dense_tile(p, tile, mt, t.nt);
     t.e = 0;
     t.m0 = static_cast<int64_t>(mt) * BT;
     t.m_end = p.m < t.m0 + BT ? p.m : t.m0 + BT;
@@ -287,7 +305,8 @@ __global__ void __launch_bounds__(threads_of<NV>(), kMxCtasPerSm) mx_gemm_kernel
         SchedIter pf = sched;
         Segment ps;
         while (pre < SL && pf.next(ps)) {
-          const int nt = ps.tile % p.num_n_tiles;
+          int mt, nt;
+          mx_dense_tile(p, ps.tile, mt, nt);
           for (int kb = ps.kb0; kb < ps.kb1 && pre < SL; ++kb, ++pre) {
             mbar_expect_tx(&full[pre], w_tx);
             load_w(pre, nt, 0, kb);

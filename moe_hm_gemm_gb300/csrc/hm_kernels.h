@@ -30,6 +30,7 @@ struct F16Params {
   int32_t num_experts;
   int32_t num_m_tiles;                // dense only
   int32_t num_n_tiles;
+  int32_t group_m;                    // dense: token tiles per group of the tile order (<= 1: m-major)
   SchedParams sched;
   uint64_t timeout_ns;
   uint64_t* trace;                    // optional per-CTA timestamps [grid][16] (diagnostics)
@@ -64,6 +65,7 @@ struct MxParams {
   int32_t num_m_tiles;
   int32_t num_n_tiles;
   int32_t k_blocks;                   // K_pad / tile_k
+  int32_t group_m;                    // dense: token tiles per group of the tile order (<= 1: m-major)
   SchedParams sched;
   uint64_t timeout_ns;
   uint64_t* trace;
