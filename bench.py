@@ -14,7 +14,10 @@ A step runs every (shape, M) point of the workload once per rotation copy of its
 point is one CUDA graph of those launches. Per-point times come from CUDA events on the
 launching stream. `value` is the aggregate TFLOP/s of the whole step; the per-point TFLOP/s,
 weight GB/s and roofline fractions are in `sweep`. `e2e` repeats one pass over the points
-through the public API with host (pinned) inputs and outputs, copies included.
+through the public API with host (pinned) inputs and outputs, copies included: each point's input
+is copied in on one stream, computed on the bench stream and its output copied back on a third, so
+that the copies of neighbouring points overlap a point's compute (per point the order is copy in,
+compute, copy out; a point's buffers are reused by the next pass only after its previous copy-out).
 
 --impl reference times the CPU oracle (fp64 NumPy) on a bounded sample of the same workload.
 Under torchrun (N > 1) every rank runs an independent replica (the path does not shard);
@@ -553,19 +556,43 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = None
         h2d = d2h = 0
         if not args.no_e2e:
+            s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+            last_out = {}      # point index -> event after its last copy-out (buffers free again)
+
             def e2e_pass():
-                for p in points:
+                for i, p in enumerate(points):
                     xh, xd, yh, yd, call = p.e2e
-                    xd.copy_(xh, non_blocking=True)
-                    call()
-                    yh.copy_(yd, non_blocking=True)
+                    with torch.cuda.stream(s_in):
+                        if i in last_out:
+                            s_in.wait_event(last_out[i])
+                        xd.copy_(xh, non_blocking=True)
+                        ready = torch.cuda.Event()
+                        ready.record(s_in)
+                    with torch.cuda.stream(stream):
+                        stream.wait_event(ready)
+                        call()
+                        done = torch.cuda.Event()
+                        done.record(stream)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(done)
+                        yh.copy_(yd, non_blocking=True)
+                        out = torch.cuda.Event()
+                        out.record(s_out)
+                    last_out[i] = out
+
             e2e_pass()
             torch.cuda.synchronize()
             reps = max(1, args.steps)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
+            s_in.wait_event(a)
+            s_out.wait_event(a)
             for _ in range(reps):
                 e2e_pass()
+            for s_ in (s_in, s_out):
+                tail = torch.cuda.Event()
+                tail.record(s_)
+                stream.wait_event(tail)
             b.record(stream)
             torch.cuda.synchronize()
             e2e_ms = a.elapsed_time(b) / reps
