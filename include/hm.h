@@ -356,7 +356,8 @@ typedef struct hm_plan_info {
   int32_t bucket;      /* M bucket index: 0: M<=16, 1: <=64, 2: <=256, 3: <=1024, 4: >1024 */
   int32_t tile_m;      /* tokens per tile (tcgen05 MMA N dimension); decode kernel: tokens it
                           is instantiated for (8, 16 or 32, >= M) */
-  int32_t tile_n;      /* weight rows per tile (tcgen05 MMA M dimension, 128) */
+  int32_t tile_n;      /* weight rows per tile (tcgen05 MMA M dimension: 128; 256 when clusters of
+                          two CTAs share each MMA, taken only with HM_PAIR=1 in the environment) */
   int32_t tile_k;      /* K per pipeline stage */
   int32_t stages;      /* load-pipeline depth */
   int32_t stream_k;    /* 1 if the K loop is split across CTAs (stream-K) */
