@@ -517,10 +517,15 @@ def summarize(points, pk, workload, hm, local_rank):
     roofline = {"bound": dom_bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
                 "frac": round(ach / peak, 4), "traffic": measured_traffic(workload, dom.label), "kernel": dom.label,
                 "peak_source": peak_source(pk, dom.kind, dom_bound)}
+    one = (pk.get("kinds") or {}).get(ONE_ISSUER_F16)
+    if dom_bound == "tensor" and dom.kind == "kind::f16" and one:
+        # what one issuing thread sustains with the 256-token tile's instruction (probe kind 5)
+        roofline["one_issuer_ceiling"] = {"value": one, "frac": round(ach / one, 4), "source": ONE_ISSUER_F16}
     return sweep, roofline
 
 
 KIND_PROBES = {"kind::f16": (0,), "kind::mxf8f6f4": (1, 3), "kind::mxf4nvf4": (2, 4)}
+ONE_ISSUER_F16 = "kind::f16 M=128 N=256, A in TMEM, one issuing thread"
 
 
 def live_kind_peaks(hm):
@@ -530,6 +535,8 @@ def live_kind_peaks(hm):
         out = {}
         for kind, probes in KIND_PROBES.items():
             out[kind] = round(max(hm.mma_peak(k, 20000 if k != 2 else 40000, repeats=3)[0] for k in probes), 1)
+        # context, not a denominator: the W4A16 256-token tile's instruction from one issuing thread
+        out[ONE_ISSUER_F16] = round(hm.mma_peak(5, 20000, repeats=3)[0], 1)
         if hm.device_error() != 0:
             return None
         return out

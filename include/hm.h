@@ -388,10 +388,12 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns, void* stream);
  * traffic in the loop): kind 0 = kind::f16 (bf16, M=128, N=256, K=16), 1 = kind::mxf8f6f4
  * block-scaled 1X (e4m3 x e4m3, UE8M0 scales, M=N=128, K=32), 2 = kind::mxf4nvf4 block-scaled 4X
  * (e2m1 x e2m1, UE4M3 scales, M=N=128, K=64), several issuing warps each; kinds 3 and 4 = kinds 1
- * and 2 with N=256 and one issuing warp. *flops_out receives the
+ * and 2 with N=256 and one issuing warp; kind 5 = kind::f16 with M=128, N=256, K=16, A read from
+ * TMEM and one issuing warp (what one issuing thread sustains with the W4A16 kernel's widest
+ * instruction); kind 6 = the same with A in shared memory. *flops_out receives the
  * FLOPs (2*M*N*K per MMA) the launch issues; the caller times it on `stream` (events) to get the
  * dense peak of that kind on this device. iters in [1, 2^24]. A completion wait that runs out (2 s)
- * sets device error bit 1. Allocates nothing; the launch holds all of TMEM on each SM. */
+ * sets device error bit 1. Allocates nothing; the launch holds all of TMEM on each SM. kind in [0, 6]. */
 hm_status hm_mma_peak_probe(int32_t kind, int32_t iters, double* flops_out, void* stream);
 
 /* Diagnostics: install (or, with NULL/0, remove) a device buffer of `bytes` bytes on the current

@@ -1066,7 +1066,7 @@ hm_status hm_debug_wait_timeout(uint64_t timeout_ns_, void* stream) {
 }
 
 hm_status hm_mma_peak_probe(int32_t kind, int32_t iters, double* flops_out, void* stream) {
-  if (kind < 0 || kind > 4 || iters < 1 || iters > (1 << 24) || flops_out == nullptr) return HM_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 6 || iters < 1 || iters > (1 << 24) || flops_out == nullptr) return HM_ERR_INVALID_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return HM_ERR_CUDA;
   return cuda_status(launch_mma_peak(kind, iters, di.num_sms, di.err, kDefaultTimeoutNs,

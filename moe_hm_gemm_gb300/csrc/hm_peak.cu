@@ -12,7 +12,10 @@
 //           K = 32, three issuers;
 //   kind 2: kind::mxf4nvf4.block_scale.scale_vec::4X, e2m1 x e2m1 with UE4M3 scales, M = N = 128,
 //           K = 64, three issuers;
-//   kinds 3 and 4: kinds 1 and 2 with N = 256 and one issuer (the widest instruction of the kind).
+//   kinds 3 and 4: kinds 1 and 2 with N = 256 and one issuer (the widest instruction of the kind);
+//   kind 5: kind::f16 with M = 128, N = 256, K = 16, A read from TMEM, one issuer (the instruction
+//           and issue pattern of the W4A16 kernel's 256-token tiles: what one issuing thread can
+//           sustain); kind 6: the same with A in shared memory.
 // The operand values are arbitrary finite numbers (the tensor pipe's rate does not depend on
 // them). The caller times the launch with events; hm_mma_peak_probe reports the FLOPs it issued.
 #include <cuda_bf16.h>
@@ -28,10 +31,11 @@ constexpr int kPeakSmem = 120 * 1024;   // keeps one CTA per SM (the probe alloc
 
 template <int KIND>
 struct PeakShape {
-  static constexpr int kN = (KIND == 0 || KIND >= 3) ? 256 : 128;
-  static constexpr int kK = KIND == 0 ? 16 : ((KIND == 1 || KIND == 3) ? 32 : 64);   // K per instruction
+  static constexpr bool kF16 = KIND == 0 || KIND >= 5;                               // kind::f16
+  static constexpr int kN = (KIND == 1 || KIND == 2) ? 128 : 256;
+  static constexpr int kK = kF16 ? 16 : ((KIND == 1 || KIND == 3) ? 32 : 64);         // K per instruction
   static constexpr int kIssuers = KIND == 0 ? 2 : (KIND >= 3 ? 1 : 3);
-  static constexpr int kBase = KIND >= 3 ? 1 : KIND;                                 // MMA kind of kinds 3, 4
+  static constexpr int kATmemCol = 256;                                               // kind 5: A in TMEM
   static constexpr int kSfCol = KIND >= 3 ? 256 : 384;                               // first scale column
   static constexpr int kAOff = 0;                                     // 128 rows x 128 bytes
   static constexpr int kBOff = 128 * 128;                             // kN rows x 128 bytes
@@ -65,7 +69,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
   for (int i = threadIdx.x; i < S::kSfOff / 4; i += kPeakThreads) {
     const uint32_t h = mix32(static_cast<uint32_t>(i) * 2654435761u + blockIdx.x);
     uint32_t v;
-    if (KIND == 0) {
+    if (S::kF16) {
       v = (h & 0x807F807Fu) | 0x3C003C00u;   // bf16 values of magnitude in [2^-7, 2^-6)
     } else if (KIND == 1 || KIND == 3) {
       v = h & 0xF7F7F7F7u;                   // e4m3 without the NaN codes (exponent field <= 14)
@@ -87,6 +91,16 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (KIND == 5) {   // A in TMEM: every warp fills its 32 lanes of the 32 columns the 4 K-steps read
+    uint32_t r[32];
+    for (int i = 0; i < 32; ++i)
+      r[i] = (mix32(static_cast<uint32_t>(i * 77 + threadIdx.x) + blockIdx.x) & 0x807F807Fu) | 0x3C003C00u;
+    tmem_st32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + S::kATmemCol, r);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 
   const int issuer = warp - 1;
   if (issuer >= 0 && issuer < S::kIssuers && (threadIdx.x & 31) == 0) {
@@ -110,7 +124,9 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int32_t iters
         const uint64_t ad = sdesc_sw128(a0 + 32 * k);
         const uint64_t bd = sdesc_sw128(b0 + 32 * k);
         const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-        if constexpr (KIND == 0) {
+        if constexpr (KIND == 5) {
+          mma_bf16_ta(d, tmem + S::kATmemCol + 8 * k, bd, idesc_bf16(128, S::kN), acc);
+        } else if constexpr (S::kF16) {
           mma_bf16(d, ad, bd, idesc_bf16(128, S::kN), acc);
         } else if constexpr (KIND == 1 || KIND == 3) {
           mma_mxf8f6f4(d, ad, bd, idesc_block_scaled(128, S::kN, 0, 0, 1, k, k), sf, sf + 4, acc);
@@ -165,6 +181,8 @@ cudaError_t launch_mma_peak(int kind, int32_t iters, int num_sms, uint32_t* err,
   if (kind == 2) return launch_peak<2>(iters, num_sms, err, timeout_ns, st, flops);
   if (kind == 3) return launch_peak<3>(iters, num_sms, err, timeout_ns, st, flops);
   if (kind == 4) return launch_peak<4>(iters, num_sms, err, timeout_ns, st, flops);
+  if (kind == 5) return launch_peak<5>(iters, num_sms, err, timeout_ns, st, flops);
+  if (kind == 6) return launch_peak<6>(iters, num_sms, err, timeout_ns, st, flops);
   return cudaErrorInvalidValue;
 }
 

@@ -379,7 +379,7 @@ def test_moe_gather_combine_argument_checks(hm):
 def test_mma_peak_probe_argument_checks(hm):
     lib = hm.lib()
     fl = ctypes.c_double(0.0)
-    assert lib.hm_mma_peak_probe(5, 10, ctypes.byref(fl), None) == 1
+    assert lib.hm_mma_peak_probe(7, 10, ctypes.byref(fl), None) == 1
     assert lib.hm_mma_peak_probe(0, 0, ctypes.byref(fl), None) == 1
     assert lib.hm_mma_peak_probe(0, 10, None, None) == 1
 

@@ -8,7 +8,8 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-NOMINAL_TFLOPS = {0: 2250.0, 1: 4500.0, 2: 13500.0, 3: 4500.0, 4: 13500.0}   # bf16, fp8, fp4 dense
+NOMINAL_TFLOPS = {0: 2250.0, 1: 4500.0, 2: 13500.0, 3: 4500.0, 4: 13500.0,   # bf16, fp8, fp4 dense
+                  5: 2250.0, 6: 2250.0}
 
 
 @pytest.fixture(scope="module")
@@ -19,7 +20,7 @@ def hm():
     return mod
 
 
-@pytest.mark.parametrize("kind", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3, 4, 5, 6])
 def test_peak_probe_runs_and_is_plausible(hm, kind):
     tflops, ms = hm.mma_peak(kind, iters=2000, repeats=2)
     assert hm.device_error() == 0
