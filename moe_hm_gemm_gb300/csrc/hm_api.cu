@@ -177,13 +177,14 @@ MxChoice mx_choice(int32_t fmt, int64_t m, int64_t n, int num_sms) {
 }
 
 // INT4 W4A16 for 16 < M <= 512: pick (token tile, stream-K) by a cost model fitted to measured
-// times on the 4096x4096, 14336x4096 and 4096x14336 layers (within ~10 %): time ~ 5 us + blocks
-// per CTA x c(tile), where a 128-K block costs c = 0.47 / 0.55 / 0.85 / 1.3 us for tiles of
+// times on the 4096x4096, 14336x4096 and 4096x14336 layers at 32..256 rows: time ~ 5 us + blocks
+// per CTA x c(tile), where a 128-K block costs c = 0.47 / 0.50 / 0.60 / 0.75 us for tiles of
 // 32 / 64 / 128 / 256 tokens, a tile-parallel CTA runs ceil(tiles / SMs) x kb blocks, and a
-// stream-K CTA runs ceil(tiles x kb / SMs) blocks plus a hand-off cost of 15 / 18 / 35 / 60
-// blocks. Narrow tiles stream weights faster per block; wide tiles do more tokens per block. (The
-// costs were fitted with stream-K ranges running across tile boundaries; with the equal K ranges
-// per tile used now the chosen configurations measured the same or up to 8 % faster.)
+// stream-K CTA runs ceil(tiles x kb / SMs) blocks plus a hand-off cost of 9 / 16 / 30 / 60
+// blocks (the 256-token hand-off, unconstrained by these points, kept at its earlier fit). Narrow
+// tiles stream weights faster per block; wide tiles do more tokens per block. With these constants
+// the choice is the fastest of the eight (tile, split) configurations at 11 of the 12 measured
+// points and within 9 % at the twelfth.
 struct F16Choice {
   int tile_m;
   bool stream_k;
@@ -191,7 +192,7 @@ struct F16Choice {
 F16Choice f16_choice(int64_t m, int64_t n, int64_t k, int num_sms) {
   const int64_t n_tiles = pad_n(n) / 128, kb = k / 128;
   const int tiles_m[4] = {32, 64, 128, 256};
-  const double cost[4] = {0.47, 0.55, 0.85, 1.3}, handoff[4] = {15, 18, 35, 60};
+  const double cost[4] = {0.47, 0.50, 0.60, 0.75}, handoff[4] = {9, 16, 30, 60};
   F16Choice best{32, true};
   double best_t = 1e30;
   for (int i = 0; i < 4; ++i) {

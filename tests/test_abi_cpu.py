@@ -120,7 +120,9 @@ def test_plan_buckets(hm):
     assert (seen[256]["tile_m"], seen[256]["stream_k"]) == (64, 0)     # 256 tiles cover the SMs
     assert (seen[64]["tile_m"], seen[64]["stream_k"]) == (32, 1)       # 64 tiles: split K
     p = hm.plan(1, 128, 4096, 4096, 152)
-    assert (p["tile_m"], p["stream_k"], p["grid"]) == (32, 0, 128)
+    assert (p["tile_m"], p["stream_k"], p["grid"]) == (64, 1, 128)   # 64 tiles, each cut in 2 K ranges
+    p = hm.plan(1, 256, 4096, 14336, 152)
+    assert (p["tile_m"], p["stream_k"]) == (128, 1)                  # long K: 128-token tiles, split
     # long K: stream-K; wide N: the 256-token tile from M = 256 on
     p = hm.plan(1, 128, 4096, 14336, 152)
     assert (p["tile_m"], p["stream_k"]) == (64, 1)
