@@ -167,8 +167,10 @@ cudaError_t launch_moe_gather(const __nv_bfloat16* x, const int32_t* token_of_ro
 cudaError_t launch_moe_combine(const __nv_bfloat16* y, const int32_t* pos, const float* w, __nv_bfloat16* out,
                                int64_t tokens, int32_t topk, int64_t rows, int64_t n, uint32_t* err, int num_sms,
                                cudaStream_t st);
-// Tensor-core throughput probe (hm_peak.cu): kind 0 kind::f16, 1 kind::mxf8f6f4, 2 kind::mxf4nvf4;
-// *flops receives the FLOPs the launch issues.
+// Tensor-core throughput probe (hm_peak.cu): kind 0 kind::f16, 1 kind::mxf8f6f4, 2 kind::mxf4nvf4
+// (several issuing warps); 3 and 4 kinds 1 and 2 at N = 256 from one issuer; 5 kind::f16 at N = 256
+// with A in TMEM from one issuer, 6 the same with A in shared memory; *flops receives the FLOPs the
+// launch issues.
 cudaError_t launch_mma_peak(int kind, int32_t iters, int num_sms, uint32_t* err, uint64_t timeout_ns,
                             cudaStream_t st, double* flops);
 cudaError_t launch_wait_timeout_probe(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
