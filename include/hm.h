@@ -368,6 +368,12 @@ typedef struct hm_plan_info {
                           17 <= M <= 32 with MXFP4 / MXINT4 or where tcgen05 would split tiles
                           along K; 2: tensor-core decode kernel (INT4, M <= 16, restored weights
                           in TMEM), taken only with HM_DECODE_TC=1 in the environment */
+  int32_t sk_tiles;    /* tiles whose K loops are cut into stream-K ranges: 0 without stream-K,
+                          else all tiles, or (W4A16 formats with more tiles than CTAs, K loops of
+                          64+ blocks, the remainder of tiles over grid at most half a wave) that
+                          remainder, run as stream-K ranges over every CTA before the others run
+                          whole in full waves; HM_SK_HYBRID=0 / 1 in the environment never / always
+                          (remainder up to 90 % of a wave) takes the latter */
 } hm_plan_info;
 hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
                   hm_plan_info* out);

@@ -142,6 +142,7 @@ struct Plan {
   int a_tmem1;   // tcgen05 at 256 tokens: restored weights in TMEM beside one accumulator
   int pair;      // tcgen05, dense: clusters of two CTAs share each MMA (tiles of 256 weight rows;
                  // grid counts CTAs, two per pair)
+  int64_t sk_tiles;   // with stream_k: the leading tiles in stream-K ranges, the rest whole (0: all)
 };
 
 int bucket_of(int64_t m) {
@@ -255,7 +256,7 @@ bool use_gemv(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
   return f16_choice(m, n, k, num_sms).stream_k;
 }
 
-Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
+Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms, bool allow_hybrid = true) {
   Plan p{};
   p.bucket = bucket_of(m);
   if (use_gemv(fmt, m, n, k, num_sms)) {
@@ -321,6 +322,25 @@ Plan make_plan(int32_t fmt, int64_t m, int64_t n, int64_t k, int num_sms) {
     p.grid = static_cast<int>(p.tiles * per);
   }
   if (p.grid < 1) p.grid = 1;
+  // Hybrid schedule (W4A16 formats, tiles of 128+ tokens, more whole tiles than CTAs): whole waves
+  // of tile-parallel work leave the last wave with only tiles mod grid tiles, so those tiles are
+  // cut into stream-K ranges over every CTA first and the waves that follow are full. The owner of
+  // a shared tile sums the others' fp32 partials (128 KB each at 256 tokens) in 16 dependent
+  // chunks, overlapped with its next tile's K loop; measured (256-token tiles, M = 4096 and 8192):
+  // +10 % on 4096x14336 at M = 4096 (remainder 37 % of a wave, 112 k-blocks per tile), neutral at a
+  // 74 % remainder, and 2-23 % slower on the K = 4096 layers, whose 32-block K loops do not hide
+  // the sum. So by default it is taken for K loops of 64+ blocks with a remainder of at most half a
+  // wave; HM_SK_HYBRID=1 takes it wherever the remainder fills at most 90 % of a wave and gives
+  // every CTA a k-block, HM_SK_HYBRID=0 never; HM_STREAM_K (either value) and HM_PAIR=1 leave it out.
+  const int64_t rem = p.tiles % p.grid;
+  const int hybrid_env = env_int("HM_SK_HYBRID", -1);
+  const bool hybrid_ok = hybrid_env == 1 ? rem * 10 <= static_cast<int64_t>(p.grid) * 9
+                                         : hybrid_env != 0 && p.kb_total >= 64 && rem * 2 <= p.grid;
+  if (allow_hybrid && unit_fmt(fmt) && !p.stream_k && sk_env < 0 && p.tile_m >= 128 && p.tiles > p.grid &&
+      rem > 0 && rem * p.kb_total >= p.grid && hybrid_ok && env_int("HM_PAIR", 0) != 1) {
+    p.stream_k = 1;
+    p.sk_tiles = rem;
+  }
   // 256-token tiles: restored weights in TMEM beside a single accumulator (measured faster on all
   // three benchmark layers from M = 256 on, 9-35 %, once the epilogue stores Y 16 bytes at a time);
   // HM_A_TMEM1=0 keeps them in shared memory with the accumulator pair
@@ -354,10 +374,12 @@ void log_plan(const char* entry, int32_t fmt, int64_t m, int64_t n, int64_t k, c
   if (!log_on()) return;
   std::fprintf(stderr,
                "[hm] %s fmt=%d M=%lld N=%lld K=%lld kernel=%s tile_m=%d tile_k=%d stages=%d stream_k=%d grid=%d "
-               "tiles=%lld%s%s\n",
+               "tiles=%lld%s%s",
                entry, fmt, static_cast<long long>(m), static_cast<long long>(n), static_cast<long long>(k),
                p.gemv ? (p.tc ? "decode-tc" : "decode") : "tcgen05", p.tile_m, p.tile_k, p.stages, p.stream_k, p.grid,
                static_cast<long long>(p.tiles), p.a_tmem1 ? " a=tmem" : "", p.pair ? " pair" : "");
+  if (p.sk_tiles > 0) std::fprintf(stderr, " sk_tiles=%lld", static_cast<long long>(p.sk_tiles));
+  std::fprintf(stderr, "\n");
 }
 
 constexpr size_t kAlign = 256;
@@ -768,6 +790,7 @@ hm_status hm_plan(int32_t fmt, int64_t M, int64_t N, int64_t K, int32_t num_sms,
   out->grid = p.grid;
   out->tiles = static_cast<int32_t>(p.tiles);
   out->kernel = p.gemv ? (p.tc ? 2 : 1) : 0;
+  out->sk_tiles = static_cast<int32_t>(p.stream_k ? (p.sk_tiles > 0 ? p.sk_tiles : p.tiles) : 0);
   return HM_OK;
 }
 
@@ -810,7 +833,7 @@ hm_status hm_gemm(int32_t fmt, const void* x, const void* x_scale, const float* 
     // HM_F16_GROUP=g: grouped tile order (measured neutral, +-3 %, on the W4A16 layers; m-major by default)
     prm.group_m = env_int("HM_F16_GROUP", 0);
     prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total),
-                            p.pair ? p.grid / 2 : p.grid, p.stream_k};
+                            p.pair ? p.grid / 2 : p.grid, p.stream_k, static_cast<int32_t>(p.sk_tiles)};
     prm.timeout_ns = timeout_ns();
     prm.a_tmem1 = p.a_tmem1;
     prm.pair = p.pair;
@@ -1006,7 +1029,12 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   if (!device_info(&di)) return HM_ERR_CUDA;
   uint8_t* scratch = noalloc_scratch(di.dev);
   if (scratch == nullptr) return HM_ERR_CUDA;
-  const Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  Plan p = make_plan(fmt, M, N, K, di.num_sms);
+  // A hybrid schedule whose stream-K partials do not fit the scratch runs whole waves instead.
+  if (p.sk_tiles > 0 && align_up(static_cast<size_t>(p.grid) * 2 * p.tile_m * 128 * sizeof(float)) +
+                                align_up(static_cast<size_t>(p.grid) * kCounterSlots * sizeof(uint32_t)) >
+                            kNoAllocScratchBytes)
+    p = make_plan(fmt, M, N, K, di.num_sms, false);
   log_plan("hm_gemm_w4a16_noalloc", fmt, M, N, K, p);
   if (!plan_fits(p)) return HM_ERR_UNSUPPORTED;
   // The arrival counters of this launch's CTAs, then their partials. Only a plan that shares tiles
@@ -1038,7 +1066,7 @@ hm_status hm_gemm_w4a16_noalloc(int32_t fmt, const void* x, const void* packed, 
   prm.num_m_tiles = static_cast<int32_t>(p.num_m_tiles);
   prm.num_n_tiles = static_cast<int32_t>(p.num_n_tiles);
   prm.sched = SchedParams{static_cast<int32_t>(p.tiles), static_cast<int32_t>(p.kb_total),
-                          p.pair ? p.grid / 2 : p.grid, p.stream_k};
+                          p.pair ? p.grid / 2 : p.grid, p.stream_k, static_cast<int32_t>(p.sk_tiles)};
   prm.timeout_ns = timeout_ns();
   prm.a_tmem1 = p.a_tmem1;
   prm.pair = p.pair;

@@ -444,6 +444,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+// Whole warp: load 16 TMEM lanes (from the lane in taddr, 16-aligned inside this warp's 32-lane
+// group) x 32 consecutive 32-bit columns, in the layout of the warp-level MMA's accumulator
+// fragment: for each group i of 8 columns, thread t receives in r[4i], r[4i+1] lane t/4, columns
+// 8i + 2(t%4) and 8i + 2(t%4) + 1, and in r[4i+2], r[4i+3] lane t/4 + 8, the same two columns.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Whole warp: store four 8x8 16-bit matrices to shared memory transposed. Register j of thread t
+// holds elements (row t/4, columns 2(t%4) and 2(t%4) + 1) of matrix j (the lower column in the low
+// half); the 16-byte shared address given by thread 8j + c receives column c of matrix j (its
+// rows 0..7 in order).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // Whole warp: store 32 consecutive 32-bit columns into this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(

@@ -688,7 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
     pdl_wait();                          // Y, partials and counters may be in use by the previous kernel
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;       // weight row within the tile
-    const int64_t total_it = static_cast<int64_t>(num_tiles) * kb_total;
+    // the flattened (tile, k-block) space of the stream-K tiles (all tiles, or the leading ones of
+    // a hybrid schedule): the hand-off indexes CTAs' ranges in it
+    const int64_t total_it = static_cast<int64_t>(sk_tiles_of(p.sched, num_tiles)) * kb_total;
     // 16-byte stores of Y through the transpose scratch (when the launch has one; Y 16-byte aligned,
     // N % 8 == 0)
     const bool vec_y = p.epi_scratch && (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && (p.n & 7) == 0;
@@ -705,12 +707,15 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         asm volatile("st.shared.u16 [%0], %1;" ::"r"(buf + (jj * 32 + lane) * 2), "h"(hb) : "memory");
       }
     };
-    auto out = [&](uint32_t buf, const TileInfo& t, int j0) {
+    // swz: the 16-byte group of rows 8 c8 .. + 7 of token tt sits at slot c8 ^ ((tt >> 1) & 3) of the
+    // token's 64 bytes (the layout the transposing matrix stores write without bank conflicts)
+    auto out = [&](uint32_t buf, const TileInfo& t, int j0, bool swz) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int piece = lane + 32 * h;   // token piece / 4, rows 8 (piece % 4) .. + 7
         const int tt = piece >> 2, c8 = piece & 3;
-        const uint4 v8 = ld_shared_v4(buf + (tt * 32 + 8 * c8) * 2);
+        const int slot = swz ? (c8 ^ ((tt >> 1) & 3)) : c8;
+        const uint4 v8 = ld_shared_v4(buf + (tt * 32 + 8 * slot) * 2);
         const int64_t m = static_cast<int64_t>(t.m0) + j0 + tt;
         const int64_t n8 = static_cast<int64_t>(t.n0) + 32 * q + 8 * c8;
         if (m < t.m_end) {
@@ -721,6 +726,25 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
             for (int e = 0; e < 8 && n8 + e < p.n; ++e)
               p.y[m * p.n + n8 + e] = __ushort_as_bfloat16(static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1))));
           }
+        }
+      }
+    };
+    // Rows' values of tokens j0 .. j0 + 15 of tile t to Y (bf16, RNE): 16-byte stores through the
+    // scratch when the launch has it, else one bf16 per thread and token.
+    auto store_y = [&](const float (&a)[16], const TileInfo& t, int j0, int64_t n) {
+      if (vec_y) {
+        uint32_t va[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) va[jj] = __float_as_uint(a[jj]);
+        put(va, sc);
+        __syncwarp();
+        out(sc, t, j0, false);
+        __syncwarp();   // the scratch is rewritten by the next chunk
+      } else if (n < p.n) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
+          if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(a[jj]);
         }
       }
     };
@@ -743,13 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       const bool full = seg.kb0 == 0 && seg.kb1 == kb_total;
       // Stream-K tile shared by CTAs c_lo .. c_hi: the owner (holding k-block 0) waits for the
       // others' published partials and adds them to its own accumulator; the others publish.
+      // With a single accumulator (kAccBufs == 1) the owner defers that sum: it stores its own
+      // partial like a publisher, frees the accumulator for the next tile's MMAs at once, and then
+      // adds its partial and the others' in the same order (so the result is the same bits).
       const bool owner = !full && seg.kb0 == 0;
+      const bool defer = S::kAccBufs == 1 && !MOE && !PAIR && owner;   // (only dense single CTAs split K)
       uint32_t* flag = full ? nullptr
                             : sk_flag(p.counters, owner ? blockIdx.x
                                                         : sk_tile_owner(seg.tile, kb_total, total_it, p.sched.grid), q);
       int64_t c_hi = 0;
       bool have = true;
-      if (owner) {
+      if (owner && !defer) {
         c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
         have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
         if (row == 0) trace_mark(p.trace, 10);
@@ -757,20 +785,36 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * S::kIss * BT;
       float* slot = p.partial + (static_cast<size_t>(blockIdx.x) * 2 + (first_seg ? 0 : 1)) * BT * 128 +
                     static_cast<size_t>(row) * BT;
-      // Whole tiles with one issuer and room for two chunks of scratch: two chunks at a time, their
-      // loads, conversions and stores interleaved (each chunk alone is a chain of dependent steps).
+      // Whole tiles with one issuer and room for two chunks of scratch: 32 tokens at a time. The
+      // accumulator is read in the warp-level MMA's fragment layout (two 16-lane halves) and each
+      // group of 8 tokens goes to the scratch as four 8x8 matrices (this warp's rows 0-7, 8-15,
+      // 16-23, 24-31) stored transposed: token m's 32 rows land in its 64 bytes of scratch, rows
+      // 8j .. 8j + 7 at 16-byte slot j ^ ((m >> 1) & 3); the bf16 rounding is put()'s (RNE per
+      // element).
       const bool two = S::kIss == 1 && full && vec_y && p.epi_scratch == 2;
 #pragma unroll 1
       for (int j0 = 0; two && j0 < BT; j0 += 32) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(tbase + j0, v0);
-        tmem_ld16(tbase + j0 + 16, v1);
+        uint32_t lo[16], hi[16];   // TMEM lanes 32q + 0..15 and 32q + 16..31, tokens j0 .. j0 + 31
+        tmem_ld_16x256b_x4(tbase + j0, lo);
+        tmem_ld_16x256b_x4(tbase + (16u << 16) + j0, hi);
         tmem_wait_ld();
-        put(v0, sc);
-        put(v1, sc + S::kEpiScratch);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // tokens j0 + 8i .. + 7: chunk i / 2, its tokens 8 (i % 2) ..
+          auto pk = [](uint32_t a, uint32_t b) {
+            return bf16x2_bits(__floats2bfloat162_rn(__uint_as_float(a), __uint_as_float(b)));
+          };
+          // lane 8j + c gives the address of token 8 (i % 2) + c, rows 8j .. 8j + 7; swizzled so that
+          // the 8 addresses of each matrix fall in 8 different bank groups
+          const int tok = 8 * (i & 1) + (lane & 7);
+          const int slot = (lane >> 3) ^ ((tok >> 1) & 3);
+          const uint32_t dst = sc + static_cast<uint32_t>(i >> 1) * S::kEpiScratch +
+                               static_cast<uint32_t>((tok * 32 + 8 * slot) * 2);
+          stmatrix_x4_trans(dst, pk(lo[4 * i], lo[4 * i + 1]), pk(lo[4 * i + 2], lo[4 * i + 3]),
+                            pk(hi[4 * i], hi[4 * i + 1]), pk(hi[4 * i + 2], hi[4 * i + 3]));
+        }
         __syncwarp();
-        out(sc, t, j0);
-        out(sc + S::kEpiScratch, t, j0 + 16);
+        out(sc, t, j0, true);
+        out(sc + S::kEpiScratch, t, j0 + 16, true);
         __syncwarp();   // the scratch is rewritten by the next pair of chunks
       }
 #pragma unroll 1
@@ -786,27 +830,13 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
         } else {
           tmem_wait_ld();
         }
-        if (full || owner) {
+        if ((full || owner) && !defer) {
           float a[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) a[jj] = __uint_as_float(v[jj]);
           if (owner)
             sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
-          if (vec_y) {
-            uint32_t va[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) va[jj] = __float_as_uint(a[jj]);
-            put(va, sc);
-            __syncwarp();
-            out(sc, t, j0);
-            __syncwarp();   // the scratch is rewritten by the next chunk
-          } else if (n < p.n) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int64_t m = static_cast<int64_t>(t.m0) + j0 + jj;
-              if (m < t.m_end) p.y[m * p.n + n] = __float2bfloat16_rn(a[jj]);
-            }
-          }
+          store_y(a, t, j0, n);
         } else {
           float4* dst = reinterpret_cast<float4*>(slot + j0);
 #pragma unroll
@@ -823,6 +853,26 @@ __global__ void __launch_bounds__(kThreads, 1) f16_gemm_kernel(const __grid_cons
       }
       ++acc_i;
       if (row == 0) trace_mark(p.trace, 9);
+      if (defer) {   // this thread reads back only its own row of the partial it stored above
+        c_hi = sk_owner(static_cast<int64_t>(seg.tile + 1) * kb_total - 1, total_it, p.sched.grid);
+        have = sk_wait(flag, static_cast<uint32_t>(c_hi - blockIdx.x), wc);
+        if (row == 0) trace_mark(p.trace, 10);
+#pragma unroll 1
+        for (int j0 = 0; j0 < BT && have; j0 += 16) {
+          float a[16];
+          const float4* own = reinterpret_cast<const float4*>(slot + j0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 f = __ldcg(own + i);
+            a[4 * i] = f.x;
+            a[4 * i + 1] = f.y;
+            a[4 * i + 2] = f.z;
+            a[4 * i + 3] = f.w;
+          }
+          sk_add_partials<BT>(p.partial, total_it, p.sched.grid, kb_total, seg.tile, blockIdx.x, c_hi, row, j0, a);
+          store_y(a, t, j0, n);
+        }
+      }
       if (!full && !owner) sk_publish(flag, lane);
       if (owner && have) {
         __syncwarp();

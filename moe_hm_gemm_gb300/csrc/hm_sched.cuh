@@ -1,13 +1,19 @@
 // Work schedules shared by the persistent GEMM kernels.
 //
-// A tile is 128 weight rows x `tile_m` tokens; its K loop has `kb_total` k-blocks. Two modes:
+// A tile is 128 weight rows x `tile_m` tokens; its K loop has `kb_total` k-blocks. Modes:
 //  * tile-parallel: CTA b takes tiles b, b+G, b+2G, ... with their whole K loop;
 //  * stream-K (small M, fewer tiles than SMs): the flattened (tile, k-block) space of
 //    num_tiles*kb_total iterations is cut into G contiguous ranges, start(c) =
 //    floor(c*total/G); a CTA's range crosses tile boundaries, so a tile may be shared by
 //    several CTAs, each producing an fp32 partial that the tile's owner (the CTA holding its
 //    first k-block) sums in k order (fixed-owner hand-off below). G <= total guarantees every
-//    range is non-empty, so the number of CTAs sharing a tile is exactly c_hi - c_lo + 1.
+//    range is non-empty, so the number of CTAs sharing a tile is exactly c_hi - c_lo + 1;
+//  * hybrid (sk_tiles = S, 0 < S < num_tiles, with stream-K): the first S tiles (the remainder
+//    of num_tiles over G, which tile-parallel waves would leave to a partly filled last wave) are
+//    cut into stream-K ranges as above over S*kb_total iterations (G <= S*kb_total), and every
+//    CTA then takes tiles S + b, S + b + G, ... whole. The stream-K part comes first, so its
+//    shared tiles are handed off as in plain stream-K; the tiles it covers are the first token
+//    tiles, few enough for their activations to stay in L2 while they are split.
 #pragma once
 #include <cstdint>
 
@@ -20,7 +26,15 @@ struct SchedParams {
   int32_t kb_total;
   int32_t grid;
   int32_t stream_k;
+  int32_t sk_tiles;   // with stream_k: tiles cut into stream-K ranges before the tile-parallel rest
+                      // (0 or >= num_tiles: all of them)
 };
+
+// Tiles the stream-K ranges cover (the hand-off below indexes the flattened space of these).
+__host__ __device__ __forceinline__ int32_t sk_tiles_of(const SchedParams& s, int32_t num_tiles) {
+  if (s.stream_k == 0) return 0;
+  return (s.sk_tiles > 0 && s.sk_tiles < num_tiles) ? s.sk_tiles : num_tiles;
+}
 
 __host__ __device__ __forceinline__ int64_t sk_start(int64_t c, int64_t total, int64_t g) {
   return c * total / g;
@@ -61,20 +75,19 @@ struct Segment {
 // long instruction sequence, and every role walks the schedule at start-up.)
 struct SchedIter {
   int32_t it, it_end;     // stream-K cursor
-  int32_t next_tile;      // tile-parallel cursor
+  int32_t next_tile;      // tile-parallel cursor (after the stream-K tiles)
   int32_t stride;
   int32_t num_tiles;
   int32_t kb_total;
-  bool stream_k;
 
   __device__ __forceinline__ void init(const SchedParams& s, int32_t num_tiles_override, int32_t b) {
     num_tiles = num_tiles_override;
     kb_total = s.kb_total;
-    stream_k = s.stream_k != 0;
     stride = s.grid;
-    next_tile = b;
-    if (stream_k) {
-      const int64_t total = static_cast<int64_t>(num_tiles) * kb_total;
+    const int32_t sk_n = sk_tiles_of(s, num_tiles);
+    next_tile = sk_n + b;
+    if (sk_n > 0) {
+      const int64_t total = static_cast<int64_t>(sk_n) * kb_total;
       it = static_cast<int32_t>(sk_start(b, total, s.grid));
       it_end = static_cast<int32_t>(sk_start(b + 1, total, s.grid));
     } else {
@@ -83,8 +96,7 @@ struct SchedIter {
   }
 
   __device__ __forceinline__ bool next(Segment& seg) {
-    if (stream_k) {
-      if (it >= it_end) return false;
+    if (it < it_end) {
       const uint32_t q = static_cast<uint32_t>(it) / static_cast<uint32_t>(kb_total);
       seg.tile = static_cast<int32_t>(q);
       seg.kb0 = it - static_cast<int32_t>(q) * kb_total;
@@ -142,6 +154,15 @@ __device__ __forceinline__ bool sk_wait(const uint32_t* flag, uint32_t expect, c
   }
 }
 
+// Row `row` of the partial that CTA c stored for `tile` ([cta][first/last segment][row][BT]): its
+// first slot when its range starts in that tile.
+template <int BT>
+__device__ __forceinline__ const float* sk_partial_row(const float* partial, int64_t total_it, int32_t grid,
+                                                       int32_t kb_total, int32_t tile, int64_t c, int row) {
+  const int which = (sk_start(c, total_it, grid) / kb_total == tile) ? 0 : 1;
+  return partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 + static_cast<size_t>(row) * BT;
+}
+
 // Owner: add columns [j0, j0 + 16) of the other contributors' partial rows (CTAs c_lo+1 .. c_hi,
 // in that order) to `acc`, which holds the owner's own values. Loads of up to four contributors
 // are in flight together.
@@ -150,9 +171,7 @@ __device__ __forceinline__ void sk_add_partials(const float* partial, int64_t to
                                                 int32_t kb_total, int32_t tile, int64_t c_lo, int64_t c_hi,
                                                 int row, int j0, float (&acc)[16]) {
   auto src = [&](int64_t c) {
-    const int which = (sk_start(c, total_it, grid) / kb_total == tile) ? 0 : 1;
-    return reinterpret_cast<const float4*>(partial + (static_cast<size_t>(c) * 2 + which) * BT * 128 +
-                                           static_cast<size_t>(row) * BT + j0);
+    return reinterpret_cast<const float4*>(sk_partial_row<BT>(partial, total_it, grid, kb_total, tile, c, row) + j0);
   };
   int64_t c = c_lo + 1;
 #pragma unroll 1

@@ -34,7 +34,8 @@ class WeightDesc(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("bucket", "tile_m", "tile_n", "tile_k", "stages", "stream_k", "grid", "tiles", "kernel")]
+                ("bucket", "tile_m", "tile_n", "tile_k", "stages", "stream_k", "grid", "tiles", "kernel",
+                 "sk_tiles")]
 
 
 def _load():

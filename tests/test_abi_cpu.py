@@ -357,6 +357,44 @@ def test_plan_invariants_random(hm):
         assert p["grid"] <= p["tiles"] * kb_total, (fmt, m, n, k, sms, p)
         if p["grid"] > p["tiles"]:
             assert p["stream_k"] == 1
+        # stream-K covers sk_tiles leading tiles with non-empty ranges; the rest run in full waves
+        assert (p["sk_tiles"] > 0) == (p["stream_k"] == 1)
+        if p["stream_k"]:
+            assert 1 <= p["sk_tiles"] <= p["tiles"] and p["grid"] <= p["sk_tiles"] * kb_total, (fmt, m, n, k, sms, p)
+            if p["sk_tiles"] < p["tiles"]:
+                assert fmt in (1, 2, 5) and p["kernel"] == 0 and p["tile_m"] >= 128
+                assert (p["tiles"] - p["sk_tiles"]) % p["grid"] == 0 and p["sk_tiles"] < p["grid"]
+
+
+def test_plan_hybrid_waves(hm, monkeypatch):
+    """W4A16 with more whole tiles than CTAs: the tiles a last partial wave would hold (tiles mod
+    grid) run as stream-K ranges first, by default for K loops of 64+ blocks with a remainder of at
+    most half a wave; HM_SK_HYBRID=1 up to 90 % of a wave, HM_SK_HYBRID=0 never; either
+    HM_STREAM_K value leaves it out (whole waves, or plain stream-K)."""
+    p = hm.plan(1, 4096, 4096, 14336, 152)    # 512 tiles of 112 k-blocks: 3 waves + 56
+    assert (p["tile_m"], p["stream_k"], p["sk_tiles"], p["grid"], p["tiles"]) == (256, 1, 56, 152, 512)
+    p = hm.plan(5, 4096, 4096, 14336, 152)    # MXINT4 restored weights: the same kernel and schedule
+    assert (p["stream_k"], p["sk_tiles"]) == (1, 56)
+    assert hm.plan(1, 8192, 4096, 14336, 152)["stream_k"] == 0      # remainder 112 of 152: whole waves
+    assert hm.plan(1, 4096, 4096, 4096, 152)["stream_k"] == 0       # 32 k-blocks per tile: whole waves
+    assert hm.plan(3, 4096, 7168, 7168, 152)["sk_tiles"] == 0      # block-scaled: its own schedule
+    monkeypatch.setenv("HM_SK_HYBRID", "1")
+    p = hm.plan(1, 4096, 4096, 4096, 152)     # 512 tiles: 3 waves + 56
+    assert (p["tile_m"], p["stream_k"], p["sk_tiles"], p["grid"], p["tiles"]) == (256, 1, 56, 152, 512)
+    p = hm.plan(1, 8192, 14336, 4096, 152)    # 3584 tiles: 23 waves + 88
+    assert (p["stream_k"], p["sk_tiles"]) == (1, 88)
+    p = hm.plan(1, 1024, 14336, 4096, 152)    # 448 tiles: 2 waves + 144 (95 % of a wave): whole waves
+    assert (p["stream_k"], p["sk_tiles"], p["grid"]) == (0, 0, 152)
+    p = hm.plan(1, 1024, 4096, 4096, 152)     # 128 tiles: one partial wave, tile-parallel
+    assert (p["stream_k"], p["sk_tiles"], p["grid"]) == (0, 0, 128)
+    monkeypatch.setenv("HM_SK_HYBRID", "0")
+    assert hm.plan(1, 4096, 4096, 14336, 152)["stream_k"] == 0
+    monkeypatch.delenv("HM_SK_HYBRID")
+    monkeypatch.setenv("HM_STREAM_K", "0")
+    assert hm.plan(1, 4096, 4096, 14336, 152)["stream_k"] == 0
+    monkeypatch.setenv("HM_STREAM_K", "1")
+    p = hm.plan(1, 4096, 4096, 14336, 152)
+    assert (p["stream_k"], p["sk_tiles"]) == (1, 512)
 
 
 def test_moe_gather_combine_argument_checks(hm):

@@ -78,6 +78,34 @@ def test_forced_configs(hm, env, tile_m, stream_k):
         run_case(hm, 1, 450, 384, 1024, True, seed=10)
 
 
+@pytest.mark.parametrize("fmt,m,n,k", [(1, 2048, 2560, 2560), (1, 2000, 2600, 2560), (2, 2304, 2560, 2560)])
+def test_hybrid_waves(hm, env, fmt, m, n, k):
+    """More whole 256-token tiles than SMs with HM_SK_HYBRID=1: the tiles a last partial wave would
+    hold run first as stream-K ranges over every CTA (their partials handed to the owner), then the
+    rest as whole tiles in full waves. Ragged M and N included; against the oracle, and
+    bit-identical on repeat."""
+    env["HM_SK_HYBRID"] = "1"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = hm.plan(fmt, m, n, k, sms)
+    assert p["stream_k"] == 1 and 0 < p["sk_tiles"] < p["tiles"] and p["grid"] == sms, p
+    w = synth.weights(n, k, seed=m)
+    z = synth.zero_points(n, k // 128, seed=m + 1) if fmt == 1 else None
+    qw = QuantWeight(fmt, w, z)
+    _, packed = qw.transform(hm)
+    x = synth.activations(m, k, seed=m + 2).cuda()
+    ys = []
+    for _ in range(2):
+        full, y = canary_out(m, n)
+        hm.gemm(fmt, x, packed, n, k, out=y)
+        ys.append((full, y))
+    torch.cuda.synchronize()
+    assert_close(ys[0][1], og.gemm(bf16_np(x.cpu()), qw.what), f"hybrid fmt={fmt} m={m} n={n} k={k}")
+    for full, _ in ys:
+        check_canary(full, m, f"hybrid fmt={fmt} m={m}")
+    assert torch.equal(ys[0][1], ys[1][1])
+    assert hm.device_error() == 0
+
+
 def test_repeated_calls_reuse_workspace(hm):
     """Stream-K counters return to zero, so a workspace serves many calls."""
     n, k, m = 1024, 4096, 8
@@ -99,7 +127,8 @@ def test_repeated_calls_reuse_workspace(hm):
 
 @pytest.mark.parametrize("n,k", [(14336, 4096), (4096, 4096), (4096, 14336)])
 def test_full_size_sampled(hm, n, k):
-    """The benchmark's three W4A16 layers at M = 8192 and M = 1, checked on sampled outputs."""
+    """The benchmark's three W4A16 layers at M = 1, 4096 (on 4096x14336 the leftover wave's tiles run
+    as stream-K ranges) and 8192, checked on sampled outputs."""
     w = synth.weights(n, k, seed=1)
     z = synth.zero_points(n, k // 128, seed=2)
     q, s = oq.quant_int4(w, zeros=z)
@@ -108,7 +137,7 @@ def test_full_size_sampled(hm, n, k):
     packed = hm.transform(d, torch.from_numpy(pack_nibbles(q)).cuda(), to_bf16(s).cuda(),
                           torch.from_numpy(z).cuda())
     rng = np.random.default_rng(0)
-    for m in (1, 8192):
+    for m in (1, 4096, 8192):
         x = synth.activations(m, k, seed=3)
         y = hm.gemm(1, x.cuda(), packed, n, k)
         torch.cuda.synchronize()
